@@ -1,0 +1,352 @@
+"""Benchmark of the KDA forward (and single-token decode) on one GB300.
+
+One step = one ``kda_fwd`` call (plan, fused prologue + intra-chunk kernel,
+inter-chunk scan) over the dense workload B=2, T=16384, H_qk=H_v=32,
+K=V=128 with an fp32 initial state and final-state output.  The timed region
+holds exactly ``--steps`` calls bracketed by a barrier and device
+synchronisation; inputs (1.4 GB per step) are larger than L2, so no flush is
+needed between steps.  Prints one JSON line (rank 0).
+
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample of
+the same workload per step (the pages publish no runnable implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import kda_inputs as KI  # noqa: E402
+
+METRIC = "KDA fwd tokens*heads/s & % bf16 TC peak (T=16K); decode state GB/s % HBM"
+UNIT = "token*heads/s"
+WORKLOAD = "KDA fwd dense B=2 T=16384 H_qk=H_v=32 K=V=128, fp32 initial/final state"
+# Algorithmic work of the forward (per token and value head, K = V = 128, chunk 64):
+#   bytes: q, k, v, graw (4 x 256 B) + b (2 B) + out (256 B); plus 2 x 64 KiB of state per (sequence, head)
+#   flops: 2 [3 K V + (C/2)(2K + (K+V) + V)] = 139,264 (causal chunked form)
+BYTES_PER_TOKEN_HEAD = 1282
+STATE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4
+FLOPS_PER_TOKEN_HEAD = 139264
+# Decode step: state read + write (2 x 64 KiB per (b, h)) plus q/k/v/graw/b/out (~1.3 KB)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return d, "measured"
+        except Exception:
+            pass
+    return FALLBACK_PEAKS, "fallback"
+
+
+def peak_value(peaks, *keys):
+    for k in keys:
+        v = peaks.get(k)
+        if isinstance(v, (int, float)):
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "median", "gbs", "tflops"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.idx = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU baseline (oracle)
+def oracle_sample(inp: KI.KdaInputs, tokens: int) -> KI.KdaInputs:
+    """The first ``tokens`` tokens of every sequence of a fixed-length
+    workload (same heads, same initial state)."""
+    sl = lambda x: x[:, :tokens].contiguous()
+    return KI.KdaInputs(q=sl(inp.q), k=sl(inp.k), v=sl(inp.v), graw=sl(inp.graw), b=sl(inp.b), A_log=inp.A_log,
+                        scale=inp.scale, initial_state=inp.initial_state, cu_seqlens=None)
+
+
+def cpu_baseline(inp: KI.KdaInputs, target_s: float = 12.0):
+    import oracle
+    nthreads = os.cpu_count() or 1
+    cal = oracle_sample(inp, 256)
+    t0 = time.perf_counter()
+    oracle.fwd_inputs(cal, nthreads=nthreads)
+    rate = cal.token_heads() / max(time.perf_counter() - t0, 1e-6)
+    tokens = int(min(inp.T, max(256, 64 * round(rate * target_s / (inp.B * inp.H_v) / 64))))
+    smp = oracle_sample(inp, tokens)
+    t0 = time.perf_counter()
+    oracle.fwd_inputs(smp, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return {"value": smp.token_heads() / dt, "unit": UNIT, "cores": min(nthreads, inp.B * inp.H_v),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"first {tokens} of {inp.T} tokens of all {inp.B}x{inp.H_v} (sequence, head) chains "
+                      f"of the timed workload ({smp.token_heads()} token*heads), fp64 C oracle"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 oracle on the host cores, each step a bounded
+    sample of the dense workload."""
+    if rank != 0:
+        return
+    import oracle
+    inp = KI.workload("dense")
+    nthreads = os.cpu_count() or 1
+    cal = oracle_sample(inp, 128)
+    t0 = time.perf_counter()
+    oracle.fwd_inputs(cal, nthreads=nthreads)
+    rate = cal.token_heads() / max(time.perf_counter() - t0, 1e-6)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    tokens = int(min(inp.T, max(64, 64 * int(rate * budget / (inp.B * inp.H_v) / 64))))
+    smp = oracle_sample(inp, tokens)
+    for _ in range(args.warmup):
+        oracle.fwd_inputs(smp, nthreads=nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fwd_inputs(smp, nthreads=nthreads)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = smp.token_heads() / dt
+    sample = (f"first {tokens} of {inp.T} tokens of all {inp.B}x{inp.H_v} (sequence, head) chains per step "
+              f"({smp.token_heads()} token*heads), fp64 C oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": 2, "T": 16384, "H_qk": 32, "H_v": 32, "sample_tokens": tokens},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def time_events(fn, steps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def run_gpu(args, rank, world, local):
+    from gated_delta_rule_40_gb300 import kda
+    kda.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    hbm_peak = peak_value(peaks, "hbm_gbs", "hbm_GBps", "hbm") or FALLBACK_PEAKS["hbm_gbs"]
+    tc_peak = peak_value(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops_sustained"]
+
+    inp = KI.workload("dense", seed=rank)
+    d = {n: getattr(inp, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log", "initial_state")}
+    out = torch.empty((inp.B, inp.T, inp.H_v, 128), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty_like(d["initial_state"])
+
+    def step():
+        kda.kda_fwd(d["q"], d["k"], d["v"], d["graw"], d["b"], d["A_log"], inp.scale,
+                    initial_state=d["initial_state"], out=out, final_state=fin, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    launches_per_step = kda.kda_last_launch_count()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = time_events(step, args.steps, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms, world)
+    status = kda.kda_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status after the timed region: {kda.status_string(status)}")
+
+    units = inp.token_heads()
+    value = world * units / (ms * 1e-3)
+    alg_bytes = units * BYTES_PER_TOKEN_HEAD + inp.N * inp.H_v * STATE_BYTES_PER_SEQ_HEAD
+    alg_flops = units * FLOPS_PER_TOKEN_HEAD
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    tflops = alg_flops / (ms * 1e-3) / 1e12
+
+    # ---- end to end through the public call with host buffers
+    pin = {n: t.pin_memory() for n, t in
+           (("q", inp.q), ("k", inp.k), ("v", inp.v), ("graw", inp.graw), ("b", inp.b),
+            ("A_log", inp.A_log), ("initial_state", inp.initial_state))}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = host_out.numel() * 2 + host_fin.numel() * 4
+
+    def e2e_step():
+        for n, t in pin.items():
+            d[n].copy_(t, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+        host_fin.copy_(fin, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 10))
+    barrier(world)
+    e2e_ms = max_over_ranks(time_events(e2e_step, e2e_steps, stream), world)
+
+    # ---- decode (B=256, H=64): state GB/s against HBM
+    dec = KI.decode_inputs(B=256, H=64, seed=rank)
+    dd = {n: getattr(dec, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log", "state")}
+    dout = torch.empty((256, 64, 128), dtype=torch.bfloat16, device=dev)
+
+    def dec_step():
+        kda.kda_decode_step(dd["q"], dd["k"], dd["v"], dd["graw"], dd["b"], dd["A_log"], dec.scale, dd["state"],
+                            out=dout, stream=stream)
+
+    for _ in range(5):
+        dec_step()
+    torch.cuda.synchronize()
+    dec_ms = time_events(dec_step, 50, stream)
+    dec_bytes = 256 * 64 * (2 * 128 * 128 * 4 + 5 * 256 + 2)
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": inp.B, "T": inp.T, "H_qk": inp.H_qk, "H_v": inp.H_v, "K": 128,
+                   "V": 128, "chunk": 64, "seed": 0,
+                   "l2": "inputs larger than L2 (1.4 GB read per step), no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "kda_fwd (plan + fused prologue/intra-chunk + scan)",
+                     "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                     "traffic": None, "peak_source": peak_src,
+                     "algorithmic_bytes_per_step": alg_bytes},
+        "tensor": {"achieved_tflops": tflops, "peak_tflops": tc_peak, "frac": tflops / tc_peak,
+                   "flops_per_step": alg_flops, "peak_source": peak_src},
+        "e2e": {"value": world * units / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "decode": {"workload": "B=256 H=64 K=V=128 fp32 state in place", "ms": dec_ms, "GB/s": dec_gbs,
+                   "hbm_peak": hbm_peak, "frac": dec_gbs / hbm_peak},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = dist_init()
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,136 @@
+// C-ABI entry points of libkda: argument validation, workspace handling and
+// kernel launches.  See include/kda.h for the contract.
+#include <cstdint>
+#include <cstdio>
+
+#include "kda_common.cuh"
+
+namespace kda {
+__device__ int g_kda_status = 0;
+
+cudaError_t launch_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                          const uint16_t *b, const float *A_log, float scale, float *state, int B, int H_qk,
+                          int H_v, uint16_t *out, cudaStream_t stream);
+cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                       const uint16_t *b, const float *A_log, float scale, const float *init, float *fin,
+                       const int32_t *cu, int N, int B, int T, int H_qk, int H_v, uint16_t *out, void *ws_ptr,
+                       cudaStream_t stream, int *launches);
+struct FwdWorkspace;
+size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspace *ws, char *base);
+}  // namespace kda
+
+namespace {
+thread_local int t_last_launches = 0;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int validate_fwd(const void *q, const void *k, const void *v, const void *graw, const void *b,
+                 const void *A_log, const void *init, const void *fin, const int32_t *cu, int N, int B, int T,
+                 int H_qk, int H_v, int K, int V, const void *out) {
+    if (K != kda::KD || V != kda::KD) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H_qk <= 0 || H_v <= 0) return KDA_ERR_INVALID_ARG;
+    if (H_v % H_qk != 0) return KDA_ERR_INVALID_ARG;
+    if (cu) {
+        if (B != 1 || N < 0) return KDA_ERR_INVALID_ARG;
+    }
+    const long long tokens = (long long)B * T;
+    if (tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (tokens > 0) {
+        if (!q || !k || !v || !graw || !b || !A_log || !out) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(graw) || !aligned16(out))
+            return KDA_ERR_INVALID_ARG;
+    }
+    if ((init && !aligned16(init)) || (fin && !aligned16(fin))) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int code) {
+    switch (code) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported head dimension (K and V must be 128)";
+        case KDA_ERR_CUDA: return "CUDA runtime or launch error";
+        case KDA_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+        case KDA_ERR_BAD_SEQLENS: return "malformed cu_seqlens";
+        case KDA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        default: return "unknown status";
+    }
+}
+
+int kda_get_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return KDA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, kda::g_kda_status, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(kda::g_kda_status, &zero, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    return v;
+}
+
+int kda_last_launch_count(void) { return t_last_launches; }
+
+size_t kda_fwd_workspace_size(int N, int B, int T, int H_qk, int H_v, int K, int V) {
+    if (K != kda::KD || V != kda::KD || B < 0 || T < 0 || H_qk <= 0 || H_v <= 0 || N < 0) return 0;
+    // varlen bound: every sequence adds at most one partial chunk
+    const size_t a = kda::fwd_workspace_bytes(N, B, T, H_v, true, nullptr, nullptr);
+    const size_t b = kda::fwd_workspace_bytes(N, B, T, H_v, false, nullptr, nullptr);
+    return a > b ? a : b;
+}
+
+int kda_fwd_ws(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+               const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
+               float *final_state, const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K,
+               int V, kda_bf16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    int rc = validate_fwd(q, k, v, graw, b, A_log, initial_state, final_state, cu_seqlens, N, B, T, H_qk, H_v,
+                          K, V, out);
+    if (rc != KDA_OK) return rc;
+    const size_t need = kda::fwd_workspace_bytes(cu_seqlens ? N : 0, B, T, H_v, cu_seqlens != nullptr, nullptr,
+                                                 nullptr);
+    if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need) return KDA_ERR_WORKSPACE;
+    int launches = 0;
+    cudaError_t e = kda::launch_fwd(q, k, v, graw, b, A_log, scale, initial_state, final_state, cu_seqlens,
+                                    cu_seqlens ? N : 0, B, T, H_qk, H_v, out, ws, stream, &launches);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    t_last_launches = launches;
+    return KDA_OK;
+}
+
+int kda_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+            const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state, float *final_state,
+            const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
+            cudaStream_t stream) {
+    int rc = validate_fwd(q, k, v, graw, b, A_log, initial_state, final_state, cu_seqlens, N, B, T, H_qk, H_v,
+                          K, V, out);
+    if (rc != KDA_OK) return rc;
+    const size_t need = kda::fwd_workspace_bytes(cu_seqlens ? N : 0, B, T, H_v, cu_seqlens != nullptr, nullptr,
+                                                 nullptr);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    rc = kda_fwd_ws(q, k, v, graw, b, A_log, scale, initial_state, final_state, cu_seqlens, N, B, T, H_qk, H_v,
+                    K, V, out, ws, need, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
+    return rc;
+}
+
+int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+                    const kda_bf16_t *b, const float *A_log, float scale, float *state, int B, int H_qk, int H_v,
+                    int K, int V, kda_bf16_t *out, cudaStream_t stream) {
+    if (K != kda::KD || V != kda::KD) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0) {
+        t_last_launches = 0;
+        return KDA_OK;
+    }
+    if (!q || !k || !v || !graw || !b || !A_log || !state || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(graw) || !aligned16(state) ||
+        !aligned16(out))
+        return KDA_ERR_INVALID_ARG;
+    cudaError_t e = kda::launch_decode(q, k, v, graw, b, A_log, scale, state, B, H_qk, H_v, out, stream);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    t_last_launches = 1;
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,182 @@
+"""Python binding of libkda (include/kda.h): argument marshalling only.
+
+Every function here takes torch tensors, checks dtype / device / layout,
+passes raw pointers and the current CUDA stream to the C ABI and raises on a
+non-zero return code.  All arithmetic runs in the CUDA kernels of libkda.so;
+there is no other code path.  If the library is missing the first call raises
+``KdaLibraryError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "kda.h")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_CUDA = -3
+KDA_ERR_DEVICE_TIMEOUT = -4
+KDA_ERR_BAD_SEQLENS = -5
+KDA_ERR_WORKSPACE = -6
+
+
+class KdaLibraryError(RuntimeError):
+    pass
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libkda.so (built in-tree by ``gated_delta_rule_40_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise KdaLibraryError(f"{LIB_PATH} is missing; run __graft_entry__.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fwd_args = [P, P, P, P, P, P, F, P, P, P, I, I, I, I, I, I, I, P]
+    lib.kda_fwd.argtypes = fwd_args + [P]
+    lib.kda_fwd.restype = I
+    lib.kda_fwd_ws.argtypes = fwd_args + [P, Z, P]
+    lib.kda_fwd_ws.restype = I
+    lib.kda_fwd_workspace_size.argtypes = [I] * 7
+    lib.kda_fwd_workspace_size.restype = Z
+    lib.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, P, P]
+    lib.kda_decode_step.restype = I
+    lib.kda_status_string.argtypes = [I]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_get_status.argtypes = [P]
+    lib.kda_get_status.restype = I
+    lib.kda_last_launch_count.argtypes = []
+    lib.kda_last_launch_count.restype = I
+    _lib = lib
+    return lib
+
+
+def declared_symbols() -> list:
+    """Names of the functions include/kda.h declares."""
+    txt = open(HEADER_PATH).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]*?\b(kda_\w+)\s*\(", txt, re.M)))
+
+
+def status_string(code: int) -> str:
+    return load().kda_status_string(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t: Optional[torch.Tensor], name: str, dtype, shape=None, optional=False):
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _raise(rc: int, where: str):
+    if rc != KDA_OK:
+        raise KdaError(rc, where)
+
+
+def kda_fwd_workspace_size(N: int, B: int, T: int, H_qk: int, H_v: int, K: int = 128, V: int = 128) -> int:
+    return int(load().kda_fwd_workspace_size(N, B, T, H_qk, H_v, K, V))
+
+
+def kda_fwd(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_seqlens=None,
+            output_final_state: bool = True, out=None, final_state=None, workspace=None,
+            stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """KDA forward.  Shapes: q, k [B,T,H_qk,K]; v, graw [B,T,H_v,*]; b [B,T,H_v]
+    (bf16); A_log [H_v] fp32; initial_state [N,H_v,V,K] fp32 or None;
+    cu_seqlens int32 [N+1] (device) or None.  Returns (out, final_state)."""
+    lib = load()
+    B, T, H_qk, K = q.shape
+    H_v, V = v.shape[2], v.shape[3]
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    bf = torch.bfloat16
+    _check(q, "q", bf, (B, T, H_qk, K))
+    _check(k, "k", bf, (B, T, H_qk, K))
+    _check(v, "v", bf, (B, T, H_v, V))
+    _check(graw, "graw", bf, (B, T, H_v, K))
+    _check(b, "b", bf, (B, T, H_v))
+    _check(A_log, "A_log", torch.float32, (H_v,))
+    _check(initial_state, "initial_state", torch.float32, (N, H_v, V, K), optional=True)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, optional=True)
+    if out is None:
+        out = torch.empty((B, T, H_v, V), dtype=bf, device=q.device)
+    _check(out, "out", bf, (B, T, H_v, V))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H_v, V, K), dtype=torch.float32, device=q.device)
+    _check(final_state, "final_state", torch.float32, (N, H_v, V, K), optional=True)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
+            _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V, _ptr(out)]
+    if workspace is None:
+        rc = lib.kda_fwd(*args, _stream(stream))
+        _raise(rc, "kda_fwd")
+    else:
+        _check(workspace, "workspace", torch.uint8)
+        rc = lib.kda_fwd_ws(*args, _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+        _raise(rc, "kda_fwd_ws")
+    return out, final_state
+
+
+def kda_decode_step(q, k, v, graw, b, A_log, scale: float, state, out=None, stream=None) -> torch.Tensor:
+    """One decode step; ``state`` [B,H_v,V,K] fp32 is updated in place.
+    Shapes: q, k [B,H_qk,K]; v, graw [B,H_v,*]; b [B,H_v] (bf16)."""
+    lib = load()
+    B, H_qk, K = q.shape
+    H_v, V = v.shape[1], v.shape[2]
+    bf = torch.bfloat16
+    _check(q, "q", bf, (B, H_qk, K))
+    _check(k, "k", bf, (B, H_qk, K))
+    _check(v, "v", bf, (B, H_v, V))
+    _check(graw, "graw", bf, (B, H_v, K))
+    _check(b, "b", bf, (B, H_v))
+    _check(A_log, "A_log", torch.float32, (H_v,))
+    _check(state, "state", torch.float32, (B, H_v, V, K))
+    if out is None:
+        out = torch.empty((B, H_v, V), dtype=bf, device=q.device)
+    _check(out, "out", bf, (B, H_v, V))
+    rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log),
+                             ctypes.c_float(scale), _ptr(state), B, H_qk, H_v, K, V, _ptr(out),
+                             _stream(stream))
+    _raise(rc, "kda_decode_step")
+    return out
+
+
+def kda_get_status(stream=None) -> int:
+    return int(load().kda_get_status(_stream(stream)))
+
+
+def kda_last_launch_count() -> int:
+    return int(load().kda_last_launch_count())

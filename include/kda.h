@@ -1,0 +1,135 @@
+/*
+ * libkda: Kimi Delta Attention (KDA) forward and single-token decode on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * KDA is a gated delta-rule linear attention with a per-channel decay.  Per
+ * sequence and value head h, with state S (V x K, fp32, S[v][k]):
+ *
+ *   qt   = scale * q / sqrt(|q|^2 + 1e-6)          kh = k / sqrt(|k|^2 + 1e-6)
+ *   beta = sigmoid(b)                               g  = -exp(A_log[h]) * softplus(graw)
+ *   S_t  = S_{t-1} Diag(exp g_t) (I - beta_t kh_t kh_t^T) + beta_t v_t kh_t^T
+ *   o_t  = S_t qt_t
+ *
+ * The fused gate activation, beta sigmoid and q/k L2 norm follow the FlashKDA
+ * library page ("FlashKDA: High-performance KDA CUDA kernels for SM90+ GPUs",
+ * section "What exact performance bottlenecks does FlashKDA address",
+ * Technical Features); the state layouts [B,H,V,K] and [N,H,V,K] with
+ * cu_seqlens and B = 1 follow its section "How does FlashKDA's
+ * stateful/streaming (chunked) support work?"; bf16 q/k/v/g/out, fp32 A_log
+ * and the K = V = 128 restriction follow its section "How to seamlessly
+ * replace flash-linear-attention's chunk_kda" (Technical Analysis).  Grouped
+ * value heads (H_v a multiple of H_qk, value head h reading query/key head
+ * h / (H_v / H_qk)) follow the h_qk / h_v columns of the FlashQLA H200 table
+ * ("benchmark_results_H200.txt", FORWARD BENCHMARKS).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major data,
+ *    owned by the caller; the library keeps no pointer after a call returns.
+ *    bf16 data is passed as its 16-bit pattern (kda_bf16_t).
+ *  - q, k, v, graw, out and the states must be 16-byte aligned.
+ *  - Calls are asynchronous and ordered on `stream`; no entry point except
+ *    kda_get_status synchronises with the host.
+ *  - The return value reports host-side validation and launch errors only.
+ *    Faults detected on the device (malformed cu_seqlens, a bounded wait that
+ *    timed out) are recorded in a per-device status word read by
+ *    kda_get_status.
+ *  - K and V must both be 128 (KDA_ERR_UNSUPPORTED otherwise).
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kda_bf16_t; /* bit pattern of a bfloat16 value */
+
+enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,    /* NULL required pointer, negative size, H_v % H_qk != 0,
+                                    cu_seqlens with B != 1, misaligned pointer */
+    KDA_ERR_UNSUPPORTED = -2,    /* K != 128 or V != 128 */
+    KDA_ERR_CUDA = -3,           /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_DEVICE_TIMEOUT = -4, /* (status word) a bounded device-side wait gave up */
+    KDA_ERR_BAD_SEQLENS = -5,    /* (status word) cu_seqlens not 0 = c0 <= c1 <= ... <= cN = T */
+    KDA_ERR_WORKSPACE = -6       /* workspace NULL, too small or not 256-byte aligned */
+};
+
+/*
+ * Chunked KDA forward (prefill).
+ *
+ *   q, k      [B, T, H_qk, K] bf16
+ *   v         [B, T, H_v,  V] bf16
+ *   graw      [B, T, H_v,  K] bf16   gate pre-activation (per channel)
+ *   b         [B, T, H_v]     bf16   beta pre-activation
+ *   A_log     [H_v]           fp32
+ *   scale                            multiplies the L2-normalised q (normally 1/sqrt(K))
+ *   initial_state [Nseq, H_v, V, K] fp32, or NULL for zeros
+ *   final_state   [Nseq, H_v, V, K] fp32 output, or NULL (not written)
+ *   cu_seqlens    int32 [N + 1] device array, or NULL.  With cu_seqlens the
+ *                 call is packed: B must be 1, sequence n covers tokens
+ *                 cu_seqlens[n] .. cu_seqlens[n+1]-1 and Nseq = N; without it
+ *                 Nseq = B sequences of length T each and N is ignored.
+ *   out       [B, T, H_v, V] bf16 output
+ *
+ * Each sequence starts from its own initial state; feeding final_state into
+ * initial_state of a call on the continuation equals one call on the whole
+ * sequence.  A zero-length sequence copies its initial state (or zeros) to
+ * final_state.  Allocates its workspace with cudaMallocAsync / cudaFreeAsync
+ * on `stream`; use kda_fwd_ws to supply it instead.
+ */
+int kda_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
+            const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log, float scale,
+            const float *initial_state, float *final_state, const int32_t *cu_seqlens,
+            int N, int B, int T, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
+            cudaStream_t stream);
+
+/* Bytes of device workspace kda_fwd_ws needs for these sizes (0 on invalid
+ * sizes).  The bound covers any cu_seqlens with N sequences and T tokens. */
+size_t kda_fwd_workspace_size(int N, int B, int T, int H_qk, int H_v, int K, int V);
+
+/* kda_fwd with a caller-owned workspace: `ws` is a device pointer, 256-byte
+ * aligned, of at least kda_fwd_workspace_size(...) bytes.  The workspace must
+ * not be used by anything else until the work queued on `stream` completes. */
+int kda_fwd_ws(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
+               const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log, float scale,
+               const float *initial_state, float *final_state, const int32_t *cu_seqlens,
+               int N, int B, int T, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
+               void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * One decode step for B independent sequences (one token each):
+ *
+ *   q, k  [B, H_qk, K] bf16     v, graw [B, H_v, V|K] bf16     b [B, H_v] bf16
+ *   A_log [H_v] fp32            state [B, H_v, V, K] fp32, updated in place
+ *   out   [B, H_v, V] bf16
+ *
+ * Equivalent to kda_fwd with T = 1, initial_state = final_state = state.
+ */
+int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
+                    const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log,
+                    float scale, float *state, int B, int H_qk, int H_v, int K, int V,
+                    kda_bf16_t *out, cudaStream_t stream);
+
+/* Human-readable name of a return or status code (static string). */
+const char *kda_status_string(int code);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word (KDA_OK if no device-side fault was recorded since the last call). */
+int kda_get_status(cudaStream_t stream);
+
+/* Number of kernel launches the most recent successful kda_fwd / kda_fwd_ws /
+ * kda_decode_step call on this host thread queued. */
+int kda_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

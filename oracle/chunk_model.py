@@ -27,7 +27,8 @@ whole chunk (that overflows for strong gates).  The decay matrix is built from
 block-row i use the reference m_i = Gam[16 i - 1] (both factors <= 1), diagonal
 blocks use, per channel, the midpoint of the block's first and last Gam as
 reference with both exponents clamped at ``clamp`` (exact unless a channel
-decays by more than ``2 * clamp`` nats across the sixteen rows).  ``rounding`` optionally rounds named operands to bf16 or tf32
+decays by more than ``2 * clamp`` nats across the sixteen rows), and the j = r
+term uses its exact factor 1.  ``rounding`` optionally rounds named operands to bf16 or tf32
 to model a kernel's operand precision.
 """
 from __future__ import annotations
@@ -88,7 +89,8 @@ def decay_pairs(Gam: np.ndarray, clamp: float = 85.0):
         colf = np.exp(np.minimum(mid - Gam[r0:r1], clamp))
         blk = rowf[:, None, :] * colf[None, :, :]
         n = r1 - r0
-        E[r0:r1, r0:r1] = blk * np.tril(np.ones((n, n)))[:, :, None]
+        E[r0:r1, r0:r1] = blk * np.tril(np.ones((n, n)), -1)[:, :, None]
+        E[np.arange(r0, r1), np.arange(r0, r1)] = 1.0   # the j = r factor is exactly 1
     return E
 
 

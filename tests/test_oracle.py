@@ -46,7 +46,7 @@ def _cmp(a, b):
     return np.abs(a - b).max() / max(np.abs(b).max(), 1e-300)
 
 
-@pytest.mark.parametrize("case", ["random", "harsh", "partial", "varlen", "slow", "gva", "zero_len"])
+@pytest.mark.parametrize("case", ["random", "harsh", "partial", "varlen", "slow", "gva", "zero_len", "forget"])
 def test_chunk_algebra_matches_oracle(case):
     """The chunked UT/WY form (with the sub-block decay references the GPU
     path uses) reproduces the token recurrence to fp64 rounding."""
@@ -62,6 +62,10 @@ def test_chunk_algebra_matches_oracle(case):
         inp = KI.make_inputs(1, 192, 1, 1, seed=34, with_state=True, graw_mean=-4.0, A_log_value=-1.0)
     elif case == "gva":
         inp = KI.make_inputs(1, 70, 1, 3, seed=35, with_state=True, scalar_gate=True)
+    elif case == "forget":
+        inp = KI.make_inputs(1, 100, 1, 1, seed=37, with_state=True)
+        inp.graw.fill_(1e4)
+        inp.b.fill_(float("inf"))
     else:
         inp = KI.make_inputs(1, 70, 1, 1, seed=36, with_state=True, seqlens=[0, 70, 0])
     o1, f1 = oracle.fwd_inputs(inp)
