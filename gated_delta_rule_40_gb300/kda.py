@@ -55,6 +55,8 @@ def load() -> ctypes.CDLL:
     lib.kda_fwd.restype = I
     lib.kda_fwd_ws.argtypes = fwd_args + [P, Z, P]
     lib.kda_fwd_ws.restype = I
+    lib.kda_fwd_noalloc.argtypes = fwd_args + [P]
+    lib.kda_fwd_noalloc.restype = I
     lib.kda_fwd_workspace_size.argtypes = [I] * 7
     lib.kda_fwd_workspace_size.restype = Z
     lib.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, P, P]
@@ -147,6 +149,41 @@ def kda_fwd(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_seqlen
         _check(workspace, "workspace", torch.uint8)
         rc = lib.kda_fwd_ws(*args, _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
         _raise(rc, "kda_fwd_ws")
+    return out, final_state
+
+
+NOALLOC_WS_BYTES = 64 << 20
+
+
+def kda_fwd_noalloc(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_seqlens=None,
+                    out=None, final_state=None, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """``kda_fwd`` for callers that cannot allocate device memory where they
+    call it: the workspace is the library's fixed 64 MiB device array, shared
+    by every call on the device (calls that overlap on the GPU race).  The
+    caller still provides ``out`` and ``final_state`` (allocated here only if
+    not given).  Raises KdaError(KDA_ERR_WORKSPACE) when the sizes need more
+    workspace than the array holds."""
+    lib = load()
+    B, T, H_qk, K = q.shape
+    H_v, V = v.shape[2], v.shape[3]
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    bf = torch.bfloat16
+    _check(q, "q", bf, (B, T, H_qk, K))
+    _check(k, "k", bf, (B, T, H_qk, K))
+    _check(v, "v", bf, (B, T, H_v, V))
+    _check(graw, "graw", bf, (B, T, H_v, K))
+    _check(b, "b", bf, (B, T, H_v))
+    _check(A_log, "A_log", torch.float32, (H_v,))
+    _check(initial_state, "initial_state", torch.float32, (N, H_v, V, K), optional=True)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, optional=True)
+    if out is None:
+        out = torch.empty((B, T, H_v, V), dtype=bf, device=q.device)
+    _check(out, "out", bf, (B, T, H_v, V))
+    _check(final_state, "final_state", torch.float32, (N, H_v, V, K), optional=True)
+    rc = lib.kda_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
+                             _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V,
+                             _ptr(out), _stream(stream))
+    _raise(rc, "kda_fwd_noalloc")
     return out, final_state
 
 

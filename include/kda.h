@@ -124,6 +124,32 @@ const char *kda_status_string(int code);
  * word (KDA_OK if no device-side fault was recorded since the last call). */
 int kda_get_status(cudaStream_t stream);
 
+/*
+ * kda_fwd without any device allocation, for callers that cannot allocate
+ * device memory where they run the forward (inside a stream-capture region or
+ * under an allocator that forbids allocations outside its own pool, in
+ * latency-critical serving loops that must not enter the driver allocator, or
+ * in hosts that own all device memory).  The paper has no counterpart; this
+ * is a deployment variant of kda_fwd with identical arguments and results.
+ *
+ * The workspace is a file-scope __device__ array of KDA_NOALLOC_WS_BYTES
+ * (64 MiB) that every GPU which loads the library holds until the process
+ * exits.  Sizes whose workspace (see kda_fwd_workspace_size; about 113 KB per
+ * 64-token chunk and value head) exceeds it return KDA_ERR_WORKSPACE without
+ * launching anything.  The first call on a device looks up the array's device
+ * address with that device current (a one-time set-up); make that first call
+ * before any stream capture.  All calls on a device share the array and it
+ * keeps the last call's contents (nothing in it needs to start at zero), so
+ * calls that overlap on the GPU (different streams without ordering between
+ * them) race: order them on one stream or with events.
+ */
+#define KDA_NOALLOC_WS_BYTES (64u << 20)
+int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
+                    const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log, float scale,
+                    const float *initial_state, float *final_state, const int32_t *cu_seqlens,
+                    int N, int B, int T, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
+                    cudaStream_t stream);
+
 /* Number of kernel launches the most recent successful kda_fwd / kda_fwd_ws /
  * kda_decode_step call on this host thread queued. */
 int kda_last_launch_count(void);
