@@ -157,6 +157,17 @@ struct IntraSmem {
     float Kg[CH][KGS];               // kh * exp(Gam) (tf32), W operand
 };
 
+// Per (chunk, value head) record written by the intra-chunk kernel and read
+// by the scan with bulk copies.  Every operand is stored as the exact shared
+// memory image the scan's tcgen05.mma reads (K-major, 128-byte swizzle):
+//   WQ  [Qg rows 0..63 ; W rows 64..127] x K=128, bf16          (32 KiB)
+//   P   rows 0..63 x 64 (j), tf32                                (16 KiB)
+//   KDT Kd^T: rows k = 0..127 x 64 (r), tf32                      (32 KiB)
+//   U   [V block 0 | V block 1], each [64 r][64 v] fp32 row-major  (32 KiB)
+//   GC  exp(Gam_C) per channel, fp32                              (512 B)
+constexpr uint32_t REC_WQ = 0, REC_P = 32768, REC_KDT = 49152, REC_U = 81920, REC_GC = 114688;
+constexpr uint32_t REC_BYTES = 115200;
+
 struct IntraParams {
     const uint16_t *q, *k, *v, *graw, *b;
     const float *A_log;
@@ -164,12 +175,7 @@ struct IntraParams {
     int H_qk, H_v;
     const ChunkDesc *chunks;
     const int *hdr;
-    uint16_t *W;    // [chunk][H_v][64][128] bf16
-    uint16_t *Qg;   // [chunk][H_v][64][128] bf16
-    float *P;       // [chunk][H_v][64][64]  tf32 in fp32
-    float *Kd;      // [chunk][H_v][64][128] tf32 in fp32
-    float *U;       // [chunk][H_v][64][128] fp32
-    float *gC;      // [chunk][H_v][128]     fp32
+    unsigned char *rec;   // [chunk][H_v] records of REC_BYTES
 };
 
 enum { OP_FK = 0, OP_FQ, OP_HK, OP_DRK, OP_DRQ, OP_DCK };
@@ -189,6 +195,7 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, tq = lane & 3;   // mma fragment coordinates
     const size_t ch = (size_t)chunk * p.H_v + h;
+    unsigned char *rec = p.rec + ch * REC_BYTES;
     const int len = cd.len;
 
     // ---- 1. stage raw rows (cp.async 16 B), zero-fill the padded rows
@@ -298,7 +305,7 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
                 s.ref[R_EB + i][c] = ex2(m[i]);
                 s.ref[R_EA + i][c] = ex2(m[4] - m[i + 1]);
             }
-            p.gC[ch * KD + c0 + c] = ex2(m[4]);
+            *reinterpret_cast<float *>(rec + REC_GC + 4 * (c0 + c)) = ex2(m[4]);
         }
         __syncthreads();
         // ---- 3d. gated operands
@@ -320,8 +327,8 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             s.op[OP_DCK][r][c] = to_tf32(kh * dc);
             const float eb = s.ref[R_EB + bl][c], ea = s.ref[R_EA + bl][c];
             s.Kg[r][c0 + c] = to_tf32(kh * f * eb);
-            p.Qg[(ch * CH + r) * KD + c0 + c] = f_to_bf16(qt * f * eb);
-            p.Kd[(ch * CH + r) * KD + c0 + c] = to_tf32(kh * hh * ea);
+            *reinterpret_cast<uint16_t *>(rec + REC_WQ + sw128_off(r, 2 * (c0 + c), 2 * CH)) = f_to_bf16(qt * f * eb);
+            *reinterpret_cast<float *>(rec + REC_KDT + sw128_off(c0 + c, 4 * r, KD)) = to_tf32(kh * hh * ea);
         }
         __syncthreads();
         // ---- 3e. partial products over this slice's 32 channels
@@ -367,7 +374,7 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
         const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
         const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
         const int r = 16 * bi + (e >> 4), j = 16 * bj + (e & 15);
-        p.P[(ch * CH + r) * CH + j] = 0.f;
+        *reinterpret_cast<float *>(rec + REC_P + sw128_off(r, 4 * j, CH)) = 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -386,7 +393,7 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             } else {
                 // the decay factor of the j = r term is exactly 1 for any gate
                 val = (j < r) ? val : (j == r ? s.qk[r] : 0.f);
-                p.P[(ch * CH + r) * CH + j] = to_tf32(val);
+                *reinterpret_cast<float *>(rec + REC_P + sw128_off(r, 4 * j, CH)) = to_tf32(val);
             }
         }
     }
@@ -471,10 +478,10 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             for (int hf = 0; hf < 2; ++hf) {
                 const int r = ra + 8 * hf;
                 if (nh == 0) {
-                    *reinterpret_cast<uint32_t *>(&p.W[(ch * CH + r) * KD + c]) =
+                    *reinterpret_cast<uint32_t *>(rec + REC_WQ + sw128_off(CH + r, 2 * c, 2 * CH)) =
                         pack_bf16x2(o[nt][2 * hf], o[nt][2 * hf + 1]);
                 } else {
-                    *reinterpret_cast<float2 *>(&p.U[(ch * CH + r) * KD + c]) =
+                    *reinterpret_cast<float2 *>(rec + REC_U + (c >> 6) * 16384 + (r * 64 + (c & 63)) * 4) =
                         make_float2(o[nt][2 * hf], o[nt][2 * hf + 1]);
                 }
             }
@@ -483,28 +490,35 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
 }
 
 // =====================================================================
-// Inter-chunk scan: one CTA per (sequence, value head, 64-row V block).
+// Inter-chunk scan on tcgen05: one CTA (4 warps) per (sequence, value head,
+// 64-row V block).  The state block S^T (k = TMEM lane / thread, 64 v) lives in
+// registers in fp32; per chunk:
+//   MMA1 (bf16)  Y[128 x 64]  = [Qg; W] S^T            (A: WQ image, B: S in bf16)
+//   Delta = U - Y[64..127]                              (threads 64..127, fp32 -> tf32)
+//   MMA3 (tf32)  Z[128 x 64]  = Kd^T Delta               (state update, k x v)
+//   MMA2 (tf32)  Y[0..63]    += P Delta                  (A = [P; 0], so rows 64.. untouched)
+//   S = S * exp(Gam_C) + Z ;  O = Y[0..63] -> out (bf16)
+// Thread 0 issues the MMAs and the bulk copies of the next chunk's record
+// parts as soon as the buffer they overwrite has been consumed.  Every wait is
+// bounded; on a timeout the CTA records KDA_ERR_DEVICE_TIMEOUT and stops.
 // =====================================================================
-constexpr int SC_THREADS = 256;
-constexpr int VB = 64;            // state rows per CTA
-constexpr int WQS = KD + 8;       // bf16 row stride of sWQ / sSb (halves)
-constexpr int PS = CH + 4;        // sP / sU stride
-constexpr int KDS = KD + 8;       // sKd stride
-constexpr int DS = VB + 8;        // sDelta stride
+constexpr int SC_THREADS = 128;
+constexpr int VB = 64;   // state rows (v) per CTA
 
-struct ScanSmem {
-    uint16_t WQ[2 * CH][WQS];   // rows 0..63: W, rows 64..127: Qg (bf16)
-    uint16_t Sb[VB][WQS];       // state block, bf16, [v][k]
-    float P[CH][PS];
-    float Kd[CH][KDS];
-    float U[CH][PS];            // U[:, vblock]
-    float D[CH][DS];            // Delta (tf32)
-    float gC[KD];
-};
+constexpr uint32_t SS_WQ = 0;          // 32 KiB  A of MMA1: 128 rows x 128 bf16
+constexpr uint32_t SS_PP = 32768;      // 32 KiB  A of MMA2: 128 rows x 64 tf32, rows 64..127 zero
+constexpr uint32_t SS_KDT = 65536;     // 32 KiB  A of MMA3: 128 rows x 64 tf32
+constexpr uint32_t SS_SB = 98304;      // 16 KiB  B of MMA1: 64 rows (v) x 128 bf16 (k)
+constexpr uint32_t SS_DT = 114688;     // 16 KiB  B of MMA2/3: 64 rows (v) x 64 tf32 (r)
+constexpr uint32_t SS_U = 131072;      // 16 KiB  U block, fp32 [64 r][64 v]
+constexpr uint32_t SS_GC = 147456;     // 512 B
+constexpr uint32_t SS_BAR = 147968;    // 6 mbarriers
+constexpr uint32_t SS_SLOT = 148032;   // TMEM address slot
+constexpr uint32_t SS_FLAG = 148036;   // abort flag
+constexpr uint32_t SS_BYTES = 148096 + 1024;   // + alignment slack
 
 struct ScanParams {
-    const uint16_t *W, *Qg;
-    const float *P, *Kd, *U, *gC;
+    const unsigned char *rec;
     const SeqDesc *seqs;
     const int *order;
     const int *hdr;
@@ -514,36 +528,12 @@ struct ScanParams {
     int H_v, nseq;
 };
 
-__device__ __forceinline__ void scan_load_wq(ScanSmem &s, const ScanParams &p, size_t ch, int tid) {
-    for (int idx = tid; idx < 2 * CH * (KD / 8); idx += SC_THREADS) {
-        const int r = idx >> 4, c8 = (idx & 15) * 8;
-        const uint16_t *src = (r < CH) ? p.W + (ch * CH + r) * KD + c8 : p.Qg + (ch * CH + r - CH) * KD + c8;
-        cp_async16(&s.WQ[r][c8], src);
-    }
-}
-__device__ __forceinline__ void scan_load_u(ScanSmem &s, const ScanParams &p, size_t ch, int vb, int tid) {
-    for (int idx = tid; idx < CH * (VB / 4); idx += SC_THREADS) {
-        const int r = idx >> 4, c4 = (idx & 15) * 4;
-        cp_async16(&s.U[r][c4], p.U + (ch * CH + r) * KD + vb * VB + c4);
-    }
-}
-__device__ __forceinline__ void scan_load_p(ScanSmem &s, const ScanParams &p, size_t ch, int tid) {
-    for (int idx = tid; idx < CH * (CH / 4); idx += SC_THREADS) {
-        const int r = idx >> 4, c4 = (idx & 15) * 4;
-        cp_async16(&s.P[r][c4], p.P + (ch * CH + r) * CH + c4);
-    }
-}
-__device__ __forceinline__ void scan_load_kd(ScanSmem &s, const ScanParams &p, size_t ch, int tid) {
-    for (int idx = tid; idx < CH * (KD / 4); idx += SC_THREADS) {
-        const int r = idx >> 5, c4 = (idx & 31) * 4;
-        cp_async16(&s.Kd[r][c4], p.Kd + (ch * CH + r) * KD + c4);
-    }
-    if (tid < KD / 4) cp_async16(&s.gC[tid * 4], p.gC + ch * KD + tid * 4);
-}
+enum { BAR_WQ = 0, BAR_PK, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MMA2 };
 
 __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ScanSmem &s = *reinterpret_cast<ScanSmem *>(smem_raw);
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment for the swizzled operand atoms
+    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     if (p.hdr[1] == 0) return;
     const int vb = blockIdx.x & 1;
     const int h = (blockIdx.x >> 1) % p.H_v;
@@ -551,176 +541,226 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
     if (rank >= p.nseq) return;
     const int seq = p.order[rank];
     const SeqDesc sd = p.seqs[seq];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int gq = lane >> 2, tq = lane & 3;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t bar = sbase + SS_BAR;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SS_FLAG);
 
-    // State ownership for the update: warp w -> v rows 16*(w&3).., k half (w>>2)*64.
-    const int sv0 = 16 * (warp & 3), sk0 = 64 * (warp >> 2);
-    float S[8][4];
-    const size_t sbase = (((size_t)seq * p.H_v + h) * KD + vb * VB) * KD;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const int v = sv0 + gq + 8 * hf, kk = sk0 + 8 * nt + 2 * tq;
-            float2 x = make_float2(0.f, 0.f);
-            if (p.init) x = *reinterpret_cast<const float2 *>(p.init + sbase + (size_t)v * KD + kk);
-            S[nt][2 * hf] = x.x;
-            S[nt][2 * hf + 1] = x.y;
-        }
-    auto store_sb = [&]() {
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int v = sv0 + gq + 8 * hf, kk = sk0 + 8 * nt + 2 * tq;
-                *reinterpret_cast<uint32_t *>(&s.Sb[v][kk]) = pack_bf16x2(S[nt][2 * hf], S[nt][2 * hf + 1]);
-            }
-    };
-    store_sb();
-
-    if (sd.nchunk > 0) {
-        const size_t ch0 = (size_t)sd.chunk0 * p.H_v + h;
-        scan_load_wq(s, p, ch0, tid);
-        cp_async_commit();
-        scan_load_u(s, p, ch0, vb, tid);
-        cp_async_commit();
-        scan_load_p(s, p, ch0, tid);
-        cp_async_commit();
-        scan_load_kd(s, p, ch0, tid);
-        cp_async_commit();
+    // zero rows 64..127 of the P operand (both K atoms); they are never rewritten
+    for (int i = tid; i < 2 * 8192 / 16; i += SC_THREADS) {
+        const int atom = i / 512, o = (i % 512) * 16;
+        *reinterpret_cast<uint4 *>(sm + SS_PP + atom * 16384 + 8192 + o) = make_uint4(0, 0, 0, 0);
     }
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(bar + 8 * i, 1);
+        mbar_fence_init();
+        *abort_flag = 0;
+    }
+    if (warp == 0) tmem_alloc(sbase + SS_SLOT, 128);
+    // state block: thread k holds S[v][k] for the 64 v of this block
+    float S[VB];
+    const size_t st0 = (((size_t)seq * p.H_v + h) * KD + (size_t)vb * VB) * KD + tid;
+#pragma unroll
+    for (int v = 0; v < VB; ++v) S[v] = p.init ? p.init[st0 + (size_t)v * KD] : 0.f;
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + SS_SLOT);
+    const uint32_t tY = tmem, tZ = tmem + 64;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
 
-    for (int c = 0; c < sd.nchunk; ++c) {
-        const size_t chc = ((size_t)sd.chunk0 + c) * p.H_v + h;
-        const size_t chn = chc + p.H_v;
-        const bool has_next = (c + 1 < sd.nchunk);
+    auto rec_of = [&](int c) { return p.rec + (((size_t)sd.chunk0 + c) * p.H_v + h) * REC_BYTES; };
+    auto issue_wq = [&](int c) {
+        mbar_expect_tx(bar + 8 * BAR_WQ, 32768);
+        bulk_g2s(sbase + SS_WQ, rec_of(c) + REC_WQ, 32768, bar + 8 * BAR_WQ);
+    };
+    auto issue_pk = [&](int c) {
+        const unsigned char *r = rec_of(c);
+        mbar_expect_tx(bar + 8 * BAR_PK, 8192 * 2 + 32768);
+        bulk_g2s(sbase + SS_PP, r + REC_P, 8192, bar + 8 * BAR_PK);
+        bulk_g2s(sbase + SS_PP + 16384, r + REC_P + 8192, 8192, bar + 8 * BAR_PK);
+        bulk_g2s(sbase + SS_KDT, r + REC_KDT, 32768, bar + 8 * BAR_PK);
+    };
+    auto issue_u = [&](int c) {
+        const unsigned char *r = rec_of(c);
+        mbar_expect_tx(bar + 8 * BAR_U, 16384 + 512);
+        bulk_g2s(sbase + SS_U, r + REC_U + vb * 16384, 16384, bar + 8 * BAR_U);
+        bulk_g2s(sbase + SS_GC, r + REC_GC, 512, bar + 8 * BAR_U);
+    };
+    // outstanding copy phases per barrier (for the bounded drain on abort)
+    int pend_wq = 0, pend_pk = 0, pend_u = 0;
+    if (tid == 0 && sd.nchunk > 0) {
+        issue_wq(0);
+        issue_pk(0);
+        issue_u(0);
+    }
+    pend_wq = pend_pk = pend_u = (sd.nchunk > 0);
+
+    const uint32_t id_b = idesc_bf16(128, VB), id_t = idesc_tf32(128, VB);
+    int c = 0;
+    for (; c < sd.nchunk; ++c) {
+        const uint32_t ph = c & 1;
+        const bool has_next = c + 1 < sd.nchunk;
         const int len = min(CH, sd.len - c * CH);
         const int tok0 = sd.tok + c * CH;
-
-        // ---- 1. Y = [W; Qg] Sb^T   (warp w: rows 16w..16w+15 of the stacked 128)
-        cp_async_wait<3>();
+        // ---- S (bf16) -> SB:  element (v, k) of the B operand
+#pragma unroll
+        for (int v = 0; v < VB; ++v)
+            *reinterpret_cast<uint16_t *>(sm + SS_SB + sw128_off(v, 2 * tid, VB)) = f_to_bf16(S[v]);
+        fence_async_smem();
+        tc_fence_before();
         __syncthreads();
-        float Y[8][4];
+        // ---- MMA1
+        if (tid == 0) {
+            if (!mbar_wait(bar + 8 * BAR_WQ, ph)) {
+                set_status(KDA_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            } else {
+                tc_fence_after();
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+                for (int ks = 0; ks < KD / 16; ++ks) {
+                    const int kb = ks * 32;
+                    const uint64_t ad = umma_desc(sbase + SS_WQ + (kb >> 7) * 16384 + (kb & 127), 16, 1024);
+                    const uint64_t bd = umma_desc(sbase + SS_SB + (kb >> 7) * 8192 + (kb & 127), 16, 1024);
+                    umma_bf16(tY, ad, bd, id_b, ks > 0);
+                }
+                umma_commit(bar + 8 * BAR_MMA1);
+            }
+            pend_wq = 0;
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+        const bool ok1 = mbar_wait(bar + 8 * BAR_MMA1, ph);
+        const bool oku = mbar_wait(bar + 8 * BAR_U, ph);
+        if (!ok1 || !oku) {
+            set_status(KDA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
+        }
+        tc_fence_after();
+        if (tid == 0 && has_next && ok1) {
+            issue_wq(c + 1);
+            pend_wq = 1;
+        }
+        const float g = reinterpret_cast<const float *>(sm + SS_GC)[tid];
+        // ---- Delta = U - W S^T (rows r = tid - 64), written as B operand (v, r)
+        if (warp >= 2 && ok1 && oku) {
+            const int r = tid - 64;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) Y[nt][e] = 0.f;
-        {
-            const int ra = 16 * warp + gq;
+            for (int half = 0; half < 2; ++half) {
+                float y[32];
+                tmem_ld32(tY + lane_off + half * 32, y);
+                const float *urow = reinterpret_cast<const float *>(sm + SS_U) + r * 64 + half * 32;
 #pragma unroll
-            for (int ks = 0; ks < KD / 16; ++ks) {
-                const int ca = 16 * ks + 2 * tq;
-                const uint32_t af[4] = {*reinterpret_cast<const uint32_t *>(&s.WQ[ra][ca]),
-                                        *reinterpret_cast<const uint32_t *>(&s.WQ[ra + 8][ca]),
-                                        *reinterpret_cast<const uint32_t *>(&s.WQ[ra][ca + 8]),
-                                        *reinterpret_cast<const uint32_t *>(&s.WQ[ra + 8][ca + 8])};
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-                    const int n = 8 * nt + gq;
-                    const uint32_t bf[2] = {*reinterpret_cast<const uint32_t *>(&s.Sb[n][ca]),
-                                            *reinterpret_cast<const uint32_t *>(&s.Sb[n][ca + 8])};
-                    mma_bf16(Y[nt], af, bf);
+                for (int j = 0; j < 32; ++j) {
+                    const int v = half * 32 + j;
+                    *reinterpret_cast<float *>(sm + SS_DT + sw128_off(v, 4 * r, VB)) = to_tf32(urow[j] - y[j]);
                 }
             }
         }
-        __syncthreads();   // everyone done with WQ and Sb
-        if (has_next) scan_load_wq(s, p, chn, tid);
-        cp_async_commit();
-
-        // ---- 2. Delta = U - W S^T   (warps 0..3)
-        cp_async_wait<3>();
+        fence_async_smem();
+        tc_fence_before();
         __syncthreads();
-        if (warp < 4) {
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int r = 16 * warp + gq + 8 * hf, v = 8 * nt + 2 * tq;
-                    s.D[r][v] = to_tf32(s.U[r][v] - Y[nt][2 * hf]);
-                    s.D[r][v + 1] = to_tf32(s.U[r][v + 1] - Y[nt][2 * hf + 1]);
-                }
-        }
-        __syncthreads();
-        if (has_next) scan_load_u(s, p, chn, vb, tid);
-        cp_async_commit();
-
-        // ---- 3. O = Qg S^T + P Delta   (warps 4..7: output rows 16(w-4)..)
-        cp_async_wait<3>();
-        __syncthreads();
-        if (warp >= 4) {
-            const int ra = 16 * (warp - 4) + gq;
-            const int kmax = (warp - 4 + 1) * 2;   // P is lower triangular
-            for (int ks = 0; ks < kmax; ++ks) {
-                const int ca = 8 * ks + tq;
-                const uint32_t af[4] = {__float_as_uint(s.P[ra][ca]), __float_as_uint(s.P[ra + 8][ca]),
-                                        __float_as_uint(s.P[ra][ca + 4]), __float_as_uint(s.P[ra + 8][ca + 4])};
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-                    const int n = 8 * nt + gq;
-                    const uint32_t bf[2] = {__float_as_uint(s.D[ca][n]), __float_as_uint(s.D[ca + 4][n])};
-                    mma_tf32(Y[nt], af, bf);
-                }
+        if (*abort_flag) break;
+        if (tid == 0) {
+            pend_u = 0;
+            if (has_next) {
+                issue_u(c + 1);
+                pend_u = 1;
             }
+            // ---- MMA3 (state update) then MMA2 (output correction)
+            if (!mbar_wait(bar + 8 * BAR_PK, ph)) {
+                set_status(KDA_ERR_DEVICE_TIMEOUT);
+                *abort_flag = 1;
+            } else {
+                tc_fence_after();
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int r = ra + 8 * hf, v = vb * VB + 8 * nt + 2 * tq;
-                    if (r < len)
-                        *reinterpret_cast<uint32_t *>(&p.out[((size_t)(tok0 + r) * p.H_v + h) * KD + v]) =
-                            pack_bf16x2(Y[nt][2 * hf], Y[nt][2 * hf + 1]);
+                for (int ks = 0; ks < CH / 8; ++ks) {
+                    const int kb = ks * 32;
+                    const uint64_t ad = umma_desc(sbase + SS_KDT + (kb >> 7) * 16384 + (kb & 127), 16, 1024);
+                    const uint64_t bd = umma_desc(sbase + SS_DT + (kb >> 7) * 8192 + (kb & 127), 16, 1024);
+                    umma_tf32(tZ, ad, bd, id_t, ks > 0);
                 }
+                umma_commit(bar + 8 * BAR_MMA3);
+#pragma unroll
+                for (int ks = 0; ks < CH / 8; ++ks) {
+                    const int kb = ks * 32;
+                    const uint64_t ad = umma_desc(sbase + SS_PP + (kb >> 7) * 16384 + (kb & 127), 16, 1024);
+                    const uint64_t bd = umma_desc(sbase + SS_DT + (kb >> 7) * 8192 + (kb & 127), 16, 1024);
+                    umma_tf32(tY, ad, bd, id_t, 1);
+                }
+                umma_commit(bar + 8 * BAR_MMA2);
+            }
+            pend_pk = 0;
         }
         __syncthreads();
-        if (has_next) scan_load_p(s, p, chn, tid);
-        cp_async_commit();
-
-        // ---- 4. S = S Diag(gC) + Delta^T Kd
-        cp_async_wait<3>();
-        __syncthreads();
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const int kk = sk0 + 8 * nt + 2 * tq;
-            const float g0 = s.gC[kk], g1 = s.gC[kk + 1];
-            S[nt][0] *= g0;
-            S[nt][1] *= g1;
-            S[nt][2] *= g0;
-            S[nt][3] *= g1;
+        if (*abort_flag) break;
+        const bool ok3 = mbar_wait(bar + 8 * BAR_MMA3, ph);
+        const bool ok2 = mbar_wait(bar + 8 * BAR_MMA2, ph);
+        if (!ok3 || !ok2) {
+            set_status(KDA_ERR_DEVICE_TIMEOUT);
+            *abort_flag = 1;
         }
-        {
-            const int va = sv0 + gq;
+        tc_fence_after();
+        if (ok3 && ok2) {
+            // ---- S = S * exp(Gam_C) + Z
 #pragma unroll
-            for (int ks = 0; ks < CH / 8; ++ks) {
-                const int ra = 8 * ks + tq;
-                const uint32_t af[4] = {__float_as_uint(s.D[ra][va]), __float_as_uint(s.D[ra][va + 8]),
-                                        __float_as_uint(s.D[ra + 4][va]), __float_as_uint(s.D[ra + 4][va + 8])};
+            for (int half = 0; half < 2; ++half) {
+                float z[32];
+                tmem_ld32(tZ + lane_off + half * 32, z);
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt) {
-                    const int n = sk0 + 8 * nt + gq;
-                    const uint32_t bf[2] = {__float_as_uint(s.Kd[ra][n]), __float_as_uint(s.Kd[ra + 4][n])};
-                    mma_tf32(S[nt], af, bf);
+                for (int j = 0; j < 32; ++j) S[half * 32 + j] = fmaf(S[half * 32 + j], g, z[j]);
+            }
+            // ---- output rows r = tid (warps 0, 1)
+            if (warp < 2) {
+                const int r = tid;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float y[32];
+                    tmem_ld32(tY + lane_off + half * 32, y);
+                    if (r < len) {
+                        uint16_t *dst = p.out + ((size_t)(tok0 + r) * p.H_v + h) * KD + vb * VB + half * 32;
+#pragma unroll
+                        for (int j = 0; j < 32; j += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(y[j], y[j + 1]);
+                            w.y = pack_bf16x2(y[j + 2], y[j + 3]);
+                            w.z = pack_bf16x2(y[j + 4], y[j + 5]);
+                            w.w = pack_bf16x2(y[j + 6], y[j + 7]);
+                            *reinterpret_cast<uint4 *>(dst + j) = w;
+                        }
+                    }
                 }
             }
         }
-        __syncthreads();   // done with D, Kd, gC
-        if (has_next) scan_load_kd(s, p, chn, tid);
-        cp_async_commit();
-        store_sb();
-        // the next iteration's first barrier publishes Sb
+        tc_fence_before();
+        __syncthreads();
+        if (*abort_flag) break;
+        if (tid == 0 && has_next) {
+            issue_pk(c + 1);
+            pend_pk = 1;
+        }
     }
-    cp_async_wait<0>();
-
-    if (p.fin) {
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int v = sv0 + gq + 8 * hf, kk = sk0 + 8 * nt + 2 * tq;
-                *reinterpret_cast<float2 *>(p.fin + sbase + (size_t)v * KD + kk) =
-                    make_float2(S[nt][2 * hf], S[nt][2 * hf + 1]);
-            }
+    // ---- drain: on abort, wait (bounded) for copies still in flight
+    if (tid == 0 && c < sd.nchunk) {
+        // copies issued for chunk c (parity c & 1) or c + 1 (the other parity)
+        for (uint32_t ph = 0; ph < 2; ++ph) {
+            if (pend_wq) mbar_wait(bar + 8 * BAR_WQ, ph, 1u << 16);
+            if (pend_pk) mbar_wait(bar + 8 * BAR_PK, ph, 1u << 16);
+            if (pend_u) mbar_wait(bar + 8 * BAR_U, ph, 1u << 16);
+            mbar_wait(bar + 8 * BAR_MMA1, ph, 1u << 16);
+            mbar_wait(bar + 8 * BAR_MMA3, ph, 1u << 16);
+            mbar_wait(bar + 8 * BAR_MMA2, ph, 1u << 16);
+        }
     }
+    if (p.fin && !*abort_flag) {
+        float *dst = p.fin + st0;
+#pragma unroll
+        for (int v = 0; v < VB; ++v) dst[(size_t)v * KD] = S[v];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // =====================================================================
@@ -731,8 +771,7 @@ struct FwdWorkspace {
     SeqDesc *seqs;
     ChunkDesc *chunks;
     int *order;
-    uint16_t *W, *Qg;
-    float *P, *Kd, *U, *gC;
+    unsigned char *rec;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -757,12 +796,7 @@ size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspa
     w.seqs = (SeqDesc *)take(sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1));
     w.chunks = (ChunkDesc *)take(sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1));
     w.order = (int *)take(sizeof(int) * (size_t)(nseq > 0 ? nseq : 1));
-    w.W = (uint16_t *)take(2 * (size_t)nch * CH * KD);
-    w.Qg = (uint16_t *)take(2 * (size_t)nch * CH * KD);
-    w.P = (float *)take(4 * (size_t)nch * CH * CH);
-    w.Kd = (float *)take(4 * (size_t)nch * CH * KD);
-    w.U = (float *)take(4 * (size_t)nch * CH * KD);
-    w.gC = (float *)take(4 * (size_t)nch * KD);
+    w.rec = (unsigned char *)take((size_t)nch * REC_BYTES);
     if (ws) *ws = w;
     return off;
 }
@@ -781,7 +815,7 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         cudaError_t e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)sizeof(IntraSmem));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(ScanSmem));
+        e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS_BYTES);
         if (e != cudaSuccess) return e;
     }
     plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu, N, B, T, ws.seqs, ws.chunks, ws.order, ws.hdr, nck);
@@ -792,7 +826,7 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         IntraParams ip;
         ip.q = q; ip.k = k; ip.v = v; ip.graw = graw; ip.b = b; ip.A_log = A_log; ip.scale = scale;
         ip.H_qk = H_qk; ip.H_v = H_v; ip.chunks = ws.chunks; ip.hdr = ws.hdr;
-        ip.W = ws.W; ip.Qg = ws.Qg; ip.P = ws.P; ip.Kd = ws.Kd; ip.U = ws.U; ip.gC = ws.gC;
+        ip.rec = ws.rec;
         intra_kernel<<<dim3((unsigned)nck, (unsigned)H_v), IN_THREADS, sizeof(IntraSmem), stream>>>(ip);
         ++*launches;
         e = cudaGetLastError();
@@ -800,11 +834,11 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     }
     if (nseq > 0) {
         ScanParams sp;
-        sp.W = ws.W; sp.Qg = ws.Qg; sp.P = ws.P; sp.Kd = ws.Kd; sp.U = ws.U; sp.gC = ws.gC;
+        sp.rec = ws.rec;
         sp.seqs = ws.seqs; sp.order = ws.order; sp.hdr = ws.hdr;
         sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq;
         const long long nblk = (long long)nseq * H_v * 2;
-        scan_kernel<<<(unsigned)nblk, SC_THREADS, sizeof(ScanSmem), stream>>>(sp);
+        scan_kernel<<<(unsigned)nblk, SC_THREADS, SS_BYTES, stream>>>(sp);
         ++*launches;
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
