@@ -17,6 +17,54 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
                        cudaStream_t stream, int *launches);
 struct FwdWorkspace;
 size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspace *ws, char *base);
+
+// ---- per-kernel event timing (measurement aid, off by default)
+namespace {
+constexpr int kMaxTimed = 8;
+struct TimingState {
+    bool enabled = false;
+    int n = 0;
+    const char *names[kMaxTimed] = {nullptr};
+    cudaEvent_t ev[kMaxTimed + 1] = {nullptr};
+};
+thread_local TimingState t_timing;
+}  // namespace
+
+int timing_enable(bool on) {
+    TimingState &t = t_timing;
+    if (on && !t.ev[0]) {
+        for (int i = 0; i <= kMaxTimed; ++i)
+            if (cudaEventCreate(&t.ev[i]) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    t.enabled = on;
+    t.n = 0;
+    return KDA_OK;
+}
+void timing_begin(cudaStream_t s) {
+    TimingState &t = t_timing;
+    t.n = 0;
+    if (t.enabled) cudaEventRecord(t.ev[0], s);
+}
+void timing_mark(const char *name, cudaStream_t s) {
+    TimingState &t = t_timing;
+    if (!t.enabled || t.n >= kMaxTimed) return;
+    t.names[t.n] = name;
+    cudaEventRecord(t.ev[t.n + 1], s);
+    ++t.n;
+}
+int timing_read(float *ms, const char **names, int max_n) {
+    TimingState &t = t_timing;
+    if (!t.enabled) return 0;
+    int n = t.n < max_n ? t.n : max_n;
+    for (int i = 0; i < n; ++i) {
+        if (cudaEventSynchronize(t.ev[i + 1]) != cudaSuccess) return KDA_ERR_CUDA;
+        float v = 0.f;
+        cudaEventElapsedTime(&v, t.ev[i], t.ev[i + 1]);
+        if (ms) ms[i] = v;
+        if (names) names[i] = t.names[i];
+    }
+    return n;
+}
 }  // namespace kda
 
 namespace {
@@ -70,6 +118,10 @@ int kda_get_status(cudaStream_t stream) {
 }
 
 int kda_last_launch_count(void) { return t_last_launches; }
+
+int kda_set_kernel_timing(int enable) { return kda::timing_enable(enable != 0); }
+
+int kda_kernel_times(float *ms, const char **names, int max_n) { return kda::timing_read(ms, names, max_n); }
 
 size_t kda_fwd_workspace_size(int N, int B, int T, int H_qk, int H_v, int K, int V) {
     if (K != kda::KD || V != kda::KD || B < 0 || T < 0 || H_qk <= 0 || H_v <= 0 || N < 0) return 0;
@@ -127,8 +179,10 @@ int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(graw) || !aligned16(state) ||
         !aligned16(out))
         return KDA_ERR_INVALID_ARG;
+    kda::timing_begin(stream);
     cudaError_t e = kda::launch_decode(q, k, v, graw, b, A_log, scale, state, B, H_qk, H_v, out, stream);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
+    kda::timing_mark("decode_kernel", stream);
     t_last_launches = 1;
     return KDA_OK;
 }

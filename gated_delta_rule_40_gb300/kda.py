@@ -67,6 +67,10 @@ def load() -> ctypes.CDLL:
     lib.kda_get_status.restype = I
     lib.kda_last_launch_count.argtypes = []
     lib.kda_last_launch_count.restype = I
+    lib.kda_set_kernel_timing.argtypes = [I]
+    lib.kda_set_kernel_timing.restype = I
+    lib.kda_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_char_p), I]
+    lib.kda_kernel_times.restype = I
     _lib = lib
     return lib
 
@@ -217,3 +221,18 @@ def kda_get_status(stream=None) -> int:
 
 def kda_last_launch_count() -> int:
     return int(load().kda_last_launch_count())
+
+
+def kda_set_kernel_timing(enable: bool) -> None:
+    _raise(load().kda_set_kernel_timing(1 if enable else 0), "kda_set_kernel_timing")
+
+
+def kda_kernel_times() -> list:
+    """[(kernel name, ms)] for the most recent call on this thread (timing on)."""
+    lib = load()
+    ms = (ctypes.c_float * 8)()
+    names = (ctypes.c_char_p * 8)()
+    n = lib.kda_kernel_times(ms, names, 8)
+    if n < 0:
+        raise KdaError(n, "kda_kernel_times")
+    return [(names[i].decode(), float(ms[i])) for i in range(n)]

@@ -154,6 +154,17 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
  * kda_decode_step call on this host thread queued. */
 int kda_last_launch_count(void);
 
+/*
+ * Measurement aid (off by default).  While enabled, kda_fwd, kda_fwd_ws and
+ * kda_decode_step record a CUDA event on `stream` before their first and
+ * after each kernel launch.  kda_kernel_times waits for the events of the most
+ * recent call on this host thread and writes up to max_n per-kernel durations
+ * in milliseconds (and static kernel names when `names` is not NULL); it
+ * returns the number written, 0 when timing is off, or KDA_ERR_CUDA.
+ */
+int kda_set_kernel_timing(int enable);
+int kda_kernel_times(float *ms, const char **names, int max_n);
+
 #ifdef __cplusplus
 }
 #endif
