@@ -127,16 +127,16 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
 }
 
 // Per (chunk, value head) record written by the intra-chunk kernel and read
-// by the scan with bulk copies.  Every operand is stored as the exact shared
-// memory image the scan's tcgen05.mma reads (K-major, 128-byte swizzle):
+// by the scan with bulk copies.  The operands are stored as the exact shared
+// memory images the scan's tcgen05.mma reads (K-major, 128-byte swizzle):
 //   WQ  [Qg rows 0..63 ; W rows 64..127] x K=128, bf16          (32 KiB)
-//   P   rows 0..63 x 64 (j), tf32                                (16 KiB)
+//   P   rows r = 0..63 x 64 (j), bf16                            (8 KiB)
 //   KDT Kd^T: rows k = 0..127 x 64 (r), tf32                      (32 KiB)
-//   U   [V block 0 | V block 1], each [64 r][68] fp32 (64 v + 4 pad)  (34 KiB)
+//   U   [V block 0 | V block 1], each [64 v][68] fp32 (64 r + 4 pad)  (34 KiB)
 //   GC  exp(Gam_C) per channel, fp32                              (512 B)
-constexpr uint32_t REC_WQ = 0, REC_P = 32768, REC_KDT = 49152, REC_U = 81920, REC_GC = 116736;
+constexpr uint32_t REC_WQ = 0, REC_P = 32768, REC_KDT = 40960, REC_U = 73728, REC_GC = 108544;
 constexpr uint32_t REC_U_BLOCK = 64 * 68 * 4;   // 17408 B per V block
-constexpr uint32_t REC_BYTES = 117248;
+constexpr uint32_t REC_BYTES = 109056;
 
 // =====================================================================
 // Intra-chunk kernel: one CTA (16 warps) per (chunk, value head).
@@ -365,28 +365,20 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             for (int rr = 0; rr < 4; ++rr) gs[(warp * 4 + rr) * GSS + cc] = loc[rr] + off;
         }
         __syncthreads();
-        // 3b. per-channel tables
-        if (tid < SL) {
-            const int cc = tid;
-            float m[5];
-            m[0] = 0.f;
-            m[1] = gs[15 * GSS + cc];
-            m[2] = gs[31 * GSS + cc];
-            m[3] = gs[47 * GSS + cc];
-            m[4] = gs[63 * GSS + cc];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float mu = 0.5f * (gs[(16 * i) * GSS + cc] + gs[(16 * i + 15) * GSS + cc]);
-                tab[(TB_MU + i) * 32 + cc] = mu;
-                tab[(TB_EB + i) * 32 + cc] = ex2(m[i]);
-                tab[(TB_EA + i) * 32 + cc] = ex2(m[4] - m[i + 1]);
-            }
-#pragma unroll
-            for (int i = 0; i < 5; ++i) tab[(TB_M + i) * 32 + cc] = m[i];
-            tab[TB_D1 * 32 + cc] = ex2(m[2] - m[1]);
-            tab[TB_D2 * 32 + cc] = ex2(m[3] - m[2]);
-            tab[TB_D12 * 32 + cc] = ex2(m[3] - m[1]);
-            *reinterpret_cast<float *>(rec + REC_GC + 4 * (c0 + cc)) = ex2(m[4]);
+        // 3b. per-channel tables: thread t computes entry t / 32 of channel t % 32
+        for (int t = tid; t < 20 * SL; t += IN_THREADS) {
+            const int cc = t & 31, e = t >> 5;
+            auto mval = [&](int i) { return i == 0 ? 0.f : gs[(16 * i - 1) * GSS + cc]; };
+            float val;
+            if (e < 4) val = 0.5f * (gs[(16 * e) * GSS + cc] + gs[(16 * e + 15) * GSS + cc]);   // mu_e
+            else if (e < 9) val = mval(e - 4);                                                     // m_i
+            else if (e < 13) val = ex2(mval(e - 9));                                               // exp(m_i)
+            else if (e < 17) val = ex2(mval(4) - mval(e - 12));                                    // exp(m_4 - m_{i+1})
+            else if (e == 17) val = ex2(mval(2) - mval(1));
+            else if (e == 18) val = ex2(mval(3) - mval(2));
+            else val = ex2(mval(3) - mval(1));
+            tab[e * 32 + cc] = val;
+            if (e == 16) *reinterpret_cast<float *>(rec + REC_GC + 4 * (c0 + cc)) = ex2(mval(4));
         }
         // the previous slice's MMAs and Kd^T stores must be done with ROWS / COLS / KDS
         if (tid == 0) {
@@ -518,15 +510,17 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
                     make_float4(o[j] * be, o[j + 1] * be, o[j + 2] * be, o[j + 3] * be);
         } else {
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                sts128(sm + IS_PI + sw128_off(r, 4 * (16 * cb + j), CH), o[j], o[j + 1], o[j + 2], o[j + 3]);
+            for (int j = 0; j < 16; j += 8)
+                *reinterpret_cast<uint4 *>(sm + IS_PI + sw128_off(r, 2 * (16 * cb + j), CH)) =
+                    make_uint4(pack_bf16x2(o[j], o[j + 1]), pack_bf16x2(o[j + 2], o[j + 3]),
+                               pack_bf16x2(o[j + 4], o[j + 5]), pack_bf16x2(o[j + 6], o[j + 7]));
         }
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-        bulk_s2g(rec + REC_P, sbase + IS_PI, 16384);
+        bulk_s2g(rec + REC_P, sbase + IS_PI, 8192);
         bulk_commit();
     }
 
@@ -609,15 +603,17 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
         float wv[16], uv[16];
         tmem_ld16(t_w + lo + r0, wv);
         tmem_ld16(t_u + lo + r0, uv);
-        float *us = reinterpret_cast<float *>(sm + IS_US) + (kk >> 6) * (CH * 68) + (kk & 63);
+        float *us = reinterpret_cast<float *>(sm + IS_US) + (kk >> 6) * (CH * 68) + (kk & 63) * 68 + r0;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int r = r0 + j;
             const uint32_t ws_off = (uint32_t)(kk >> 6) * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
                                     (((((2 * kk) & 127) >> 4) ^ (r & 7)) << 4) + ((2 * kk) & 15);
             *reinterpret_cast<uint16_t *>(sm + IS_WS + ws_off) = f_to_bf16(wv[j]);
-            us[r * 68] = uv[j];
         }
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<float4 *>(us + j) = make_float4(uv[j], uv[j + 1], uv[j + 2], uv[j + 3]);
     }
     fence_async_smem();
     tc_fence_before();
@@ -634,32 +630,41 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
 }
 
 // =====================================================================
-// Inter-chunk scan on tcgen05: one CTA (4 warps) per (sequence, value head,
-// 64-row V block).  The state block S^T (k = TMEM lane / thread, 64 v) lives in
-// registers in fp32; per chunk:
-//   MMA1 (bf16)  Y[128 x 64]  = [Qg; W] S^T            (A: WQ image, B: S in bf16)
-//   Delta = U - Y[64..127]                              (threads 64..127, fp32 -> tf32)
-//   MMA3 (tf32)  Z[128 x 64]  = Kd^T Delta               (state update, k x v)
-//   MMA2 (tf32)  Y[0..63]    += P Delta                  (A = [P; 0], so rows 64.. untouched)
-//   S = S * exp(Gam_C) + Z ;  O = Y[0..63] -> out (bf16)
-// Thread 0 issues the MMAs and the bulk copies of the next chunk's record
-// parts as soon as the buffer they overwrite has been consumed.  Every wait is
-// bounded; on a timeout the CTA records KDA_ERR_DEVICE_TIMEOUT and stops.
+// Inter-chunk scan on tcgen05: one CTA per (sequence, value head, 64-row V
+// block): four epilogue warps and one issuer warp.
+//
+// Epilogue thread (k, half) keeps S[v][k] for the 32 v of its half of the
+// block in fp32 registers (warps w and w + 4 share TMEM lane quarter w).  Per chunk, in transposed form:
+//   MMA1 (bf16, M=64)   Y^T[v][m] = sum_k S[v][k] [Qg; W][m][k]      (A: S, MN-major; B: WQ image)
+//   Delta^T[v][r] = U[r][v] - Y^T[v][64 + r]                         (threads v)
+//   MMA3 (tf32, M=128)  Z[k][v]   = sum_r Kd^T[k][r] Delta^T[v][r]   (state update)
+//   MMA2 (bf16, M=64)   Y^T[v][r] += sum_j Delta^T[v][j] P[r][j]     (output correction)
+//   S = S * exp(Gam_C) + Z ;  O[r][v] = Y^T[v][r] -> out (bf16, via an smem transpose)
+// The issuer warp waits for the epilogue's "S written" and "Delta written"
+// mbarriers, issues the MMAs and the bulk copies of the chunk records (double
+// buffered, fetched a chunk ahead, L2-prefetched two chunks ahead), so MMA
+// issue never stalls the epilogue warps; the epilogue waits on the MMA commit
+// barriers.  The two Y^T accumulators alternate so the output epilogue of chunk
+// c overlaps MMA1 of chunk c + 1.  Every wait is bounded; a timeout records
+// KDA_ERR_DEVICE_TIMEOUT and both roles stop.
 // =====================================================================
-constexpr int SC_THREADS = 128;
-constexpr int VB = 64;   // state rows (v) per CTA
+constexpr int SC_EPI = 256;                // epilogue threads (warps 0..7)
+constexpr int SC_THREADS = SC_EPI + 32;    // + issuer warp
+constexpr int VB = 64;                     // state rows (v) per CTA
 
-constexpr uint32_t SS_WQ = 0;          // 32 KiB  A of MMA1: 128 rows x 128 bf16
-constexpr uint32_t SS_PP = 32768;      // 32 KiB  A of MMA2: 128 rows x 64 tf32, rows 64..127 zero
-constexpr uint32_t SS_KDT = 65536;     // 32 KiB  A of MMA3: 128 rows x 64 tf32
-constexpr uint32_t SS_SB = 98304;      // 16 KiB  B of MMA1: 64 rows (v) x 128 bf16 (k)
-constexpr uint32_t SS_DT = 114688;     // 16 KiB  B of MMA2/3: 64 rows (v) x 64 tf32 (r)
-constexpr uint32_t SS_U = 131072;      // 17 KiB  U block, fp32 [64 r][68]
-constexpr uint32_t SS_GC = 148480;     // 512 B
-constexpr uint32_t SS_BAR = 148992;    // 6 mbarriers
-constexpr uint32_t SS_SLOT = 149056;   // TMEM address slot
-constexpr uint32_t SS_FLAG = 149060;   // abort flag
-constexpr uint32_t SS_BYTES = 149120 + 1024;   // + alignment slack
+constexpr uint32_t SS_WQ = 0;          // 2 x 32 KiB  B of MMA1: 128 rows x 128 bf16 (K-major)
+constexpr uint32_t SS_KDT = 65536;     // 2 x 32 KiB  A of MMA3: 128 rows x 64 tf32
+constexpr uint32_t SS_P = 131072;      // 2 x 8 KiB   B of MMA2: 64 rows (r) x 64 bf16 (j)
+constexpr uint32_t SS_SB = 147456;     // 16 KiB      A of MMA1: S, MN-major bf16 (64 v x 128 k)
+constexpr uint32_t SS_DT = 163840;     // 16 KiB      Delta^T tf32: 64 rows (v) x 64 (r)   (B of MMA3)
+constexpr uint32_t SS_DTB = 180224;    // 8 KiB       Delta^T bf16: 64 rows (v) x 64 (j)  (A of MMA2)
+constexpr uint32_t SS_U = 188416;      // 17 KiB      U block, fp32 [64 v][68]
+constexpr uint32_t SS_OS = 205824;     // 8 KiB       output transpose, bf16 [64 r][64 v]
+constexpr uint32_t SS_GC = 214016;     // 512 B
+constexpr uint32_t SS_BAR = 214528;    // mbarriers
+constexpr uint32_t SS_SLOT = 214656;   // TMEM address slot
+constexpr uint32_t SS_FLAG = 214660;   // abort flag
+constexpr uint32_t SS_BYTES = 214720 + 1024;   // + alignment slack
 
 struct ScanParams {
     const unsigned char *rec;
@@ -672,11 +677,10 @@ struct ScanParams {
     int H_v, nseq;
 };
 
-enum { BAR_WQ = 0, BAR_PK, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MMA2 };
+enum { BAR_WQ0 = 0, BAR_WQ1, BAR_PK0, BAR_PK1, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MMA2, BAR_SBR, BAR_DTR };
 
 __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p) {
     extern __shared__ unsigned char smem_raw[];
-    // 1024-byte alignment for the swizzled operand atoms
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     if (p.hdr[1] == 0) return;
     const int vb = blockIdx.x & 1;
@@ -685,238 +689,221 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
     if (rank >= p.nseq) return;
     const int seq = p.order[rank];
     const SeqDesc sd = p.seqs[seq];
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t bar = sbase + SS_BAR;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + SS_FLAG);
+    const int n = sd.nchunk;
 
-    // zero rows 64..127 of the P operand (both K atoms); they are never rewritten
-    for (int i = tid; i < 2 * 8192 / 16; i += SC_THREADS) {
-        const int atom = i / 512, o = (i % 512) * 16;
-        *reinterpret_cast<uint4 *>(sm + SS_PP + atom * 16384 + 8192 + o) = make_uint4(0, 0, 0, 0);
-    }
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(bar + 8 * i, 1);
+        for (int i = 0; i < BAR_SBR; ++i) mbar_init(bar + 8 * i, 1);
+        mbar_init(bar + 8 * BAR_SBR, SC_EPI);
+        mbar_init(bar + 8 * BAR_DTR, SC_EPI);
         mbar_fence_init();
         *abort_flag = 0;
     }
-    if (warp == 0) tmem_alloc(sbase + SS_SLOT, 128);
-    // state block: thread k holds S[v][k] for the 64 v of this block
-    float S[VB];
-    const size_t st0 = (((size_t)seq * p.H_v + h) * KD + (size_t)vb * VB) * KD + tid;
-#pragma unroll
-    for (int v = 0; v < VB; ++v) S[v] = p.init ? p.init[st0 + (size_t)v * KD] : 0.f;
-    fence_async_smem();
+    if (warp == 0) tmem_alloc(sbase + SS_SLOT, 512);
+    // epilogue thread: channel k = tid & 127, v half = tid >> 7 (v = 32 half .. 32 half + 31)
+    const int kme = tid & 127, vhalf = (tid >> 7) & 1;
+    const size_t st0 = (((size_t)seq * p.H_v + h) * KD + (size_t)vb * VB + 32 * vhalf) * KD + kme;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + SS_SLOT);
-    const uint32_t tY = tmem, tZ = tmem + 64;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tZ = tmem + 256;   // 64 columns, lanes = k
 
     auto rec_of = [&](int c) { return p.rec + (((size_t)sd.chunk0 + c) * p.H_v + h) * REC_BYTES; };
-    auto issue_wq = [&](int c) {
-        mbar_expect_tx(bar + 8 * BAR_WQ, 32768);
-        bulk_g2s(sbase + SS_WQ, rec_of(c) + REC_WQ, 32768, bar + 8 * BAR_WQ);
+    auto fail = [&]() {
+        set_status(KDA_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
     };
-    auto issue_pk = [&](int c) {
-        const unsigned char *r = rec_of(c);
-        mbar_expect_tx(bar + 8 * BAR_PK, 8192 * 2 + 32768);
-        bulk_g2s(sbase + SS_PP, r + REC_P, 8192, bar + 8 * BAR_PK);
-        bulk_g2s(sbase + SS_PP + 16384, r + REC_P + 8192, 8192, bar + 8 * BAR_PK);
-        bulk_g2s(sbase + SS_KDT, r + REC_KDT, 32768, bar + 8 * BAR_PK);
-    };
-    auto issue_u = [&](int c) {
-        const unsigned char *r = rec_of(c);
-        mbar_expect_tx(bar + 8 * BAR_U, REC_U_BLOCK + 512);
-        bulk_g2s(sbase + SS_U, r + REC_U + vb * REC_U_BLOCK, REC_U_BLOCK, bar + 8 * BAR_U);
-        bulk_g2s(sbase + SS_GC, r + REC_GC, 512, bar + 8 * BAR_U);
-    };
-    // outstanding copy phases per barrier (for the bounded drain on abort)
-    int pend_wq = 0, pend_pk = 0, pend_u = 0;
-    if (tid == 0 && sd.nchunk > 0) {
-        issue_wq(0);
-        issue_pk(0);
-        issue_u(0);
-    }
-    pend_wq = pend_pk = pend_u = (sd.nchunk > 0);
 
-    const uint32_t id_b = idesc_bf16(128, VB), id_t = idesc_tf32(128, VB);
-    int c = 0;
-    for (; c < sd.nchunk; ++c) {
-        const uint32_t ph = c & 1;
-        const bool has_next = c + 1 < sd.nchunk;
-        const int len = min(CH, sd.len - c * CH);
-        const int tok0 = sd.tok + c * CH;
-        // ---- S (bf16) -> SB, MN-major B operand (v contiguous): row k of K-group k / 8
-#pragma unroll
-        for (int c8 = 0; c8 < VB / 8; ++c8) {
-            uint4 w;
-            w.x = pack_bf16x2(S[8 * c8 + 0], S[8 * c8 + 1]);
-            w.y = pack_bf16x2(S[8 * c8 + 2], S[8 * c8 + 3]);
-            w.z = pack_bf16x2(S[8 * c8 + 4], S[8 * c8 + 5]);
-            w.w = pack_bf16x2(S[8 * c8 + 6], S[8 * c8 + 7]);
-            *reinterpret_cast<uint4 *>(sm + SS_SB + (tid >> 3) * 1024 + (tid & 7) * 128 + ((c8 ^ (tid & 7)) << 4)) = w;
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- MMA1
-        if (tid == 0) {
-            if (!mbar_wait(bar + 8 * BAR_WQ, ph)) {
-                set_status(KDA_ERR_DEVICE_TIMEOUT);
-                *abort_flag = 1;
-            } else {
+    if (warp == SC_EPI / 32) {
+        // ------------------------------------------------------------ issuer
+        if (lane == 0) {
+            auto issue_wq = [&](int c) {
+                const uint32_t b = bar + 8 * (BAR_WQ0 + (c & 1));
+                mbar_expect_tx(b, 32768);
+                bulk_g2s(sbase + SS_WQ + (c & 1) * 32768, rec_of(c) + REC_WQ, 32768, b);
+            };
+            auto issue_pk = [&](int c) {
+                const unsigned char *r = rec_of(c);
+                const uint32_t b = bar + 8 * (BAR_PK0 + (c & 1));
+                mbar_expect_tx(b, 8192 + 32768);
+                bulk_g2s(sbase + SS_P + (c & 1) * 8192, r + REC_P, 8192, b);
+                bulk_g2s(sbase + SS_KDT + (c & 1) * 32768, r + REC_KDT, 32768, b);
+            };
+            auto issue_u = [&](int c) {
+                const unsigned char *r = rec_of(c);
+                mbar_expect_tx(bar + 8 * BAR_U, REC_U_BLOCK + 512);
+                bulk_g2s(sbase + SS_U, r + REC_U + vb * REC_U_BLOCK, REC_U_BLOCK, bar + 8 * BAR_U);
+                bulk_g2s(sbase + SS_GC, r + REC_GC, 512, bar + 8 * BAR_U);
+            };
+            const uint32_t id1 = idesc_bf16(64, 128) | (1u << 15);   // A (S) MN-major
+            const uint32_t id2 = idesc_bf16(64, 64), id3 = idesc_tf32(128, VB);
+            if (n > 0) {
+                issue_wq(0);
+                issue_pk(0);
+                issue_u(0);
+            }
+            for (int c = 0; c < n && !*abort_flag; ++c) {
+                const int b = c & 1;
+                const uint32_t pp = (c >> 1) & 1;
+                const uint32_t tY = tmem + b * 128;
+                if (!mbar_wait(bar + 8 * BAR_SBR, c & 1) || !mbar_wait(bar + 8 * (BAR_WQ0 + b), pp)) { fail(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < KD / 16; ++ks) {
                     const int kb = ks * 32;
-                    const uint64_t ad = umma_desc(sbase + SS_WQ + (kb >> 7) * 16384 + (kb & 127), 16, 1024);
-                    // 16 k per instruction = two 8-row K groups of the MN-major image
-                    const uint64_t bd = umma_desc(sbase + SS_SB + ks * 2048, 8192, 1024);
-                    umma_bf16(tY, ad, bd, id_b | (1u << 16), ks > 0);
+                    umma_bf16(tY, umma_desc(sbase + SS_SB + ks * 2048, 8192, 1024),
+                              umma_desc(sbase + SS_WQ + b * 32768 + (kb >> 7) * 16384 + (kb & 127), 16, 1024), id1,
+                              ks > 0);
                 }
                 umma_commit(bar + 8 * BAR_MMA1);
-            }
-            pend_wq = 0;
-        }
-        __syncthreads();
-        if (*abort_flag) break;
-        const bool ok1 = mbar_wait(bar + 8 * BAR_MMA1, ph);
-        const bool oku = mbar_wait(bar + 8 * BAR_U, ph);
-        if (!ok1 || !oku) {
-            set_status(KDA_ERR_DEVICE_TIMEOUT);
-            *abort_flag = 1;
-        }
-        tc_fence_after();
-        if (tid == 0 && has_next && ok1) {
-            issue_wq(c + 1);
-            pend_wq = 1;
-        }
-        const float g = reinterpret_cast<const float *>(sm + SS_GC)[tid];
-        // ---- Delta = U - W S^T (rows r = tid - 64), written as B operand (v, r)
-        if (warp >= 2 && ok1 && oku) {
-            const int r = tid - 64;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float y[32];
-                tmem_ld32(tY + lane_off + half * 32, y);
-                const float *urow = reinterpret_cast<const float *>(sm + SS_U) + r * 68 + half * 32;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 u4 = *reinterpret_cast<const float4 *>(urow + j);
-                    const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int v = half * 32 + j + e;
-                        *reinterpret_cast<float *>(sm + SS_DT + sw128_off(v, 4 * r, VB)) = to_tf32(uu[e] - y[j + e]);
-                    }
+                if (c + 1 < n) {
+                    // buffers (c + 1) & 1 were last read by the MMAs of chunk c - 1
+                    if (c >= 1 && !mbar_wait(bar + 8 * BAR_MMA2, (c - 1) & 1)) { fail(); break; }
+                    issue_wq(c + 1);
+                    issue_pk(c + 1);
                 }
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (*abort_flag) break;
-        if (tid == 0) {
-            pend_u = 0;
-            if (has_next) {
-                issue_u(c + 1);
-                pend_u = 1;
-            }
-            // ---- MMA3 (state update) then MMA2 (output correction)
-            if (!mbar_wait(bar + 8 * BAR_PK, ph)) {
-                set_status(KDA_ERR_DEVICE_TIMEOUT);
-                *abort_flag = 1;
-            } else {
+                if (c + 2 < n) {
+                    const unsigned char *r2 = rec_of(c + 2);
+                    prefetch_l2(r2 + REC_WQ, 32768 + 8192 + 32768);
+                    prefetch_l2(r2 + REC_U + vb * REC_U_BLOCK, REC_U_BLOCK);
+                    prefetch_l2(r2 + REC_GC, 512);
+                }
+                if (!mbar_wait(bar + 8 * BAR_DTR, c & 1)) { fail(); break; }
+                if (c + 1 < n) issue_u(c + 1);
+                if (!mbar_wait(bar + 8 * (BAR_PK0 + b), pp)) { fail(); break; }
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < CH / 8; ++ks) {
                     const int kb = ks * 32;
-                    const uint64_t ad = umma_desc(sbase + SS_KDT + (kb >> 7) * 16384 + (kb & 127), 16, 1024);
-                    const uint64_t bd = umma_desc(sbase + SS_DT + (kb >> 7) * 8192 + (kb & 127), 16, 1024);
-                    umma_tf32(tZ, ad, bd, id_t, ks > 0);
+                    umma_tf32(tZ, umma_desc(sbase + SS_KDT + b * 32768 + (kb >> 7) * 16384 + (kb & 127), 16, 1024),
+                              umma_desc(sbase + SS_DT + (kb >> 7) * 8192 + (kb & 127), 16, 1024), id3, ks > 0);
                 }
                 umma_commit(bar + 8 * BAR_MMA3);
 #pragma unroll
-                for (int ks = 0; ks < CH / 8; ++ks) {
-                    const int kb = ks * 32;
-                    const uint64_t ad = umma_desc(sbase + SS_PP + (kb >> 7) * 16384 + (kb & 127), 16, 1024);
-                    const uint64_t bd = umma_desc(sbase + SS_DT + (kb >> 7) * 8192 + (kb & 127), 16, 1024);
-                    umma_tf32(tY, ad, bd, id_t, 1);
+                for (int ks = 0; ks < CH / 16; ++ks) {
+                    umma_bf16(tY, umma_desc(sbase + SS_DTB + ks * 32, 16, 1024),
+                              umma_desc(sbase + SS_P + b * 8192 + ks * 32, 16, 1024), id2, 1);
                 }
                 umma_commit(bar + 8 * BAR_MMA2);
             }
-            pend_pk = 0;
+            // drain whatever is still in flight (bounded)
+            for (int i = 0; i < BAR_SBR; ++i)
+                for (uint32_t pp = 0; pp < 2; ++pp) mbar_wait(bar + 8 * i, pp, *abort_flag ? (1u << 14) : 0u);
         }
-        __syncthreads();
-        if (*abort_flag) break;
-        const bool ok3 = mbar_wait(bar + 8 * BAR_MMA3, ph);
-        const bool ok2 = mbar_wait(bar + 8 * BAR_MMA2, ph);
-        if (!ok3 || !ok2) {
-            set_status(KDA_ERR_DEVICE_TIMEOUT);
-            *abort_flag = 1;
-        }
-        tc_fence_after();
-        if (ok3 && ok2) {
-            // ---- S = S * exp(Gam_C) + Z
+    } else {
+        // ------------------------------------------------------------ epilogue (thread k = tid)
+        constexpr int VH = VB / 2;
+        float S[VH];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float z[32];
-                tmem_ld32(tZ + lane_off + half * 32, z);
+        for (int v = 0; v < VH; ++v) S[v] = p.init ? p.init[st0 + (size_t)v * KD] : 0.f;
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+        const int vme = q * 16 + lane;      // v owned in the M = 64 layout (lane < 16)
+        const bool vact = lane < 16;
+        auto emit_output = [&](int cc) {
+            if (!mbar_wait(bar + 8 * BAR_MMA2, cc & 1)) fail();
+            tc_fence_after();
+            const uint32_t tY = tmem + (cc & 1) * 128;
+            uint32_t y0[32];
+            tmem_ld32_nowait(tY + lane_off + 32 * vhalf, y0);
+            tmem_wait_ld();
+            uint16_t *os = reinterpret_cast<uint16_t *>(sm + SS_OS);
+            if (vact) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) S[half * 32 + j] = fmaf(S[half * 32 + j], g, z[j]);
+                for (int j = 0; j < 32; ++j) os[(32 * vhalf + j) * VB + vme] = f_to_bf16(__uint_as_float(y0[j]));
             }
-            // ---- output rows r = tid (warps 0, 1)
-            if (warp < 2) {
-                const int r = tid;
+            named_bar(1, SC_EPI);
+            const int len = min(CH, sd.len - cc * CH);
+            const int tok0 = sd.tok + cc * CH;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float y[32];
-                    tmem_ld32(tY + lane_off + half * 32, y);
-                    if (r < len) {
-                        uint16_t *dst = p.out + ((size_t)(tok0 + r) * p.H_v + h) * KD + vb * VB + half * 32;
+            for (int i = 0; i < 2; ++i) {
+                const int idx = i * SC_EPI + tid, r = idx >> 3, c8 = (idx & 7) * 8;
+                if (r < len)
+                    *reinterpret_cast<uint4 *>(p.out + ((size_t)(tok0 + r) * p.H_v + h) * KD + vb * VB + c8) =
+                        *reinterpret_cast<const uint4 *>(os + r * VB + c8);
+            }
+            named_bar(1, SC_EPI);
+        };
+        int c = 0;
+        for (; c < n; ++c) {
+            if (*abort_flag) break;
+            const int b = c & 1;
+            const uint32_t tY = tmem + b * 128;
+            // ---- S (bf16) -> SB: MN-major A operand, thread (k, half) writes half of row k of K-group k / 8
 #pragma unroll
-                        for (int j = 0; j < 32; j += 8) {
-                            uint4 w;
-                            w.x = pack_bf16x2(y[j], y[j + 1]);
-                            w.y = pack_bf16x2(y[j + 2], y[j + 3]);
-                            w.z = pack_bf16x2(y[j + 4], y[j + 5]);
-                            w.w = pack_bf16x2(y[j + 6], y[j + 7]);
-                            *reinterpret_cast<uint4 *>(dst + j) = w;
-                        }
+            for (int c4 = 0; c4 < VH / 8; ++c4) {
+                const int c8 = 4 * vhalf + c4;
+                uint4 w;
+                w.x = pack_bf16x2(S[8 * c4 + 0], S[8 * c4 + 1]);
+                w.y = pack_bf16x2(S[8 * c4 + 2], S[8 * c4 + 3]);
+                w.z = pack_bf16x2(S[8 * c4 + 4], S[8 * c4 + 5]);
+                w.w = pack_bf16x2(S[8 * c4 + 6], S[8 * c4 + 7]);
+                *reinterpret_cast<uint4 *>(sm + SS_SB + (kme >> 3) * 1024 + (kme & 7) * 128 + ((c8 ^ (kme & 7)) << 4)) = w;
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar + 8 * BAR_SBR);
+            // ---- Delta^T = U^T - (W S^T)^T, as tf32 (B of MMA3) and bf16 (A of MMA2)
+            if (!mbar_wait(bar + 8 * BAR_MMA1, c & 1) || !mbar_wait(bar + 8 * BAR_U, c & 1)) fail();
+            tc_fence_after();
+            const float g = reinterpret_cast<const float *>(sm + SS_GC)[kme];
+            {
+                // this thread: v = vme, r = 32 vhalf .. 32 vhalf + 31
+                uint32_t ys[32];
+                tmem_ld32_nowait(tY + lane_off + 64 + 32 * vhalf, ys);
+                tmem_wait_ld();
+                if (vact) {
+                    const float *urow = reinterpret_cast<const float *>(sm + SS_U) + vme * 68 + 32 * vhalf;
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 8) {
+                        const int j = 32 * vhalf + jj;
+                        const float4 ua = *reinterpret_cast<const float4 *>(urow + jj);
+                        const float4 ub = *reinterpret_cast<const float4 *>(urow + jj + 4);
+                        const float d0 = ua.x - __uint_as_float(ys[jj + 0]), d1 = ua.y - __uint_as_float(ys[jj + 1]);
+                        const float d2 = ua.z - __uint_as_float(ys[jj + 2]), d3 = ua.w - __uint_as_float(ys[jj + 3]);
+                        const float d4 = ub.x - __uint_as_float(ys[jj + 4]), d5 = ub.y - __uint_as_float(ys[jj + 5]);
+                        const float d6 = ub.z - __uint_as_float(ys[jj + 6]), d7 = ub.w - __uint_as_float(ys[jj + 7]);
+                        *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j, VB)) =
+                            make_uint4(tf32_bits(d0), tf32_bits(d1), tf32_bits(d2), tf32_bits(d3));
+                        *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j + 16, VB)) =
+                            make_uint4(tf32_bits(d4), tf32_bits(d5), tf32_bits(d6), tf32_bits(d7));
+                        *reinterpret_cast<uint4 *>(sm + SS_DTB + sw128_off(vme, 2 * j, VB)) =
+                            make_uint4(pack_bf16x2(d0, d1), pack_bf16x2(d2, d3), pack_bf16x2(d4, d5),
+                                       pack_bf16x2(d6, d7));
                     }
                 }
             }
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (*abort_flag) break;
-        if (tid == 0 && has_next) {
-            issue_pk(c + 1);
-            pend_pk = 1;
-        }
-    }
-    // ---- drain: on abort, wait (bounded) for copies still in flight
-    if (tid == 0 && c < sd.nchunk) {
-        // copies issued for chunk c (parity c & 1) or c + 1 (the other parity)
-        for (uint32_t ph = 0; ph < 2; ++ph) {
-            if (pend_wq) mbar_wait(bar + 8 * BAR_WQ, ph, 1u << 16);
-            if (pend_pk) mbar_wait(bar + 8 * BAR_PK, ph, 1u << 16);
-            if (pend_u) mbar_wait(bar + 8 * BAR_U, ph, 1u << 16);
-            mbar_wait(bar + 8 * BAR_MMA1, ph, 1u << 16);
-            mbar_wait(bar + 8 * BAR_MMA3, ph, 1u << 16);
-            mbar_wait(bar + 8 * BAR_MMA2, ph, 1u << 16);
-        }
-    }
-    if (p.fin && !*abort_flag) {
-        float *dst = p.fin + st0;
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar + 8 * BAR_DTR);
+            // ---- previous chunk's output (overlaps MMA3 of this chunk)
+            if (c > 0) emit_output(c - 1);
+            // ---- S = S * exp(Gam_C) + Z   (lanes k of Z, columns v of this half)
+            if (!mbar_wait(bar + 8 * BAR_MMA3, c & 1)) fail();
+            tc_fence_after();
+            {
+                uint32_t z0[32];
+                tmem_ld32_nowait(tZ + lane_off + 32 * vhalf, z0);
+                tmem_wait_ld();
 #pragma unroll
-        for (int v = 0; v < VB; ++v) dst[(size_t)v * KD] = S[v];
+                for (int j = 0; j < 32; ++j) S[j] = fmaf(S[j], g, __uint_as_float(z0[j]));
+            }
+            tc_fence_before();
+        }
+        if (!*abort_flag && n > 0) emit_output(n - 1);
+        if (p.fin && !*abort_flag) {
+            float *dst = p.fin + st0;
+#pragma unroll
+            for (int v = 0; v < VH; ++v) dst[(size_t)v * KD] = S[v];
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // =====================================================================
