@@ -139,7 +139,8 @@ constexpr uint32_t REC_U_BLOCK = 64 * 68 * 4;   // 17408 B per V block
 constexpr uint32_t REC_BYTES = 109056;
 
 // =====================================================================
-// Intra-chunk kernel: one CTA (16 warps) per (chunk, value head).
+// Intra-chunk kernel: persistent CTAs (16 warps), each looping over
+// (chunk, value head) work items.
 //
 // Fuses the per-token pre-processing (L2 norms, beta sigmoid, gate
 // activation, in-chunk prefix sum of the gate) with the UT/WY factorisation
@@ -157,40 +158,42 @@ constexpr uint32_t REC_BYTES = 109056;
 //   D_off [128 x 96] = [F_k ; F_q] . [H versions]^T     (all below-diagonal blocks)
 //   D_diag[128 x 64] = [R_k ; R_q] . [C_k]^T            (the four diagonal blocks)
 // into TMEM; rows 0..63 give A (times beta_r), rows 64..127 give P.  After the
-// blocked inversion T = (I + A)^{-1}, two more MMAs give W^T = Kg^T T'^T and
-// U^T = V^T T'^T with T' = T diag(beta).
+// blocked inversion T = (I + A)^{-1}, one bf16 MMA chain gives
+//   [W | U] = (T'_hi + T'_lo) [Kg | V],   T' = T diag(beta) split into two bf16 terms,
+// with [Kg | V] an MN-major operand: V rows are copied straight from global
+// memory and Kg (the gated key) is written in bf16.
 // =====================================================================
 constexpr int IN_THREADS = 512;
-constexpr int IN_WARPS = IN_THREADS / 32;
 constexpr int SL = 32;                  // channels per slice (one 128-byte tf32 atom)
 constexpr int RAWS = 136;               // raw row stride in bf16 (272 B)
-constexpr int GSS = 36;                 // Gam slice row stride (floats)
+constexpr int GAS = 132;                // Gam row stride (floats), all 128 channels
 constexpr int AS = CH + 4;              // A / T row stride (floats)
 constexpr int ZS = 20;                  // inversion scratch row stride (floats)
 
 constexpr uint32_t IS_Q = 0;            // raw q, k, graw: [64][136] bf16 each
 constexpr uint32_t IS_K = 17408;
 constexpr uint32_t IS_G = 34816;
-constexpr uint32_t IS_VT = 53248;       // V^T  : 128 rows (v) x 64 (j) tf32  (A of the U MMA)
-constexpr uint32_t IS_KGT = 86016;      // Kg^T : 128 rows (k) x 64 (j) tf32  (A of the W MMA)
-constexpr uint32_t IS_ROWS = 118784;    // 256 rows x 32 ch tf32: F_k, F_q, R_k, R_q
-constexpr uint32_t IS_COLS = 151552;    // 160 rows x 32 ch tf32: C_k (64), H versions (96)
-constexpr uint32_t IS_GS = 172032;      // Gam slice fp32 [64][36]
-constexpr uint32_t IS_KDS = 181248;     // Kd^T slice staging, 2 x 4 KiB
-constexpr uint32_t IS_TAB = 189440;     // per-channel tables [24][32] fp32
-constexpr uint32_t IS_RV = 192512;      // rq, rk, beta, qk [4][64] fp32
-constexpr uint32_t IS_SEG = 193536;     // prefix-sum segment totals [16][32]
-constexpr uint32_t IS_BAR = 195584;     // 2 mbarriers
-constexpr uint32_t IS_SLOT = 195600;    // TMEM address
-constexpr uint32_t IS_BYTES = 195616 + 1024;
+constexpr uint32_t IS_KV = 53248;       // B of the W/U MMA: [Kg | V] MN-major bf16, N = 256, K = 64 (32 KiB)
+constexpr uint32_t IS_ROWS = 86016;     // 256 rows x 32 ch tf32: F_k, F_q, R_k, R_q
+constexpr uint32_t IS_COLS = 118784;    // 160 rows x 32 ch tf32: C_k (64), H versions (96)
+constexpr uint32_t IS_GA = 139264;      // Gam, fp32 [64][132] (log2 units)
+constexpr uint32_t IS_TAB = 173056;     // per-channel tables [20][128] fp32
+constexpr uint32_t IS_KDS = 183296;     // Kd^T slice staging, 2 x 4 KiB
+constexpr uint32_t IS_RV = 191488;      // rq, rk, beta, qk [4][64] fp32
+constexpr uint32_t IS_SEG = 192512;     // prefix-sum segment totals [4][128]
+constexpr uint32_t IS_GCS = 194560;     // exp(Gam_C) staging [128]
+constexpr uint32_t IS_BAR = 195072;     // 2 mbarriers
+constexpr uint32_t IS_SLOT = 195088;    // TMEM address
+constexpr uint32_t IS_BYTES = 195104 + 1024;
 // aliases once the slices are done
 constexpr uint32_t IS_A = 0;            // fp32 [64][68]
 constexpr uint32_t IS_T = 17408;        // fp32 [64][68]
-constexpr uint32_t IS_Z = 34816;        // fp32 [3][16][20] per-warp scratch of the inversion
-constexpr uint32_t IS_TP = IS_ROWS;     // T' : 64 rows (r) x 64 (j) tf32 (B of the W / U MMAs)
-constexpr uint32_t IS_PI = IS_ROWS + 16384;   // P image staging
+constexpr uint32_t IS_Z = 34816;        // fp32 [3][16][20]
+constexpr uint32_t IS_TPH = IS_ROWS;    // A of the W/U MMA: T'_hi, 64 rows (r) x 64 (j) bf16 (8 KiB)
+constexpr uint32_t IS_TPL = IS_ROWS + 8192;    // T'_lo
+constexpr uint32_t IS_PI = IS_ROWS + 16384;    // P image staging (bf16, 8 KiB)
 constexpr uint32_t IS_WS = IS_COLS;     // W half of the WQ image (2 x 8 KiB)
-constexpr uint32_t IS_US = IS_VT;       // U image staging (2 x 64 x 68 fp32), after the U MMA
+constexpr uint32_t IS_US = IS_GA;       // U image staging (2 x 64 x 68 fp32)
 
 enum { TB_MU = 0, TB_M = 4, TB_EB = 9, TB_EA = 13, TB_D1 = 17, TB_D2 = 18, TB_D12 = 19 };
 enum { RV_RQ = 0, RV_RK = 64, RV_BETA = 128, RV_QK = 192 };
@@ -208,423 +211,480 @@ struct IntraParams {
 __device__ __forceinline__ void sts128(unsigned char *p, float a, float b, float c, float d) {
     *reinterpret_cast<uint4 *>(p) = make_uint4(tf32_bits(a), tf32_bits(b), tf32_bits(c), tf32_bits(d));
 }
+// byte offset of element (n, kk) in an MN-major bf16 operand with 64-element
+// atoms along N (stride 8 KiB) and 8-row K groups (stride 1 KiB)
+__device__ __forceinline__ uint32_t mn_off_bf16(int n, int kk) {
+    return (uint32_t)((n >> 6) * 8192 + (kk >> 3) * 1024 + (kk & 7) * 128 + ((((n & 63) >> 3) ^ (kk & 7)) << 4) +
+                      ((n & 7) << 1));
+}
 
-// One warp: Z (16 x 16) = sum over kk in [k0, k1) of X[r][kk] * Y[kk][c], X and Y in
-// row-major smem with the given strides.  Lane owns row lane >> 1, columns 8 (lane & 1) ..
-__device__ __forceinline__ void warp_mm16(const float *X, int xs, const float *Y, int ys, int k0, int k1,
-                                          float (&acc)[8], int lane) {
-    const int r = lane >> 1, c0 = (lane & 1) * 8;
+// Four warps (wq = 0..3 of the group): Z (16 x 16) = sum over kk in [k0, k1) of X[r][kk] Y[kk][c];
+// warp wq computes rows 4 wq .. 4 wq + 3, lane = (row, column pair).
+__device__ __forceinline__ void quad_mm16(const float *X, int xs, const float *Y, int ys, int k0, int k1,
+                                          float (&acc)[2], int wq, int lane) {
+    const int r = 4 * wq + (lane >> 3), c = (lane & 7) * 2;
     for (int kk = k0; kk < k1; ++kk) {
         const float a = X[r * xs + kk];
-        const float4 y0 = *reinterpret_cast<const float4 *>(Y + kk * ys + c0);
-        const float4 y1 = *reinterpret_cast<const float4 *>(Y + kk * ys + c0 + 4);
-        acc[0] = fmaf(a, y0.x, acc[0]);
-        acc[1] = fmaf(a, y0.y, acc[1]);
-        acc[2] = fmaf(a, y0.z, acc[2]);
-        acc[3] = fmaf(a, y0.w, acc[3]);
-        acc[4] = fmaf(a, y1.x, acc[4]);
-        acc[5] = fmaf(a, y1.y, acc[5]);
-        acc[6] = fmaf(a, y1.z, acc[6]);
-        acc[7] = fmaf(a, y1.w, acc[7]);
+        const float2 y = *reinterpret_cast<const float2 *>(Y + kk * ys + c);
+        acc[0] = fmaf(a, y.x, acc[0]);
+        acc[1] = fmaf(a, y.y, acc[1]);
     }
 }
 
 __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const int chunk = blockIdx.x, h = blockIdx.y;
-    if (p.hdr[1] == 0 || chunk >= p.hdr[0]) return;
-    const ChunkDesc cd = p.chunks[chunk];
-    const int hq = h / (p.H_v / p.H_qk);
+    if (p.hdr[1] == 0) return;
+    const long long n_items = (long long)p.hdr[0] * p.H_v;
+    if ((long long)blockIdx.x >= n_items) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const size_t ch = (size_t)chunk * p.H_v + h;
-    unsigned char *rec = p.rec + ch * REC_BYTES;
-    const int len = cd.len;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t bar_ap = sbase + IS_BAR, bar_wu = sbase + IS_BAR + 8;
     float *rv = reinterpret_cast<float *>(sm + IS_RV);
     float *tab = reinterpret_cast<float *>(sm + IS_TAB);
-    float *gs = reinterpret_cast<float *>(sm + IS_GS);
-
-    // ---- 1. stage raw q, k, graw rows (cp.async), build V^T directly
-    for (int idx = tid; idx < CH * (KD / 8); idx += IN_THREADS) {
-        const int r = idx >> 4, c8 = (idx & 15) * 8;
-        unsigned char *dq = sm + IS_Q + (r * RAWS + c8) * 2;
-        unsigned char *dk = sm + IS_K + (r * RAWS + c8) * 2;
-        unsigned char *dg = sm + IS_G + (r * RAWS + c8) * 2;
-        if (r < len) {
-            const size_t tok = (size_t)cd.tok + r;
-            cp_async16(dq, p.q + (tok * p.H_qk + hq) * KD + c8);
-            cp_async16(dk, p.k + (tok * p.H_qk + hq) * KD + c8);
-            cp_async16(dg, p.graw + (tok * p.H_v + h) * KD + c8);
-        } else {
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(dq) = z;
-            *reinterpret_cast<uint4 *>(dk) = z;
-            *reinterpret_cast<uint4 *>(dg) = z;
-        }
-    }
-    cp_async_commit();
-    for (int u = 0; u < 2; ++u) {
-        const int item = u * IN_THREADS + tid;
-        const int g8 = item >> 6, j = item & 63;
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (j < len) w = *reinterpret_cast<const uint4 *>(p.v + (((size_t)cd.tok + j) * p.H_v + h) * KD + g8 * 8);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t bits = (i & 1) ? (ws[i >> 1] & 0xffff0000u) : (ws[i >> 1] << 16);
-            *reinterpret_cast<uint32_t *>(sm + IS_VT + sw128_off(g8 * 8 + i, 4 * j, KD)) = bits;
-        }
-    }
-    if (tid < CH) {
-        float be = 0.f;
-        if (tid < len) {
-            const float bb = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
-            be = 1.0f / (1.0f + ex2(-bb * LOG2E));
-        }
-        rv[RV_BETA + tid] = be;
-    }
+    float *ga = reinterpret_cast<float *>(sm + IS_GA);
+    float *sA = reinterpret_cast<float *>(sm + IS_A);
+    float *sT = reinterpret_cast<float *>(sm + IS_T);
+    float *sZ = reinterpret_cast<float *>(sm + IS_Z);
     if (tid == 0) {
         mbar_init(bar_ap, 1);
         mbar_init(bar_wu, 1);
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(sbase + IS_SLOT, 256);
-    const float a_gate = ex2(p.A_log[h] * LOG2E);
-    cp_async_wait<0>();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + IS_SLOT);
-    const uint32_t t_off = tmem, t_diag = tmem + 96, t_w = tmem, t_u = tmem + 64;
+    const uint32_t t_off = tmem, t_diag = tmem + 96, t_wu = tmem;
 
-    // ---- 2. row norms: warp w, rows 4w..4w+3; lane sums 4 channels, then 3 x 4 warp sums
-    {
-        float sq[4], sk[4], sqk[4];
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int r = warp * 4 + rr;
-            const uint2 qw = *reinterpret_cast<const uint2 *>(sm + IS_Q + (r * RAWS + 4 * lane) * 2);
-            const uint2 kw = *reinterpret_cast<const uint2 *>(sm + IS_K + (r * RAWS + 4 * lane) * 2);
-            const float a0 = bf16_lo(qw.x), a1 = bf16_hi(qw.x), a2 = bf16_lo(qw.y), a3 = bf16_hi(qw.y);
-            const float b0 = bf16_lo(kw.x), b1 = bf16_hi(kw.x), b2 = bf16_lo(kw.y), b3 = bf16_hi(kw.y);
-            sq[rr] = a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
-            sk[rr] = b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
-            sqk[rr] = a0 * b0 + a1 * b1 + a2 * b2 + a3 * b3;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
-                sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
-                sqk[rr] += __shfl_xor_sync(0xffffffffu, sqk[rr], o);
+    int it = 0;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+        const int chunk = (int)(item / p.H_v), h = (int)(item % p.H_v);
+        const ChunkDesc cd = p.chunks[chunk];
+        const int hq = h / (p.H_v / p.H_qk);
+        const size_t ch = (size_t)chunk * p.H_v + h;
+        unsigned char *rec = p.rec + ch * REC_BYTES;
+        const int len = cd.len;
+        const float a_gate = ex2(p.A_log[h] * LOG2E);
+
+        // ---- 0. the previous item's bulk stores must be done reading shared memory
+        if (tid == 0) bulk_wait_read_all();
+        __syncthreads();
+
+        // ---- 1. stage raw q, k, graw rows and the V part of [Kg | V] (cp.async)
+        for (int idx = tid; idx < CH * (KD / 8); idx += IN_THREADS) {
+            const int r = idx >> 4, c8 = (idx & 15) * 8;
+            unsigned char *dq = sm + IS_Q + (r * RAWS + c8) * 2;
+            unsigned char *dk = sm + IS_K + (r * RAWS + c8) * 2;
+            unsigned char *dg = sm + IS_G + (r * RAWS + c8) * 2;
+            unsigned char *dv = sm + IS_KV + mn_off_bf16(KD + c8, r);
+            if (r < len) {
+                const size_t tok = (size_t)cd.tok + r;
+                cp_async16(dq, p.q + (tok * p.H_qk + hq) * KD + c8);
+                cp_async16(dk, p.k + (tok * p.H_qk + hq) * KD + c8);
+                cp_async16(dg, p.graw + (tok * p.H_v + h) * KD + c8);
+                cp_async16(dv, p.v + (tok * p.H_v + h) * KD + c8);
+            } else {
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(dq) = z;
+                *reinterpret_cast<uint4 *>(dk) = z;
+                *reinterpret_cast<uint4 *>(dg) = z;
+                *reinterpret_cast<uint4 *>(dv) = z;
             }
-        if (lane < 4) {
-            const int r = warp * 4 + lane;
-            float a = sq[0], bq = sk[0], c = sqk[0];
-#pragma unroll
-            for (int rr = 1; rr < 4; ++rr)
-                if (lane == rr) {
-                    a = sq[rr];
-                    bq = sk[rr];
-                    c = sqk[rr];
-                }
-            const float rq = p.scale * rsqrtf(a + L2_EPS), rk = rsqrtf(bq + L2_EPS);
-            rv[RV_RQ + r] = rq;
-            rv[RV_RK + r] = rk;
-            rv[RV_QK + r] = c * rq * rk;
         }
-    }
-    __syncthreads();
-
-    // ---- 3. channel slices
-    for (int sl = 0; sl < KD / SL; ++sl) {
-        const int c0 = sl * SL;
-        // 3a. gate (log2 units) and in-chunk prefix sum: warp w = rows 4w..4w+3, lane = channel
+        cp_async_commit();
+        // pull the next item's rows into L2 while this one is processed
         {
-            const int cc = lane;
-            float loc[4], run = 0.f;
+            const long long nitem = item + gridDim.x;
+            if (nitem < n_items && tid < 4 * CH) {
+                const int nchunk = (int)(nitem / p.H_v), nh = (int)(nitem % p.H_v);
+                const ChunkDesc nd = p.chunks[nchunk];
+                const int r = tid & 63, which = tid >> 6;
+                if (r < nd.len) {
+                    const size_t tok = (size_t)nd.tok + r;
+                    const int nhq = nh / (p.H_v / p.H_qk);
+                    const uint16_t *src = which == 0 ? p.q + (tok * p.H_qk + nhq) * KD
+                                        : which == 1 ? p.k + (tok * p.H_qk + nhq) * KD
+                                        : which == 2 ? p.graw + (tok * p.H_v + nh) * KD
+                                                     : p.v + (tok * p.H_v + nh) * KD;
+                    prefetch_l2(src, KD * 2);
+                }
+            }
+        }
+        if (tid < CH) {
+            float be = 0.f;
+            if (tid < len) {
+                const float bb = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
+                be = 1.0f / (1.0f + ex2(-bb * LOG2E));
+            }
+            rv[RV_BETA + tid] = be;
+        }
+        cp_async_wait<0>();
+        __syncthreads();
+
+        // ---- 2. row norms: warp w, rows 4w..4w+3
+        {
+            float sq[4], sk[4], sqk[4];
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const int r = warp * 4 + rr;
+                const uint2 qw = *reinterpret_cast<const uint2 *>(sm + IS_Q + (r * RAWS + 4 * lane) * 2);
+                const uint2 kw = *reinterpret_cast<const uint2 *>(sm + IS_K + (r * RAWS + 4 * lane) * 2);
+                const float a0 = bf16_lo(qw.x), a1 = bf16_hi(qw.x), a2 = bf16_lo(qw.y), a3 = bf16_hi(qw.y);
+                const float b0 = bf16_lo(kw.x), b1 = bf16_hi(kw.x), b2 = bf16_lo(kw.y), b3 = bf16_hi(kw.y);
+                sq[rr] = a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
+                sk[rr] = b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
+                sqk[rr] = a0 * b0 + a1 * b1 + a2 * b2 + a3 * b3;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
+                    sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
+                    sqk[rr] += __shfl_xor_sync(0xffffffffu, sqk[rr], o);
+                }
+            if (lane < 4) {
+                const int r = warp * 4 + lane;
+                float a = sq[0], bq = sk[0], c = sqk[0];
+#pragma unroll
+                for (int rr = 1; rr < 4; ++rr)
+                    if (lane == rr) {
+                        a = sq[rr];
+                        bq = sk[rr];
+                        c = sqk[rr];
+                    }
+                const float rq = p.scale * rsqrtf(a + L2_EPS), rk = rsqrtf(bq + L2_EPS);
+                rv[RV_RQ + r] = rq;
+                rv[RV_RK + r] = rk;
+                rv[RV_QK + r] = c * rq * rk;
+            }
+        }
+        // ---- 3. gate (log2 units) and its in-chunk prefix sum for all 128 channels:
+        //         thread = (channel c, 16-row segment)
+        {
+            const int c = tid & 127, sg = tid >> 7;
+            float loc[16], run = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const int r = sg * 16 + rr;
                 float g2 = 0.f;
                 if (r < len) {
-                    const uint16_t gb = *reinterpret_cast<const uint16_t *>(sm + IS_G + (r * RAWS + c0 + cc) * 2);
+                    const uint16_t gb = *reinterpret_cast<const uint16_t *>(sm + IS_G + (r * RAWS + c) * 2);
                     g2 = -a_gate * softplus_log2(bf16_to_f(gb));
                 }
                 run += g2;
                 loc[rr] = run;
             }
-            reinterpret_cast<float *>(sm + IS_SEG)[warp * 32 + cc] = run;
+            reinterpret_cast<float *>(sm + IS_SEG)[sg * 128 + c] = run;
             __syncthreads();
             float off = 0.f;
-            for (int w2 = 0; w2 < warp; ++w2) off += reinterpret_cast<const float *>(sm + IS_SEG)[w2 * 32 + cc];
+            for (int s2 = 0; s2 < sg; ++s2) off += reinterpret_cast<const float *>(sm + IS_SEG)[s2 * 128 + c];
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) gs[(warp * 4 + rr) * GSS + cc] = loc[rr] + off;
+            for (int rr = 0; rr < 16; ++rr) ga[(sg * 16 + rr) * GAS + c] = loc[rr] + off;
         }
         __syncthreads();
-        // 3b. per-channel tables: thread t computes entry t / 32 of channel t % 32
-        for (int t = tid; t < 20 * SL; t += IN_THREADS) {
-            const int cc = t & 31, e = t >> 5;
-            auto mval = [&](int i) { return i == 0 ? 0.f : gs[(16 * i - 1) * GSS + cc]; };
+        // ---- 4. per-channel tables (20 entries x 128 channels)
+        for (int t = tid; t < 20 * KD; t += IN_THREADS) {
+            const int c = t & 127, e = t >> 7;
+            const float m1 = ga[15 * GAS + c], m2 = ga[31 * GAS + c], m3 = ga[47 * GAS + c], m4 = ga[63 * GAS + c];
             float val;
-            if (e < 4) val = 0.5f * (gs[(16 * e) * GSS + cc] + gs[(16 * e + 15) * GSS + cc]);   // mu_e
-            else if (e < 9) val = mval(e - 4);                                                     // m_i
-            else if (e < 13) val = ex2(mval(e - 9));                                               // exp(m_i)
-            else if (e < 17) val = ex2(mval(4) - mval(e - 12));                                    // exp(m_4 - m_{i+1})
-            else if (e == 17) val = ex2(mval(2) - mval(1));
-            else if (e == 18) val = ex2(mval(3) - mval(2));
-            else val = ex2(mval(3) - mval(1));
-            tab[e * 32 + cc] = val;
-            if (e == 16) *reinterpret_cast<float *>(rec + REC_GC + 4 * (c0 + cc)) = ex2(mval(4));
+            if (e < 4) {
+                val = 0.5f * (ga[(16 * e) * GAS + c] + ga[(16 * e + 15) * GAS + c]);
+            } else if (e < 13) {
+                const int i = e < 9 ? e - 4 : e - 9;
+                const float mi = i == 0 ? 0.f : (i == 1 ? m1 : (i == 2 ? m2 : (i == 3 ? m3 : m4)));
+                val = e < 9 ? mi : ex2(mi);
+            } else if (e < 17) {
+                const int i = e - 13;
+                const float mi1 = i == 0 ? m1 : (i == 1 ? m2 : (i == 2 ? m3 : m4));
+                val = ex2(m4 - mi1);
+            } else if (e == 17) {
+                val = ex2(m2 - m1);
+            } else if (e == 18) {
+                val = ex2(m3 - m2);
+            } else {
+                val = ex2(m3 - m1);
+            }
+            tab[e * 128 + c] = val;
+            if (e == 16) reinterpret_cast<float *>(sm + IS_GCS)[c] = ex2(m4);
         }
-        // the previous slice's MMAs and Kd^T stores must be done with ROWS / COLS / KDS
-        if (tid == 0) {
-            bulk_wait_read_all();
-            if (sl > 0 && !mbar_wait(bar_ap, (sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+        __syncthreads();
+
+        // ---- 5. channel slices: operands, then the A / P MMAs of the slice
+        for (int sl = 0; sl < KD / SL; ++sl) {
+            const int c0 = sl * SL;
+            if (sl > 0) {
+                // the previous slice's MMAs and Kd^T stores must be done with ROWS / COLS / KDS
+                if (tid == 0) {
+                    bulk_wait_read_all();
+                    if (!mbar_wait(bar_ap, (sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+                }
+                __syncthreads();
+                tc_fence_after();
+            }
+            {
+                const int g4 = tid >> 6, r = tid & 63, bi = r >> 4, cl = 4 * g4, c = c0 + cl;
+                const float4 G = *reinterpret_cast<const float4 *>(ga + r * GAS + c);
+                const float4 MU = *reinterpret_cast<const float4 *>(tab + (TB_MU + bi) * 128 + c);
+                const float4 M0 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi) * 128 + c);
+                const float4 M1 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi + 1) * 128 + c);
+                const float4 EB = *reinterpret_cast<const float4 *>(tab + (TB_EB + bi) * 128 + c);
+                const float4 EA = *reinterpret_cast<const float4 *>(tab + (TB_EA + bi) * 128 + c);
+                const uint2 qw = *reinterpret_cast<const uint2 *>(sm + IS_Q + (r * RAWS + c) * 2);
+                const uint2 kw = *reinterpret_cast<const uint2 *>(sm + IS_K + (r * RAWS + c) * 2);
+                const float rq = rv[RV_RQ + r], rk = rv[RV_RK + r];
+                const float g[4] = {G.x, G.y, G.z, G.w}, mu[4] = {MU.x, MU.y, MU.z, MU.w};
+                const float m0[4] = {M0.x, M0.y, M0.z, M0.w}, m1[4] = {M1.x, M1.y, M1.z, M1.w};
+                const float eb[4] = {EB.x, EB.y, EB.z, EB.w}, ea[4] = {EA.x, EA.y, EA.z, EA.w};
+                const float kh[4] = {bf16_lo(kw.x) * rk, bf16_hi(kw.x) * rk, bf16_lo(kw.y) * rk, bf16_hi(kw.y) * rk};
+                const float qt[4] = {bf16_lo(qw.x) * rq, bf16_hi(qw.x) * rq, bf16_lo(qw.y) * rq, bf16_hi(qw.y) * rq};
+                float fk[4], fq[4], dk[4], dq[4], ck[4], hk[4], kd[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float dr = ex2(fminf(g[e] - mu[e], DIAG_CLAMP2));
+                    const float dc = ex2(fminf(mu[e] - g[e], DIAG_CLAMP2));
+                    // block-relative factors (always <= 1, exact for any gate strength)
+                    const float f = ex2(g[e] - m0[e]), hh = ex2(m1[e] - g[e]);
+                    fk[e] = kh[e] * f;
+                    fq[e] = qt[e] * f;
+                    dk[e] = kh[e] * dr;
+                    dq[e] = qt[e] * dr;
+                    ck[e] = kh[e] * dc;
+                    hk[e] = kh[e] * hh;
+                    kd[e] = hk[e] * ea[e];
+                }
+                // Kg (bf16) into the MN-major [Kg | V] operand: element (k = c .. c + 3, j = r)
+                *reinterpret_cast<uint2 *>(sm + IS_KV + mn_off_bf16(c, r)) =
+                    make_uint2(pack_bf16x2(fk[0] * eb[0], fk[1] * eb[1]), pack_bf16x2(fk[2] * eb[2], fk[3] * eb[3]));
+                // Kd^T slice staging: element (k, r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int kl = cl + e, k = c + e;
+                    const uint32_t kds = (uint32_t)(r >> 5) * 4096 + (kl >> 3) * 1024 + (kl & 7) * 128 +
+                                         (((((4 * r) & 127) >> 4) ^ (k & 7)) << 4) + ((4 * r) & 15);
+                    *reinterpret_cast<uint32_t *>(sm + IS_KDS + kds) = tf32_bits(kd[e]);
+                }
+                const int kb = 16 * g4;
+                sts128(sm + IS_ROWS + sw128_off(r, kb, 256), fk[0], fk[1], fk[2], fk[3]);
+                sts128(sm + IS_ROWS + sw128_off(64 + r, kb, 256), fq[0], fq[1], fq[2], fq[3]);
+                sts128(sm + IS_ROWS + sw128_off(128 + r, kb, 256), dk[0], dk[1], dk[2], dk[3]);
+                sts128(sm + IS_ROWS + sw128_off(192 + r, kb, 256), dq[0], dq[1], dq[2], dq[3]);
+                sts128(sm + IS_COLS + sw128_off(r, kb, 160), ck[0], ck[1], ck[2], ck[3]);
+                const int rl = r & 15;
+                if (bi == 0) {
+                    const float4 D1 = *reinterpret_cast<const float4 *>(tab + TB_D1 * 128 + c);
+                    const float4 D12 = *reinterpret_cast<const float4 *>(tab + TB_D12 * 128 + c);
+                    sts128(sm + IS_COLS + sw128_off(64 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+                    sts128(sm + IS_COLS + sw128_off(80 + rl, kb, 160), hk[0] * D1.x, hk[1] * D1.y, hk[2] * D1.z,
+                           hk[3] * D1.w);
+                    sts128(sm + IS_COLS + sw128_off(112 + rl, kb, 160), hk[0] * D12.x, hk[1] * D12.y,
+                           hk[2] * D12.z, hk[3] * D12.w);
+                } else if (bi == 1) {
+                    const float4 D2 = *reinterpret_cast<const float4 *>(tab + TB_D2 * 128 + c);
+                    sts128(sm + IS_COLS + sw128_off(96 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+                    sts128(sm + IS_COLS + sw128_off(128 + rl, kb, 160), hk[0] * D2.x, hk[1] * D2.y, hk[2] * D2.z,
+                           hk[3] * D2.w);
+                } else if (bi == 2) {
+                    sts128(sm + IS_COLS + sw128_off(144 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+                }
+                // Qg (bf16) straight into the WQ image rows 0..63
+                *reinterpret_cast<uint2 *>(rec + REC_WQ + sw128_off(r, 2 * c, 2 * CH)) =
+                    make_uint2(pack_bf16x2(fq[0] * eb[0], fq[1] * eb[1]), pack_bf16x2(fq[2] * eb[2], fq[3] * eb[3]));
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id_off = idesc_tf32(128, 96), id_diag = idesc_tf32(128, 64);
+#pragma unroll
+                for (int ks = 0; ks < SL / 8; ++ks) {
+                    const uint32_t acc = (sl > 0 || ks > 0) ? 1u : 0u;
+                    umma_tf32(t_off, umma_desc(sbase + IS_ROWS + ks * 32, 16, 1024),
+                              umma_desc(sbase + IS_COLS + 8192 + ks * 32, 16, 1024), id_off, acc);
+                    umma_tf32(t_diag, umma_desc(sbase + IS_ROWS + 16384 + ks * 32, 16, 1024),
+                              umma_desc(sbase + IS_COLS + ks * 32, 16, 1024), id_diag, acc);
+                }
+                umma_commit(bar_ap);
+                bulk_s2g(rec + REC_KDT + c0 * 128, sbase + IS_KDS, 4096);
+                bulk_s2g(rec + REC_KDT + 16384 + c0 * 128, sbase + IS_KDS + 4096, 4096);
+                bulk_commit();
+            }
         }
+        if (tid == 0 && !mbar_wait(bar_ap, (KD / SL - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
         __syncthreads();
         tc_fence_after();
-        // 3c. operands: warp = 32 consecutive rows, one 4-channel group
+
+        // ---- 6. A (times beta) to smem, P image (bf16) to staging.  Warp w: TMEM lanes
+        //         32 (w & 3) .. (K rows 0..63, Q rows 64..127), 16-column block cb = w >> 2.
         {
-            const int g4 = tid >> 6, r = tid & 63, bi = r >> 4, cl = 4 * g4, c = c0 + cl;
-            const float4 G = *reinterpret_cast<const float4 *>(gs + r * GSS + cl);
-            const float4 MU = *reinterpret_cast<const float4 *>(tab + (TB_MU + bi) * 32 + cl);
-            const float4 M0 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi) * 32 + cl);
-            const float4 M1 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi + 1) * 32 + cl);
-            const float4 EB = *reinterpret_cast<const float4 *>(tab + (TB_EB + bi) * 32 + cl);
-            const float4 EA = *reinterpret_cast<const float4 *>(tab + (TB_EA + bi) * 32 + cl);
-            const uint2 qw = *reinterpret_cast<const uint2 *>(sm + IS_Q + (r * RAWS + c) * 2);
-            const uint2 kw = *reinterpret_cast<const uint2 *>(sm + IS_K + (r * RAWS + c) * 2);
-            const float rq = rv[RV_RQ + r], rk = rv[RV_RK + r];
-            const float g[4] = {G.x, G.y, G.z, G.w}, mu[4] = {MU.x, MU.y, MU.z, MU.w};
-            const float m0[4] = {M0.x, M0.y, M0.z, M0.w}, m1[4] = {M1.x, M1.y, M1.z, M1.w};
-            const float eb[4] = {EB.x, EB.y, EB.z, EB.w}, ea[4] = {EA.x, EA.y, EA.z, EA.w};
-            const float kh[4] = {bf16_lo(kw.x) * rk, bf16_hi(kw.x) * rk, bf16_lo(kw.y) * rk, bf16_hi(kw.y) * rk};
-            const float qt[4] = {bf16_lo(qw.x) * rq, bf16_hi(qw.x) * rq, bf16_lo(qw.y) * rq, bf16_hi(qw.y) * rq};
-            float fk[4], fq[4], dk[4], dq[4], ck[4], hk[4];
-            const uint32_t kg_base = sw128_off(c, 4 * r, KD);   // row c, (k & 7) = (c & 7) + e below
+            const int q = warp & 3, cb = warp >> 2;
+            const int l = q * 32 + lane, r = l & 63, bi = r >> 4, rl = r & 15, isq = l >> 6;
+            const uint32_t lo = (uint32_t)(q * 32) << 16;
+            const int bia = 2 * (q & 1), bib = bia + 1;
+            // column offsets of the below-diagonal versions of row blocks 1, 2, 3 in D_off
+            const int nsa = bia == 0 ? 0 : 16, nsb = bib == 1 ? 0 : 48;
+            uint32_t va[16], vb2[16], vd[16];
+            if (cb < bia) tmem_ld16_nowait(t_off + lo + nsa + 16 * cb, va);
+            if (cb < bib) tmem_ld16_nowait(t_off + lo + nsb + 16 * cb, vb2);
+            if (cb == bia || cb == bib) tmem_ld16_nowait(t_diag + lo + 16 * cb, vd);
+            tmem_wait_ld();
+            float o[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float dr = ex2(fminf(g[e] - mu[e], DIAG_CLAMP2));
-                const float dc = ex2(fminf(mu[e] - g[e], DIAG_CLAMP2));
-                // block-relative factors (always <= 1, exact for any gate strength)
-                const float f = ex2(g[e] - m0[e]), hh = ex2(m1[e] - g[e]);
-                fk[e] = kh[e] * f;
-                fq[e] = qt[e] * f;
-                dk[e] = kh[e] * dr;
-                dq[e] = qt[e] * dr;
-                ck[e] = kh[e] * dc;
-                hk[e] = kh[e] * hh;
-                const int k = c + e, kl = cl + e;
-                *reinterpret_cast<uint32_t *>(sm + IS_KGT + sw128_off(k, 4 * r, KD)) = tf32_bits(fk[e] * eb[e]);
-                const uint32_t kds = (uint32_t)(r >> 5) * 4096 + (kl >> 3) * 1024 + (kl & 7) * 128 +
-                                     (((((4 * r) & 127) >> 4) ^ (k & 7)) << 4) + ((4 * r) & 15);
-                *reinterpret_cast<uint32_t *>(sm + IS_KDS + kds) = tf32_bits(hk[e] * ea[e]);
+            for (int j = 0; j < 16; ++j) {
+                float x = 0.f;
+                if (cb < bi) x = __uint_as_float(bi == bia ? va[j] : vb2[j]);
+                else if (cb == bi) x = (j < rl) ? __uint_as_float(vd[j]) : ((isq && j == rl) ? rv[RV_QK + r] : 0.f);
+                o[j] = x;
             }
-            (void)kg_base;
-            const int kb = 16 * g4;
-            sts128(sm + IS_ROWS + sw128_off(r, kb, 256), fk[0], fk[1], fk[2], fk[3]);
-            sts128(sm + IS_ROWS + sw128_off(64 + r, kb, 256), fq[0], fq[1], fq[2], fq[3]);
-            sts128(sm + IS_ROWS + sw128_off(128 + r, kb, 256), dk[0], dk[1], dk[2], dk[3]);
-            sts128(sm + IS_ROWS + sw128_off(192 + r, kb, 256), dq[0], dq[1], dq[2], dq[3]);
-            sts128(sm + IS_COLS + sw128_off(r, kb, 160), ck[0], ck[1], ck[2], ck[3]);
-            const int rl = r & 15;
-            if (bi == 0) {
-                const float4 D1 = *reinterpret_cast<const float4 *>(tab + TB_D1 * 32 + cl);
-                const float4 D12 = *reinterpret_cast<const float4 *>(tab + TB_D12 * 32 + cl);
-                sts128(sm + IS_COLS + sw128_off(64 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
-                sts128(sm + IS_COLS + sw128_off(80 + rl, kb, 160), hk[0] * D1.x, hk[1] * D1.y, hk[2] * D1.z,
-                       hk[3] * D1.w);
-                sts128(sm + IS_COLS + sw128_off(112 + rl, kb, 160), hk[0] * D12.x, hk[1] * D12.y, hk[2] * D12.z,
-                       hk[3] * D12.w);
-            } else if (bi == 1) {
-                const float4 D2 = *reinterpret_cast<const float4 *>(tab + TB_D2 * 32 + cl);
-                sts128(sm + IS_COLS + sw128_off(96 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
-                sts128(sm + IS_COLS + sw128_off(128 + rl, kb, 160), hk[0] * D2.x, hk[1] * D2.y, hk[2] * D2.z,
-                       hk[3] * D2.w);
-            } else if (bi == 2) {
-                sts128(sm + IS_COLS + sw128_off(144 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+            if (!isq) {
+                const float be = rv[RV_BETA + r];
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    *reinterpret_cast<float4 *>(sA + r * AS + 16 * cb + j) =
+                        make_float4(o[j] * be, o[j + 1] * be, o[j + 2] * be, o[j + 3] * be);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; j += 8)
+                    *reinterpret_cast<uint4 *>(sm + IS_PI + sw128_off(r, 2 * (16 * cb + j), CH)) =
+                        make_uint4(pack_bf16x2(o[j], o[j + 1]), pack_bf16x2(o[j + 2], o[j + 3]),
+                                   pack_bf16x2(o[j + 4], o[j + 5]), pack_bf16x2(o[j + 6], o[j + 7]));
             }
-            // Qg (bf16) straight into the WQ image rows 0..63
-            uint2 qg;
-            qg.x = pack_bf16x2(fq[0] * eb[0], fq[1] * eb[1]);
-            qg.y = pack_bf16x2(fq[2] * eb[2], fq[3] * eb[3]);
-            *reinterpret_cast<uint2 *>(rec + REC_WQ + sw128_off(r, 2 * c, 2 * CH)) = qg;
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        // 3d. MMAs of this slice and the Kd^T slice store
+        if (tid == 0) {
+            bulk_s2g(rec + REC_P, sbase + IS_PI, 8192);
+            bulk_s2g(rec + REC_GC, sbase + IS_GCS, 512);
+            bulk_commit();
+        }
+
+        // ---- 7. T = (I + A)^{-1}: diagonal 16 x 16 blocks by forward substitution, then
+        //         T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, four warps per block, level by level.
+        if (tid < 64) {
+            const int bi = tid >> 4, c = tid & 15, o = 16 * bi;
+            float t[SUB];
+#pragma unroll
+            for (int r = 0; r < SUB; ++r) {
+                float sacc = (r == c) ? 1.f : 0.f;
+#pragma unroll
+                for (int j = 0; j < r; ++j) sacc = fmaf(-sA[(o + r) * AS + o + j], t[j], sacc);
+                t[r] = sacc;
+            }
+#pragma unroll
+            for (int r = 0; r < SUB; ++r) sT[(o + r) * AS + o + c] = t[r];
+        } else {
+            for (int idx = tid - 64; idx < 6 * 256; idx += IN_THREADS - 64) {
+                const int blk = idx >> 8, e = idx & 255;
+                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                sT[(16 * bi + (e >> 4)) * AS + 16 * bj + (e & 15)] = 0.f;
+            }
+        }
+        __syncthreads();
+        for (int dist = 1; dist <= 3; ++dist) {
+            const int nblk = 4 - dist, grp = warp >> 2, wq = warp & 3;
+            const int r = 4 * wq + (lane >> 3), cc = (lane & 7) * 2;
+            if (grp < nblk) {
+                const int bj = grp, bi = bj + dist;
+                float acc[2] = {0.f, 0.f};
+                quad_mm16(sA + (16 * bi) * AS, AS, sT + 16 * bj, AS, 16 * bj, 16 * bi, acc, wq, lane);
+                float *z = sZ + grp * 16 * ZS;
+                *reinterpret_cast<float2 *>(z + r * ZS + cc) = make_float2(acc[0], acc[1]);
+            }
+            __syncthreads();
+            if (grp < nblk) {
+                const int bj = grp, bi = bj + dist;
+                float t2[2] = {0.f, 0.f};
+                quad_mm16(sT + (16 * bi) * AS + 16 * bi, AS, sZ + grp * 16 * ZS, ZS, 0, r + 1, t2, wq, lane);
+                *reinterpret_cast<float2 *>(sT + (16 * bi + r) * AS + 16 * bj + cc) = make_float2(-t2[0], -t2[1]);
+            }
+            __syncthreads();
+        }
+        // T' = T diag(beta), split into bf16 hi + lo, as the A operand (K-major, 64 r x 64 j)
+        for (int idx = tid; idx < CH * (CH / 8); idx += IN_THREADS) {
+            const int r = idx >> 3, j = (idx & 7) * 8;
+            float x[8];
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = sT[r * AS + j + e] * rv[RV_BETA + j + e];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const uint32_t h2 = pack_bf16x2(x[e], x[e + 1]);
+                hi[e >> 1] = h2;
+                lo[e >> 1] = pack_bf16x2(x[e] - bf16_lo(h2), x[e + 1] - bf16_hi(h2));
+            }
+            *reinterpret_cast<uint4 *>(sm + IS_TPH + sw128_off(r, 2 * j, CH)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sm + IS_TPL + sw128_off(r, 2 * j, CH)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- 8. [W | U] = T'_hi [Kg | V] + T'_lo [Kg | V]   (M = 64, N = 256, K = 64, bf16)
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id_off = idesc_tf32(128, 96), id_diag = idesc_tf32(128, 64);
+            const uint32_t id = idesc_bf16(64, 256) | (1u << 16);   // B MN-major
 #pragma unroll
-            for (int ks = 0; ks < SL / 8; ++ks) {
-                const uint32_t acc = (sl > 0 || ks > 0) ? 1u : 0u;
-                umma_tf32(t_off, umma_desc(sbase + IS_ROWS + ks * 32, 16, 1024),
-                          umma_desc(sbase + IS_COLS + 8192 + ks * 32, 16, 1024), id_off, acc);
-                umma_tf32(t_diag, umma_desc(sbase + IS_ROWS + 16384 + ks * 32, 16, 1024),
-                          umma_desc(sbase + IS_COLS + ks * 32, 16, 1024), id_diag, acc);
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int ks = 0; ks < CH / 16; ++ks)
+                    umma_bf16(t_wu, umma_desc(sbase + (part ? IS_TPL : IS_TPH) + ks * 32, 16, 1024),
+                              umma_desc(sbase + IS_KV + ks * 2048, 8192, 1024), id, (part > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(bar_wu);
+            if (!mbar_wait(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+        }
+        __syncthreads();
+        tc_fence_after();
+        {
+            // M = 64 layout: row r = 16 (w & 3) + lane for lane < 16; warp w >> 2 selects 64 columns
+            const int q = warp & 3, cb = warp >> 2, r = q * 16 + lane;
+            const uint32_t lo = (uint32_t)(q * 32) << 16;
+            uint32_t x0[32], x1[32];
+            tmem_ld32_nowait(t_wu + lo + 64 * cb, x0);
+            tmem_ld32_nowait(t_wu + lo + 64 * cb + 32, x1);
+            tmem_wait_ld();
+            if (lane < 16) {
+                if (cb < 2) {
+                    // W[r][k], k = 64 cb .. : row 64 + r of the WQ image (bf16)
+#pragma unroll
+                    for (int j = 0; j < 64; j += 8) {
+                        const uint32_t *xs = j < 32 ? x0 : x1;
+                        const int jj = j & 31, k = 64 * cb + j;
+                        const uint32_t off = (uint32_t)cb * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                             ((((2 * k) & 127) >> 4) ^ (r & 7)) * 16;
+                        *reinterpret_cast<uint4 *>(sm + IS_WS + off) = make_uint4(
+                            pack_bf16x2(__uint_as_float(xs[jj]), __uint_as_float(xs[jj + 1])),
+                            pack_bf16x2(__uint_as_float(xs[jj + 2]), __uint_as_float(xs[jj + 3])),
+                            pack_bf16x2(__uint_as_float(xs[jj + 4]), __uint_as_float(xs[jj + 5])),
+                            pack_bf16x2(__uint_as_float(xs[jj + 6]), __uint_as_float(xs[jj + 7])));
+                    }
+                } else {
+                    // U[r][v], v = 64 (cb - 2) .. : U image block cb - 2, row v, column r
+                    float *us = reinterpret_cast<float *>(sm + IS_US) + (cb - 2) * (CH * 68) + r;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        us[j * 68] = __uint_as_float(x0[j]);
+                        us[(32 + j) * 68] = __uint_as_float(x1[j]);
+                    }
+                }
             }
-            umma_commit(bar_ap);
-            bulk_s2g(rec + REC_KDT + c0 * 128, sbase + IS_KDS, 4096);
-            bulk_s2g(rec + REC_KDT + 16384 + c0 * 128, sbase + IS_KDS + 4096, 4096);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(rec + REC_WQ + 8192, sbase + IS_WS, 8192);
+            bulk_s2g(rec + REC_WQ + 16384 + 8192, sbase + IS_WS + 8192, 8192);
+            bulk_s2g(rec + REC_U, sbase + IS_US, 2 * CH * 68 * 4);
             bulk_commit();
         }
     }
-    if (tid == 0 && !mbar_wait(bar_ap, (KD / SL - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- 4. A (times beta) to smem, P image to staging.  Warp w: TMEM lanes 32 (w & 3) ..
-    //         (rows l = K rows 0..63, Q rows 64..127), 16-column block cb = w >> 2 of the row.
-    float *sA = reinterpret_cast<float *>(sm + IS_A);
-    float *sT = reinterpret_cast<float *>(sm + IS_T);
-    {
-        const int q = warp & 3, cb = warp >> 2;
-        const int l = q * 32 + lane, r = l & 63, bi = r >> 4, rl = r & 15, isq = l >> 6;
-        const uint32_t lo = (uint32_t)(q * 32) << 16;
-        // the two row blocks of this warp's lanes
-        const int bia = 2 * (q & 1), bib = bia + 1;
-        const int nst[4] = {0, 0, 16, 48};
-        float va[16], vb[16], vd[16];
-        if (cb < bia) tmem_ld16(t_off + lo + nst[bia] + 16 * cb, va);
-        if (cb < bib) tmem_ld16(t_off + lo + nst[bib] + 16 * cb, vb);
-        if (cb == bia || cb == bib) tmem_ld16(t_diag + lo + 16 * cb, vd);
-        float o[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            float x = 0.f;
-            if (cb < bi) x = (bi == bia) ? va[j] : vb[j];
-            else if (cb == bi) x = (j < rl) ? vd[j] : ((isq && j == rl) ? rv[RV_QK + r] : 0.f);
-            o[j] = x;
-        }
-        if (!isq) {
-            const float be = rv[RV_BETA + r];
-#pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4 *>(sA + r * AS + 16 * cb + j) =
-                    make_float4(o[j] * be, o[j + 1] * be, o[j + 2] * be, o[j + 3] * be);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; j += 8)
-                *reinterpret_cast<uint4 *>(sm + IS_PI + sw128_off(r, 2 * (16 * cb + j), CH)) =
-                    make_uint4(pack_bf16x2(o[j], o[j + 1]), pack_bf16x2(o[j + 2], o[j + 3]),
-                               pack_bf16x2(o[j + 4], o[j + 5]), pack_bf16x2(o[j + 6], o[j + 7]));
-        }
-    }
-    fence_async_smem();
+    if (tid == 0) bulk_wait_all();
     tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_s2g(rec + REC_P, sbase + IS_PI, 8192);
-        bulk_commit();
-    }
-
-    // ---- 5. T = (I + A)^{-1}: diagonal 16 x 16 blocks by forward substitution, then
-    //         T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, one warp per block, level by level.
-    if (tid < 64) {
-        const int bi = tid >> 4, c = tid & 15, o = 16 * bi;
-        float t[SUB];
-#pragma unroll
-        for (int r = 0; r < SUB; ++r) {
-            float sacc = (r == c) ? 1.f : 0.f;
-#pragma unroll
-            for (int j = 0; j < r; ++j) sacc = fmaf(-sA[(o + r) * AS + o + j], t[j], sacc);
-            t[r] = sacc;
-        }
-#pragma unroll
-        for (int r = 0; r < SUB; ++r) sT[(o + r) * AS + o + c] = t[r];
-    } else {
-        // zero the blocks of T above the block diagonal
-        for (int idx = tid - 64; idx < 6 * 256; idx += IN_THREADS - 64) {
-            const int blk = idx >> 8, e = idx & 255;
-            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            sT[(16 * bi + (e >> 4)) * AS + 16 * bj + (e & 15)] = 0.f;
-        }
-    }
-    __syncthreads();
-    float *sZ = reinterpret_cast<float *>(sm + IS_Z);
-    for (int dist = 1; dist <= 3; ++dist) {
-        const int nblk = 4 - dist;
-        if (warp < nblk) {
-            const int bj = warp, bi = bj + dist;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            // Z = A[block row bi, cols 16bj .. 16bi) T[rows 16bj .. 16bi, block col bj]
-            warp_mm16(sA + (16 * bi) * AS, AS, sT + 16 * bj, AS, 16 * bj, 16 * bi, acc, lane);
-            float *z = sZ + warp * 16 * ZS;
-            const int r = lane >> 1, c0 = (lane & 1) * 8;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) z[r * ZS + c0 + e] = acc[e];
-            __syncwarp();
-            float t2[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            warp_mm16(sT + (16 * bi) * AS + 16 * bi, AS, z, ZS, 0, 16, t2, lane);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sT[(16 * bi + r) * AS + 16 * bj + c0 + e] = -t2[e];
-        }
-        __syncthreads();
-    }
-    // T' = T diag(beta) as the B operand (N = r, K = j) of the W / U MMAs
-    for (int idx = tid; idx < CH * (CH / 4); idx += IN_THREADS) {
-        const int r = idx >> 4, j = (idx & 15) * 4;
-        const float4 t4 = *reinterpret_cast<const float4 *>(sT + r * AS + j);
-        sts128(sm + IS_TP + sw128_off(r, 4 * j, CH), t4.x * rv[RV_BETA + j], t4.y * rv[RV_BETA + j + 1],
-               t4.z * rv[RV_BETA + j + 2], t4.w * rv[RV_BETA + j + 3]);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- 6. W^T = Kg^T T'^T and U^T = V^T T'^T
-    if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_tf32(128, 64);
-#pragma unroll
-        for (int ks = 0; ks < CH / 8; ++ks) {
-            const int kb = ks * 32;
-            const uint64_t bd = umma_desc(sbase + IS_TP + (kb >> 7) * 8192 + (kb & 127), 16, 1024);
-            umma_tf32(t_w, umma_desc(sbase + IS_KGT + (kb >> 7) * 16384 + (kb & 127), 16, 1024), bd, id, ks > 0);
-            umma_tf32(t_u, umma_desc(sbase + IS_VT + (kb >> 7) * 16384 + (kb & 127), 16, 1024), bd, id, ks > 0);
-        }
-        umma_commit(bar_wu);
-        if (!mbar_wait(bar_wu, 0)) set_status(KDA_ERR_DEVICE_TIMEOUT);
-    }
-    __syncthreads();
-    tc_fence_after();
-    {
-        // warp w: TMEM lanes 32 (w & 3) .. (channel k for W, value v for U), columns r 16 (w >> 2) ..
-        const int q = warp & 3, r0 = (warp >> 2) * 16;
-        const int kk = q * 32 + lane;
-        const uint32_t lo = (uint32_t)(q * 32) << 16;
-        float wv[16], uv[16];
-        tmem_ld16(t_w + lo + r0, wv);
-        tmem_ld16(t_u + lo + r0, uv);
-        float *us = reinterpret_cast<float *>(sm + IS_US) + (kk >> 6) * (CH * 68) + (kk & 63) * 68 + r0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int r = r0 + j;
-            const uint32_t ws_off = (uint32_t)(kk >> 6) * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
-                                    (((((2 * kk) & 127) >> 4) ^ (r & 7)) << 4) + ((2 * kk) & 15);
-            *reinterpret_cast<uint16_t *>(sm + IS_WS + ws_off) = f_to_bf16(wv[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4 *>(us + j) = make_float4(uv[j], uv[j + 1], uv[j + 2], uv[j + 3]);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_s2g(rec + REC_WQ + 8192, sbase + IS_WS, 8192);
-        bulk_s2g(rec + REC_WQ + 16384 + 8192, sbase + IS_WS + 8192, 8192);
-        bulk_s2g(rec + REC_U, sbase + IS_US, 2 * CH * 68 * 4);
-        bulk_commit();
-        bulk_wait_all();
-    }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
@@ -975,7 +1035,12 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         ip.q = q; ip.k = k; ip.v = v; ip.graw = graw; ip.b = b; ip.A_log = A_log; ip.scale = scale;
         ip.H_qk = H_qk; ip.H_v = H_v; ip.chunks = ws.chunks; ip.hdr = ws.hdr;
         ip.rec = ws.rec;
-        intra_kernel<<<dim3((unsigned)nck, (unsigned)H_v), IN_THREADS, IS_BYTES, stream>>>(ip);
+        int dev = 0, nsm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        const long long items = nck * (long long)H_v;
+        const unsigned grid = (unsigned)(items < nsm ? items : nsm);   // persistent: one CTA per SM
+        intra_kernel<<<grid, IN_THREADS, IS_BYTES, stream>>>(ip);
         ++*launches;
         timing_mark("intra_kernel", stream);
         e = cudaGetLastError();
