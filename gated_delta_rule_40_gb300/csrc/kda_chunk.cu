@@ -183,7 +183,7 @@ constexpr uint32_t IS_RV = 191488;      // rq, rk, beta, qk [4][64] fp32
 constexpr uint32_t IS_SEG = 192512;     // prefix-sum segment totals [4][128]
 constexpr uint32_t IS_GCS = 194560;     // exp(Gam_C) staging [128]
 constexpr uint32_t IS_BAR = 195072;     // 2 mbarriers
-constexpr uint32_t IS_SLOT = 195088;    // TMEM address
+constexpr uint32_t IS_SLOT = 195096;    // TMEM address
 constexpr uint32_t IS_BYTES = 195104 + 1024;
 // aliases once the slices are done
 constexpr uint32_t IS_A = 0;            // fp32 [64][68]
@@ -223,11 +223,14 @@ __device__ __forceinline__ uint32_t mn_off_bf16(int n, int kk) {
 __device__ __forceinline__ void quad_mm16(const float *X, int xs, const float *Y, int ys, int k0, int k1,
                                           float (&acc)[2], int wq, int lane) {
     const int r = 4 * wq + (lane >> 3), c = (lane & 7) * 2;
-    for (int kk = k0; kk < k1; ++kk) {
-        const float a = X[r * xs + kk];
-        const float2 y = *reinterpret_cast<const float2 *>(Y + kk * ys + c);
-        acc[0] = fmaf(a, y.x, acc[0]);
-        acc[1] = fmaf(a, y.y, acc[1]);
+    for (int kb = k0; kb < k1; kb += 16) {   // k1 - k0 is a multiple of 16
+#pragma unroll
+        for (int kk = kb; kk < kb + 16; ++kk) {
+            const float a = X[r * xs + kk];
+            const float2 y = *reinterpret_cast<const float2 *>(Y + kk * ys + c);
+            acc[0] = fmaf(a, y.x, acc[0]);
+            acc[1] = fmaf(a, y.y, acc[1]);
+        }
     }
 }
 
@@ -240,6 +243,7 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t bar_ap = sbase + IS_BAR, bar_wu = sbase + IS_BAR + 8;
+    const uint64_t pol_ef = l2_evict_first_policy();
     float *rv = reinterpret_cast<float *>(sm + IS_RV);
     float *tab = reinterpret_cast<float *>(sm + IS_TAB);
     float *ga = reinterpret_cast<float *>(sm + IS_GA);
@@ -272,7 +276,11 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
         if (tid == 0) bulk_wait_read_all();
         __syncthreads();
 
-        // ---- 1. stage raw q, k, graw rows and the V part of [Kg | V] (cp.async)
+        // beta's global load goes first so its latency overlaps the copies below
+        float bb_raw = 0.f;
+        if (tid < len) bb_raw = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
+        // ---- 1. stage raw q, k, graw rows and the V part of [Kg | V] (cp.async; V lands in
+        //         the swizzled MN-major operand), zero-filling padded rows
         for (int idx = tid; idx < CH * (KD / 8); idx += IN_THREADS) {
             const int r = idx >> 4, c8 = (idx & 15) * 8;
             unsigned char *dq = sm + IS_Q + (r * RAWS + c8) * 2;
@@ -312,15 +320,8 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
                 }
             }
         }
-        if (tid < CH) {
-            float be = 0.f;
-            if (tid < len) {
-                const float bb = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
-                be = 1.0f / (1.0f + ex2(-bb * LOG2E));
-            }
-            rv[RV_BETA + tid] = be;
-        }
         cp_async_wait<0>();
+        if (tid < CH) rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-bb_raw * LOG2E)) : 0.f;
         __syncthreads();
 
         // ---- 2. row norms: warp w, rows 4w..4w+3
@@ -385,30 +386,36 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             for (int rr = 0; rr < 16; ++rr) ga[(sg * 16 + rr) * GAS + c] = loc[rr] + off;
         }
         __syncthreads();
-        // ---- 4. per-channel tables (20 entries x 128 channels)
-        for (int t = tid; t < 20 * KD; t += IN_THREADS) {
-            const int c = t & 127, e = t >> 7;
+        // ---- 4. per-channel tables: four threads per channel (mu and m; exp(m_i); exp(m_4 - m_{i+1});
+        //         block decays and exp(Gam_C))
+        {
+            const int c = tid & 127, part = tid >> 7;
             const float m1 = ga[15 * GAS + c], m2 = ga[31 * GAS + c], m3 = ga[47 * GAS + c], m4 = ga[63 * GAS + c];
-            float val;
-            if (e < 4) {
-                val = 0.5f * (ga[(16 * e) * GAS + c] + ga[(16 * e + 15) * GAS + c]);
-            } else if (e < 13) {
-                const int i = e < 9 ? e - 4 : e - 9;
-                const float mi = i == 0 ? 0.f : (i == 1 ? m1 : (i == 2 ? m2 : (i == 3 ? m3 : m4)));
-                val = e < 9 ? mi : ex2(mi);
-            } else if (e < 17) {
-                const int i = e - 13;
-                const float mi1 = i == 0 ? m1 : (i == 1 ? m2 : (i == 2 ? m3 : m4));
-                val = ex2(m4 - mi1);
-            } else if (e == 17) {
-                val = ex2(m2 - m1);
-            } else if (e == 18) {
-                val = ex2(m3 - m2);
+            if (part == 0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    tab[(TB_MU + i) * 128 + c] = 0.5f * (ga[(16 * i) * GAS + c] + ga[(16 * i + 15) * GAS + c]);
+                tab[(TB_M + 0) * 128 + c] = 0.f;
+                tab[(TB_M + 1) * 128 + c] = m1;
+                tab[(TB_M + 2) * 128 + c] = m2;
+                tab[(TB_M + 3) * 128 + c] = m3;
+                tab[(TB_M + 4) * 128 + c] = m4;
+            } else if (part == 1) {
+                tab[(TB_EB + 0) * 128 + c] = 1.f;
+                tab[(TB_EB + 1) * 128 + c] = ex2(m1);
+                tab[(TB_EB + 2) * 128 + c] = ex2(m2);
+                tab[(TB_EB + 3) * 128 + c] = ex2(m3);
+            } else if (part == 2) {
+                tab[(TB_EA + 0) * 128 + c] = ex2(m4 - m1);
+                tab[(TB_EA + 1) * 128 + c] = ex2(m4 - m2);
+                tab[(TB_EA + 2) * 128 + c] = ex2(m4 - m3);
+                tab[(TB_EA + 3) * 128 + c] = 1.f;
             } else {
-                val = ex2(m3 - m1);
+                tab[TB_D1 * 128 + c] = ex2(m2 - m1);
+                tab[TB_D2 * 128 + c] = ex2(m3 - m2);
+                tab[TB_D12 * 128 + c] = ex2(m3 - m1);
+                reinterpret_cast<float *>(sm + IS_GCS)[c] = ex2(m4);
             }
-            tab[e * 128 + c] = val;
-            if (e == 16) reinterpret_cast<float *>(sm + IS_GCS)[c] = ex2(m4);
         }
         __syncthreads();
 
@@ -508,8 +515,8 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
                               umma_desc(sbase + IS_COLS + ks * 32, 16, 1024), id_diag, acc);
                 }
                 umma_commit(bar_ap);
-                bulk_s2g(rec + REC_KDT + c0 * 128, sbase + IS_KDS, 4096);
-                bulk_s2g(rec + REC_KDT + 16384 + c0 * 128, sbase + IS_KDS + 4096, 4096);
+                bulk_s2g_hint(rec + REC_KDT + c0 * 128, sbase + IS_KDS, 4096, pol_ef);
+                bulk_s2g_hint(rec + REC_KDT + 16384 + c0 * 128, sbase + IS_KDS + 4096, 4096, pol_ef);
                 bulk_commit();
             }
         }
@@ -527,9 +534,9 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             // column offsets of the below-diagonal versions of row blocks 1, 2, 3 in D_off
             const int nsa = bia == 0 ? 0 : 16, nsb = bib == 1 ? 0 : 48;
             uint32_t va[16], vb2[16], vd[16];
-            if (cb < bia) tmem_ld16_nowait(t_off + lo + nsa + 16 * cb, va);
-            if (cb < bib) tmem_ld16_nowait(t_off + lo + nsb + 16 * cb, vb2);
-            if (cb == bia || cb == bib) tmem_ld16_nowait(t_diag + lo + 16 * cb, vd);
+            tmem_ld16_nowait(t_off + lo + nsa + 16 * (cb < 3 ? cb : 2), va);
+            tmem_ld16_nowait(t_off + lo + nsb + 16 * (cb < 3 ? cb : 2), vb2);
+            tmem_ld16_nowait(t_diag + lo + 16 * cb, vd);
             tmem_wait_ld();
             float o[16];
 #pragma unroll
@@ -557,8 +564,8 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
-            bulk_s2g(rec + REC_P, sbase + IS_PI, 8192);
-            bulk_s2g(rec + REC_GC, sbase + IS_GCS, 512);
+            bulk_s2g_hint(rec + REC_P, sbase + IS_PI, 8192, pol_ef);
+            bulk_s2g_hint(rec + REC_GC, sbase + IS_GCS, 512, pol_ef);
             bulk_commit();
         }
 
@@ -599,7 +606,8 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             if (grp < nblk) {
                 const int bj = grp, bi = bj + dist;
                 float t2[2] = {0.f, 0.f};
-                quad_mm16(sT + (16 * bi) * AS + 16 * bi, AS, sZ + grp * 16 * ZS, ZS, 0, r + 1, t2, wq, lane);
+                // T_ii is lower triangular (zeros above its diagonal), so the full 16 terms are exact
+                quad_mm16(sT + (16 * bi) * AS + 16 * bi, AS, sZ + grp * 16 * ZS, ZS, 0, 16, t2, wq, lane);
                 *reinterpret_cast<float2 *>(sT + (16 * bi + r) * AS + 16 * bj + cc) = make_float2(-t2[0], -t2[1]);
             }
             __syncthreads();
@@ -677,9 +685,9 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
-            bulk_s2g(rec + REC_WQ + 8192, sbase + IS_WS, 8192);
-            bulk_s2g(rec + REC_WQ + 16384 + 8192, sbase + IS_WS + 8192, 8192);
-            bulk_s2g(rec + REC_U, sbase + IS_US, 2 * CH * 68 * 4);
+            bulk_s2g_hint(rec + REC_WQ + 8192, sbase + IS_WS, 8192, pol_ef);
+            bulk_s2g_hint(rec + REC_WQ + 16384 + 8192, sbase + IS_WS + 8192, 8192, pol_ef);
+            bulk_s2g_hint(rec + REC_U, sbase + IS_US, 2 * CH * 68 * 4, pol_ef);
             bulk_commit();
         }
     }

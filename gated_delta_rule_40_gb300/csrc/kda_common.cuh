@@ -277,3 +277,18 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[1
         : "r"(taddr));
 }
 }  // namespace kda
+
+namespace kda {
+// L2 policy: lines written by the following accesses are evicted first.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+// Bulk shared -> global copy with an L2 cache-eviction hint.
+__device__ __forceinline__ void bulk_s2g_hint(void *dst, uint32_t src_smem, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;\n" ::"l"(dst),
+                 "r"(src_smem), "r"(bytes), "l"(pol)
+                 : "memory");
+}
+}  // namespace kda
