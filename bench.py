@@ -44,6 +44,21 @@ FLOPS_PER_TOKEN_HEAD = 139264
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
+    when the record is for another kernel or the kernel source changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    try:
+        rec = json.load(open(path))
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    except Exception:
+        return None
+    if rec.get("kernel") != kernel or hashlib.sha256(src).hexdigest() != rec.get("source_sha256"):
+        return None
+    return rec["dram_read_bytes"] + rec["dram_write_bytes"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -87,6 +102,13 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def whole_job_value(units_per_rank: int, ms_max: float, world: int) -> float:
+    """Throughput of the whole job: every rank processes its own replica of the
+    workload (no data-path exchange), so the units add up and the slowest rank
+    sets the time."""
+    return world * units_per_rank / (ms_max * 1e-3)
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -252,7 +274,7 @@ def run_gpu(args, rank, world, local):
         raise RuntimeError(f"device status after the timed region: {kda.status_string(status)}")
 
     units = inp.token_heads()
-    value = world * units / (ms * 1e-3)
+    value = whole_job_value(units, ms, world)
     alg_bytes = units * BYTES_PER_TOKEN_HEAD + inp.N * inp.H_v * STATE_BYTES_PER_SEQ_HEAD
     alg_flops = units * FLOPS_PER_TOKEN_HEAD
     gbs = alg_bytes / (ms * 1e-3) / 1e9
@@ -327,7 +349,7 @@ def run_gpu(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": dom,
                      "achieved": alg_bytes / (dom_ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": alg_bytes / (dom_ms * 1e-3) / 1e9 / hbm_peak, "traffic": None,
+                     "frac": alg_bytes / (dom_ms * 1e-3) / 1e9 / hbm_peak, "traffic": recorded_traffic(dom),
                      "peak_source": peak_src, "kernel_ms": dom_ms,
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "note": "the forward's algorithmic bytes (1282 B per token*head + 128 KiB state per "
