@@ -139,8 +139,10 @@ constexpr uint32_t REC_U_BLOCK = 64 * 68 * 4;   // 17408 B per V block
 constexpr uint32_t REC_BYTES = 109056;
 
 // =====================================================================
-// Intra-chunk kernel: persistent CTAs (16 warps), each looping over
-// (chunk, value head) work items.
+// Intra-chunk kernel: persistent CTAs of 8 warps, two resident per SM, each
+// looping over (chunk, value head) work items.  With two CTAs per SM the
+// serial steps of one item (MMA round trips, the blocked inversion, barrier
+// waits) overlap the elementwise work of the other.
 //
 // Fuses the per-token pre-processing (L2 norms, beta sigmoid, gate
 // activation, in-chunk prefix sum of the gate) with the UT/WY factorisation
@@ -153,47 +155,56 @@ constexpr uint32_t REC_BYTES = 109056;
 // sub-blocks i > b + 1 also needs the block decays between them,
 // X = exp(m_i - m_{b+1}) = prod D, which is folded into per-pair versions of
 // the column operand.  Diagonal sub-blocks use the per-channel midpoint mu of
-// the block's first and last Gam (exponents clamped at 85 nats).  Per 32-channel
-// slice, two tcgen05 MMAs (tf32, M = 128) accumulate
+// the block's first and last Gam (exponents clamped at 85 nats).  The 128
+// channels are processed in four slices of 32; per slice the gate of the
+// slice's channels is activated and prefix-summed inside each warp (4
+// channels x 64 rows per warp), and two tcgen05 MMAs (tf32, M = 128) accumulate
 //   D_off [128 x 96] = [F_k ; F_q] . [H versions]^T     (all below-diagonal blocks)
 //   D_diag[128 x 64] = [R_k ; R_q] . [C_k]^T            (the four diagonal blocks)
 // into TMEM; rows 0..63 give A (times beta_r), rows 64..127 give P.  After the
-// blocked inversion T = (I + A)^{-1}, one bf16 MMA chain gives
-//   [W | U] = (T'_hi + T'_lo) [Kg | V],   T' = T diag(beta) split into two bf16 terms,
-// with [Kg | V] an MN-major operand: V rows are copied straight from global
-// memory and Kg (the gated key) is written in bf16.
+// blocked inversion T = (I + A)^{-1}, two bf16 MMA chains give
+//   W = (T'_hi + T'_lo) Kg,  U = (T'_hi + T'_lo) V,   T' = T diag(beta) split into two bf16 terms,
+// with Kg (the gated key, written in bf16 by the slices) and V as MN-major operands.
 // =====================================================================
-constexpr int IN_THREADS = 512;
+constexpr int IN_THREADS = 256;
+constexpr int IN_CTAS_PER_SM = 2;
 constexpr int SL = 32;                  // channels per slice (one 128-byte tf32 atom)
-constexpr int RAWS = 136;               // raw row stride in bf16 (272 B)
-constexpr int GAS = 132;                // Gam row stride (floats), all 128 channels
+constexpr int GAS = 36;                 // Gam slice row stride (floats)
 constexpr int AS = CH + 4;              // A / T row stride (floats)
-constexpr int ZS = 20;                  // inversion scratch row stride (floats)
+constexpr int XS = 36;                  // inversion scratch row stride (floats)
+constexpr int ZS = 20;                  // 16 x 16 inversion scratch row stride (floats)
+constexpr int TBS = 36;                 // table row stride (floats)
+constexpr uint32_t RAW_T = 4096;        // one tensor of a raw slice: 64 rows x 32 bf16 (64-byte rows)
+constexpr uint32_t RAW_SLICE = 3 * RAW_T;   // q, k, graw
 
-constexpr uint32_t IS_Q = 0;            // raw q, k, graw: [64][136] bf16 each
-constexpr uint32_t IS_K = 17408;
-constexpr uint32_t IS_G = 34816;
-constexpr uint32_t IS_KV = 53248;       // B of the W/U MMA: [Kg | V] MN-major bf16, N = 256, K = 64 (32 KiB)
-constexpr uint32_t IS_ROWS = 86016;     // 256 rows x 32 ch tf32: F_k, F_q, R_k, R_q
-constexpr uint32_t IS_COLS = 118784;    // 160 rows x 32 ch tf32: C_k (64), H versions (96)
-constexpr uint32_t IS_GA = 139264;      // Gam, fp32 [64][132] (log2 units)
-constexpr uint32_t IS_TAB = 173056;     // per-channel tables [20][128] fp32
-constexpr uint32_t IS_KDS = 183296;     // Kd^T slice staging, 2 x 4 KiB
-constexpr uint32_t IS_RV = 191488;      // rq, rk, beta, qk [4][64] fp32
-constexpr uint32_t IS_SEG = 192512;     // prefix-sum segment totals [4][128]
-constexpr uint32_t IS_GCS = 194560;     // exp(Gam_C) staging [128]
-constexpr uint32_t IS_BAR = 195072;     // 2 mbarriers
-constexpr uint32_t IS_SLOT = 195096;    // TMEM address
-constexpr uint32_t IS_BYTES = 195104 + 1024;
+constexpr uint32_t IS_KG = 0;                // B of the W MMA: Kg, MN-major bf16, N = 128 (k), K = 64 (j)
+constexpr uint32_t IS_R1 = 16384;            // 52 KiB: slice operands; then A, T, scratch, P; then W, U staging
+constexpr uint32_t IS_ROWS = IS_R1;          // 256 rows x 32 ch tf32: F_k, F_q, R_k, R_q
+constexpr uint32_t IS_COLS = IS_R1 + 32768;  // 160 rows x 32 ch tf32: C_k (64), H versions (96)
+constexpr uint32_t IS_R2 = 69632;            // raw q / k / graw slices (two buffers); then V
+constexpr uint32_t IS_R3 = 94208;            // Gam slice and tables; then T'_hi, T'_lo
+constexpr uint32_t IS_GA = IS_R3;            // Gam slice, fp32 [64][36] (log2 units), 16-byte units swizzled
+constexpr uint32_t IS_TAB = IS_R3 + 9216;    // per-channel tables [20][36] fp32
+constexpr uint32_t IS_MISC = 110592;
+constexpr uint32_t IS_RV = IS_MISC;          // rq, rk, beta, qk [4][64] fp32
+constexpr uint32_t IS_GCS = IS_MISC + 1024;  // exp(Gam_C) [128]
+constexpr uint32_t IS_BAR = IS_MISC + 1536;  // 2 mbarriers
+constexpr uint32_t IS_SLOT = IS_MISC + 1552; // TMEM address
+constexpr uint32_t IS_BYTES = IS_MISC + 1568 + 1024;   // + alignment slack
 // aliases once the slices are done
-constexpr uint32_t IS_A = 0;            // fp32 [64][68]
-constexpr uint32_t IS_T = 17408;        // fp32 [64][68]
-constexpr uint32_t IS_Z = 34816;        // fp32 [3][16][20]
-constexpr uint32_t IS_TPH = IS_ROWS;    // A of the W/U MMA: T'_hi, 64 rows (r) x 64 (j) bf16 (8 KiB)
-constexpr uint32_t IS_TPL = IS_ROWS + 8192;    // T'_lo
-constexpr uint32_t IS_PI = IS_ROWS + 16384;    // P image staging (bf16, 8 KiB)
-constexpr uint32_t IS_WS = IS_COLS;     // W half of the WQ image (2 x 8 KiB)
-constexpr uint32_t IS_US = IS_GA;       // U image staging (2 x 64 x 68 fp32)
+constexpr uint32_t IS_A = IS_R1;             // fp32 [64][68]
+constexpr uint32_t IS_T = IS_R1 + 17408;     // fp32 [64][68]
+constexpr uint32_t IS_X = IS_R1 + 34816;     // fp32 [32][36] (or [2][16][20])
+constexpr uint32_t IS_PI = IS_R1 + 39424;    // P image staging (bf16, 8 KiB)
+constexpr uint32_t IS_V = IS_R2;             // B of the U MMA: V, MN-major bf16, N = 128 (v), K = 64 (j)
+constexpr uint32_t IS_TPH = IS_R3;           // A of the W/U MMAs: T'_hi, 64 rows (r) x 64 (j) bf16
+constexpr uint32_t IS_TPL = IS_R3 + 8192;    // T'_lo
+constexpr uint32_t IS_WS = IS_R1;            // W half of the WQ image (2 x 8 KiB)
+constexpr uint32_t IS_US = IS_R1 + 16384;    // U image staging (2 x 64 x 68 fp32)
+static_assert(IS_PI + 8192 <= IS_R2 && IS_US + 2 * CH * 68 * 4 <= IS_R2, "R1 aliases overflow");
+static_assert(IS_R2 + 2 * RAW_SLICE <= IS_R3 && IS_TAB + 20 * TBS * 4 <= IS_MISC && IS_TPL + 8192 <= IS_MISC,
+              "R2 / R3 overflow");
+static_assert(IN_CTAS_PER_SM * (IS_BYTES + 1024) <= 228 * 1024, "two CTAs per SM must fit");
 
 enum { TB_MU = 0, TB_M = 4, TB_EB = 9, TB_EA = 13, TB_D1 = 17, TB_D2 = 18, TB_D12 = 19 };
 enum { RV_RQ = 0, RV_RK = 64, RV_BETA = 128, RV_QK = 192 };
@@ -217,24 +228,23 @@ __device__ __forceinline__ uint32_t mn_off_bf16(int n, int kk) {
     return (uint32_t)((n >> 6) * 8192 + (kk >> 3) * 1024 + (kk & 7) * 128 + ((((n & 63) >> 3) ^ (kk & 7)) << 4) +
                       ((n & 7) << 1));
 }
+// raw slice rows are 64 bytes (four 16-byte units); q and k swizzle the unit
+// with (r / 2) % 4 (row-parallel readers), graw with (r / 8) % 4 (readers 8 rows apart)
+__device__ __forceinline__ uint32_t raw_off_qk(int r, int unit) { return (uint32_t)(r * 64 + ((unit ^ ((r >> 1) & 3)) << 4)); }
+__device__ __forceinline__ uint32_t raw_off_g(int r, int unit) { return (uint32_t)(r * 64 + ((unit ^ ((r >> 3) & 3)) << 4)); }
+// Gam slice: element (r, c) of the 32-channel slice; 16-byte unit swizzled with r / 8
+__device__ __forceinline__ int ga_idx(int r, int c) { return r * GAS + ((((c >> 2) ^ (r >> 3)) & 7) << 2) + (c & 3); }
 
-// Four warps (wq = 0..3 of the group): Z (16 x 16) = sum over kk in [k0, k1) of X[r][kk] Y[kk][c];
-// warp wq computes rows 4 wq .. 4 wq + 3, lane = (row, column pair).
-__device__ __forceinline__ void quad_mm16(const float *X, int xs, const float *Y, int ys, int k0, int k1,
-                                          float (&acc)[2], int wq, int lane) {
-    const int r = 4 * wq + (lane >> 3), c = (lane & 7) * 2;
-    for (int kb = k0; kb < k1; kb += 16) {   // k1 - k0 is a multiple of 16
-#pragma unroll
-        for (int kk = kb; kk < kb + 16; ++kk) {
-            const float a = X[r * xs + kk];
-            const float2 y = *reinterpret_cast<const float2 *>(Y + kk * ys + c);
-            acc[0] = fmaf(a, y.x, acc[0]);
-            acc[1] = fmaf(a, y.y, acc[1]);
-        }
-    }
+__device__ __forceinline__ void stg_hint_b32(void *p, uint32_t v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;\n" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void stg_hint_v4(void *p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;\n" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
 }
 
-__global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams p) {
+__global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const IntraParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     if (p.hdr[1] == 0) return;
@@ -247,9 +257,10 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
     float *rv = reinterpret_cast<float *>(sm + IS_RV);
     float *tab = reinterpret_cast<float *>(sm + IS_TAB);
     float *ga = reinterpret_cast<float *>(sm + IS_GA);
+    float *gcs = reinterpret_cast<float *>(sm + IS_GCS);
     float *sA = reinterpret_cast<float *>(sm + IS_A);
     float *sT = reinterpret_cast<float *>(sm + IS_T);
-    float *sZ = reinterpret_cast<float *>(sm + IS_Z);
+    float *sX = reinterpret_cast<float *>(sm + IS_X);
     if (tid == 0) {
         mbar_init(bar_ap, 1);
         mbar_init(bar_wu, 1);
@@ -260,7 +271,7 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + IS_SLOT);
-    const uint32_t t_off = tmem, t_diag = tmem + 96, t_wu = tmem;
+    const uint32_t t_off = tmem, t_diag = tmem + 96, t_w = tmem, t_u = tmem + 128;
 
     int it = 0;
     for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
@@ -271,41 +282,38 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
         unsigned char *rec = p.rec + ch * REC_BYTES;
         const int len = cd.len;
         const float a_gate = ex2(p.A_log[h] * LOG2E);
+        const uint16_t *qrow = p.q + ((size_t)cd.tok * p.H_qk + hq) * KD;   // row r at + r * H_qk * KD
+        const uint16_t *krow = p.k + ((size_t)cd.tok * p.H_qk + hq) * KD;
+        const uint16_t *grow = p.graw + ((size_t)cd.tok * p.H_v + h) * KD;  // row r at + r * H_v * KD
+        const uint16_t *vrow = p.v + ((size_t)cd.tok * p.H_v + h) * KD;
+        const size_t qk_stride = (size_t)p.H_qk * KD, gv_stride = (size_t)p.H_v * KD;
 
-        // ---- 0. the previous item's bulk stores must be done reading shared memory
-        if (tid == 0) bulk_wait_read_all();
-        __syncthreads();
+        // raw q / k / graw of slice s (32 channels) into buffer s % 2, zero rows past len
+        auto issue_raw = [&](int s) {
+            unsigned char *base = sm + IS_R2 + (s & 1) * RAW_SLICE;
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const int idx = tid + IN_THREADS * i, t = idx >> 8, r = (idx >> 2) & 63, u = idx & 3;
+                unsigned char *dst = base + t * RAW_T + (t < 2 ? raw_off_qk(r, u) : raw_off_g(r, u));
+                if (r < len) {
+                    const uint16_t *src = t == 0 ? qrow + r * qk_stride : t == 1 ? krow + r * qk_stride
+                                                                                 : grow + r * gv_stride;
+                    cp_async16(dst, src + s * SL + u * 8);
+                } else {
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            cp_async_commit();
+        };
 
-        // beta's global load goes first so its latency overlaps the copies below
         float bb_raw = 0.f;
         if (tid < len) bb_raw = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
-        // ---- 1. stage raw q, k, graw rows and the V part of [Kg | V] (cp.async; V lands in
-        //         the swizzled MN-major operand), zero-filling padded rows
-        for (int idx = tid; idx < CH * (KD / 8); idx += IN_THREADS) {
-            const int r = idx >> 4, c8 = (idx & 15) * 8;
-            unsigned char *dq = sm + IS_Q + (r * RAWS + c8) * 2;
-            unsigned char *dk = sm + IS_K + (r * RAWS + c8) * 2;
-            unsigned char *dg = sm + IS_G + (r * RAWS + c8) * 2;
-            unsigned char *dv = sm + IS_KV + mn_off_bf16(KD + c8, r);
-            if (r < len) {
-                const size_t tok = (size_t)cd.tok + r;
-                cp_async16(dq, p.q + (tok * p.H_qk + hq) * KD + c8);
-                cp_async16(dk, p.k + (tok * p.H_qk + hq) * KD + c8);
-                cp_async16(dg, p.graw + (tok * p.H_v + h) * KD + c8);
-                cp_async16(dv, p.v + (tok * p.H_v + h) * KD + c8);
-            } else {
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(dq) = z;
-                *reinterpret_cast<uint4 *>(dk) = z;
-                *reinterpret_cast<uint4 *>(dg) = z;
-                *reinterpret_cast<uint4 *>(dv) = z;
-            }
-        }
-        cp_async_commit();
+        issue_raw(0);
+        issue_raw(1);
         // pull the next item's rows into L2 while this one is processed
         {
             const long long nitem = item + gridDim.x;
-            if (nitem < n_items && tid < 4 * CH) {
+            if (nitem < n_items) {
                 const int nchunk = (int)(nitem / p.H_v), nh = (int)(nitem % p.H_v);
                 const ChunkDesc nd = p.chunks[nchunk];
                 const int r = tid & 63, which = tid >> 6;
@@ -320,186 +328,196 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
                 }
             }
         }
-        cp_async_wait<0>();
-        if (tid < CH) rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-bb_raw * LOG2E)) : 0.f;
-        __syncthreads();
-
-        // ---- 2. row norms: warp w, rows 4w..4w+3
+        // ---- 1. row norms from global memory: thread (row, quarter of the channels)
         {
-            float sq[4], sk[4], sqk[4];
+            const int r = tid >> 2, part = tid & 3;
+            float sq = 0.f, sk = 0.f, sqk = 0.f;
+            if (r < len) {
+                const uint4 *qs = reinterpret_cast<const uint4 *>(qrow + r * qk_stride + part * 32);
+                const uint4 *ks = reinterpret_cast<const uint4 *>(krow + r * qk_stride + part * 32);
+                uint4 qa[4], ka[4];
 #pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const int r = warp * 4 + rr;
-                const uint2 qw = *reinterpret_cast<const uint2 *>(sm + IS_Q + (r * RAWS + 4 * lane) * 2);
-                const uint2 kw = *reinterpret_cast<const uint2 *>(sm + IS_K + (r * RAWS + 4 * lane) * 2);
-                const float a0 = bf16_lo(qw.x), a1 = bf16_hi(qw.x), a2 = bf16_lo(qw.y), a3 = bf16_hi(qw.y);
-                const float b0 = bf16_lo(kw.x), b1 = bf16_hi(kw.x), b2 = bf16_lo(kw.y), b3 = bf16_hi(kw.y);
-                sq[rr] = a0 * a0 + a1 * a1 + a2 * a2 + a3 * a3;
-                sk[rr] = b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
-                sqk[rr] = a0 * b0 + a1 * b1 + a2 * b2 + a3 * b3;
+                for (int i = 0; i < 4; ++i) {
+                    qa[i] = __ldg(qs + i);
+                    ka[i] = __ldg(ks + i);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t qw[4] = {qa[i].x, qa[i].y, qa[i].z, qa[i].w};
+                    const uint32_t kw[4] = {ka[i].x, ka[i].y, ka[i].z, ka[i].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float a0 = bf16_lo(qw[j]), a1 = bf16_hi(qw[j]);
+                        const float b0 = bf16_lo(kw[j]), b1 = bf16_hi(kw[j]);
+                        sq = fmaf(a0, a0, fmaf(a1, a1, sq));
+                        sk = fmaf(b0, b0, fmaf(b1, b1, sk));
+                        sqk = fmaf(a0, b0, fmaf(a1, b1, sqk));
+                    }
+                }
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    sq[rr] += __shfl_xor_sync(0xffffffffu, sq[rr], o);
-                    sk[rr] += __shfl_xor_sync(0xffffffffu, sk[rr], o);
-                    sqk[rr] += __shfl_xor_sync(0xffffffffu, sqk[rr], o);
-                }
-            if (lane < 4) {
-                const int r = warp * 4 + lane;
-                float a = sq[0], bq = sk[0], c = sqk[0];
-#pragma unroll
-                for (int rr = 1; rr < 4; ++rr)
-                    if (lane == rr) {
-                        a = sq[rr];
-                        bq = sk[rr];
-                        c = sqk[rr];
-                    }
-                const float rq = p.scale * rsqrtf(a + L2_EPS), rk = rsqrtf(bq + L2_EPS);
+            for (int o = 1; o < 4; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
+            }
+            if (part == 0) {
+                const float rq = p.scale * rsqrtf(sq + L2_EPS), rk = rsqrtf(sk + L2_EPS);
                 rv[RV_RQ + r] = rq;
                 rv[RV_RK + r] = rk;
-                rv[RV_QK + r] = c * rq * rk;
+                rv[RV_QK + r] = sqk * rq * rk;
             }
+            if (tid < CH) rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-bb_raw * LOG2E)) : 0.f;
         }
-        // ---- 3. gate (log2 units) and its in-chunk prefix sum for all 128 channels:
-        //         thread = (channel c, 16-row segment)
-        {
-            const int c = tid & 127, sg = tid >> 7;
-            float loc[16], run = 0.f;
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                const int r = sg * 16 + rr;
-                float g2 = 0.f;
-                if (r < len) {
-                    const uint16_t gb = *reinterpret_cast<const uint16_t *>(sm + IS_G + (r * RAWS + c) * 2);
-                    g2 = -a_gate * softplus_log2(bf16_to_f(gb));
-                }
-                run += g2;
-                loc[rr] = run;
-            }
-            reinterpret_cast<float *>(sm + IS_SEG)[sg * 128 + c] = run;
-            __syncthreads();
-            float off = 0.f;
-            for (int s2 = 0; s2 < sg; ++s2) off += reinterpret_cast<const float *>(sm + IS_SEG)[s2 * 128 + c];
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) ga[(sg * 16 + rr) * GAS + c] = loc[rr] + off;
-        }
-        __syncthreads();
-        // ---- 4. per-channel tables: four threads per channel (mu and m; exp(m_i); exp(m_4 - m_{i+1});
-        //         block decays and exp(Gam_C))
-        {
-            const int c = tid & 127, part = tid >> 7;
-            const float m1 = ga[15 * GAS + c], m2 = ga[31 * GAS + c], m3 = ga[47 * GAS + c], m4 = ga[63 * GAS + c];
-            if (part == 0) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    tab[(TB_MU + i) * 128 + c] = 0.5f * (ga[(16 * i) * GAS + c] + ga[(16 * i + 15) * GAS + c]);
-                tab[(TB_M + 0) * 128 + c] = 0.f;
-                tab[(TB_M + 1) * 128 + c] = m1;
-                tab[(TB_M + 2) * 128 + c] = m2;
-                tab[(TB_M + 3) * 128 + c] = m3;
-                tab[(TB_M + 4) * 128 + c] = m4;
-            } else if (part == 1) {
-                tab[(TB_EB + 0) * 128 + c] = 1.f;
-                tab[(TB_EB + 1) * 128 + c] = ex2(m1);
-                tab[(TB_EB + 2) * 128 + c] = ex2(m2);
-                tab[(TB_EB + 3) * 128 + c] = ex2(m3);
-            } else if (part == 2) {
-                tab[(TB_EA + 0) * 128 + c] = ex2(m4 - m1);
-                tab[(TB_EA + 1) * 128 + c] = ex2(m4 - m2);
-                tab[(TB_EA + 2) * 128 + c] = ex2(m4 - m3);
-                tab[(TB_EA + 3) * 128 + c] = 1.f;
-            } else {
-                tab[TB_D1 * 128 + c] = ex2(m2 - m1);
-                tab[TB_D2 * 128 + c] = ex2(m3 - m2);
-                tab[TB_D12 * 128 + c] = ex2(m3 - m1);
-                reinterpret_cast<float *>(sm + IS_GCS)[c] = ex2(m4);
-            }
-        }
+        cp_async_wait<1>();   // slice 0 landed (this thread's copies)
+        // the previous item's bulk stores must be done reading shared memory (W/U staging, P, exp(Gam_C))
+        if (tid == 0) bulk_wait_read_all();
         __syncthreads();
 
-        // ---- 5. channel slices: operands, then the A / P MMAs of the slice
+        // ---- 2. channel slices
         for (int sl = 0; sl < KD / SL; ++sl) {
             const int c0 = sl * SL;
-            if (sl > 0) {
-                // the previous slice's MMAs and Kd^T stores must be done with ROWS / COLS / KDS
-                if (tid == 0) {
-                    bulk_wait_read_all();
-                    if (!mbar_wait(bar_ap, (sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
-                }
-                __syncthreads();
-                tc_fence_after();
-            }
+            const unsigned char *rawb = sm + IS_R2 + (sl & 1) * RAW_SLICE;
+            // 2a. gate (log2 units), its in-chunk prefix sum and the per-channel tables.
+            //     Warp w: channels 4w .. 4w + 3 of the slice; lane = (8-row segment, channel).
             {
-                const int g4 = tid >> 6, r = tid & 63, bi = r >> 4, cl = 4 * g4, c = c0 + cl;
-                const float4 G = *reinterpret_cast<const float4 *>(ga + r * GAS + c);
-                const float4 MU = *reinterpret_cast<const float4 *>(tab + (TB_MU + bi) * 128 + c);
-                const float4 M0 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi) * 128 + c);
-                const float4 M1 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi + 1) * 128 + c);
-                const float4 EB = *reinterpret_cast<const float4 *>(tab + (TB_EB + bi) * 128 + c);
-                const float4 EA = *reinterpret_cast<const float4 *>(tab + (TB_EA + bi) * 128 + c);
-                const uint2 qw = *reinterpret_cast<const uint2 *>(sm + IS_Q + (r * RAWS + c) * 2);
-                const uint2 kw = *reinterpret_cast<const uint2 *>(sm + IS_K + (r * RAWS + c) * 2);
-                const float rq = rv[RV_RQ + r], rk = rv[RV_RK + r];
-                const float g[4] = {G.x, G.y, G.z, G.w}, mu[4] = {MU.x, MU.y, MU.z, MU.w};
-                const float m0[4] = {M0.x, M0.y, M0.z, M0.w}, m1[4] = {M1.x, M1.y, M1.z, M1.w};
-                const float eb[4] = {EB.x, EB.y, EB.z, EB.w}, ea[4] = {EA.x, EA.y, EA.z, EA.w};
-                const float kh[4] = {bf16_lo(kw.x) * rk, bf16_hi(kw.x) * rk, bf16_lo(kw.y) * rk, bf16_hi(kw.y) * rk};
-                const float qt[4] = {bf16_lo(qw.x) * rq, bf16_hi(qw.x) * rq, bf16_lo(qw.y) * rq, bf16_hi(qw.y) * rq};
-                float fk[4], fq[4], dk[4], dq[4], ck[4], hk[4], kd[4];
+                const int seg = lane >> 2, cl = lane & 3, cs = 4 * warp + cl;
+                float loc[8], run = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float dr = ex2(fminf(g[e] - mu[e], DIAG_CLAMP2));
-                    const float dc = ex2(fminf(mu[e] - g[e], DIAG_CLAMP2));
-                    // block-relative factors (always <= 1, exact for any gate strength)
-                    const float f = ex2(g[e] - m0[e]), hh = ex2(m1[e] - g[e]);
-                    fk[e] = kh[e] * f;
-                    fq[e] = qt[e] * f;
-                    dk[e] = kh[e] * dr;
-                    dq[e] = qt[e] * dr;
-                    ck[e] = kh[e] * dc;
-                    hk[e] = kh[e] * hh;
-                    kd[e] = hk[e] * ea[e];
+                for (int i = 0; i < 8; ++i) {
+                    const int r = 8 * seg + i;
+                    const uint16_t gb = *reinterpret_cast<const uint16_t *>(
+                        rawb + 2 * RAW_T + raw_off_g(r, cs >> 3) + (cs & 7) * 2);
+                    const float g2 = r < len ? -a_gate * softplus_log2(bf16_to_f(gb)) : 0.f;
+                    run += g2;
+                    loc[i] = run;
                 }
-                // Kg (bf16) into the MN-major [Kg | V] operand: element (k = c .. c + 3, j = r)
-                *reinterpret_cast<uint2 *>(sm + IS_KV + mn_off_bf16(c, r)) =
-                    make_uint2(pack_bf16x2(fk[0] * eb[0], fk[1] * eb[1]), pack_bf16x2(fk[2] * eb[2], fk[3] * eb[3]));
-                // Kd^T slice staging: element (k, r)
+                float incl = run;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int kl = cl + e, k = c + e;
-                    const uint32_t kds = (uint32_t)(r >> 5) * 4096 + (kl >> 3) * 1024 + (kl & 7) * 128 +
-                                         (((((4 * r) & 127) >> 4) ^ (k & 7)) << 4) + ((4 * r) & 15);
-                    *reinterpret_cast<uint32_t *>(sm + IS_KDS + kds) = tf32_bits(kd[e]);
+                for (int o = 4; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
                 }
-                const int kb = 16 * g4;
-                sts128(sm + IS_ROWS + sw128_off(r, kb, 256), fk[0], fk[1], fk[2], fk[3]);
-                sts128(sm + IS_ROWS + sw128_off(64 + r, kb, 256), fq[0], fq[1], fq[2], fq[3]);
-                sts128(sm + IS_ROWS + sw128_off(128 + r, kb, 256), dk[0], dk[1], dk[2], dk[3]);
-                sts128(sm + IS_ROWS + sw128_off(192 + r, kb, 256), dq[0], dq[1], dq[2], dq[3]);
-                sts128(sm + IS_COLS + sw128_off(r, kb, 160), ck[0], ck[1], ck[2], ck[3]);
-                const int rl = r & 15;
-                if (bi == 0) {
-                    const float4 D1 = *reinterpret_cast<const float4 *>(tab + TB_D1 * 128 + c);
-                    const float4 D12 = *reinterpret_cast<const float4 *>(tab + TB_D12 * 128 + c);
-                    sts128(sm + IS_COLS + sw128_off(64 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
-                    sts128(sm + IS_COLS + sw128_off(80 + rl, kb, 160), hk[0] * D1.x, hk[1] * D1.y, hk[2] * D1.z,
-                           hk[3] * D1.w);
-                    sts128(sm + IS_COLS + sw128_off(112 + rl, kb, 160), hk[0] * D12.x, hk[1] * D12.y,
-                           hk[2] * D12.z, hk[3] * D12.w);
-                } else if (bi == 1) {
-                    const float4 D2 = *reinterpret_cast<const float4 *>(tab + TB_D2 * 128 + c);
-                    sts128(sm + IS_COLS + sw128_off(96 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
-                    sts128(sm + IS_COLS + sw128_off(128 + rl, kb, 160), hk[0] * D2.x, hk[1] * D2.y, hk[2] * D2.z,
-                           hk[3] * D2.w);
-                } else if (bi == 2) {
-                    sts128(sm + IS_COLS + sw128_off(144 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+                const float off = incl - run;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ga[ga_idx(8 * seg + i, cs)] = loc[i] + off;
+                const float last = loc[7] + off, first = loc[0] + off;
+                float m[5], fi[4];
+                m[0] = 0.f;
+#pragma unroll
+                for (int kk = 1; kk <= 4; ++kk) m[kk] = __shfl_sync(0xffffffffu, last, (2 * kk - 1) * 4 + cl);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) fi[i] = __shfl_sync(0xffffffffu, first, 8 * i + cl);
+                float *tb = tab + cs;
+                switch (seg) {
+                    case 0:
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) tb[(TB_MU + i) * TBS] = 0.5f * (fi[i] + m[i + 1]);
+                        break;
+                    case 1:
+#pragma unroll
+                        for (int kk = 0; kk < 5; ++kk) tb[(TB_M + kk) * TBS] = m[kk];
+                        break;
+                    case 2:
+                        tb[TB_EB * TBS] = 1.f;
+#pragma unroll
+                        for (int i = 1; i < 4; ++i) tb[(TB_EB + i) * TBS] = ex2(m[i]);
+                        break;
+                    case 3:
+#pragma unroll
+                        for (int i = 0; i < 3; ++i) tb[(TB_EA + i) * TBS] = ex2(m[4] - m[i + 1]);
+                        tb[(TB_EA + 3) * TBS] = 1.f;
+                        break;
+                    case 4:
+                        tb[TB_D1 * TBS] = ex2(m[2] - m[1]);
+                        tb[TB_D2 * TBS] = ex2(m[3] - m[2]);
+                        tb[TB_D12 * TBS] = ex2(m[3] - m[1]);
+                        break;
+                    case 5:
+                        gcs[c0 + cs] = ex2(m[4]);
+                        break;
+                    default:
+                        break;
                 }
-                // Qg (bf16) straight into the WQ image rows 0..63
-                *reinterpret_cast<uint2 *>(rec + REC_WQ + sw128_off(r, 2 * c, 2 * CH)) =
-                    make_uint2(pack_bf16x2(fq[0] * eb[0], fq[1] * eb[1]), pack_bf16x2(fq[2] * eb[2], fq[3] * eb[3]));
             }
+            // the previous slice's MMAs must be done with ROWS / COLS
+            if (sl > 0 && tid == 0 && !mbar_wait(bar_ap, (sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            __syncthreads();
+            tc_fence_after();
+            // 2b. operands: thread (row r, 8-channel group g), two halves of 4 channels
+            {
+                const int r = tid & 63, g = tid >> 6, bi = r >> 4, rl = r & 15;
+                const float rq = rv[RV_RQ + r], rk = rv[RV_RK + r];
+                const uint4 qw = *reinterpret_cast<const uint4 *>(rawb + raw_off_qk(r, g));
+                const uint4 kw = *reinterpret_cast<const uint4 *>(rawb + RAW_T + raw_off_qk(r, g));
+                uint32_t kg2[4], qg2[4];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int cls = 8 * g + 4 * hh, c = c0 + cls;
+                    const float4 G = *reinterpret_cast<const float4 *>(ga + ga_idx(r, cls));
+                    const float4 MU = *reinterpret_cast<const float4 *>(tab + (TB_MU + bi) * TBS + cls);
+                    const float4 M0 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi) * TBS + cls);
+                    const float4 M1 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi + 1) * TBS + cls);
+                    const float4 EB = *reinterpret_cast<const float4 *>(tab + (TB_EB + bi) * TBS + cls);
+                    const float4 EA = *reinterpret_cast<const float4 *>(tab + (TB_EA + bi) * TBS + cls);
+                    const uint32_t q0 = hh ? qw.z : qw.x, q1 = hh ? qw.w : qw.y;
+                    const uint32_t k0 = hh ? kw.z : kw.x, k1 = hh ? kw.w : kw.y;
+                    const float gg[4] = {G.x, G.y, G.z, G.w}, mu[4] = {MU.x, MU.y, MU.z, MU.w};
+                    const float m0[4] = {M0.x, M0.y, M0.z, M0.w}, m1[4] = {M1.x, M1.y, M1.z, M1.w};
+                    const float eb[4] = {EB.x, EB.y, EB.z, EB.w}, ea[4] = {EA.x, EA.y, EA.z, EA.w};
+                    const float kh[4] = {bf16_lo(k0) * rk, bf16_hi(k0) * rk, bf16_lo(k1) * rk, bf16_hi(k1) * rk};
+                    const float qt[4] = {bf16_lo(q0) * rq, bf16_hi(q0) * rq, bf16_lo(q1) * rq, bf16_hi(q1) * rq};
+                    float fk[4], fq[4], dk[4], dq[4], ck[4], hk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float dr = ex2(fminf(gg[e] - mu[e], DIAG_CLAMP2));
+                        const float dc = ex2(fminf(mu[e] - gg[e], DIAG_CLAMP2));
+                        // block-relative factors (always <= 1, exact for any gate strength)
+                        const float f = ex2(gg[e] - m0[e]), hf = ex2(m1[e] - gg[e]);
+                        fk[e] = kh[e] * f;
+                        fq[e] = qt[e] * f;
+                        dk[e] = kh[e] * dr;
+                        dq[e] = qt[e] * dr;
+                        ck[e] = kh[e] * dc;
+                        hk[e] = kh[e] * hf;
+                        // Kd^T element (k = c + e, r) straight into the record (a warp writes one 128-byte line)
+                        stg_hint_b32(rec + REC_KDT + sw128_off(c + e, 4 * r, KD), tf32_bits(hk[e] * ea[e]), pol_ef);
+                    }
+                    kg2[2 * hh] = pack_bf16x2(fk[0] * eb[0], fk[1] * eb[1]);
+                    kg2[2 * hh + 1] = pack_bf16x2(fk[2] * eb[2], fk[3] * eb[3]);
+                    qg2[2 * hh] = pack_bf16x2(fq[0] * eb[0], fq[1] * eb[1]);
+                    qg2[2 * hh + 1] = pack_bf16x2(fq[2] * eb[2], fq[3] * eb[3]);
+                    const int kb = 4 * cls;
+                    sts128(sm + IS_ROWS + sw128_off(r, kb, 256), fk[0], fk[1], fk[2], fk[3]);
+                    sts128(sm + IS_ROWS + sw128_off(64 + r, kb, 256), fq[0], fq[1], fq[2], fq[3]);
+                    sts128(sm + IS_ROWS + sw128_off(128 + r, kb, 256), dk[0], dk[1], dk[2], dk[3]);
+                    sts128(sm + IS_ROWS + sw128_off(192 + r, kb, 256), dq[0], dq[1], dq[2], dq[3]);
+                    sts128(sm + IS_COLS + sw128_off(r, kb, 160), ck[0], ck[1], ck[2], ck[3]);
+                    if (bi == 0) {
+                        const float4 D1 = *reinterpret_cast<const float4 *>(tab + TB_D1 * TBS + cls);
+                        const float4 D12 = *reinterpret_cast<const float4 *>(tab + TB_D12 * TBS + cls);
+                        sts128(sm + IS_COLS + sw128_off(64 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+                        sts128(sm + IS_COLS + sw128_off(80 + rl, kb, 160), hk[0] * D1.x, hk[1] * D1.y, hk[2] * D1.z,
+                               hk[3] * D1.w);
+                        sts128(sm + IS_COLS + sw128_off(112 + rl, kb, 160), hk[0] * D12.x, hk[1] * D12.y,
+                               hk[2] * D12.z, hk[3] * D12.w);
+                    } else if (bi == 1) {
+                        const float4 D2 = *reinterpret_cast<const float4 *>(tab + TB_D2 * TBS + cls);
+                        sts128(sm + IS_COLS + sw128_off(96 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+                        sts128(sm + IS_COLS + sw128_off(128 + rl, kb, 160), hk[0] * D2.x, hk[1] * D2.y,
+                               hk[2] * D2.z, hk[3] * D2.w);
+                    } else if (bi == 2) {
+                        sts128(sm + IS_COLS + sw128_off(144 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+                    }
+                }
+                // Kg (bf16) into the MN-major operand: element (k = c0 + 8 g .. + 7, j = r)
+                *reinterpret_cast<uint4 *>(sm + IS_KG + mn_off_bf16(c0 + 8 * g, r)) =
+                    make_uint4(kg2[0], kg2[1], kg2[2], kg2[3]);
+                // Qg (bf16) straight into the WQ image rows 0..63
+                stg_hint_v4(rec + REC_WQ + sw128_off(r, 2 * (c0 + 8 * g), 2 * CH), make_uint4(qg2[0], qg2[1], qg2[2], qg2[3]),
+                            pol_ef);
+            }
+            if (sl + 1 < KD / SL) cp_async_wait<0>();   // the next slice's raw rows (this thread's copies)
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -515,49 +533,63 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
                               umma_desc(sbase + IS_COLS + ks * 32, 16, 1024), id_diag, acc);
                 }
                 umma_commit(bar_ap);
-                bulk_s2g_hint(rec + REC_KDT + c0 * 128, sbase + IS_KDS, 4096, pol_ef);
-                bulk_s2g_hint(rec + REC_KDT + 16384 + c0 * 128, sbase + IS_KDS + 4096, 4096, pol_ef);
-                bulk_commit();
+            }
+            if (sl + 2 < KD / SL) {
+                issue_raw(sl + 2);
+            } else if (sl + 1 == KD / SL) {
+                // V into the MN-major operand of the U MMA (the raw buffers are free now)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int idx = tid + IN_THREADS * i, r = idx >> 4, c8 = (idx & 15) * 8;
+                    unsigned char *dv = sm + IS_V + mn_off_bf16(c8, r);
+                    if (r < len) cp_async16(dv, vrow + r * gv_stride + c8);
+                    else *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
+                }
+                cp_async_commit();
             }
         }
         if (tid == 0 && !mbar_wait(bar_ap, (KD / SL - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
         __syncthreads();
         tc_fence_after();
 
-        // ---- 6. A (times beta) to smem, P image (bf16) to staging.  Warp w: TMEM lanes
-        //         32 (w & 3) .. (K rows 0..63, Q rows 64..127), 16-column block cb = w >> 2.
+        // ---- 3. A (times beta) to smem, P image (bf16) to staging.  Warp w: TMEM lanes
+        //         32 (w & 3) .. (K rows 0..63, Q rows 64..127), 16-column blocks 2 (w >> 2) and 2 (w >> 2) + 1.
         {
-            const int q = warp & 3, cb = warp >> 2;
+            const int q = warp & 3, hf = warp >> 2;
             const int l = q * 32 + lane, r = l & 63, bi = r >> 4, rl = r & 15, isq = l >> 6;
             const uint32_t lo = (uint32_t)(q * 32) << 16;
             const int bia = 2 * (q & 1), bib = bia + 1;
             // column offsets of the below-diagonal versions of row blocks 1, 2, 3 in D_off
             const int nsa = bia == 0 ? 0 : 16, nsb = bib == 1 ? 0 : 48;
-            uint32_t va[16], vb2[16], vd[16];
-            tmem_ld16_nowait(t_off + lo + nsa + 16 * (cb < 3 ? cb : 2), va);
-            tmem_ld16_nowait(t_off + lo + nsb + 16 * (cb < 3 ? cb : 2), vb2);
-            tmem_ld16_nowait(t_diag + lo + 16 * cb, vd);
-            tmem_wait_ld();
-            float o[16];
+            const float be = rv[RV_BETA + r], qkd = rv[RV_QK + r];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                float x = 0.f;
-                if (cb < bi) x = __uint_as_float(bi == bia ? va[j] : vb2[j]);
-                else if (cb == bi) x = (j < rl) ? __uint_as_float(vd[j]) : ((isq && j == rl) ? rv[RV_QK + r] : 0.f);
-                o[j] = x;
-            }
-            if (!isq) {
-                const float be = rv[RV_BETA + r];
+            for (int cbi = 0; cbi < 2; ++cbi) {
+                const int cb = 2 * hf + cbi;
+                uint32_t va[16], vb2[16], vd[16];
+                tmem_ld16_nowait(t_off + lo + nsa + 16 * (cb < 3 ? cb : 2), va);
+                tmem_ld16_nowait(t_off + lo + nsb + 16 * (cb < 3 ? cb : 2), vb2);
+                tmem_ld16_nowait(t_diag + lo + 16 * cb, vd);
+                tmem_wait_ld();
+                float o[16];
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4 *>(sA + r * AS + 16 * cb + j) =
-                        make_float4(o[j] * be, o[j + 1] * be, o[j + 2] * be, o[j + 3] * be);
-            } else {
+                for (int j = 0; j < 16; ++j) {
+                    float x = 0.f;
+                    if (cb < bi) x = __uint_as_float(bi == bia ? va[j] : vb2[j]);
+                    else if (cb == bi) x = (j < rl) ? __uint_as_float(vd[j]) : ((isq && j == rl) ? qkd : 0.f);
+                    o[j] = x;
+                }
+                if (!isq) {
 #pragma unroll
-                for (int j = 0; j < 16; j += 8)
-                    *reinterpret_cast<uint4 *>(sm + IS_PI + sw128_off(r, 2 * (16 * cb + j), CH)) =
-                        make_uint4(pack_bf16x2(o[j], o[j + 1]), pack_bf16x2(o[j + 2], o[j + 3]),
-                                   pack_bf16x2(o[j + 4], o[j + 5]), pack_bf16x2(o[j + 6], o[j + 7]));
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4 *>(sA + r * AS + 16 * cb + j) =
+                            make_float4(o[j] * be, o[j + 1] * be, o[j + 2] * be, o[j + 3] * be);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 8)
+                        *reinterpret_cast<uint4 *>(sm + IS_PI + sw128_off(r, 2 * (16 * cb + j), CH)) =
+                            make_uint4(pack_bf16x2(o[j], o[j + 1]), pack_bf16x2(o[j + 2], o[j + 3]),
+                                       pack_bf16x2(o[j + 4], o[j + 5]), pack_bf16x2(o[j + 6], o[j + 7]));
+                }
             }
         }
         fence_async_smem();
@@ -569,8 +601,9 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             bulk_commit();
         }
 
-        // ---- 7. T = (I + A)^{-1}: diagonal 16 x 16 blocks by forward substitution, then
-        //         T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, four warps per block, level by level.
+        // ---- 4. T = (I + A)^{-1}.  Diagonal 16 x 16 blocks by forward substitution; then
+        //         T10 = -T11 A10 T00 and T32 = -T33 A32 T22; then the lower-left 32 x 32 block
+        //         T21 = -T2 (A21 T1) with T1, T2 the diagonal 32 x 32 blocks.
         if (tid < 64) {
             const int bi = tid >> 4, c = tid & 15, o = 16 * bi;
             float t[SUB];
@@ -592,26 +625,59 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             }
         }
         __syncthreads();
-        for (int dist = 1; dist <= 3; ++dist) {
-            const int nblk = 4 - dist, grp = warp >> 2, wq = warp & 3;
-            const int r = 4 * wq + (lane >> 3), cc = (lane & 7) * 2;
-            if (grp < nblk) {
-                const int bj = grp, bi = bj + dist;
-                float acc[2] = {0.f, 0.f};
-                quad_mm16(sA + (16 * bi) * AS, AS, sT + 16 * bj, AS, 16 * bj, 16 * bi, acc, wq, lane);
-                float *z = sZ + grp * 16 * ZS;
-                *reinterpret_cast<float2 *>(z + r * ZS + cc) = make_float2(acc[0], acc[1]);
+        {
+            // Z_b = A_{i,j} T_jj for (i, j) = (1, 0), (3, 2); thread: block b, row r, column pair cc
+            const int b = tid >> 7, e = tid & 127, r = e >> 3, cc = (e & 7) * 2;
+            const int bi = 2 * b + 1, bj = 2 * b;
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < SUB; ++kk) {
+                const float a = sA[(16 * bi + r) * AS + 16 * bj + kk];
+                const float2 y = *reinterpret_cast<const float2 *>(sT + (16 * bj + kk) * AS + 16 * bj + cc);
+                acc0 = fmaf(a, y.x, acc0);
+                acc1 = fmaf(a, y.y, acc1);
             }
+            *reinterpret_cast<float2 *>(sX + b * 16 * ZS + r * ZS + cc) = make_float2(acc0, acc1);
             __syncthreads();
-            if (grp < nblk) {
-                const int bj = grp, bi = bj + dist;
-                float t2[2] = {0.f, 0.f};
-                // T_ii is lower triangular (zeros above its diagonal), so the full 16 terms are exact
-                quad_mm16(sT + (16 * bi) * AS + 16 * bi, AS, sZ + grp * 16 * ZS, ZS, 0, 16, t2, wq, lane);
-                *reinterpret_cast<float2 *>(sT + (16 * bi + r) * AS + 16 * bj + cc) = make_float2(-t2[0], -t2[1]);
+            float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < SUB; ++kk) {
+                const float a = sT[(16 * bi + r) * AS + 16 * bi + kk];
+                const float2 z = *reinterpret_cast<const float2 *>(sX + b * 16 * ZS + kk * ZS + cc);
+                t0 = fmaf(a, z.x, t0);
+                t1 = fmaf(a, z.y, t1);
             }
-            __syncthreads();
+            *reinterpret_cast<float2 *>(sT + (16 * bi + r) * AS + 16 * bj + cc) = make_float2(-t0, -t1);
         }
+        __syncthreads();
+        {
+            // X = A21 T1 (rows 32..63, columns 0..31), then T21 = -T2 X; thread: row r, 4 columns
+            const int r = tid >> 3, c4 = (tid & 7) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int kk = 0; kk < 32; ++kk) {
+                const float a = sA[(32 + r) * AS + kk];
+                const float4 y = *reinterpret_cast<const float4 *>(sT + kk * AS + c4);
+                acc.x = fmaf(a, y.x, acc.x);
+                acc.y = fmaf(a, y.y, acc.y);
+                acc.z = fmaf(a, y.z, acc.z);
+                acc.w = fmaf(a, y.w, acc.w);
+            }
+            *reinterpret_cast<float4 *>(sX + r * XS + c4) = acc;
+            __syncthreads();
+            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int kk = 0; kk < 32; ++kk) {
+                const float a = sT[(32 + r) * AS + 32 + kk];
+                const float4 x = *reinterpret_cast<const float4 *>(sX + kk * XS + c4);
+                t.x = fmaf(a, x.x, t.x);
+                t.y = fmaf(a, x.y, t.y);
+                t.z = fmaf(a, x.z, t.z);
+                t.w = fmaf(a, x.w, t.w);
+            }
+            *reinterpret_cast<float4 *>(sT + (32 + r) * AS + c4) = make_float4(-t.x, -t.y, -t.z, -t.w);
+        }
+        __syncthreads();
         // T' = T diag(beta), split into bf16 hi + lo, as the A operand (K-major, 64 r x 64 j)
         for (int idx = tid; idx < CH * (CH / 8); idx += IN_THREADS) {
             const int r = idx >> 3, j = (idx & 7) * 8;
@@ -628,55 +694,63 @@ __global__ __launch_bounds__(IN_THREADS, 1) void intra_kernel(const IntraParams 
             *reinterpret_cast<uint4 *>(sm + IS_TPH + sw128_off(r, 2 * j, CH)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4 *>(sm + IS_TPL + sw128_off(r, 2 * j, CH)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+        cp_async_wait<0>();   // V (this thread's copies)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ---- 8. [W | U] = T'_hi [Kg | V] + T'_lo [Kg | V]   (M = 64, N = 256, K = 64, bf16)
+        // ---- 5. W = T'_hi Kg + T'_lo Kg, U = T'_hi V + T'_lo V   (M = 64, N = 128, K = 64, bf16)
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16(64, 256) | (1u << 16);   // B MN-major
+            const uint32_t id = idesc_bf16(64, 128) | (1u << 16);   // B MN-major
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
-                for (int ks = 0; ks < CH / 16; ++ks)
-                    umma_bf16(t_wu, umma_desc(sbase + (part ? IS_TPL : IS_TPH) + ks * 32, 16, 1024),
-                              umma_desc(sbase + IS_KV + ks * 2048, 8192, 1024), id, (part > 0 || ks > 0) ? 1u : 0u);
+                for (int ks = 0; ks < CH / 16; ++ks) {
+                    const uint64_t a = umma_desc(sbase + (part ? IS_TPL : IS_TPH) + ks * 32, 16, 1024);
+                    const uint32_t acc = (part > 0 || ks > 0) ? 1u : 0u;
+                    umma_bf16(t_w, a, umma_desc(sbase + IS_KG + ks * 2048, 8192, 1024), id, acc);
+                    umma_bf16(t_u, a, umma_desc(sbase + IS_V + ks * 2048, 8192, 1024), id, acc);
+                }
             umma_commit(bar_wu);
             if (!mbar_wait(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            bulk_wait_read_all();   // the P image store is done reading before W / U staging reuses it
         }
         __syncthreads();
         tc_fence_after();
         {
-            // M = 64 layout: row r = 16 (w & 3) + lane for lane < 16; warp w >> 2 selects 64 columns
-            const int q = warp & 3, cb = warp >> 2, r = q * 16 + lane;
+            // M = 64 layout: row r = 16 (w & 3) + lane for lane < 16; warps 0..3 read W, 4..7 read U
+            const int q = warp & 3, hf = warp >> 2, r = q * 16 + lane;
             const uint32_t lo = (uint32_t)(q * 32) << 16;
-            uint32_t x0[32], x1[32];
-            tmem_ld32_nowait(t_wu + lo + 64 * cb, x0);
-            tmem_ld32_nowait(t_wu + lo + 64 * cb + 32, x1);
-            tmem_wait_ld();
-            if (lane < 16) {
-                if (cb < 2) {
-                    // W[r][k], k = 64 cb .. : row 64 + r of the WQ image (bf16)
 #pragma unroll
-                    for (int j = 0; j < 64; j += 8) {
-                        const uint32_t *xs = j < 32 ? x0 : x1;
-                        const int jj = j & 31, k = 64 * cb + j;
-                        const uint32_t off = (uint32_t)cb * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
-                                             ((((2 * k) & 127) >> 4) ^ (r & 7)) * 16;
-                        *reinterpret_cast<uint4 *>(sm + IS_WS + off) = make_uint4(
-                            pack_bf16x2(__uint_as_float(xs[jj]), __uint_as_float(xs[jj + 1])),
-                            pack_bf16x2(__uint_as_float(xs[jj + 2]), __uint_as_float(xs[jj + 3])),
-                            pack_bf16x2(__uint_as_float(xs[jj + 4]), __uint_as_float(xs[jj + 5])),
-                            pack_bf16x2(__uint_as_float(xs[jj + 6]), __uint_as_float(xs[jj + 7])));
-                    }
-                } else {
-                    // U[r][v], v = 64 (cb - 2) .. : U image block cb - 2, row v, column r
-                    float *us = reinterpret_cast<float *>(sm + IS_US) + (cb - 2) * (CH * 68) + r;
+            for (int rd = 0; rd < 2; ++rd) {
+                uint32_t x0[32], x1[32];
+                tmem_ld32_nowait(t_w + 128 * hf + lo + 64 * rd, x0);
+                tmem_ld32_nowait(t_w + 128 * hf + lo + 64 * rd + 32, x1);
+                tmem_wait_ld();
+                if (lane < 16) {
+                    if (hf == 0) {
+                        // W[r][k], k = 64 rd .. : row 64 + r of the WQ image (bf16)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        us[j * 68] = __uint_as_float(x0[j]);
-                        us[(32 + j) * 68] = __uint_as_float(x1[j]);
+                        for (int j = 0; j < 64; j += 8) {
+                            const uint32_t *xs = j < 32 ? x0 : x1;
+                            const int jj = j & 31, k = 64 * rd + j;
+                            const uint32_t off = (uint32_t)rd * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                                 ((((2 * k) & 127) >> 4) ^ (r & 7)) * 16;
+                            *reinterpret_cast<uint4 *>(sm + IS_WS + off) = make_uint4(
+                                pack_bf16x2(__uint_as_float(xs[jj]), __uint_as_float(xs[jj + 1])),
+                                pack_bf16x2(__uint_as_float(xs[jj + 2]), __uint_as_float(xs[jj + 3])),
+                                pack_bf16x2(__uint_as_float(xs[jj + 4]), __uint_as_float(xs[jj + 5])),
+                                pack_bf16x2(__uint_as_float(xs[jj + 6]), __uint_as_float(xs[jj + 7])));
+                        }
+                    } else {
+                        // U[r][v], v = 64 rd .. : U image block rd, row v, column r
+                        float *us = reinterpret_cast<float *>(sm + IS_US) + rd * (CH * 68) + r;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            us[j * 68] = __uint_as_float(x0[j]);
+                            us[(32 + j) * 68] = __uint_as_float(x1[j]);
+                        }
                     }
                 }
             }
@@ -1047,7 +1121,8 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
         const long long items = nck * (long long)H_v;
-        const unsigned grid = (unsigned)(items < nsm ? items : nsm);   // persistent: one CTA per SM
+        const long long slots = (long long)nsm * IN_CTAS_PER_SM;   // persistent: two CTAs per SM
+        const unsigned grid = (unsigned)(items < slots ? items : slots);
         intra_kernel<<<grid, IN_THREADS, IS_BYTES, stream>>>(ip);
         ++*launches;
         timing_mark("intra_kernel", stream);
