@@ -273,86 +273,155 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + IS_SLOT);
     const uint32_t t_off = tmem, t_diag = tmem + 96, t_w = tmem, t_u = tmem + 128;
 
-    int it = 0;
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
-        const int chunk = (int)(item / p.H_v), h = (int)(item % p.H_v);
-        const ChunkDesc cd = p.chunks[chunk];
-        const int hq = h / (p.H_v / p.H_qk);
+    const size_t qk_stride = (size_t)p.H_qk * KD, gv_stride = (size_t)p.H_v * KD;
+    const int group = p.H_v / p.H_qk;
+    // raw q / k / graw of slice s (32 channels) of item (d, hh) into buffer s % 2, zero rows past its length
+    auto issue_raw = [&](const ChunkDesc &d, int hh, int s) {
+        const int hq_ = hh / group;
+        const uint16_t *qr = p.q + ((size_t)d.tok * p.H_qk + hq_) * KD + s * SL;
+        const uint16_t *kr = p.k + ((size_t)d.tok * p.H_qk + hq_) * KD + s * SL;
+        const uint16_t *gr = p.graw + ((size_t)d.tok * p.H_v + hh) * KD + s * SL;
+        unsigned char *base = sm + IS_R2 + (s & 1) * RAW_SLICE;
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int idx = tid + IN_THREADS * i, t = idx >> 8, r = (idx >> 2) & 63, u = idx & 3;
+            unsigned char *dst = base + t * RAW_T + (t < 2 ? raw_off_qk(r, u) : raw_off_g(r, u));
+            if (r < d.len) {
+                const uint16_t *src = t == 0 ? qr + r * qk_stride : t == 1 ? kr + r * qk_stride : gr + r * gv_stride;
+                cp_async16(dst, src + u * 8);
+            } else {
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        cp_async_commit();
+    };
+
+    // The description of the next item (chunk, head, A_log) is fetched while the
+    // current one is processed, and its first two raw slices are issued as soon as
+    // the current item's W / U MMAs have released the raw buffers.
+    long long item = blockIdx.x;
+    int h_next = (int)(item % p.H_v);
+    ChunkDesc cd_next = p.chunks[item / p.H_v];
+    float alog_next = p.A_log[h_next];
+    issue_raw(cd_next, h_next, 0);
+    issue_raw(cd_next, h_next, 1);
+    for (int it = 0; item < n_items; item += gridDim.x, ++it) {
+        const int chunk = (int)(item / p.H_v), h = h_next;
+        const ChunkDesc cd = cd_next;
+        const float a_gate = ex2(alog_next * LOG2E);
+        const int hq = h / group;
         const size_t ch = (size_t)chunk * p.H_v + h;
         unsigned char *rec = p.rec + ch * REC_BYTES;
         const int len = cd.len;
-        const float a_gate = ex2(p.A_log[h] * LOG2E);
         const uint16_t *qrow = p.q + ((size_t)cd.tok * p.H_qk + hq) * KD;   // row r at + r * H_qk * KD
         const uint16_t *krow = p.k + ((size_t)cd.tok * p.H_qk + hq) * KD;
-        const uint16_t *grow = p.graw + ((size_t)cd.tok * p.H_v + h) * KD;  // row r at + r * H_v * KD
-        const uint16_t *vrow = p.v + ((size_t)cd.tok * p.H_v + h) * KD;
-        const size_t qk_stride = (size_t)p.H_qk * KD, gv_stride = (size_t)p.H_v * KD;
+        const uint16_t *vrow = p.v + ((size_t)cd.tok * p.H_v + h) * KD;    // row r at + r * H_v * KD
+        const long long nitem = item + gridDim.x;
+        const bool has_next = nitem < n_items;
+        if (has_next) {
+            h_next = (int)(nitem % p.H_v);
+            cd_next = p.chunks[nitem / p.H_v];
+            alog_next = p.A_log[h_next];
+        }
 
-        // raw q / k / graw of slice s (32 channels) into buffer s % 2, zero rows past len
-        auto issue_raw = [&](int s) {
-            unsigned char *base = sm + IS_R2 + (s & 1) * RAW_SLICE;
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                const int idx = tid + IN_THREADS * i, t = idx >> 8, r = (idx >> 2) & 63, u = idx & 3;
-                unsigned char *dst = base + t * RAW_T + (t < 2 ? raw_off_qk(r, u) : raw_off_g(r, u));
-                if (r < len) {
-                    const uint16_t *src = t == 0 ? qrow + r * qk_stride : t == 1 ? krow + r * qk_stride
-                                                                                 : grow + r * gv_stride;
-                    cp_async16(dst, src + s * SL + u * 8);
-                } else {
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-                }
-            }
-            cp_async_commit();
-        };
-
+        // ---- 1. loads for the row norms (global memory, consumed after the first gate step):
+        //         thread (row, quarter of the channels); beta
         float bb_raw = 0.f;
         if (tid < len) bb_raw = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
-        issue_raw(0);
-        issue_raw(1);
-        // pull the next item's rows into L2 while this one is processed
+        uint4 nq[4], nk[4];
         {
-            const long long nitem = item + gridDim.x;
-            if (nitem < n_items) {
-                const int nchunk = (int)(nitem / p.H_v), nh = (int)(nitem % p.H_v);
-                const ChunkDesc nd = p.chunks[nchunk];
-                const int r = tid & 63, which = tid >> 6;
-                if (r < nd.len) {
-                    const size_t tok = (size_t)nd.tok + r;
-                    const int nhq = nh / (p.H_v / p.H_qk);
-                    const uint16_t *src = which == 0 ? p.q + (tok * p.H_qk + nhq) * KD
-                                        : which == 1 ? p.k + (tok * p.H_qk + nhq) * KD
-                                        : which == 2 ? p.graw + (tok * p.H_v + nh) * KD
-                                                     : p.v + (tok * p.H_v + nh) * KD;
-                    prefetch_l2(src, KD * 2);
-                }
+            const int r = tid >> 2, part = tid & 3;
+            const uint4 *qs = reinterpret_cast<const uint4 *>(qrow + r * qk_stride + part * 32);
+            const uint4 *ks = reinterpret_cast<const uint4 *>(krow + r * qk_stride + part * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                nq[i] = r < len ? __ldg(qs + i) : make_uint4(0, 0, 0, 0);
+                nk[i] = r < len ? __ldg(ks + i) : make_uint4(0, 0, 0, 0);
             }
         }
-        // ---- 1. row norms from global memory: thread (row, quarter of the channels)
+        cp_async_wait<1>();   // slice 0 landed (this thread's copies)
+        // the previous item's bulk stores must be done reading shared memory (W/U staging, P, exp(Gam_C))
+        if (tid == 0) bulk_wait_read_all();
+        __syncthreads();
+
+        // gate (log2 units) of slice s, its in-chunk prefix sum and the per-channel tables.
+        // Warp w: channels 4w .. 4w + 3 of the slice; lane = (8-row segment, channel).
+        auto gate_tables = [&](int s) {
+            const unsigned char *rawb = sm + IS_R2 + (s & 1) * RAW_SLICE;
+            const int seg = lane >> 2, cl = lane & 3, cs = 4 * warp + cl;
+            float loc[8], run = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 8 * seg + i;
+                const uint16_t gb =
+                    *reinterpret_cast<const uint16_t *>(rawb + 2 * RAW_T + raw_off_g(r, cs >> 3) + (cs & 7) * 2);
+                const float g2 = r < len ? -a_gate * softplus_log2(bf16_to_f(gb)) : 0.f;
+                run += g2;
+                loc[i] = run;
+            }
+            float incl = run;
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const float off = incl - run;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ga[ga_idx(8 * seg + i, cs)] = loc[i] + off;
+            const float last = loc[7] + off, first = loc[0] + off;
+            float m[5], fi[4];
+            m[0] = 0.f;
+#pragma unroll
+            for (int kk = 1; kk <= 4; ++kk) m[kk] = __shfl_sync(0xffffffffu, last, (2 * kk - 1) * 4 + cl);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) fi[i] = __shfl_sync(0xffffffffu, first, 8 * i + cl);
+            // every lane forms the exponentials (no divergent waits); segment seg stores its share
+            const float eb1 = ex2(m[1]), eb2 = ex2(m[2]), eb3 = ex2(m[3]);
+            const float ea0 = ex2(m[4] - m[1]), ea1 = ex2(m[4] - m[2]), ea2 = ex2(m[4] - m[3]);
+            const float d1 = ex2(m[2] - m[1]), d2 = ex2(m[3] - m[2]), d12 = ex2(m[3] - m[1]), gc = ex2(m[4]);
+            float *tb = tab + cs;
+            if (seg == 0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) tb[(TB_MU + i) * TBS] = 0.5f * (fi[i] + m[i + 1]);
+            } else if (seg == 1) {
+#pragma unroll
+                for (int kk = 0; kk < 5; ++kk) tb[(TB_M + kk) * TBS] = m[kk];
+            } else if (seg == 2) {
+                tb[TB_EB * TBS] = 1.f;
+                tb[(TB_EB + 1) * TBS] = eb1;
+                tb[(TB_EB + 2) * TBS] = eb2;
+                tb[(TB_EB + 3) * TBS] = eb3;
+            } else if (seg == 3) {
+                tb[TB_EA * TBS] = ea0;
+                tb[(TB_EA + 1) * TBS] = ea1;
+                tb[(TB_EA + 2) * TBS] = ea2;
+                tb[(TB_EA + 3) * TBS] = 1.f;
+            } else if (seg == 4) {
+                tb[TB_D1 * TBS] = d1;
+                tb[TB_D2 * TBS] = d2;
+                tb[TB_D12 * TBS] = d12;
+            } else if (seg == 5) {
+                gcs[s * SL + cs] = gc;
+            }
+        };
+
+        // ---- 2. channel slices.  Order per slice s: operands(s), MMAs(s), gate/tables(s + 1),
+        //         wait for MMAs(s); the gate of slice 0 and the row norms come first.
+        gate_tables(0);
         {
             const int r = tid >> 2, part = tid & 3;
             float sq = 0.f, sk = 0.f, sqk = 0.f;
-            if (r < len) {
-                const uint4 *qs = reinterpret_cast<const uint4 *>(qrow + r * qk_stride + part * 32);
-                const uint4 *ks = reinterpret_cast<const uint4 *>(krow + r * qk_stride + part * 32);
-                uint4 qa[4], ka[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    qa[i] = __ldg(qs + i);
-                    ka[i] = __ldg(ks + i);
-                }
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t qw[4] = {nq[i].x, nq[i].y, nq[i].z, nq[i].w};
+                const uint32_t kw[4] = {nk[i].x, nk[i].y, nk[i].z, nk[i].w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t qw[4] = {qa[i].x, qa[i].y, qa[i].z, qa[i].w};
-                    const uint32_t kw[4] = {ka[i].x, ka[i].y, ka[i].z, ka[i].w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float a0 = bf16_lo(qw[j]), a1 = bf16_hi(qw[j]);
-                        const float b0 = bf16_lo(kw[j]), b1 = bf16_hi(kw[j]);
-                        sq = fmaf(a0, a0, fmaf(a1, a1, sq));
-                        sk = fmaf(b0, b0, fmaf(b1, b1, sk));
-                        sqk = fmaf(a0, b0, fmaf(a1, b1, sqk));
-                    }
+                for (int j = 0; j < 4; ++j) {
+                    const float a0 = bf16_lo(qw[j]), a1 = bf16_hi(qw[j]);
+                    const float b0 = bf16_lo(kw[j]), b1 = bf16_hi(kw[j]);
+                    sq = fmaf(a0, a0, fmaf(a1, a1, sq));
+                    sk = fmaf(b0, b0, fmaf(b1, b1, sk));
+                    sqk = fmaf(a0, b0, fmaf(a1, b1, sqk));
                 }
             }
 #pragma unroll
@@ -369,81 +438,23 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             }
             if (tid < CH) rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-bb_raw * LOG2E)) : 0.f;
         }
-        cp_async_wait<1>();   // slice 0 landed (this thread's copies)
-        // the previous item's bulk stores must be done reading shared memory (W/U staging, P, exp(Gam_C))
-        if (tid == 0) bulk_wait_read_all();
+        // pull the next item's rows into L2 while this one is processed
+        if (has_next) {
+            const int r = tid & 63, which = tid >> 6;
+            if (r < cd_next.len) {
+                const size_t tok = (size_t)cd_next.tok + r;
+                const int nhq = h_next / group;
+                const uint16_t *src = which == 0 ? p.q + (tok * p.H_qk + nhq) * KD
+                                    : which == 1 ? p.k + (tok * p.H_qk + nhq) * KD
+                                    : which == 2 ? p.graw + (tok * p.H_v + h_next) * KD
+                                                 : p.v + (tok * p.H_v + h_next) * KD;
+                prefetch_l2(src, KD * 2);
+            }
+        }
         __syncthreads();
-
-        // ---- 2. channel slices
         for (int sl = 0; sl < KD / SL; ++sl) {
             const int c0 = sl * SL;
             const unsigned char *rawb = sm + IS_R2 + (sl & 1) * RAW_SLICE;
-            // 2a. gate (log2 units), its in-chunk prefix sum and the per-channel tables.
-            //     Warp w: channels 4w .. 4w + 3 of the slice; lane = (8-row segment, channel).
-            {
-                const int seg = lane >> 2, cl = lane & 3, cs = 4 * warp + cl;
-                float loc[8], run = 0.f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = 8 * seg + i;
-                    const uint16_t gb = *reinterpret_cast<const uint16_t *>(
-                        rawb + 2 * RAW_T + raw_off_g(r, cs >> 3) + (cs & 7) * 2);
-                    const float g2 = r < len ? -a_gate * softplus_log2(bf16_to_f(gb)) : 0.f;
-                    run += g2;
-                    loc[i] = run;
-                }
-                float incl = run;
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const float off = incl - run;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) ga[ga_idx(8 * seg + i, cs)] = loc[i] + off;
-                const float last = loc[7] + off, first = loc[0] + off;
-                float m[5], fi[4];
-                m[0] = 0.f;
-#pragma unroll
-                for (int kk = 1; kk <= 4; ++kk) m[kk] = __shfl_sync(0xffffffffu, last, (2 * kk - 1) * 4 + cl);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) fi[i] = __shfl_sync(0xffffffffu, first, 8 * i + cl);
-                float *tb = tab + cs;
-                switch (seg) {
-                    case 0:
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) tb[(TB_MU + i) * TBS] = 0.5f * (fi[i] + m[i + 1]);
-                        break;
-                    case 1:
-#pragma unroll
-                        for (int kk = 0; kk < 5; ++kk) tb[(TB_M + kk) * TBS] = m[kk];
-                        break;
-                    case 2:
-                        tb[TB_EB * TBS] = 1.f;
-#pragma unroll
-                        for (int i = 1; i < 4; ++i) tb[(TB_EB + i) * TBS] = ex2(m[i]);
-                        break;
-                    case 3:
-#pragma unroll
-                        for (int i = 0; i < 3; ++i) tb[(TB_EA + i) * TBS] = ex2(m[4] - m[i + 1]);
-                        tb[(TB_EA + 3) * TBS] = 1.f;
-                        break;
-                    case 4:
-                        tb[TB_D1 * TBS] = ex2(m[2] - m[1]);
-                        tb[TB_D2 * TBS] = ex2(m[3] - m[2]);
-                        tb[TB_D12 * TBS] = ex2(m[3] - m[1]);
-                        break;
-                    case 5:
-                        gcs[c0 + cs] = ex2(m[4]);
-                        break;
-                    default:
-                        break;
-                }
-            }
-            // the previous slice's MMAs must be done with ROWS / COLS
-            if (sl > 0 && tid == 0 && !mbar_wait(bar_ap, (sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
-            __syncthreads();
-            tc_fence_after();
             // 2b. operands: thread (row r, 8-channel group g), two halves of 4 channels
             {
                 const int r = tid & 63, g = tid >> 6, bi = r >> 4, rl = r & 15;
@@ -535,7 +546,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                 umma_commit(bar_ap);
             }
             if (sl + 2 < KD / SL) {
-                issue_raw(sl + 2);
+                issue_raw(cd, h, sl + 2);
             } else if (sl + 1 == KD / SL) {
                 // V into the MN-major operand of the U MMA (the raw buffers are free now)
 #pragma unroll
@@ -547,10 +558,12 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                 }
                 cp_async_commit();
             }
+            if (sl + 1 < KD / SL) gate_tables(sl + 1);
+            // this slice's MMAs must be done with ROWS / COLS (and, after the last, with TMEM)
+            if (tid == 0 && !mbar_wait(bar_ap, sl & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            __syncthreads();
+            tc_fence_after();
         }
-        if (tid == 0 && !mbar_wait(bar_ap, (KD / SL - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
-        __syncthreads();
-        tc_fence_after();
 
         // ---- 3. A (times beta) to smem, P image (bf16) to staging.  Warp w: TMEM lanes
         //         32 (w & 3) .. (K rows 0..63, Q rows 64..127), 16-column blocks 2 (w >> 2) and 2 (w >> 2) + 1.
@@ -718,6 +731,11 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         }
         __syncthreads();
         tc_fence_after();
+        // the raw buffers (V) are free: start the next item's first two slices
+        if (has_next) {
+            issue_raw(cd_next, h_next, 0);
+            issue_raw(cd_next, h_next, 1);
+        }
         {
             // M = 64 layout: row r = 16 (w & 3) + lane for lane < 16; warps 0..3 read W, 4..7 read U
             const int q = warp & 3, hf = warp >> 2, r = q * 16 + lane;
