@@ -219,8 +219,10 @@ struct IntraParams {
     unsigned char *rec;   // [chunk][H_v] records of REC_BYTES
 };
 
+// A / P operands are stored as fp32 bit patterns: the tf32 MMA uses their upper 19 bits
+// (truncation), which the chunk-algebra error study shows costs nothing measurable here
 __device__ __forceinline__ void sts128(unsigned char *p, float a, float b, float c, float d) {
-    *reinterpret_cast<uint4 *>(p) = make_uint4(tf32_bits(a), tf32_bits(b), tf32_bits(c), tf32_bits(d));
+    *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
 }
 // byte offset of element (n, kk) in an MN-major bf16 operand with 64-element
 // atoms along N (stride 8 KiB) and 8-row K groups (stride 1 KiB)
@@ -262,7 +264,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     float *sT = reinterpret_cast<float *>(sm + IS_T);
     float *sX = reinterpret_cast<float *>(sm + IS_X);
     if (tid == 0) {
-        mbar_init(bar_ap, 1);
+        mbar_init(bar_ap, 2);
         mbar_init(bar_wu, 1);
         mbar_fence_init();
     }
@@ -299,14 +301,16 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     // The description of the next item (chunk, head, A_log) is fetched while the
     // current one is processed, and its first two raw slices are issued as soon as
     // the current item's W / U MMAs have released the raw buffers.
+    // item = chunk * H_v + head advances by gridDim.x: keep (chunk, head) incrementally
+    const int step_c = (int)(gridDim.x / p.H_v), step_h = (int)(gridDim.x % p.H_v);
     long long item = blockIdx.x;
-    int h_next = (int)(item % p.H_v);
-    ChunkDesc cd_next = p.chunks[item / p.H_v];
+    int chunk_next = (int)(item / p.H_v), h_next = (int)(item % p.H_v);
+    ChunkDesc cd_next = p.chunks[chunk_next];
     float alog_next = p.A_log[h_next];
     issue_raw(cd_next, h_next, 0);
     issue_raw(cd_next, h_next, 1);
     for (int it = 0; item < n_items; item += gridDim.x, ++it) {
-        const int chunk = (int)(item / p.H_v), h = h_next;
+        const int chunk = chunk_next, h = h_next;
         const ChunkDesc cd = cd_next;
         const float a_gate = ex2(alog_next * LOG2E);
         const int hq = h / group;
@@ -319,8 +323,13 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         const long long nitem = item + gridDim.x;
         const bool has_next = nitem < n_items;
         if (has_next) {
-            h_next = (int)(nitem % p.H_v);
-            cd_next = p.chunks[nitem / p.H_v];
+            chunk_next += step_c;
+            h_next += step_h;
+            if (h_next >= p.H_v) {
+                h_next -= p.H_v;
+                ++chunk_next;
+            }
+            cd_next = p.chunks[chunk_next];
             alog_next = p.A_log[h_next];
         }
 
@@ -448,7 +457,8 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                                     : which == 1 ? p.k + (tok * p.H_qk + nhq) * KD
                                     : which == 2 ? p.graw + (tok * p.H_v + h_next) * KD
                                                  : p.v + (tok * p.H_v + h_next) * KD;
-                prefetch_l2(src, KD * 2);
+                prefetch_line_l2(src);
+                prefetch_line_l2(src + 64);
             }
         }
         __syncthreads();
@@ -532,17 +542,17 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
-            if (tid == 0) {
+            // the two accumulators are issued by lane 0 of warps 0 and 4 (each in k order), each
+            // committing to the slice barrier, so neither warp carries the whole issue time
+            if (tid == 0 || tid == 128) {
                 tc_fence_after();
-                const uint32_t id_off = idesc_tf32(128, 96), id_diag = idesc_tf32(128, 64);
+                const bool off = tid == 0;
+                const uint32_t id = off ? idesc_tf32(128, 96) : idesc_tf32(128, 64);
+                const uint32_t arow = sbase + IS_ROWS + (off ? 0u : 16384u), bcol = sbase + IS_COLS + (off ? 8192u : 0u);
 #pragma unroll
-                for (int ks = 0; ks < SL / 8; ++ks) {
-                    const uint32_t acc = (sl > 0 || ks > 0) ? 1u : 0u;
-                    umma_tf32(t_off, umma_desc(sbase + IS_ROWS + ks * 32, 16, 1024),
-                              umma_desc(sbase + IS_COLS + 8192 + ks * 32, 16, 1024), id_off, acc);
-                    umma_tf32(t_diag, umma_desc(sbase + IS_ROWS + 16384 + ks * 32, 16, 1024),
-                              umma_desc(sbase + IS_COLS + ks * 32, 16, 1024), id_diag, acc);
-                }
+                for (int ks = 0; ks < SL / 8; ++ks)
+                    umma_tf32(off ? t_off : t_diag, umma_desc(arow + ks * 32, 16, 1024), umma_desc(bcol + ks * 32, 16, 1024),
+                              id, (sl > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(bar_ap);
             }
             if (sl + 2 < KD / SL) {

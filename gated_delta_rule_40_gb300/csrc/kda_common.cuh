@@ -238,6 +238,10 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 }  // namespace kda
 
 namespace kda {
+// Prefetch the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_line_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
 // Bulk prefetch of a global range into L2 (no shared memory involved).
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
