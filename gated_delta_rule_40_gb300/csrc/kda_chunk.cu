@@ -467,8 +467,16 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             const unsigned char *rawb = sm + IS_R2 + (sl & 1) * RAW_SLICE;
             // 2b. operands: thread (row r, 8-channel group g), two halves of 4 channels
             {
-                const int r = tid & 63, g = tid >> 6, bi = r >> 4, rl = r & 15;
+                const int r = tid & 63, g = tid >> 6, bi = r >> 4, rl = r & 15, r7 = r & 7;
                 const float rq = rv[RV_RQ + r], rk = rv[RV_RK + r];
+                // swizzled row bases: ROWS / COLS rows r + 64 i share r % 8, so they differ by 8 KiB per i;
+                // the H versions sit at COLS rows 64 + 16 v + rl
+                unsigned char *const rows_r = sm + IS_ROWS + (r >> 3) * 1024 + r7 * 128;
+                unsigned char *const cols_r = sm + IS_COLS + (r >> 3) * 1024 + r7 * 128;
+                unsigned char *const cols_v = sm + IS_COLS + (rl >> 3) * 1024 + r7 * 128;
+                // Kd^T element (k, r) of the record: k / 8 = c0 / 8 + g, k % 8 = 4 hh + e
+                unsigned char *const kd_r = rec + REC_KDT + (r >> 5) * 16384 + (c0 / 8 + g) * 1024 + (r & 3) * 4;
+                const int x4 = (r & 31) >> 2;
                 const uint4 qw = *reinterpret_cast<const uint4 *>(rawb + raw_off_qk(r, g));
                 const uint4 kw = *reinterpret_cast<const uint4 *>(rawb + RAW_T + raw_off_qk(r, g));
                 uint32_t kg2[4], qg2[4];
@@ -502,33 +510,31 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                         ck[e] = kh[e] * dc;
                         hk[e] = kh[e] * hf;
                         // Kd^T element (k = c + e, r) straight into the record (a warp writes one 128-byte line)
-                        stg_hint_b32(rec + REC_KDT + sw128_off(c + e, 4 * r, KD), tf32_bits(hk[e] * ea[e]), pol_ef);
+                        const int kk = 4 * hh + e;
+                        stg_hint_b32(kd_r + kk * 128 + ((x4 ^ kk) << 4), tf32_bits(hk[e] * ea[e]), pol_ef);
                     }
                     kg2[2 * hh] = pack_bf16x2(fk[0] * eb[0], fk[1] * eb[1]);
                     kg2[2 * hh + 1] = pack_bf16x2(fk[2] * eb[2], fk[3] * eb[3]);
                     qg2[2 * hh] = pack_bf16x2(fq[0] * eb[0], fq[1] * eb[1]);
                     qg2[2 * hh + 1] = pack_bf16x2(fq[2] * eb[2], fq[3] * eb[3]);
-                    const int kb = 4 * cls;
-                    sts128(sm + IS_ROWS + sw128_off(r, kb, 256), fk[0], fk[1], fk[2], fk[3]);
-                    sts128(sm + IS_ROWS + sw128_off(64 + r, kb, 256), fq[0], fq[1], fq[2], fq[3]);
-                    sts128(sm + IS_ROWS + sw128_off(128 + r, kb, 256), dk[0], dk[1], dk[2], dk[3]);
-                    sts128(sm + IS_ROWS + sw128_off(192 + r, kb, 256), dq[0], dq[1], dq[2], dq[3]);
-                    sts128(sm + IS_COLS + sw128_off(r, kb, 160), ck[0], ck[1], ck[2], ck[3]);
+                    const uint32_t sw = (uint32_t)(((2 * g + hh) ^ r7) << 4);   // swizzled 16-byte unit
+                    sts128(rows_r + sw, fk[0], fk[1], fk[2], fk[3]);
+                    sts128(rows_r + 8192 + sw, fq[0], fq[1], fq[2], fq[3]);
+                    sts128(rows_r + 16384 + sw, dk[0], dk[1], dk[2], dk[3]);
+                    sts128(rows_r + 24576 + sw, dq[0], dq[1], dq[2], dq[3]);
+                    sts128(cols_r + sw, ck[0], ck[1], ck[2], ck[3]);
                     if (bi == 0) {
                         const float4 D1 = *reinterpret_cast<const float4 *>(tab + TB_D1 * TBS + cls);
                         const float4 D12 = *reinterpret_cast<const float4 *>(tab + TB_D12 * TBS + cls);
-                        sts128(sm + IS_COLS + sw128_off(64 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
-                        sts128(sm + IS_COLS + sw128_off(80 + rl, kb, 160), hk[0] * D1.x, hk[1] * D1.y, hk[2] * D1.z,
-                               hk[3] * D1.w);
-                        sts128(sm + IS_COLS + sw128_off(112 + rl, kb, 160), hk[0] * D12.x, hk[1] * D12.y,
-                               hk[2] * D12.z, hk[3] * D12.w);
+                        sts128(cols_v + 8 * 1024 + sw, hk[0], hk[1], hk[2], hk[3]);
+                        sts128(cols_v + 10 * 1024 + sw, hk[0] * D1.x, hk[1] * D1.y, hk[2] * D1.z, hk[3] * D1.w);
+                        sts128(cols_v + 14 * 1024 + sw, hk[0] * D12.x, hk[1] * D12.y, hk[2] * D12.z, hk[3] * D12.w);
                     } else if (bi == 1) {
                         const float4 D2 = *reinterpret_cast<const float4 *>(tab + TB_D2 * TBS + cls);
-                        sts128(sm + IS_COLS + sw128_off(96 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
-                        sts128(sm + IS_COLS + sw128_off(128 + rl, kb, 160), hk[0] * D2.x, hk[1] * D2.y,
-                               hk[2] * D2.z, hk[3] * D2.w);
+                        sts128(cols_v + 12 * 1024 + sw, hk[0], hk[1], hk[2], hk[3]);
+                        sts128(cols_v + 16 * 1024 + sw, hk[0] * D2.x, hk[1] * D2.y, hk[2] * D2.z, hk[3] * D2.w);
                     } else if (bi == 2) {
-                        sts128(sm + IS_COLS + sw128_off(144 + rl, kb, 160), hk[0], hk[1], hk[2], hk[3]);
+                        sts128(cols_v + 18 * 1024 + sw, hk[0], hk[1], hk[2], hk[3]);
                     }
                 }
                 // Kg (bf16) into the MN-major operand: element (k = c0 + 8 g .. + 7, j = r)
