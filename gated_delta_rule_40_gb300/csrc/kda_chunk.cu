@@ -246,6 +246,33 @@ __device__ __forceinline__ void stg_hint_v4(void *p, uint4 v, uint64_t pol) {
                  : "memory");
 }
 
+// tf32 hi / lo split of an fp32 value: x ~ hi + lo with about 21 significant bits
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    hi = tf32_bits(x);
+    lo = tf32_bits(x - __uint_as_float(hi));
+}
+// One warp: D (16 x 8) += X (16 x 32, row-major, stride xs) . Y (32 x 8, row-major, stride ys)
+// with mma.sync m16n8k8 tf32 and the three-term split (hi*lo + lo*hi + hi*hi).
+// Fragment layout of m16n8k8: a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4);
+// b0 (k = t, n = g), b1 (k = t + 4, n = g); d0 (g, 2t), d1 (g, 2t + 1), d2 (g + 8, 2t), d3 (g + 8, 2t + 1).
+__device__ __forceinline__ void split_mma_32(const float *X, int xs, const float *Y, int ys, int g, int t,
+                                             float (&d)[4]) {
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        const int k = 8 * ks;
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(X[g * xs + k + t], ah[0], al[0]);
+        split_tf32(X[(g + 8) * xs + k + t], ah[1], al[1]);
+        split_tf32(X[g * xs + k + t + 4], ah[2], al[2]);
+        split_tf32(X[(g + 8) * xs + k + t + 4], ah[3], al[3]);
+        split_tf32(Y[(k + t) * ys + g], bh[0], bl[0]);
+        split_tf32(Y[(k + t + 4) * ys + g], bh[1], bl[1]);
+        mma_tf32(d, ah, bl);
+        mma_tf32(d, al, bh);
+        mma_tf32(d, ah, bh);
+    }
+}
+
 __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const IntraParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -680,31 +707,23 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         }
         __syncthreads();
         {
-            // X = A21 T1 (rows 32..63, columns 0..31), then T21 = -T2 X; thread: row r, 4 columns
-            const int r = tid >> 3, c4 = (tid & 7) * 4;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int kk = 0; kk < 32; ++kk) {
-                const float a = sA[(32 + r) * AS + kk];
-                const float4 y = *reinterpret_cast<const float4 *>(sT + kk * AS + c4);
-                acc.x = fmaf(a, y.x, acc.x);
-                acc.y = fmaf(a, y.y, acc.y);
-                acc.z = fmaf(a, y.z, acc.z);
-                acc.w = fmaf(a, y.w, acc.w);
-            }
-            *reinterpret_cast<float4 *>(sX + r * XS + c4) = acc;
+            // X = A21 T1 (rows 32..63, columns 0..31), then T21 = -T2 X, on mma.sync (m16n8k8 tf32)
+            // with both operands split into tf32 hi + lo terms (hi*lo + lo*hi + hi*hi, about fp32
+            // accuracy).  Warp w owns the 16 x 8 output tile (rows 16 (w >> 2), columns 8 (w & 3)).
+            const int gid = lane >> 2, tig = lane & 3, m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            split_mma_32(sA + (32 + m0) * AS, AS, sT + n0, AS, gid, tig, d);
+            sX[(m0 + gid) * XS + n0 + 2 * tig] = d[0];
+            sX[(m0 + gid) * XS + n0 + 2 * tig + 1] = d[1];
+            sX[(m0 + gid + 8) * XS + n0 + 2 * tig] = d[2];
+            sX[(m0 + gid + 8) * XS + n0 + 2 * tig + 1] = d[3];
             __syncthreads();
-            float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int kk = 0; kk < 32; ++kk) {
-                const float a = sT[(32 + r) * AS + 32 + kk];
-                const float4 x = *reinterpret_cast<const float4 *>(sX + kk * XS + c4);
-                t.x = fmaf(a, x.x, t.x);
-                t.y = fmaf(a, x.y, t.y);
-                t.z = fmaf(a, x.z, t.z);
-                t.w = fmaf(a, x.w, t.w);
-            }
-            *reinterpret_cast<float4 *>(sT + (32 + r) * AS + c4) = make_float4(-t.x, -t.y, -t.z, -t.w);
+            float t[4] = {0.f, 0.f, 0.f, 0.f};
+            split_mma_32(sT + (32 + m0) * AS + 32, AS, sX + n0, XS, gid, tig, t);
+            sT[(32 + m0 + gid) * AS + n0 + 2 * tig] = -t[0];
+            sT[(32 + m0 + gid) * AS + n0 + 2 * tig + 1] = -t[1];
+            sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig] = -t[2];
+            sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig + 1] = -t[3];
         }
         __syncthreads();
         // T' = T diag(beta), split into bf16 hi + lo, as the A operand (K-major, 64 r x 64 j)
