@@ -251,14 +251,14 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) 
     hi = tf32_bits(x);
     lo = tf32_bits(x - __uint_as_float(hi));
 }
-// One warp: D (16 x 8) += X (16 x 32, row-major, stride xs) . Y (32 x 8, row-major, stride ys)
+// One warp: D (16 x 8) += X (16 x 8 KS, row-major, stride xs) . Y (8 KS x 8, row-major, stride ys)
 // with mma.sync m16n8k8 tf32 and the three-term split (hi*lo + lo*hi + hi*hi).
 // Fragment layout of m16n8k8: a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4);
 // b0 (k = t, n = g), b1 (k = t + 4, n = g); d0 (g, 2t), d1 (g, 2t + 1), d2 (g + 8, 2t), d3 (g + 8, 2t + 1).
-__device__ __forceinline__ void split_mma_32(const float *X, int xs, const float *Y, int ys, int g, int t,
-                                             float (&d)[4]) {
+template <int KS>
+__device__ __forceinline__ void split_mma(const float *X, int xs, const float *Y, int ys, int g, int t, float (&d)[4]) {
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
+    for (int ks = 0; ks < KS; ++ks) {
         const int k = 8 * ks;
         uint32_t ah[4], al[4], bh[2], bl[2];
         split_tf32(X[g * xs + k + t], ah[0], al[0]);
@@ -662,14 +662,14 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         //         T21 = -T2 (A21 T1) with T1, T2 the diagonal 32 x 32 blocks.
         if (tid < 64) {
             const int bi = tid >> 4, c = tid & 15, o = 16 * bi;
+            // right-looking: once t[j] is final, subtract its column from the later rows
             float t[SUB];
 #pragma unroll
-            for (int r = 0; r < SUB; ++r) {
-                float sacc = (r == c) ? 1.f : 0.f;
+            for (int r = 0; r < SUB; ++r) t[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
-                for (int j = 0; j < r; ++j) sacc = fmaf(-sA[(o + r) * AS + o + j], t[j], sacc);
-                t[r] = sacc;
-            }
+            for (int j = 0; j < SUB; ++j)
+#pragma unroll
+                for (int r = j + 1; r < SUB; ++r) t[r] = fmaf(-sA[(o + r) * AS + o + j], t[j], t[r]);
 #pragma unroll
             for (int r = 0; r < SUB; ++r) sT[(o + r) * AS + o + c] = t[r];
         } else {
@@ -682,28 +682,29 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         }
         __syncthreads();
         {
-            // Z_b = A_{i,j} T_jj for (i, j) = (1, 0), (3, 2); thread: block b, row r, column pair cc
-            const int b = tid >> 7, e = tid & 127, r = e >> 3, cc = (e & 7) * 2;
+            // Z_b = A_{i,j} T_jj, then T_ij = -T_ii Z_b for (i, j) = (1, 0), (3, 2), on mma.sync with
+            // the three-term split; warps 0..3: block b = w >> 1, 8-column half w & 1
+            const int gid = lane >> 2, tig = lane & 3, b = warp >> 1, n0 = 8 * (warp & 1);
             const int bi = 2 * b + 1, bj = 2 * b;
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < SUB; ++kk) {
-                const float a = sA[(16 * bi + r) * AS + 16 * bj + kk];
-                const float2 y = *reinterpret_cast<const float2 *>(sT + (16 * bj + kk) * AS + 16 * bj + cc);
-                acc0 = fmaf(a, y.x, acc0);
-                acc1 = fmaf(a, y.y, acc1);
+            float *z = sX + b * 16 * ZS;
+            if (warp < 4) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
+                split_mma<2>(sA + (16 * bi) * AS + 16 * bj, AS, sT + (16 * bj) * AS + 16 * bj + n0, AS, gid, tig, d);
+                z[gid * ZS + n0 + 2 * tig] = d[0];
+                z[gid * ZS + n0 + 2 * tig + 1] = d[1];
+                z[(gid + 8) * ZS + n0 + 2 * tig] = d[2];
+                z[(gid + 8) * ZS + n0 + 2 * tig + 1] = d[3];
             }
-            *reinterpret_cast<float2 *>(sX + b * 16 * ZS + r * ZS + cc) = make_float2(acc0, acc1);
             __syncthreads();
-            float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < SUB; ++kk) {
-                const float a = sT[(16 * bi + r) * AS + 16 * bi + kk];
-                const float2 z = *reinterpret_cast<const float2 *>(sX + b * 16 * ZS + kk * ZS + cc);
-                t0 = fmaf(a, z.x, t0);
-                t1 = fmaf(a, z.y, t1);
+            if (warp < 4) {
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+                split_mma<2>(sT + (16 * bi) * AS + 16 * bi, AS, z + n0, ZS, gid, tig, t);
+                float *dst = sT + (16 * bi) * AS + 16 * bj + n0;
+                dst[gid * AS + 2 * tig] = -t[0];
+                dst[gid * AS + 2 * tig + 1] = -t[1];
+                dst[(gid + 8) * AS + 2 * tig] = -t[2];
+                dst[(gid + 8) * AS + 2 * tig + 1] = -t[3];
             }
-            *reinterpret_cast<float2 *>(sT + (16 * bi + r) * AS + 16 * bj + cc) = make_float2(-t0, -t1);
         }
         __syncthreads();
         {
@@ -712,14 +713,14 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             // accuracy).  Warp w owns the 16 x 8 output tile (rows 16 (w >> 2), columns 8 (w & 3)).
             const int gid = lane >> 2, tig = lane & 3, m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
             float d[4] = {0.f, 0.f, 0.f, 0.f};
-            split_mma_32(sA + (32 + m0) * AS, AS, sT + n0, AS, gid, tig, d);
+            split_mma<4>(sA + (32 + m0) * AS, AS, sT + n0, AS, gid, tig, d);
             sX[(m0 + gid) * XS + n0 + 2 * tig] = d[0];
             sX[(m0 + gid) * XS + n0 + 2 * tig + 1] = d[1];
             sX[(m0 + gid + 8) * XS + n0 + 2 * tig] = d[2];
             sX[(m0 + gid + 8) * XS + n0 + 2 * tig + 1] = d[3];
             __syncthreads();
             float t[4] = {0.f, 0.f, 0.f, 0.f};
-            split_mma_32(sT + (32 + m0) * AS + 32, AS, sX + n0, XS, gid, tig, t);
+            split_mma<4>(sT + (32 + m0) * AS + 32, AS, sX + n0, XS, gid, tig, t);
             sT[(32 + m0 + gid) * AS + n0 + 2 * tig] = -t[0];
             sT[(32 + m0 + gid) * AS + n0 + 2 * tig + 1] = -t[1];
             sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig] = -t[2];
