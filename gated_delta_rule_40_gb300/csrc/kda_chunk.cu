@@ -618,28 +618,51 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             // column offsets of the below-diagonal versions of row blocks 1, 2, 3 in D_off
             const int nsa = bia == 0 ? 0 : 16, nsb = bib == 1 ? 0 : 48;
             const float be = rv[RV_BETA + r], qkd = rv[RV_QK + r];
+            // Lanes 0..15 hold row block bia, lanes 16..31 row block bib = bia + 1 (half = lane >> 4).
+            // A: the inversion reads only the blocks below the diagonal and the strict lower part of
+            // the diagonal blocks, so A is stored unmasked.  P is the scan's exact lower-triangular
+            // operand: masked diagonal blocks, zeros above.  Every case below is warp-uniform.
+            const bool half = lane >= 16;
+            // o = half ? (column block at cy) : (column block at cx), both read from TMEM
+            auto load_pair = [&](uint32_t cx, uint32_t cy, float (&o)[16]) {
+                uint32_t x[16], y[16];
+                tmem_ld16_nowait(cx, x);
+                tmem_ld16_nowait(cy, y);
+                tmem_wait_ld();
 #pragma unroll
+                for (int j = 0; j < 16; ++j) o[j] = __uint_as_float(half ? y[j] : x[j]);
+            };
+#pragma unroll 1
             for (int cbi = 0; cbi < 2; ++cbi) {
                 const int cb = 2 * hf + cbi;
-                uint32_t va[16], vb2[16], vd[16];
-                tmem_ld16_nowait(t_off + lo + nsa + 16 * (cb < 3 ? cb : 2), va);
-                tmem_ld16_nowait(t_off + lo + nsb + 16 * (cb < 3 ? cb : 2), vb2);
-                tmem_ld16_nowait(t_diag + lo + 16 * cb, vd);
-                tmem_wait_ld();
+                const uint32_t ca = t_off + lo + nsa + 16 * cb, cbb = t_off + lo + nsb + 16 * cb, cd = t_diag + lo + 16 * cb;
                 float o[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    float x = 0.f;
-                    if (cb < bi) x = __uint_as_float(bi == bia ? va[j] : vb2[j]);
-                    else if (cb == bi) x = (j < rl) ? __uint_as_float(vd[j]) : ((isq && j == rl) ? qkd : 0.f);
-                    o[j] = x;
-                }
                 if (!isq) {
+                    if (cb > bib) continue;
+                    if (cb < bia) load_pair(ca, cbb, o);
+                    else if (cb == bia) load_pair(cd, cbb, o);
+                    else load_pair(cd, cd, o);
 #pragma unroll
                     for (int j = 0; j < 16; j += 4)
                         *reinterpret_cast<float4 *>(sA + r * AS + 16 * cb + j) =
                             make_float4(o[j] * be, o[j + 1] * be, o[j + 2] * be, o[j + 3] * be);
                 } else {
+                    if (cb < bia) {
+                        load_pair(ca, cbb, o);
+                    } else if (cb <= bib) {
+                        // lanes whose diagonal block this is keep j < rl and put q.k at j = rl; for
+                        // cb == bia the other half holds its off-diagonal block, for cb == bib zeros
+                        const bool diag = (cb == bia) != half;
+                        load_pair(cd, cb == bia ? cbb : cd, o);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float dv = j < rl ? o[j] : (j == rl ? qkd : 0.f);
+                            o[j] = diag ? dv : (cb == bia ? o[j] : 0.f);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) o[j] = 0.f;
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; j += 8)
                         *reinterpret_cast<uint4 *>(sm + IS_PI + sw128_off(r, 2 * (16 * cb + j), CH)) =
