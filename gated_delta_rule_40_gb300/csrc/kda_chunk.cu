@@ -771,18 +771,21 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         tc_fence_before();
         __syncthreads();
 
-        // ---- 5. W = T'_hi Kg + T'_lo Kg, U = T'_hi V + T'_lo V   (M = 64, N = 128, K = 64, bf16)
+        // ---- 5. W = (T'_hi + T'_lo) Kg   (M = 64 r, N = 128 k, K = 64 j, bf16; B MN-major) and
+        //         U^T = V^T (T'_hi + T'_lo)^T   (M = 128 v, N = 64 r, K = 64 j; A = V MN-major, B = T'
+        //         K-major), so that each TMEM lane v holds one row of the U image
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16(64, 128) | (1u << 16);   // B MN-major
+            const uint32_t id_w = idesc_bf16(64, 128) | (1u << 16);
+            const uint32_t id_u = idesc_bf16(128, 64) | (1u << 15);
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks) {
-                    const uint64_t a = umma_desc(sbase + (part ? IS_TPL : IS_TPH) + ks * 32, 16, 1024);
+                    const uint64_t tp = umma_desc(sbase + (part ? IS_TPL : IS_TPH) + ks * 32, 16, 1024);
                     const uint32_t acc = (part > 0 || ks > 0) ? 1u : 0u;
-                    umma_bf16(t_w, a, umma_desc(sbase + IS_KG + ks * 2048, 8192, 1024), id, acc);
-                    umma_bf16(t_u, a, umma_desc(sbase + IS_V + ks * 2048, 8192, 1024), id, acc);
+                    umma_bf16(t_w, tp, umma_desc(sbase + IS_KG + ks * 2048, 8192, 1024), id_w, acc);
+                    umma_bf16(t_u, umma_desc(sbase + IS_V + ks * 2048, 8192, 1024), tp, id_u, acc);
                 }
             umma_commit(bar_wu);
             if (!mbar_wait(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
@@ -796,17 +799,33 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             issue_raw(cd_next, h_next, 1);
         }
         {
-            // M = 64 layout: row r = 16 (w & 3) + lane for lane < 16; warps 0..3 read W, 4..7 read U
-            const int q = warp & 3, hf = warp >> 2, r = q * 16 + lane;
+            const int q = warp & 3;
             const uint32_t lo = (uint32_t)(q * 32) << 16;
-#pragma unroll
-            for (int rd = 0; rd < 2; ++rd) {
+            if (warp < 4) {
+                // U^T: lane v = 32 q + lane holds U[r][v] for r = 0..63, i.e. row v of the U image
+                const int v = q * 32 + lane;
                 uint32_t x0[32], x1[32];
-                tmem_ld32_nowait(t_w + 128 * hf + lo + 64 * rd, x0);
-                tmem_ld32_nowait(t_w + 128 * hf + lo + 64 * rd + 32, x1);
+                tmem_ld32_nowait(t_u + lo, x0);
+                tmem_ld32_nowait(t_u + lo + 32, x1);
                 tmem_wait_ld();
-                if (lane < 16) {
-                    if (hf == 0) {
+                float *us = reinterpret_cast<float *>(sm + IS_US) + (v >> 6) * (CH * 68) + (v & 63) * 68;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    *reinterpret_cast<float4 *>(us + j) = make_float4(__uint_as_float(x0[j]), __uint_as_float(x0[j + 1]),
+                                                                      __uint_as_float(x0[j + 2]), __uint_as_float(x0[j + 3]));
+                    *reinterpret_cast<float4 *>(us + 32 + j) = make_float4(__uint_as_float(x1[j]), __uint_as_float(x1[j + 1]),
+                                                                           __uint_as_float(x1[j + 2]), __uint_as_float(x1[j + 3]));
+                }
+            } else {
+                // W, M = 64 layout: row r = 16 q + lane for lane < 16
+                const int r = q * 16 + lane;
+#pragma unroll
+                for (int rd = 0; rd < 2; ++rd) {
+                    uint32_t x0[32], x1[32];
+                    tmem_ld32_nowait(t_w + lo + 64 * rd, x0);
+                    tmem_ld32_nowait(t_w + lo + 64 * rd + 32, x1);
+                    tmem_wait_ld();
+                    if (lane < 16) {
                         // W[r][k], k = 64 rd .. : row 64 + r of the WQ image (bf16)
 #pragma unroll
                         for (int j = 0; j < 64; j += 8) {
@@ -819,14 +838,6 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                                 pack_bf16x2(__uint_as_float(xs[jj + 2]), __uint_as_float(xs[jj + 3])),
                                 pack_bf16x2(__uint_as_float(xs[jj + 4]), __uint_as_float(xs[jj + 5])),
                                 pack_bf16x2(__uint_as_float(xs[jj + 6]), __uint_as_float(xs[jj + 7])));
-                        }
-                    } else {
-                        // U[r][v], v = 64 rd .. : U image block rd, row v, column r
-                        float *us = reinterpret_cast<float *>(sm + IS_US) + rd * (CH * 68) + r;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            us[j * 68] = __uint_as_float(x0[j]);
-                            us[(32 + j) * 68] = __uint_as_float(x1[j]);
                         }
                     }
                 }
