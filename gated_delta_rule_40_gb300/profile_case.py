@@ -1,0 +1,41 @@
+"""Run the KDA forward a few times on one seeded workload, for profilers.
+
+    python -m gated_delta_rule_40_gb300.profile_case --B 1 --T 8192 --H 32 --iters 4
+
+Inputs come from ``kda_inputs`` (same recipe as the tests and the benchmark);
+the workspace is allocated once, so every iteration is exactly the three
+kernel launches of ``kda_fwd``.  A profiler then selects launches by kernel
+name and index (e.g. ``ncu -k regex:intra_kernel -s 2 -c 1``).
+"""
+import argparse
+import os
+import sys
+
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import kda_inputs  # noqa: E402
+from gated_delta_rule_40_gb300 import kda  # noqa: E402
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--B", type=int, default=1)
+    ap.add_argument("--T", type=int, default=8192)
+    ap.add_argument("--H", type=int, default=32, help="value heads (= q/k heads)")
+    ap.add_argument("--iters", type=int, default=4)
+    ap.add_argument("--seed", type=int, default=0)
+    a = ap.parse_args()
+    x = kda_inputs.make_inputs(B=a.B, T=a.T, H_qk=a.H, H_v=a.H, seed=a.seed, with_state=True)
+    dev = lambda t: t.cuda() if t is not None else None  # noqa: E731
+    q, k, v, g, b, A, s0 = map(dev, (x.q, x.k, x.v, x.graw, x.b, x.A_log, x.initial_state))
+    ws = torch.empty(kda.kda_fwd_workspace_size(a.B, a.B, a.T, a.H, a.H), dtype=torch.uint8, device="cuda")
+    for _ in range(a.iters):
+        out, fin = kda.kda_fwd(q, k, v, g, b, A, x.scale, initial_state=s0, workspace=ws)
+    torch.cuda.synchronize()
+    print(f"kda_fwd B={a.B} T={a.T} H={a.H} x{a.iters}: |out| {float(out.float().abs().mean()):.6f} "
+          f"|S| {float(fin.abs().mean()):.6f}")
+
+
+if __name__ == "__main__":
+    main()
