@@ -14,7 +14,7 @@ namespace kda {
 constexpr int DEC_WARPS = 8;
 constexpr int DEC_ROWS = KD / DEC_WARPS;  // state rows per warp
 
-__global__ __launch_bounds__(DEC_WARPS * 32) void decode_kernel(
+__global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
     const uint16_t *__restrict__ graw, const uint16_t *__restrict__ b, const float *__restrict__ A_log,
     float scale, float *__restrict__ state, int H_qk, int H_v, uint16_t *__restrict__ out) {
