@@ -603,7 +603,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             }
             if (sl + 1 < KD / SL) gate_tables(sl + 1);
             // this slice's MMAs must be done with ROWS / COLS (and, after the last, with TMEM)
-            if (tid == 0 && !mbar_wait(bar_ap, sl & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            if (tid == 0 && !mbar_spin(bar_ap, sl & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
             __syncthreads();
             tc_fence_after();
         }
@@ -788,7 +788,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                     umma_bf16(t_u, umma_desc(sbase + IS_V + ks * 2048, 8192, 1024), tp, id_u, acc);
                 }
             umma_commit(bar_wu);
-            if (!mbar_wait(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            if (!mbar_spin(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
             bulk_wait_read_all();   // the P image store is done reading before W / U staging reuses it
         }
         __syncthreads();
@@ -927,8 +927,9 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
 
     if (tid == 0) {
         for (int i = 0; i < BAR_SBR; ++i) mbar_init(bar + 8 * i, 1);
-        mbar_init(bar + 8 * BAR_SBR, SC_EPI);
-        mbar_init(bar + 8 * BAR_DTR, SC_EPI);
+        // one arrival per epilogue warp (lane 0, after the warp's proxy fences and a warp sync)
+        mbar_init(bar + 8 * BAR_SBR, SC_EPI / 32);
+        mbar_init(bar + 8 * BAR_DTR, SC_EPI / 32);
         mbar_fence_init();
         *abort_flag = 0;
     }
@@ -1003,7 +1004,6 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                     prefetch_l2(r2 + REC_GC, 512);
                 }
                 if (!mbar_wait(bar + 8 * BAR_DTR, c & 1)) { fail(); break; }
-                if (c + 1 < n) issue_u(c + 1);
                 if (!mbar_wait(bar + 8 * (BAR_PK0 + b), pp)) { fail(); break; }
                 tc_fence_after();
 #pragma unroll
@@ -1019,6 +1019,8 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                               umma_desc(sbase + SS_P + b * 8192 + ks * 32, 16, 1024), id2, 1);
                 }
                 umma_commit(bar + 8 * BAR_MMA2);
+                // the U buffer is free once Delta of chunk c is written (after the MMAs: off the chain)
+                if (c + 1 < n) issue_u(c + 1);
             }
             // drain whatever is still in flight (bounded)
             for (int i = 0; i < BAR_SBR; ++i)
@@ -1035,7 +1037,7 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
         const int vme = q * 16 + lane;      // v owned in the M = 64 layout (lane < 16)
         const bool vact = lane < 16;
         auto emit_output = [&](int cc) {
-            if (!mbar_wait(bar + 8 * BAR_MMA2, cc & 1)) fail();
+            if (!mbar_spin(bar + 8 * BAR_MMA2, cc & 1)) fail();
             tc_fence_after();
             const uint32_t tY = tmem + (cc & 1) * 128;
             uint32_t y0[32];
@@ -1076,9 +1078,12 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar + 8 * BAR_SBR);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + 8 * BAR_SBR);
+            // ---- previous chunk's output, while MMA1 of this chunk runs
+            if (c > 0) emit_output(c - 1);
             // ---- Delta^T = U^T - (W S^T)^T, as tf32 (B of MMA3) and bf16 (A of MMA2)
-            if (!mbar_wait(bar + 8 * BAR_MMA1, c & 1) || !mbar_wait(bar + 8 * BAR_U, c & 1)) fail();
+            if (!mbar_spin(bar + 8 * BAR_MMA1, c & 1) || !mbar_spin(bar + 8 * BAR_U, c & 1)) fail();
             tc_fence_after();
             const float g = reinterpret_cast<const float *>(sm + SS_GC)[kme];
             {
@@ -1109,11 +1114,10 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(bar + 8 * BAR_DTR);
-            // ---- previous chunk's output (overlaps MMA3 of this chunk)
-            if (c > 0) emit_output(c - 1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + 8 * BAR_DTR);
             // ---- S = S * exp(Gam_C) + Z   (lanes k of Z, columns v of this half)
-            if (!mbar_wait(bar + 8 * BAR_MMA3, c & 1)) fail();
+            if (!mbar_spin(bar + 8 * BAR_MMA3, c & 1)) fail();
             tc_fence_after();
             {
                 uint32_t z0[32];

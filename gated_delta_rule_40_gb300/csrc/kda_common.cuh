@@ -205,6 +205,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32
     }
     return false;
 }
+// Bounded spin on the phase with the given parity with the non-suspending probe
+// (test_wait): a thread on a latency-critical hand-off resumes within a probe's
+// latency of the phase completing, where a suspended try_wait can take several
+// hundred cycles to wake.  False if it gave up.
+__device__ __forceinline__ bool mbar_spin(uint32_t mbar, uint32_t parity, uint32_t limit = (1u << 24)) {
+    uint32_t done = 0;
+    for (uint32_t it = 0; it < limit; ++it) {
+        asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
 // Bulk (non-tensor) async copy global -> shared, completion on an mbarrier.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void *src, uint32_t bytes, uint32_t mbar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
