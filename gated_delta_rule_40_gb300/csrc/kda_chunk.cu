@@ -509,7 +509,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                 uint32_t kg2[4], qg2[4];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int cls = 8 * g + 4 * hh, c = c0 + cls;
+                    const int cls = 8 * g + 4 * hh;
                     const float4 G = *reinterpret_cast<const float4 *>(ga + ga_idx(r, cls));
                     const float4 MU = *reinterpret_cast<const float4 *>(tab + (TB_MU + bi) * TBS + cls);
                     const float4 M0 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi) * TBS + cls);
@@ -612,7 +612,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         //         32 (w & 3) .. (K rows 0..63, Q rows 64..127), 16-column blocks 2 (w >> 2) and 2 (w >> 2) + 1.
         {
             const int q = warp & 3, hf = warp >> 2;
-            const int l = q * 32 + lane, r = l & 63, bi = r >> 4, rl = r & 15, isq = l >> 6;
+            const int l = q * 32 + lane, r = l & 63, rl = r & 15, isq = l >> 6;
             const uint32_t lo = (uint32_t)(q * 32) << 16;
             const int bia = 2 * (q & 1), bib = bia + 1;
             // column offsets of the below-diagonal versions of row blocks 1, 2, 3 in D_off
