@@ -134,9 +134,9 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
 //   KDT Kd^T: rows k = 0..127 x 64 (r), tf32                      (32 KiB)
 //   U   [V block 0 | V block 1], each [64 v][68] fp32 (64 r + 4 pad)  (34 KiB)
 //   GC  exp(Gam_C) per channel, fp32                              (512 B)
-constexpr uint32_t REC_WQ = 0, REC_P = 32768, REC_KDT = 40960, REC_U = 73728, REC_GC = 108544;
+constexpr uint32_t REC_WQ = 0, REC_P = 32768, REC_KDT = 40960, REC_U = 73728, REC_GC = 108544, REC_RN = 109056;
 constexpr uint32_t REC_U_BLOCK = 64 * 68 * 4;   // 17408 B per V block
-constexpr uint32_t REC_BYTES = 109056;
+constexpr uint32_t REC_BYTES = 109568;
 
 // =====================================================================
 // Intra-chunk kernel: persistent CTAs of 8 warps, two resident per SM, each
@@ -197,6 +197,9 @@ constexpr uint32_t IS_T = IS_R1 + 17408;     // fp32 [64][68]
 constexpr uint32_t IS_X = IS_R1 + 34816;     // fp32 [32][36] (or [2][16][20])
 constexpr uint32_t IS_PI = IS_R1 + 39424;    // P image staging (bf16, 8 KiB)
 constexpr uint32_t IS_V = IS_R2;             // B of the U MMA: V, MN-major bf16, N = 128 (v), K = 64 (j)
+constexpr uint32_t IS_PN = IS_R2 + RAW_SLICE + 2 * RAW_T;   // row-norm partial sums [256] float4 (graw of buffer 1)
+constexpr uint32_t IS_TWH = IS_A;            // A of the W MMA: T'_W = T diag(beta rk), hi / lo (A is dead by then)
+constexpr uint32_t IS_TWL = IS_A + 8192;
 constexpr uint32_t IS_TPH = IS_R3;           // A of the W/U MMAs: T'_hi, 64 rows (r) x 64 (j) bf16
 constexpr uint32_t IS_TPL = IS_R3 + 8192;    // T'_lo
 constexpr uint32_t IS_WS = IS_R1;            // W half of the WQ image (2 x 8 KiB)
@@ -340,12 +343,9 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         const int chunk = chunk_next, h = h_next;
         const ChunkDesc cd = cd_next;
         const float a_gate = ex2(alog_next * LOG2E);
-        const int hq = h / group;
         const size_t ch = (size_t)chunk * p.H_v + h;
         unsigned char *rec = p.rec + ch * REC_BYTES;
         const int len = cd.len;
-        const uint16_t *qrow = p.q + ((size_t)cd.tok * p.H_qk + hq) * KD;   // row r at + r * H_qk * KD
-        const uint16_t *krow = p.k + ((size_t)cd.tok * p.H_qk + hq) * KD;
         const uint16_t *vrow = p.v + ((size_t)cd.tok * p.H_v + h) * KD;    // row r at + r * H_v * KD
         const long long nitem = item + gridDim.x;
         const bool has_next = nitem < n_items;
@@ -360,21 +360,9 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             alog_next = p.A_log[h_next];
         }
 
-        // ---- 1. loads for the row norms (global memory, consumed after the first gate step):
-        //         thread (row, quarter of the channels); beta
+        // ---- 1. beta (global load, consumed after the first gate step)
         float bb_raw = 0.f;
         if (tid < len) bb_raw = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
-        uint4 nq[4], nk[4];
-        {
-            const int r = tid >> 2, part = tid & 3;
-            const uint4 *qs = reinterpret_cast<const uint4 *>(qrow + r * qk_stride + part * 32);
-            const uint4 *ks = reinterpret_cast<const uint4 *>(krow + r * qk_stride + part * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                nq[i] = r < len ? __ldg(qs + i) : make_uint4(0, 0, 0, 0);
-                nk[i] = r < len ? __ldg(ks + i) : make_uint4(0, 0, 0, 0);
-            }
-        }
         cp_async_wait<1>();   // slice 0 landed (this thread's copies)
         // the previous item's bulk stores must be done reading shared memory (W/U staging, P, exp(Gam_C))
         if (tid == 0) bulk_wait_read_all();
@@ -442,38 +430,13 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         };
 
         // ---- 2. channel slices.  Order per slice s: operands(s), MMAs(s), gate/tables(s + 1),
-        //         wait for MMAs(s); the gate of slice 0 and the row norms come first.
+        //         wait for MMAs(s); the gate of slice 0 comes first.  q and k enter the operands
+        //         unnormalised: every product below is linear in a row's q or k, so the L2
+        //         norms (summed from the staged slices) are applied afterwards: to A and P in
+        //         their epilogue, to Kg through T' for W, and by the scan to Kd and Qg.
+        float psq = 0.f, psk = 0.f, psqk = 0.f;   // this thread's partial sums of q.q, k.k, q.k
         gate_tables(0);
-        {
-            const int r = tid >> 2, part = tid & 3;
-            float sq = 0.f, sk = 0.f, sqk = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t qw[4] = {nq[i].x, nq[i].y, nq[i].z, nq[i].w};
-                const uint32_t kw[4] = {nk[i].x, nk[i].y, nk[i].z, nk[i].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float a0 = bf16_lo(qw[j]), a1 = bf16_hi(qw[j]);
-                    const float b0 = bf16_lo(kw[j]), b1 = bf16_hi(kw[j]);
-                    sq = fmaf(a0, a0, fmaf(a1, a1, sq));
-                    sk = fmaf(b0, b0, fmaf(b1, b1, sk));
-                    sqk = fmaf(a0, b0, fmaf(a1, b1, sqk));
-                }
-            }
-#pragma unroll
-            for (int o = 1; o < 4; o <<= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-                sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
-            }
-            if (part == 0) {
-                const float rq = p.scale * rsqrtf(sq + L2_EPS), rk = rsqrtf(sk + L2_EPS);
-                rv[RV_RQ + r] = rq;
-                rv[RV_RK + r] = rk;
-                rv[RV_QK + r] = sqk * rq * rk;
-            }
-            if (tid < CH) rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-bb_raw * LOG2E)) : 0.f;
-        }
+        if (tid < CH) rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-bb_raw * LOG2E)) : 0.f;
         // pull the next item's rows into L2 while this one is processed
         if (has_next) {
             const int r = tid & 63, which = tid >> 6;
@@ -495,7 +458,6 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             // 2b. operands: thread (row r, 8-channel group g), two halves of 4 channels
             {
                 const int r = tid & 63, g = tid >> 6, bi = r >> 4, rl = r & 15, r7 = r & 7;
-                const float rq = rv[RV_RQ + r], rk = rv[RV_RK + r];
                 // swizzled row bases: ROWS / COLS rows r + 64 i share r % 8, so they differ by 8 KiB per i;
                 // the H versions sit at COLS rows 64 + 16 v + rl
                 unsigned char *const rows_r = sm + IS_ROWS + (r >> 3) * 1024 + r7 * 128;
@@ -521,8 +483,14 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                     const float gg[4] = {G.x, G.y, G.z, G.w}, mu[4] = {MU.x, MU.y, MU.z, MU.w};
                     const float m0[4] = {M0.x, M0.y, M0.z, M0.w}, m1[4] = {M1.x, M1.y, M1.z, M1.w};
                     const float eb[4] = {EB.x, EB.y, EB.z, EB.w}, ea[4] = {EA.x, EA.y, EA.z, EA.w};
-                    const float kh[4] = {bf16_lo(k0) * rk, bf16_hi(k0) * rk, bf16_lo(k1) * rk, bf16_hi(k1) * rk};
-                    const float qt[4] = {bf16_lo(q0) * rq, bf16_hi(q0) * rq, bf16_lo(q1) * rq, bf16_hi(q1) * rq};
+                    const float kh[4] = {bf16_lo(k0), bf16_hi(k0), bf16_lo(k1), bf16_hi(k1)};   // unnormalised
+                    const float qt[4] = {bf16_lo(q0), bf16_hi(q0), bf16_lo(q1), bf16_hi(q1)};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        psq = fmaf(qt[e], qt[e], psq);
+                        psk = fmaf(kh[e], kh[e], psk);
+                        psqk = fmaf(qt[e], kh[e], psqk);
+                    }
                     float fk[4], fq[4], dk[4], dq[4], ck[4], hk[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -571,7 +539,12 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                 stg_hint_v4(rec + REC_WQ + sw128_off(r, 2 * (c0 + 8 * g), 2 * CH), make_uint4(qg2[0], qg2[1], qg2[2], qg2[3]),
                             pol_ef);
             }
-            if (sl + 1 < KD / SL) cp_async_wait<0>();   // the next slice's raw rows (this thread's copies)
+            if (sl + 1 < KD / SL) {
+                cp_async_wait<0>();   // the next slice's raw rows (this thread's copies)
+            } else {
+                // the four partial sums of row r (threads r + 64 g) go to the graw part of raw buffer 1
+                reinterpret_cast<float4 *>(sm + IS_PN)[tid] = make_float4(psq, psk, psqk, 0.f);
+            }
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -607,6 +580,17 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             __syncthreads();
             tc_fence_after();
         }
+        // row norms: rq = scale / |q|, rk = 1 / |k|; QK keeps the raw q.k (the P diagonal is
+        // q.k rk; the column scaling of the epilogue supplies rk)
+        if (tid < CH) {
+            const float4 *pn = reinterpret_cast<const float4 *>(sm + IS_PN);
+            const float4 a0 = pn[tid], a1 = pn[tid + 64], a2 = pn[tid + 128], a3 = pn[tid + 192];
+            const float sq = (a0.x + a1.x) + (a2.x + a3.x), sk = (a0.y + a1.y) + (a2.y + a3.y);
+            rv[RV_RQ + tid] = p.scale * rsqrtf(sq + L2_EPS);
+            rv[RV_RK + tid] = rsqrtf(sk + L2_EPS);
+            rv[RV_QK + tid] = (a0.z + a1.z) + (a2.z + a3.z);
+        }
+        __syncthreads();
 
         // ---- 3. A (times beta) to smem, P image (bf16) to staging.  Warp w: TMEM lanes
         //         32 (w & 3) .. (K rows 0..63, Q rows 64..127), 16-column blocks 2 (w >> 2) and 2 (w >> 2) + 1.
@@ -617,7 +601,8 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             const int bia = 2 * (q & 1), bib = bia + 1;
             // column offsets of the below-diagonal versions of row blocks 1, 2, 3 in D_off
             const int nsa = bia == 0 ? 0 : 16, nsb = bib == 1 ? 0 : 48;
-            const float be = rv[RV_BETA + r], qkd = rv[RV_QK + r];
+            // A = beta_r rk_r rk_j (raw product); the P image holds P / rq_r = rk_j (raw product)
+            const float be = rv[RV_BETA + r] * rv[RV_RK + r], qkd = rv[RV_QK + r];
             // Lanes 0..15 hold row block bia, lanes 16..31 row block bib = bia + 1 (half = lane >> 4).
             // A: the inversion reads only the blocks below the diagonal and the strict lower part of
             // the diagonal blocks, so A is stored unmasked.  P is the scan's exact lower-triangular
@@ -636,7 +621,15 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             for (int cbi = 0; cbi < 2; ++cbi) {
                 const int cb = 2 * hf + cbi;
                 const uint32_t ca = t_off + lo + nsa + 16 * cb, cbb = t_off + lo + nsb + 16 * cb, cd = t_diag + lo + 16 * cb;
-                float o[16];
+                float o[16], ck[16];   // ck: column scales rk_j of this 16-column block
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(rv + RV_RK + 16 * cb + j);
+                    ck[j] = t4.x;
+                    ck[j + 1] = t4.y;
+                    ck[j + 2] = t4.z;
+                    ck[j + 3] = t4.w;
+                }
                 if (!isq) {
                     if (cb > bib) continue;
                     if (cb < bia) load_pair(ca, cbb, o);
@@ -645,7 +638,8 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
 #pragma unroll
                     for (int j = 0; j < 16; j += 4)
                         *reinterpret_cast<float4 *>(sA + r * AS + 16 * cb + j) =
-                            make_float4(o[j] * be, o[j + 1] * be, o[j + 2] * be, o[j + 3] * be);
+                            make_float4(o[j] * be * ck[j], o[j + 1] * be * ck[j + 1], o[j + 2] * be * ck[j + 2],
+                                        o[j + 3] * be * ck[j + 3]);
                 } else {
                     if (cb < bia) {
                         load_pair(ca, cbb, o);
@@ -664,6 +658,8 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                         for (int j = 0; j < 16; ++j) o[j] = 0.f;
                     }
 #pragma unroll
+                    for (int j = 0; j < 16; ++j) o[j] *= ck[j];
+#pragma unroll
                     for (int j = 0; j < 16; j += 8)
                         *reinterpret_cast<uint4 *>(sm + IS_PI + sw128_off(r, 2 * (16 * cb + j), CH)) =
                             make_uint4(pack_bf16x2(o[j], o[j + 1]), pack_bf16x2(o[j + 2], o[j + 3]),
@@ -677,6 +673,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         if (tid == 0) {
             bulk_s2g_hint(rec + REC_P, sbase + IS_PI, 8192, pol_ef);
             bulk_s2g_hint(rec + REC_GC, sbase + IS_GCS, 512, pol_ef);
+            bulk_s2g_hint(rec + REC_RN, sbase + IS_RV, 512, pol_ef);   // rq[64], rk[64] for the scan
             bulk_commit();
         }
 
@@ -750,28 +747,38 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig + 1] = -t[3];
         }
         __syncthreads();
-        // T' = T diag(beta), split into bf16 hi + lo, as the A operand (K-major, 64 r x 64 j)
+        // T' = T diag(beta) (for U) and T'_W = T diag(beta rk) (for W: Kg is unnormalised), each
+        // split into bf16 hi + lo, as A operands (K-major, 64 r x 64 j)
         for (int idx = tid; idx < CH * (CH / 8); idx += IN_THREADS) {
             const int r = idx >> 3, j = (idx & 7) * 8;
-            float x[8];
-            uint32_t hi[4], lo[4];
+            float x[8], xw[8];
+            uint32_t hi[4], lo[4], hw[4], lw[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = sT[r * AS + j + e] * rv[RV_BETA + j + e];
+            for (int e = 0; e < 8; ++e) {
+                x[e] = sT[r * AS + j + e] * rv[RV_BETA + j + e];
+                xw[e] = x[e] * rv[RV_RK + j + e];
+            }
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
                 const uint32_t h2 = pack_bf16x2(x[e], x[e + 1]);
                 hi[e >> 1] = h2;
                 lo[e >> 1] = pack_bf16x2(x[e] - bf16_lo(h2), x[e + 1] - bf16_hi(h2));
+                const uint32_t w2 = pack_bf16x2(xw[e], xw[e + 1]);
+                hw[e >> 1] = w2;
+                lw[e >> 1] = pack_bf16x2(xw[e] - bf16_lo(w2), xw[e + 1] - bf16_hi(w2));
             }
-            *reinterpret_cast<uint4 *>(sm + IS_TPH + sw128_off(r, 2 * j, CH)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(sm + IS_TPL + sw128_off(r, 2 * j, CH)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            const uint32_t off = sw128_off(r, 2 * j, CH);
+            *reinterpret_cast<uint4 *>(sm + IS_TPH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sm + IS_TPL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(sm + IS_TWH + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(sm + IS_TWL + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
         cp_async_wait<0>();   // V (this thread's copies)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ---- 5. W = (T'_hi + T'_lo) Kg   (M = 64 r, N = 128 k, K = 64 j, bf16; B MN-major) and
+        // ---- 5. W = (T'_W,hi + T'_W,lo) Kg   (M = 64 r, N = 128 k, K = 64 j, bf16; B MN-major) and
         //         U^T = V^T (T'_hi + T'_lo)^T   (M = 128 v, N = 64 r, K = 64 j; A = V MN-major, B = T'
         //         K-major), so that each TMEM lane v holds one row of the U image
         if (tid == 0) {
@@ -783,8 +790,9 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks) {
                     const uint64_t tp = umma_desc(sbase + (part ? IS_TPL : IS_TPH) + ks * 32, 16, 1024);
+                    const uint64_t tw = umma_desc(sbase + (part ? IS_TWL : IS_TWH) + ks * 32, 16, 1024);
                     const uint32_t acc = (part > 0 || ks > 0) ? 1u : 0u;
-                    umma_bf16(t_w, tp, umma_desc(sbase + IS_KG + ks * 2048, 8192, 1024), id_w, acc);
+                    umma_bf16(t_w, tw, umma_desc(sbase + IS_KG + ks * 2048, 8192, 1024), id_w, acc);
                     umma_bf16(t_u, umma_desc(sbase + IS_V + ks * 2048, 8192, 1024), tp, id_u, acc);
                 }
             umma_commit(bar_wu);
@@ -890,11 +898,12 @@ constexpr uint32_t SS_DT = 163840;     // 16 KiB      Delta^T tf32: 64 rows (v) 
 constexpr uint32_t SS_DTB = 180224;    // 8 KiB       Delta^T bf16: 64 rows (v) x 64 (j)  (A of MMA2)
 constexpr uint32_t SS_U = 188416;      // 17 KiB      U block, fp32 [64 v][68]
 constexpr uint32_t SS_OS = 205824;     // 8 KiB       output transpose, bf16 [64 r][64 v]
-constexpr uint32_t SS_GC = 214016;     // 512 B
-constexpr uint32_t SS_BAR = 214528;    // mbarriers
-constexpr uint32_t SS_SLOT = 214656;   // TMEM address slot
-constexpr uint32_t SS_FLAG = 214660;   // abort flag
-constexpr uint32_t SS_BYTES = 214720 + 1024;   // + alignment slack
+constexpr uint32_t SS_GC = 214016;     // 1 KiB       exp(Gam_C) [128], then rq [64], rk [64] (record order)
+constexpr uint32_t SS_RQ = 215040;     // 256 B       rq of the chunk whose output is emitted next
+constexpr uint32_t SS_BAR = 215296;    // mbarriers
+constexpr uint32_t SS_SLOT = 215424;   // TMEM address slot
+constexpr uint32_t SS_FLAG = 215428;   // abort flag
+constexpr uint32_t SS_BYTES = 215488 + 1024;   // + alignment slack
 
 struct ScanParams {
     const unsigned char *rec;
@@ -966,9 +975,9 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
             };
             auto issue_u = [&](int c) {
                 const unsigned char *r = rec_of(c);
-                mbar_expect_tx(bar + 8 * BAR_U, REC_U_BLOCK + 512);
+                mbar_expect_tx(bar + 8 * BAR_U, REC_U_BLOCK + 1024);
                 bulk_g2s(sbase + SS_U, r + REC_U + vb * REC_U_BLOCK, REC_U_BLOCK, bar + 8 * BAR_U);
-                bulk_g2s(sbase + SS_GC, r + REC_GC, 512, bar + 8 * BAR_U);
+                bulk_g2s(sbase + SS_GC, r + REC_GC, 1024, bar + 8 * BAR_U);   // exp(Gam_C), rq, rk
             };
             const uint32_t id1 = idesc_bf16(64, 128) | (1u << 15);   // A (S) MN-major
             const uint32_t id2 = idesc_bf16(64, 64), id3 = idesc_tf32(128, VB);
@@ -1001,7 +1010,7 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                     const unsigned char *r2 = rec_of(c + 2);
                     prefetch_l2(r2 + REC_WQ, 32768 + 8192 + 32768);
                     prefetch_l2(r2 + REC_U + vb * REC_U_BLOCK, REC_U_BLOCK);
-                    prefetch_l2(r2 + REC_GC, 512);
+                    prefetch_l2(r2 + REC_GC, 1024);
                 }
                 if (!mbar_wait(bar + 8 * BAR_DTR, c & 1)) { fail(); break; }
                 if (!mbar_wait(bar + 8 * (BAR_PK0 + b), pp)) { fail(); break; }
@@ -1045,8 +1054,16 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
             tmem_wait_ld();
             uint16_t *os = reinterpret_cast<uint16_t *>(sm + SS_OS);
             if (vact) {
+                // the record's Qg and P carry 1 / rq_r: O[r][v] = rq_r Y^T[v][r]
+                const float *rq = reinterpret_cast<const float *>(sm + SS_RQ) + 32 * vhalf;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) os[(32 * vhalf + j) * VB + vme] = f_to_bf16(__uint_as_float(y0[j]));
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 f = *reinterpret_cast<const float4 *>(rq + j);
+                    os[(32 * vhalf + j) * VB + vme] = f_to_bf16(__uint_as_float(y0[j]) * f.x);
+                    os[(32 * vhalf + j + 1) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 1]) * f.y);
+                    os[(32 * vhalf + j + 2) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 2]) * f.z);
+                    os[(32 * vhalf + j + 3) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 3]) * f.w);
+                }
             }
             named_bar(1, SC_EPI);
             const int len = min(CH, sd.len - cc * CH);
@@ -1086,6 +1103,9 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
             if (!mbar_spin(bar + 8 * BAR_MMA1, c & 1) || !mbar_spin(bar + 8 * BAR_U, c & 1)) fail();
             tc_fence_after();
             const float g = reinterpret_cast<const float *>(sm + SS_GC)[kme];
+            // keep this chunk's rq for its output, emitted during the next chunk (the record area
+            // is reloaded before that)
+            if (tid < CH) reinterpret_cast<float *>(sm + SS_RQ)[tid] = reinterpret_cast<const float *>(sm + SS_GC)[128 + tid];
             {
                 // this thread: v = vme, r = 32 vhalf .. 32 vhalf + 31
                 uint32_t ys[32];
@@ -1093,6 +1113,8 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                 tmem_wait_ld();
                 if (vact) {
                     const float *urow = reinterpret_cast<const float *>(sm + SS_U) + vme * 68 + 32 * vhalf;
+                    // Kd in the record is unnormalised: the state update takes Delta_r rk_r
+                    const float *rkr = reinterpret_cast<const float *>(sm + SS_GC) + 192 + 32 * vhalf;
 #pragma unroll
                     for (int jj = 0; jj < 32; jj += 8) {
                         const int j = 32 * vhalf + jj;
@@ -1102,10 +1124,12 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                         const float d2 = ua.z - __uint_as_float(ys[jj + 2]), d3 = ua.w - __uint_as_float(ys[jj + 3]);
                         const float d4 = ub.x - __uint_as_float(ys[jj + 4]), d5 = ub.y - __uint_as_float(ys[jj + 5]);
                         const float d6 = ub.z - __uint_as_float(ys[jj + 6]), d7 = ub.w - __uint_as_float(ys[jj + 7]);
+                        const float4 ka = *reinterpret_cast<const float4 *>(rkr + jj);
+                        const float4 kb = *reinterpret_cast<const float4 *>(rkr + jj + 4);
                         *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j, VB)) =
-                            make_uint4(tf32_bits(d0), tf32_bits(d1), tf32_bits(d2), tf32_bits(d3));
+                            make_uint4(tf32_bits(d0 * ka.x), tf32_bits(d1 * ka.y), tf32_bits(d2 * ka.z), tf32_bits(d3 * ka.w));
                         *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j + 16, VB)) =
-                            make_uint4(tf32_bits(d4), tf32_bits(d5), tf32_bits(d6), tf32_bits(d7));
+                            make_uint4(tf32_bits(d4 * kb.x), tf32_bits(d5 * kb.y), tf32_bits(d6 * kb.z), tf32_bits(d7 * kb.w));
                         *reinterpret_cast<uint4 *>(sm + SS_DTB + sw128_off(vme, 2 * j, VB)) =
                             make_uint4(pack_bf16x2(d0, d1), pack_bf16x2(d2, d3), pack_bf16x2(d4, d5),
                                        pack_bf16x2(d6, d7));
