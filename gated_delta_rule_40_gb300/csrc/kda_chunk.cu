@@ -373,15 +373,22 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         auto gate_tables = [&](int s) {
             const unsigned char *rawb = sm + IS_R2 + (s & 1) * RAW_SLICE;
             const int seg = lane >> 2, cl = lane & 3, cs = 4 * warp + cl;
+            // running sums of softplus (log2 units); the factor -exp(A_log) is applied once at the end
             float loc[8], run = 0.f;
+            const unsigned char *gp = rawb + 2 * RAW_T + raw_off_g(8 * seg, cs >> 3) + (cs & 7) * 2;   // + 64 i: row 8 seg + i
+            if (len == CH) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = 8 * seg + i;
-                const uint16_t gb =
-                    *reinterpret_cast<const uint16_t *>(rawb + 2 * RAW_T + raw_off_g(r, cs >> 3) + (cs & 7) * 2);
-                const float g2 = r < len ? -a_gate * softplus_log2(bf16_to_f(gb)) : 0.f;
-                run += g2;
-                loc[i] = run;
+                for (int i = 0; i < 8; ++i) {
+                    run += softplus_log2(bf16_to_f(*reinterpret_cast<const uint16_t *>(gp + 64 * i)));
+                    loc[i] = run;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float sp = softplus_log2(bf16_to_f(*reinterpret_cast<const uint16_t *>(gp + 64 * i)));
+                    run += 8 * seg + i < len ? sp : 0.f;
+                    loc[i] = run;
+                }
             }
             float incl = run;
 #pragma unroll
@@ -389,10 +396,10 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                 const float y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            const float off = incl - run;
+            const float na = -a_gate, off = (incl - run) * na;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ga[ga_idx(8 * seg + i, cs)] = loc[i] + off;
-            const float last = loc[7] + off, first = loc[0] + off;
+            for (int i = 0; i < 8; ++i) ga[ga_idx(8 * seg + i, cs)] = fmaf(loc[i], na, off);
+            const float last = fmaf(loc[7], na, off), first = fmaf(loc[0], na, off);
             float m[5], fi[4];
             m[0] = 0.f;
 #pragma unroll
