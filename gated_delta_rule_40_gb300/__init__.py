@@ -9,6 +9,8 @@ from .kda import (  # noqa: F401
     KdaLibraryError,
     kda_decode_step,
     kda_fwd,
+    kda_fwd_host,
+    kda_fwd_noalloc,
     kda_fwd_workspace_size,
     kda_get_status,
     kda_last_launch_count,

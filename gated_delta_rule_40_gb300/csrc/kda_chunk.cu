@@ -216,10 +216,11 @@ struct IntraParams {
     const uint16_t *q, *k, *v, *graw, *b;
     const float *A_log;
     float scale;
-    int H_qk, H_v;
+    int H_qk, H_v;        // head counts of the tensors (their strides)
+    int h0, Hw;           // value-head window [h0, h0 + Hw) this launch processes
     const ChunkDesc *chunks;
     const int *hdr;
-    unsigned char *rec;   // [chunk][H_v] records of REC_BYTES
+    unsigned char *rec;   // [chunk][Hw] records of REC_BYTES
 };
 
 // A / P operands are stored as fp32 bit patterns: the tf32 MMA uses their upper 19 bits
@@ -280,7 +281,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     if (p.hdr[1] == 0) return;
-    const long long n_items = (long long)p.hdr[0] * p.H_v;
+    const long long n_items = (long long)p.hdr[0] * p.Hw;
     if ((long long)blockIdx.x >= n_items) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t sbase = smem_u32(sm);
@@ -331,10 +332,10 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     // The description of the next item (chunk, head, A_log) is fetched while the
     // current one is processed, and its first two raw slices are issued as soon as
     // the current item's W / U MMAs have released the raw buffers.
-    // item = chunk * H_v + head advances by gridDim.x: keep (chunk, head) incrementally
-    const int step_c = (int)(gridDim.x / p.H_v), step_h = (int)(gridDim.x % p.H_v);
+    // item = chunk * Hw + (head - h0) advances by gridDim.x: keep (chunk, head) incrementally
+    const int step_c = (int)(gridDim.x / p.Hw), step_h = (int)(gridDim.x % p.Hw);
     long long item = blockIdx.x;
-    int chunk_next = (int)(item / p.H_v), h_next = (int)(item % p.H_v);
+    int chunk_next = (int)(item / p.Hw), h_next = p.h0 + (int)(item % p.Hw);
     ChunkDesc cd_next = p.chunks[chunk_next];
     float alog_next = p.A_log[h_next];
     issue_raw(cd_next, h_next, 0);
@@ -343,7 +344,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         const int chunk = chunk_next, h = h_next;
         const ChunkDesc cd = cd_next;
         const float a_gate = ex2(alog_next * LOG2E);
-        const size_t ch = (size_t)chunk * p.H_v + h;
+        const size_t ch = (size_t)chunk * p.Hw + (h - p.h0);
         unsigned char *rec = p.rec + ch * REC_BYTES;
         const int len = cd.len;
         const uint16_t *vrow = p.v + ((size_t)cd.tok * p.H_v + h) * KD;    // row r at + r * H_v * KD
@@ -352,8 +353,8 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         if (has_next) {
             chunk_next += step_c;
             h_next += step_h;
-            if (h_next >= p.H_v) {
-                h_next -= p.H_v;
+            if (h_next >= p.h0 + p.Hw) {
+                h_next -= p.Hw;
                 ++chunk_next;
             }
             cd_next = p.chunks[chunk_next];
@@ -921,6 +922,7 @@ struct ScanParams {
     float *fin;
     uint16_t *out;
     int H_v, nseq;
+    int h0, Hw;   // value-head window [h0, h0 + Hw); records are [chunk][Hw]
 };
 
 enum { BAR_WQ0 = 0, BAR_WQ1, BAR_PK0, BAR_PK1, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MMA2, BAR_SBR, BAR_DTR };
@@ -930,8 +932,8 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     if (p.hdr[1] == 0) return;
     const int vb = blockIdx.x & 1;
-    const int h = (blockIdx.x >> 1) % p.H_v;
-    const int rank = (blockIdx.x >> 1) / p.H_v;
+    const int h = p.h0 + (blockIdx.x >> 1) % p.Hw;
+    const int rank = (blockIdx.x >> 1) / p.Hw;
     if (rank >= p.nseq) return;
     const int seq = p.order[rank];
     const SeqDesc sd = p.seqs[seq];
@@ -959,7 +961,7 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + SS_SLOT);
     const uint32_t tZ = tmem + 256;   // 64 columns, lanes = k
 
-    auto rec_of = [&](int c) { return p.rec + (((size_t)sd.chunk0 + c) * p.H_v + h) * REC_BYTES; };
+    auto rec_of = [&](int c) { return p.rec + (((size_t)sd.chunk0 + c) * p.Hw + (h - p.h0)) * REC_BYTES; };
     auto fail = [&]() {
         set_status(KDA_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
@@ -1212,14 +1214,17 @@ size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspa
     return off;
 }
 
-cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
-                       const uint16_t *b, const float *A_log, float scale, const float *init, float *fin,
-                       const int32_t *cu, int N, int B, int T, int H_qk, int H_v, uint16_t *out, void *ws_ptr,
-                       cudaStream_t stream, int *launches) {
+// Forward for the value heads [h0, h0 + Hw) of the tensors (strides from H_qk, H_v); the
+// workspace holds records for Hw heads.  With plan == false the chunk tables already in the
+// workspace (from an earlier call on the same sequences) are reused.
+cudaError_t launch_fwd_heads(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                             const uint16_t *b, const float *A_log, float scale, const float *init, float *fin,
+                             const int32_t *cu, int N, int B, int T, int H_qk, int H_v, int h0, int Hw, bool plan,
+                             uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches) {
     const bool varlen = cu != nullptr;
     const int nseq = varlen ? N : B;
     FwdWorkspace ws;
-    fwd_workspace_bytes(N, B, T, H_v, varlen, &ws, (char *)ws_ptr);
+    fwd_workspace_bytes(N, B, T, Hw, varlen, &ws, (char *)ws_ptr);
     const long long nck = max_chunks_for(N, B, T, varlen);
     *launches = 0;
     {
@@ -1229,21 +1234,24 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS_BYTES);
         if (e != cudaSuccess) return e;
     }
+    cudaError_t e = cudaSuccess;
     timing_begin(stream);
-    plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu, N, B, T, ws.seqs, ws.chunks, ws.order, ws.hdr, nck);
-    ++*launches;
-    timing_mark("plan_kernel", stream);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (plan) {
+        plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu, N, B, T, ws.seqs, ws.chunks, ws.order, ws.hdr, nck);
+        ++*launches;
+        timing_mark("plan_kernel", stream);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (nck > 0) {
         IntraParams ip;
         ip.q = q; ip.k = k; ip.v = v; ip.graw = graw; ip.b = b; ip.A_log = A_log; ip.scale = scale;
-        ip.H_qk = H_qk; ip.H_v = H_v; ip.chunks = ws.chunks; ip.hdr = ws.hdr;
+        ip.H_qk = H_qk; ip.H_v = H_v; ip.h0 = h0; ip.Hw = Hw; ip.chunks = ws.chunks; ip.hdr = ws.hdr;
         ip.rec = ws.rec;
         int dev = 0, nsm = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-        const long long items = nck * (long long)H_v;
+        const long long items = nck * (long long)Hw;
         const long long slots = (long long)nsm * IN_CTAS_PER_SM;   // persistent: two CTAs per SM
         const unsigned grid = (unsigned)(items < slots ? items : slots);
         intra_kernel<<<grid, IN_THREADS, IS_BYTES, stream>>>(ip);
@@ -1256,8 +1264,8 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         ScanParams sp;
         sp.rec = ws.rec;
         sp.seqs = ws.seqs; sp.order = ws.order; sp.hdr = ws.hdr;
-        sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq;
-        const long long nblk = (long long)nseq * H_v * 2;
+        sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = h0; sp.Hw = Hw;
+        const long long nblk = (long long)nseq * Hw * 2;
         scan_kernel<<<(unsigned)nblk, SC_THREADS, SS_BYTES, stream>>>(sp);
         ++*launches;
         timing_mark("scan_kernel", stream);
@@ -1265,6 +1273,14 @@ cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                       const uint16_t *b, const float *A_log, float scale, const float *init, float *fin,
+                       const int32_t *cu, int N, int B, int T, int H_qk, int H_v, uint16_t *out, void *ws_ptr,
+                       cudaStream_t stream, int *launches) {
+    return launch_fwd_heads(q, k, v, graw, b, A_log, scale, init, fin, cu, N, B, T, H_qk, H_v, 0, H_v, true, out,
+                            ws_ptr, stream, launches);
 }
 
 }  // namespace kda

@@ -57,6 +57,8 @@ def load() -> ctypes.CDLL:
     lib.kda_fwd_ws.restype = I
     lib.kda_fwd_noalloc.argtypes = fwd_args + [P]
     lib.kda_fwd_noalloc.restype = I
+    lib.kda_fwd_host.argtypes = fwd_args + [P]
+    lib.kda_fwd_host.restype = I
     lib.kda_fwd_workspace_size.argtypes = [I] * 7
     lib.kda_fwd_workspace_size.restype = Z
     lib.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, P, P]
@@ -95,15 +97,15 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check(t: Optional[torch.Tensor], name: str, dtype, shape=None, optional=False):
+def _check(t: Optional[torch.Tensor], name: str, dtype, shape=None, optional=False, device: str = "cuda"):
     if t is None:
         if optional:
             return
         raise ValueError(f"{name} is required")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
-    if t.device.type != "cuda":
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.type != device:
+        raise ValueError(f"{name} must be a {'CUDA' if device == 'cuda' else 'host'} tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -153,6 +155,45 @@ def kda_fwd(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_seqlen
         _check(workspace, "workspace", torch.uint8)
         rc = lib.kda_fwd_ws(*args, _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
         _raise(rc, "kda_fwd_ws")
+    return out, final_state
+
+
+def kda_fwd_host(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_seqlens=None,
+                 output_final_state: bool = True, out=None, final_state=None, stream=None,
+                 synchronize: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """``kda_fwd`` on host (CPU) tensors: the library copies the inputs to the
+    GPU, runs the forward and copies ``out`` / ``final_state`` back, overlapping
+    the copies of one head group with the kernels of another.  Pinned inputs
+    (``tensor.pin_memory()``) run at the host link's bandwidth; outputs are
+    allocated pinned when not given.  With ``synchronize`` the call waits for
+    ``stream``, so the returned host tensors hold the results; without it they
+    are valid once the stream has passed the call."""
+    lib = load()
+    B, T, H_qk, K = q.shape
+    H_v, V = v.shape[2], v.shape[3]
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    bf, cpu = torch.bfloat16, "cpu"
+    _check(q, "q", bf, (B, T, H_qk, K), device=cpu)
+    _check(k, "k", bf, (B, T, H_qk, K), device=cpu)
+    _check(v, "v", bf, (B, T, H_v, V), device=cpu)
+    _check(graw, "graw", bf, (B, T, H_v, K), device=cpu)
+    _check(b, "b", bf, (B, T, H_v), device=cpu)
+    _check(A_log, "A_log", torch.float32, (H_v,), device=cpu)
+    _check(initial_state, "initial_state", torch.float32, (N, H_v, V, K), optional=True, device=cpu)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, optional=True, device=cpu)
+    if out is None:
+        out = torch.empty((B, T, H_v, V), dtype=bf).pin_memory()
+    _check(out, "out", bf, (B, T, H_v, V), device=cpu)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H_v, V, K), dtype=torch.float32).pin_memory()
+    _check(final_state, "final_state", torch.float32, (N, H_v, V, K), optional=True, device=cpu)
+    s = _stream(stream)
+    rc = lib.kda_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
+                          _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V,
+                          _ptr(out), s)
+    _raise(rc, "kda_fwd_host")
+    if synchronize:
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
     return out, final_state
 
 

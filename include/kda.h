@@ -104,6 +104,26 @@ int kda_fwd_ws(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
                void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * kda_fwd on host buffers: the same problem and the same results, with every
+ * tensor (cu_seqlens included) in host memory.  Pinned (page-locked) buffers let
+ * the copies run at the host link's bandwidth; pageable ones work, more slowly.
+ * The call copies the inputs to the device, runs the forward and copies out and
+ * final_state back, splitting the value heads into up to four groups so that
+ * one group's copies overlap another group's kernels (the link, not the
+ * kernels, bounds such a call).  Device buffers come from cudaMallocAsync /
+ * cudaFreeAsync on `stream`; two copy streams per device are created on the
+ * first call and kept.  Asynchronous like kda_fwd: the results are in host
+ * memory once `stream` has passed the call (e.g. after cudaStreamSynchronize),
+ * and the host buffers must stay valid and unchanged until then.  Same return
+ * codes as kda_fwd.
+ */
+int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
+                 const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log, float scale,
+                 const float *initial_state, float *final_state, const int32_t *cu_seqlens,
+                 int N, int B, int T, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
+                 cudaStream_t stream);
+
+/*
  * One decode step for B independent sequences (one token each):
  *
  *   q, k  [B, H_qk, K] bf16     v, graw [B, H_v, V|K] bf16     b [B, H_v] bf16
