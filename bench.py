@@ -305,7 +305,7 @@ def run_gpu(args, rank, world, local):
 
     def e2e_step():
         # one C-ABI call on host buffers: H2D of the inputs, the forward and D2H of out and the
-        # final state, overlapped by head group inside the library
+        # final state, overlapped piece by piece inside the library
         kda.kda_fwd_host(pin["q"], pin["k"], pin["v"], pin["graw"], pin["b"], pin["A_log"], inp.scale,
                          initial_state=pin["initial_state"], out=host_out, final_state=host_fin, stream=stream,
                          synchronize=False)

@@ -1,11 +1,18 @@
 // kda_fwd_host: the chunked forward on host buffers.  The inputs are copied to
-// the device and the results back inside the call, split into groups of value
-// heads so that the copies of one group overlap the kernels of another: the
-// host link is the bottleneck of such a call (its bytes take several times the
-// kernels' time), so the kernels and the return copies hide behind the input
-// copies.
+// the device and the results back inside the call, in pieces of consecutive
+// tokens so that the copies of one piece overlap the kernels of the previous
+// one: the host link is the bottleneck of such a call (its bytes take several
+// times the kernels' time), so the kernels hide behind the input copies and
+// only the last piece's kernels and output copy remain exposed.
+//
+// A piece is a token range of the packed [sequence][token] layout (dense input
+// is B sequences of length T); a sequence that crosses a piece boundary is cut
+// at a multiple of the chunk length from its start and its state is carried on
+// the device from one piece to the next, which is exactly the chunking and the
+// arithmetic of a single call.
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "kda_common.cuh"
 
@@ -21,7 +28,7 @@ cudaError_t launch_fwd_heads(const uint16_t *q, const uint16_t *k, const uint16_
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxGroups = 4;
+constexpr int kPieces = 4;
 std::mutex g_stream_mutex;
 cudaStream_t g_h2d[kMaxDevices] = {nullptr}, g_d2h[kMaxDevices] = {nullptr};
 
@@ -41,21 +48,13 @@ int copy_streams(cudaStream_t *h2d, cudaStream_t *d2h) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Rows of `width` bytes at `pitch` (the same on both sides): one head group of a
-// [rows][heads][...] tensor.
-cudaError_t copy_rows(void *dst, const void *src, size_t width, size_t pitch, size_t rows, cudaMemcpyKind kind,
-                      cudaStream_t s) {
-    if (rows == 0 || width == 0) return cudaSuccess;
-    if (width == pitch) return cudaMemcpyAsync(dst, src, width * rows, kind, s);
-    return cudaMemcpy2DAsync(dst, pitch, src, pitch, width, rows, kind, s);
-}
-
 }  // namespace
 
 extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
                             const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
                             float *final_state, const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v,
                             int K, int V, kda_bf16_t *out, cudaStream_t stream) {
+    using kda::CH;
     using kda::KD;
     if (K != KD || V != KD) return KDA_ERR_UNSUPPORTED;
     if (B < 0 || T < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0) return KDA_ERR_INVALID_ARG;
@@ -63,20 +62,58 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
     const long long tokens = (long long)B * T;
     if (tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (tokens > 0 && (!q || !k || !v || !graw || !b || !A_log || !out)) return KDA_ERR_INVALID_ARG;
-    const bool varlen = cu_seqlens != nullptr;
-    const int nseq = varlen ? N : B;
+    const int nseq = cu_seqlens ? N : B;
 
-    // head groups: a divisor of H_qk (so every group holds whole q/k head groups)
-    int P = 1;
-    for (int c = kMaxGroups; c > 1; --c)
-        if (tokens > 0 && H_qk % c == 0) {
-            P = c;
-            break;
+    // packed sequence boundaries (host copy; checked here, so a malformed array is an error return)
+    std::vector<int32_t> cu((size_t)nseq + 1);
+    for (int i = 0; i <= nseq; ++i) cu[i] = cu_seqlens ? cu_seqlens[i] : (int32_t)((long long)i * T);
+    if (cu[0] != 0 || cu[nseq] != tokens) return KDA_ERR_BAD_SEQLENS;
+    for (int i = 0; i < nseq; ++i)
+        if (cu[i + 1] < cu[i]) return KDA_ERR_BAD_SEQLENS;
+
+    // pieces [t0, t1): about tokens / P each, cut at a chunk boundary of the sequence they fall in
+    const int P = tokens >= (long long)kPieces * 4096 ? kPieces : 1;
+    std::vector<int> cuts = {0};
+    for (int p = 1; p < P; ++p) {
+        const long long target = tokens * p / P;
+        int s = 0;
+        while (s < nseq && cu[s + 1] <= target) ++s;
+        long long t = s < nseq ? cu[s] + ((target - cu[s] + CH / 2) / CH) * CH : tokens;
+        if (s < nseq && t > cu[s + 1]) t = cu[s + 1];
+        if (t > cuts.back() && t < tokens) cuts.push_back((int)t);
+    }
+    cuts.push_back((int)tokens);
+    const int np = (int)cuts.size() - 1;
+    struct Piece {
+        int t0, t1, n0, n1;
+        size_t cu_off;   // offset of its local boundaries in the device cu array (ints)
+    };
+    std::vector<Piece> pieces(np);
+    std::vector<int32_t> cu_all;
+    size_t ws_bytes = 0;
+    for (int p = 0; p < np; ++p) {
+        Piece &pc = pieces[p];
+        pc.t0 = cuts[p];
+        pc.t1 = cuts[p + 1];
+        pc.n0 = 0;
+        if (p > 0)
+            while (pc.n0 < nseq && cu[pc.n0 + 1] <= pc.t0) ++pc.n0;
+        pc.n1 = nseq;
+        if (p + 1 < np) {
+            pc.n1 = pc.n0;
+            while (pc.n1 < nseq && cu[pc.n1] < pc.t1) ++pc.n1;
         }
-    const int hq_p = H_qk / P, hv_p = H_v / P;
+        pc.cu_off = cu_all.size();
+        for (int i = pc.n0; i <= pc.n1; ++i) {
+            const int32_t c = cu[i] < pc.t0 ? pc.t0 : (cu[i] > pc.t1 ? pc.t1 : cu[i]);
+            cu_all.push_back(c - pc.t0);
+        }
+        const size_t w = kda::fwd_workspace_bytes(pc.n1 - pc.n0, 1, pc.t1 - pc.t0, H_v, true, nullptr, nullptr);
+        if (w > ws_bytes) ws_bytes = w;
+    }
 
-    const size_t qk_row = (size_t)H_qk * KD * 2, v_row = (size_t)H_v * KD * 2;   // bytes per token
-    const size_t st_row = (size_t)H_v * KD * KD * 4;                              // bytes per sequence
+    const size_t qk_row = (size_t)H_qk * KD * 2, v_row = (size_t)H_v * KD * 2, b_row = (size_t)H_v * 2;
+    const size_t st_row = (size_t)H_v * KD * KD * 4;   // bytes of one sequence's state
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -85,90 +122,79 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
     };
     const size_t o_q = take(tokens * qk_row), o_k = take(tokens * qk_row);
     const size_t o_v = take(tokens * v_row), o_g = take(tokens * v_row), o_out = take(tokens * v_row);
-    const size_t o_b = take((size_t)tokens * H_v * 2), o_a = take((size_t)H_v * 4);
-    const size_t o_init = take(initial_state ? nseq * st_row : 0), o_fin = take(final_state ? nseq * st_row : 0);
-    const size_t o_cu = take(varlen ? (size_t)(N + 1) * 4 : 0);
-    const size_t o_ws = take(kda::fwd_workspace_bytes(varlen ? N : 0, B, T, hv_p, varlen, nullptr, nullptr));
+    const size_t o_b = take(tokens * b_row), o_a = take((size_t)H_v * 4);
+    const size_t o_st = take((size_t)nseq * st_row), o_cu = take(cu_all.size() * 4), o_ws = take(ws_bytes);
 
     cudaStream_t h2d = nullptr, d2h = nullptr;
     int rc = copy_streams(&h2d, &d2h);
     if (rc != KDA_OK) return rc;
     char *base = nullptr;
     if (cudaMallocAsync((void **)&base, off, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    cudaEvent_t ev_start, ev_end, ev_in[kMaxGroups], ev_out[kMaxGroups];
+    std::vector<cudaEvent_t> ev_in(np), ev_out(np);
+    cudaEvent_t ev_start, ev_end;
     cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
     cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming);
-    for (int p = 0; p < P; ++p) {
+    for (int p = 0; p < np; ++p) {
         cudaEventCreateWithFlags(&ev_in[p], cudaEventDisableTiming);
         cudaEventCreateWithFlags(&ev_out[p], cudaEventDisableTiming);
     }
-    auto dptr = [&](size_t o) { return (void *)(base + o); };
+    auto dp = [&](size_t o) { return base + o; };
     cudaError_t e = cudaSuccess;
     auto ok = [&](cudaError_t x) {
         if (x != cudaSuccess && e == cudaSuccess) e = x;
-        return e == cudaSuccess;
     };
-    int launches = 0;
+    const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
 
-    // inputs: the whole-tensor parts, then each head group
+    // inputs: the per-call parts (boundaries, A_log, the initial states, which the pieces then
+    // update in place), then each piece's token rows
     ok(cudaEventRecord(ev_start, stream));
     ok(cudaStreamWaitEvent(h2d, ev_start, 0));
-    if (tokens > 0) {
-        ok(cudaMemcpyAsync(dptr(o_b), b, (size_t)tokens * H_v * 2, cudaMemcpyHostToDevice, h2d));
-        ok(cudaMemcpyAsync(dptr(o_a), A_log, (size_t)H_v * 4, cudaMemcpyHostToDevice, h2d));
-    }
-    if (varlen) ok(cudaMemcpyAsync(dptr(o_cu), cu_seqlens, (size_t)(N + 1) * 4, cudaMemcpyHostToDevice, h2d));
-    for (int p = 0; p < P && e == cudaSuccess; ++p) {
-        const size_t qo = (size_t)p * hq_p * KD * 2, vo = (size_t)p * hv_p * KD * 2;
-        const size_t qw = (size_t)hq_p * KD * 2, vw = (size_t)hv_p * KD * 2;
-        ok(copy_rows((char *)dptr(o_q) + qo, (const char *)q + qo, qw, qk_row, tokens, cudaMemcpyHostToDevice, h2d));
-        ok(copy_rows((char *)dptr(o_k) + qo, (const char *)k + qo, qw, qk_row, tokens, cudaMemcpyHostToDevice, h2d));
-        ok(copy_rows((char *)dptr(o_v) + vo, (const char *)v + vo, vw, v_row, tokens, cudaMemcpyHostToDevice, h2d));
-        ok(copy_rows((char *)dptr(o_g) + vo, (const char *)graw + vo, vw, v_row, tokens, cudaMemcpyHostToDevice,
-                     h2d));
-        if (initial_state) {
-            const size_t so = (size_t)p * hv_p * KD * KD * 4, sw = (size_t)hv_p * KD * KD * 4;
-            ok(copy_rows((char *)dptr(o_init) + so, (const char *)initial_state + so, sw, st_row, nseq,
-                         cudaMemcpyHostToDevice, h2d));
+    ok(cudaMemcpyAsync(dp(o_cu), cu_all.data(), cu_all.size() * 4, H2D, h2d));
+    if (tokens > 0) ok(cudaMemcpyAsync(dp(o_a), A_log, (size_t)H_v * 4, H2D, h2d));
+    if (initial_state) ok(cudaMemcpyAsync(dp(o_st), initial_state, (size_t)nseq * st_row, H2D, h2d));
+    else ok(cudaMemsetAsync(dp(o_st), 0, (size_t)nseq * st_row, h2d));
+    for (int p = 0; p < np && e == cudaSuccess; ++p) {
+        const size_t t0 = pieces[p].t0, nt = (size_t)(pieces[p].t1 - pieces[p].t0);
+        if (nt > 0) {
+            ok(cudaMemcpyAsync(dp(o_q) + t0 * qk_row, (const char *)q + t0 * qk_row, nt * qk_row, H2D, h2d));
+            ok(cudaMemcpyAsync(dp(o_k) + t0 * qk_row, (const char *)k + t0 * qk_row, nt * qk_row, H2D, h2d));
+            ok(cudaMemcpyAsync(dp(o_v) + t0 * v_row, (const char *)v + t0 * v_row, nt * v_row, H2D, h2d));
+            ok(cudaMemcpyAsync(dp(o_g) + t0 * v_row, (const char *)graw + t0 * v_row, nt * v_row, H2D, h2d));
+            ok(cudaMemcpyAsync(dp(o_b) + t0 * b_row, (const char *)b + t0 * b_row, nt * b_row, H2D, h2d));
         }
         ok(cudaEventRecord(ev_in[p], h2d));
     }
-    // kernels, group by group on the caller's stream (the chunk tables are built once)
-    for (int p = 0; p < P && e == cudaSuccess; ++p) {
+    // kernels, piece by piece on the caller's stream; each piece's sequences start from, and
+    // write back, their rows of the device state array
+    for (int p = 0; p < np && e == cudaSuccess; ++p) {
+        const Piece &pc = pieces[p];
+        const size_t t0 = pc.t0;
         ok(cudaStreamWaitEvent(stream, ev_in[p], 0));
+        float *st = (float *)(dp(o_st) + (size_t)pc.n0 * st_row);
         int n = 0;
-        ok(kda::launch_fwd_heads((const uint16_t *)dptr(o_q), (const uint16_t *)dptr(o_k),
-                                 (const uint16_t *)dptr(o_v), (const uint16_t *)dptr(o_g),
-                                 (const uint16_t *)dptr(o_b), (const float *)dptr(o_a), scale,
-                                 initial_state ? (const float *)dptr(o_init) : nullptr,
-                                 final_state ? (float *)dptr(o_fin) : nullptr,
-                                 varlen ? (const int32_t *)dptr(o_cu) : nullptr, varlen ? N : 0, B, T, H_qk, H_v,
-                                 p * hv_p, hv_p, p == 0, (uint16_t *)dptr(o_out), dptr(o_ws), stream, &n));
-        launches += n;
+        ok(kda::launch_fwd_heads((const uint16_t *)(dp(o_q) + t0 * qk_row), (const uint16_t *)(dp(o_k) + t0 * qk_row),
+                                 (const uint16_t *)(dp(o_v) + t0 * v_row), (const uint16_t *)(dp(o_g) + t0 * v_row),
+                                 (const uint16_t *)(dp(o_b) + t0 * b_row), (const float *)dp(o_a), scale, st, st,
+                                 (const int32_t *)dp(o_cu) + pc.cu_off, pc.n1 - pc.n0, 1, pc.t1 - pc.t0, H_qk, H_v, 0,
+                                 H_v, true, (uint16_t *)(dp(o_out) + t0 * v_row), dp(o_ws), stream, &n));
         ok(cudaEventRecord(ev_out[p], stream));
     }
-    // results, group by group
-    for (int p = 0; p < P && e == cudaSuccess; ++p) {
+    // results, piece by piece, then the final states
+    for (int p = 0; p < np && e == cudaSuccess; ++p) {
         ok(cudaStreamWaitEvent(d2h, ev_out[p], 0));
-        const size_t vo = (size_t)p * hv_p * KD * 2, vw = (size_t)hv_p * KD * 2;
-        ok(copy_rows((char *)out + vo, (const char *)dptr(o_out) + vo, vw, v_row, tokens, cudaMemcpyDeviceToHost,
-                     d2h));
-        if (final_state) {
-            const size_t so = (size_t)p * hv_p * KD * KD * 4, sw = (size_t)hv_p * KD * KD * 4;
-            ok(copy_rows((char *)final_state + so, (const char *)dptr(o_fin) + so, sw, st_row, nseq,
-                         cudaMemcpyDeviceToHost, d2h));
-        }
+        const size_t t0 = pieces[p].t0, nt = (size_t)(pieces[p].t1 - pieces[p].t0);
+        if (nt > 0) ok(cudaMemcpyAsync((char *)out + t0 * v_row, dp(o_out) + t0 * v_row, nt * v_row, D2H, d2h));
     }
+    if (final_state) ok(cudaMemcpyAsync(final_state, dp(o_st), (size_t)nseq * st_row, D2H, d2h));
     ok(cudaEventRecord(ev_end, d2h));
     ok(cudaStreamWaitEvent(stream, ev_end, 0));
     const cudaError_t ef = cudaFreeAsync(base, stream);
     cudaEventDestroy(ev_start);
     cudaEventDestroy(ev_end);
-    for (int p = 0; p < P; ++p) {
+    for (int p = 0; p < np; ++p) {
         cudaEventDestroy(ev_in[p]);
         cudaEventDestroy(ev_out[p]);
     }
-    (void)launches;
     if (e != cudaSuccess || ef != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }

@@ -163,7 +163,7 @@ def kda_fwd_host(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_s
                  synchronize: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """``kda_fwd`` on host (CPU) tensors: the library copies the inputs to the
     GPU, runs the forward and copies ``out`` / ``final_state`` back, overlapping
-    the copies of one head group with the kernels of another.  Pinned inputs
+    the copies of one token piece with the kernels of the previous one.  Pinned inputs
     (``tensor.pin_memory()``) run at the host link's bandwidth; outputs are
     allocated pinned when not given.  With ``synchronize`` the call waits for
     ``stream``, so the returned host tensors hold the results; without it they

@@ -108,14 +108,17 @@ int kda_fwd_ws(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
  * tensor (cu_seqlens included) in host memory.  Pinned (page-locked) buffers let
  * the copies run at the host link's bandwidth; pageable ones work, more slowly.
  * The call copies the inputs to the device, runs the forward and copies out and
- * final_state back, splitting the value heads into up to four groups so that
- * one group's copies overlap another group's kernels (the link, not the
- * kernels, bounds such a call).  Device buffers come from cudaMallocAsync /
- * cudaFreeAsync on `stream`; two copy streams per device are created on the
- * first call and kept.  Asynchronous like kda_fwd: the results are in host
- * memory once `stream` has passed the call (e.g. after cudaStreamSynchronize),
- * and the host buffers must stay valid and unchanged until then.  Same return
- * codes as kda_fwd.
+ * final_state back, in up to four pieces of consecutive tokens so that one
+ * piece's copies overlap the previous piece's kernels (the link, not the
+ * kernels, bounds such a call).  A sequence crossing a piece boundary is cut at
+ * a chunk boundary and its state carried on the device, which is the chunking
+ * and arithmetic of a single call.  cu_seqlens is checked on the host: a
+ * malformed array returns KDA_ERR_BAD_SEQLENS before anything is queued.
+ * Device buffers come from cudaMallocAsync / cudaFreeAsync on `stream`; two
+ * copy streams per device are created on the first call and kept.
+ * Asynchronous like kda_fwd: the results are in host memory once `stream` has
+ * passed the call (e.g. after cudaStreamSynchronize), and the host buffers must
+ * stay valid and unchanged until then.
  */
 int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
                  const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log, float scale,

@@ -1,8 +1,10 @@
 """GPU tests of kda_fwd_host (the forward on host buffers, through the C ABI).
 
-The host entry point runs the same kernels as kda_fwd, one group of value heads
-at a time, so its results must equal kda_fwd's bit for bit; the first cases also
-check it against the fp64 oracle at the method's tolerances."""
+The host entry point runs the same kernels as kda_fwd on consecutive token
+pieces, cutting sequences at chunk boundaries and carrying their states on the
+device, which is the same chunking and arithmetic as one call: its results must
+equal kda_fwd's bit for bit.  The first cases also check it against the fp64
+oracle at the method's tolerances."""
 import pytest
 import torch
 
@@ -73,9 +75,27 @@ def test_host_zero_tokens_copies_state():
 
 
 def test_host_full_size_dense_equals_device():
-    """The benchmark's dense workload (B=2, T=16384, H=32) in four head groups."""
+    """The benchmark's dense workload (B=2, T=16384, H=32), copied and computed in four token pieces."""
     inp = KI.workload("dense")
     ho, hf = _host_fwd(inp)
     do, df = gpu_fwd(inp)
     _same(ho, do)
     _same(hf, df)
+
+
+def test_host_varlen_workload_equals_device():
+    """The skewed 20-sequence workload (T=16384): pieces cut sequences at chunk boundaries."""
+    inp = KI.workload("varlen")
+    ho, hf = _host_fwd(inp)
+    do, df = gpu_fwd(inp)
+    _same(ho, do)
+    _same(hf, df)
+
+
+def test_host_rejects_malformed_cu_seqlens():
+    from gated_delta_rule_40_gb300 import kda
+    inp = KI.make_inputs(1, 100, 1, 1, seed=314, with_state=False, seqlens=[60, 40])
+    bad = torch.tensor([0, 70, 60], dtype=torch.int32)
+    with pytest.raises(kda.KdaError) as ei:
+        kda.kda_fwd_host(inp.q, inp.k, inp.v, inp.graw, inp.b, inp.A_log, inp.scale, cu_seqlens=bad)
+    assert ei.value.code == kda.KDA_ERR_BAD_SEQLENS
