@@ -11,6 +11,7 @@ from .kda import (  # noqa: F401
     kda_fwd,
     kda_fwd_host,
     kda_fwd_noalloc,
+    kda_fwd_scalar_gate,
     kda_fwd_workspace_size,
     kda_get_status,
     kda_last_launch_count,

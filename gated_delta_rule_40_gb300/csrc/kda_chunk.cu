@@ -1173,6 +1173,461 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// T = (I + A)^{-1} for a strictly lower-triangular 64 x 64 A (fp32, row stride AS): the
+// diagonal 16 x 16 blocks by right-looking forward substitution, T10 and T32 as
+// -T_ii A_ij T_jj, then the lower-left 32 x 32 block as -T2 (A21 T1), the block products
+// on mma.sync with the three-term split.  Reads only the strict lower part of A; all
+// threads of the CTA call it (it synchronises them).
+__device__ __forceinline__ void invert_unit_lower64(const float *sA, float *sT, float *sX, int tid, int warp,
+                                                    int lane) {
+    if (tid < 64) {
+        const int bi = tid >> 4, c = tid & 15, o = 16 * bi;
+        float t[SUB];
+#pragma unroll
+        for (int r = 0; r < SUB; ++r) t[r] = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int j = 0; j < SUB; ++j)
+#pragma unroll
+            for (int r = j + 1; r < SUB; ++r) t[r] = fmaf(-sA[(o + r) * AS + o + j], t[j], t[r]);
+#pragma unroll
+        for (int r = 0; r < SUB; ++r) sT[(o + r) * AS + o + c] = t[r];
+    } else {
+        for (int idx = tid - 64; idx < 6 * 256; idx += IN_THREADS - 64) {
+            const int blk = idx >> 8, e = idx & 255;
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            sT[(16 * bi + (e >> 4)) * AS + 16 * bj + (e & 15)] = 0.f;
+        }
+    }
+    __syncthreads();
+    const int gid = lane >> 2, tig = lane & 3;
+    {
+        const int b = warp >> 1, n0 = 8 * (warp & 1), bi = 2 * b + 1, bj = 2 * b;
+        float *z = sX + b * 16 * ZS;
+        if (warp < 4) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            split_mma<2>(sA + (16 * bi) * AS + 16 * bj, AS, sT + (16 * bj) * AS + 16 * bj + n0, AS, gid, tig, d);
+            z[gid * ZS + n0 + 2 * tig] = d[0];
+            z[gid * ZS + n0 + 2 * tig + 1] = d[1];
+            z[(gid + 8) * ZS + n0 + 2 * tig] = d[2];
+            z[(gid + 8) * ZS + n0 + 2 * tig + 1] = d[3];
+        }
+        __syncthreads();
+        if (warp < 4) {
+            float t[4] = {0.f, 0.f, 0.f, 0.f};
+            split_mma<2>(sT + (16 * bi) * AS + 16 * bi, AS, z + n0, ZS, gid, tig, t);
+            float *dst = sT + (16 * bi) * AS + 16 * bj + n0;
+            dst[gid * AS + 2 * tig] = -t[0];
+            dst[gid * AS + 2 * tig + 1] = -t[1];
+            dst[(gid + 8) * AS + 2 * tig] = -t[2];
+            dst[(gid + 8) * AS + 2 * tig + 1] = -t[3];
+        }
+    }
+    __syncthreads();
+    {
+        const int m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        split_mma<4>(sA + (32 + m0) * AS, AS, sT + n0, AS, gid, tig, d);
+        sX[(m0 + gid) * XS + n0 + 2 * tig] = d[0];
+        sX[(m0 + gid) * XS + n0 + 2 * tig + 1] = d[1];
+        sX[(m0 + gid + 8) * XS + n0 + 2 * tig] = d[2];
+        sX[(m0 + gid + 8) * XS + n0 + 2 * tig + 1] = d[3];
+        __syncthreads();
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        split_mma<4>(sT + (32 + m0) * AS + 32, AS, sX + n0, XS, gid, tig, t);
+        sT[(32 + m0 + gid) * AS + n0 + 2 * tig] = -t[0];
+        sT[(32 + m0 + gid) * AS + n0 + 2 * tig + 1] = -t[1];
+        sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig] = -t[2];
+        sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig + 1] = -t[3];
+    }
+    __syncthreads();
+}
+
+// W (M = 64 accumulator at t_w, 128 columns) to the W rows of the WQ image (bf16, two 8 KiB
+// atoms at ws) and U^T (M = 128 accumulator at t_u, 64 columns, lane v) to the U image
+// [v / 64][v % 64][68] fp32 at us.  Warps 0..3 take U, 4..7 take W.
+__device__ __forceinline__ void store_wu(unsigned char *ws, unsigned char *us, uint32_t t_w, uint32_t t_u, int warp,
+                                         int lane) {
+    const int q = warp & 3;
+    const uint32_t lo = (uint32_t)(q * 32) << 16;
+    if (warp < 4) {
+        const int v = q * 32 + lane;
+        uint32_t x0[32], x1[32];
+        tmem_ld32_nowait(t_u + lo, x0);
+        tmem_ld32_nowait(t_u + lo + 32, x1);
+        tmem_wait_ld();
+        float *u = reinterpret_cast<float *>(us) + (v >> 6) * (CH * 68) + (v & 63) * 68;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            *reinterpret_cast<float4 *>(u + j) = make_float4(__uint_as_float(x0[j]), __uint_as_float(x0[j + 1]),
+                                                             __uint_as_float(x0[j + 2]), __uint_as_float(x0[j + 3]));
+            *reinterpret_cast<float4 *>(u + 32 + j) = make_float4(__uint_as_float(x1[j]), __uint_as_float(x1[j + 1]),
+                                                                  __uint_as_float(x1[j + 2]), __uint_as_float(x1[j + 3]));
+        }
+    } else {
+        const int r = q * 16 + lane;
+#pragma unroll
+        for (int rd = 0; rd < 2; ++rd) {
+            uint32_t x0[32], x1[32];
+            tmem_ld32_nowait(t_w + lo + 64 * rd, x0);
+            tmem_ld32_nowait(t_w + lo + 64 * rd + 32, x1);
+            tmem_wait_ld();
+            if (lane < 16) {
+#pragma unroll
+                for (int j = 0; j < 64; j += 8) {
+                    const uint32_t *xs = j < 32 ? x0 : x1;
+                    const int jj = j & 31, k = 64 * rd + j;
+                    const uint32_t off = (uint32_t)rd * 8192 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                         ((((2 * k) & 127) >> 4) ^ (r & 7)) * 16;
+                    *reinterpret_cast<uint4 *>(ws + off) = make_uint4(
+                        pack_bf16x2(__uint_as_float(xs[jj]), __uint_as_float(xs[jj + 1])),
+                        pack_bf16x2(__uint_as_float(xs[jj + 2]), __uint_as_float(xs[jj + 3])),
+                        pack_bf16x2(__uint_as_float(xs[jj + 4]), __uint_as_float(xs[jj + 5])),
+                        pack_bf16x2(__uint_as_float(xs[jj + 6]), __uint_as_float(xs[jj + 7])));
+                }
+            }
+        }
+    }
+}
+
+// =====================================================================
+// Intra-chunk kernel for a scalar gate (one decay per token and value head,
+// graw [B, T, H_v]): the gated-delta-net special case.  The decay
+// exp(Gam_r - Gam_j) is then the same for every channel, so
+//   A[r,j] = beta_r rk_r rk_j exp(Gam_r - Gam_j) (k_r . k_j),   P[r,j] = rq_r rk_j exp(Gam_r - Gam_j) (q_r . k_j)
+// come from one bf16 MMA of the raw inputs (exact products, fp32 accumulate)
+// followed by a 64 x 64 decay mask, and W = T diag(beta rk exp(Gam)) K takes the
+// staged raw K as its operand.  The record is the general kernel's (raw Qg, Kd
+// and P with the row scales rq, rk), so the same scan follows.
+// Persistent CTAs of 8 warps, two per SM, one (chunk, value head) item at a time.
+// =====================================================================
+constexpr uint32_t GD_QK = 0;               // [K rows 0..63; Q rows 64..127] K-major bf16 (2 x 16 KiB atoms);
+                                            // after the A/P MMA: V (MN-major, 16 KiB) and K (MN-major, 16 KiB)
+constexpr uint32_t GD_V = GD_QK, GD_KMN = GD_QK + 16384;
+constexpr uint32_t GD_AT = 32768;           // A, T fp32 [64][68] and the inversion scratch; then U staging
+constexpr uint32_t GD_A = GD_AT, GD_T = GD_AT + 17408, GD_X = GD_AT + 34816;
+constexpr uint32_t GD_TP = 73728;           // T'_hi, T'_lo, T'_W hi, T'_W lo (4 x 8 KiB); the P image before them;
+                                            // then W staging
+constexpr uint32_t GD_PI = GD_TP, GD_TPH = GD_TP, GD_TPL = GD_TP + 8192, GD_TWH = GD_TP + 16384, GD_TWL = GD_TP + 24576;
+constexpr uint32_t GD_MISC = 106496;
+constexpr uint32_t GD_RV = GD_MISC;         // rq, rk, beta, raw q.k [4][64]
+constexpr uint32_t GD_GAM = GD_MISC + 1024; // Gam [64] (log2 units)
+constexpr uint32_t GD_EG = GD_MISC + 1280;  // exp(Gam) [64]
+constexpr uint32_t GD_GCS = GD_MISC + 1536; // exp(Gam_C) [128] (the record's per-channel layout)
+constexpr uint32_t GD_SCR = GD_MISC + 2048; // gate-scan carry
+constexpr uint32_t GD_BAR = GD_MISC + 2112; // 2 mbarriers
+constexpr uint32_t GD_SLOT = GD_MISC + 2128;
+constexpr uint32_t GD_BYTES = GD_MISC + 2144 + 1024;
+static_assert(GD_X + 32 * XS * 4 <= GD_TP && GD_TWL + 8192 <= GD_MISC, "scalar-gate layout overflow");
+static_assert(IN_CTAS_PER_SM * (GD_BYTES + 1024) <= 228 * 1024, "two CTAs per SM must fit");
+
+struct GdnParams {
+    const uint16_t *q, *k, *v, *graw, *b;   // graw [B, T, H_v]
+    const float *A_log;
+    float scale;
+    int H_qk, H_v;
+    const ChunkDesc *chunks;
+    const int *hdr;
+    unsigned char *rec;                     // [chunk][H_v] records of REC_BYTES
+};
+
+__global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(const GdnParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    if (p.hdr[1] == 0) return;
+    const long long n_items = (long long)p.hdr[0] * p.H_v;
+    if ((long long)blockIdx.x >= n_items) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t bar_ap = sbase + GD_BAR, bar_wu = sbase + GD_BAR + 8;
+    const uint64_t pol_ef = l2_evict_first_policy();
+    float *rv = reinterpret_cast<float *>(sm + GD_RV);
+    float *gam = reinterpret_cast<float *>(sm + GD_GAM);
+    float *eg = reinterpret_cast<float *>(sm + GD_EG);
+    float *gcs = reinterpret_cast<float *>(sm + GD_GCS);
+    float *sA = reinterpret_cast<float *>(sm + GD_A);
+    float *sT = reinterpret_cast<float *>(sm + GD_T);
+    float *sX = reinterpret_cast<float *>(sm + GD_X);
+    if (tid == 0) {
+        mbar_init(bar_ap, 1);
+        mbar_init(bar_wu, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) tmem_alloc(sbase + GD_SLOT, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + GD_SLOT);
+    const uint32_t t_ap = tmem, t_w = tmem, t_u = tmem + 128;
+    const size_t qk_stride = (size_t)p.H_qk * KD, gv_stride = (size_t)p.H_v * KD;
+    const int group = p.H_v / p.H_qk;
+
+    int it = 0;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+        const int chunk = (int)(item / p.H_v), h = (int)(item % p.H_v), hq = h / group;
+        const ChunkDesc cd = p.chunks[chunk];
+        const int len = cd.len;
+        unsigned char *rec = p.rec + ((size_t)chunk * p.H_v + h) * REC_BYTES;
+        const uint16_t *qrow = p.q + ((size_t)cd.tok * p.H_qk + hq) * KD;   // row r at + r * qk_stride
+        const uint16_t *krow = p.k + ((size_t)cd.tok * p.H_qk + hq) * KD;
+        const uint16_t *vrow = p.v + ((size_t)cd.tok * p.H_v + h) * KD;     // row r at + r * gv_stride
+
+        // ---- 1. raw K and Q rows into the [K; Q] operand (16-byte units, zero rows past len); the
+        //         gate scalars and beta
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = tid + IN_THREADS * i, isq = idx >> 10, r = (idx >> 4) & 63, u = idx & 15;
+            unsigned char *dst = sm + GD_QK + sw128_off(64 * isq + r, 16 * u, 2 * CH);
+            if (r < len) cp_async16(dst, (isq ? qrow : krow) + r * qk_stride + 8 * u);
+            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+        }
+        cp_async_commit();
+        float graw_r = 0.f, b_r = 0.f;
+        if (tid < len) {
+            const size_t row = ((size_t)cd.tok + tid) * p.H_v + h;
+            graw_r = bf16_to_f(p.graw[row]);
+            b_r = bf16_to_f(p.b[row]);
+        }
+        // pull the next item's rows into L2
+        {
+            const long long nitem = item + gridDim.x;
+            if (nitem < n_items) {
+                const int nchunk = (int)(nitem / p.H_v), nh = (int)(nitem % p.H_v);
+                const ChunkDesc nd = p.chunks[nchunk];
+                const int r = tid & 63, which = tid >> 6;
+                if (which < 3 && r < nd.len) {
+                    const size_t tok = (size_t)nd.tok + r;
+                    const uint16_t *src = which == 0 ? p.q + (tok * p.H_qk + nh / group) * KD
+                                        : which == 1 ? p.k + (tok * p.H_qk + nh / group) * KD
+                                                     : p.v + (tok * p.H_v + nh) * KD;
+                    prefetch_line_l2(src);
+                    prefetch_line_l2(src + 64);
+                }
+            }
+        }
+        cp_async_wait<0>();
+        // the previous item's bulk stores must be done reading shared memory (staging, P, tables)
+        if (tid == 0) bulk_wait_read_all();
+        __syncthreads();
+
+        // ---- 2. row norms from the staged rows (thread: row, quarter of the channels); gate and
+        //         its prefix sum over the chunk (warps 0, 1: one row per lane)
+        {
+            const int r = tid >> 2, part = tid & 3;
+            float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int ub = 16 * (4 * part + u);
+                const uint4 kw = *reinterpret_cast<const uint4 *>(sm + GD_QK + sw128_off(r, ub, 2 * CH));
+                const uint4 qw = *reinterpret_cast<const uint4 *>(sm + GD_QK + sw128_off(64 + r, ub, 2 * CH));
+                const uint32_t ka[4] = {kw.x, kw.y, kw.z, kw.w}, qa[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float k0 = bf16_lo(ka[e]), k1 = bf16_hi(ka[e]), q0 = bf16_lo(qa[e]), q1 = bf16_hi(qa[e]);
+                    sq = fmaf(q0, q0, fmaf(q1, q1, sq));
+                    sk = fmaf(k0, k0, fmaf(k1, k1, sk));
+                    sqk = fmaf(q0, k0, fmaf(q1, k1, sqk));
+                }
+            }
+#pragma unroll
+            for (int o = 1; o < 4; o <<= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
+            }
+            if (part == 0) {
+                rv[RV_RQ + r] = p.scale * rsqrtf(sq + L2_EPS);
+                rv[RV_RK + r] = rsqrtf(sk + L2_EPS);
+                rv[RV_QK + r] = sqk;
+            }
+        }
+        if (warp < 2) {
+            const float a_gate = ex2(p.A_log[h] * LOG2E);
+            float g2 = tid < len ? -a_gate * softplus_log2(graw_r) : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, g2, o);
+                if (lane >= o) g2 += y;
+            }
+            if (tid == 31) reinterpret_cast<float *>(sm + GD_SCR)[0] = g2;
+            named_bar(1, 64);
+            if (warp == 1) g2 += reinterpret_cast<const float *>(sm + GD_SCR)[0];
+            gam[tid] = g2;
+            eg[tid] = ex2(g2);
+            rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-b_r * LOG2E)) : 0.f;
+            if (tid == CH - 1) reinterpret_cast<float *>(sm + GD_SCR)[1] = ex2(g2);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- 3. D[m][j] = [K; Q][m] . K[j]  (M = 128, N = 64, K = 128, bf16, raw inputs)
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 64);
+#pragma unroll
+            for (int ks = 0; ks < KD / 16; ++ks) {
+                const uint32_t a = sbase + GD_QK + (ks >> 2) * 16384 + (ks & 3) * 32;
+                umma_bf16(t_ap, umma_desc(a, 16, 1024), umma_desc(a, 16, 1024), id, ks > 0 ? 1u : 0u);
+            }
+            umma_commit(bar_ap);
+        }
+        if (tid < KD) gcs[tid] = reinterpret_cast<const float *>(sm + GD_SCR)[1];
+        // ---- 4. meanwhile: Qg = q exp(Gam_r) (bf16) and Kd^T = k exp(Gam_C - Gam_r) (tf32) straight
+        //         into the record (raw rows; the scan applies rq and rk).  Thread: row r, 32 channels.
+        {
+            const int r = tid & 63, g = tid >> 6;
+            const float er = eg[r], ed = ex2(gam[CH - 1] - gam[r]);
+            unsigned char *const kd_r = rec + REC_KDT + (r >> 5) * 16384 + (r & 3) * 4;
+            const int x4 = (r & 31) >> 2;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = 32 * g + 8 * u;   // channels c .. c + 7
+                const uint4 qw = *reinterpret_cast<const uint4 *>(sm + GD_QK + sw128_off(64 + r, 2 * c, 2 * CH));
+                const uint4 kw = *reinterpret_cast<const uint4 *>(sm + GD_QK + sw128_off(r, 2 * c, 2 * CH));
+                const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, ka[4] = {kw.x, kw.y, kw.z, kw.w};
+                uint32_t qg[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    qg[e] = pack_bf16x2(bf16_lo(qa[e]) * er, bf16_hi(qa[e]) * er);
+                    const int k0 = c + 2 * e;
+                    // Kd^T element (k, r) of the record: k / 8 = c / 8, k % 8 = 2 e (+1)
+                    stg_hint_b32(kd_r + (k0 >> 3) * 1024 + (k0 & 7) * 128 + ((x4 ^ (k0 & 7)) << 4),
+                                 tf32_bits(bf16_lo(ka[e]) * ed), pol_ef);
+                    stg_hint_b32(kd_r + (k0 >> 3) * 1024 + ((k0 + 1) & 7) * 128 + ((x4 ^ ((k0 + 1) & 7)) << 4),
+                                 tf32_bits(bf16_hi(ka[e]) * ed), pol_ef);
+                }
+                stg_hint_v4(rec + REC_WQ + sw128_off(r, 2 * c, 2 * CH), make_uint4(qg[0], qg[1], qg[2], qg[3]), pol_ef);
+            }
+        }
+        if (tid == 0 && !mbar_spin(bar_ap, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+        __syncthreads();
+        tc_fence_after();
+        // the [K; Q] operand is free: V and K (MN-major) for the W / U MMAs
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = tid + IN_THREADS * i, isk = idx >> 10, r = (idx >> 4) & 63, c8 = (idx & 15) * 8;
+            unsigned char *dst = sm + (isk ? GD_KMN : GD_V) + mn_off_bf16(c8, r);
+            if (r < len) cp_async16(dst, (isk ? krow + r * qk_stride : vrow + r * gv_stride) + c8);
+            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+        }
+        cp_async_commit();
+
+        // ---- 5. A and P from TMEM with the decay mask.  M = 128 layout: row m in lane m; warp w
+        //         reads lanes 32 (w & 3) .. (rows of K for w & 3 < 2, of Q otherwise), columns 32 (w >> 2) ..
+        {
+            const int q = warp & 3, hf = warp >> 2, isq = q >> 1, r = 32 * (q & 1) + lane;
+            const uint32_t lo = (uint32_t)(q * 32) << 16;
+            uint32_t x[32];
+            tmem_ld32_nowait(t_ap + lo + 32 * hf, x);
+            tmem_wait_ld();
+            const float gr = gam[r];
+            const float rs = isq ? 1.f : rv[RV_BETA + r] * rv[RV_RK + r];   // row scale (P / rq, A)
+            float o[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4) {
+                const int j = 32 * hf + jj;
+                const float4 gj = *reinterpret_cast<const float4 *>(gam + j);
+                const float4 kj = *reinterpret_cast<const float4 *>(rv + RV_RK + j);
+                const float gv[4] = {gj.x, gj.y, gj.z, gj.w}, kv[4] = {kj.x, kj.y, kj.z, kj.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const bool keep = isq ? (j + e <= r) : (j + e < r);
+                    o[jj + e] = keep ? __uint_as_float(x[jj + e]) * ex2(gr - gv[e]) * rs * kv[e] : 0.f;
+                }
+            }
+            if (!isq) {
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 4)
+                    *reinterpret_cast<float4 *>(sA + r * AS + 32 * hf + jj) = make_float4(o[jj], o[jj + 1], o[jj + 2], o[jj + 3]);
+            } else {
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 8)
+                    *reinterpret_cast<uint4 *>(sm + GD_PI + sw128_off(r, 2 * (32 * hf + jj), CH)) =
+                        make_uint4(pack_bf16x2(o[jj], o[jj + 1]), pack_bf16x2(o[jj + 2], o[jj + 3]),
+                                   pack_bf16x2(o[jj + 4], o[jj + 5]), pack_bf16x2(o[jj + 6], o[jj + 7]));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g_hint(rec + REC_P, sbase + GD_PI, 8192, pol_ef);
+            bulk_s2g_hint(rec + REC_GC, sbase + GD_GCS, 512, pol_ef);
+            bulk_s2g_hint(rec + REC_RN, sbase + GD_RV, 512, pol_ef);
+            bulk_commit();
+        }
+
+        // ---- 6. T = (I + A)^{-1}
+        invert_unit_lower64(sA, sT, sX, tid, warp, lane);
+        // the P image store must be done reading before T' overwrites it
+        if (tid == 0) bulk_wait_read_all();
+        __syncthreads();
+        // T' = T diag(beta) (for U) and T'_W = T diag(beta rk exp(Gam)) (for W on the raw K)
+        for (int idx = tid; idx < CH * (CH / 8); idx += IN_THREADS) {
+            const int r = idx >> 3, j = (idx & 7) * 8;
+            float x[8], xw[8];
+            uint32_t hi[4], lo[4], hw[4], lw[4];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                x[e] = sT[r * AS + j + e] * rv[RV_BETA + j + e];
+                xw[e] = x[e] * rv[RV_RK + j + e] * eg[j + e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const uint32_t h2 = pack_bf16x2(x[e], x[e + 1]);
+                hi[e >> 1] = h2;
+                lo[e >> 1] = pack_bf16x2(x[e] - bf16_lo(h2), x[e + 1] - bf16_hi(h2));
+                const uint32_t w2 = pack_bf16x2(xw[e], xw[e + 1]);
+                hw[e >> 1] = w2;
+                lw[e >> 1] = pack_bf16x2(xw[e] - bf16_lo(w2), xw[e + 1] - bf16_hi(w2));
+            }
+            const uint32_t off = sw128_off(r, 2 * j, CH);
+            *reinterpret_cast<uint4 *>(sm + GD_TPH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4 *>(sm + GD_TPL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4 *>(sm + GD_TWH + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(sm + GD_TWL + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        cp_async_wait<0>();   // V and K (this thread's copies)
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- 7. W = T'_W K (M = 64, N = 128, B = K MN-major) and U^T = V T'^T (M = 128 over v, N = 64)
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id_w = idesc_bf16(64, 128) | (1u << 16);
+            const uint32_t id_u = idesc_bf16(128, 64) | (1u << 15);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int ks = 0; ks < CH / 16; ++ks) {
+                    const uint64_t tp = umma_desc(sbase + (part ? GD_TPL : GD_TPH) + ks * 32, 16, 1024);
+                    const uint64_t tw = umma_desc(sbase + (part ? GD_TWL : GD_TWH) + ks * 32, 16, 1024);
+                    const uint32_t acc = (part > 0 || ks > 0) ? 1u : 0u;
+                    umma_bf16(t_w, tw, umma_desc(sbase + GD_KMN + ks * 2048, 8192, 1024), id_w, acc);
+                    umma_bf16(t_u, umma_desc(sbase + GD_V + ks * 2048, 8192, 1024), tp, id_u, acc);
+                }
+            umma_commit(bar_wu);
+            if (!mbar_spin(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+        }
+        __syncthreads();
+        tc_fence_after();
+        store_wu(sm + GD_TP, sm + GD_AT, t_w, t_u, warp, lane);
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g_hint(rec + REC_WQ + 8192, sbase + GD_TP, 8192, pol_ef);
+            bulk_s2g_hint(rec + REC_WQ + 16384 + 8192, sbase + GD_TP + 8192, 8192, pol_ef);
+            bulk_s2g_hint(rec + REC_U, sbase + GD_AT, 2 * CH * 68 * 4, pol_ef);
+            bulk_commit();
+        }
+    }
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
 // =====================================================================
 // Host-side launch of the three kernels.
 // =====================================================================
@@ -1271,6 +1726,53 @@ cudaError_t launch_fwd_heads(const uint16_t *q, const uint16_t *k, const uint16_
         timing_mark("scan_kernel", stream);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// Forward with a scalar gate per token and value head (graw [B, T, H_v]): plan, the
+// scalar-gate intra-chunk kernel, then the common scan.
+cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                                   const uint16_t *b, const float *A_log, float scale, const float *init,
+                                   float *fin, const int32_t *cu, int N, int B, int T, int H_qk, int H_v,
+                                   uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches) {
+    const bool varlen = cu != nullptr;
+    const int nseq = varlen ? N : B;
+    FwdWorkspace ws;
+    fwd_workspace_bytes(N, B, T, H_v, varlen, &ws, (char *)ws_ptr);
+    const long long nck = max_chunks_for(N, B, T, varlen);
+    *launches = 0;
+    cudaError_t e = cudaFuncSetAttribute(intra_gdn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GD_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS_BYTES);
+    if (e != cudaSuccess) return e;
+    timing_begin(stream);
+    plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu, N, B, T, ws.seqs, ws.chunks, ws.order, ws.hdr, nck);
+    ++*launches;
+    timing_mark("plan_kernel", stream);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (nck > 0) {
+        GdnParams gp;
+        gp.q = q; gp.k = k; gp.v = v; gp.graw = graw; gp.b = b; gp.A_log = A_log; gp.scale = scale;
+        gp.H_qk = H_qk; gp.H_v = H_v; gp.chunks = ws.chunks; gp.hdr = ws.hdr; gp.rec = ws.rec;
+        int dev = 0, nsm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        const long long items = nck * (long long)H_v, slots = (long long)nsm * IN_CTAS_PER_SM;
+        intra_gdn_kernel<<<(unsigned)(items < slots ? items : slots), IN_THREADS, GD_BYTES, stream>>>(gp);
+        ++*launches;
+        timing_mark("intra_gdn_kernel", stream);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (nseq > 0) {
+        ScanParams sp;
+        sp.rec = ws.rec;
+        sp.seqs = ws.seqs; sp.order = ws.order; sp.hdr = ws.hdr;
+        sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = 0; sp.Hw = H_v;
+        scan_kernel<<<(unsigned)((long long)nseq * H_v * 2), SC_THREADS, SS_BYTES, stream>>>(sp);
+        ++*launches;
+        timing_mark("scan_kernel", stream);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

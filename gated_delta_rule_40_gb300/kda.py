@@ -59,6 +59,8 @@ def load() -> ctypes.CDLL:
     lib.kda_fwd_noalloc.restype = I
     lib.kda_fwd_host.argtypes = fwd_args + [P]
     lib.kda_fwd_host.restype = I
+    lib.kda_fwd_scalar_gate.argtypes = fwd_args + [P]
+    lib.kda_fwd_scalar_gate.restype = I
     lib.kda_fwd_workspace_size.argtypes = [I] * 7
     lib.kda_fwd_workspace_size.restype = Z
     lib.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, P, P]
@@ -155,6 +157,38 @@ def kda_fwd(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_seqlen
         _check(workspace, "workspace", torch.uint8)
         rc = lib.kda_fwd_ws(*args, _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
         _raise(rc, "kda_fwd_ws")
+    return out, final_state
+
+
+def kda_fwd_scalar_gate(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_seqlens=None,
+                        output_final_state: bool = True, out=None, final_state=None,
+                        stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """KDA forward with one gate value per token and value head: graw [B,T,H_v]
+    (bf16).  Other shapes as ``kda_fwd``; equals ``kda_fwd`` with graw broadcast
+    along K."""
+    lib = load()
+    B, T, H_qk, K = q.shape
+    H_v, V = v.shape[2], v.shape[3]
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    bf = torch.bfloat16
+    _check(q, "q", bf, (B, T, H_qk, K))
+    _check(k, "k", bf, (B, T, H_qk, K))
+    _check(v, "v", bf, (B, T, H_v, V))
+    _check(graw, "graw", bf, (B, T, H_v))
+    _check(b, "b", bf, (B, T, H_v))
+    _check(A_log, "A_log", torch.float32, (H_v,))
+    _check(initial_state, "initial_state", torch.float32, (N, H_v, V, K), optional=True)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, optional=True)
+    if out is None:
+        out = torch.empty((B, T, H_v, V), dtype=bf, device=q.device)
+    _check(out, "out", bf, (B, T, H_v, V))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H_v, V, K), dtype=torch.float32, device=q.device)
+    _check(final_state, "final_state", torch.float32, (N, H_v, V, K), optional=True)
+    rc = lib.kda_fwd_scalar_gate(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
+                                 _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V,
+                                 _ptr(out), _stream(stream))
+    _raise(rc, "kda_fwd_scalar_gate")
     return out, final_state
 
 

@@ -104,6 +104,20 @@ int kda_fwd_ws(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
                void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * kda_fwd for a scalar gate: graw is [B, T, H_v] bf16, one gate pre-activation per
+ * token and value head shared by all K channels (the gated delta rule's per-head
+ * decay, "broadcast across K").  Every other argument, and the result, as kda_fwd:
+ * the output equals kda_fwd's with graw broadcast along K.  A dedicated
+ * intra-chunk kernel uses the scalar decay: the gate read shrinks 128-fold and the
+ * chunk's products come from one MMA of the raw q and k times a decay mask.
+ */
+int kda_fwd_scalar_gate(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
+                        const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log, float scale,
+                        const float *initial_state, float *final_state, const int32_t *cu_seqlens,
+                        int N, int B, int T, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
+                        cudaStream_t stream);
+
+/*
  * kda_fwd on host buffers: the same problem and the same results, with every
  * tensor (cu_seqlens included) in host memory.  Pinned (page-locked) buffers let
  * the copies run at the host link's bandwidth; pageable ones work, more slowly.
