@@ -317,6 +317,37 @@ def run_gpu(args, rank, world, local):
     barrier(world)
     e2e_ms = max_over_ranks(time_events(e2e_step, e2e_steps, stream), world)
 
+    # ---- scalar gate (one gate value per token and value head): the grouped-value-head
+    # workload (28672 + 4096 tokens, H_qk=16, H_v=64) through kda_fwd_scalar_gate, and the
+    # general kernel on the same inputs with the gate broadcast along K
+    sg = KI.workload("gva")
+    sd = {n: getattr(sg, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log", "initial_state", "cu_seqlens")}
+    sg_g = sg.graw[..., 0].contiguous().to(dev)
+    sg_out = torch.empty_like(sd["v"])
+    sg_fin = torch.empty_like(sd["initial_state"])
+
+    def sg_step():
+        kda.kda_fwd_scalar_gate(sd["q"], sd["k"], sd["v"], sg_g, sd["b"], sd["A_log"], sg.scale,
+                                initial_state=sd["initial_state"], cu_seqlens=sd["cu_seqlens"], out=sg_out,
+                                final_state=sg_fin, stream=stream)
+
+    def sg_general_step():
+        kda.kda_fwd(sd["q"], sd["k"], sd["v"], sd["graw"], sd["b"], sd["A_log"], sg.scale,
+                    initial_state=sd["initial_state"], cu_seqlens=sd["cu_seqlens"], out=sg_out, final_state=sg_fin,
+                    stream=stream)
+
+    for _ in range(3):
+        sg_step()
+        sg_general_step()
+    torch.cuda.synchronize()
+    sg_ms = time_events(sg_step, 10, stream)
+    sg_gen_ms = time_events(sg_general_step, 10, stream)
+    sg_units = sg.token_heads()
+    ntok = sg.q.shape[0] * sg.q.shape[1]
+    sg_bytes = (ntok * sg.H_qk * 2 * 256 + ntok * sg.H_v * (256 + 2 + 2 + 256)
+                + 2 * sg.N * sg.H_v * STATE_BYTES_PER_SEQ_HEAD)
+    del sd, sg_g, sg_out, sg_fin
+
     # ---- decode (B=256, H=64): state GB/s against HBM
     dec = KI.decode_inputs(B=256, H=64, seed=rank)
     dd = {n: getattr(dec, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log", "state")}
@@ -361,6 +392,11 @@ def run_gpu(args, rank, world, local):
                    "flops_per_step": alg_flops, "peak_source": peak_src},
         "e2e": {"value": world * units / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "scalar_gate": {"workload": "grouped value heads, 28672+4096 tokens, H_qk=16 H_v=64, scalar gate",
+                        "value": sg_units / (sg_ms * 1e-3), "unit": UNIT, "ms": sg_ms,
+                        "general_path_ms": sg_gen_ms, "algorithmic_bytes": sg_bytes,
+                        "GB/s": sg_bytes / (sg_ms * 1e-3) / 1e9, "hbm_peak": hbm_peak,
+                        "frac": sg_bytes / (sg_ms * 1e-3) / 1e9 / hbm_peak},
         "decode": {"workload": "B=256 H=64 K=V=128 fp32 state in place", "ms": dec_ms, "GB/s": dec_gbs,
                    "hbm_peak": hbm_peak, "frac": dec_gbs / hbm_peak},
         "gpu_launches": launches_per_step * args.steps,
