@@ -8,6 +8,7 @@ from .kda import (  # noqa: F401
     KdaError,
     KdaLibraryError,
     kda_decode_step,
+    kda_decode_tokens,
     kda_fwd,
     kda_fwd_host,
     kda_fwd_noalloc,

@@ -19,6 +19,9 @@ cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const u
                                    const uint16_t *b, const float *A_log, float scale, const float *init,
                                    float *fin, const int32_t *cu, int N, int B, int T, int H_qk, int H_v,
                                    uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches);
+cudaError_t launch_decode_tokens(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                                 const uint16_t *b, const float *A_log, float scale, void *state, bool bf16_state,
+                                 int B, int Tq, int H_qk, int H_v, uint16_t *out, cudaStream_t stream);
 struct FwdWorkspace;
 size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspace *ws, char *base);
 
@@ -189,6 +192,30 @@ int kda_fwd_scalar_gate(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16
     if (rc == KDA_OK) t_last_launches = launches;
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
     return rc;
+}
+
+int kda_decode_tokens(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+                      const kda_bf16_t *b, const float *A_log, float scale, void *state, int state_is_bf16, int B,
+                      int Tq, int H_qk, int H_v, int K, int V, kda_bf16_t *out, cudaStream_t stream) {
+    if (K != kda::KD || V != kda::KD) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || Tq < 1 || Tq > KDA_DECODE_MAX_TOKENS || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0 ||
+        (state_is_bf16 != 0 && state_is_bf16 != 1))
+        return KDA_ERR_INVALID_ARG;
+    if (B == 0) {
+        t_last_launches = 0;
+        return KDA_OK;
+    }
+    if (!q || !k || !v || !graw || !b || !A_log || !state || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(graw) || !aligned16(state) ||
+        !aligned16(out))
+        return KDA_ERR_INVALID_ARG;
+    kda::timing_begin(stream);
+    const cudaError_t e = kda::launch_decode_tokens(q, k, v, graw, b, A_log, scale, state, state_is_bf16 != 0, B, Tq,
+                                                    H_qk, H_v, out, stream);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    kda::timing_mark("decode_tokens_kernel", stream);
+    t_last_launches = 1;
+    return KDA_OK;
 }
 
 int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,

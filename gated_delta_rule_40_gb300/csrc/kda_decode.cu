@@ -99,3 +99,143 @@ cudaError_t launch_decode(const uint16_t *q, const uint16_t *k, const uint16_t *
 }
 
 }  // namespace kda
+
+// =====================================================================
+// Multi-token decode: Tq <= 8 consecutive tokens per (b, h) applied to the
+// state in one pass (read once, Tq updates in registers, written once), the
+// state stored in fp32 or bf16.  Warp t < Tq first prepares token t (normalised
+// q and k, per-channel decay, beta, k.q, v) in shared memory; then each warp
+// streams 16 state rows through all Tq tokens.
+// =====================================================================
+namespace kda {
+
+constexpr int DEC_MAX_T = 8;
+
+template <bool BF16_STATE>
+__global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
+    const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
+    const uint16_t *__restrict__ graw, const uint16_t *__restrict__ b, const float *__restrict__ A_log, float scale,
+    void *__restrict__ state, int Tq, int H_qk, int H_v, uint16_t *__restrict__ out) {
+    __shared__ float s_qt[DEC_MAX_T][KD], s_kh[DEC_MAX_T][KD], s_dec[DEC_MAX_T][KD], s_v[DEC_MAX_T][KD];
+    __shared__ float s_beta[DEC_MAX_T], s_kq[DEC_MAX_T];
+    const int bh = blockIdx.x;
+    const int bi = bh / H_v, h = bh - bi * H_v;
+    const int hq = h / (H_v / H_qk);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    // ---- token preparation: warp t handles token t; lane owns channels 4 lane .. 4 lane + 3
+    if (warp < Tq) {
+        const int t = warp;
+        const size_t row_qk = (((size_t)bi * Tq + t) * H_qk + hq) * KD + 4 * lane;
+        const size_t row_v = (((size_t)bi * Tq + t) * H_v + h) * KD;
+        const uint2 qw = *reinterpret_cast<const uint2 *>(q + row_qk);
+        const uint2 kw = *reinterpret_cast<const uint2 *>(k + row_qk);
+        const uint2 gw = *reinterpret_cast<const uint2 *>(graw + row_v + 4 * lane);
+        const uint2 vw = *reinterpret_cast<const uint2 *>(v + row_v + 4 * lane);
+        const float qv[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
+        const float kv[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
+        const float gv[4] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y)};
+        const float vv[4] = {bf16_lo(vw.x), bf16_hi(vw.x), bf16_lo(vw.y), bf16_hi(vw.y)};
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sq = fmaf(qv[i], qv[i], sq);
+            sk = fmaf(kv[i], kv[i], sk);
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        const float rq = scale * rsqrtf(sq + L2_EPS), rk = rsqrtf(sk + L2_EPS);
+        const float a = ex2(A_log[h] * LOG2E);
+        float kq = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = 4 * lane + i;
+            s_qt[t][c] = qv[i] * rq;
+            s_kh[t][c] = kv[i] * rk;
+            s_dec[t][c] = ex2(-a * softplus_log2(gv[i]));
+            s_v[t][c] = vv[i];
+            kq = fmaf(kv[i] * rk, qv[i] * rq, kq);
+        }
+        kq = warp_sum(kq);
+        if (lane == 0) {
+            s_kq[t] = kq;
+            s_beta[t] = 1.0f / (1.0f + ex2(-bf16_to_f(b[((size_t)bi * Tq + t) * H_v + h]) * LOG2E));
+        }
+    }
+    __syncthreads();
+
+    // ---- the warp's 16 state rows, fp32 in registers
+    const int r0 = warp * DEC_ROWS;
+    const size_t st0 = ((size_t)bh * KD + r0) * KD;
+    float4 s[DEC_ROWS];
+    if (BF16_STATE) {
+        const uint16_t *S = reinterpret_cast<const uint16_t *>(state) + st0;
+#pragma unroll
+        for (int i = 0; i < DEC_ROWS; ++i) {
+            const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(S + (size_t)i * KD) + lane);
+            s[i] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+        }
+    } else {
+        const float *S = reinterpret_cast<const float *>(state) + st0;
+#pragma unroll
+        for (int i = 0; i < DEC_ROWS; ++i) s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)i * KD) + lane);
+    }
+    for (int t = 0; t < Tq; ++t) {
+        const float4 dec = *reinterpret_cast<const float4 *>(&s_dec[t][4 * lane]);
+        const float4 kh = *reinterpret_cast<const float4 *>(&s_kh[t][4 * lane]);
+        const float4 qt = *reinterpret_cast<const float4 *>(&s_qt[t][4 * lane]);
+        const float beta = s_beta[t], kq = s_kq[t];
+        const float vmine = s_v[t][r0 + (lane & (DEC_ROWS - 1))];
+        float o_mine = 0.f;
+#pragma unroll
+        for (int i = 0; i < DEC_ROWS; ++i) {
+            float4 x = s[i];
+            x.x *= dec.x;
+            x.y *= dec.y;
+            x.z *= dec.z;
+            x.w *= dec.w;
+            float dk = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
+            float dq = x.x * qt.x + x.y * qt.y + x.z * qt.z + x.w * qt.w;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                dk += __shfl_xor_sync(0xffffffffu, dk, o);
+                dq += __shfl_xor_sync(0xffffffffu, dq, o);
+            }
+            const float delta = beta * (__shfl_sync(0xffffffffu, vmine, i) - dk);
+            x.x = fmaf(delta, kh.x, x.x);
+            x.y = fmaf(delta, kh.y, x.y);
+            x.z = fmaf(delta, kh.z, x.z);
+            x.w = fmaf(delta, kh.w, x.w);
+            s[i] = x;
+            if (lane == i) o_mine = fmaf(delta, kq, dq);
+        }
+        if (lane < DEC_ROWS) out[(((size_t)bi * Tq + t) * H_v + h) * KD + r0 + lane] = f_to_bf16(o_mine);
+    }
+    if (BF16_STATE) {
+        uint16_t *S = reinterpret_cast<uint16_t *>(state) + st0;
+#pragma unroll
+        for (int i = 0; i < DEC_ROWS; ++i)
+            __stcs(reinterpret_cast<uint2 *>(S + (size_t)i * KD) + lane,
+                   make_uint2(pack_bf16x2(s[i].x, s[i].y), pack_bf16x2(s[i].z, s[i].w)));
+    } else {
+        float *S = reinterpret_cast<float *>(state) + st0;
+#pragma unroll
+        for (int i = 0; i < DEC_ROWS; ++i) __stcs(reinterpret_cast<float4 *>(S + (size_t)i * KD) + lane, s[i]);
+    }
+}
+
+cudaError_t launch_decode_tokens(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                                 const uint16_t *b, const float *A_log, float scale, void *state, bool bf16_state,
+                                 int B, int Tq, int H_qk, int H_v, uint16_t *out, cudaStream_t stream) {
+    const long long nblk = (long long)B * H_v;
+    if (nblk == 0) return cudaSuccess;
+    if (bf16_state)
+        decode_tokens_kernel<true><<<(unsigned)nblk, DEC_WARPS * 32, 0, stream>>>(q, k, v, graw, b, A_log, scale,
+                                                                                   state, Tq, H_qk, H_v, out);
+    else
+        decode_tokens_kernel<false><<<(unsigned)nblk, DEC_WARPS * 32, 0, stream>>>(q, k, v, graw, b, A_log, scale,
+                                                                                    state, Tq, H_qk, H_v, out);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -65,6 +65,8 @@ def load() -> ctypes.CDLL:
     lib.kda_fwd_workspace_size.restype = Z
     lib.kda_decode_step.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, P, P]
     lib.kda_decode_step.restype = I
+    lib.kda_decode_tokens.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, P, P]
+    lib.kda_decode_tokens.restype = I
     lib.kda_status_string.argtypes = [I]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_get_status.argtypes = [P]
@@ -311,3 +313,33 @@ def kda_kernel_times() -> list:
     if n < 0:
         raise KdaError(n, "kda_kernel_times")
     return [(names[i].decode(), float(ms[i])) for i in range(n)]
+
+
+DECODE_MAX_TOKENS = 8
+
+
+def kda_decode_tokens(q, k, v, graw, b, A_log, scale: float, state, out=None, stream=None) -> torch.Tensor:
+    """Decode of Tq <= 8 consecutive tokens per (b, h) in one pass over ``state``
+    [B,H_v,V,K] (fp32 or bf16, updated in place).  Shapes: q, k [B,Tq,H_qk,K];
+    v, graw [B,Tq,H_v,*]; b [B,Tq,H_v] (bf16).  Returns out [B,Tq,H_v,V]."""
+    lib = load()
+    B, Tq, H_qk, K = q.shape
+    H_v, V = v.shape[2], v.shape[3]
+    bf = torch.bfloat16
+    _check(q, "q", bf, (B, Tq, H_qk, K))
+    _check(k, "k", bf, (B, Tq, H_qk, K))
+    _check(v, "v", bf, (B, Tq, H_v, V))
+    _check(graw, "graw", bf, (B, Tq, H_v, K))
+    _check(b, "b", bf, (B, Tq, H_v))
+    _check(A_log, "A_log", torch.float32, (H_v,))
+    if state.dtype not in (torch.float32, bf):
+        raise TypeError(f"state must be float32 or bfloat16, got {state.dtype}")
+    _check(state, "state", state.dtype, (B, H_v, V, K))
+    if out is None:
+        out = torch.empty((B, Tq, H_v, V), dtype=bf, device=q.device)
+    _check(out, "out", bf, (B, Tq, H_v, V))
+    rc = lib.kda_decode_tokens(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
+                               _ptr(state), 1 if state.dtype == bf else 0, B, Tq, H_qk, H_v, K, V, _ptr(out),
+                               _stream(stream))
+    _raise(rc, "kda_decode_tokens")
+    return out

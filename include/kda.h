@@ -154,6 +154,27 @@ int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
                     float scale, float *state, int B, int H_qk, int H_v, int K, int V,
                     kda_bf16_t *out, cudaStream_t stream);
 
+/*
+ * Decode of Tq (1..KDA_DECODE_MAX_TOKENS) consecutive tokens per (b, h) in one
+ * pass over the state, which is read once and written once (for example the
+ * verification step of speculative decoding), with the state stored in fp32
+ * (state_is_bf16 = 0) or bf16 (state_is_bf16 = 1; the recurrence runs in fp32
+ * and the updated state is rounded to bf16 once, at the end of the pass).
+ *
+ *   q, k   [B, Tq, H_qk, K] bf16      v, graw [B, Tq, H_v, *] bf16
+ *   b      [B, Tq, H_v] bf16          A_log [H_v] fp32
+ *   state  [B, H_v, V, K] fp32 or bf16, updated in place
+ *   out    [B, Tq, H_v, V] bf16
+ *
+ * The result equals Tq calls of kda_decode_step (for an fp32 state) up to
+ * rounding order.  Returns KDA_ERR_INVALID_ARG for Tq outside 1..8.
+ */
+#define KDA_DECODE_MAX_TOKENS 8
+int kda_decode_tokens(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
+                      const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log,
+                      float scale, void *state, int state_is_bf16, int B, int Tq, int H_qk,
+                      int H_v, int K, int V, kda_bf16_t *out, cudaStream_t stream);
+
 /* Human-readable name of a return or status code (static string). */
 const char *kda_status_string(int code);
 
