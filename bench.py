@@ -364,6 +364,28 @@ def run_gpu(args, rank, world, local):
     dec_bytes = 256 * 64 * (2 * 128 * 128 * 4 + 5 * 256 + 2)
     dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
 
+    # ---- multi-token decode (kda_decode_tokens): Tq = 1 and 4 tokens per pass, fp32 and bf16 state
+    multi = {}
+    for tq in (1, 4):
+        mt = KI.make_inputs(256, tq, 64, 64, seed=rank + 7, with_state=True)
+        md = {n: getattr(mt, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log")}
+        mout = torch.empty((256, tq, 64, 128), dtype=torch.bfloat16, device=dev)
+        for sdt, sname, sbytes in ((torch.float32, "fp32", 4), (torch.bfloat16, "bf16", 2)):
+            mst = mt.initial_state.to(sdt).to(dev)
+
+            def mstep():
+                kda.kda_decode_tokens(md["q"], md["k"], md["v"], md["graw"], md["b"], md["A_log"], mt.scale, mst,
+                                      out=mout, stream=stream)
+
+            for _ in range(3):
+                mstep()
+            torch.cuda.synchronize()
+            mms = time_events(mstep, 30, stream)
+            mbytes = 256 * 64 * (2 * 128 * 128 * sbytes + tq * (5 * 256 + 2))
+            multi[f"T{tq}_{sname}_state"] = {"ms": mms, "tokens_per_s": 256 * tq / (mms * 1e-3),
+                                             "GB/s": mbytes / (mms * 1e-3) / 1e9}
+        del md, mst, mout
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp)
@@ -397,6 +419,7 @@ def run_gpu(args, rank, world, local):
                         "general_path_ms": sg_gen_ms, "algorithmic_bytes": sg_bytes,
                         "GB/s": sg_bytes / (sg_ms * 1e-3) / 1e9, "hbm_peak": hbm_peak,
                         "frac": sg_bytes / (sg_ms * 1e-3) / 1e9 / hbm_peak},
+        "decode_tokens": {"workload": "B=256 H=64 K=V=128, Tq tokens per pass, state in place", **multi},
         "decode": {"workload": "B=256 H=64 K=V=128 fp32 state in place", "ms": dec_ms, "GB/s": dec_gbs,
                    "hbm_peak": hbm_peak, "frac": dec_gbs / hbm_peak},
         "gpu_launches": launches_per_step * args.steps,

@@ -184,9 +184,8 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
         const float4 dec = *reinterpret_cast<const float4 *>(&s_dec[t][4 * lane]);
         const float4 kh = *reinterpret_cast<const float4 *>(&s_kh[t][4 * lane]);
         const float4 qt = *reinterpret_cast<const float4 *>(&s_qt[t][4 * lane]);
-        const float beta = s_beta[t], kq = s_kq[t];
-        const float vmine = s_v[t][r0 + (lane & (DEC_ROWS - 1))];
-        float o_mine = 0.f;
+        // per row i: dk_i = s'_i . kh (value 2 i) and dq_i = s'_i . qt (value 2 i + 1), lane partials
+        float red[2 * DEC_ROWS];
 #pragma unroll
         for (int i = 0; i < DEC_ROWS; ++i) {
             float4 x = s[i];
@@ -194,22 +193,38 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
             x.y *= dec.y;
             x.z *= dec.z;
             x.w *= dec.w;
-            float dk = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
-            float dq = x.x * qt.x + x.y * qt.y + x.z * qt.z + x.w * qt.w;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                dk += __shfl_xor_sync(0xffffffffu, dk, o);
-                dq += __shfl_xor_sync(0xffffffffu, dq, o);
-            }
-            const float delta = beta * (__shfl_sync(0xffffffffu, vmine, i) - dk);
-            x.x = fmaf(delta, kh.x, x.x);
-            x.y = fmaf(delta, kh.y, x.y);
-            x.z = fmaf(delta, kh.z, x.z);
-            x.w = fmaf(delta, kh.w, x.w);
             s[i] = x;
-            if (lane == i) o_mine = fmaf(delta, kq, dq);
+            red[2 * i] = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
+            red[2 * i + 1] = x.x * qt.x + x.y * qt.y + x.z * qt.z + x.w * qt.w;
         }
-        if (lane < DEC_ROWS) out[(((size_t)bi * Tq + t) * H_v + h) * KD + r0 + lane] = f_to_bf16(o_mine);
+        // reduce-scatter over the warp: at each level a lane keeps half of its values (the half
+        // selected by its lane bit) and adds the partner's copy of that half; after five levels
+        // lane l holds the warp total of value l (31 shuffles for 32 sums)
+#pragma unroll
+        for (int o = 16, n = 16; o >= 1; o >>= 1, n >>= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < n; ++i) {
+                const float send = upper ? red[i] : red[i + n];
+                const float keep = upper ? red[i + n] : red[i];
+                red[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        // lane 2 i: dk_i -> delta_i; lane 2 i + 1: dq_i -> o_i = dq_i + delta_i (k.q)
+        const int row = lane >> 1;
+        const float dk_or_dq = red[0];
+        const float delta_mine = s_beta[t] * (s_v[t][r0 + row] - dk_or_dq);
+        const float delta_pair = __shfl_xor_sync(0xffffffffu, delta_mine, 1);
+        if (lane & 1)
+            out[(((size_t)bi * Tq + t) * H_v + h) * KD + r0 + row] = f_to_bf16(fmaf(delta_pair, s_kq[t], dk_or_dq));
+#pragma unroll
+        for (int i = 0; i < DEC_ROWS; ++i) {
+            const float delta = __shfl_sync(0xffffffffu, delta_mine, 2 * i);
+            s[i].x = fmaf(delta, kh.x, s[i].x);
+            s[i].y = fmaf(delta, kh.y, s[i].y);
+            s[i].z = fmaf(delta, kh.z, s[i].z);
+            s[i].w = fmaf(delta, kh.w, s[i].w);
+        }
     }
     if (BF16_STATE) {
         uint16_t *S = reinterpret_cast<uint16_t *>(state) + st0;
