@@ -74,6 +74,20 @@ int timing_read(float *ms, const char **names, int max_n) {
 }
 }  // namespace kda
 
+namespace kda {
+// One thread waits, with a small bound, on an mbarrier phase that nothing completes; the
+// bounded wait gives up and records KDA_ERR_DEVICE_TIMEOUT, exactly as a stalled hand-off
+// in the forward kernels would, and the kernel returns normally.
+__global__ void selftest_wait_timeout_kernel(uint32_t limit) {
+    __shared__ __align__(8) unsigned long long bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t mb = smem_u32(&bar);
+    mbar_init(mb, 1);
+    mbar_fence_init();
+    if (!mbar_spin(mb, 0, limit)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+}
+}  // namespace kda
+
 namespace {
 thread_local int t_last_launches = 0;
 
@@ -125,6 +139,11 @@ int kda_get_status(cudaStream_t stream) {
 }
 
 int kda_last_launch_count(void) { return t_last_launches; }
+
+int kda_selftest_wait_timeout(cudaStream_t stream) {
+    kda::selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>(1u << 12);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
 
 int kda_set_kernel_timing(int enable) { return kda::timing_enable(enable != 0); }
 

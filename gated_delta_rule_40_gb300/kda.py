@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_get_status.argtypes = [P]
     lib.kda_get_status.restype = I
+    lib.kda_selftest_wait_timeout.argtypes = [P]
+    lib.kda_selftest_wait_timeout.restype = I
     lib.kda_last_launch_count.argtypes = []
     lib.kda_last_launch_count.restype = I
     lib.kda_set_kernel_timing.argtypes = [I]
@@ -343,3 +345,9 @@ def kda_decode_tokens(q, k, v, graw, b, A_log, scale: float, state, out=None, st
                                _stream(stream))
     _raise(rc, "kda_decode_tokens")
     return out
+
+
+def kda_selftest_wait_timeout(stream=None) -> None:
+    """Queue the self-test whose bounded device wait gives up and records
+    KDA_ERR_DEVICE_TIMEOUT in the status word (see ``kda_get_status``)."""
+    _raise(load().kda_selftest_wait_timeout(_stream(stream)), "kda_selftest_wait_timeout")

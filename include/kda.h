@@ -208,6 +208,13 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
                     int N, int B, int T, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
                     cudaStream_t stream);
 
+/* Self-test of the device-side failure path: queues one tiny kernel whose bounded
+ * wait on a barrier that nothing completes gives up, recording
+ * KDA_ERR_DEVICE_TIMEOUT in the status word (read it with kda_get_status); the
+ * kernel returns normally and the context stays usable.  No counterpart on the
+ * pages; it checks the library's own error reporting. */
+int kda_selftest_wait_timeout(cudaStream_t stream);
+
 /* Number of kernel launches the most recent successful kda_fwd / kda_fwd_ws /
  * kda_decode_step call on this host thread queued. */
 int kda_last_launch_count(void);

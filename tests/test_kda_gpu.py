@@ -204,3 +204,16 @@ def test_decode_equals_fwd_t1():
     out_f, fin_f = gpu_fwd(inp)
     assert rel_l2(out_d.double().cpu().numpy(), out_f[:, 0].double().cpu().numpy()) < 5e-3
     assert rel_l2(st_d.double().cpu().numpy(), fin_f.double().cpu().numpy()) < 1e-3
+
+
+# ---------------------------------------------------------------- device-side failure path
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A bounded wait on a barrier that nothing completes gives up, records
+    KDA_ERR_DEVICE_TIMEOUT in the status word and returns; reading the status clears it
+    and the next forward on the same context is still exact against the oracle."""
+    from gated_delta_rule_40_gb300 import kda
+    assert kda.kda_get_status() == 0
+    kda.kda_selftest_wait_timeout()
+    assert kda.kda_get_status() == kda.KDA_ERR_DEVICE_TIMEOUT
+    assert kda.kda_get_status() == 0
+    _check_full(KI.make_inputs(1, 130, 1, 2, seed=77, with_state=True, name="after-timeout"))
