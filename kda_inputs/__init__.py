@@ -17,6 +17,19 @@ on GB200 and FlashQLA's gated-delta-rule tables on H200):
   scalar-decay gated delta rule as a special case of the per-channel gate).
 * ``decode``  B=256, H=64, one token, state ~ N(0, 0.02) updated in place.
 
+Lightning attention (linear attention with a fixed per-head decay; shapes from
+cuLA's lightning-attention tables, whose head count was lost from the page, and
+its ``la_decode`` run with 64 heads of dimension 128):
+
+* ``la_dense``   B=2, T=16384, H=64, q/k/v ~ N(0, 1), initial state ~ N(0, 1).
+* ``la_varlen``  20 packed sequences, total T=16380 (one of 8190, the other 19
+  log-uniform in [16, 4096] rescaled), H=64.
+* ``la_decode``  B=256, H=64, one token, state ~ N(0, 1) updated in place.
+
+The per-head decay rates are the geometric sequence ``2^(-8 (h+1) / H)``
+(largest 2^(-8/H), smallest 2^-8): a fixed input pattern, not drawn.  Draw
+order: q, k, v, initial_state.
+
 Draw order for one workload: q, k, v, graw, b, A_log, initial_state, all from
 one ``torch.Generator`` seeded with ``seed``.  Normal draws are fp32 and then
 rounded to bf16 (round-to-nearest-even), so the oracle and the GPU path see
@@ -220,3 +233,123 @@ def hadamard(n: int) -> torch.Tensor:
         h = torch.cat([torch.cat([h, h], 1), torch.cat([h, -h], 1)], 0)
     assert h.shape[0] == n
     return h
+
+
+# ---------------------------------------------------------------------------
+# Lightning attention inputs
+# ---------------------------------------------------------------------------
+LA_STATE_STD = 1.0
+
+
+def geometric_slopes(H: int) -> torch.Tensor:
+    """Per-head decay rates 2^(-8 (h+1) / H), h = 0..H-1 (fp32)."""
+    return torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=torch.float32)
+
+
+@dataclass
+class LaInputs:
+    """Host tensors for one lightning-attention forward: q, k ``[B,T,H_qk,K]``
+    bf16; v ``[B,T,H_v,V]`` bf16; slope ``[H_v]`` fp32; initial_state
+    ``[N,H_v,V,K]`` fp32 or None; cu_seqlens ``[N+1]`` int32 or None."""
+
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    slope: torch.Tensor
+    scale: float
+    initial_state: Optional[torch.Tensor]
+    cu_seqlens: Optional[torch.Tensor]
+    name: str = ""
+
+    @property
+    def B(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def T(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def H_qk(self) -> int:
+        return self.q.shape[2]
+
+    @property
+    def H_v(self) -> int:
+        return self.v.shape[2]
+
+    @property
+    def N(self) -> int:
+        return self.B if self.cu_seqlens is None else self.cu_seqlens.numel() - 1
+
+    def seqlens(self) -> List[int]:
+        if self.cu_seqlens is None:
+            return [self.T] * self.B
+        c = self.cu_seqlens.tolist()
+        return [c[i + 1] - c[i] for i in range(len(c) - 1)]
+
+    def token_heads(self) -> int:
+        return self.B * self.T * self.H_v
+
+
+def make_la_inputs(B: int, T: int, H_qk: int, H_v: int, *, seed: int = 0, with_state: bool = True,
+                   seqlens: Optional[List[int]] = None, slope: Optional[torch.Tensor] = None,
+                   name: str = "") -> LaInputs:
+    """Draw one lightning-attention forward problem (packed when ``seqlens``
+    is given: B must be 1 and T == sum(seqlens))."""
+    if seqlens is not None:
+        assert B == 1 and T == sum(seqlens)
+        cu = torch.tensor([0] + list(torch.cumsum(torch.tensor(seqlens), 0).tolist()), dtype=torch.int32)
+        n_seq = len(seqlens)
+    else:
+        cu = None
+        n_seq = B
+    g = torch.Generator().manual_seed(seed)
+    q = _bf16_normal(g, (B, T, H_qk, K_DIM))
+    k = _bf16_normal(g, (B, T, H_qk, K_DIM))
+    v = _bf16_normal(g, (B, T, H_v, V_DIM))
+    init = None
+    if with_state:
+        init = torch.randn((n_seq, H_v, V_DIM, K_DIM), generator=g, dtype=torch.float32) * LA_STATE_STD
+    return LaInputs(q=q, k=k, v=v, slope=geometric_slopes(H_v) if slope is None else slope.to(torch.float32),
+                    scale=1.0 / math.sqrt(K_DIM), initial_state=init, cu_seqlens=cu, name=name)
+
+
+def la_workload(name: str, seed: int = 0) -> LaInputs:
+    """The named lightning-attention forward workloads (module docstring)."""
+    if name == "la_dense":
+        return make_la_inputs(2, 16384, 64, 64, seed=seed, name=name)
+    if name == "la_varlen":
+        lens = skewed_seqlens(16380, 20, 8190, 16, 4096, seed + 1)
+        return make_la_inputs(1, 16380, 64, 64, seed=seed, seqlens=lens, name=name)
+    raise KeyError(name)
+
+
+@dataclass
+class LaDecodeInputs:
+    """One lightning-attention step: q, k ``[B,H_qk,K]``, v ``[B,H_v,V]`` bf16;
+    slope ``[H_v]`` fp32; state ``[B,H_v,V,K]`` fp32 (updated in place)."""
+
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    slope: torch.Tensor
+    scale: float
+    state: torch.Tensor
+
+    @property
+    def B(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def H_v(self) -> int:
+        return self.v.shape[1]
+
+
+def la_decode_inputs(B: int = 256, H: int = 64, *, H_qk: Optional[int] = None, seed: int = 0) -> LaDecodeInputs:
+    H_qk = H if H_qk is None else H_qk
+    g = torch.Generator().manual_seed(seed)
+    q = _bf16_normal(g, (B, H_qk, K_DIM))
+    k = _bf16_normal(g, (B, H_qk, K_DIM))
+    v = _bf16_normal(g, (B, H, V_DIM))
+    state = torch.randn((B, H, V_DIM, K_DIM), generator=g, dtype=torch.float32) * LA_STATE_STD
+    return LaDecodeInputs(q=q, k=k, v=v, slope=geometric_slopes(H), scale=1.0 / math.sqrt(K_DIM), state=state)
