@@ -22,6 +22,12 @@ cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const u
 cudaError_t launch_decode_tokens(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
                                  const uint16_t *b, const float *A_log, float scale, void *state, bool bf16_state,
                                  int B, int Tq, int H_qk, int H_v, uint16_t *out, cudaStream_t stream);
+cudaError_t launch_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *slope, float scale,
+                          const float *init, float *fin, const int32_t *cu, int N, int B, int T, int H_qk, int H_v,
+                          uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches);
+size_t la_workspace_bytes(int N, int B, int T, bool varlen);
+cudaError_t launch_la_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *slope, float scale,
+                             float *state, int B, int H_qk, int H_v, uint16_t *out, cudaStream_t stream);
 struct FwdWorkspace;
 size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspace *ws, char *base);
 
@@ -254,6 +260,56 @@ int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
     cudaError_t e = kda::launch_decode(q, k, v, graw, b, A_log, scale, state, B, H_qk, H_v, out, stream);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     kda::timing_mark("decode_kernel", stream);
+    t_last_launches = 1;
+    return KDA_OK;
+}
+
+int kda_la_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const float *slope, float scale,
+               const float *initial_state, float *final_state, const int32_t *cu_seqlens, int N, int B, int T,
+               int H_qk, int H_v, int K, int V, kda_bf16_t *out, cudaStream_t stream) {
+    if (K != kda::KD || V != kda::KD) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || T < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0) return KDA_ERR_INVALID_ARG;
+    if (cu_seqlens && (B != 1 || N < 0)) return KDA_ERR_INVALID_ARG;
+    const long long tokens = (long long)B * T;
+    if (tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    const int nseq = cu_seqlens ? N : B;
+    if (nseq > 0 && !slope) return KDA_ERR_INVALID_ARG;
+    if (tokens > 0) {
+        if (!q || !k || !v || !out) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return KDA_ERR_INVALID_ARG;
+    }
+    if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)))
+        return KDA_ERR_INVALID_ARG;
+    const size_t need = kda::la_workspace_bytes(cu_seqlens ? N : 0, B, T, cu_seqlens != nullptr);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    int launches = 0;
+    kda::timing_begin(stream);
+    const cudaError_t e = kda::launch_la_fwd(q, k, v, slope, scale, initial_state, final_state, cu_seqlens,
+                                             cu_seqlens ? N : 0, B, T, H_qk, H_v, out, ws, stream, &launches);
+    int rc = e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    if (rc == KDA_OK) {
+        kda::timing_mark("la_fwd_kernel", stream);
+        t_last_launches = launches;
+    }
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
+    return rc;
+}
+
+int kda_la_decode(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const float *slope, float scale,
+                  float *state, int B, int H_qk, int H_v, int K, int V, kda_bf16_t *out, cudaStream_t stream) {
+    if (K != kda::KD || V != kda::KD) return KDA_ERR_UNSUPPORTED;
+    if (B < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0) {
+        t_last_launches = 0;
+        return KDA_OK;
+    }
+    if (!q || !k || !v || !slope || !state || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(state)) return KDA_ERR_INVALID_ARG;
+    kda::timing_begin(stream);
+    const cudaError_t e = kda::launch_la_decode(q, k, v, slope, scale, state, B, H_qk, H_v, out, stream);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    kda::timing_mark("la_decode_kernel", stream);
     t_last_launches = 1;
     return KDA_OK;
 }

@@ -1644,6 +1644,12 @@ static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 void timing_begin(cudaStream_t s);
 void timing_mark(const char *name, cudaStream_t s);
 
+cudaError_t launch_plan(const int32_t *cu, int N, int B, int T, SeqDesc *seqs, ChunkDesc *chunks, int *order,
+                        int *hdr, long long max_chunks, cudaStream_t stream) {
+    plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu, N, B, T, seqs, chunks, order, hdr, max_chunks);
+    return cudaGetLastError();
+}
+
 long long max_chunks_for(int N, int B, int T, bool varlen) {
     if (varlen) return (long long)T / CH + (long long)N + 1;
     return (long long)B * ((T + CH - 1) / CH);

@@ -1,0 +1,433 @@
+// Lightning attention forward: linear attention with a fixed per-head decay,
+// one fused chunked pass per (sequence, value head).
+//
+// Per sequence and value head h (state S in R^{V x K}, lambda = exp(-slope[h])):
+//   S_t = lambda S_{t-1} + v_t k_t^T,        o_t = scale S_t q_t.
+// Over a chunk of C = 64 rows starting from S_0, with Gam_r = -(r + 1) slope
+// (in-chunk log decay up to and including row r) and len rows:
+//   O   = scale [ (Q * exp(Gam)) S_0^T + P V ],   P[r][j] = exp(Gam_r - Gam_j) q_r.k_j  (j <= r)
+//   S_C = exp(Gam_len) S_0 + sum_r k_r (v_r exp(Gam_len - Gam_r))^T  (as V x K: Z^T)
+// The state update Z = K^T Vd does not depend on S_0, so the only serial step
+// from chunk to chunk is S <- exp(Gam_len) S + Z, one FMA per state element.
+//
+// One CTA per (sequence, value head): 16 epilogue warps keep S (fp32) in
+// registers, thread (k, column group) owning S[v][k] for 32 values of v; one
+// producer warp streams q, k, v chunks with TMA (three stages, zero fill past
+// the tensor) and issues the tcgen05 MMAs:
+//   A   Da = Q K^T                      (bf16, M = 64, N = 64,  K = 128)
+//   M3  Z  = K^T (Vd_hi + Vd_lo)        (bf16, M = 128, N = 128, K = 64; K and Vd MN-major)
+//   M12 Y  = Qg S^T + P V               (bf16, M = 64, N = 128; S and V MN-major)
+// Vd is split into two bf16 terms so the state update keeps ~16 bits; S and
+// Qg enter the output product rounded to bf16, like the output itself.
+// Every wait is bounded; a timeout records KDA_ERR_DEVICE_TIMEOUT and both
+// roles stop.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+cudaError_t launch_plan(const int32_t *cu, int N, int B, int T, SeqDesc *seqs, ChunkDesc *chunks, int *order,
+                        int *hdr, long long max_chunks, cudaStream_t stream);
+long long max_chunks_for(int N, int B, int T, bool varlen);
+
+constexpr int LA_EPI_WARPS = 16;
+constexpr int LA_EPI = LA_EPI_WARPS * 32;
+constexpr int LA_THREADS = LA_EPI + 32;   // + producer warp
+constexpr int LA_NST = 3;                 // load stages
+
+// A stage holds one chunk: Q, K, V as 64 rows x 128 bf16, each as two 8 KiB
+// 128-byte-swizzled atoms (channels 0..63, 64..127), the layout a TMA box of
+// 64 x 64 elements writes.  Row-major [row][channel] in this layout is at once
+// the K-major operand over channels and the MN-major operand over rows.
+constexpr uint32_t LA_STAGE = 49152;
+constexpr uint32_t LA_Q = 0, LA_K = 16384, LA_V = 32768;
+constexpr uint32_t LA_PB = LA_NST * LA_STAGE;   // 2 x 8 KiB   P [r][j] bf16, K-major
+constexpr uint32_t LA_VD = LA_PB + 16384;       // 2 x 16 KiB  Vd hi, lo (stage layout)
+constexpr uint32_t LA_SB = LA_VD + 32768;       // 32 KiB      S bf16, MN-major over v: 2 atoms of 16 KiB
+constexpr uint32_t LA_BAR = LA_SB + 32768;
+constexpr uint32_t LA_SLOT = LA_BAR + 128;
+constexpr uint32_t LA_FLAG = LA_BAR + 132;
+constexpr uint32_t LA_BYTES = LA_BAR + 256 + 1024;   // + alignment slack
+static_assert(LA_BYTES <= 232448, "lightning-attention shared memory exceeds 227 KiB");
+
+enum { LB_LD0 = 0, LB_A = LA_NST, LB_M3, LB_M12_0, LB_M12_1, LB_E1R, LB_SBR, LB_OUT0, LB_OUT1, LB_COUNT };
+static_assert(8 * LB_COUNT <= 128, "barrier area");
+
+struct LaParams {
+    const SeqDesc *seqs;
+    const int *order;
+    const int *hdr;
+    const float *slope;
+    float scale;
+    const float *init;
+    float *fin;
+    uint16_t *out;
+    int H_qk, H_v, nseq;
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];\n" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
+        : "memory");
+}
+
+// S (bf16) as the MN-major B operand of the output MMA: element (v, k) of the
+// 128 x 128 matrix; v atoms of 64 are 16 KiB apart (128 k rows each).
+__device__ __forceinline__ uint32_t la_sb_off(int v8, int k) {   // v8: 8-element group of v
+    return (uint32_t)((v8 >> 3) * 16384 + (k >> 3) * 1024 + (k & 7) * 128 + (((v8 & 7) ^ (k & 7)) << 4));
+}
+
+__global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_constant__ CUtensorMap tq,
+                                                               const __grid_constant__ CUtensorMap tk,
+                                                               const __grid_constant__ CUtensorMap tv,
+                                                               const LaParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    if (p.hdr[1] == 0) return;
+    const int h = blockIdx.x % p.H_v, rank = blockIdx.x / p.H_v;
+    if (rank >= p.nseq) return;
+    const int seq = p.order[rank];
+    const SeqDesc sd = p.seqs[seq];
+    const int n = sd.nchunk, hq = h / (p.H_v / p.H_qk);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t sbase = smem_u32(sm), bar = sbase + LA_BAR;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + LA_FLAG);
+
+    if (tid == 0) {
+        for (int i = 0; i < LB_E1R; ++i) mbar_init(bar + 8 * i, 1);
+        mbar_init(bar + 8 * LB_E1R, LA_EPI_WARPS);
+        mbar_init(bar + 8 * LB_SBR, LA_EPI_WARPS);
+        mbar_init(bar + 8 * LB_OUT0, LA_EPI_WARPS);
+        mbar_init(bar + 8 * LB_OUT1, LA_EPI_WARPS);
+        mbar_fence_init();
+        *abort_flag = 0;
+    }
+    if (warp == 0) tmem_alloc(sbase + LA_SLOT, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + LA_SLOT);
+    const uint32_t tZ = tmem, tDa = tmem + 384;   // Y[b] at tmem + 128 + 128 b
+    const float sl2 = p.slope[h] * LOG2E;         // decay per token, log2 units
+    auto fail = [&]() {
+        set_status(KDA_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+    };
+
+    if (warp == LA_EPI_WARPS) {
+        // ------------------------------------------------------------ producer / MMA issuer
+        if (lane == 0) {
+            auto load = [&](int c) {
+                const int s = c % LA_NST;
+                const uint32_t b = bar + 8 * (LB_LD0 + s), dst = sbase + s * LA_STAGE;
+                const int row = sd.tok + c * CH;
+                mbar_expect_tx(b, LA_STAGE);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    tma_load_3d(dst + LA_Q + half * 8192, &tq, 64 * half, hq, row, b);
+                    tma_load_3d(dst + LA_K + half * 8192, &tk, 64 * half, hq, row, b);
+                    tma_load_3d(dst + LA_V + half * 8192, &tv, 64 * half, h, row, b);
+                }
+            };
+            const uint32_t id_a = idesc_bf16(64, 64);
+            const uint32_t id_3 = idesc_bf16(128, 128) | (1u << 15) | (1u << 16);
+            const uint32_t id_12 = idesc_bf16(64, 128) | (1u << 16);
+            auto mma_a = [&](int c) {
+                const uint32_t st = sbase + (c % LA_NST) * LA_STAGE;
+#pragma unroll
+                for (int ks = 0; ks < KD / 16; ++ks) {
+                    const uint32_t o = (ks >> 2) * 8192 + (ks & 3) * 32;
+                    umma_bf16(tDa, umma_desc(st + LA_Q + o, 16, 1024), umma_desc(st + LA_K + o, 16, 1024), id_a,
+                              ks > 0 ? 1u : 0u);
+                }
+                umma_commit(bar + 8 * LB_A);
+            };
+            for (int c = 0; c < n && c < LA_NST; ++c) load(c);
+            bool ok = true;
+            if (n > 0) {
+                if (!mbar_wait(bar + 8 * LB_LD0, 0)) ok = false;
+                else {
+                    tc_fence_after();
+                    mma_a(0);
+                }
+            }
+            for (int c = 0; ok && c < n && !*abort_flag; ++c) {
+                const uint32_t st = sbase + (c % LA_NST) * LA_STAGE;
+                // M3: Vd of chunk c written (E1R #c) and Z read by the previous state update (SBR #c)
+                if (!mbar_wait(bar + 8 * LB_E1R, c & 1) || !mbar_wait(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int ks = 0; ks < CH / 16; ++ks)
+                        umma_bf16(tZ, umma_desc(st + LA_K + ks * 2048, 8192, 1024),
+                                  umma_desc(sbase + LA_VD + part * 16384 + ks * 2048, 8192, 1024), id_3,
+                                  (part > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(bar + 8 * LB_M3);
+                // M12: Y[c & 1] read out by the output of chunk c - 2
+                if (c >= 2 && !mbar_wait(bar + 8 * (LB_OUT0 + (c & 1)), ((c >> 1) - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tY = tmem + 128 + 128 * (c & 1);
+#pragma unroll
+                for (int ks = 0; ks < KD / 16; ++ks)
+                    umma_bf16(tY, umma_desc(st + LA_Q + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
+                              umma_desc(sbase + LA_SB + ks * 2048, 16384, 1024), id_12, ks > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < CH / 16; ++ks)
+                    umma_bf16(tY, umma_desc(sbase + LA_PB + (c & 1) * 8192 + ks * 32, 16, 1024),
+                              umma_desc(st + LA_V + ks * 2048, 8192, 1024), id_12, 1u);
+                umma_commit(bar + 8 * (LB_M12_0 + (c & 1)));
+                // A of the next chunk (Da was read by E1 of chunk c)
+                if (c + 1 < n) {
+                    if (!mbar_wait(bar + 8 * (LB_LD0 + (c + 1) % LA_NST), ((c + 1) / LA_NST) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    mma_a(c + 1);
+                }
+                // refill this stage once M3 and M12 of chunk c have read it
+                if (c + LA_NST < n) {
+                    if (!mbar_wait(bar + 8 * LB_M3, c & 1) ||
+                        !mbar_wait(bar + 8 * (LB_M12_0 + (c & 1)), (c >> 1) & 1)) { ok = false; break; }
+                    load(c + LA_NST);
+                }
+            }
+            if (!ok) fail();
+            if (*abort_flag) {
+                // let whatever is still in flight land before the CTA releases TMEM (bounded)
+                for (int i = 0; i < LB_E1R; ++i)
+                    for (uint32_t pp = 0; pp < 2; ++pp) mbar_wait(bar + 8 * i, pp, 1u << 14);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q4 = warp & 3, cg = warp >> 2;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const int kme = q4 * 32 + lane;   // state channel (Z lanes)
+        const int rme = q4 * 16 + lane;   // chunk row in the M = 64 accumulator layout (lanes < 16)
+        float S[32];                      // S[32 cg + j][kme]
+        const size_t st0 = (((size_t)seq * p.H_v + h) * KD + 32 * cg) * KD + kme;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[j] = p.init ? p.init[st0 + (size_t)j * KD] : 0.f;
+        auto write_sb = [&]() {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                uint4 w;
+                w.x = pack_bf16x2(S[8 * u + 0], S[8 * u + 1]);
+                w.y = pack_bf16x2(S[8 * u + 2], S[8 * u + 3]);
+                w.z = pack_bf16x2(S[8 * u + 4], S[8 * u + 5]);
+                w.w = pack_bf16x2(S[8 * u + 6], S[8 * u + 7]);
+                *reinterpret_cast<uint4 *>(sm + LA_SB + la_sb_off(4 * cg + u, kme)) = w;
+            }
+            fence_async_smem();
+        };
+        write_sb();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar + 8 * LB_SBR);
+
+        // E1 of chunk c: P from Da, Qg = Q exp(Gam_r) in place, Vd = V exp(Gam_len - Gam_r) (hi, lo)
+        auto e1 = [&](int c) -> bool {
+            const int s = c % LA_NST;
+            unsigned char *stg = sm + s * LA_STAGE;
+            const int len = min(CH, sd.len - c * CH);
+            if (!mbar_spin(bar + 8 * (LB_LD0 + s), (c / LA_NST) & 1) || !mbar_spin(bar + 8 * LB_A, c & 1)) return false;
+            if (c >= 1 && !mbar_spin(bar + 8 * LB_M3, (c - 1) & 1)) return false;                       // Vd free
+            if (c >= 2 && !mbar_spin(bar + 8 * (LB_M12_0 + (c & 1)), ((c >> 1) - 1) & 1)) return false;   // P free
+            tc_fence_after();
+            {
+                uint32_t x[16];
+                tmem_ld16_nowait(tDa + lane_off + 16 * cg, x);
+                tmem_wait_ld();
+                if (lane < 16) {
+                    float o[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = 16 * cg + e;
+                        o[e] = j <= rme ? __uint_as_float(x[e]) * ex2(-sl2 * (float)(rme - j)) : 0.f;
+                    }
+                    unsigned char *pb = sm + LA_PB + (c & 1) * 8192;
+#pragma unroll
+                    for (int hlf = 0; hlf < 2; ++hlf)
+                        *reinterpret_cast<uint4 *>(pb + sw128_off(rme, 32 * cg + 16 * hlf, CH)) =
+                            make_uint4(pack_bf16x2(o[8 * hlf + 0], o[8 * hlf + 1]), pack_bf16x2(o[8 * hlf + 2], o[8 * hlf + 3]),
+                                       pack_bf16x2(o[8 * hlf + 4], o[8 * hlf + 5]), pack_bf16x2(o[8 * hlf + 6], o[8 * hlf + 7]));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int u = tid + LA_EPI * i, r = u >> 4, c16 = u & 15;
+                const uint32_t off = sw128_off(r, 16 * c16, CH);
+                const float eq = ex2(-sl2 * (float)(r + 1));
+                const float ed = r < len ? ex2(-sl2 * (float)(len - 1 - r)) : 0.f;
+                const uint4 qw = *reinterpret_cast<const uint4 *>(stg + LA_Q + off);
+                const uint4 vw = *reinterpret_cast<const uint4 *>(stg + LA_V + off);
+                const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, va[4] = {vw.x, vw.y, vw.z, vw.w};
+                uint32_t qg[4], vh[4], vl[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    qg[e] = pack_bf16x2(bf16_lo(qa[e]) * eq, bf16_hi(qa[e]) * eq);
+                    const float d0 = bf16_lo(va[e]) * ed, d1 = bf16_hi(va[e]) * ed;
+                    vh[e] = pack_bf16x2(d0, d1);
+                    vl[e] = pack_bf16x2(d0 - bf16_lo(vh[e]), d1 - bf16_hi(vh[e]));
+                }
+                *reinterpret_cast<uint4 *>(stg + LA_Q + off) = make_uint4(qg[0], qg[1], qg[2], qg[3]);
+                *reinterpret_cast<uint4 *>(sm + LA_VD + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
+                *reinterpret_cast<uint4 *>(sm + LA_VD + 16384 + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + 8 * LB_E1R);
+            return true;
+        };
+        // E2 of chunk c: S <- exp(Gam_len) S + Z; S (bf16) for the next chunk's output MMA
+        auto e2 = [&](int c) -> bool {
+            const int len = min(CH, sd.len - c * CH);
+            if (!mbar_spin(bar + 8 * LB_M3, c & 1) || !mbar_spin(bar + 8 * (LB_M12_0 + (c & 1)), (c >> 1) & 1))
+                return false;
+            tc_fence_after();
+            const float g = ex2(-sl2 * (float)len);
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                uint32_t z[16];
+                tmem_ld16_nowait(tZ + lane_off + 32 * cg + 16 * hlf, z);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) S[16 * hlf + j] = fmaf(S[16 * hlf + j], g, __uint_as_float(z[j]));
+            }
+            write_sb();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + 8 * LB_SBR);
+            return true;
+        };
+        // output of chunk c: O = scale Y (rows rme, columns 32 cg ..)
+        auto emit = [&](int c) {
+            const int len = min(CH, sd.len - c * CH);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(sd.tok + c * CH + rme) * p.H_v + h) * KD + 32 * cg);
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                uint32_t y[16];
+                tmem_ld16_nowait(tmem + 128 + 128 * (c & 1) + lane_off + 32 * cg + 16 * hlf, y);
+                tmem_wait_ld();
+                if (lane < 16 && rme < len) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        dst[2 * hlf + u] = make_uint4(
+                            pack_bf16x2(p.scale * __uint_as_float(y[8 * u + 0]), p.scale * __uint_as_float(y[8 * u + 1])),
+                            pack_bf16x2(p.scale * __uint_as_float(y[8 * u + 2]), p.scale * __uint_as_float(y[8 * u + 3])),
+                            pack_bf16x2(p.scale * __uint_as_float(y[8 * u + 4]), p.scale * __uint_as_float(y[8 * u + 5])),
+                            pack_bf16x2(p.scale * __uint_as_float(y[8 * u + 6]), p.scale * __uint_as_float(y[8 * u + 7])));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + 8 * (LB_OUT0 + (c & 1)));
+        };
+        bool ok = n == 0 || e1(0);
+        for (int c = 0; ok && c < n; ++c) {
+            if (*abort_flag) { ok = false; break; }
+            if (c + 1 < n && !e1(c + 1)) { ok = false; break; }
+            if (!e2(c)) { ok = false; break; }
+            emit(c);
+        }
+        if (!ok) fail();
+        if (ok && p.fin) {
+            float *dst = p.fin + st0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[(size_t)j * KD] = S[j];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+cudaError_t get_encoder() {
+    if (g_encode) return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+// [rows][heads][128] bf16 as a 3-D tensor (channel, head, row), boxes of 64 channels x 1 head x 64 rows,
+// 128-byte swizzle, zero fill past the last row.
+cudaError_t make_map(CUtensorMap *m, const void *base, long long rows, int heads) {
+    const cuuint64_t dims[3] = {(cuuint64_t)KD, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)KD * 2, (cuuint64_t)heads * KD * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)CH};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+size_t align256_la(size_t x) { return (x + 255) & ~(size_t)255; }
+}  // namespace
+
+// Plan tables only: header, sequence table, chunk table, order.
+size_t la_workspace_bytes(int N, int B, int T, bool varlen) {
+    const long long nseq = varlen ? N : B;
+    const long long nck = max_chunks_for(N, B, T, varlen);
+    size_t off = align256_la(256);
+    off = align256_la(off + sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1));
+    off = align256_la(off + sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1));
+    off = align256_la(off + sizeof(int) * (size_t)(nseq > 0 ? nseq : 1));
+    return off;
+}
+
+cudaError_t launch_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *slope, float scale,
+                          const float *init, float *fin, const int32_t *cu, int N, int B, int T, int H_qk, int H_v,
+                          uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches) {
+    const bool varlen = cu != nullptr;
+    const int nseq = varlen ? N : B;
+    const long long nck = max_chunks_for(N, B, T, varlen);
+    char *base = static_cast<char *>(ws_ptr);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *p = base + off;
+        off = align256_la(off + bytes);
+        return p;
+    };
+    int *hdr = reinterpret_cast<int *>(take(256));
+    SeqDesc *seqs = reinterpret_cast<SeqDesc *>(take(sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1)));
+    ChunkDesc *chunks = reinterpret_cast<ChunkDesc *>(take(sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1)));
+    int *order = reinterpret_cast<int *>(take(sizeof(int) * (size_t)(nseq > 0 ? nseq : 1)));
+    *launches = 0;
+    cudaError_t e = launch_plan(cu, N, B, T, seqs, chunks, order, hdr, nck, stream);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if (nseq == 0) return cudaSuccess;
+    const long long rows = (long long)B * T;
+    CUtensorMap mq, mk, mv;
+    if ((e = get_encoder()) != cudaSuccess) return e;
+    // a map needs at least one row; with no tokens the kernel only copies the states
+    const void *qb = rows > 0 ? (const void *)q : (const void *)hdr;
+    const void *kb = rows > 0 ? (const void *)k : (const void *)hdr;
+    const void *vb = rows > 0 ? (const void *)v : (const void *)hdr;
+    const long long r = rows > 0 ? rows : 1;
+    if ((e = make_map(&mq, qb, r, rows > 0 ? H_qk : 1)) != cudaSuccess) return e;
+    if ((e = make_map(&mk, kb, r, rows > 0 ? H_qk : 1)) != cudaSuccess) return e;
+    if ((e = make_map(&mv, vb, r, rows > 0 ? H_v : 1)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(la_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LA_BYTES)) !=
+        cudaSuccess)
+        return e;
+    LaParams lp;
+    lp.seqs = seqs; lp.order = order; lp.hdr = hdr; lp.slope = slope; lp.scale = scale;
+    lp.init = init; lp.fin = fin; lp.out = out; lp.H_qk = H_qk; lp.H_v = H_v; lp.nseq = nseq;
+    la_fwd_kernel<<<(unsigned)((long long)nseq * H_v), LA_THREADS, LA_BYTES, stream>>>(mq, mk, mv, lp);
+    ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -67,6 +67,10 @@ def load() -> ctypes.CDLL:
     lib.kda_decode_step.restype = I
     lib.kda_decode_tokens.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, P, P]
     lib.kda_decode_tokens.restype = I
+    lib.kda_la_fwd.argtypes = [P, P, P, P, F, P, P, P, I, I, I, I, I, I, I, P, P]
+    lib.kda_la_fwd.restype = I
+    lib.kda_la_decode.argtypes = [P, P, P, P, F, P, I, I, I, I, I, P, P]
+    lib.kda_la_decode.restype = I
     lib.kda_status_string.argtypes = [I]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_get_status.argtypes = [P]
@@ -351,3 +355,54 @@ def kda_selftest_wait_timeout(stream=None) -> None:
     """Queue the self-test whose bounded device wait gives up and records
     KDA_ERR_DEVICE_TIMEOUT in the status word (see ``kda_get_status``)."""
     _raise(load().kda_selftest_wait_timeout(_stream(stream)), "kda_selftest_wait_timeout")
+
+
+def kda_la_fwd(q, k, v, slope, scale: float, initial_state=None, cu_seqlens=None,
+               output_final_state: bool = True, out=None, final_state=None,
+               stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Lightning-attention forward (fixed per-head decay exp(-slope[h])).
+    Shapes: q, k [B,T,H_qk,K]; v [B,T,H_v,V] (bf16); slope [H_v] fp32;
+    initial_state [N,H_v,V,K] fp32 or None; cu_seqlens int32 [N+1] (device) or
+    None.  Returns (out, final_state)."""
+    lib = load()
+    B, T, H_qk, K = q.shape
+    H_v, V = v.shape[2], v.shape[3]
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    bf = torch.bfloat16
+    _check(q, "q", bf, (B, T, H_qk, K))
+    _check(k, "k", bf, (B, T, H_qk, K))
+    _check(v, "v", bf, (B, T, H_v, V))
+    _check(slope, "slope", torch.float32, (H_v,))
+    _check(initial_state, "initial_state", torch.float32, (N, H_v, V, K), optional=True)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, optional=True)
+    if out is None:
+        out = torch.empty((B, T, H_v, V), dtype=bf, device=q.device)
+    _check(out, "out", bf, (B, T, H_v, V))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H_v, V, K), dtype=torch.float32, device=q.device)
+    _check(final_state, "final_state", torch.float32, (N, H_v, V, K), optional=True)
+    rc = lib.kda_la_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(slope), ctypes.c_float(scale), _ptr(initial_state),
+                        _ptr(final_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V, _ptr(out), _stream(stream))
+    _raise(rc, "kda_la_fwd")
+    return out, final_state
+
+
+def kda_la_decode(q, k, v, slope, scale: float, state, out=None, stream=None) -> torch.Tensor:
+    """One lightning-attention decode step; ``state`` [B,H_v,V,K] fp32 is
+    updated in place.  Shapes: q, k [B,H_qk,K]; v [B,H_v,V] (bf16); slope [H_v]."""
+    lib = load()
+    B, H_qk, K = q.shape
+    H_v, V = v.shape[1], v.shape[2]
+    bf = torch.bfloat16
+    _check(q, "q", bf, (B, H_qk, K))
+    _check(k, "k", bf, (B, H_qk, K))
+    _check(v, "v", bf, (B, H_v, V))
+    _check(slope, "slope", torch.float32, (H_v,))
+    _check(state, "state", torch.float32, (B, H_v, V, K))
+    if out is None:
+        out = torch.empty((B, H_v, V), dtype=bf, device=q.device)
+    _check(out, "out", bf, (B, H_v, V))
+    rc = lib.kda_la_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(slope), ctypes.c_float(scale), _ptr(state), B, H_qk,
+                           H_v, K, V, _ptr(out), _stream(stream))
+    _raise(rc, "kda_la_decode")
+    return out

@@ -208,6 +208,49 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
                     int N, int B, int T, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
                     cudaStream_t stream);
 
+/*
+ * Lightning attention: linear attention with a fixed per-head decay.  The cuLA
+ * page ("cuLA benchmark results on GB200") times a lightning-attention forward
+ * (fixed-length and varlen tables) and a single-token la_decode with 64 heads of
+ * dimension 128, and prints no formula; these calls compute the standard
+ * lightning-attention recurrence, per sequence and value head h with
+ * lambda = exp(-slope[h]):
+ *
+ *   S_t = lambda S_{t-1} + v_t k_t^T,      o_t = scale S_t q_t
+ *
+ * with q and k used as given (no normalisation) and no gate.
+ *
+ *   q, k   [B, T, H_qk, K] bf16        v, out [B, T, H_v, V] bf16
+ *   slope  [H_v] fp32 (decay rate per token; >= 0 for a decaying state)
+ *   initial_state / final_state [N, H_v, V, K] fp32, NULL for zeros / not written
+ *   cu_seqlens as kda_fwd (B = 1, N packed sequences), else B sequences of T
+ *
+ * K = V = 128 and H_v a multiple of H_qk (value head h reads q/k head
+ * h / (H_v / H_qk)); q, k, v and out 16-byte aligned.  One fused kernel per
+ * call (after the sequence plan) streams q, k, v once and writes out once; a
+ * few KB of plan tables come from cudaMallocAsync on `stream`.  Errors and
+ * asynchrony as kda_fwd (a malformed cu_seqlens sets KDA_ERR_BAD_SEQLENS in
+ * the status word and writes nothing).
+ */
+int kda_la_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const float *slope,
+               float scale, const float *initial_state, float *final_state,
+               const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V,
+               kda_bf16_t *out, cudaStream_t stream);
+
+/*
+ * One lightning-attention decode step (the la_decode of the same page) for B
+ * independent sequences:
+ *
+ *   q, k [B, H_qk, K] bf16   v [B, H_v, V] bf16   slope [H_v] fp32
+ *   state [B, H_v, V, K] fp32, updated in place   out [B, H_v, V] bf16
+ *
+ * Equal to kda_la_fwd with T = 1 and initial_state = final_state = state; one
+ * pass over the state.  Errors as kda_decode_step.
+ */
+int kda_la_decode(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const float *slope,
+                  float scale, float *state, int B, int H_qk, int H_v, int K, int V, kda_bf16_t *out,
+                  cudaStream_t stream);
+
 /* Self-test of the device-side failure path: queues one tiny kernel whose bounded
  * wait on a barrier that nothing completes gives up, recording
  * KDA_ERR_DEVICE_TIMEOUT in the status word (read it with kda_get_status); the
