@@ -6,19 +6,23 @@
 // Over a chunk of C = 64 rows starting from S_0, with Gam_r = -(r + 1) slope
 // (in-chunk log decay up to and including row r) and len rows:
 //   O   = scale [ (Q * exp(Gam)) S_0^T + P V ],   P[r][j] = exp(Gam_r - Gam_j) q_r.k_j  (j <= r)
-//   S_C = exp(Gam_len) S_0 + sum_r k_r (v_r exp(Gam_len - Gam_r))^T  (as V x K: Z^T)
-// The state update Z = K^T Vd does not depend on S_0, so the only serial step
+//   S_C = exp(Gam_len) S_0 + sum_r v_r (k_r exp(Gam_len - Gam_r))^T  (as Z[k][v] = (Kd^T V)[k][v])
+// The state update Z = Kd^T V does not depend on S_0, so the only serial step
 // from chunk to chunk is S <- exp(Gam_len) S + Z, one FMA per state element.
 //
 // One CTA per (sequence, value head): 16 epilogue warps keep S (fp32) in
-// registers, thread (k, column group) owning S[v][k] for 32 values of v; one
-// producer warp streams q, k, v chunks with TMA (three stages, zero fill past
-// the tensor) and issues the tcgen05 MMAs:
+// registers, thread (k, column group) owning S[v][k] for 32 values of v.  Two
+// issuer threads (one lane of each of two more warps) drive the tensor core,
+// since one thread issues at most one MMA every ~65 cycles: the state issuer
+// streams q, k, v chunks with TMA (three stages, zero fill past the tensor) and
+// issues A and M3; the output issuer issues M12.  The MMAs:
 //   A   Da = Q K^T                      (bf16, M = 64, N = 64,  K = 128)
-//   M3  Z  = K^T (Vd_hi + Vd_lo)        (bf16, M = 128, N = 128, K = 64; K and Vd MN-major)
+//   M3  Z  = (Kd_hi + Kd_lo)^T V        (bf16, M = 128, N = 128, K = 64; Kd and V MN-major)
 //   M12 Y  = Qg S^T + P V               (bf16, M = 64, N = 128; S and V MN-major)
-// Vd is split into two bf16 terms so the state update keeps ~16 bits; S and
-// Qg enter the output product rounded to bf16, like the output itself.
+// Once A has read a stage, the epilogue rewrites its Q rows as Qg and its K
+// rows as Kd_hi in place (Kd_lo goes to a double buffer).  Kd is split into
+// two bf16 terms so the state update keeps ~16 bits; S and Qg enter the
+// output product rounded to bf16, like the output itself.
 // Every wait is bounded; a timeout records KDA_ERR_DEVICE_TIMEOUT and both
 // roles stop.
 #include <cuda.h>
@@ -34,7 +38,7 @@ long long max_chunks_for(int N, int B, int T, bool varlen);
 
 constexpr int LA_EPI_WARPS = 16;
 constexpr int LA_EPI = LA_EPI_WARPS * 32;
-constexpr int LA_THREADS = LA_EPI + 32;   // + producer warp
+constexpr int LA_THREADS = LA_EPI + 64;   // + two issuer warps
 constexpr int LA_NST = 3;                 // load stages
 
 // A stage holds one chunk: Q, K, V as 64 rows x 128 bf16, each as two 8 KiB
@@ -44,15 +48,15 @@ constexpr int LA_NST = 3;                 // load stages
 constexpr uint32_t LA_STAGE = 49152;
 constexpr uint32_t LA_Q = 0, LA_K = 16384, LA_V = 32768;
 constexpr uint32_t LA_PB = LA_NST * LA_STAGE;   // 2 x 8 KiB   P [r][j] bf16, K-major
-constexpr uint32_t LA_VD = LA_PB + 16384;       // 2 x 16 KiB  Vd hi, lo (stage layout)
-constexpr uint32_t LA_SB = LA_VD + 32768;       // 32 KiB      S bf16, MN-major over v: 2 atoms of 16 KiB
+constexpr uint32_t LA_KL = LA_PB + 16384;       // 2 x 16 KiB  Kd_lo (stage layout)
+constexpr uint32_t LA_SB = LA_KL + 32768;       // 32 KiB      S bf16, MN-major over v: 2 atoms of 16 KiB
 constexpr uint32_t LA_BAR = LA_SB + 32768;
 constexpr uint32_t LA_SLOT = LA_BAR + 128;
 constexpr uint32_t LA_FLAG = LA_BAR + 132;
 constexpr uint32_t LA_BYTES = LA_BAR + 256 + 1024;   // + alignment slack
 static_assert(LA_BYTES <= 232448, "lightning-attention shared memory exceeds 227 KiB");
 
-enum { LB_LD0 = 0, LB_A = LA_NST, LB_M3, LB_M12_0, LB_M12_1, LB_E1R, LB_SBR, LB_OUT0, LB_OUT1, LB_COUNT };
+enum { LB_LD0 = 0, LB_A = LA_NST, LB_M3, LB_M12_0, LB_M12_1, LB_E1R0, LB_E1R1, LB_SBR, LB_OUT0, LB_OUT1, LB_COUNT };
 static_assert(8 * LB_COUNT <= 128, "barrier area");
 
 struct LaParams {
@@ -98,8 +102,9 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + LA_FLAG);
 
     if (tid == 0) {
-        for (int i = 0; i < LB_E1R; ++i) mbar_init(bar + 8 * i, 1);
-        mbar_init(bar + 8 * LB_E1R, LA_EPI_WARPS);
+        for (int i = 0; i < LB_E1R0; ++i) mbar_init(bar + 8 * i, 1);
+        mbar_init(bar + 8 * LB_E1R0, LA_EPI_WARPS);
+        mbar_init(bar + 8 * LB_E1R1, LA_EPI_WARPS);
         mbar_init(bar + 8 * LB_SBR, LA_EPI_WARPS);
         mbar_init(bar + 8 * LB_OUT0, LA_EPI_WARPS);
         mbar_init(bar + 8 * LB_OUT1, LA_EPI_WARPS);
@@ -118,9 +123,20 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         *abort_flag = 1;
     };
 
-    if (warp == LA_EPI_WARPS) {
-        // ------------------------------------------------------------ producer / MMA issuer
-        if (lane == 0) {
+    if (warp >= LA_EPI_WARPS) {
+        // ------------------------------------------------------------ issuers (one lane each)
+        const uint32_t id_a = idesc_bf16(64, 64);
+        const uint32_t id_3 = idesc_bf16(128, 128) | (1u << 15) | (1u << 16);
+        const uint32_t id_12 = idesc_bf16(64, 128) | (1u << 16);
+        // descriptors of stage 0 / buffer 0; other operands add (byte offset >> 4) to the address field
+        const uint64_t dQ = umma_desc(sbase + LA_Q, 16, 1024), dK = umma_desc(sbase + LA_K, 16, 1024);
+        const uint64_t dKm = umma_desc(sbase + LA_K, 8192, 1024), dV = umma_desc(sbase + LA_V, 8192, 1024);
+        const uint64_t dKL = umma_desc(sbase + LA_KL, 8192, 1024), dPB = umma_desc(sbase + LA_PB, 16, 1024);
+        const uint64_t dSB = umma_desc(sbase + LA_SB, 16384, 1024);
+        auto stg = [](int c) { return (uint64_t)((c % LA_NST) * (LA_STAGE >> 4)); };
+        bool ok = true;
+        if (lane == 0 && warp == LA_EPI_WARPS) {
+            // ---- state issuer: loads, A (Da = Q K^T), M3 (Z = Kd^T V)
             auto load = [&](int c) {
                 const int s = c % LA_NST;
                 const uint32_t b = bar + 8 * (LB_LD0 + s), dst = sbase + s * LA_STAGE;
@@ -133,21 +149,16 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                     tma_load_3d(dst + LA_V + half * 8192, &tv, 64 * half, h, row, b);
                 }
             };
-            const uint32_t id_a = idesc_bf16(64, 64);
-            const uint32_t id_3 = idesc_bf16(128, 128) | (1u << 15) | (1u << 16);
-            const uint32_t id_12 = idesc_bf16(64, 128) | (1u << 16);
             auto mma_a = [&](int c) {
-                const uint32_t st = sbase + (c % LA_NST) * LA_STAGE;
+                const uint64_t o = stg(c);
 #pragma unroll
                 for (int ks = 0; ks < KD / 16; ++ks) {
-                    const uint32_t o = (ks >> 2) * 8192 + (ks & 3) * 32;
-                    umma_bf16(tDa, umma_desc(st + LA_Q + o, 16, 1024), umma_desc(st + LA_K + o, 16, 1024), id_a,
-                              ks > 0 ? 1u : 0u);
+                    const uint32_t kb = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+                    umma_bf16(tDa, dQ + o + kb, dK + o + kb, id_a, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(bar + 8 * LB_A);
             };
             for (int c = 0; c < n && c < LA_NST; ++c) load(c);
-            bool ok = true;
             if (n > 0) {
                 if (!mbar_wait(bar + 8 * LB_LD0, 0)) ok = false;
                 else {
@@ -156,37 +167,24 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                 }
             }
             for (int c = 0; ok && c < n && !*abort_flag; ++c) {
-                const uint32_t st = sbase + (c % LA_NST) * LA_STAGE;
-                // M3: Vd of chunk c written (E1R #c) and Z read by the previous state update (SBR #c)
-                if (!mbar_wait(bar + 8 * LB_E1R, c & 1) || !mbar_wait(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
+                const uint64_t o = stg(c);
+                // E1 of chunk c is done: Da is free, so A of the next chunk goes first
+                if (!mbar_spin(bar + 8 * (LB_E1R0 + (c & 1)), (c >> 1) & 1)) { ok = false; break; }
+                if (c + 1 < n) {
+                    if (!mbar_spin(bar + 8 * (LB_LD0 + (c + 1) % LA_NST), ((c + 1) / LA_NST) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    mma_a(c + 1);
+                }
+                // M3: Z was read by the previous state update (SBR #c)
+                if (!mbar_spin(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < CH / 16; ++ks)
-                        umma_bf16(tZ, umma_desc(st + LA_K + ks * 2048, 8192, 1024),
-                                  umma_desc(sbase + LA_VD + part * 16384 + ks * 2048, 8192, 1024), id_3,
-                                  (part > 0 || ks > 0) ? 1u : 0u);
+                        umma_bf16(tZ, (part ? dKL + (uint64_t)((c & 1) * (16384 >> 4)) : dKm + o) + ks * (2048 >> 4),
+                                  dV + o + ks * (2048 >> 4), id_3, (part > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(bar + 8 * LB_M3);
-                // M12: Y[c & 1] read out by the output of chunk c - 2
-                if (c >= 2 && !mbar_wait(bar + 8 * (LB_OUT0 + (c & 1)), ((c >> 1) - 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t tY = tmem + 128 + 128 * (c & 1);
-#pragma unroll
-                for (int ks = 0; ks < KD / 16; ++ks)
-                    umma_bf16(tY, umma_desc(st + LA_Q + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024),
-                              umma_desc(sbase + LA_SB + ks * 2048, 16384, 1024), id_12, ks > 0 ? 1u : 0u);
-#pragma unroll
-                for (int ks = 0; ks < CH / 16; ++ks)
-                    umma_bf16(tY, umma_desc(sbase + LA_PB + (c & 1) * 8192 + ks * 32, 16, 1024),
-                              umma_desc(st + LA_V + ks * 2048, 8192, 1024), id_12, 1u);
-                umma_commit(bar + 8 * (LB_M12_0 + (c & 1)));
-                // A of the next chunk (Da was read by E1 of chunk c)
-                if (c + 1 < n) {
-                    if (!mbar_wait(bar + 8 * (LB_LD0 + (c + 1) % LA_NST), ((c + 1) / LA_NST) & 1)) { ok = false; break; }
-                    tc_fence_after();
-                    mma_a(c + 1);
-                }
                 // refill this stage once M3 and M12 of chunk c have read it
                 if (c + LA_NST < n) {
                     if (!mbar_wait(bar + 8 * LB_M3, c & 1) ||
@@ -194,10 +192,32 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                     load(c + LA_NST);
                 }
             }
+        } else if (lane == 0) {
+            // ---- output issuer: M12 (Y = P V, then += Qg S^T once S of the previous chunk is written)
+            for (int c = 0; ok && c < n && !*abort_flag; ++c) {
+                const uint64_t o = stg(c);
+                if (!mbar_spin(bar + 8 * (LB_LD0 + c % LA_NST), (c / LA_NST) & 1) ||
+                    !mbar_spin(bar + 8 * (LB_E1R0 + (c & 1)), (c >> 1) & 1)) { ok = false; break; }
+                if (c >= 2 && !mbar_spin(bar + 8 * (LB_OUT0 + (c & 1)), ((c >> 1) - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t tY = tmem + 128 + 128 * (c & 1);
+#pragma unroll
+                for (int ks = 0; ks < CH / 16; ++ks)
+                    umma_bf16(tY, dPB + (uint64_t)((c & 1) * (8192 >> 4) + ks * 2), dV + o + ks * (2048 >> 4), id_12,
+                              ks > 0 ? 1u : 0u);
+                if (!mbar_spin(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < KD / 16; ++ks)
+                    umma_bf16(tY, dQ + o + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), dSB + ks * (2048 >> 4), id_12, 1u);
+                umma_commit(bar + 8 * (LB_M12_0 + (c & 1)));
+            }
+        }
+        if (lane == 0) {
             if (!ok) fail();
             if (*abort_flag) {
                 // let whatever is still in flight land before the CTA releases TMEM (bounded)
-                for (int i = 0; i < LB_E1R; ++i)
+                for (int i = 0; i < LB_E1R0; ++i)
                     for (uint32_t pp = 0; pp < 2; ++pp) mbar_wait(bar + 8 * i, pp, 1u << 14);
             }
         }
@@ -227,14 +247,14 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         __syncwarp();
         if (lane == 0) mbar_arrive(bar + 8 * LB_SBR);
 
-        // E1 of chunk c: P from Da, Qg = Q exp(Gam_r) in place, Vd = V exp(Gam_len - Gam_r) (hi, lo)
+        // E1 of chunk c: P from Da; Qg = Q exp(Gam_r) and Kd = K exp(Gam_len - Gam_r) (hi in place, lo
+        // in its buffer).  P[c & 1] and Kd_lo[c & 1] were last read by M12 / M3 of chunk c - 2, which the
+        // state update of chunk c - 2 waited for, earlier in program order.
         auto e1 = [&](int c) -> bool {
             const int s = c % LA_NST;
             unsigned char *stg = sm + s * LA_STAGE;
             const int len = min(CH, sd.len - c * CH);
-            if (!mbar_spin(bar + 8 * (LB_LD0 + s), (c / LA_NST) & 1) || !mbar_spin(bar + 8 * LB_A, c & 1)) return false;
-            if (c >= 1 && !mbar_spin(bar + 8 * LB_M3, (c - 1) & 1)) return false;                       // Vd free
-            if (c >= 2 && !mbar_spin(bar + 8 * (LB_M12_0 + (c & 1)), ((c >> 1) - 1) & 1)) return false;   // P free
+            if (!mbar_wait(bar + 8 * (LB_LD0 + s), (c / LA_NST) & 1) || !mbar_wait(bar + 8 * LB_A, c & 1)) return false;
             tc_fence_after();
             {
                 uint32_t x[16];
@@ -262,30 +282,30 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                 const float eq = ex2(-sl2 * (float)(r + 1));
                 const float ed = r < len ? ex2(-sl2 * (float)(len - 1 - r)) : 0.f;
                 const uint4 qw = *reinterpret_cast<const uint4 *>(stg + LA_Q + off);
-                const uint4 vw = *reinterpret_cast<const uint4 *>(stg + LA_V + off);
-                const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, va[4] = {vw.x, vw.y, vw.z, vw.w};
-                uint32_t qg[4], vh[4], vl[4];
+                const uint4 kw = *reinterpret_cast<const uint4 *>(stg + LA_K + off);
+                const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, ka[4] = {kw.x, kw.y, kw.z, kw.w};
+                uint32_t qg[4], kh[4], kl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     qg[e] = pack_bf16x2(bf16_lo(qa[e]) * eq, bf16_hi(qa[e]) * eq);
-                    const float d0 = bf16_lo(va[e]) * ed, d1 = bf16_hi(va[e]) * ed;
-                    vh[e] = pack_bf16x2(d0, d1);
-                    vl[e] = pack_bf16x2(d0 - bf16_lo(vh[e]), d1 - bf16_hi(vh[e]));
+                    const float d0 = bf16_lo(ka[e]) * ed, d1 = bf16_hi(ka[e]) * ed;
+                    kh[e] = pack_bf16x2(d0, d1);
+                    kl[e] = pack_bf16x2(d0 - bf16_lo(kh[e]), d1 - bf16_hi(kh[e]));
                 }
                 *reinterpret_cast<uint4 *>(stg + LA_Q + off) = make_uint4(qg[0], qg[1], qg[2], qg[3]);
-                *reinterpret_cast<uint4 *>(sm + LA_VD + off) = make_uint4(vh[0], vh[1], vh[2], vh[3]);
-                *reinterpret_cast<uint4 *>(sm + LA_VD + 16384 + off) = make_uint4(vl[0], vl[1], vl[2], vl[3]);
+                *reinterpret_cast<uint4 *>(stg + LA_K + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
+                *reinterpret_cast<uint4 *>(sm + LA_KL + (c & 1) * 16384 + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
             }
             fence_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar + 8 * LB_E1R);
+            if (lane == 0) mbar_arrive(bar + 8 * (LB_E1R0 + (c & 1)));
             return true;
         };
         // E2 of chunk c: S <- exp(Gam_len) S + Z; S (bf16) for the next chunk's output MMA
         auto e2 = [&](int c) -> bool {
             const int len = min(CH, sd.len - c * CH);
-            if (!mbar_spin(bar + 8 * LB_M3, c & 1) || !mbar_spin(bar + 8 * (LB_M12_0 + (c & 1)), (c >> 1) & 1))
+            if (!mbar_wait(bar + 8 * LB_M3, c & 1) || !mbar_wait(bar + 8 * (LB_M12_0 + (c & 1)), (c >> 1) & 1))
                 return false;
             tc_fence_after();
             const float g = ex2(-sl2 * (float)len);

@@ -1,10 +1,11 @@
-"""Run the KDA forward a few times on one seeded workload, for profilers.
+"""Run the KDA (or lightning-attention) forward a few times on one seeded workload, for profilers.
 
     python -m gated_delta_rule_40_gb300.profile_case --B 1 --T 8192 --H 32 --iters 4
+    python -m gated_delta_rule_40_gb300.profile_case --method la --B 1 --T 8192 --H 64 --iters 4
 
 Inputs come from ``kda_inputs`` (same recipe as the tests and the benchmark);
 the workspace is allocated once, so every iteration is exactly the three
-kernel launches of ``kda_fwd``.  A profiler then selects launches by kernel
+kernel launches of ``kda_fwd`` (two for ``kda_la_fwd``: plan and la_fwd_kernel).  A profiler then selects launches by kernel
 name and index (e.g. ``ncu -k regex:intra_kernel -s 2 -c 1``).
 """
 import argparse
@@ -25,7 +26,17 @@ def main() -> None:
     ap.add_argument("--H", type=int, default=32, help="value heads (= q/k heads)")
     ap.add_argument("--iters", type=int, default=4)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--method", choices=["kda", "la"], default="kda")
     a = ap.parse_args()
+    if a.method == "la":
+        x = kda_inputs.make_la_inputs(a.B, a.T, a.H, a.H, seed=a.seed)
+        q, k, v, sl, s0 = (t.cuda() for t in (x.q, x.k, x.v, x.slope, x.initial_state))
+        for _ in range(a.iters):
+            out, fin = kda.kda_la_fwd(q, k, v, sl, x.scale, initial_state=s0)
+        torch.cuda.synchronize()
+        print(f"kda_la_fwd B={a.B} T={a.T} H={a.H} x{a.iters}: |out| {float(out.float().abs().mean()):.6f} "
+              f"|S| {float(fin.abs().mean()):.6f}")
+        return
     x = kda_inputs.make_inputs(B=a.B, T=a.T, H_qk=a.H, H_v=a.H, seed=a.seed, with_state=True)
     dev = lambda t: t.cuda() if t is not None else None  # noqa: E731
     q, k, v, g, b, A, s0 = map(dev, (x.q, x.k, x.v, x.graw, x.b, x.A_log, x.initial_state))
