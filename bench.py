@@ -345,7 +345,7 @@ def run_gpu(args, rank, world, local):
     sg_units = sg.token_heads()
     ntok = sg.q.shape[0] * sg.q.shape[1]
     sg_bytes = (ntok * sg.H_qk * 2 * 256 + ntok * sg.H_v * (256 + 2 + 2 + 256)
-                + 2 * sg.N * sg.H_v * STATE_BYTES_PER_SEQ_HEAD)
+                + sg.N * sg.H_v * STATE_BYTES_PER_SEQ_HEAD)
     del sd, sg_g, sg_out, sg_fin
 
     # ---- decode (B=256, H=64): state GB/s against HBM
@@ -386,6 +386,51 @@ def run_gpu(args, rank, world, local):
                                              "GB/s": mbytes / (mms * 1e-3) / 1e9}
         del md, mst, mout
 
+    # ---- lightning attention (fixed per-head decay): forward on the dense and varlen workloads
+    # (kda_la_fwd) and the single-token step at B=256, H=64 (kda_la_decode)
+    lightning = {}
+    for wname in ("la_dense", "la_varlen"):
+        la = KI.la_workload(wname, seed=rank)
+        ld = {n: getattr(la, n).to(dev) for n in ("q", "k", "v", "slope", "initial_state")}
+        lcu = None if la.cu_seqlens is None else la.cu_seqlens.to(dev)
+        lout = torch.empty_like(ld["v"])
+        lfin = torch.empty_like(ld["initial_state"])
+
+        def la_step():
+            kda.kda_la_fwd(ld["q"], ld["k"], ld["v"], ld["slope"], la.scale, initial_state=ld["initial_state"],
+                           cu_seqlens=lcu, out=lout, final_state=lfin, stream=stream)
+
+        for _ in range(3):
+            la_step()
+        torch.cuda.synchronize()
+        la_ms = time_events(la_step, 10, stream)
+        ntok = la.B * la.T
+        la_bytes = ntok * (2 * la.H_qk + 2 * la.H_v) * 256 + la.N * la.H_v * STATE_BYTES_PER_SEQ_HEAD
+        lightning[wname] = {"B": la.B, "T": la.T, "N": la.N, "H": la.H_v, "ms": la_ms,
+                            "value": la.token_heads() / (la_ms * 1e-3), "unit": UNIT,
+                            "algorithmic_bytes": la_bytes, "GB/s": la_bytes / (la_ms * 1e-3) / 1e9,
+                            "hbm_peak": hbm_peak, "frac": la_bytes / (la_ms * 1e-3) / 1e9 / hbm_peak}
+        del ld, lout, lfin
+    lad = KI.la_decode_inputs(B=256, H=64, seed=rank)
+    ldd = {n: getattr(lad, n).to(dev) for n in ("q", "k", "v", "slope", "state")}
+    ldout = torch.empty((256, 64, 128), dtype=torch.bfloat16, device=dev)
+
+    def la_dec_step():
+        kda.kda_la_decode(ldd["q"], ldd["k"], ldd["v"], ldd["slope"], lad.scale, ldd["state"], out=ldout,
+                          stream=stream)
+
+    for _ in range(5):
+        la_dec_step()
+    torch.cuda.synchronize()
+    la_dec_ms = time_events(la_dec_step, 50, stream)
+    la_dec_bytes = 256 * 64 * (2 * 128 * 128 * 4 + 3 * 256)
+    lightning["la_decode"] = {"B": 256, "H": 64, "ms": la_dec_ms, "GB/s": la_dec_bytes / (la_dec_ms * 1e-3) / 1e9,
+                              "hbm_peak": hbm_peak, "frac": la_dec_bytes / (la_dec_ms * 1e-3) / 1e9 / hbm_peak}
+    del ldd, ldout
+    status = kda.kda_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status after the side measurements: {kda.status_string(status)}")
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp)
@@ -422,6 +467,8 @@ def run_gpu(args, rank, world, local):
         "decode_tokens": {"workload": "B=256 H=64 K=V=128, Tq tokens per pass, state in place", **multi},
         "decode": {"workload": "B=256 H=64 K=V=128 fp32 state in place", "ms": dec_ms, "GB/s": dec_gbs,
                    "hbm_peak": hbm_peak, "frac": dec_gbs / hbm_peak},
+        "lightning": {"method": "linear attention with a fixed per-head decay (lightning attention)",
+                      "slopes": "2^(-8 (h+1) / H)", **lightning},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -250,6 +250,15 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         // E1 of chunk c: P from Da; Qg = Q exp(Gam_r) and Kd = K exp(Gam_len - Gam_r) (hi in place, lo
         // in its buffer).  P[c & 1] and Kd_lo[c & 1] were last read by M12 / M3 of chunk c - 2, which the
         // state update of chunk c - 2 waited for, earlier in program order.
+        // row decays of this thread's two 16-byte units (rows tid / 16 and tid / 16 + 32): exp(Gam_r)
+        // and, for full chunks, exp(Gam_63 - Gam_r)
+        float eqr[2], edr[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = (tid >> 4) + 32 * i;
+            eqr[i] = ex2(-sl2 * (float)(r + 1));
+            edr[i] = ex2(-sl2 * (float)(CH - 1 - r));
+        }
         auto e1 = [&](int c) -> bool {
             const int s = c % LA_NST;
             unsigned char *stg = sm + s * LA_STAGE;
@@ -257,17 +266,26 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             if (!mbar_wait(bar + 8 * (LB_LD0 + s), (c / LA_NST) & 1) || !mbar_wait(bar + 8 * LB_A, c & 1)) return false;
             tc_fence_after();
             {
-                uint32_t x[16];
-                tmem_ld16_nowait(tDa + lane_off + 16 * cg, x);
-                tmem_wait_ld();
-                if (lane < 16) {
-                    float o[16];
+                // P block (rows 16 q4 .., columns 16 cg ..): zero above the diagonal block, decay
+                // lambda^(r - j) = 2^(-sl2 (r - 16 cg) + sl2 e) below it, masked on it
+                unsigned char *pb = sm + LA_PB + (c & 1) * 8192;
+                float o[16];
+                if (cg > q4) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int j = 16 * cg + e;
-                        o[e] = j <= rme ? __uint_as_float(x[e]) * ex2(-sl2 * (float)(rme - j)) : 0.f;
+                    for (int e = 0; e < 16; ++e) o[e] = 0.f;
+                } else {
+                    uint32_t x[16];
+                    tmem_ld16_nowait(tDa + lane_off + 16 * cg, x);
+                    tmem_wait_ld();
+                    const float c0 = -sl2 * (float)(rme - 16 * cg);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = __uint_as_float(x[e]) * ex2(fmaf(sl2, (float)e, c0));
+                    if (cg == q4) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) o[e] = e <= lane ? o[e] : 0.f;
                     }
-                    unsigned char *pb = sm + LA_PB + (c & 1) * 8192;
+                }
+                if (lane < 16) {
 #pragma unroll
                     for (int hlf = 0; hlf < 2; ++hlf)
                         *reinterpret_cast<uint4 *>(pb + sw128_off(rme, 32 * cg + 16 * hlf, CH)) =
@@ -279,8 +297,8 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             for (int i = 0; i < 2; ++i) {
                 const int u = tid + LA_EPI * i, r = u >> 4, c16 = u & 15;
                 const uint32_t off = sw128_off(r, 16 * c16, CH);
-                const float eq = ex2(-sl2 * (float)(r + 1));
-                const float ed = r < len ? ex2(-sl2 * (float)(len - 1 - r)) : 0.f;
+                const float eq = eqr[i];
+                const float ed = len == CH ? edr[i] : (r < len ? ex2(-sl2 * (float)(len - 1 - r)) : 0.f);
                 const uint4 qw = *reinterpret_cast<const uint4 *>(stg + LA_Q + off);
                 const uint4 kw = *reinterpret_cast<const uint4 *>(stg + LA_K + off);
                 const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, ka[4] = {kw.x, kw.y, kw.z, kw.w};
