@@ -5,26 +5,29 @@
 //   S_t = lambda S_{t-1} + v_t k_t^T,        o_t = scale S_t q_t.
 // Over a chunk of C = 64 rows starting from S_0, with Gam_r = -(r + 1) slope
 // (in-chunk log decay up to and including row r) and len rows:
-//   O   = scale [ (Q * exp(Gam)) S_0^T + P V ],   P[r][j] = exp(Gam_r - Gam_j) q_r.k_j  (j <= r)
-//   S_C = exp(Gam_len) S_0 + sum_r v_r (k_r exp(Gam_len - Gam_r))^T  (as Z[k][v] = (Kd^T V)[k][v])
-// The state update Z = Kd^T V does not depend on S_0, so the only serial step
-// from chunk to chunk is S <- exp(Gam_len) S + Z, one FMA per state element.
+//   O[r] = scale [ exp(Gam_r) (S_0 q_r) + sum_{j<=r} P[r][j] v_j ],   P[r][j] = exp(Gam_r - Gam_j) q_r.k_j
+//   S_C  = exp(Gam_len) S_0 + Z^T,   Z^T[v][k] = sum_r v_r[v] k_r[k] exp(Gam_len - Gam_r)
+// Z does not depend on S_0, so the only serial step from chunk to chunk is
+// S <- exp(Gam_len) S + Z^T, one FMA per state element.
 //
-// One CTA per (sequence, value head): 16 epilogue warps keep S (fp32) in
-// registers, thread (k, column group) owning S[v][k] for 32 values of v.  Two
-// issuer threads (one lane of each of two more warps) drive the tensor core,
-// since one thread issues at most one MMA every ~65 cycles: the state issuer
-// streams q, k, v chunks with TMA (three stages, zero fill past the tensor) and
-// issues A and M3; the output issuer issues M12.  The MMAs:
-//   A   Da = Q K^T                      (bf16, M = 64, N = 64,  K = 128)
-//   M3  Z  = (Kd_hi + Kd_lo)^T V        (bf16, M = 128, N = 128, K = 64; Kd and V MN-major)
-//   M12 Y  = Qg S^T + P V               (bf16, M = 64, N = 128; S and V MN-major)
-// Once A has read a stage, the epilogue rewrites its Q rows as Qg and its K
-// rows as Kd_hi in place (Kd_lo goes to a double buffer).  Kd is split into
-// two bf16 terms so the state update keeps ~16 bits; S and Qg enter the
-// output product rounded to bf16, like the output itself.
-// Every wait is bounded; a timeout records KDA_ERR_DEVICE_TIMEOUT and both
-// roles stop.
+// One CTA per (sequence, value head).  16 epilogue warps keep S (fp32) in
+// registers, thread (v, column group) owning S[v][k] for 32 values of k, and
+// keep a bf16 copy of S in tensor memory as the A operand of the output MMA.
+// Two issuer threads (one lane of each of two more warps) drive the tensor
+// core, since one thread issues at most one MMA every ~65 cycles: the state
+// issuer streams q, k, v chunks with TMA (three stages, zero fill past the
+// tensor) and issues A and M3; the output issuer issues M2 and M1:
+//   A   Da   = Q K^T                  (M = 64,  N = 64, K = 128; A, B from shared memory)
+//   M3  Z^T  = V^T (Kd_hi + Kd_lo)     (M = 128, N = 128, K = 64; V and Kd MN-major)
+//   M2  Y2^T = V^T P^T                 (M = 128, N = 64,  K = 64)
+//   M1  Y1^T = S Q^T                   (M = 128, N = 64,  K = 128; S from tensor memory)
+// All bf16 with fp32 accumulation.  Once A has read a stage, the epilogue
+// rewrites its K rows in place as Kd_hi = bf16(k exp(Gam_len - Gam_r)) and
+// stores the remainder Kd_lo in a double buffer, so the state update keeps
+// ~16 bits; S and P enter the output products rounded to bf16, like the output
+// itself.  The output O = scale (exp(Gam_r) Y1 + Y2) is transposed through
+// shared memory and written with 16-byte stores.  Every wait is bounded; a
+// timeout records KDA_ERR_DEVICE_TIMEOUT and all roles stop.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -49,12 +52,15 @@ constexpr uint32_t LA_STAGE = 49152;
 constexpr uint32_t LA_Q = 0, LA_K = 16384, LA_V = 32768;
 constexpr uint32_t LA_PB = LA_NST * LA_STAGE;   // 2 x 8 KiB   P [r][j] bf16, K-major
 constexpr uint32_t LA_KL = LA_PB + 16384;       // 2 x 16 KiB  Kd_lo (stage layout)
-constexpr uint32_t LA_SB = LA_KL + 32768;       // 32 KiB      S bf16, MN-major over v: 2 atoms of 16 KiB
-constexpr uint32_t LA_BAR = LA_SB + 32768;
+constexpr uint32_t LA_OS = LA_KL + 32768;       // 2 x 16 KiB  output staging, bf16 [64 r][128 v]
+constexpr uint32_t LA_BAR = LA_OS + 32768;
 constexpr uint32_t LA_SLOT = LA_BAR + 128;
 constexpr uint32_t LA_FLAG = LA_BAR + 132;
 constexpr uint32_t LA_BYTES = LA_BAR + 256 + 1024;   // + alignment slack
 static_assert(LA_BYTES <= 232448, "lightning-attention shared memory exceeds 227 KiB");
+
+// tensor memory columns
+constexpr uint32_t LT_Z = 0, LT_SA = 128, LT_Y1 = 192, LT_Y2 = 320, LT_DA = 448;
 
 enum { LB_LD0 = 0, LB_A = LA_NST, LB_M3, LB_M12_0, LB_M12_1, LB_E1R0, LB_E1R1, LB_SBR, LB_OUT0, LB_OUT1, LB_COUNT };
 static_assert(8 * LB_COUNT <= 128, "barrier area");
@@ -78,11 +84,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "[%5];\n" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
         : "memory");
 }
-
-// S (bf16) as the MN-major B operand of the output MMA: element (v, k) of the
-// 128 x 128 matrix; v atoms of 64 are 16 KiB apart (128 k rows each).
-__device__ __forceinline__ uint32_t la_sb_off(int v8, int k) {   // v8: 8-element group of v
-    return (uint32_t)((v8 >> 3) * 16384 + (k >> 3) * 1024 + (k & 7) * 128 + (((v8 & 7) ^ (k & 7)) << 4));
+// MMA with the A operand in tensor memory (row m in lane m; column c holds K elements 2c, 2c + 1)
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                             uint32_t acc) {
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 }
 
 __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_constant__ CUtensorMap tq,
@@ -103,11 +121,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
 
     if (tid == 0) {
         for (int i = 0; i < LB_E1R0; ++i) mbar_init(bar + 8 * i, 1);
-        mbar_init(bar + 8 * LB_E1R0, LA_EPI_WARPS);
-        mbar_init(bar + 8 * LB_E1R1, LA_EPI_WARPS);
-        mbar_init(bar + 8 * LB_SBR, LA_EPI_WARPS);
-        mbar_init(bar + 8 * LB_OUT0, LA_EPI_WARPS);
-        mbar_init(bar + 8 * LB_OUT1, LA_EPI_WARPS);
+        for (int i = LB_E1R0; i < LB_COUNT; ++i) mbar_init(bar + 8 * i, LA_EPI_WARPS);
         mbar_fence_init();
         *abort_flag = 0;
     }
@@ -116,8 +130,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + LA_SLOT);
-    const uint32_t tZ = tmem, tDa = tmem + 384;   // Y[b] at tmem + 128 + 128 b
-    const float sl2 = p.slope[h] * LOG2E;         // decay per token, log2 units
+    const float sl2 = p.slope[h] * LOG2E;   // decay per token, log2 units
     auto fail = [&]() {
         set_status(KDA_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
@@ -127,16 +140,17 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         // ------------------------------------------------------------ issuers (one lane each)
         const uint32_t id_a = idesc_bf16(64, 64);
         const uint32_t id_3 = idesc_bf16(128, 128) | (1u << 15) | (1u << 16);
-        const uint32_t id_12 = idesc_bf16(64, 128) | (1u << 16);
+        const uint32_t id_2 = idesc_bf16(128, 64) | (1u << 15);
+        const uint32_t id_1 = idesc_bf16(128, 64);
         // descriptors of stage 0 / buffer 0; other operands add (byte offset >> 4) to the address field
         const uint64_t dQ = umma_desc(sbase + LA_Q, 16, 1024), dK = umma_desc(sbase + LA_K, 16, 1024);
         const uint64_t dKm = umma_desc(sbase + LA_K, 8192, 1024), dV = umma_desc(sbase + LA_V, 8192, 1024);
         const uint64_t dKL = umma_desc(sbase + LA_KL, 8192, 1024), dPB = umma_desc(sbase + LA_PB, 16, 1024);
-        const uint64_t dSB = umma_desc(sbase + LA_SB, 16384, 1024);
         auto stg = [](int c) { return (uint64_t)((c % LA_NST) * (LA_STAGE >> 4)); };
+        auto kmaj = [](int ks) { return (uint64_t)((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4); };
         bool ok = true;
         if (lane == 0 && warp == LA_EPI_WARPS) {
-            // ---- state issuer: loads, A (Da = Q K^T), M3 (Z = Kd^T V)
+            // ---- state issuer: loads, A (Da = Q K^T), M3 (Z^T = V^T Kd)
             auto load = [&](int c) {
                 const int s = c % LA_NST;
                 const uint32_t b = bar + 8 * (LB_LD0 + s), dst = sbase + s * LA_STAGE;
@@ -152,10 +166,8 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             auto mma_a = [&](int c) {
                 const uint64_t o = stg(c);
 #pragma unroll
-                for (int ks = 0; ks < KD / 16; ++ks) {
-                    const uint32_t kb = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-                    umma_bf16(tDa, dQ + o + kb, dK + o + kb, id_a, ks > 0 ? 1u : 0u);
-                }
+                for (int ks = 0; ks < KD / 16; ++ks)
+                    umma_bf16(tmem + LT_DA, dQ + o + kmaj(ks), dK + o + kmaj(ks), id_a, ks > 0 ? 1u : 0u);
                 umma_commit(bar + 8 * LB_A);
             };
             for (int c = 0; c < n && c < LA_NST; ++c) load(c);
@@ -182,10 +194,11 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int ks = 0; ks < CH / 16; ++ks)
-                        umma_bf16(tZ, (part ? dKL + (uint64_t)((c & 1) * (16384 >> 4)) : dKm + o) + ks * (2048 >> 4),
-                                  dV + o + ks * (2048 >> 4), id_3, (part > 0 || ks > 0) ? 1u : 0u);
+                        umma_bf16(tmem + LT_Z, dV + o + ks * (2048 >> 4),
+                                  (part ? dKL + (uint64_t)((c & 1) * (16384 >> 4)) : dKm + o) + ks * (2048 >> 4), id_3,
+                                  (part > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(bar + 8 * LB_M3);
-                // refill this stage once M3 and M12 of chunk c have read it
+                // refill this stage once M3, M2 and M1 of chunk c have read it
                 if (c + LA_NST < n) {
                     if (!mbar_wait(bar + 8 * LB_M3, c & 1) ||
                         !mbar_wait(bar + 8 * (LB_M12_0 + (c & 1)), (c >> 1) & 1)) { ok = false; break; }
@@ -193,24 +206,25 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                 }
             }
         } else if (lane == 0) {
-            // ---- output issuer: M12 (Y = P V, then += Qg S^T once S of the previous chunk is written)
+            // ---- output issuer: M2 (Y2^T = V^T P^T), then M1 (Y1^T = S Q^T) once S of the previous chunk is
+            //      in tensor memory
             for (int c = 0; ok && c < n && !*abort_flag; ++c) {
                 const uint64_t o = stg(c);
+                const int b = c & 1;
                 if (!mbar_spin(bar + 8 * (LB_LD0 + c % LA_NST), (c / LA_NST) & 1) ||
-                    !mbar_spin(bar + 8 * (LB_E1R0 + (c & 1)), (c >> 1) & 1)) { ok = false; break; }
-                if (c >= 2 && !mbar_spin(bar + 8 * (LB_OUT0 + (c & 1)), ((c >> 1) - 1) & 1)) { ok = false; break; }
+                    !mbar_spin(bar + 8 * (LB_E1R0 + b), (c >> 1) & 1)) { ok = false; break; }
+                if (c >= 2 && !mbar_spin(bar + 8 * (LB_OUT0 + b), ((c >> 1) - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t tY = tmem + 128 + 128 * (c & 1);
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks)
-                    umma_bf16(tY, dPB + (uint64_t)((c & 1) * (8192 >> 4) + ks * 2), dV + o + ks * (2048 >> 4), id_12,
-                              ks > 0 ? 1u : 0u);
+                    umma_bf16(tmem + LT_Y2 + 64 * b, dV + o + ks * (2048 >> 4), dPB + (uint64_t)(b * (8192 >> 4) + ks * 2),
+                              id_2, ks > 0 ? 1u : 0u);
                 if (!mbar_spin(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < KD / 16; ++ks)
-                    umma_bf16(tY, dQ + o + (((ks >> 2) * 8192 + (ks & 3) * 32) >> 4), dSB + ks * (2048 >> 4), id_12, 1u);
-                umma_commit(bar + 8 * (LB_M12_0 + (c & 1)));
+                    umma_bf16_ta(tmem + LT_Y1 + 64 * b, tmem + LT_SA + 8 * ks, dQ + o + kmaj(ks), id_1, ks > 0 ? 1u : 0u);
+                umma_commit(bar + 8 * (LB_M12_0 + b));
             }
         }
         if (lane == 0) {
@@ -225,40 +239,43 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         // ------------------------------------------------------------ epilogue
         const int q4 = warp & 3, cg = warp >> 2;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-        const int kme = q4 * 32 + lane;   // state channel (Z lanes)
-        const int rme = q4 * 16 + lane;   // chunk row in the M = 64 accumulator layout (lanes < 16)
-        float S[32];                      // S[32 cg + j][kme]
-        const size_t st0 = (((size_t)seq * p.H_v + h) * KD + 32 * cg) * KD + kme;
+        const int vme = q4 * 32 + lane;   // state row v (lane of the M = 128 accumulators)
+        const int rme = q4 * 16 + lane;   // chunk row of the M = 64 accumulator Da (lanes < 16)
+        float S[32];                      // S[vme][32 cg + j]
+        const size_t st0 = (((size_t)seq * p.H_v + h) * KD + vme) * KD + 32 * cg;
+        if (p.init) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[j] = p.init ? p.init[st0 + (size_t)j * KD] : 0.f;
-        auto write_sb = [&]() {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                uint4 w;
-                w.x = pack_bf16x2(S[8 * u + 0], S[8 * u + 1]);
-                w.y = pack_bf16x2(S[8 * u + 2], S[8 * u + 3]);
-                w.z = pack_bf16x2(S[8 * u + 4], S[8 * u + 5]);
-                w.w = pack_bf16x2(S[8 * u + 6], S[8 * u + 7]);
-                *reinterpret_cast<uint4 *>(sm + LA_SB + la_sb_off(4 * cg + u, kme)) = w;
+            for (int j = 0; j < 32; j += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(p.init + st0 + j);
+                S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
             }
-            fence_async_smem();
-        };
-        write_sb();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar + 8 * LB_SBR);
-
-        // E1 of chunk c: P from Da; Qg = Q exp(Gam_r) and Kd = K exp(Gam_len - Gam_r) (hi in place, lo
-        // in its buffer).  P[c & 1] and Kd_lo[c & 1] were last read by M12 / M3 of chunk c - 2, which the
-        // state update of chunk c - 2 waited for, earlier in program order.
-        // row decays of this thread's two 16-byte units (rows tid / 16 and tid / 16 + 32): exp(Gam_r)
-        // and, for full chunks, exp(Gam_63 - Gam_r)
-        float eqr[2], edr[2];
+        } else {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int r = (tid >> 4) + 32 * i;
-            eqr[i] = ex2(-sl2 * (float)(r + 1));
-            edr[i] = ex2(-sl2 * (float)(CH - 1 - r));
+            for (int j = 0; j < 32; ++j) S[j] = 0.f;
         }
+        // bf16 S (columns 16 cg .. 16 cg + 15 of the A operand: k = 32 cg + 2 w, 2 w + 1) and release
+        auto write_sa = [&]() {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(S[2 * i], S[2 * i + 1]);
+            tmem_st16(tmem + LT_SA + lane_off + 16 * cg, w);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar + 8 * LB_SBR);
+        };
+        write_sa();
+        const float lam = ex2(-sl2);
+        // row decays of this thread's two 16-byte units of K (rows tid / 16 and tid / 16 + 32) for a
+        // full chunk: exp(Gam_63 - Gam_r)
+        float edr[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) edr[i] = ex2(-sl2 * (float)(CH - 1 - ((tid >> 4) + 32 * i)));
+        const float eq0 = ex2(-sl2 * (float)(16 * cg + 1));   // exp(Gam_r) of this thread's first output row
+
+        // E1 of chunk c: P from Da; Kd = K exp(Gam_len - Gam_r) (hi in place, lo in its buffer).
+        // P[c & 1] and Kd_lo[c & 1] were last read by M2 / M3 of chunk c - 2, which the state
+        // update of chunk c - 2 waited for, earlier in program order.
         auto e1 = [&](int c) -> bool {
             const int s = c % LA_NST;
             unsigned char *stg = sm + s * LA_STAGE;
@@ -275,7 +292,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                     for (int e = 0; e < 16; ++e) o[e] = 0.f;
                 } else {
                     uint32_t x[16];
-                    tmem_ld16_nowait(tDa + lane_off + 16 * cg, x);
+                    tmem_ld16_nowait(tmem + LT_DA + lane_off + 16 * cg, x);
                     tmem_wait_ld();
                     const float c0 = -sl2 * (float)(rme - 16 * cg);
 #pragma unroll
@@ -295,22 +312,18 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             }
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const int u = tid + LA_EPI * i, r = u >> 4, c16 = u & 15;
+                const int r = (tid >> 4) + 32 * i, c16 = tid & 15;
                 const uint32_t off = sw128_off(r, 16 * c16, CH);
-                const float eq = eqr[i];
                 const float ed = len == CH ? edr[i] : (r < len ? ex2(-sl2 * (float)(len - 1 - r)) : 0.f);
-                const uint4 qw = *reinterpret_cast<const uint4 *>(stg + LA_Q + off);
                 const uint4 kw = *reinterpret_cast<const uint4 *>(stg + LA_K + off);
-                const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, ka[4] = {kw.x, kw.y, kw.z, kw.w};
-                uint32_t qg[4], kh[4], kl[4];
+                const uint32_t ka[4] = {kw.x, kw.y, kw.z, kw.w};
+                uint32_t kh[4], kl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    qg[e] = pack_bf16x2(bf16_lo(qa[e]) * eq, bf16_hi(qa[e]) * eq);
                     const float d0 = bf16_lo(ka[e]) * ed, d1 = bf16_hi(ka[e]) * ed;
                     kh[e] = pack_bf16x2(d0, d1);
                     kl[e] = pack_bf16x2(d0 - bf16_lo(kh[e]), d1 - bf16_hi(kh[e]));
                 }
-                *reinterpret_cast<uint4 *>(stg + LA_Q + off) = make_uint4(qg[0], qg[1], qg[2], qg[3]);
                 *reinterpret_cast<uint4 *>(stg + LA_K + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
                 *reinterpret_cast<uint4 *>(sm + LA_KL + (c & 1) * 16384 + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
             }
@@ -320,7 +333,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(bar + 8 * (LB_E1R0 + (c & 1)));
             return true;
         };
-        // E2 of chunk c: S <- exp(Gam_len) S + Z; S (bf16) for the next chunk's output MMA
+        // E2 of chunk c: S <- exp(Gam_len) S + Z^T, then the bf16 copy for the next chunk's M1
         auto e2 = [&](int c) -> bool {
             const int len = min(CH, sd.len - c * CH);
             if (!mbar_wait(bar + 8 * LB_M3, c & 1) || !mbar_wait(bar + 8 * (LB_M12_0 + (c & 1)), (c >> 1) & 1))
@@ -330,39 +343,46 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
                 uint32_t z[16];
-                tmem_ld16_nowait(tZ + lane_off + 32 * cg + 16 * hlf, z);
+                tmem_ld16_nowait(tmem + LT_Z + lane_off + 32 * cg + 16 * hlf, z);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j) S[16 * hlf + j] = fmaf(S[16 * hlf + j], g, __uint_as_float(z[j]));
             }
-            write_sb();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar + 8 * LB_SBR);
+            write_sa();
             return true;
         };
-        // output of chunk c: O = scale Y (rows rme, columns 32 cg ..)
+        // output of chunk c: O[r][v] = scale (exp(Gam_r) Y1^T[v][r] + Y2^T[v][r]) for r = 16 cg .. 16 cg + 15,
+        // through the staging buffer to 16-byte stores of whole rows
         auto emit = [&](int c) {
-            const int len = min(CH, sd.len - c * CH);
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(sd.tok + c * CH + rme) * p.H_v + h) * KD + 32 * cg);
+            const int b = c & 1, len = min(CH, sd.len - c * CH);
+            uint16_t *os = reinterpret_cast<uint16_t *>(sm + LA_OS + b * 16384);
+            float f = eq0 * p.scale;
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
-                uint32_t y[16];
-                tmem_ld16_nowait(tmem + 128 + 128 * (c & 1) + lane_off + 32 * cg + 16 * hlf, y);
+                uint32_t y1[8], y2[8];
+                tmem_ld8_nowait(tmem + LT_Y1 + 64 * b + lane_off + 16 * cg + 8 * hlf, y1);
+                tmem_ld8_nowait(tmem + LT_Y2 + 64 * b + lane_off + 16 * cg + 8 * hlf, y2);
                 tmem_wait_ld();
-                if (lane < 16 && rme < len) {
+                if (hlf == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar + 8 * (LB_OUT0 + b));
+                }
 #pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        dst[2 * hlf + u] = make_uint4(
-                            pack_bf16x2(p.scale * __uint_as_float(y[8 * u + 0]), p.scale * __uint_as_float(y[8 * u + 1])),
-                            pack_bf16x2(p.scale * __uint_as_float(y[8 * u + 2]), p.scale * __uint_as_float(y[8 * u + 3])),
-                            pack_bf16x2(p.scale * __uint_as_float(y[8 * u + 4]), p.scale * __uint_as_float(y[8 * u + 5])),
-                            pack_bf16x2(p.scale * __uint_as_float(y[8 * u + 6]), p.scale * __uint_as_float(y[8 * u + 7])));
+                for (int j = 0; j < 8; ++j) {
+                    os[(16 * cg + 8 * hlf + j) * KD + vme] =
+                        f_to_bf16(fmaf(f, __uint_as_float(y1[j]), p.scale * __uint_as_float(y2[j])));
+                    f *= lam;
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar + 8 * (LB_OUT0 + (c & 1)));
+            named_bar(1, LA_EPI);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int u = tid + LA_EPI * i, r = u >> 4, c16 = u & 15;
+                if (r < len)
+                    *reinterpret_cast<uint4 *>(p.out + ((size_t)(sd.tok + c * CH + r) * p.H_v + h) * KD + 8 * c16) =
+                        *reinterpret_cast<const uint4 *>(os + r * KD + 8 * c16);
+            }
         };
         bool ok = n == 0 || e1(0);
         for (int c = 0; ok && c < n; ++c) {
@@ -373,9 +393,9 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         }
         if (!ok) fail();
         if (ok && p.fin) {
-            float *dst = p.fin + st0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dst[(size_t)j * KD] = S[j];
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(p.fin + st0 + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
     }
     tc_fence_before();
