@@ -25,7 +25,8 @@
 // rewrites its K rows in place as Kd_hi = bf16(k exp(Gam_len - Gam_r)) and
 // stores the remainder Kd_lo in a double buffer, so the state update keeps
 // ~16 bits; S and P enter the output products rounded to bf16, like the output
-// itself.  The output O = scale (exp(Gam_r) Y1 + Y2) is transposed through
+// itself.  P carries the factor scale, and the output
+// O = scale exp(Gam_r) Y1 + Y2 is transposed through
 // shared memory and written with 16-byte stores.  Every wait is bounded; a
 // timeout records KDA_ERR_DEVICE_TIMEOUT and all roles stop.
 #include <cuda.h>
@@ -181,14 +182,14 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             for (int c = 0; ok && c < n && !*abort_flag; ++c) {
                 const uint64_t o = stg(c);
                 // E1 of chunk c is done: Da is free, so A of the next chunk goes first
-                if (!mbar_spin(bar + 8 * (LB_E1R0 + (c & 1)), (c >> 1) & 1)) { ok = false; break; }
+                if (!mbar_wait(bar + 8 * (LB_E1R0 + (c & 1)), (c >> 1) & 1)) { ok = false; break; }
                 if (c + 1 < n) {
-                    if (!mbar_spin(bar + 8 * (LB_LD0 + (c + 1) % LA_NST), ((c + 1) / LA_NST) & 1)) { ok = false; break; }
+                    if (!mbar_wait(bar + 8 * (LB_LD0 + (c + 1) % LA_NST), ((c + 1) / LA_NST) & 1)) { ok = false; break; }
                     tc_fence_after();
                     mma_a(c + 1);
                 }
                 // M3: Z was read by the previous state update (SBR #c)
-                if (!mbar_spin(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
+                if (!mbar_wait(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
@@ -211,15 +212,15 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             for (int c = 0; ok && c < n && !*abort_flag; ++c) {
                 const uint64_t o = stg(c);
                 const int b = c & 1;
-                if (!mbar_spin(bar + 8 * (LB_LD0 + c % LA_NST), (c / LA_NST) & 1) ||
-                    !mbar_spin(bar + 8 * (LB_E1R0 + b), (c >> 1) & 1)) { ok = false; break; }
-                if (c >= 2 && !mbar_spin(bar + 8 * (LB_OUT0 + b), ((c >> 1) - 1) & 1)) { ok = false; break; }
+                if (!mbar_wait(bar + 8 * (LB_LD0 + c % LA_NST), (c / LA_NST) & 1) ||
+                    !mbar_wait(bar + 8 * (LB_E1R0 + b), (c >> 1) & 1)) { ok = false; break; }
+                if (c >= 2 && !mbar_wait(bar + 8 * (LB_OUT0 + b), ((c >> 1) - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks)
                     umma_bf16(tmem + LT_Y2 + 64 * b, dV + o + ks * (2048 >> 4), dPB + (uint64_t)(b * (8192 >> 4) + ks * 2),
                               id_2, ks > 0 ? 1u : 0u);
-                if (!mbar_spin(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
+                if (!mbar_wait(bar + 8 * LB_SBR, c & 1)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < KD / 16; ++ks)
@@ -271,7 +272,11 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         float edr[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) edr[i] = ex2(-sl2 * (float)(CH - 1 - ((tid >> 4) + 32 * i)));
-        const float eq0 = ex2(-sl2 * (float)(16 * cg + 1));   // exp(Gam_r) of this thread's first output row
+        const float eq0 = p.scale * ex2(-sl2 * (float)(16 * cg + 1));   // scale exp(Gam_r), first output row
+        // P factors: below the diagonal block the walk starts at column e = 15 with scale lambda^(r - j)
+        // (r - j >= 1); on it the factor only advances on kept columns (e <= lane), starting at scale
+        const float pscale0 = p.scale * ex2(-sl2 * (float)max(rme - 16 * cg - 15, 0));
+        const float pscale_diag = p.scale;
 
         // E1 of chunk c: P from Da; Kd = K exp(Gam_len - Gam_r) (hi in place, lo in its buffer).
         // P[c & 1] and Kd_lo[c & 1] were last read by M2 / M3 of chunk c - 2, which the state
@@ -283,8 +288,9 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             if (!mbar_wait(bar + 8 * (LB_LD0 + s), (c / LA_NST) & 1) || !mbar_wait(bar + 8 * LB_A, c & 1)) return false;
             tc_fence_after();
             {
-                // P block (rows 16 q4 .., columns 16 cg ..): zero above the diagonal block, decay
-                // lambda^(r - j) = 2^(-sl2 (r - 16 cg) + sl2 e) below it, masked on it
+                // P block (rows 16 q4 .., columns 16 cg ..) times scale: zero above the diagonal block;
+                // below and on it scale lambda^(r - j), built from lambda^(r - 16 cg - 15) by factors of
+                // lambda going down the columns, masked (j > r) on the diagonal block
                 unsigned char *pb = sm + LA_PB + (c & 1) * 8192;
                 float o[16];
                 if (cg > q4) {
@@ -293,10 +299,13 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                 } else {
                     uint32_t x[16];
                     tmem_ld16_nowait(tmem + LT_DA + lane_off + 16 * cg, x);
+                    float f = cg < q4 ? pscale0 : pscale_diag;
                     tmem_wait_ld();
-                    const float c0 = -sl2 * (float)(rme - 16 * cg);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = __uint_as_float(x[e]) * ex2(fmaf(sl2, (float)e, c0));
+                    for (int e = 15; e >= 0; --e) {
+                        o[e] = __uint_as_float(x[e]) * f;
+                        if (cg < q4 || e <= lane) f *= lam;
+                    }
                     if (cg == q4) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) o[e] = e <= lane ? o[e] : 0.f;
@@ -356,7 +365,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         auto emit = [&](int c) {
             const int b = c & 1, len = min(CH, sd.len - c * CH);
             uint16_t *os = reinterpret_cast<uint16_t *>(sm + LA_OS + b * 16384);
-            float f = eq0 * p.scale;
+            float f = eq0;
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
                 uint32_t y1[8], y2[8];
@@ -370,8 +379,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    os[(16 * cg + 8 * hlf + j) * KD + vme] =
-                        f_to_bf16(fmaf(f, __uint_as_float(y1[j]), p.scale * __uint_as_float(y2[j])));
+                    os[(16 * cg + 8 * hlf + j) * KD + vme] = f_to_bf16(fmaf(f, __uint_as_float(y1[j]), __uint_as_float(y2[j])));
                     f *= lam;
                 }
             }
