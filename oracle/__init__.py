@@ -18,6 +18,9 @@ Contents
   fixed per-head decay), the token recurrence in plain C (``la_oracle.c``).
 * ``la_quadratic``: the same method in its parallel (attention-matrix) form in
   NumPy fp64, a second formulation that pins the recurrence.
+* ``backward.bwd``: gradients of the KDA forward with respect to all inputs
+  (fp64 autograd through the token recurrence), pinned by finite differences
+  of ``brute_force``.
 
 The recurrence (KDA, the method the page "FlashKDA: High-performance KDA CUDA
 kernels for SM90+ GPUs" implements; gate, sigmoid and L2-norm fusion under its

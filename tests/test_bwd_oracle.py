@@ -1,0 +1,95 @@
+"""CPU tests pinning the backward oracle (fp64 autograd through the token
+recurrence) to central finite differences of the independent explicit-matrix
+forward (``oracle.brute_force``), on small fp64 problems."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import backward as OB
+
+
+def _problem(seed, B=1, T=4, H_qk=1, H_v=2, K=4, V=4, seqlens=None, with_state=True):
+    g = torch.Generator().manual_seed(seed)
+    r = lambda *s: torch.randn(*s, generator=g, dtype=torch.float64)  # noqa: E731
+    if seqlens is not None:
+        assert B == 1 and sum(seqlens) == T
+        cu = torch.tensor([0] + list(np.cumsum(seqlens)), dtype=torch.int32)
+        N = len(seqlens)
+    else:
+        cu, N = None, B
+    x = dict(q=r(B, T, H_qk, K), k=r(B, T, H_qk, K), v=r(B, T, H_v, V), graw=r(B, T, H_v, K), b=r(B, T, H_v),
+             A_log=0.5 * r(H_v), h0=0.3 * r(N, H_v, V, K) if with_state else None)
+    do, dht = r(B, T, H_v, V), r(N, H_v, V, K)
+    return x, cu, do, dht
+
+
+def _loss(x, cu, do, dht, scale):
+    o, f = oracle.brute_force(torch.as_tensor(x["q"]), torch.as_tensor(x["k"]), torch.as_tensor(x["v"]),
+                              torch.as_tensor(x["graw"]), torch.as_tensor(x["b"]), torch.as_tensor(x["A_log"]),
+                              scale, None if x["h0"] is None else torch.as_tensor(x["h0"]), cu)
+    return float((o * do.numpy()).sum() + (f * dht.numpy()).sum())
+
+
+def _fd(x, cu, do, dht, scale, name, h=1e-6):
+    base = {k_: (None if v_ is None else v_.clone()) for k_, v_ in x.items()}
+    grad = torch.zeros_like(base[name])
+    flat = base[name].view(-1)
+    gflat = grad.view(-1)
+    for i in range(flat.numel()):
+        old = float(flat[i])
+        flat[i] = old + h
+        lp = _loss(base, cu, do, dht, scale)
+        flat[i] = old - h
+        lm = _loss(base, cu, do, dht, scale)
+        flat[i] = old
+        gflat[i] = (lp - lm) / (2 * h)
+    return grad
+
+
+NAMES = {"q": "dq", "k": "dk", "v": "dv", "graw": "dgraw", "b": "db", "A_log": "dA_log", "h0": "dh0"}
+
+
+def _max_rel(a, b):
+    return float((a - b).abs().max() / max(float(b.abs().max()), 1e-300))
+
+
+def _check(seed, mutation=0, **kw):
+    scale = 0.5
+    x, cu, do, dht = _problem(seed, **kw)
+    got = OB.bwd(x["q"], x["k"], x["v"], x["graw"], x["b"], x["A_log"], scale, x["h0"], cu, do=do, dht=dht,
+                 mutation=mutation)
+    err = 0.0
+    for name, gname in NAMES.items():
+        if x[name] is None:
+            continue
+        err = max(err, _max_rel(got[gname], _fd(x, cu, do, dht, scale, name)))
+    return err
+
+
+@pytest.mark.parametrize("case", ["plain", "gva_varlen", "no_state"])
+def test_bwd_oracle_matches_finite_differences(case):
+    if case == "plain":
+        err = _check(1)
+    elif case == "gva_varlen":
+        err = _check(2, T=5, H_qk=1, H_v=2, seqlens=[3, 0, 2])
+    else:
+        err = _check(3, with_state=False, B=2, T=3)
+    assert err <= 1e-6, err
+
+
+@pytest.mark.parametrize("m", [1, 2], ids=["decay gradient dropped", "erase-term gradient dropped"])
+def test_fd_pin_catches_planted_mistake(m):
+    assert _check(1, mutation=m) > 1e-3
+
+
+def test_bwd_oracle_forward_equals_c_oracle():
+    """The differentiable recurrence is the forward oracle's: same outputs on bf16 inputs."""
+    import kda_inputs as KI
+    inp = KI.make_inputs(1, 20, 1, 2, seed=5, with_state=True, seqlens=[12, 8])
+    o, f = OB._recurrence(*(t.double() for t in (inp.q, inp.k, inp.v, inp.graw, inp.b, inp.A_log)),
+                          float(torch.tensor(inp.scale, dtype=torch.float32)), inp.initial_state.double(),
+                          inp.cu_seqlens, inp.H_qk)
+    ro, rf = oracle.fwd_inputs(inp)
+    assert np.abs(o.detach().numpy() - ro).max() <= 1e-9 * max(1.0, np.abs(ro).max())
+    assert np.abs(f.detach().numpy() - rf).max() <= 1e-9 * max(1.0, np.abs(rf).max())
