@@ -8,6 +8,7 @@ Build the library with ``gated_delta_rule_40_gb300.build.build()``.
 from .kda import (  # noqa: F401
     KdaError,
     KdaLibraryError,
+    kda_bwd,
     kda_decode_step,
     kda_decode_tokens,
     kda_fwd,

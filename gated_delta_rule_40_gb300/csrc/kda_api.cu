@@ -28,6 +28,13 @@ cudaError_t launch_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *
 size_t la_workspace_bytes(int N, int B, int T, bool varlen);
 cudaError_t launch_la_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v, const float *slope, float scale,
                              float *state, int B, int H_qk, int H_v, uint16_t *out, cudaStream_t stream);
+size_t bwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, int grid);
+int bwd_grid(int nseq, int H_v);
+cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                       const uint16_t *b, const float *A_log, float scale, const float *init, const int32_t *cu, int N,
+                       int B, int T, int H_qk, int H_v, const uint16_t *dout, const float *dht, float *dq, float *dk,
+                       float *dv, float *dgraw, float *db, float *dA_log, float *dh0, void *ws_ptr, int grid,
+                       cudaStream_t stream, int *launches);
 struct FwdWorkspace;
 size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspace *ws, char *base);
 
@@ -262,6 +269,39 @@ int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
     kda::timing_mark("decode_kernel", stream);
     t_last_launches = 1;
     return KDA_OK;
+}
+
+int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+            const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
+            const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V, const kda_bf16_t *dout,
+            const float *dht, float *dq, float *dk, float *dv, float *dgraw, float *db, float *dA_log, float *dh0,
+            cudaStream_t stream) {
+    int rc = validate_fwd(q, k, v, graw, b, A_log, initial_state, nullptr, cu_seqlens, N, B, T, H_qk, H_v, K, V,
+                          dout);
+    if (rc != KDA_OK) return rc;
+    const long long tokens = (long long)B * T;
+    if (!A_log || !dA_log || !dh0) return KDA_ERR_INVALID_ARG;
+    if (tokens > 0 && (!dq || !dk || !dv || !dgraw || !db)) return KDA_ERR_INVALID_ARG;
+    if ((dht && !aligned16(dht)) || !aligned16(dh0) ||
+        (tokens > 0 && (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dgraw))))
+        return KDA_ERR_INVALID_ARG;
+    const bool varlen = cu_seqlens != nullptr;
+    const int grid = kda::bwd_grid(varlen ? N : B, H_v);
+    const size_t need = kda::bwd_workspace_bytes(varlen ? N : 0, B, T, H_v, varlen, grid);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    int launches = 0;
+    kda::timing_begin(stream);
+    const cudaError_t e = kda::launch_bwd(q, k, v, graw, b, A_log, scale, initial_state, cu_seqlens, varlen ? N : 0,
+                                          B, T, H_qk, H_v, dout, dht, dq, dk, dv, dgraw, db, dA_log, dh0, ws, grid,
+                                          stream, &launches);
+    rc = e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    if (rc == KDA_OK) {
+        kda::timing_mark("bwd (plan, recurrence, prologue)", stream);
+        t_last_launches = launches;
+    }
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
+    return rc;
 }
 
 int kda_la_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const float *slope, float scale,

@@ -1,0 +1,381 @@
+// KDA backward: gradients of the forward with respect to q, k, v, graw, b,
+// A_log and the initial state, given the gradients of the outputs (do) and of
+// the final states (dht).
+//
+// Per sequence and value head, token t (qt, kh normalised, e = exp(g), beta):
+//   S' = S_{t-1} Diag(e),  d = S' kh,  delta = beta (v - d),  S_t = S' + delta kh^T,  o = S_t qt
+// and, walking t backwards with dS = dL/dS_t (rows v of the state are
+// independent in both directions; only the per-token parameter gradients sum
+// over v):
+//   dS   += do qt^T                     dqt  = S_t^T do
+//   ddel  = dS kh                       dkh  = dS^T delta + S'^T dd,   dd = -beta ddel
+//   dv    = beta ddel                   dbeta = ddel . (v - d)
+//   dS'   = dS + dd kh^T                de    = colsum(S_{t-1} * dS')
+//   dS_{t-1} = dS' Diag(e)
+// then the prologue's Jacobians map dqt, dkh, de, dbeta to dq, dk, dgraw,
+// dA_log, db (dq and dk sum over the value heads of a query/key group).
+//
+// bwd_recur_kernel: persistent CTAs of 16 warps, one (sequence, value head)
+// chain at a time; warp w owns state rows 8w .. 8w + 7, lane owns channels
+// 4 lane .. 4 lane + 3, so S and dS live in registers (32 values each).  A
+// first pass runs the recurrence and stores the state at every 64-token chunk
+// start; the backward pass then takes the chunks in reverse: it recomputes the
+// chunk's states from its checkpoint into a per-CTA scratch area (each thread
+// reads back only what it wrote), then walks the chunk's tokens backwards.
+// The per-token vectors (qt, kh, e, v, do, beta) of a chunk are staged in
+// shared memory; the sums over v of dqt, dkh, de and dbeta are reduced across
+// warps through shared memory and written per (token, head) for
+// bwd_prologue_kernel.  This is the token recurrence on CUDA cores in fp32, a
+// correct first form; its cost is O(T K V) per chain with no tensor-core use.
+#include "kda_common.cuh"
+
+namespace kda {
+
+cudaError_t launch_plan(const int32_t *cu, int N, int B, int T, SeqDesc *seqs, ChunkDesc *chunks, int *order,
+                        int *hdr, long long max_chunks, cudaStream_t stream);
+long long max_chunks_for(int N, int B, int T, bool varlen);
+
+constexpr int BW_WARPS = 16;
+constexpr int BW_THREADS = BW_WARPS * 32;
+constexpr int BW_ROWS = KD / BW_WARPS;   // 8 state rows per warp
+constexpr uint32_t BW_VEC = CH * KD * 4;  // one [64][128] fp32 table
+constexpr uint32_t BW_QT = 0, BW_KH = BW_VEC, BW_E = 2 * BW_VEC, BW_V = 3 * BW_VEC, BW_DO = 4 * BW_VEC;
+constexpr uint32_t BW_BETA = 5 * BW_VEC;            // [64]
+constexpr uint32_t BW_RED = BW_BETA + 256;          // [16 warps][3][128]
+constexpr uint32_t BW_REDB = BW_RED + BW_WARPS * 3 * KD * 4;   // [16]
+constexpr uint32_t BW_BYTES = BW_REDB + 64;
+static_assert(BW_BYTES <= 227 * 1024, "backward shared memory");
+
+struct BwdParams {
+    const uint16_t *q, *k, *v, *graw, *b, *dout;
+    const float *A_log, *init, *dht;
+    float scale;
+    int H_qk, H_v, nseq;
+    const SeqDesc *seqs;
+    const int *order;
+    const int *hdr;
+    float *ckpt;      // [chunk][H_v][V][K]
+    float *scratch;   // [gridDim.x][64][V][K]
+    float *dqt, *dkh, *de, *dbeta;   // [token][H_v][128] (dbeta [token][H_v])
+    float *dv, *dh0;                 // [token][H_v][V], [N][H_v][V][K]
+};
+
+// Per-token vectors of tokens tok0 .. tok0 + len - 1 into the shared tables; warp w takes tokens w, w + 16, ...
+__device__ __forceinline__ void bwd_stage_chunk(const BwdParams &p, unsigned char *sm, int tok0, int len, int h,
+                                                int hq, float a_gate, bool with_do, int warp, int lane) {
+    float *sqt = reinterpret_cast<float *>(sm + BW_QT), *skh = reinterpret_cast<float *>(sm + BW_KH);
+    float *se = reinterpret_cast<float *>(sm + BW_E), *sv = reinterpret_cast<float *>(sm + BW_V);
+    float *sdo = reinterpret_cast<float *>(sm + BW_DO), *sbeta = reinterpret_cast<float *>(sm + BW_BETA);
+    for (int r = warp; r < len; r += BW_WARPS) {
+        const size_t tok = (size_t)tok0 + r;
+        const size_t qo = (tok * p.H_qk + hq) * KD + 4 * lane, vo = (tok * p.H_v + h) * KD + 4 * lane;
+        const uint2 qw = *reinterpret_cast<const uint2 *>(p.q + qo), kw = *reinterpret_cast<const uint2 *>(p.k + qo);
+        const uint2 gw = *reinterpret_cast<const uint2 *>(p.graw + vo), vw = *reinterpret_cast<const uint2 *>(p.v + vo);
+        const float qv[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
+        const float kv[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
+        const float gv[4] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y)};
+        const float vv[4] = {bf16_lo(vw.x), bf16_hi(vw.x), bf16_lo(vw.y), bf16_hi(vw.y)};
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            sq = fmaf(qv[i], qv[i], sq);
+            sk = fmaf(kv[i], kv[i], sk);
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        const float rq = p.scale * rsqrtf(sq + L2_EPS), rk = rsqrtf(sk + L2_EPS);
+        float4 a, bq, c, d;
+        a.x = qv[0] * rq; a.y = qv[1] * rq; a.z = qv[2] * rq; a.w = qv[3] * rq;
+        bq.x = kv[0] * rk; bq.y = kv[1] * rk; bq.z = kv[2] * rk; bq.w = kv[3] * rk;
+        c.x = ex2(-a_gate * softplus_log2(gv[0])); c.y = ex2(-a_gate * softplus_log2(gv[1]));
+        c.z = ex2(-a_gate * softplus_log2(gv[2])); c.w = ex2(-a_gate * softplus_log2(gv[3]));
+        d.x = vv[0]; d.y = vv[1]; d.z = vv[2]; d.w = vv[3];
+        reinterpret_cast<float4 *>(sqt + r * KD)[lane] = a;
+        reinterpret_cast<float4 *>(skh + r * KD)[lane] = bq;
+        reinterpret_cast<float4 *>(se + r * KD)[lane] = c;
+        reinterpret_cast<float4 *>(sv + r * KD)[lane] = d;
+        if (with_do) {
+            const uint2 ow = *reinterpret_cast<const uint2 *>(p.dout + vo);
+            reinterpret_cast<float4 *>(sdo + r * KD)[lane] =
+                make_float4(bf16_lo(ow.x), bf16_hi(ow.x), bf16_lo(ow.y), bf16_hi(ow.y));
+        }
+        if (lane == 0) {
+            const float bb = bf16_to_f(p.b[tok * p.H_v + h]);
+            sbeta[r] = 1.0f / (1.0f + ex2(-bb * LOG2E));
+        }
+    }
+}
+
+// One forward token on this thread's 8 rows x 4 channels: S <- S Diag(e) + beta (v - S Diag(e) kh) kh^T.
+// Returns nothing; S is updated in place.
+__device__ __forceinline__ void bwd_fwd_token(float4 (&S)[BW_ROWS], const float4 kh, const float4 e, float beta,
+                                              const float *vrow, int r0) {
+#pragma unroll
+    for (int i = 0; i < BW_ROWS; ++i) {
+        float4 x = S[i];
+        x.x *= e.x; x.y *= e.y; x.z *= e.z; x.w *= e.w;
+        const float d = warp_sum(x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w);
+        const float del = beta * (vrow[r0 + i] - d);
+        x.x = fmaf(del, kh.x, x.x); x.y = fmaf(del, kh.y, x.y); x.z = fmaf(del, kh.z, x.z); x.w = fmaf(del, kh.w, x.w);
+        S[i] = x;
+    }
+}
+
+__global__ __launch_bounds__(BW_THREADS, 1) void bwd_recur_kernel(const BwdParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+    if (p.hdr[1] == 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int r0 = warp * BW_ROWS;
+    const float *sqt = reinterpret_cast<const float *>(sm + BW_QT), *skh = reinterpret_cast<const float *>(sm + BW_KH);
+    const float *se = reinterpret_cast<const float *>(sm + BW_E), *sv = reinterpret_cast<const float *>(sm + BW_V);
+    const float *sdo = reinterpret_cast<const float *>(sm + BW_DO), *sbeta = reinterpret_cast<const float *>(sm + BW_BETA);
+    float *red = reinterpret_cast<float *>(sm + BW_RED), *redb = reinterpret_cast<float *>(sm + BW_REDB);
+    float *scr = p.scratch + (size_t)blockIdx.x * CH * KD * KD;
+    const int n_items = p.nseq * p.H_v;
+    const int group = p.H_v / p.H_qk;
+
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int h = item % p.H_v, seq = p.order[item / p.H_v], hq = h / group;
+        const SeqDesc sd = p.seqs[seq];
+        const float a_gate = ex2(p.A_log[h] * LOG2E);
+        // this thread's slice of a [V][K] matrix: rows r0 + i, channels 4 lane ..
+        const size_t sh = ((size_t)seq * p.H_v + h) * KD * KD;
+        auto slice = [&](size_t base, int i) { return base + (size_t)(r0 + i) * KD + 4 * lane; };
+        float4 S[BW_ROWS];
+#pragma unroll
+        for (int i = 0; i < BW_ROWS; ++i)
+            S[i] = p.init ? *reinterpret_cast<const float4 *>(p.init + slice(sh, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+
+        // ---- pass 1: the recurrence, storing the state at each chunk start
+        for (int c = 0; c < sd.nchunk; ++c) {
+            const int len = min(CH, sd.len - c * CH), tok0 = sd.tok + c * CH;
+            const size_t cb = ((size_t)(sd.chunk0 + c) * p.H_v + h) * KD * KD;
+#pragma unroll
+            for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(p.ckpt + slice(cb, i)) = S[i];
+            __syncthreads();   // the previous chunk's tables are no longer read
+            bwd_stage_chunk(p, sm, tok0, len, h, hq, a_gate, false, warp, lane);
+            __syncthreads();
+            for (int r = 0; r < len; ++r)
+                bwd_fwd_token(S, reinterpret_cast<const float4 *>(skh + r * KD)[lane],
+                              reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0);
+        }
+
+        // ---- pass 2: chunks in reverse
+        float4 dS[BW_ROWS];
+#pragma unroll
+        for (int i = 0; i < BW_ROWS; ++i)
+            dS[i] = p.dht ? *reinterpret_cast<const float4 *>(p.dht + slice(sh, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = sd.nchunk - 1; c >= 0; --c) {
+            const int len = min(CH, sd.len - c * CH), tok0 = sd.tok + c * CH;
+            const size_t cb = ((size_t)(sd.chunk0 + c) * p.H_v + h) * KD * KD;
+            __syncthreads();
+            bwd_stage_chunk(p, sm, tok0, len, h, hq, a_gate, true, warp, lane);
+            __syncthreads();
+            // recompute the chunk's states; scratch[r] = state before token r (this thread's slice)
+#pragma unroll
+            for (int i = 0; i < BW_ROWS; ++i) S[i] = *reinterpret_cast<const float4 *>(p.ckpt + slice(cb, i));
+            for (int r = 0; r < len; ++r) {
+#pragma unroll
+                for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(scr + slice((size_t)r * KD * KD, i)) = S[i];
+                if (r + 1 < len)
+                    bwd_fwd_token(S, reinterpret_cast<const float4 *>(skh + r * KD)[lane],
+                                  reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0);
+            }
+            // tokens backwards
+            for (int r = len - 1; r >= 0; --r) {
+                const float4 kh = reinterpret_cast<const float4 *>(skh + r * KD)[lane];
+                const float4 qt = reinterpret_cast<const float4 *>(sqt + r * KD)[lane];
+                const float4 e = reinterpret_cast<const float4 *>(se + r * KD)[lane];
+                const float beta = sbeta[r];
+                float4 pq = make_float4(0.f, 0.f, 0.f, 0.f), pk = pq, pe = pq;
+                float pb = 0.f;
+#pragma unroll
+                for (int i = 0; i < BW_ROWS; ++i) {
+                    const float4 sp = *reinterpret_cast<const float4 *>(scr + slice((size_t)r * KD * KD, i));
+                    float4 s1;   // S' = S_{t-1} Diag(e)
+                    s1.x = sp.x * e.x; s1.y = sp.y * e.y; s1.z = sp.z * e.z; s1.w = sp.w * e.w;
+                    const float d = warp_sum(s1.x * kh.x + s1.y * kh.y + s1.z * kh.z + s1.w * kh.w);
+                    const float vr = sv[r * KD + r0 + i], dor = sdo[r * KD + r0 + i];
+                    const float del = beta * (vr - d);
+                    float4 st;   // S_t
+                    st.x = fmaf(del, kh.x, s1.x); st.y = fmaf(del, kh.y, s1.y);
+                    st.z = fmaf(del, kh.z, s1.z); st.w = fmaf(del, kh.w, s1.w);
+                    // dS += do qt^T ; dqt += S_t^T do
+                    float4 g = dS[i];
+                    g.x = fmaf(dor, qt.x, g.x); g.y = fmaf(dor, qt.y, g.y); g.z = fmaf(dor, qt.z, g.z); g.w = fmaf(dor, qt.w, g.w);
+                    pq.x = fmaf(st.x, dor, pq.x); pq.y = fmaf(st.y, dor, pq.y);
+                    pq.z = fmaf(st.z, dor, pq.z); pq.w = fmaf(st.w, dor, pq.w);
+                    // ddel = dS kh ; dkh += dS^T delta
+                    const float ddel = warp_sum(g.x * kh.x + g.y * kh.y + g.z * kh.z + g.w * kh.w);
+                    pk.x = fmaf(g.x, del, pk.x); pk.y = fmaf(g.y, del, pk.y);
+                    pk.z = fmaf(g.z, del, pk.z); pk.w = fmaf(g.w, del, pk.w);
+                    if (lane == 0) p.dv[((size_t)(tok0 + r) * p.H_v + h) * KD + r0 + i] = beta * ddel;
+                    pb = fmaf(ddel, vr - d, pb);
+                    // dd = -beta ddel ; dS' = dS + dd kh^T ; dkh += S'^T dd ; de += S_{t-1} * dS'
+                    const float dd = -beta * ddel;
+                    g.x = fmaf(dd, kh.x, g.x); g.y = fmaf(dd, kh.y, g.y); g.z = fmaf(dd, kh.z, g.z); g.w = fmaf(dd, kh.w, g.w);
+                    pk.x = fmaf(s1.x, dd, pk.x); pk.y = fmaf(s1.y, dd, pk.y);
+                    pk.z = fmaf(s1.z, dd, pk.z); pk.w = fmaf(s1.w, dd, pk.w);
+                    pe.x = fmaf(sp.x, g.x, pe.x); pe.y = fmaf(sp.y, g.y, pe.y);
+                    pe.z = fmaf(sp.z, g.z, pe.z); pe.w = fmaf(sp.w, g.w, pe.w);
+                    // dS_{t-1} = dS' Diag(e)
+                    g.x *= e.x; g.y *= e.y; g.z *= e.z; g.w *= e.w;
+                    dS[i] = g;
+                }
+                // sums over the 16 warps' rows
+                reinterpret_cast<float4 *>(red + (warp * 3 + 0) * KD)[lane] = pq;
+                reinterpret_cast<float4 *>(red + (warp * 3 + 1) * KD)[lane] = pk;
+                reinterpret_cast<float4 *>(red + (warp * 3 + 2) * KD)[lane] = pe;
+                if (lane == 0) redb[warp] = pb;
+                __syncthreads();
+                if (tid < 3 * KD) {
+                    const int which = tid / KD, ch = tid % KD;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < BW_WARPS; ++w) acc += red[(w * 3 + which) * KD + ch];
+                    float *dst = which == 0 ? p.dqt : which == 1 ? p.dkh : p.de;
+                    dst[((size_t)(tok0 + r) * p.H_v + h) * KD + ch] = acc;
+                } else if (tid == 3 * KD) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < BW_WARPS; ++w) acc += redb[w];
+                    p.dbeta[(size_t)(tok0 + r) * p.H_v + h] = acc;
+                }
+                __syncthreads();
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(p.dh0 + slice(sh, i)) = dS[i];
+    }
+}
+
+// Per (token, query/key head): the prologue's Jacobians.  One 128-thread CTA, thread = channel.
+//   dq = scale r_q dqt_sum - scale r_q^3 q (q . dqt_sum),  r_q = 1 / sqrt(|q|^2 + eps)   (dk alike, scale 1)
+//   dgraw = de e (-a) sigmoid(graw),  dA_log += sum_c de e g,  db = dbeta beta (1 - beta)
+__global__ __launch_bounds__(KD) void bwd_prologue_kernel(const BwdParams p, float *dq, float *dk, float *dgraw,
+                                                          float *db, float *dA_log, long long tokens) {
+    __shared__ float red[4][4];
+    const long long blk = blockIdx.x;
+    const long long tok = blk / p.H_qk;
+    const int hq = (int)(blk % p.H_qk), c = threadIdx.x, lane = c & 31, w = c >> 5;
+    if (tok >= tokens) return;
+    const int group = p.H_v / p.H_qk;
+    const size_t qo = ((size_t)tok * p.H_qk + hq) * KD + c;
+    const float qv = bf16_to_f(p.q[qo]), kv = bf16_to_f(p.k[qo]);
+    float sq = 0.f, sk = 0.f;
+    for (int g = 0; g < group; ++g) {
+        const size_t ho = ((size_t)tok * p.H_v + hq * group + g) * KD + c;
+        sq += p.dqt[ho];
+        sk += p.dkh[ho];
+    }
+    auto block_sum = [&](float x, int slot) {
+        x = warp_sum(x);
+        if (lane == 0) red[slot][w] = x;
+        __syncthreads();
+        const float s = red[slot][0] + red[slot][1] + red[slot][2] + red[slot][3];
+        return s;
+    };
+    const float nq = block_sum(qv * qv, 0), nk = block_sum(kv * kv, 1);
+    const float qd = block_sum(qv * sq, 2), kd = block_sum(kv * sk, 3);
+    const float rq = rsqrtf(nq + L2_EPS), rk = rsqrtf(nk + L2_EPS);
+    dq[qo] = p.scale * rq * (sq - rq * rq * qv * qd);
+    dk[qo] = rk * (sk - rk * rk * kv * kd);
+    for (int g = 0; g < group; ++g) {
+        const int h = hq * group + g;
+        const size_t ho = ((size_t)tok * p.H_v + h) * KD + c;
+        const float a = ex2(p.A_log[h] * LOG2E);
+        const float gr = bf16_to_f(p.graw[ho]);
+        const float sp = softplus_log2(gr) * (1.0f / LOG2E);   // softplus (natural units)
+        const float gg = -a * sp, ee = __expf(gg);
+        const float sig = 1.0f / (1.0f + __expf(-gr));
+        const float dg = p.de[ho] * ee;
+        dgraw[ho] = dg * (-a) * sig;
+        float part = warp_sum(dg * gg);
+        if (lane == 0) atomicAdd(&dA_log[h], part);
+        if (c == 0) {
+            const float bb = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
+            const float beta = 1.0f / (1.0f + __expf(-bb));
+            db[(size_t)tok * p.H_v + h] = p.dbeta[(size_t)tok * p.H_v + h] * beta * (1.0f - beta);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+namespace {
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+}
+
+size_t bwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, int grid) {
+    const long long nseq = varlen ? N : B, nck = max_chunks_for(N, B, T, varlen), tokens = (long long)B * T;
+    size_t off = a256(256);
+    off = a256(off + sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1));
+    off = a256(off + sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1));
+    off = a256(off + sizeof(int) * (size_t)(nseq > 0 ? nseq : 1));
+    off = a256(off + (size_t)(nck > 0 ? nck : 1) * H_v * KD * KD * 4);    // checkpoints
+    off = a256(off + (size_t)grid * CH * KD * KD * 4);                    // scratch
+    off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * KD * 4 * 3);   // dqt, dkh, de
+    off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * 4);            // dbeta
+    return off;
+}
+
+int bwd_grid(int nseq, int H_v) {
+    int dev = 0, nsm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const long long items = (long long)nseq * H_v;
+    return (int)(items < nsm ? (items > 0 ? items : 1) : nsm);
+}
+
+cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                       const uint16_t *b, const float *A_log, float scale, const float *init, const int32_t *cu, int N,
+                       int B, int T, int H_qk, int H_v, const uint16_t *dout, const float *dht, float *dq, float *dk,
+                       float *dv, float *dgraw, float *db, float *dA_log, float *dh0, void *ws_ptr, int grid,
+                       cudaStream_t stream, int *launches) {
+    const bool varlen = cu != nullptr;
+    const int nseq = varlen ? N : B;
+    const long long nck = max_chunks_for(N, B, T, varlen), tokens = (long long)B * T;
+    char *base = static_cast<char *>(ws_ptr);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *p = base + off;
+        off = a256(off + bytes);
+        return p;
+    };
+    int *hdr = reinterpret_cast<int *>(take(256));
+    SeqDesc *seqs = reinterpret_cast<SeqDesc *>(take(sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1)));
+    ChunkDesc *chunks = reinterpret_cast<ChunkDesc *>(take(sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1)));
+    int *order = reinterpret_cast<int *>(take(sizeof(int) * (size_t)(nseq > 0 ? nseq : 1)));
+    BwdParams bp;
+    bp.ckpt = reinterpret_cast<float *>(take((size_t)(nck > 0 ? nck : 1) * H_v * KD * KD * 4));
+    bp.scratch = reinterpret_cast<float *>(take((size_t)grid * CH * KD * KD * 4));
+    const size_t tv = (size_t)(tokens > 0 ? tokens : 1) * H_v * KD;
+    float *t3 = reinterpret_cast<float *>(take(tv * 4 * 3));
+    bp.dqt = t3; bp.dkh = t3 + tv; bp.de = t3 + 2 * tv;
+    bp.dbeta = reinterpret_cast<float *>(take((size_t)(tokens > 0 ? tokens : 1) * H_v * 4));
+    bp.q = q; bp.k = k; bp.v = v; bp.graw = graw; bp.b = b; bp.dout = dout;
+    bp.A_log = A_log; bp.init = init; bp.dht = dht; bp.scale = scale;
+    bp.H_qk = H_qk; bp.H_v = H_v; bp.nseq = nseq; bp.seqs = seqs; bp.order = order; bp.hdr = hdr;
+    bp.dv = dv; bp.dh0 = dh0;
+    *launches = 0;
+    cudaError_t e = launch_plan(cu, N, B, T, seqs, chunks, order, hdr, nck, stream);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if ((e = cudaMemsetAsync(dA_log, 0, sizeof(float) * H_v, stream)) != cudaSuccess) return e;
+    if (nseq > 0) {
+        if ((e = cudaFuncSetAttribute(bwd_recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)(BW_BYTES + 128))) != cudaSuccess)
+            return e;
+        bwd_recur_kernel<<<grid, BW_THREADS, BW_BYTES + 128, stream>>>(bp);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (tokens > 0) {
+        bwd_prologue_kernel<<<(unsigned)(tokens * H_qk), KD, 0, stream>>>(bp, dq, dk, dgraw, db, dA_log, tokens);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace kda

@@ -67,6 +67,8 @@ def load() -> ctypes.CDLL:
     lib.kda_decode_step.restype = I
     lib.kda_decode_tokens.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, P, P]
     lib.kda_decode_tokens.restype = I
+    lib.kda_bwd.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P]
+    lib.kda_bwd.restype = I
     lib.kda_la_fwd.argtypes = [P, P, P, P, F, P, P, P, I, I, I, I, I, I, I, P, P]
     lib.kda_la_fwd.restype = I
     lib.kda_la_decode.argtypes = [P, P, P, P, F, P, I, I, I, I, I, P, P]
@@ -406,3 +408,40 @@ def kda_la_decode(q, k, v, slope, scale: float, state, out=None, stream=None) ->
                            H_v, K, V, _ptr(out), _stream(stream))
     _raise(rc, "kda_la_decode")
     return out
+
+
+def kda_bwd(q, k, v, graw, b, A_log, scale: float, dout, initial_state=None, cu_seqlens=None, dht=None,
+            stream=None) -> dict:
+    """Backward of ``kda_fwd``: returns fp32 gradients ``dq, dk`` [B,T,H_qk,K],
+    ``dv`` [B,T,H_v,V], ``dgraw`` [B,T,H_v,K], ``db`` [B,T,H_v], ``dA_log``
+    [H_v] and ``dh0`` [N,H_v,V,K] of a loss given ``dout`` (bf16, shape of
+    out) and optionally ``dht`` (fp32, shape of the final state)."""
+    lib = load()
+    B, T, H_qk, K = q.shape
+    H_v, V = v.shape[2], v.shape[3]
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    bf, f32 = torch.bfloat16, torch.float32
+    _check(q, "q", bf, (B, T, H_qk, K))
+    _check(k, "k", bf, (B, T, H_qk, K))
+    _check(v, "v", bf, (B, T, H_v, V))
+    _check(graw, "graw", bf, (B, T, H_v, K))
+    _check(b, "b", bf, (B, T, H_v))
+    _check(A_log, "A_log", f32, (H_v,))
+    _check(dout, "dout", bf, (B, T, H_v, V))
+    _check(initial_state, "initial_state", f32, (N, H_v, V, K), optional=True)
+    _check(dht, "dht", f32, (N, H_v, V, K), optional=True)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, optional=True)
+    dev = q.device
+    g = {"dq": torch.empty((B, T, H_qk, K), dtype=f32, device=dev),
+         "dk": torch.empty((B, T, H_qk, K), dtype=f32, device=dev),
+         "dv": torch.empty((B, T, H_v, V), dtype=f32, device=dev),
+         "dgraw": torch.empty((B, T, H_v, K), dtype=f32, device=dev),
+         "db": torch.empty((B, T, H_v), dtype=f32, device=dev),
+         "dA_log": torch.empty((H_v,), dtype=f32, device=dev),
+         "dh0": torch.empty((N, H_v, V, K), dtype=f32, device=dev)}
+    rc = lib.kda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
+                     _ptr(initial_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V, _ptr(dout), _ptr(dht),
+                     _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dgraw"]), _ptr(g["db"]), _ptr(g["dA_log"]),
+                     _ptr(g["dh0"]), _stream(stream))
+    _raise(rc, "kda_bwd")
+    return g

@@ -209,6 +209,34 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
                     cudaStream_t stream);
 
 /*
+ * Backward of kda_fwd: gradients of a loss L with respect to every input, given
+ * dL/dout and dL/dfinal_state.  The pages report timings of a gated-delta-rule
+ * backward (FlashQLA "benchmark_results_H200.txt", BACKWARD BENCHMARKS) without
+ * a formula; the gradients are those of the forward recurrence documented above.
+ *
+ *   inputs   q, k, v, graw, b, A_log, scale, initial_state, cu_seqlens, N, B, T,
+ *            H_qk, H_v, K, V exactly as kda_fwd
+ *   dout     [B, T, H_v, V] bf16 (dL/dout, required when B*T > 0)
+ *   dht      [N, H_v, V, K] fp32 (dL/dfinal_state) or NULL for zero
+ *   dq, dk   [B, T, H_qk, K] fp32 (summed over the value heads of each group)
+ *   dv       [B, T, H_v, V] fp32      dgraw [B, T, H_v, K] fp32    db [B, T, H_v] fp32
+ *   dA_log   [H_v] fp32               dh0 [N, H_v, V, K] fp32 (dL/dinitial_state)
+ *
+ * All outputs are written (dA_log is zeroed, then accumulated).  Gradient
+ * buffers must be 16-byte aligned (db excepted).  Asynchronous on `stream`; the
+ * workspace (state checkpoints at every 64-token chunk, 64 KiB per chunk and
+ * value head, plus per-CTA scratch and per-token partial gradients) comes from
+ * cudaMallocAsync on `stream`.  This is the token recurrence run backwards on
+ * CUDA cores in fp32 (one persistent CTA per (sequence, value head) chain);
+ * errors as kda_fwd.
+ */
+int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+            const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
+            const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V,
+            const kda_bf16_t *dout, const float *dht, float *dq, float *dk, float *dv, float *dgraw,
+            float *db, float *dA_log, float *dh0, cudaStream_t stream);
+
+/*
  * Lightning attention: linear attention with a fixed per-head decay.  The cuLA
  * page ("cuLA benchmark results on GB200") times a lightning-attention forward
  * (fixed-length and varlen tables) and a single-token la_decode with 64 heads of

@@ -1,0 +1,88 @@
+"""GPU parity tests of kda_bwd (the backward of the KDA forward) against the
+fp64 autograd oracle, through the C ABI.
+
+The GPU computes the token recurrence backwards in fp32 from the exact bf16 /
+fp32 inputs, so the gradients differ from the fp64 oracle by fp32 rounding
+accumulated over the sequence: each gradient tensor must match to relative L2
+<= 1e-3 and max-abs <= 1e-2 of its largest reference magnitude."""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as KI
+from oracle import backward as OB
+from kda_testutil import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-3
+MAX_FRAC = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_40_gb300 import kda
+    kda.load()
+    yield
+    assert kda.kda_get_status() == 0
+
+
+def _grads(inp, seed, with_dht=True):
+    g = torch.Generator().manual_seed(seed)
+    do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
+    dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1 if with_dht else None
+    return do, dht
+
+
+def _run(inp, do, dht):
+    from gated_delta_rule_40_gb300 import kda
+    dev = lambda t: None if t is None else t.cuda()  # noqa: E731
+    got = kda.kda_bwd(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.graw), dev(inp.b), dev(inp.A_log), inp.scale,
+                      dev(do), initial_state=dev(inp.initial_state), cu_seqlens=dev(inp.cu_seqlens), dht=dev(dht))
+    torch.cuda.synchronize()
+    return {k_: v_.double().cpu().numpy() for k_, v_ in got.items()}
+
+
+def _check(inp, seed, with_dht=True):
+    do, dht = _grads(inp, seed, with_dht)
+    got = _run(inp, do, dht)
+    ref = {k_: v_.numpy() for k_, v_ in OB.bwd_inputs(inp, do, dht).items()}
+    for name in ("dq", "dk", "dv", "dgraw", "db", "dA_log", "dh0"):
+        a, r = got[name], ref[name]
+        assert a.shape == r.shape, (name, a.shape, r.shape)
+        assert np.isfinite(a).all(), name
+        if r.size == 0 or not np.abs(r).max() > 0:
+            assert np.abs(a).max() <= 1e-6 if a.size else True, name
+            continue
+        e = rel_l2(a, r)
+        m = np.abs(a - r).max() / np.abs(r).max()
+        assert e <= REL and m <= MAX_FRAC, f"{name}: rel-L2 {e:.2e}, max {m:.2e}"
+
+
+@pytest.mark.parametrize("B,T,Hq,Hv", [(1, 100, 1, 2), (2, 70, 2, 2), (1, 129, 2, 4), (3, 1, 1, 1)])
+def test_bwd_ragged(B, T, Hq, Hv):
+    _check(KI.make_inputs(B, T, Hq, Hv, seed=700 + T, with_state=True), seed=1)
+
+
+def test_bwd_varlen_with_empty_sequences():
+    _check(KI.make_inputs(1, 200, 1, 2, seed=701, with_state=True, seqlens=[0, 65, 1, 0, 70, 64]), seed=2)
+
+
+def test_bwd_no_state_no_dht_and_harsh_gate():
+    _check(KI.make_inputs(1, 150, 1, 1, seed=702, with_state=False), seed=3, with_dht=False)
+    _check(KI.make_inputs(1, 130, 1, 1, seed=703, with_state=True, graw_mean=3.0, A_log_value=1.0), seed=4)
+
+
+def test_bwd_zero_tokens_passes_dht():
+    inp = KI.make_inputs(2, 0, 1, 2, seed=704, with_state=True)
+    do, dht = _grads(inp, 5)
+    got = _run(inp, do, dht)
+    assert np.array_equal(got["dh0"], dht.double().numpy())
+    assert np.abs(got["dA_log"]).max() == 0.0
+
+
+def test_bwd_longer_sequence():
+    """T = 1024 (16 chunks): checkpoints and the chunk-by-chunk reverse pass."""
+    _check(KI.make_inputs(1, 1024, 1, 1, seed=705, with_state=True), seed=6)
