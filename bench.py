@@ -41,6 +41,10 @@ BYTES_PER_TOKEN_HEAD = 1282
 STATE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4
 FLOPS_PER_TOKEN_HEAD = 139264
 # Decode step: state read + write (2 x 64 KiB per (b, h)) plus q/k/v/graw/b/out (~1.3 KB)
+# Backward (token recurrence run twice forwards and once backwards on CUDA cores): per token and
+# value head 2 x 3 K V (recomputed updates) + 11 K V (the backward step's products) multiply-adds,
+# 2 flops each.
+BWD_FLOPS_PER_TOKEN_HEAD = 2 * (2 * 3 + 11) * 128 * 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -431,6 +435,34 @@ def run_gpu(args, rank, world, local):
     if status != 0:
         raise RuntimeError(f"device status after the side measurements: {kda.status_string(status)}")
 
+    # ---- backward of the forward (kda_bwd) on the dense workload: all input gradients from dL/dout
+    # and dL/dfinal_state; the token recurrence on CUDA cores, so its roofline is the fp32 FMA rate
+    gd = torch.randn(out.shape, generator=torch.Generator().manual_seed(rank), dtype=torch.float32)
+    gout = gd.to(torch.bfloat16).to(dev)
+    ght = (torch.randn(fin.shape, generator=torch.Generator().manual_seed(rank + 1)) * 0.1).to(dev)
+    del gd
+
+    def bwd_step():
+        kda.kda_bwd(d["q"], d["k"], d["v"], d["graw"], d["b"], d["A_log"], inp.scale, gout,
+                    initial_state=d["initial_state"], dht=ght, stream=stream)
+
+    bwd_step()
+    torch.cuda.synchronize()
+    bwd_ms = time_events(bwd_step, 3, stream)
+    bwd_flops = units * BWD_FLOPS_PER_TOKEN_HEAD
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = sm_count * 128 * 2 * (clk.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    backward = {"workload": WORKLOAD, "ms": bwd_ms, "value": units / (bwd_ms * 1e-3), "unit": UNIT,
+                "roofline": {"bound": "alu", "achieved": bwd_flops / (bwd_ms * 1e-3) / 1e12,
+                             "peak": alu_peak, "unit": "TFLOP/s",
+                             "frac": bwd_flops / (bwd_ms * 1e-3) / 1e12 / alu_peak,
+                             "peak_source": "SMs x 128 fp32 lanes x 2 flops x max SM clock",
+                             "flops_per_token_head": BWD_FLOPS_PER_TOKEN_HEAD}}
+    del gout, ght
+    status = kda.kda_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status after the backward: {kda.status_string(status)}")
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp)
@@ -467,6 +499,7 @@ def run_gpu(args, rank, world, local):
         "decode_tokens": {"workload": "B=256 H=64 K=V=128, Tq tokens per pass, state in place", **multi},
         "decode": {"workload": "B=256 H=64 K=V=128 fp32 state in place", "ms": dec_ms, "GB/s": dec_gbs,
                    "hbm_peak": hbm_peak, "frac": dec_gbs / hbm_peak},
+        "backward": backward,
         "lightning": {"method": "linear attention with a fixed per-head decay (lightning attention)",
                       "slopes": "2^(-8 (h+1) / H)", **lightning},
         "gpu_launches": launches_per_step * args.steps,

@@ -15,17 +15,19 @@
 // then the prologue's Jacobians map dqt, dkh, de, dbeta to dq, dk, dgraw,
 // dA_log, db (dq and dk sum over the value heads of a query/key group).
 //
-// bwd_recur_kernel: persistent CTAs of 16 warps, one (sequence, value head)
-// chain at a time; warp w owns state rows 8w .. 8w + 7, lane owns channels
-// 4 lane .. 4 lane + 3, so S and dS live in registers (32 values each).  A
-// first pass runs the recurrence and stores the state at every 64-token chunk
-// start; the backward pass then takes the chunks in reverse: it recomputes the
-// chunk's states from its checkpoint into a per-CTA scratch area (each thread
-// reads back only what it wrote), then walks the chunk's tokens backwards.
-// The per-token vectors (qt, kh, e, v, do, beta) of a chunk are staged in
-// shared memory; the sums over v of dqt, dkh, de and dbeta are reduced across
-// warps through shared memory and written per (token, head) for
-// bwd_prologue_kernel.  This is the token recurrence on CUDA cores in fp32, a
+// bwd_recur_kernel: persistent CTAs of 8 warps, two per SM, one (sequence,
+// value head, quarter of the state rows) item at a time: the 128 rows of a
+// chain are independent, so four CTAs share a chain.  Warp w owns rows
+// 4w .. 4w + 3 of the quarter, lane owns channels 4 lane .. 4 lane + 3, so S and
+// dS live in registers (16 values each).  A first pass runs the recurrence and
+// stores the state at every 32-token block start; the backward pass then takes
+// the blocks in reverse: it recomputes the block's states from its checkpoint
+// into a per-CTA scratch area (512 KiB; each thread reads back only what it
+// wrote), then walks the block's tokens backwards.  The per-token vectors (qt,
+// kh, e, v, do, beta) of a block are staged in shared memory; the sums over the
+// quarter's rows of dqt, dkh, de and dbeta are reduced across warps through
+// shared memory and written per (token, head, quarter) for bwd_prologue_kernel,
+// which adds the quarters and the value heads of a group.  This is the token recurrence on CUDA cores in fp32, a
 // correct first form; its cost is O(T K V) per chain with no tensor-core use.
 #include "kda_common.cuh"
 
@@ -35,16 +37,18 @@ cudaError_t launch_plan(const int32_t *cu, int N, int B, int T, SeqDesc *seqs, C
                         int *hdr, long long max_chunks, cudaStream_t stream);
 long long max_chunks_for(int N, int B, int T, bool varlen);
 
-constexpr int BW_WARPS = 16;
+constexpr int BW_WARPS = 8;
 constexpr int BW_THREADS = BW_WARPS * 32;
-constexpr int BW_ROWS = KD / BW_WARPS;   // 8 state rows per warp
-constexpr uint32_t BW_VEC = CH * KD * 4;  // one [64][128] fp32 table
+constexpr int BW_PARTS = 4;                            // CTAs per chain
+constexpr int BW_ROWS = KD / BW_PARTS / BW_WARPS;      // 4 state rows per warp
+constexpr int BW_CT = 32;                              // tokens per block (checkpoint interval)
+constexpr uint32_t BW_VEC = BW_CT * KD * 4;            // one [32][128] fp32 table
 constexpr uint32_t BW_QT = 0, BW_KH = BW_VEC, BW_E = 2 * BW_VEC, BW_V = 3 * BW_VEC, BW_DO = 4 * BW_VEC;
-constexpr uint32_t BW_BETA = 5 * BW_VEC;            // [64]
-constexpr uint32_t BW_RED = BW_BETA + 256;          // [16 warps][3][128]
-constexpr uint32_t BW_REDB = BW_RED + BW_WARPS * 3 * KD * 4;   // [16]
+constexpr uint32_t BW_BETA = 5 * BW_VEC;            // [32]
+constexpr uint32_t BW_RED = BW_BETA + 128;          // 2 x [8 warps][3][128] (alternating tokens)
+constexpr uint32_t BW_REDB = BW_RED + 2 * BW_WARPS * 3 * KD * 4;   // 2 x [8]
 constexpr uint32_t BW_BYTES = BW_REDB + 64;
-static_assert(BW_BYTES <= 227 * 1024, "backward shared memory");
+static_assert(2 * (BW_BYTES + 128 + 1024) <= 228 * 1024, "two backward CTAs per SM");
 
 struct BwdParams {
     const uint16_t *q, *k, *v, *graw, *b, *dout;
@@ -54,13 +58,13 @@ struct BwdParams {
     const SeqDesc *seqs;
     const int *order;
     const int *hdr;
-    float *ckpt;      // [chunk][H_v][V][K]
-    float *scratch;   // [gridDim.x][64][V][K]
-    float *dqt, *dkh, *de, *dbeta;   // [token][H_v][128] (dbeta [token][H_v])
+    float *ckpt;      // [2 chunk + block][H_v][V][K]
+    float *scratch;   // [gridDim.x][32][32 rows][K]
+    float *dqt, *dkh, *de, *dbeta;   // [token][H_v][part][128] (dbeta [token][H_v][part])
     float *dv, *dh0;                 // [token][H_v][V], [N][H_v][V][K]
 };
 
-// Per-token vectors of tokens tok0 .. tok0 + len - 1 into the shared tables; warp w takes tokens w, w + 16, ...
+// Per-token vectors of tokens tok0 .. tok0 + len - 1 into the shared tables; warp w takes tokens w, w + 8, ...
 __device__ __forceinline__ void bwd_stage_chunk(const BwdParams &p, unsigned char *sm, int tok0, int len, int h,
                                                 int hq, float a_gate, bool with_do, int warp, int lane) {
     float *sqt = reinterpret_cast<float *>(sm + BW_QT), *skh = reinterpret_cast<float *>(sm + BW_KH);
@@ -106,7 +110,7 @@ __device__ __forceinline__ void bwd_stage_chunk(const BwdParams &p, unsigned cha
     }
 }
 
-// One forward token on this thread's 8 rows x 4 channels: S <- S Diag(e) + beta (v - S Diag(e) kh) kh^T.
+// One forward token on this thread's 4 rows x 4 channels: S <- S Diag(e) + beta (v - S Diag(e) kh) kh^T.
 // Returns nothing; S is updated in place.
 __device__ __forceinline__ void bwd_fwd_token(float4 (&S)[BW_ROWS], const float4 kh, const float4 e, float beta,
                                               const float *vrow, int r0) {
@@ -121,39 +125,42 @@ __device__ __forceinline__ void bwd_fwd_token(float4 (&S)[BW_ROWS], const float4
     }
 }
 
-__global__ __launch_bounds__(BW_THREADS, 1) void bwd_recur_kernel(const BwdParams p) {
+__global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
     if (p.hdr[1] == 0) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r0 = warp * BW_ROWS;
     const float *sqt = reinterpret_cast<const float *>(sm + BW_QT), *skh = reinterpret_cast<const float *>(sm + BW_KH);
     const float *se = reinterpret_cast<const float *>(sm + BW_E), *sv = reinterpret_cast<const float *>(sm + BW_V);
     const float *sdo = reinterpret_cast<const float *>(sm + BW_DO), *sbeta = reinterpret_cast<const float *>(sm + BW_BETA);
     float *red = reinterpret_cast<float *>(sm + BW_RED), *redb = reinterpret_cast<float *>(sm + BW_REDB);
-    float *scr = p.scratch + (size_t)blockIdx.x * CH * KD * KD;
-    const int n_items = p.nseq * p.H_v;
+    float *scr = p.scratch + (size_t)blockIdx.x * BW_CT * (KD / BW_PARTS) * KD;
+    const int n_items = p.nseq * p.H_v * BW_PARTS;
     const int group = p.H_v / p.H_qk;
 
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int h = item % p.H_v, seq = p.order[item / p.H_v], hq = h / group;
+        const int part = item % BW_PARTS, h = (item / BW_PARTS) % p.H_v;
+        const int seq = p.order[item / (BW_PARTS * p.H_v)], hq = h / group;
         const SeqDesc sd = p.seqs[seq];
+        const int nblk = (sd.len + BW_CT - 1) / BW_CT;
         const float a_gate = ex2(p.A_log[h] * LOG2E);
-        // this thread's slice of a [V][K] matrix: rows r0 + i, channels 4 lane ..
+        // rows of this thread in the full [V][K] matrix, and their offset within the quarter
+        const int r0 = part * (KD / BW_PARTS) + warp * BW_ROWS, q0 = warp * BW_ROWS;
         const size_t sh = ((size_t)seq * p.H_v + h) * KD * KD;
         auto slice = [&](size_t base, int i) { return base + (size_t)(r0 + i) * KD + 4 * lane; };
+        auto sslice = [&](int r, int i) { return ((size_t)r * (KD / BW_PARTS) + q0 + i) * KD + 4 * lane; };
         float4 S[BW_ROWS];
 #pragma unroll
         for (int i = 0; i < BW_ROWS; ++i)
             S[i] = p.init ? *reinterpret_cast<const float4 *>(p.init + slice(sh, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
 
-        // ---- pass 1: the recurrence, storing the state at each chunk start
-        for (int c = 0; c < sd.nchunk; ++c) {
-            const int len = min(CH, sd.len - c * CH), tok0 = sd.tok + c * CH;
-            const size_t cb = ((size_t)(sd.chunk0 + c) * p.H_v + h) * KD * KD;
+        // ---- pass 1: the recurrence, storing the state at each block start
+        for (int c = 0; c < nblk; ++c) {
+            const int len = min(BW_CT, sd.len - c * BW_CT), tok0 = sd.tok + c * BW_CT;
+            const size_t cb = ((size_t)(2 * sd.chunk0 + c) * p.H_v + h) * KD * KD;
 #pragma unroll
             for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(p.ckpt + slice(cb, i)) = S[i];
-            __syncthreads();   // the previous chunk's tables are no longer read
+            __syncthreads();   // the previous block's tables are no longer read
             bwd_stage_chunk(p, sm, tok0, len, h, hq, a_gate, false, warp, lane);
             __syncthreads();
             for (int r = 0; r < len; ++r)
@@ -161,28 +168,32 @@ __global__ __launch_bounds__(BW_THREADS, 1) void bwd_recur_kernel(const BwdParam
                               reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0);
         }
 
-        // ---- pass 2: chunks in reverse
+        // ---- pass 2: blocks in reverse
         float4 dS[BW_ROWS];
 #pragma unroll
         for (int i = 0; i < BW_ROWS; ++i)
             dS[i] = p.dht ? *reinterpret_cast<const float4 *>(p.dht + slice(sh, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = sd.nchunk - 1; c >= 0; --c) {
-            const int len = min(CH, sd.len - c * CH), tok0 = sd.tok + c * CH;
-            const size_t cb = ((size_t)(sd.chunk0 + c) * p.H_v + h) * KD * KD;
+        for (int c = nblk - 1; c >= 0; --c) {
+            const int len = min(BW_CT, sd.len - c * BW_CT), tok0 = sd.tok + c * BW_CT;
+            const size_t cb = ((size_t)(2 * sd.chunk0 + c) * p.H_v + h) * KD * KD;
             __syncthreads();
             bwd_stage_chunk(p, sm, tok0, len, h, hq, a_gate, true, warp, lane);
             __syncthreads();
-            // recompute the chunk's states; scratch[r] = state before token r (this thread's slice)
+            // recompute the block's states; scratch[r] = state before token r (this thread's slice)
 #pragma unroll
             for (int i = 0; i < BW_ROWS; ++i) S[i] = *reinterpret_cast<const float4 *>(p.ckpt + slice(cb, i));
             for (int r = 0; r < len; ++r) {
 #pragma unroll
-                for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(scr + slice((size_t)r * KD * KD, i)) = S[i];
+                for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(scr + sslice(r, i)) = S[i];
                 if (r + 1 < len)
                     bwd_fwd_token(S, reinterpret_cast<const float4 *>(skh + r * KD)[lane],
                                   reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0);
             }
-            // tokens backwards
+            // tokens backwards; the states of token r - 1 are loaded while token r is processed, and the
+            // reduction areas alternate so one barrier per token suffices
+            float4 spn[BW_ROWS];
+#pragma unroll
+            for (int i = 0; i < BW_ROWS; ++i) spn[i] = *reinterpret_cast<const float4 *>(scr + sslice(len - 1, i));
             for (int r = len - 1; r >= 0; --r) {
                 const float4 kh = reinterpret_cast<const float4 *>(skh + r * KD)[lane];
                 const float4 qt = reinterpret_cast<const float4 *>(sqt + r * KD)[lane];
@@ -190,11 +201,17 @@ __global__ __launch_bounds__(BW_THREADS, 1) void bwd_recur_kernel(const BwdParam
                 const float beta = sbeta[r];
                 float4 pq = make_float4(0.f, 0.f, 0.f, 0.f), pk = pq, pe = pq;
                 float pb = 0.f;
+                float4 sp[BW_ROWS];
+#pragma unroll
+                for (int i = 0; i < BW_ROWS; ++i) sp[i] = spn[i];
+                if (r > 0) {
+#pragma unroll
+                    for (int i = 0; i < BW_ROWS; ++i) spn[i] = *reinterpret_cast<const float4 *>(scr + sslice(r - 1, i));
+                }
 #pragma unroll
                 for (int i = 0; i < BW_ROWS; ++i) {
-                    const float4 sp = *reinterpret_cast<const float4 *>(scr + slice((size_t)r * KD * KD, i));
                     float4 s1;   // S' = S_{t-1} Diag(e)
-                    s1.x = sp.x * e.x; s1.y = sp.y * e.y; s1.z = sp.z * e.z; s1.w = sp.w * e.w;
+                    s1.x = sp[i].x * e.x; s1.y = sp[i].y * e.y; s1.z = sp[i].z * e.z; s1.w = sp[i].w * e.w;
                     const float d = warp_sum(s1.x * kh.x + s1.y * kh.y + s1.z * kh.z + s1.w * kh.w);
                     const float vr = sv[r * KD + r0 + i], dor = sdo[r * KD + r0 + i];
                     const float del = beta * (vr - d);
@@ -217,32 +234,34 @@ __global__ __launch_bounds__(BW_THREADS, 1) void bwd_recur_kernel(const BwdParam
                     g.x = fmaf(dd, kh.x, g.x); g.y = fmaf(dd, kh.y, g.y); g.z = fmaf(dd, kh.z, g.z); g.w = fmaf(dd, kh.w, g.w);
                     pk.x = fmaf(s1.x, dd, pk.x); pk.y = fmaf(s1.y, dd, pk.y);
                     pk.z = fmaf(s1.z, dd, pk.z); pk.w = fmaf(s1.w, dd, pk.w);
-                    pe.x = fmaf(sp.x, g.x, pe.x); pe.y = fmaf(sp.y, g.y, pe.y);
-                    pe.z = fmaf(sp.z, g.z, pe.z); pe.w = fmaf(sp.w, g.w, pe.w);
+                    pe.x = fmaf(sp[i].x, g.x, pe.x); pe.y = fmaf(sp[i].y, g.y, pe.y);
+                    pe.z = fmaf(sp[i].z, g.z, pe.z); pe.w = fmaf(sp[i].w, g.w, pe.w);
                     // dS_{t-1} = dS' Diag(e)
                     g.x *= e.x; g.y *= e.y; g.z *= e.z; g.w *= e.w;
                     dS[i] = g;
                 }
-                // sums over the 16 warps' rows
-                reinterpret_cast<float4 *>(red + (warp * 3 + 0) * KD)[lane] = pq;
-                reinterpret_cast<float4 *>(red + (warp * 3 + 1) * KD)[lane] = pk;
-                reinterpret_cast<float4 *>(red + (warp * 3 + 2) * KD)[lane] = pe;
-                if (lane == 0) redb[warp] = pb;
+                // sums over the quarter's rows (8 warps)
+                float *rd = red + (r & 1) * (BW_WARPS * 3 * KD), *rdb = redb + (r & 1) * BW_WARPS;
+                reinterpret_cast<float4 *>(rd + (warp * 3 + 0) * KD)[lane] = pq;
+                reinterpret_cast<float4 *>(rd + (warp * 3 + 1) * KD)[lane] = pk;
+                reinterpret_cast<float4 *>(rd + (warp * 3 + 2) * KD)[lane] = pe;
+                if (lane == 0) rdb[warp] = pb;
                 __syncthreads();
-                if (tid < 3 * KD) {
-                    const int which = tid / KD, ch = tid % KD;
+                const size_t tp = ((size_t)(tok0 + r) * p.H_v + h) * BW_PARTS + part;
+                for (int x = tid; x < 3 * KD; x += BW_THREADS) {
+                    const int which = x / KD, ch = x % KD;
                     float acc = 0.f;
 #pragma unroll
-                    for (int w = 0; w < BW_WARPS; ++w) acc += red[(w * 3 + which) * KD + ch];
+                    for (int w = 0; w < BW_WARPS; ++w) acc += rd[(w * 3 + which) * KD + ch];
                     float *dst = which == 0 ? p.dqt : which == 1 ? p.dkh : p.de;
-                    dst[((size_t)(tok0 + r) * p.H_v + h) * KD + ch] = acc;
-                } else if (tid == 3 * KD) {
+                    dst[tp * KD + ch] = acc;
+                }
+                if (tid == 0) {
                     float acc = 0.f;
 #pragma unroll
-                    for (int w = 0; w < BW_WARPS; ++w) acc += redb[w];
-                    p.dbeta[(size_t)(tok0 + r) * p.H_v + h] = acc;
+                    for (int w = 0; w < BW_WARPS; ++w) acc += rdb[w];
+                    p.dbeta[tp] = acc;
                 }
-                __syncthreads();
             }
         }
 #pragma unroll
@@ -264,11 +283,13 @@ __global__ __launch_bounds__(KD) void bwd_prologue_kernel(const BwdParams p, flo
     const size_t qo = ((size_t)tok * p.H_qk + hq) * KD + c;
     const float qv = bf16_to_f(p.q[qo]), kv = bf16_to_f(p.k[qo]);
     float sq = 0.f, sk = 0.f;
-    for (int g = 0; g < group; ++g) {
-        const size_t ho = ((size_t)tok * p.H_v + hq * group + g) * KD + c;
-        sq += p.dqt[ho];
-        sk += p.dkh[ho];
-    }
+    for (int g = 0; g < group; ++g)
+#pragma unroll
+        for (int pt = 0; pt < BW_PARTS; ++pt) {
+            const size_t ho = (((size_t)tok * p.H_v + hq * group + g) * BW_PARTS + pt) * KD + c;
+            sq += p.dqt[ho];
+            sk += p.dkh[ho];
+        }
     auto block_sum = [&](float x, int slot) {
         x = warp_sum(x);
         if (lane == 0) red[slot][w] = x;
@@ -289,14 +310,20 @@ __global__ __launch_bounds__(KD) void bwd_prologue_kernel(const BwdParams p, flo
         const float sp = softplus_log2(gr) * (1.0f / LOG2E);   // softplus (natural units)
         const float gg = -a * sp, ee = __expf(gg);
         const float sig = 1.0f / (1.0f + __expf(-gr));
-        const float dg = p.de[ho] * ee;
+        float de_sum = 0.f, dbeta_sum = 0.f;
+#pragma unroll
+        for (int pt = 0; pt < BW_PARTS; ++pt) {
+            de_sum += p.de[(((size_t)tok * p.H_v + h) * BW_PARTS + pt) * KD + c];
+            dbeta_sum += p.dbeta[((size_t)tok * p.H_v + h) * BW_PARTS + pt];
+        }
+        const float dg = de_sum * ee;
         dgraw[ho] = dg * (-a) * sig;
         float part = warp_sum(dg * gg);
         if (lane == 0) atomicAdd(&dA_log[h], part);
         if (c == 0) {
             const float bb = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
             const float beta = 1.0f / (1.0f + __expf(-bb));
-            db[(size_t)tok * p.H_v + h] = p.dbeta[(size_t)tok * p.H_v + h] * beta * (1.0f - beta);
+            db[(size_t)tok * p.H_v + h] = dbeta_sum * beta * (1.0f - beta);
         }
     }
 }
@@ -312,10 +339,10 @@ size_t bwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, int grid) 
     off = a256(off + sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1));
     off = a256(off + sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1));
     off = a256(off + sizeof(int) * (size_t)(nseq > 0 ? nseq : 1));
-    off = a256(off + (size_t)(nck > 0 ? nck : 1) * H_v * KD * KD * 4);    // checkpoints
-    off = a256(off + (size_t)grid * CH * KD * KD * 4);                    // scratch
-    off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * KD * 4 * 3);   // dqt, dkh, de
-    off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * 4);            // dbeta
+    off = a256(off + (size_t)2 * (nck > 0 ? nck : 1) * H_v * KD * KD * 4);       // checkpoints
+    off = a256(off + (size_t)grid * BW_CT * (KD / BW_PARTS) * KD * 4);          // scratch
+    off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * KD * 4 * 3);   // dqt, dkh, de
+    off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * 4);            // dbeta
     return off;
 }
 
@@ -323,8 +350,8 @@ int bwd_grid(int nseq, int H_v) {
     int dev = 0, nsm = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    const long long items = (long long)nseq * H_v;
-    return (int)(items < nsm ? (items > 0 ? items : 1) : nsm);
+    const long long items = (long long)nseq * H_v * BW_PARTS, slots = 2LL * nsm;
+    return (int)(items < slots ? (items > 0 ? items : 1) : slots);
 }
 
 cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
@@ -347,12 +374,12 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     ChunkDesc *chunks = reinterpret_cast<ChunkDesc *>(take(sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1)));
     int *order = reinterpret_cast<int *>(take(sizeof(int) * (size_t)(nseq > 0 ? nseq : 1)));
     BwdParams bp;
-    bp.ckpt = reinterpret_cast<float *>(take((size_t)(nck > 0 ? nck : 1) * H_v * KD * KD * 4));
-    bp.scratch = reinterpret_cast<float *>(take((size_t)grid * CH * KD * KD * 4));
-    const size_t tv = (size_t)(tokens > 0 ? tokens : 1) * H_v * KD;
+    bp.ckpt = reinterpret_cast<float *>(take((size_t)2 * (nck > 0 ? nck : 1) * H_v * KD * KD * 4));
+    bp.scratch = reinterpret_cast<float *>(take((size_t)grid * BW_CT * (KD / BW_PARTS) * KD * 4));
+    const size_t tv = (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * KD;
     float *t3 = reinterpret_cast<float *>(take(tv * 4 * 3));
     bp.dqt = t3; bp.dkh = t3 + tv; bp.de = t3 + 2 * tv;
-    bp.dbeta = reinterpret_cast<float *>(take((size_t)(tokens > 0 ? tokens : 1) * H_v * 4));
+    bp.dbeta = reinterpret_cast<float *>(take((size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * 4));
     bp.q = q; bp.k = k; bp.v = v; bp.graw = graw; bp.b = b; bp.dout = dout;
     bp.A_log = A_log; bp.init = init; bp.dht = dht; bp.scale = scale;
     bp.H_qk = H_qk; bp.H_v = H_v; bp.nseq = nseq; bp.seqs = seqs; bp.order = order; bp.hdr = hdr;
