@@ -2,10 +2,12 @@
 
     python -m gated_delta_rule_40_gb300.profile_case --B 1 --T 8192 --H 32 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method la --B 1 --T 8192 --H 64 --iters 4
+    python -m gated_delta_rule_40_gb300.profile_case --method bwd --B 1 --T 2048 --H 8 --iters 3
 
 Inputs come from ``kda_inputs`` (same recipe as the tests and the benchmark);
 the workspace is allocated once, so every iteration is exactly the three
-kernel launches of ``kda_fwd`` (two for ``kda_la_fwd``: plan and la_fwd_kernel).  A profiler then selects launches by kernel
+kernel launches of ``kda_fwd`` (two for ``kda_la_fwd``: plan and la_fwd_kernel; three for
+``kda_bwd``: plan, bwd_recur_kernel and bwd_prologue_kernel).  A profiler then selects launches by kernel
 name and index (e.g. ``ncu -k regex:intra_kernel -s 2 -c 1``).
 """
 import argparse
@@ -26,7 +28,7 @@ def main() -> None:
     ap.add_argument("--H", type=int, default=32, help="value heads (= q/k heads)")
     ap.add_argument("--iters", type=int, default=4)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--method", choices=["kda", "la"], default="kda")
+    ap.add_argument("--method", choices=["kda", "la", "bwd"], default="kda")
     a = ap.parse_args()
     if a.method == "la":
         x = kda_inputs.make_la_inputs(a.B, a.T, a.H, a.H, seed=a.seed)
@@ -38,6 +40,16 @@ def main() -> None:
               f"|S| {float(fin.abs().mean()):.6f}")
         return
     x = kda_inputs.make_inputs(B=a.B, T=a.T, H_qk=a.H, H_v=a.H, seed=a.seed, with_state=True)
+    if a.method == "bwd":
+        g = torch.Generator().manual_seed(a.seed + 1)
+        dout = torch.randn(x.v.shape, generator=g).to(torch.bfloat16).cuda()
+        q, k, v, gr, b, A, s0 = (t.cuda() for t in (x.q, x.k, x.v, x.graw, x.b, x.A_log, x.initial_state))
+        for _ in range(a.iters):
+            grads = kda.kda_bwd(q, k, v, gr, b, A, x.scale, dout, initial_state=s0)
+        torch.cuda.synchronize()
+        print(f"kda_bwd B={a.B} T={a.T} H={a.H} x{a.iters}: |dq| {float(grads['dq'].abs().mean()):.6f} "
+              f"|dh0| {float(grads['dh0'].abs().mean()):.6f}")
+        return
     dev = lambda t: t.cuda() if t is not None else None  # noqa: E731
     q, k, v, g, b, A, s0 = map(dev, (x.q, x.k, x.v, x.graw, x.b, x.A_log, x.initial_state))
     ws = torch.empty(kda.kda_fwd_workspace_size(a.B, a.B, a.T, a.H, a.H), dtype=torch.uint8, device="cuda")
