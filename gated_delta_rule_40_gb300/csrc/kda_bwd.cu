@@ -110,18 +110,47 @@ __device__ __forceinline__ void bwd_stage_chunk(const BwdParams &p, unsigned cha
     }
 }
 
+// Warp sums of four per-lane partials (one per state row), returned on every lane.  A
+// reduce-scatter (xor 16 keeps two rows, xor 8 one, xor 4, 2, 1 finish it) leaves lane l with
+// the sum of row 2 b4 + b3 (b = bits of l); four broadcasts return them: 10 shuffles instead
+// of 20 for four butterflies.
+__device__ __forceinline__ void warp_sum4(float (&a)[4], int lane) {
+    const bool u16 = (lane & 16) != 0, u8 = (lane & 8) != 0;
+    float b0 = u16 ? a[2] : a[0], b1 = u16 ? a[3] : a[1];
+    const float s0 = u16 ? a[0] : a[2], s1 = u16 ? a[1] : a[3];
+    b0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+    b1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+    float c = u8 ? b1 : b0;
+    c += __shfl_xor_sync(0xffffffffu, u8 ? b0 : b1, 8);
+    c += __shfl_xor_sync(0xffffffffu, c, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    a[0] = __shfl_sync(0xffffffffu, c, 0);
+    a[1] = __shfl_sync(0xffffffffu, c, 8);
+    a[2] = __shfl_sync(0xffffffffu, c, 16);
+    a[3] = __shfl_sync(0xffffffffu, c, 24);
+}
+static_assert(BW_ROWS == 4, "warp_sum4 reduces four rows");
+
+__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
+    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+}
+
 // One forward token on this thread's 4 rows x 4 channels: S <- S Diag(e) + beta (v - S Diag(e) kh) kh^T.
-// Returns nothing; S is updated in place.
 __device__ __forceinline__ void bwd_fwd_token(float4 (&S)[BW_ROWS], const float4 kh, const float4 e, float beta,
-                                              const float *vrow, int r0) {
+                                              const float *vrow, int r0, int lane) {
+    float d[BW_ROWS];
 #pragma unroll
     for (int i = 0; i < BW_ROWS; ++i) {
-        float4 x = S[i];
-        x.x *= e.x; x.y *= e.y; x.z *= e.z; x.w *= e.w;
-        const float d = warp_sum(x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w);
-        const float del = beta * (vrow[r0 + i] - d);
-        x.x = fmaf(del, kh.x, x.x); x.y = fmaf(del, kh.y, x.y); x.z = fmaf(del, kh.z, x.z); x.w = fmaf(del, kh.w, x.w);
-        S[i] = x;
+        S[i].x *= e.x; S[i].y *= e.y; S[i].z *= e.z; S[i].w *= e.w;
+        d[i] = dot4(S[i], kh);
+    }
+    warp_sum4(d, lane);
+#pragma unroll
+    for (int i = 0; i < BW_ROWS; ++i) {
+        const float del = beta * (vrow[r0 + i] - d[i]);
+        S[i].x = fmaf(del, kh.x, S[i].x); S[i].y = fmaf(del, kh.y, S[i].y);
+        S[i].z = fmaf(del, kh.z, S[i].z); S[i].w = fmaf(del, kh.w, S[i].w);
     }
 }
 
@@ -165,7 +194,7 @@ __global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParam
             __syncthreads();
             for (int r = 0; r < len; ++r)
                 bwd_fwd_token(S, reinterpret_cast<const float4 *>(skh + r * KD)[lane],
-                              reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0);
+                              reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0, lane);
         }
 
         // ---- pass 2: blocks in reverse
@@ -187,7 +216,7 @@ __global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParam
                 for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(scr + sslice(r, i)) = S[i];
                 if (r + 1 < len)
                     bwd_fwd_token(S, reinterpret_cast<const float4 *>(skh + r * KD)[lane],
-                                  reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0);
+                                  reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0, lane);
             }
             // tokens backwards; the states of token r - 1 are loaded while token r is processed, and the
             // reduction areas alternate so one barrier per token suffices
@@ -208,37 +237,49 @@ __global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParam
 #pragma unroll
                     for (int i = 0; i < BW_ROWS; ++i) spn[i] = *reinterpret_cast<const float4 *>(scr + sslice(r - 1, i));
                 }
+                // S' = S_{t-1} Diag(e) and d = S' kh for the four rows
+                float4 s1[BW_ROWS], g[BW_ROWS];
+                float d[BW_ROWS], dd4[BW_ROWS], del[BW_ROWS];
 #pragma unroll
                 for (int i = 0; i < BW_ROWS; ++i) {
-                    float4 s1;   // S' = S_{t-1} Diag(e)
-                    s1.x = sp[i].x * e.x; s1.y = sp[i].y * e.y; s1.z = sp[i].z * e.z; s1.w = sp[i].w * e.w;
-                    const float d = warp_sum(s1.x * kh.x + s1.y * kh.y + s1.z * kh.z + s1.w * kh.w);
-                    const float vr = sv[r * KD + r0 + i], dor = sdo[r * KD + r0 + i];
-                    const float del = beta * (vr - d);
-                    float4 st;   // S_t
-                    st.x = fmaf(del, kh.x, s1.x); st.y = fmaf(del, kh.y, s1.y);
-                    st.z = fmaf(del, kh.z, s1.z); st.w = fmaf(del, kh.w, s1.w);
-                    // dS += do qt^T ; dqt += S_t^T do
-                    float4 g = dS[i];
-                    g.x = fmaf(dor, qt.x, g.x); g.y = fmaf(dor, qt.y, g.y); g.z = fmaf(dor, qt.z, g.z); g.w = fmaf(dor, qt.w, g.w);
+                    s1[i].x = sp[i].x * e.x; s1[i].y = sp[i].y * e.y; s1[i].z = sp[i].z * e.z; s1[i].w = sp[i].w * e.w;
+                    d[i] = dot4(s1[i], kh);
+                }
+                warp_sum4(d, lane);
+                // delta, S_t; dS += do qt^T; dqt += S_t^T do; ddel = dS kh
+#pragma unroll
+                for (int i = 0; i < BW_ROWS; ++i) {
+                    const float dor = sdo[r * KD + r0 + i];
+                    del[i] = beta * (sv[r * KD + r0 + i] - d[i]);
+                    float4 st;
+                    st.x = fmaf(del[i], kh.x, s1[i].x); st.y = fmaf(del[i], kh.y, s1[i].y);
+                    st.z = fmaf(del[i], kh.z, s1[i].z); st.w = fmaf(del[i], kh.w, s1[i].w);
+                    g[i] = dS[i];
+                    g[i].x = fmaf(dor, qt.x, g[i].x); g[i].y = fmaf(dor, qt.y, g[i].y);
+                    g[i].z = fmaf(dor, qt.z, g[i].z); g[i].w = fmaf(dor, qt.w, g[i].w);
                     pq.x = fmaf(st.x, dor, pq.x); pq.y = fmaf(st.y, dor, pq.y);
                     pq.z = fmaf(st.z, dor, pq.z); pq.w = fmaf(st.w, dor, pq.w);
-                    // ddel = dS kh ; dkh += dS^T delta
-                    const float ddel = warp_sum(g.x * kh.x + g.y * kh.y + g.z * kh.z + g.w * kh.w);
-                    pk.x = fmaf(g.x, del, pk.x); pk.y = fmaf(g.y, del, pk.y);
-                    pk.z = fmaf(g.z, del, pk.z); pk.w = fmaf(g.w, del, pk.w);
+                    dd4[i] = dot4(g[i], kh);
+                }
+                warp_sum4(dd4, lane);   // ddel per row
+#pragma unroll
+                for (int i = 0; i < BW_ROWS; ++i) {
+                    const float ddel = dd4[i];
+                    // dkh += dS^T delta ; dv ; dbeta
+                    pk.x = fmaf(g[i].x, del[i], pk.x); pk.y = fmaf(g[i].y, del[i], pk.y);
+                    pk.z = fmaf(g[i].z, del[i], pk.z); pk.w = fmaf(g[i].w, del[i], pk.w);
                     if (lane == 0) p.dv[((size_t)(tok0 + r) * p.H_v + h) * KD + r0 + i] = beta * ddel;
-                    pb = fmaf(ddel, vr - d, pb);
+                    pb = fmaf(ddel, sv[r * KD + r0 + i] - d[i], pb);
                     // dd = -beta ddel ; dS' = dS + dd kh^T ; dkh += S'^T dd ; de += S_{t-1} * dS'
                     const float dd = -beta * ddel;
-                    g.x = fmaf(dd, kh.x, g.x); g.y = fmaf(dd, kh.y, g.y); g.z = fmaf(dd, kh.z, g.z); g.w = fmaf(dd, kh.w, g.w);
-                    pk.x = fmaf(s1.x, dd, pk.x); pk.y = fmaf(s1.y, dd, pk.y);
-                    pk.z = fmaf(s1.z, dd, pk.z); pk.w = fmaf(s1.w, dd, pk.w);
-                    pe.x = fmaf(sp[i].x, g.x, pe.x); pe.y = fmaf(sp[i].y, g.y, pe.y);
-                    pe.z = fmaf(sp[i].z, g.z, pe.z); pe.w = fmaf(sp[i].w, g.w, pe.w);
+                    g[i].x = fmaf(dd, kh.x, g[i].x); g[i].y = fmaf(dd, kh.y, g[i].y);
+                    g[i].z = fmaf(dd, kh.z, g[i].z); g[i].w = fmaf(dd, kh.w, g[i].w);
+                    pk.x = fmaf(s1[i].x, dd, pk.x); pk.y = fmaf(s1[i].y, dd, pk.y);
+                    pk.z = fmaf(s1[i].z, dd, pk.z); pk.w = fmaf(s1[i].w, dd, pk.w);
+                    pe.x = fmaf(sp[i].x, g[i].x, pe.x); pe.y = fmaf(sp[i].y, g[i].y, pe.y);
+                    pe.z = fmaf(sp[i].z, g[i].z, pe.z); pe.w = fmaf(sp[i].w, g[i].w, pe.w);
                     // dS_{t-1} = dS' Diag(e)
-                    g.x *= e.x; g.y *= e.y; g.z *= e.z; g.w *= e.w;
-                    dS[i] = g;
+                    dS[i].x = g[i].x * e.x; dS[i].y = g[i].y * e.y; dS[i].z = g[i].z * e.z; dS[i].w = g[i].w * e.w;
                 }
                 // sums over the quarter's rows (8 warps)
                 float *rd = red + (r & 1) * (BW_WARPS * 3 * KD), *rdb = redb + (r & 1) * BW_WARPS;
@@ -269,62 +310,109 @@ __global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParam
     }
 }
 
-// Per (token, query/key head): the prologue's Jacobians.  One 128-thread CTA, thread = channel.
+// The prologue's Jacobians, one warp per (query/key head, token range); lane = channels
+// 4 lane .. 4 lane + 3:
 //   dq = scale r_q dqt_sum - scale r_q^3 q (q . dqt_sum),  r_q = 1 / sqrt(|q|^2 + eps)   (dk alike, scale 1)
 //   dgraw = de e (-a) sigmoid(graw),  dA_log += sum_c de e g,  db = dbeta beta (1 - beta)
-__global__ __launch_bounds__(KD) void bwd_prologue_kernel(const BwdParams p, float *dq, float *dk, float *dgraw,
-                                                          float *db, float *dA_log, long long tokens) {
-    __shared__ float red[4][4];
-    const long long blk = blockIdx.x;
-    const long long tok = blk / p.H_qk;
-    const int hq = (int)(blk % p.H_qk), c = threadIdx.x, lane = c & 31, w = c >> 5;
-    if (tok >= tokens) return;
+// with dqt_sum / dkh_sum / de / dbeta the sums over the four row quarters (and, for dqt and dkh,
+// over the value heads of the group).  dA_log is accumulated per warp and added once per head
+// (per token and head when a group has more than 16 value heads).
+constexpr int BP_WARPS = 8;
+constexpr int BP_TOKENS = 64;   // tokens per warp
+
+__global__ __launch_bounds__(BP_WARPS * 32) void bwd_prologue_kernel(const BwdParams p, float *dq, float *dk,
+                                                                     float *dgraw, float *db, float *dA_log,
+                                                                     long long tokens) {
+    const int lane = threadIdx.x & 31;
+    const long long gw = (long long)blockIdx.x * BP_WARPS + (threadIdx.x >> 5);
+    const long long n_ranges = (tokens + BP_TOKENS - 1) / BP_TOKENS;
+    if (gw >= n_ranges * p.H_qk) return;
+    const int hq = (int)(gw % p.H_qk);
+    const long long t0 = (gw / p.H_qk) * BP_TOKENS, t1 = min(t0 + BP_TOKENS, tokens);
     const int group = p.H_v / p.H_qk;
-    const size_t qo = ((size_t)tok * p.H_qk + hq) * KD + c;
-    const float qv = bf16_to_f(p.q[qo]), kv = bf16_to_f(p.k[qo]);
-    float sq = 0.f, sk = 0.f;
-    for (int g = 0; g < group; ++g)
+    constexpr int MAXG = 16;
+    float dal[MAXG];
 #pragma unroll
-        for (int pt = 0; pt < BW_PARTS; ++pt) {
-            const size_t ho = (((size_t)tok * p.H_v + hq * group + g) * BW_PARTS + pt) * KD + c;
-            sq += p.dqt[ho];
-            sk += p.dkh[ho];
-        }
-    auto block_sum = [&](float x, int slot) {
-        x = warp_sum(x);
-        if (lane == 0) red[slot][w] = x;
-        __syncthreads();
-        const float s = red[slot][0] + red[slot][1] + red[slot][2] + red[slot][3];
-        return s;
-    };
-    const float nq = block_sum(qv * qv, 0), nk = block_sum(kv * kv, 1);
-    const float qd = block_sum(qv * sq, 2), kd = block_sum(kv * sk, 3);
-    const float rq = rsqrtf(nq + L2_EPS), rk = rsqrtf(nk + L2_EPS);
-    dq[qo] = p.scale * rq * (sq - rq * rq * qv * qd);
-    dk[qo] = rk * (sk - rk * rk * kv * kd);
-    for (int g = 0; g < group; ++g) {
-        const int h = hq * group + g;
-        const size_t ho = ((size_t)tok * p.H_v + h) * KD + c;
-        const float a = ex2(p.A_log[h] * LOG2E);
-        const float gr = bf16_to_f(p.graw[ho]);
-        const float sp = softplus_log2(gr) * (1.0f / LOG2E);   // softplus (natural units)
-        const float gg = -a * sp, ee = __expf(gg);
-        const float sig = 1.0f / (1.0f + __expf(-gr));
-        float de_sum = 0.f, dbeta_sum = 0.f;
+    for (int g = 0; g < MAXG; ++g) dal[g] = 0.f;
+    for (long long tok = t0; tok < t1; ++tok) {
+        const size_t qo = ((size_t)tok * p.H_qk + hq) * KD + 4 * lane;
+        const uint2 qw = *reinterpret_cast<const uint2 *>(p.q + qo), kw = *reinterpret_cast<const uint2 *>(p.k + qo);
+        const float qv[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
+        const float kv[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
+        float sq[4] = {0.f, 0.f, 0.f, 0.f}, sk[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int g = 0; g < group; ++g)
 #pragma unroll
-        for (int pt = 0; pt < BW_PARTS; ++pt) {
-            de_sum += p.de[(((size_t)tok * p.H_v + h) * BW_PARTS + pt) * KD + c];
-            dbeta_sum += p.dbeta[((size_t)tok * p.H_v + h) * BW_PARTS + pt];
+            for (int pt = 0; pt < BW_PARTS; ++pt) {
+                const size_t ho = (((size_t)tok * p.H_v + hq * group + g) * BW_PARTS + pt) * KD + 4 * lane;
+                const float4 a = *reinterpret_cast<const float4 *>(p.dqt + ho);
+                const float4 b = *reinterpret_cast<const float4 *>(p.dkh + ho);
+                sq[0] += a.x; sq[1] += a.y; sq[2] += a.z; sq[3] += a.w;
+                sk[0] += b.x; sk[1] += b.y; sk[2] += b.z; sk[3] += b.w;
+            }
+        float nq = 0.f, nk = 0.f, qd = 0.f, kd = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            nq = fmaf(qv[i], qv[i], nq);
+            nk = fmaf(kv[i], kv[i], nk);
+            qd = fmaf(qv[i], sq[i], qd);
+            kd = fmaf(kv[i], sk[i], kd);
         }
-        const float dg = de_sum * ee;
-        dgraw[ho] = dg * (-a) * sig;
-        float part = warp_sum(dg * gg);
-        if (lane == 0) atomicAdd(&dA_log[h], part);
-        if (c == 0) {
-            const float bb = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
-            const float beta = 1.0f / (1.0f + __expf(-bb));
-            db[(size_t)tok * p.H_v + h] = dbeta_sum * beta * (1.0f - beta);
+        nq = warp_sum(nq);
+        nk = warp_sum(nk);
+        qd = warp_sum(qd);
+        kd = warp_sum(kd);
+        const float rq = rsqrtf(nq + L2_EPS), rk = rsqrtf(nk + L2_EPS);
+        float4 oq, ok;
+        oq.x = p.scale * rq * (sq[0] - rq * rq * qv[0] * qd); oq.y = p.scale * rq * (sq[1] - rq * rq * qv[1] * qd);
+        oq.z = p.scale * rq * (sq[2] - rq * rq * qv[2] * qd); oq.w = p.scale * rq * (sq[3] - rq * rq * qv[3] * qd);
+        ok.x = rk * (sk[0] - rk * rk * kv[0] * kd); ok.y = rk * (sk[1] - rk * rk * kv[1] * kd);
+        ok.z = rk * (sk[2] - rk * rk * kv[2] * kd); ok.w = rk * (sk[3] - rk * rk * kv[3] * kd);
+        *reinterpret_cast<float4 *>(dq + qo) = oq;
+        *reinterpret_cast<float4 *>(dk + qo) = ok;
+#pragma unroll 1
+        for (int g = 0; g < group; ++g) {
+            const int h = hq * group + g;
+            const size_t vo = ((size_t)tok * p.H_v + h) * KD + 4 * lane;
+            const float a = ex2(p.A_log[h] * LOG2E);
+            const uint2 gw2 = *reinterpret_cast<const uint2 *>(p.graw + vo);
+            const float gr[4] = {bf16_lo(gw2.x), bf16_hi(gw2.x), bf16_lo(gw2.y), bf16_hi(gw2.y)};
+            float de[4] = {0.f, 0.f, 0.f, 0.f}, dbeta = 0.f;
+#pragma unroll
+            for (int pt = 0; pt < BW_PARTS; ++pt) {
+                const float4 x = *reinterpret_cast<const float4 *>(p.de + (((size_t)tok * p.H_v + h) * BW_PARTS + pt) * KD + 4 * lane);
+                de[0] += x.x; de[1] += x.y; de[2] += x.z; de[3] += x.w;
+                dbeta += p.dbeta[((size_t)tok * p.H_v + h) * BW_PARTS + pt];
+            }
+            float out[4], acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float sp = softplus_log2(gr[i]) * (1.0f / LOG2E);   // softplus (natural units)
+                const float gg = -a * sp, ee = __expf(gg);
+                const float sig = 1.0f / (1.0f + __expf(-gr[i]));
+                const float dg = de[i] * ee;
+                out[i] = dg * (-a) * sig;
+                acc = fmaf(dg, gg, acc);
+            }
+            *reinterpret_cast<float4 *>(dgraw + vo) = make_float4(out[0], out[1], out[2], out[3]);
+            acc = warp_sum(acc);
+            if (group <= MAXG) {
+#pragma unroll
+                for (int gg2 = 0; gg2 < MAXG; ++gg2)
+                    if (gg2 == g) dal[gg2] += acc;
+            } else if (lane == 0) {
+                atomicAdd(&dA_log[h], acc);
+            }
+            if (lane == 0) {
+                const float bb = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
+                const float beta = 1.0f / (1.0f + __expf(-bb));
+                db[(size_t)tok * p.H_v + h] = dbeta * beta * (1.0f - beta);
+            }
         }
+    }
+    if (lane == 0 && group <= MAXG) {
+#pragma unroll
+        for (int g = 0; g < MAXG; ++g)
+            if (g < group) atomicAdd(&dA_log[hq * group + g], dal[g]);
     }
 }
 
@@ -398,7 +486,9 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (tokens > 0) {
-        bwd_prologue_kernel<<<(unsigned)(tokens * H_qk), KD, 0, stream>>>(bp, dq, dk, dgraw, db, dA_log, tokens);
+        const long long warps = ((tokens + BP_TOKENS - 1) / BP_TOKENS) * H_qk;
+        bwd_prologue_kernel<<<(unsigned)((warps + BP_WARPS - 1) / BP_WARPS), BP_WARPS * 32, 0, stream>>>(
+            bp, dq, dk, dgraw, db, dA_log, tokens);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
