@@ -104,3 +104,92 @@ def bwd_inputs(inp, do, dht=None, **kw):
     """``bwd`` on a ``kda_inputs.KdaInputs``."""
     return bwd(inp.q, inp.k, inp.v, inp.graw, inp.b, inp.A_log, inp.scale, inp.initial_state, inp.cu_seqlens,
                do=do, dht=dht, **kw)
+
+
+def bwd_recurrent(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=None, do=None, dht=None,
+                  checkpoint: int = 64) -> Dict[str, "object"]:
+    """The same gradients as ``bwd``, by an explicit reverse pass in NumPy fp64
+    with the state stored every ``checkpoint`` tokens (memory O(T/checkpoint)
+    states per chain instead of autograd's tape), for long sequences.  Per
+    token, walking backwards with dS = dL/dS_t:
+    dS += do qt^T, dqt = S_t^T do, ddel = dS kh, dkh = dS^T delta + S'^T dd
+    (dd = -beta ddel), dv = beta ddel, dbeta = ddel . (v - d), dS' = dS + dd kh^T,
+    de = colsum(S_{t-1} * dS'), dS_{t-1} = dS' Diag(e); then the Jacobians of
+    the norms, the gate and the sigmoid.  Pinned to ``bwd`` (autograd) by the
+    tests."""
+    import numpy as np
+    f64 = lambda t: t.detach().to(torch.float64).numpy()  # noqa: E731
+    qq, kk, vv, gg, bb, aa = (f64(t) for t in (q, k, v, graw, b, A_log))
+    B, T, H_qk, K = qq.shape
+    H_v, V = vv.shape[2], vv.shape[3]
+    G = H_v // H_qk
+    segs = ([(bi, 0, T) for bi in range(B)] if cu_seqlens is None else
+            [(0, int(cu_seqlens[i]), int(cu_seqlens[i + 1])) for i in range(cu_seqlens.numel() - 1)])
+    sc = float(np.float32(scale))
+    nq = np.sqrt((qq * qq).sum(-1, keepdims=True) + EPS)
+    nk = np.sqrt((kk * kk).sum(-1, keepdims=True) + EPS)
+    qt, kh = sc * qq / nq, kk / nk
+    beta = 1.0 / (1.0 + np.exp(-bb))
+    a = np.exp(aa)
+    sp = np.maximum(gg, 0.0) + np.log1p(np.exp(-np.abs(gg)))
+    g = -a[None, None, :, None] * sp
+    e = np.exp(g)
+    dO = np.zeros(vv.shape) if do is None else f64(do)
+    dqt, dkh = np.zeros((B, T, H_v, K)), np.zeros((B, T, H_v, K))
+    de, dbeta, dv = np.zeros((B, T, H_v, K)), np.zeros((B, T, H_v)), np.zeros(vv.shape)
+    dh0 = np.zeros((len(segs), H_v, V, K))
+    for n, (bi, t0, t1) in enumerate(segs):
+        for h in range(H_v):
+            hq = h // G
+            S = np.zeros((V, K)) if initial_state is None else f64(initial_state[n, h]).copy()
+            ck = {}
+            for t in range(t0, t1):
+                if (t - t0) % checkpoint == 0:
+                    ck[t] = S.copy()
+                S = S * e[bi, t, h][None, :]
+                S = S + beta[bi, t, h] * np.outer(vv[bi, t, h] - S @ kh[bi, t, hq], kh[bi, t, hq])
+            dS = np.zeros((V, K)) if dht is None else f64(dht[n, h]).copy()
+            starts = sorted(ck.keys(), reverse=True)
+            for c0 in starts:
+                c1 = min(c0 + checkpoint, t1)
+                states = [ck[c0].copy()]
+                for t in range(c0, c1 - 1):
+                    Sx = states[-1] * e[bi, t, h][None, :]
+                    states.append(Sx + beta[bi, t, h] * np.outer(vv[bi, t, h] - Sx @ kh[bi, t, hq], kh[bi, t, hq]))
+                for t in range(c1 - 1, c0 - 1, -1):
+                    Sp = states[t - c0]
+                    k_, q_, b_ = kh[bi, t, hq], qt[bi, t, hq], beta[bi, t, h]
+                    S1 = Sp * e[bi, t, h][None, :]
+                    d = S1 @ k_
+                    delta = b_ * (vv[bi, t, h] - d)
+                    St = S1 + np.outer(delta, k_)
+                    dS = dS + np.outer(dO[bi, t, h], q_)
+                    dqt[bi, t, h] = St.T @ dO[bi, t, h]
+                    ddel = dS @ k_
+                    dv[bi, t, h] = b_ * ddel
+                    dbeta[bi, t, h] = ddel @ (vv[bi, t, h] - d)
+                    dd = -b_ * ddel
+                    dkh[bi, t, h] = dS.T @ delta + S1.T @ dd
+                    dS = dS + np.outer(dd, k_)
+                    de[bi, t, h] = (Sp * dS).sum(0)
+                    dS = dS * e[bi, t, h][None, :]
+            dh0[n, h] = dS
+    # Jacobians: norms (dq, dk summed over each group's value heads), gate, sigmoid
+    dqs = dqt.reshape(B, T, H_qk, G, K).sum(3)
+    dks = dkh.reshape(B, T, H_qk, G, K).sum(3)
+    rq, rk = 1.0 / nq, 1.0 / nk
+    dq = sc * rq * (dqs - rq * rq * qq * (qq * dqs).sum(-1, keepdims=True))
+    dk = rk * (dks - rk * rk * kk * (kk * dks).sum(-1, keepdims=True))
+    dg = de * e
+    sig = 1.0 / (1.0 + np.exp(-gg))
+    dgraw = dg * (-a[None, None, :, None]) * sig
+    dA_log = (dg * g).sum(axis=(0, 1, 3))
+    db = dbeta * beta * (1.0 - beta)
+    out = dict(dq=dq, dk=dk, dv=dv, dgraw=dgraw, db=db, dA_log=dA_log, dh0=dh0)
+    return {n_: torch.from_numpy(np.ascontiguousarray(x)) for n_, x in out.items()}
+
+
+def bwd_recurrent_inputs(inp, do, dht=None, **kw):
+    """``bwd_recurrent`` on a ``kda_inputs.KdaInputs``."""
+    return bwd_recurrent(inp.q, inp.k, inp.v, inp.graw, inp.b, inp.A_log, inp.scale, inp.initial_state,
+                         inp.cu_seqlens, do=do, dht=dht, **kw)

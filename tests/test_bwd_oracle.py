@@ -93,3 +93,25 @@ def test_bwd_oracle_forward_equals_c_oracle():
     ro, rf = oracle.fwd_inputs(inp)
     assert np.abs(o.detach().numpy() - ro).max() <= 1e-9 * max(1.0, np.abs(ro).max())
     assert np.abs(f.detach().numpy() - rf).max() <= 1e-9 * max(1.0, np.abs(rf).max())
+
+
+@pytest.mark.parametrize("case", ["plain", "gva_varlen", "no_state", "short_checkpoints"])
+def test_recurrent_backward_matches_autograd(case):
+    """The explicit reverse pass (for long sequences) equals the autograd oracle."""
+    import kda_inputs as KI
+    if case == "plain":
+        inp, ck = KI.make_inputs(1, 70, 1, 2, seed=20, with_state=True), 64
+    elif case == "gva_varlen":
+        inp, ck = KI.make_inputs(1, 90, 1, 2, seed=21, with_state=True, seqlens=[40, 0, 1, 49]), 16
+    elif case == "no_state":
+        inp, ck = KI.make_inputs(2, 33, 2, 2, seed=22, with_state=False), 64
+    else:
+        inp, ck = KI.make_inputs(1, 50, 1, 1, seed=23, with_state=True, graw_mean=3.0, A_log_value=1.0), 7
+    g = torch.Generator().manual_seed(30)
+    do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
+    dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1
+    a = OB.bwd_inputs(inp, do, dht)
+    r = OB.bwd_recurrent_inputs(inp, do, dht, checkpoint=ck)
+    for name in a:
+        err = _max_rel(r[name], a[name])
+        assert err <= 1e-9, (name, err)

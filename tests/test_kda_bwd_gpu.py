@@ -86,3 +86,29 @@ def test_bwd_zero_tokens_passes_dht():
 def test_bwd_longer_sequence():
     """T = 1024 (16 chunks): checkpoints and the chunk-by-chunk reverse pass."""
     _check(KI.make_inputs(1, 1024, 1, 1, seed=705, with_state=True), seed=6)
+
+
+def test_bwd_full_size_dense_sampled_heads():
+    """The benchmark's dense workload (B=2, T=16384, H=32) at full size; the fp64
+    reverse-pass oracle (checkpointed, pinned to autograd) recomputes every
+    gradient of q/k heads 0 and 31 (each chain is independent)."""
+    from gated_delta_rule_40_gb300 import kda
+    from kda_testutil import head_subset
+    inp = KI.workload("dense")
+    do, dht = _grads(inp, 7)
+    dev = lambda t: None if t is None else t.cuda()  # noqa: E731
+    got = kda.kda_bwd(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.graw), dev(inp.b), dev(inp.A_log), inp.scale,
+                      dev(do), initial_state=dev(inp.initial_state), dht=dev(dht))
+    torch.cuda.synchronize()
+    for hq in (0, 31):
+        sub = head_subset(inp, [hq])
+        ref = OB.bwd_recurrent_inputs(sub, do[:, :, hq:hq + 1].contiguous(), dht[:, hq:hq + 1].contiguous())
+        sel = {"dq": got["dq"][:, :, hq:hq + 1], "dk": got["dk"][:, :, hq:hq + 1], "dv": got["dv"][:, :, hq:hq + 1],
+               "dgraw": got["dgraw"][:, :, hq:hq + 1], "db": got["db"][:, :, hq:hq + 1],
+               "dA_log": got["dA_log"][hq:hq + 1], "dh0": got["dh0"][:, hq:hq + 1]}
+        for name, a in sel.items():
+            a = a.double().cpu().numpy()
+            r = ref[name].numpy()
+            e = rel_l2(a, r)
+            m = np.abs(a - r).max() / max(np.abs(r).max(), 1e-30)
+            assert e <= REL and m <= MAX_FRAC, f"head {hq} {name}: rel-L2 {e:.2e}, max {m:.2e}"
