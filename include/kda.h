@@ -227,7 +227,7 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
  * workspace comes from cudaMallocAsync on `stream`: state checkpoints every 32
  * tokens (2 KiB per token and value head), per-token partial sums of four
  * row quarters (6 KiB per token and value head) and 512 KiB of scratch per
- * resident CTA, i.e. about 8 KiB per token and value head (8.6 GB for B=2,
+ * resident CTA, i.e. about 8 KiB per token and value head (8.7 GB for B=2,
  * T=16384, H_v=32); a failed allocation returns KDA_ERR_CUDA.  This is the token recurrence run backwards on
  * CUDA cores in fp32 (one persistent CTA per (sequence, value head) chain);
  * errors as kda_fwd.
