@@ -71,3 +71,38 @@ def test_decode_rejects_bad_args(lib):
     rc = lib.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.1), FAKE, 0, 1, 1, 128, 128,
                              FAKE, None)
     assert rc == kda.KDA_OK
+
+
+def test_la_fwd_rejects_bad_args(lib):
+    f = ctypes.c_float(0.1)
+    la = lambda K=128, V=128, H_qk=1, H_v=1, B=1, T=4, N=0, cu=None, q=FAKE, slope=FAKE: lib.kda_la_fwd(  # noqa: E731
+        q, FAKE, FAKE, slope, f, None, None, cu, N, B, T, H_qk, H_v, K, V, FAKE, None)
+    assert la(K=64) == kda.KDA_ERR_UNSUPPORTED
+    assert la(H_qk=2, H_v=3) == kda.KDA_ERR_INVALID_ARG
+    assert la(T=-1) == kda.KDA_ERR_INVALID_ARG
+    assert la(B=2, N=1, cu=FAKE) == kda.KDA_ERR_INVALID_ARG
+    assert la(q=FAKE_ODD) == kda.KDA_ERR_INVALID_ARG     # TMA needs 16-byte aligned tensors
+    assert la(slope=None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_la_decode_rejects_bad_args(lib):
+    f = ctypes.c_float(0.1)
+    assert lib.kda_la_decode(FAKE, FAKE, FAKE, FAKE, f, FAKE, 1, 1, 1, 128, 64, FAKE, None) == kda.KDA_ERR_UNSUPPORTED
+    assert lib.kda_la_decode(FAKE, FAKE, FAKE, None, f, FAKE, 1, 1, 1, 128, 128, FAKE, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_la_decode(FAKE, FAKE, FAKE, FAKE, f, FAKE, 1, 2, 3, 128, 128, FAKE, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_la_decode(FAKE, FAKE, FAKE, FAKE, f, FAKE, 0, 1, 1, 128, 128, FAKE, None) == kda.KDA_OK
+
+
+def test_bwd_rejects_bad_args(lib):
+    f = ctypes.c_float(0.1)
+
+    def bwd(K=128, H_qk=1, H_v=1, dout=FAKE, dq=FAKE, dA=FAKE, dh0=FAKE):
+        return lib.kda_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, f, None, None, 0, 1, 4, H_qk, H_v, K, 128, dout, None,
+                           dq, FAKE, FAKE, FAKE, FAKE, dA, dh0, None)
+    assert bwd(K=64) == kda.KDA_ERR_UNSUPPORTED
+    assert bwd(H_qk=2, H_v=3) == kda.KDA_ERR_INVALID_ARG
+    assert bwd(dout=None) == kda.KDA_ERR_INVALID_ARG
+    assert bwd(dq=None) == kda.KDA_ERR_INVALID_ARG
+    assert bwd(dq=FAKE_ODD) == kda.KDA_ERR_INVALID_ARG
+    assert bwd(dA=None) == kda.KDA_ERR_INVALID_ARG
+    assert bwd(dh0=None) == kda.KDA_ERR_INVALID_ARG
