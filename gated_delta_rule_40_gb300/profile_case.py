@@ -3,6 +3,7 @@
     python -m gated_delta_rule_40_gb300.profile_case --B 1 --T 8192 --H 32 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method la --B 1 --T 8192 --H 64 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method bwd --B 1 --T 2048 --H 8 --iters 3
+    python -m gated_delta_rule_40_gb300.profile_case --method la_decode --B 256 --H 64 --iters 4
 
 Inputs come from ``kda_inputs`` (same recipe as the tests and the benchmark);
 the workspace is allocated once, so every iteration is exactly the three
@@ -28,8 +29,16 @@ def main() -> None:
     ap.add_argument("--H", type=int, default=32, help="value heads (= q/k heads)")
     ap.add_argument("--iters", type=int, default=4)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--method", choices=["kda", "la", "bwd"], default="kda")
+    ap.add_argument("--method", choices=["kda", "la", "bwd", "la_decode"], default="kda")
     a = ap.parse_args()
+    if a.method == "la_decode":
+        d = kda_inputs.la_decode_inputs(B=a.B, H=a.H, seed=a.seed)
+        q, k, v, sl, st = (t.cuda() for t in (d.q, d.k, d.v, d.slope, d.state))
+        for _ in range(a.iters):
+            o = kda.kda_la_decode(q, k, v, sl, d.scale, st)
+        torch.cuda.synchronize()
+        print(f"kda_la_decode B={a.B} H={a.H} x{a.iters}: |o| {float(o.float().abs().mean()):.6f}")
+        return
     if a.method == "la":
         x = kda_inputs.make_la_inputs(a.B, a.T, a.H, a.H, seed=a.seed)
         q, k, v, sl, s0 = (t.cuda() for t in (x.q, x.k, x.v, x.slope, x.initial_state))
