@@ -25,10 +25,9 @@
 // rewrites its K rows in place as Kd_hi = bf16(k exp(Gam_len - Gam_r)) and
 // stores the remainder Kd_lo in a double buffer, so the state update keeps
 // ~16 bits; S and P enter the output products rounded to bf16, like the output
-// itself.  P carries the factor scale, and the output
-// O = scale exp(Gam_r) Y1 + Y2 is transposed through
-// shared memory and written with 16-byte stores.  Every wait is bounded; a
-// timeout records KDA_ERR_DEVICE_TIMEOUT and all roles stop.
+// itself.  P carries the factor scale, and the output O = scale exp(Gam_r) Y1 + Y2
+// is transposed through shared memory and written with 16-byte stores.  Every
+// wait is bounded; a timeout records KDA_ERR_DEVICE_TIMEOUT and all roles stop.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
