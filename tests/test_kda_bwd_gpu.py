@@ -112,3 +112,9 @@ def test_bwd_full_size_dense_sampled_heads():
             e = rel_l2(a, r)
             m = np.abs(a - r).max() / max(np.abs(r).max(), 1e-30)
             assert e <= REL and m <= MAX_FRAC, f"head {hq} {name}: rel-L2 {e:.2e}, max {m:.2e}"
+
+
+def test_bwd_large_value_head_group():
+    """20 value heads share one q/k head (more than the 16 the Jacobian kernel keeps dA_log
+    partials for in registers): dq and dk sum over all 20, dA_log per head."""
+    _check(KI.make_inputs(1, 40, 1, 20, seed=706, with_state=True), seed=8)
