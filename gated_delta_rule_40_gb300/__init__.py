@@ -12,6 +12,7 @@ from .kda import (  # noqa: F401
     kda_decode_step,
     kda_decode_tokens,
     kda_fwd,
+    kda_fwd_bf16_state,
     kda_fwd_host,
     kda_fwd_noalloc,
     kda_fwd_scalar_gate,

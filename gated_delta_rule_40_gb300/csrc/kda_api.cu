@@ -35,6 +35,10 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
                        int B, int T, int H_qk, int H_v, const uint16_t *dout, const float *dht, float *dq, float *dk,
                        float *dv, float *dgraw, float *db, float *dA_log, float *dh0, void *ws_ptr, int grid,
                        cudaStream_t stream, int *launches);
+cudaError_t launch_fwd_bf16_state(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                                  const uint16_t *b, const float *A_log, float scale, const uint16_t *init,
+                                  uint16_t *fin, const int32_t *cu, int N, int B, int T, int H_qk, int H_v,
+                                  uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches);
 struct FwdWorkspace;
 size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspace *ws, char *base);
 
@@ -201,6 +205,27 @@ int kda_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const
     if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
     rc = kda_fwd_ws(q, k, v, graw, b, A_log, scale, initial_state, final_state, cu_seqlens, N, B, T, H_qk, H_v,
                     K, V, out, ws, need, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
+    return rc;
+}
+
+int kda_fwd_bf16_state(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+                       const kda_bf16_t *b, const float *A_log, float scale, const kda_bf16_t *initial_state,
+                       kda_bf16_t *final_state, const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v,
+                       int K, int V, kda_bf16_t *out, cudaStream_t stream) {
+    int rc = validate_fwd(q, k, v, graw, b, A_log, initial_state, final_state, cu_seqlens, N, B, T, H_qk, H_v,
+                          K, V, out);
+    if (rc != KDA_OK) return rc;
+    const size_t need = kda::fwd_workspace_bytes(cu_seqlens ? N : 0, B, T, H_v, cu_seqlens != nullptr, nullptr,
+                                                 nullptr);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    int launches = 0;
+    const cudaError_t e = kda::launch_fwd_bf16_state(q, k, v, graw, b, A_log, scale, initial_state, final_state,
+                                                     cu_seqlens, cu_seqlens ? N : 0, B, T, H_qk, H_v, out, ws, stream,
+                                                     &launches);
+    rc = e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    if (rc == KDA_OK) t_last_launches = launches;
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
     return rc;
 }

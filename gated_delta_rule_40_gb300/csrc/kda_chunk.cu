@@ -923,6 +923,7 @@ struct ScanParams {
     uint16_t *out;
     int H_v, nseq;
     int h0, Hw;   // value-head window [h0, h0 + Hw); records are [chunk][Hw]
+    int state_bf16;   // init / fin hold bf16 values (the recurrence itself stays fp32)
 };
 
 enum { BAR_WQ0 = 0, BAR_WQ1, BAR_PK0, BAR_PK1, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MMA2, BAR_SBR, BAR_DTR };
@@ -1049,7 +1050,10 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
         constexpr int VH = VB / 2;
         float S[VH];
 #pragma unroll
-        for (int v = 0; v < VH; ++v) S[v] = p.init ? p.init[st0 + (size_t)v * KD] : 0.f;
+        for (int v = 0; v < VH; ++v)
+            S[v] = !p.init ? 0.f
+                 : p.state_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t *>(p.init)[st0 + (size_t)v * KD])
+                                : p.init[st0 + (size_t)v * KD];
         const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(q * 32) << 16;
         const int vme = q * 16 + lane;      // v owned in the M = 64 layout (lane < 16)
@@ -1163,9 +1167,15 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
         }
         if (!*abort_flag && n > 0) emit_output(n - 1);
         if (p.fin && !*abort_flag) {
-            float *dst = p.fin + st0;
+            if (p.state_bf16) {
+                uint16_t *dst = reinterpret_cast<uint16_t *>(p.fin) + st0;
 #pragma unroll
-            for (int v = 0; v < VH; ++v) dst[(size_t)v * KD] = S[v];
+                for (int v = 0; v < VH; ++v) dst[(size_t)v * KD] = f_to_bf16(S[v]);
+            } else {
+                float *dst = p.fin + st0;
+#pragma unroll
+                for (int v = 0; v < VH; ++v) dst[(size_t)v * KD] = S[v];
+            }
         }
     }
     tc_fence_before();
@@ -1678,10 +1688,11 @@ size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspa
 // Forward for the value heads [h0, h0 + Hw) of the tensors (strides from H_qk, H_v); the
 // workspace holds records for Hw heads.  With plan == false the chunk tables already in the
 // workspace (from an earlier call on the same sequences) are reused.
-cudaError_t launch_fwd_heads(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
-                             const uint16_t *b, const float *A_log, float scale, const float *init, float *fin,
-                             const int32_t *cu, int N, int B, int T, int H_qk, int H_v, int h0, int Hw, bool plan,
-                             uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches) {
+static cudaError_t launch_fwd_impl(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                                   const uint16_t *b, const float *A_log, float scale, const float *init, float *fin,
+                                   const int32_t *cu, int N, int B, int T, int H_qk, int H_v, int h0, int Hw,
+                                   bool plan, uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches,
+                                   bool state_bf16) {
     const bool varlen = cu != nullptr;
     const int nseq = varlen ? N : B;
     FwdWorkspace ws;
@@ -1726,6 +1737,7 @@ cudaError_t launch_fwd_heads(const uint16_t *q, const uint16_t *k, const uint16_
         sp.rec = ws.rec;
         sp.seqs = ws.seqs; sp.order = ws.order; sp.hdr = ws.hdr;
         sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = h0; sp.Hw = Hw;
+        sp.state_bf16 = state_bf16 ? 1 : 0;
         const long long nblk = (long long)nseq * Hw * 2;
         scan_kernel<<<(unsigned)nblk, SC_THREADS, SS_BYTES, stream>>>(sp);
         ++*launches;
@@ -1775,12 +1787,31 @@ cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const u
         sp.rec = ws.rec;
         sp.seqs = ws.seqs; sp.order = ws.order; sp.hdr = ws.hdr;
         sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = 0; sp.Hw = H_v;
+        sp.state_bf16 = 0;
         scan_kernel<<<(unsigned)((long long)nseq * H_v * 2), SC_THREADS, SS_BYTES, stream>>>(sp);
         ++*launches;
         timing_mark("scan_kernel", stream);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_fwd_heads(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                             const uint16_t *b, const float *A_log, float scale, const float *init, float *fin,
+                             const int32_t *cu, int N, int B, int T, int H_qk, int H_v, int h0, int Hw, bool plan,
+                             uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches) {
+    return launch_fwd_impl(q, k, v, graw, b, A_log, scale, init, fin, cu, N, B, T, H_qk, H_v, h0, Hw, plan, out, ws_ptr,
+                           stream, launches, false);
+}
+
+// The forward with the initial and final states stored as bf16.
+cudaError_t launch_fwd_bf16_state(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
+                                  const uint16_t *b, const float *A_log, float scale, const uint16_t *init,
+                                  uint16_t *fin, const int32_t *cu, int N, int B, int T, int H_qk, int H_v,
+                                  uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches) {
+    return launch_fwd_impl(q, k, v, graw, b, A_log, scale, reinterpret_cast<const float *>(init),
+                           reinterpret_cast<float *>(fin), cu, N, B, T, H_qk, H_v, 0, H_v, true, out, ws_ptr, stream,
+                           launches, true);
 }
 
 cudaError_t launch_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,

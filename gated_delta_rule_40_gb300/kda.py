@@ -67,6 +67,8 @@ def load() -> ctypes.CDLL:
     lib.kda_decode_step.restype = I
     lib.kda_decode_tokens.argtypes = [P, P, P, P, P, P, F, P, I, I, I, I, I, I, I, P, P]
     lib.kda_decode_tokens.restype = I
+    lib.kda_fwd_bf16_state.argtypes = [P, P, P, P, P, P, F, P, P, P, I, I, I, I, I, I, I, P, P]
+    lib.kda_fwd_bf16_state.restype = I
     lib.kda_bwd.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P]
     lib.kda_bwd.restype = I
     lib.kda_la_fwd.argtypes = [P, P, P, P, F, P, P, P, I, I, I, I, I, I, I, P, P]
@@ -445,3 +447,34 @@ def kda_bwd(q, k, v, graw, b, A_log, scale: float, dout, initial_state=None, cu_
                      _ptr(g["dh0"]), _stream(stream))
     _raise(rc, "kda_bwd")
     return g
+
+
+def kda_fwd_bf16_state(q, k, v, graw, b, A_log, scale: float, initial_state=None, cu_seqlens=None,
+                       output_final_state: bool = True, out=None, final_state=None,
+                       stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """``kda_fwd`` with the initial / final states in bf16 ([N,H_v,V,K]); the
+    recurrence itself keeps an fp32 state."""
+    lib = load()
+    B, T, H_qk, K = q.shape
+    H_v, V = v.shape[2], v.shape[3]
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else B
+    bf = torch.bfloat16
+    _check(q, "q", bf, (B, T, H_qk, K))
+    _check(k, "k", bf, (B, T, H_qk, K))
+    _check(v, "v", bf, (B, T, H_v, V))
+    _check(graw, "graw", bf, (B, T, H_v, K))
+    _check(b, "b", bf, (B, T, H_v))
+    _check(A_log, "A_log", torch.float32, (H_v,))
+    _check(initial_state, "initial_state", bf, (N, H_v, V, K), optional=True)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, optional=True)
+    if out is None:
+        out = torch.empty((B, T, H_v, V), dtype=bf, device=q.device)
+    _check(out, "out", bf, (B, T, H_v, V))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H_v, V, K), dtype=bf, device=q.device)
+    _check(final_state, "final_state", bf, (N, H_v, V, K), optional=True)
+    rc = lib.kda_fwd_bf16_state(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
+                                _ptr(initial_state), _ptr(final_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V,
+                                _ptr(out), _stream(stream))
+    _raise(rc, "kda_fwd_bf16_state")
+    return out, final_state

@@ -141,6 +141,20 @@ int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
                  cudaStream_t stream);
 
 /*
+ * kda_fwd with the initial and final states stored as bf16 ([N, H_v, V, K];
+ * FlashKDA's interface admits fp32 or bf16 states, "How does FlashKDA's
+ * stateful/streaming (chunked) support work?").  The recurrence runs with an
+ * fp32 state exactly as in kda_fwd; the initial state is widened on load and the
+ * final state rounded to bf16 (nearest even) once, on store.  Other arguments,
+ * asynchrony and errors as kda_fwd.
+ */
+int kda_fwd_bf16_state(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
+                       const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log, float scale,
+                       const kda_bf16_t *initial_state, kda_bf16_t *final_state,
+                       const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V,
+                       kda_bf16_t *out, cudaStream_t stream);
+
+/*
  * One decode step for B independent sequences (one token each):
  *
  *   q, k  [B, H_qk, K] bf16     v, graw [B, H_v, V|K] bf16     b [B, H_v] bf16
