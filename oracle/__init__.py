@@ -18,6 +18,8 @@ Contents
   fixed per-head decay), the token recurrence in plain C (``la_oracle.c``).
 * ``la_quadratic``: the same method in its parallel (attention-matrix) form in
   NumPy fp64, a second formulation that pins the recurrence.
+* ``la_chunk_model``: the chunked lightning-attention algebra in NumPy fp64
+  with the kernel's operand roundings on request (its precision study).
 * ``backward.bwd``: gradients of the KDA forward with respect to all inputs
   (fp64 autograd through the token recurrence), pinned by finite differences
   of ``brute_force``.
