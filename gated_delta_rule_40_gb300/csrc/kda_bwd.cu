@@ -26,9 +26,12 @@
 // wrote), then walks the block's tokens backwards.  The per-token vectors (qt,
 // kh, e, v, do, beta) of a block are staged in shared memory; the sums over the
 // quarter's rows of dqt, dkh, de and dbeta are reduced across warps through
-// shared memory and written per (token, head, quarter) for bwd_prologue_kernel,
-// which adds the quarters and the value heads of a group.  This is the token recurrence on CUDA cores in fp32, a
-// correct first form; its cost is O(T K V) per chain with no tensor-core use.
+// shared memory (one barrier per token, alternating areas) and written per
+// (token, head, quarter) for bwd_prologue_kernel, which adds the quarters and the
+// value heads of a group.  The per-row dot products of a warp's four rows use one
+// four-value warp reduce-scatter.  This is the token recurrence on CUDA cores in
+// fp32, a correct first form; its cost is O(T K V) per chain with no tensor-core
+// use.
 #include "kda_common.cuh"
 
 namespace kda {
