@@ -205,6 +205,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32
     }
     return false;
 }
+// Bounded wait that lets the thread sleep up to `hint_ns` per probe (mbarrier.try_wait's
+// suspend-time hint): a warp that waits long re-polls rarely and leaves issue slots to the
+// others.  The bound is about limit x hint_ns in total; false if it gave up.
+__device__ __forceinline__ bool mbar_wait_hint(uint32_t mbar, uint32_t parity, uint32_t hint_ns = 10000u,
+                                               uint32_t limit = 200000u) {
+    uint32_t done = 0;
+    for (uint32_t it = 0; it < limit; ++it) {
+        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done) : "r"(mbar), "r"(parity), "r"(hint_ns));
+        if (done) return true;
+    }
+    return false;
+}
 // Bounded spin on the phase with the given parity with the non-suspending probe
 // (test_wait): a thread on a latency-critical hand-off resumes within a probe's
 // latency of the phase completing, where a suspended try_wait can take several

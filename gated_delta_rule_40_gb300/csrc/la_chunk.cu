@@ -284,7 +284,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             const int s = c % LA_NST;
             unsigned char *stg = sm + s * LA_STAGE;
             const int len = min(CH, sd.len - c * CH);
-            if (!mbar_wait(bar + 8 * (LB_LD0 + s), (c / LA_NST) & 1) || !mbar_wait(bar + 8 * LB_A, c & 1)) return false;
+            if (!mbar_wait_hint(bar + 8 * (LB_LD0 + s), (c / LA_NST) & 1) || !mbar_wait_hint(bar + 8 * LB_A, c & 1)) return false;
             tc_fence_after();
             {
                 // P block (rows 16 q4 .., columns 16 cg ..) times scale: zero above the diagonal block;
@@ -344,7 +344,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
         // E2 of chunk c: S <- exp(Gam_len) S + Z^T, then the bf16 copy for the next chunk's M1
         auto e2 = [&](int c) -> bool {
             const int len = min(CH, sd.len - c * CH);
-            if (!mbar_wait(bar + 8 * LB_M3, c & 1) || !mbar_wait(bar + 8 * (LB_M12_0 + (c & 1)), (c >> 1) & 1))
+            if (!mbar_wait_hint(bar + 8 * LB_M3, c & 1) || !mbar_wait_hint(bar + 8 * (LB_M12_0 + (c & 1)), (c >> 1) & 1))
                 return false;
             tc_fence_after();
             const float g = ex2(-sl2 * (float)len);
