@@ -20,6 +20,8 @@ Contents
   NumPy fp64, a second formulation that pins the recurrence.
 * ``la_chunk_model``: the chunked lightning-attention algebra in NumPy fp64
   with the kernel's operand roundings on request (its precision study).
+* ``chunk_bwd_model``: the same gradients from the chunked (UT/WY) formulas, the
+  algebra a tensor-core backward builds on, pinned to ``backward.bwd``.
 * ``backward.bwd``: gradients of the KDA forward with respect to all inputs
   (fp64 autograd through the token recurrence), pinned by finite differences
   of ``brute_force``.

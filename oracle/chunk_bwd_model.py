@@ -1,0 +1,137 @@
+"""Chunked (UT / WY) backward of the KDA forward in NumPy fp64.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  The algebra a chunked,
+tensor-core backward is built on, written out plainly so the tests can pin it
+against the autograd oracle; the GPU code shares nothing with it.
+
+Forward per chunk (C rows; S_0 the state entering it; Gam the inclusive in-chunk
+prefix of the log decay g, per channel; Gam_C its last row; natural units):
+
+  Kg = Kh e^{Gam},  Kn = Kh e^{-Gam},  Qg = Qt e^{Gam},  Kd = Kh e^{Gam_C - Gam}
+  A  = strict_lower(diag(beta) Kg Kn^T),   P = lower(Qg Kn^T),   T = (I + A)^{-1}
+  U  = T diag(beta) V,   W = T diag(beta) Kg,   Delta = U - W S_0^T
+  O  = Qg S_0^T + P Delta,   S_C = S_0 Diag(e^{Gam_C}) + Delta^T Kd
+
+Backward of one chunk, given dO and dS_C (products read right to left):
+
+  dDelta = P^T dO + Kd dS_C^T          dKd = Delta dS_C         dQg = dO S_0
+  dS_0   = dO^T Qg + dS_C Diag(e^{Gam_C}) - dDelta^T W
+  dP     = lower(dO Delta^T)           dU = dDelta              dW = -dDelta S_0
+  dT     = dU (diag(beta) V)^T + dW (diag(beta) Kg)^T
+  dA     = strict_lower(-T^T dT T^T)
+  then the products A, P, U, W and the decayed copies pass their gradients to
+  Kh, Qt, V, beta and Gam, and dg_s = sum_{r >= s} dGam_r (plus the Gam_C terms).
+
+Chunks are visited in reverse with dS carried from each chunk's S_0 to the
+previous chunk's S_C; the forward states S_0 come from a forward pass.  The
+prologue's Jacobians (norms, gate, sigmoid) are those of ``backward.bwd``.
+"""
+from __future__ import annotations
+
+from typing import Dict
+
+import numpy as np
+import torch
+
+from .backward import EPS
+
+
+def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=None, do=None, dht=None,
+              C: int = 64) -> Dict[str, torch.Tensor]:
+    """Gradients as ``backward.bwd`` returns them (fp64 tensors), computed with
+    the chunked formulas above."""
+    f64 = lambda t: t.detach().to(torch.float64).numpy()  # noqa: E731
+    qq, kk, vv, gg, bb, aa = (f64(t) for t in (q, k, v, graw, b, A_log))
+    B, T, H_qk, K = qq.shape
+    H_v, V = vv.shape[2], vv.shape[3]
+    G = H_v // H_qk
+    segs = ([(bi, 0, T) for bi in range(B)] if cu_seqlens is None else
+            [(0, int(cu_seqlens[i]), int(cu_seqlens[i + 1])) for i in range(cu_seqlens.numel() - 1)])
+    sc = float(np.float32(scale))
+    nq = np.sqrt((qq * qq).sum(-1, keepdims=True) + EPS)
+    nk = np.sqrt((kk * kk).sum(-1, keepdims=True) + EPS)
+    qt_all, kh_all = sc * qq / nq, kk / nk
+    beta_all = 1.0 / (1.0 + np.exp(-bb))
+    a = np.exp(aa)
+    sp = np.maximum(gg, 0.0) + np.log1p(np.exp(-np.abs(gg)))
+    g_all = -a[None, None, :, None] * sp
+    dO_all = np.zeros(vv.shape) if do is None else f64(do)
+    dqt, dkh = np.zeros((B, T, H_v, K)), np.zeros((B, T, H_v, K))
+    dg, dbeta, dv = np.zeros((B, T, H_v, K)), np.zeros((B, T, H_v)), np.zeros(vv.shape)
+    dh0 = np.zeros((len(segs), H_v, V, K))
+    for n, (bi, t0, t1) in enumerate(segs):
+        for h in range(H_v):
+            hq = h // G
+            S = np.zeros((V, K)) if initial_state is None else f64(initial_state[n, h]).copy()
+            starts = list(range(t0, t1, C))
+            S0s = []
+            for c0 in starts:                                  # forward: states at chunk starts
+                S0s.append(S.copy())
+                for t in range(c0, min(c0 + C, t1)):
+                    S = S * np.exp(g_all[bi, t, h])[None, :]
+                    kh = kh_all[bi, t, hq]
+                    S = S + beta_all[bi, t, h] * np.outer(vv[bi, t, h] - S @ kh, kh)
+            dS = np.zeros((V, K)) if dht is None else f64(dht[n, h]).copy()
+            for c0, S0 in reversed(list(zip(starts, S0s))):
+                c1 = min(c0 + C, t1)
+                Qt, Kh = qt_all[bi, c0:c1, hq], kh_all[bi, c0:c1, hq]
+                Vc, be, gc = vv[bi, c0:c1, h], beta_all[bi, c0:c1, h], g_all[bi, c0:c1, h]
+                dO = dO_all[bi, c0:c1, h]
+                L = c1 - c0
+                Gam = np.cumsum(gc, axis=0)
+                GC = Gam[-1]
+                eG, enG = np.exp(Gam), np.exp(-Gam)
+                Kg, Kn, Qg, Kd = Kh * eG, Kh * enG, Qt * eG, Kh * np.exp(GC[None, :] - Gam)
+                strict = np.tril(np.ones((L, L)), -1)
+                incl = np.tril(np.ones((L, L)))
+                A = strict * ((be[:, None] * Kg) @ Kn.T)
+                P = incl * (Qg @ Kn.T)
+                Tm = np.linalg.inv(np.eye(L) + A)
+                BV, BW = be[:, None] * Vc, be[:, None] * Kg
+                U, W = Tm @ BV, Tm @ BW
+                Delta = U - W @ S0.T
+                # ---- backward of the chunk
+                dDelta = P.T @ dO + Kd @ dS.T
+                dKd = Delta @ dS
+                dQg = dO @ S0
+                dS0 = dO.T @ Qg + dS * np.exp(GC)[None, :] - dDelta.T @ W
+                dGC = (S0 * dS).sum(0) * np.exp(GC)
+                dP = incl * (dO @ Delta.T)
+                dU, dW = dDelta, -dDelta @ S0
+                dT = dU @ BV.T + dW @ BW.T
+                dBV, dBW = Tm.T @ dU, Tm.T @ dW
+                dA = strict * (-(Tm.T @ dT @ Tm.T))
+                dbe = (dBV * Vc).sum(1) + (dBW * Kg).sum(1) + (dA * ((Kg @ Kn.T))).sum(1)
+                dVc = be[:, None] * dBV
+                dKg = be[:, None] * dBW + be[:, None] * (dA @ Kn)
+                dKn = dA.T @ (be[:, None] * Kg) + dP.T @ Qg
+                dQg = dQg + dP @ Kn
+                dKh_c = dKg * eG + dKn * enG + dKd * np.exp(GC[None, :] - Gam)
+                dGam = dKg * Kg - dKn * Kn + dQg * Qg - dKd * Kd
+                dGC = dGC + (dKd * Kd).sum(0)
+                dQt_c = dQg * eG
+                # Gam_r = sum_{s <= r} g_s and Gam_C = Gam_{L-1}: dg_s = sum_{r >= s} dGam_r + dGam_C
+                dgc = np.cumsum(dGam[::-1], axis=0)[::-1] + dGC[None, :]
+                dqt[bi, c0:c1, h] = dQt_c
+                dkh[bi, c0:c1, h] = dKh_c
+                dv[bi, c0:c1, h] = dVc
+                dbeta[bi, c0:c1, h] = dbe
+                dg[bi, c0:c1, h] = dgc
+                dS = dS0
+            dh0[n, h] = dS
+    dqs = dqt.reshape(B, T, H_qk, G, K).sum(3)
+    dks = dkh.reshape(B, T, H_qk, G, K).sum(3)
+    rq, rk = 1.0 / nq, 1.0 / nk
+    dq = sc * rq * (dqs - rq * rq * qq * (qq * dqs).sum(-1, keepdims=True))
+    dk = rk * (dks - rk * rk * kk * (kk * dks).sum(-1, keepdims=True))
+    sig = 1.0 / (1.0 + np.exp(-gg))
+    dgraw = dg * (-a[None, None, :, None]) * sig
+    dA_log = (dg * g_all).sum(axis=(0, 1, 3))
+    db = dbeta * beta_all * (1.0 - beta_all)
+    out = dict(dq=dq, dk=dk, dv=dv, dgraw=dgraw, db=db, dA_log=dA_log, dh0=dh0)
+    return {n_: torch.from_numpy(np.ascontiguousarray(x)) for n_, x in out.items()}
+
+
+def chunk_bwd_inputs(inp, do, dht=None, **kw):
+    return chunk_bwd(inp.q, inp.k, inp.v, inp.graw, inp.b, inp.A_log, inp.scale, inp.initial_state,
+                     inp.cu_seqlens, do=do, dht=dht, **kw)

@@ -115,3 +115,27 @@ def test_recurrent_backward_matches_autograd(case):
     for name in a:
         err = _max_rel(r[name], a[name])
         assert err <= 1e-9, (name, err)
+
+
+@pytest.mark.parametrize("case", ["plain", "gva_varlen", "no_state", "small_chunks"])
+def test_chunked_backward_algebra_matches_autograd(case):
+    """The chunked (UT/WY) backward formulas, the algebra a tensor-core backward
+    uses, give the autograd oracle's gradients."""
+    import kda_inputs as KI
+    from oracle import chunk_bwd_model as CB
+    if case == "plain":
+        inp, C = KI.make_inputs(1, 150, 1, 2, seed=50, with_state=True), 64
+    elif case == "gva_varlen":
+        inp, C = KI.make_inputs(1, 140, 1, 2, seed=51, with_state=True, seqlens=[70, 0, 1, 69]), 64
+    elif case == "no_state":
+        inp, C = KI.make_inputs(2, 65, 2, 2, seed=52, with_state=False), 64
+    else:
+        inp, C = KI.make_inputs(1, 50, 1, 1, seed=53, with_state=True), 16
+    g = torch.Generator().manual_seed(31)
+    do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
+    dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1
+    a = OB.bwd_inputs(inp, do, dht)
+    c = CB.chunk_bwd_inputs(inp, do, dht, C=C)
+    for name in a:
+        err = _max_rel(c[name], a[name])
+        assert err <= 1e-9, (name, err)
