@@ -4,12 +4,17 @@
     python -m gated_delta_rule_40_gb300.profile_case --method la --B 1 --T 8192 --H 64 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method bwd --B 1 --T 2048 --H 8 --iters 3
     python -m gated_delta_rule_40_gb300.profile_case --method la_decode --B 256 --H 64 --iters 4
+    python -m gated_delta_rule_40_gb300.profile_case --method gdn --B 1 --T 8192 --H 32 --iters 4
+    python -m gated_delta_rule_40_gb300.profile_case --method decode_tokens --B 256 --T 4 --H 64 --iters 4
 
 Inputs come from ``kda_inputs`` (same recipe as the tests and the benchmark);
 the workspace is allocated once, so every iteration is exactly the three
-kernel launches of ``kda_fwd`` (two for ``kda_la_fwd``: plan and la_fwd_kernel; three for
-``kda_bwd``: plan, bwd_recur_kernel and bwd_prologue_kernel).  A profiler then selects launches by kernel
-name and index (e.g. ``ncu -k regex:intra_kernel -s 2 -c 1``).
+kernel launches of ``kda_fwd`` (three for ``kda_fwd_scalar_gate``: plan, intra_gdn_kernel
+and scan_kernel; two for ``kda_la_fwd``: plan and la_fwd_kernel; three for ``kda_bwd``:
+plan, bwd_recur_kernel and bwd_prologue_kernel; one for ``kda_decode_tokens``, whose
+``--T`` is the token count Tq of the step and whose state is fp32 unless
+``--bf16-state``).  A profiler then selects launches by kernel name and index (e.g.
+``ncu -k regex:intra_kernel -s 2 -c 1``).
 """
 import argparse
 import os
@@ -29,8 +34,19 @@ def main() -> None:
     ap.add_argument("--H", type=int, default=32, help="value heads (= q/k heads)")
     ap.add_argument("--iters", type=int, default=4)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--method", choices=["kda", "la", "bwd", "la_decode"], default="kda")
+    ap.add_argument("--method", choices=["kda", "gdn", "la", "bwd", "la_decode", "decode_tokens"], default="kda")
+    ap.add_argument("--bf16-state", action="store_true", help="decode_tokens: bf16 state")
     a = ap.parse_args()
+    if a.method == "decode_tokens":
+        x = kda_inputs.make_inputs(a.B, a.T, a.H, a.H, seed=a.seed, with_state=True)
+        q, k, v, gr, b, A = (t.cuda() for t in (x.q, x.k, x.v, x.graw, x.b, x.A_log))
+        st = x.initial_state.to(torch.bfloat16 if a.bf16_state else torch.float32).cuda()
+        for _ in range(a.iters):
+            o = kda.kda_decode_tokens(q, k, v, gr, b, A, x.scale, st)
+        torch.cuda.synchronize()
+        print(f"kda_decode_tokens B={a.B} Tq={a.T} H={a.H} state {st.dtype} x{a.iters}: "
+              f"|o| {float(o.float().abs().mean()):.6f}")
+        return
     if a.method == "la_decode":
         d = kda_inputs.la_decode_inputs(B=a.B, H=a.H, seed=a.seed)
         q, k, v, sl, st = (t.cuda() for t in (d.q, d.k, d.v, d.slope, d.state))
@@ -48,7 +64,17 @@ def main() -> None:
         print(f"kda_la_fwd B={a.B} T={a.T} H={a.H} x{a.iters}: |out| {float(out.float().abs().mean()):.6f} "
               f"|S| {float(fin.abs().mean()):.6f}")
         return
-    x = kda_inputs.make_inputs(B=a.B, T=a.T, H_qk=a.H, H_v=a.H, seed=a.seed, with_state=True)
+    x = kda_inputs.make_inputs(B=a.B, T=a.T, H_qk=a.H, H_v=a.H, seed=a.seed, with_state=True,
+                               scalar_gate=a.method == "gdn")
+    if a.method == "gdn":
+        q, k, v, b, A, s0 = (t.cuda() for t in (x.q, x.k, x.v, x.b, x.A_log, x.initial_state))
+        gr = x.graw[..., 0].contiguous().cuda()
+        for _ in range(a.iters):
+            out, fin = kda.kda_fwd_scalar_gate(q, k, v, gr, b, A, x.scale, initial_state=s0)
+        torch.cuda.synchronize()
+        print(f"kda_fwd_scalar_gate B={a.B} T={a.T} H={a.H} x{a.iters}: |out| {float(out.float().abs().mean()):.6f} "
+              f"|S| {float(fin.abs().mean()):.6f}")
+        return
     if a.method == "bwd":
         g = torch.Generator().manual_seed(a.seed + 1)
         dout = torch.randn(x.v.shape, generator=g).to(torch.bfloat16).cuda()
