@@ -20,10 +20,11 @@
 // chain are independent, so four CTAs share a chain.  Warp w owns rows
 // 4w .. 4w + 3 of the quarter, lane owns channels 4 lane .. 4 lane + 3, so S and
 // dS live in registers (16 values each).  A first pass runs the recurrence and
-// stores the state at every 32-token block start; the backward pass then takes
+// stores the state at every 16-token block start; the backward pass then takes
 // the blocks in reverse: it recomputes the block's states from its checkpoint
-// into a per-CTA scratch area (512 KiB; each thread reads back only what it
-// wrote), then walks the block's tokens backwards.  The per-token vectors (qt,
+// into a per-CTA scratch area (256 KiB; each thread reads back only what it
+// wrote; the scratch of all resident CTAs stays within L2), then walks the
+// block's tokens backwards.  The per-token vectors (qt,
 // kh, e, v, do, beta) of a block are staged in shared memory; the sums over the
 // quarter's rows of dqt, dkh, de and dbeta are reduced across warps through
 // shared memory (one barrier per token, alternating areas) and written per
@@ -44,10 +45,12 @@ constexpr int BW_WARPS = 8;
 constexpr int BW_THREADS = BW_WARPS * 32;
 constexpr int BW_PARTS = 4;                            // CTAs per chain
 constexpr int BW_ROWS = KD / BW_PARTS / BW_WARPS;      // 4 state rows per warp
-constexpr int BW_CT = 32;                              // tokens per block (checkpoint interval)
-constexpr uint32_t BW_VEC = BW_CT * KD * 4;            // one [32][128] fp32 table
+constexpr int BW_CT = 16;                              // tokens per block (checkpoint interval)
+constexpr int BW_BPC = CH / BW_CT;                     // blocks per 64-token chunk
+static_assert(CH % BW_CT == 0, "blocks tile a chunk");
+constexpr uint32_t BW_VEC = BW_CT * KD * 4;            // one [BW_CT][128] fp32 table
 constexpr uint32_t BW_QT = 0, BW_KH = BW_VEC, BW_E = 2 * BW_VEC, BW_V = 3 * BW_VEC, BW_DO = 4 * BW_VEC;
-constexpr uint32_t BW_BETA = 5 * BW_VEC;            // [32]
+constexpr uint32_t BW_BETA = 5 * BW_VEC;            // [BW_CT]
 constexpr uint32_t BW_RED = BW_BETA + 128;          // 2 x [8 warps][3][128] (alternating tokens)
 constexpr uint32_t BW_REDB = BW_RED + 2 * BW_WARPS * 3 * KD * 4;   // 2 x [8]
 constexpr uint32_t BW_BYTES = BW_REDB + 64;
@@ -61,8 +64,8 @@ struct BwdParams {
     const SeqDesc *seqs;
     const int *order;
     const int *hdr;
-    float *ckpt;      // [2 chunk + block][H_v][V][K]
-    float *scratch;   // [gridDim.x][32][32 rows][K]
+    float *ckpt;      // [BW_BPC chunk + block][H_v][V][K]
+    float *scratch;   // [gridDim.x][BW_CT][32 rows][K]
     float *dqt, *dkh, *de, *dbeta;   // [token][H_v][part][128] (dbeta [token][H_v][part])
     float *dv, *dh0;                 // [token][H_v][V], [N][H_v][V][K]
 };
@@ -189,7 +192,7 @@ __global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParam
         // ---- pass 1: the recurrence, storing the state at each block start
         for (int c = 0; c < nblk; ++c) {
             const int len = min(BW_CT, sd.len - c * BW_CT), tok0 = sd.tok + c * BW_CT;
-            const size_t cb = ((size_t)(2 * sd.chunk0 + c) * p.H_v + h) * KD * KD;
+            const size_t cb = ((size_t)(BW_BPC * sd.chunk0 + c) * p.H_v + h) * KD * KD;
 #pragma unroll
             for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(p.ckpt + slice(cb, i)) = S[i];
             __syncthreads();   // the previous block's tables are no longer read
@@ -207,7 +210,7 @@ __global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParam
             dS[i] = p.dht ? *reinterpret_cast<const float4 *>(p.dht + slice(sh, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
         for (int c = nblk - 1; c >= 0; --c) {
             const int len = min(BW_CT, sd.len - c * BW_CT), tok0 = sd.tok + c * BW_CT;
-            const size_t cb = ((size_t)(2 * sd.chunk0 + c) * p.H_v + h) * KD * KD;
+            const size_t cb = ((size_t)(BW_BPC * sd.chunk0 + c) * p.H_v + h) * KD * KD;
             __syncthreads();
             bwd_stage_chunk(p, sm, tok0, len, h, hq, a_gate, true, warp, lane);
             __syncthreads();
@@ -430,7 +433,7 @@ size_t bwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, int grid) 
     off = a256(off + sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1));
     off = a256(off + sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1));
     off = a256(off + sizeof(int) * (size_t)(nseq > 0 ? nseq : 1));
-    off = a256(off + (size_t)2 * (nck > 0 ? nck : 1) * H_v * KD * KD * 4);       // checkpoints
+    off = a256(off + (size_t)BW_BPC * (nck > 0 ? nck : 1) * H_v * KD * KD * 4);       // checkpoints
     off = a256(off + (size_t)grid * BW_CT * (KD / BW_PARTS) * KD * 4);          // scratch
     off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * KD * 4 * 3);   // dqt, dkh, de
     off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * 4);            // dbeta
@@ -465,7 +468,7 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     ChunkDesc *chunks = reinterpret_cast<ChunkDesc *>(take(sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1)));
     int *order = reinterpret_cast<int *>(take(sizeof(int) * (size_t)(nseq > 0 ? nseq : 1)));
     BwdParams bp;
-    bp.ckpt = reinterpret_cast<float *>(take((size_t)2 * (nck > 0 ? nck : 1) * H_v * KD * KD * 4));
+    bp.ckpt = reinterpret_cast<float *>(take((size_t)BW_BPC * (nck > 0 ? nck : 1) * H_v * KD * KD * 4));
     bp.scratch = reinterpret_cast<float *>(take((size_t)grid * BW_CT * (KD / BW_PARTS) * KD * 4));
     const size_t tv = (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * KD;
     float *t3 = reinterpret_cast<float *>(take(tv * 4 * 3));

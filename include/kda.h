@@ -238,13 +238,14 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
  *
  * All outputs are written (dA_log is zeroed, then accumulated).  Gradient
  * buffers must be 16-byte aligned (db excepted).  Asynchronous on `stream`; the
- * workspace comes from cudaMallocAsync on `stream`: state checkpoints every 32
- * tokens (2 KiB per token and value head), per-token partial sums of four
- * row quarters (6 KiB per token and value head) and 512 KiB of scratch per
- * resident CTA, i.e. about 8 KiB per token and value head (8.7 GB for B=2,
- * T=16384, H_v=32); a failed allocation returns KDA_ERR_CUDA.  This is the token recurrence run backwards on
- * CUDA cores in fp32 (one persistent CTA per (sequence, value head) chain);
- * errors as kda_fwd.
+ * workspace comes from cudaMallocAsync on `stream`: state checkpoints every 16
+ * tokens (4 KiB per token and value head), per-token partial sums of four
+ * row quarters (6 KiB per token and value head) and 256 KiB of scratch per
+ * resident CTA, i.e. about 10 KiB per token and value head (10.8 GB for B=2,
+ * T=16384, H_v=32); a failed allocation returns KDA_ERR_CUDA.  This is the
+ * token recurrence run backwards on CUDA cores in fp32 (persistent CTAs, four
+ * per (sequence, value head) chain, one per quarter of the state rows); errors
+ * as kda_fwd.
  */
 int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
             const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
