@@ -110,6 +110,13 @@ thread_local int t_last_launches = 0;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Work items carry 32-bit block indices: (sequence, value head) chains times up to four row
+// blocks (the scan's two V blocks, the backward's four row quarters) and (b, h) decode pairs
+// must stay below 2^31, or a launch would cover only part of the work.
+constexpr long long kMaxItems = 0x7fffffffLL;
+bool chains_fit(long long nseq, int H_v) { return nseq * H_v * 4 <= kMaxItems; }
+bool pairs_fit(int B, int H_v) { return (long long)B * H_v <= kMaxItems; }
+
 int validate_fwd(const void *q, const void *k, const void *v, const void *graw, const void *b,
                  const void *A_log, const void *init, const void *fin, const int32_t *cu, int N, int B, int T,
                  int H_qk, int H_v, int K, int V, const void *out) {
@@ -120,7 +127,7 @@ int validate_fwd(const void *q, const void *k, const void *v, const void *graw, 
         if (B != 1 || N < 0) return KDA_ERR_INVALID_ARG;
     }
     const long long tokens = (long long)B * T;
-    if (tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (tokens > 0x7fffffffLL || !chains_fit(cu ? N : B, H_v)) return KDA_ERR_INVALID_ARG;
     if (tokens > 0) {
         if (!q || !k || !v || !graw || !b || !A_log || !out) return KDA_ERR_INVALID_ARG;
         if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(graw) || !aligned16(out))
@@ -256,7 +263,7 @@ int kda_decode_tokens(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t
                       int Tq, int H_qk, int H_v, int K, int V, kda_bf16_t *out, cudaStream_t stream) {
     if (K != kda::KD || V != kda::KD) return KDA_ERR_UNSUPPORTED;
     if (B < 0 || Tq < 1 || Tq > KDA_DECODE_MAX_TOKENS || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0 ||
-        (state_is_bf16 != 0 && state_is_bf16 != 1))
+        (state_is_bf16 != 0 && state_is_bf16 != 1) || !pairs_fit(B, H_v))
         return KDA_ERR_INVALID_ARG;
     if (B == 0) {
         t_last_launches = 0;
@@ -279,7 +286,7 @@ int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
                     const kda_bf16_t *b, const float *A_log, float scale, float *state, int B, int H_qk, int H_v,
                     int K, int V, kda_bf16_t *out, cudaStream_t stream) {
     if (K != kda::KD || V != kda::KD) return KDA_ERR_UNSUPPORTED;
-    if (B < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0) return KDA_ERR_INVALID_ARG;
+    if (B < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0 || !pairs_fit(B, H_v)) return KDA_ERR_INVALID_ARG;
     if (B == 0) {
         t_last_launches = 0;
         return KDA_OK;
@@ -336,8 +343,8 @@ int kda_la_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, co
     if (B < 0 || T < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0) return KDA_ERR_INVALID_ARG;
     if (cu_seqlens && (B != 1 || N < 0)) return KDA_ERR_INVALID_ARG;
     const long long tokens = (long long)B * T;
-    if (tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     const int nseq = cu_seqlens ? N : B;
+    if (tokens > 0x7fffffffLL || !chains_fit(nseq, H_v)) return KDA_ERR_INVALID_ARG;
     if (nseq > 0 && !slope) return KDA_ERR_INVALID_ARG;
     if (tokens > 0) {
         if (!q || !k || !v || !out) return KDA_ERR_INVALID_ARG;
@@ -364,7 +371,7 @@ int kda_la_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, co
 int kda_la_decode(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const float *slope, float scale,
                   float *state, int B, int H_qk, int H_v, int K, int V, kda_bf16_t *out, cudaStream_t stream) {
     if (K != kda::KD || V != kda::KD) return KDA_ERR_UNSUPPORTED;
-    if (B < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0) return KDA_ERR_INVALID_ARG;
+    if (B < 0 || H_qk <= 0 || H_v <= 0 || H_v % H_qk != 0 || !pairs_fit(B, H_v)) return KDA_ERR_INVALID_ARG;
     if (B == 0) {
         t_last_launches = 0;
         return KDA_OK;

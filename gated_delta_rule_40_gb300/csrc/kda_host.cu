@@ -63,6 +63,7 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
     if (tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (tokens > 0 && (!q || !k || !v || !graw || !b || !A_log || !out)) return KDA_ERR_INVALID_ARG;
     const int nseq = cu_seqlens ? N : B;
+    if ((long long)nseq * H_v * 4 > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;   // 32-bit work-item indices
 
     // packed sequence boundaries (host copy; checked here, so a malformed array is an error return)
     std::vector<int32_t> cu((size_t)nseq + 1);

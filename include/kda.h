@@ -53,7 +53,10 @@ typedef uint16_t kda_bf16_t; /* bit pattern of a bfloat16 value */
 enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = -1,    /* NULL required pointer, negative size, H_v % H_qk != 0,
-                                    cu_seqlens with B != 1, misaligned pointer */
+                                    cu_seqlens with B != 1, misaligned pointer, more than
+                                    2^31 - 1 tokens (B * T), sequences * H_v above
+                                    2^29 - 1 (chunked calls) or B * H_v above 2^31 - 1
+                                    (decode calls): work items carry 32-bit indices */
     KDA_ERR_UNSUPPORTED = -2,    /* K != 128 or V != 128 */
     KDA_ERR_CUDA = -3,           /* a CUDA runtime call or kernel launch failed */
     KDA_ERR_DEVICE_TIMEOUT = -4, /* (status word) a bounded device-side wait gave up */

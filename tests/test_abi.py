@@ -106,3 +106,25 @@ def test_bwd_rejects_bad_args(lib):
     assert bwd(dq=FAKE_ODD) == kda.KDA_ERR_INVALID_ARG
     assert bwd(dA=None) == kda.KDA_ERR_INVALID_ARG
     assert bwd(dh0=None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_work_item_limits(lib):
+    """Calls whose 32-bit work-item indices would overflow are rejected before any device
+    call: 2^28 sequences x 2 value heads x 4 row blocks, and 2^30 x 2 decode pairs."""
+    f = ctypes.c_float(0.1)
+    big = 1 << 28
+    assert _fwd(lib, H_v=2, B=1, T=4, N=big, cu=FAKE) == kda.KDA_ERR_INVALID_ARG
+    assert _fwd(lib, H_v=2, B=big, T=1) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_fwd_host(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, f, None, None, FAKE, big, 1, 4, 1, 2, 128, 128,
+                            FAKE, None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_la_fwd(FAKE, FAKE, FAKE, FAKE, f, None, None, FAKE, big, 1, 4, 1, 2, 128, 128, FAKE,
+                          None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, f, None, None, 0, big, 1, 1, 2, 128, 128, FAKE, None,
+                       FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None) == kda.KDA_ERR_INVALID_ARG
+    pairs = 1 << 30
+    assert lib.kda_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, f, FAKE, pairs, 1, 2, 128, 128, FAKE,
+                               None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_tokens(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, f, FAKE, 0, pairs, 1, 1, 2, 128, 128, FAKE,
+                                 None) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_la_decode(FAKE, FAKE, FAKE, FAKE, f, FAKE, pairs, 1, 2, 128, 128, FAKE,
+                             None) == kda.KDA_ERR_INVALID_ARG
