@@ -449,6 +449,11 @@ def run_gpu(args, rank, world, local):
     bwd_step()
     torch.cuda.synchronize()
     bwd_ms = time_events(bwd_step, 3, stream)
+    # per-kernel split of one more call (events recorded by the library between its launches)
+    kda.kda_set_kernel_timing(True)
+    bwd_step()
+    bwd_kernels = {name: t for name, t in kda.kda_kernel_times()}
+    kda.kda_set_kernel_timing(False)
     bwd_flops = units * BWD_FLOPS_PER_TOKEN_HEAD
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     alu_peak = sm_count * 128 * 2 * (clk.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
@@ -457,7 +462,8 @@ def run_gpu(args, rank, world, local):
                              "peak": alu_peak, "unit": "TFLOP/s",
                              "frac": bwd_flops / (bwd_ms * 1e-3) / 1e12 / alu_peak,
                              "peak_source": "SMs x 128 fp32 lanes x 2 flops x max SM clock",
-                             "flops_per_token_head": BWD_FLOPS_PER_TOKEN_HEAD}}
+                             "flops_per_token_head": BWD_FLOPS_PER_TOKEN_HEAD},
+                "kernels_ms": bwd_kernels}
     del gout, ght
     status = kda.kda_get_status()
     if status != 0:

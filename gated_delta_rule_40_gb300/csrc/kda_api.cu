@@ -328,10 +328,7 @@ int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const
                                           B, T, H_qk, H_v, dout, dht, dq, dk, dv, dgraw, db, dA_log, dh0, ws, grid,
                                           stream, &launches);
     rc = e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
-    if (rc == KDA_OK) {
-        kda::timing_mark("bwd (plan, recurrence, prologue)", stream);
-        t_last_launches = launches;
-    }
+    if (rc == KDA_OK) t_last_launches = launches;
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
     return rc;
 }

@@ -40,6 +40,7 @@ namespace kda {
 cudaError_t launch_plan(const int32_t *cu, int N, int B, int T, SeqDesc *seqs, ChunkDesc *chunks, int *order,
                         int *hdr, long long max_chunks, cudaStream_t stream);
 long long max_chunks_for(int N, int B, int T, bool varlen);
+void timing_mark(const char *name, cudaStream_t s);
 
 constexpr int BW_WARPS = 8;
 constexpr int BW_THREADS = BW_WARPS * 32;
@@ -483,6 +484,7 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     if (e != cudaSuccess) return e;
     ++*launches;
     if ((e = cudaMemsetAsync(dA_log, 0, sizeof(float) * H_v, stream)) != cudaSuccess) return e;
+    timing_mark("plan_kernel", stream);
     if (nseq > 0) {
         if ((e = cudaFuncSetAttribute(bwd_recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)(BW_BYTES + 128))) != cudaSuccess)
@@ -490,6 +492,7 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         bwd_recur_kernel<<<grid, BW_THREADS, BW_BYTES + 128, stream>>>(bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        timing_mark("bwd_recur_kernel", stream);
     }
     if (tokens > 0) {
         const long long warps = ((tokens + BP_TOKENS - 1) / BP_TOKENS) * H_qk;
@@ -497,6 +500,7 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
             bp, dq, dk, dgraw, db, dA_log, tokens);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        timing_mark("bwd_prologue_kernel", stream);
     }
     return cudaSuccess;
 }

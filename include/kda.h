@@ -311,9 +311,9 @@ int kda_selftest_wait_timeout(cudaStream_t stream);
 int kda_last_launch_count(void);
 
 /*
- * Measurement aid (off by default).  While enabled, kda_fwd, kda_fwd_ws and
- * kda_decode_step record a CUDA event on `stream` before their first and
- * after each kernel launch.  kda_kernel_times waits for the events of the most
+ * Measurement aid (off by default).  While enabled, the forward, decode,
+ * backward and lightning-attention entry points record a CUDA event on
+ * `stream` before their first and after each kernel launch.  kda_kernel_times waits for the events of the most
  * recent call on this host thread and writes up to max_n per-kernel durations
  * in milliseconds (and static kernel names when `names` is not NULL); it
  * returns the number written, 0 when timing is off, or KDA_ERR_CUDA.
