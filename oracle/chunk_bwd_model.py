@@ -25,21 +25,52 @@ Backward of one chunk, given dO and dS_C (products read right to left):
 Chunks are visited in reverse with dS carried from each chunk's S_0 to the
 previous chunk's S_C; the forward states S_0 come from a forward pass.  The
 prologue's Jacobians (norms, gate, sigmoid) are those of ``backward.bwd``.
+
+``rounding`` maps operand names to a number format the operand is rounded to
+where it enters a product (``"bf16"`` nearest-even, ``"tf32"`` nearest-even to
+10 fraction bits, ``"tf32_trunc"`` the low 13 bits dropped), so the tests can
+choose a tensor-core backward's operand formats: the state side S0, dS, W, Qg
+(in dOᵀQg), P, Kd, Delta, dDelta, dW, BV = diag(beta) V, T, dT, dA and dP.  The
+key-side decay products (Kg, Kn and diag(beta) Kg against dA and dP) are not
+offered: in the e^{+Gam} / e^{-Gam} split written here they cancel, so a kernel
+forms them against in-chunk reference points (as the forward does) and their
+rounding has to be studied in that form.
 """
 from __future__ import annotations
 
-from typing import Dict
+from typing import Dict, Optional
 
 import numpy as np
 import torch
 
 from .backward import EPS
 
+ROUNDABLE = ("S0", "dS", "W", "Qg", "P", "Kd", "Delta", "dDelta", "dW", "BV", "T", "dT", "dA", "dP")
+
+
+def _round(x: np.ndarray, fmt: str) -> np.ndarray:
+    """``x`` rounded to ``fmt`` (through fp32) and returned in fp64."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    if fmt == "bf16":
+        u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    elif fmt == "tf32":
+        u = (u + 0xFFF + ((u >> 13) & 1)) & 0xFFFFE000
+    elif fmt == "tf32_trunc":
+        u = u & 0xFFFFE000
+    else:
+        raise ValueError(fmt)
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
 
 def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=None, do=None, dht=None,
-              C: int = 64) -> Dict[str, torch.Tensor]:
+              C: int = 64, rounding: Optional[Dict[str, str]] = None) -> Dict[str, torch.Tensor]:
     """Gradients as ``backward.bwd`` returns them (fp64 tensors), computed with
-    the chunked formulas above."""
+    the chunked formulas above (operands rounded as ``rounding`` names)."""
+    rnd = dict(rounding or {})
+    bad = set(rnd) - set(ROUNDABLE)
+    if bad:
+        raise ValueError(f"not roundable here: {sorted(bad)}")
+    r = lambda name, x: _round(x, rnd[name]) if name in rnd else x  # noqa: E731
     f64 = lambda t: t.detach().to(torch.float64).numpy()  # noqa: E731
     qq, kk, vv, gg, bb, aa = (f64(t) for t in (q, k, v, graw, b, A_log))
     B, T, H_qk, K = qq.shape
@@ -90,22 +121,28 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
                 BV, BW = be[:, None] * Vc, be[:, None] * Kg
                 U, W = Tm @ BV, Tm @ BW
                 Delta = U - W @ S0.T
-                # ---- backward of the chunk
-                dDelta = P.T @ dO + Kd @ dS.T
-                dKd = Delta @ dS
-                dQg = dO @ S0
-                dS0 = dO.T @ Qg + dS * np.exp(GC)[None, :] - dDelta.T @ W
+                # ---- backward of the chunk (r(): an operand as it enters a product)
+                S0r, dSr, Wr = r("S0", S0), r("dS", dS), r("W", W)
+                if rnd:
+                    Delta = U - Wr @ S0r.T
+                dDelta = r("P", P).T @ dO + r("Kd", Kd) @ dSr.T
+                dKd = r("Delta", Delta) @ dSr
+                dQg = dO @ S0r
+                dDr = r("dDelta", dDelta)
+                dS0 = dO.T @ r("Qg", Qg) + dS * np.exp(GC)[None, :] - dDr.T @ Wr
                 dGC = (S0 * dS).sum(0) * np.exp(GC)
-                dP = incl * (dO @ Delta.T)
-                dU, dW = dDelta, -dDelta @ S0
-                dT = dU @ BV.T + dW @ BW.T
-                dBV, dBW = Tm.T @ dU, Tm.T @ dW
-                dA = strict * (-(Tm.T @ dT @ Tm.T))
+                dP = incl * (dO @ r("Delta", Delta).T)
+                dU, dW = dDelta, -dDr @ S0r
+                dWr, Tr = r("dW", dW), r("T", Tm)
+                dT = dDr @ r("BV", BV).T + dWr @ BW.T
+                dBV, dBW = Tr.T @ dDr, Tr.T @ dWr
+                dA = strict * (-(Tr.T @ r("dT", dT) @ Tr.T))
                 dbe = (dBV * Vc).sum(1) + (dBW * Kg).sum(1) + (dA * ((Kg @ Kn.T))).sum(1)
                 dVc = be[:, None] * dBV
-                dKg = be[:, None] * dBW + be[:, None] * (dA @ Kn)
-                dKn = dA.T @ (be[:, None] * Kg) + dP.T @ Qg
-                dQg = dQg + dP @ Kn
+                dAr, dPr = r("dA", dA), r("dP", dP)
+                dKg = be[:, None] * dBW + be[:, None] * (dAr @ Kn)
+                dKn = dAr.T @ (be[:, None] * Kg) + dPr.T @ Qg
+                dQg = dQg + dPr @ Kn
                 dKh_c = dKg * eG + dKn * enG + dKd * np.exp(GC[None, :] - Gam)
                 dGam = dKg * Kg - dKn * Kn + dQg * Qg - dKd * Kd
                 dGC = dGC + (dKd * Kd).sum(0)
@@ -133,5 +170,6 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
 
 
 def chunk_bwd_inputs(inp, do, dht=None, **kw):
+    """``chunk_bwd`` on a ``kda_inputs.KdaInputs``."""
     return chunk_bwd(inp.q, inp.k, inp.v, inp.graw, inp.b, inp.A_log, inp.scale, inp.initial_state,
                      inp.cu_seqlens, do=do, dht=dht, **kw)
