@@ -26,6 +26,24 @@ Chunks are visited in reverse with dS carried from each chunk's S_0 to the
 previous chunk's S_C; the forward states S_0 come from a forward pass.  The
 prologue's Jacobians (norms, gate, sigmoid) are those of ``backward.bwd``.
 
+``form="pairwise"`` writes the products that pair a key with an earlier key or
+query (A, P and their gradients) with the pairwise decays e^{Gam_r - Gam_j}
+(j <= r, at most 1) instead of the e^{+Gam} / e^{-Gam} split, so no factor
+overflows however strong the gate (the split's e^{-Gam} exceeds the fp64 range
+once a chunk's decay passes 709 nats).  With M = diag(beta) dA and N = dP:
+
+  dKh_r += sum_j M_rj Kh_j e^{Gam_r - Gam_j} + sum_i M_ir Kh_i e^{Gam_i - Gam_r}
+           + sum_i N_ir Qt_i e^{Gam_i - Gam_r}
+  dQt_r += sum_j N_rj Kh_j e^{Gam_r - Gam_j}
+  dGam_r  gets each term above times Kh_r or Qt_r, with the sign of Gam_r in its
+          exponent (plus for the row side, minus for the column side); P's diagonal
+          (decay e^0) enters dQt and dKh but not dGam
+
+and the other terms as in the split form, except that Kd_r = Kh_r e^{Gam_C - Gam_r},
+which depends on g_s for s > r only, reaches dg through an exclusive prefix sum
+(the split form adds it to every token through Gam_C and takes it back from the
+tokens s <= r, two equal amounts that cancel when the gate is strong).
+
 ``rounding`` maps operand names to a number format the operand is rounded to
 where it enters a product (``"bf16"`` nearest-even, ``"tf32"`` nearest-even to
 10 fraction bits, ``"tf32_trunc"`` the low 13 bits dropped), so the tests can
@@ -63,9 +81,13 @@ def _round(x: np.ndarray, fmt: str) -> np.ndarray:
 
 
 def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=None, do=None, dht=None,
-              C: int = 64, rounding: Optional[Dict[str, str]] = None) -> Dict[str, torch.Tensor]:
+              C: int = 64, rounding: Optional[Dict[str, str]] = None, form: str = "split") -> Dict[str, torch.Tensor]:
     """Gradients as ``backward.bwd`` returns them (fp64 tensors), computed with
-    the chunked formulas above (operands rounded as ``rounding`` names)."""
+    the chunked formulas above (operands rounded as ``rounding`` names; key
+    products in the ``form`` "split" or "pairwise")."""
+    if form not in ("split", "pairwise"):
+        raise ValueError(form)
+    pairwise = form == "pairwise"
     rnd = dict(rounding or {})
     bad = set(rnd) - set(ROUNDABLE)
     if bad:
@@ -111,12 +133,21 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
                 L = c1 - c0
                 Gam = np.cumsum(gc, axis=0)
                 GC = Gam[-1]
-                eG, enG = np.exp(Gam), np.exp(-Gam)
-                Kg, Kn, Qg, Kd = Kh * eG, Kh * enG, Qt * eG, Kh * np.exp(GC[None, :] - Gam)
+                eG = np.exp(Gam)
+                Kg, Qg, Kd = Kh * eG, Qt * eG, Kh * np.exp(GC[None, :] - Gam)
                 strict = np.tril(np.ones((L, L)), -1)
                 incl = np.tril(np.ones((L, L)))
-                A = strict * ((be[:, None] * Kg) @ Kn.T)
-                P = incl * (Qg @ Kn.T)
+                if pairwise:
+                    # E[r, j, c] = e^{Gam_rc - Gam_jc} for j <= r, 0 above the diagonal
+                    E = np.exp(np.where(incl[:, :, None] > 0, Gam[:, None, :] - Gam[None, :, :], -np.inf))
+                    KK = np.einsum("rc,jc,rjc->rj", Kh, Kh, E)
+                    P = incl * np.einsum("rc,jc,rjc->rj", Qt, Kh, E)
+                else:
+                    enG = np.exp(-Gam)
+                    Kn = Kh * enG
+                    KK = Kg @ Kn.T
+                    P = incl * (Qg @ Kn.T)
+                A = strict * (be[:, None] * KK)
                 Tm = np.linalg.inv(np.eye(L) + A)
                 BV, BW = be[:, None] * Vc, be[:, None] * Kg
                 U, W = Tm @ BV, Tm @ BW
@@ -137,18 +168,39 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
                 dT = dDr @ r("BV", BV).T + dWr @ BW.T
                 dBV, dBW = Tr.T @ dDr, Tr.T @ dWr
                 dA = strict * (-(Tr.T @ r("dT", dT) @ Tr.T))
-                dbe = (dBV * Vc).sum(1) + (dBW * Kg).sum(1) + (dA * ((Kg @ Kn.T))).sum(1)
+                dbe = (dBV * Vc).sum(1) + (dBW * Kg).sum(1) + (dA * KK).sum(1)
                 dVc = be[:, None] * dBV
                 dAr, dPr = r("dA", dA), r("dP", dP)
-                dKg = be[:, None] * dBW + be[:, None] * (dAr @ Kn)
-                dKn = dAr.T @ (be[:, None] * Kg) + dPr.T @ Qg
-                dQg = dQg + dPr @ Kn
-                dKh_c = dKg * eG + dKn * enG + dKd * np.exp(GC[None, :] - Gam)
-                dGam = dKg * Kg - dKn * Kn + dQg * Qg - dKd * Kd
-                dGC = dGC + (dKd * Kd).sum(0)
-                dQt_c = dQg * eG
+                if pairwise:
+                    M = be[:, None] * dAr
+                    XA = np.einsum("rj,jc,rjc->rc", M, Kh, E)      # row side of A
+                    YA = np.einsum("rj,rc,rjc->jc", M, Kh, E)      # column side of A
+                    # P's diagonal (decay e^0 = 1) has no Gam gradient: its terms enter dQt and dKh
+                    # only, so the Gam terms never add and subtract O(1) amounts that cancel exactly
+                    dPs, dPd = strict * dPr, np.diag(dPr)[:, None]
+                    XP = np.einsum("rj,jc,rjc->rc", dPs, Kh, E)    # row side of P (the query)
+                    YP = np.einsum("rj,rc,rjc->jc", dPs, Qt, E)    # column side of P (the key)
+                    dKgW = be[:, None] * dBW
+                    dKh_c = dKgW * eG + XA + YA + YP + dPd * Qt + dKd * np.exp(GC[None, :] - Gam)
+                    dQt_c = dQg * eG + XP + dPd * Kh
+                    dGam = dKgW * Kg + Kh * (XA - YA - YP) + dQg * Qg + Qt * XP
+                else:
+                    dKg = be[:, None] * dBW + be[:, None] * (dAr @ Kn)
+                    dKn = dAr.T @ (be[:, None] * Kg) + dPr.T @ Qg
+                    dQg = dQg + dPr @ Kn
+                    dKh_c = dKg * eG + dKn * enG + dKd * np.exp(GC[None, :] - Gam)
+                    dGam = dKg * Kg - dKn * Kn + dQg * Qg - dKd * Kd
+                    dQt_c = dQg * eG
+                if not pairwise:
+                    dGC = dGC + (dKd * Kd).sum(0)
                 # Gam_r = sum_{s <= r} g_s and Gam_C = Gam_{L-1}: dg_s = sum_{r >= s} dGam_r + dGam_C
-                dgc = np.cumsum(dGam[::-1], axis=0)[::-1] + dGC[None, :]
+                if pairwise:
+                    # Kd_r = Kh_r e^{Gam_C - Gam_r} depends on g_s for s > r only: an exclusive
+                    # prefix sum, instead of a whole-chunk term minus the rows r >= s
+                    kdk = dKd * Kd
+                    dgc = np.cumsum(dGam[::-1], axis=0)[::-1] + dGC[None, :] + np.cumsum(kdk, axis=0) - kdk
+                else:
+                    dgc = np.cumsum(dGam[::-1], axis=0)[::-1] + dGC[None, :]
                 dqt[bi, c0:c1, h] = dQt_c
                 dkh[bi, c0:c1, h] = dKh_c
                 dv[bi, c0:c1, h] = dVc

@@ -185,3 +185,37 @@ def test_chunk_model_rejects_key_side_rounding():
     inp = KI.make_inputs(1, 8, 1, 1, seed=1, with_state=False)
     with pytest.raises(ValueError):
         CB.chunk_bwd_inputs(inp, torch.zeros(inp.v.shape), rounding={"Kn": "bf16"})
+
+
+def test_chunked_backward_pairwise_form_equals_split():
+    """The pairwise-decay form of the key products gives the split form's gradients."""
+    import kda_inputs as KI
+    from oracle import chunk_bwd_model as CB
+    inp = KI.make_inputs(1, 140, 1, 2, seed=51, with_state=True, seqlens=[70, 0, 1, 69])
+    g = torch.Generator().manual_seed(32)
+    do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
+    dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1
+    a = CB.chunk_bwd_inputs(inp, do, dht)
+    b = CB.chunk_bwd_inputs(inp, do, dht, form="pairwise")
+    for name in a:
+        assert _max_rel(b[name], a[name]) <= 1e-10, name
+
+
+def test_chunked_backward_pairwise_form_survives_strong_gates():
+    """A gate of about -22 nats per token (e^{A_log} = e^2, softplus(3)) takes a 64-token
+    chunk's decay past 1400 nats: the split form's e^{-Gam} overflows, the pairwise form
+    (every factor at most 1) still gives the reverse-pass oracle's gradients."""
+    import kda_inputs as KI
+    from oracle import chunk_bwd_model as CB
+    inp = KI.make_inputs(1, 100, 1, 2, seed=54, with_state=True, graw_mean=3.0, graw_std=0.5, A_log_value=2.0)
+    g = torch.Generator().manual_seed(33)
+    do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
+    dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1
+    ref = OB.bwd_recurrent_inputs(inp, do, dht)
+    got = CB.chunk_bwd_inputs(inp, do, dht, form="pairwise")
+    for name in ref:
+        assert torch.isfinite(got[name]).all(), name
+        assert _max_rel(got[name], ref[name]) <= 1e-9, (name, _max_rel(got[name], ref[name]))
+    with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
+        split = CB.chunk_bwd_inputs(inp, do, dht)
+    assert not all(bool(torch.isfinite(split[n]).all()) for n in split)
