@@ -44,15 +44,26 @@ which depends on g_s for s > r only, reaches dg through an exclusive prefix sum
 (the split form adds it to every token through Gam_C and takes it back from the
 tokens s <= r, two equal amounts that cancel when the gate is strong).
 
+``form="blocked"`` computes those key products as a kernel does: per pair of
+16-row sub-blocks, one product of the gradient block (diag(beta) dA or dP) with a
+decayed operand (Kh or Qt times a factor <= 1 against the block's reference point,
+as the forward builds A and P; diagonal blocks use the midpoint with exponents
+clamped at ``clamp``, exact while a channel decays by less than 2 clamp nats
+across a block), scaled afterwards by the other factor.  Its Gam terms multiply
+the products by the same (rounded) decayed operands that entered them, so that a
+pair (r, j) reaches row r and row j as one and the same product and the two
+cancel in dg's suffix sums as they do in exact arithmetic.
+
 ``rounding`` maps operand names to a number format the operand is rounded to
 where it enters a product (``"bf16"`` nearest-even, ``"tf32"`` nearest-even to
-10 fraction bits, ``"tf32_trunc"`` the low 13 bits dropped), so the tests can
-choose a tensor-core backward's operand formats: the state side S0, dS, W, Qg
-(in dOᵀQg), P, Kd, Delta, dDelta, dW, BV = diag(beta) V, T, dT, dA and dP.  The
-key-side decay products (Kg, Kn and diag(beta) Kg against dA and dP) are not
-offered: in the e^{+Gam} / e^{-Gam} split written here they cancel, so a kernel
-forms them against in-chunk reference points (as the forward does) and their
-rounding has to be studied in that form.
+10 fraction bits, ``"tf32_trunc"`` the low 13 bits dropped, ``"f32"``), so the
+tests can choose a tensor-core backward's operand formats: the state side S0,
+dS, W, Qg (in dOᵀQg), P, Kd, Delta, dDelta, dW, BV = diag(beta) V, T, dT, dA and
+dP, and in the blocked form the decayed keys and queries (Kdec, Qdec), whose
+products then accumulate in fp32.  The split and pairwise forms do not round the
+key products: in the split form they cancel (bf16 there costs rel-L2 0.3 to 11
+on dk and dgraw), and the pairwise form is the definition the blocked form
+factors.
 """
 from __future__ import annotations
 
@@ -63,7 +74,9 @@ import torch
 
 from .backward import EPS
 
-ROUNDABLE = ("S0", "dS", "W", "Qg", "P", "Kd", "Delta", "dDelta", "dW", "BV", "T", "dT", "dA", "dP")
+ROUNDABLE = ("S0", "dS", "W", "Qg", "P", "Kd", "Delta", "dDelta", "dW", "BV", "T", "dT", "dA", "dP",
+             "Kdec", "Qdec")
+SUB = 16   # sub-block rows of the blocked form (the forward's decay blocks)
 
 
 def _round(x: np.ndarray, fmt: str) -> np.ndarray:
@@ -75,23 +88,85 @@ def _round(x: np.ndarray, fmt: str) -> np.ndarray:
         u = (u + 0xFFF + ((u >> 13) & 1)) & 0xFFFFE000
     elif fmt == "tf32_trunc":
         u = u & 0xFFFFE000
+    elif fmt == "f32":
+        pass
     else:
         raise ValueError(fmt)
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def _block_factors(Gam: np.ndarray, clamp: float):
+    """Per (row block i, column block b <= i) of SUB rows: (rowf, colf) with
+    e^{Gam_r - Gam_j} = rowf[r] * colf[j] (per channel) for r in block i, j in block b,
+    j < r.  Below the diagonal the reference is Gam at the end of block i - 1 (both
+    factors <= 1); on it, the block's per-channel midpoint with both exponents
+    clamped at ``clamp`` (exact unless a channel decays by more than 2 clamp nats
+    across the block), as the forward builds A and P."""
+    L = Gam.shape[0]
+    nb = (L + SUB - 1) // SUB
+    out = {}
+    for i in range(nb):
+        r0, r1 = i * SUB, min(L, (i + 1) * SUB)
+        if i > 0:
+            m = Gam[r0 - 1]
+            rowf = np.exp(Gam[r0:r1] - m)
+            for bb in range(i):
+                out[(i, bb)] = (rowf, np.exp(m - Gam[bb * SUB:(bb + 1) * SUB]))
+        mid = 0.5 * (Gam[r0] + Gam[r1 - 1])
+        out[(i, i)] = (np.exp(np.minimum(Gam[r0:r1] - mid, clamp)), np.exp(np.minimum(mid - Gam[r0:r1], clamp)))
+    return out, nb
+
+
+def _key_products(M, Kh, Qt, Gam, clamp, rk, rq, acc=lambda x: x):
+    """For a strictly lower L x L matrix M (diag(beta) dA, or dP without its
+    diagonal) the four contractions of the key products, block pair by block pair
+    as a kernel forms them: one product of M's block with a decayed operand
+    (``rk`` / ``rq``: its rounding), scaled afterwards by the other factor.
+      XK[r] = sum_j M_rj Kh_j e^{Gam_r - Gam_j}     YK[j] = sum_r M_rj Kh_r e^{Gam_r - Gam_j}
+      YQ[j] = sum_r M_rj Qt_r e^{Gam_r - Gam_j}
+    (XK with the keys is also the query-side sum of P's gradient), each product's
+    accumulator passed through ``acc``; and the four Gam-side terms Kh_r XK_r,
+    Kh_j YK_j, Qt_r XK_r, Kh_j YQ_j formed from the rounded operands."""
+    L, K = Kh.shape
+    fac, nb = _block_factors(Gam, clamp)
+    XK, YK, YQ = np.zeros((L, K)), np.zeros((L, K)), np.zeros((L, K))
+    gXK, gYK, gXQ, gYQ = (np.zeros((L, K)) for _ in range(4))
+    strict16 = np.tril(np.ones((SUB, SUB)), -1)
+    for (i, bb), (rowf, colf) in fac.items():
+        r0, r1 = i * SUB, min(L, (i + 1) * SUB)
+        j0, j1 = bb * SUB, min(L, (bb + 1) * SUB)
+        Mb = M[r0:r1, j0:j1]
+        if i == bb:
+            Mb = Mb * strict16[:r1 - r0, :j1 - j0]
+        Hk = rk(Kh[j0:j1] * colf)          # the decayed operands as they enter the products
+        Fk = rk(Kh[r0:r1] * rowf)
+        Fq = rq(Qt[r0:r1] * rowf)
+        MH, MtF, MtQ = acc(Mb @ Hk), acc(Mb.T @ Fk), acc(Mb.T @ Fq)
+        XK[r0:r1] += rowf * MH
+        YK[j0:j1] += colf * MtF
+        YQ[j0:j1] += colf * MtQ
+        # the Gam terms multiply by the same rounded operands, so that each pair (r, j)
+        # enters row r and row j as the same product and the two cancel in dg's suffix sums
+        gXK[r0:r1] += Fk * MH
+        gYK[j0:j1] += Hk * MtF
+        gXQ[r0:r1] += Fq * MH
+        gYQ[j0:j1] += Hk * MtQ
+    return XK, YK, YQ, (gXK, gYK, gXQ, gYQ)
+
+
 def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=None, do=None, dht=None,
-              C: int = 64, rounding: Optional[Dict[str, str]] = None, form: str = "split") -> Dict[str, torch.Tensor]:
+              C: int = 64, rounding: Optional[Dict[str, str]] = None, form: str = "split",
+              clamp: float = 85.0) -> Dict[str, torch.Tensor]:
     """Gradients as ``backward.bwd`` returns them (fp64 tensors), computed with
     the chunked formulas above (operands rounded as ``rounding`` names; key
     products in the ``form`` "split" or "pairwise")."""
-    if form not in ("split", "pairwise"):
+    if form not in ("split", "pairwise", "blocked"):
         raise ValueError(form)
-    pairwise = form == "pairwise"
+    pairwise = form in ("pairwise", "blocked")
     rnd = dict(rounding or {})
-    bad = set(rnd) - set(ROUNDABLE)
+    bad = set(rnd) - set(ROUNDABLE if form == "blocked" else ROUNDABLE[:-2])
     if bad:
-        raise ValueError(f"not roundable here: {sorted(bad)}")
+        raise ValueError(f"not roundable in the {form} form: {sorted(bad)}")
     r = lambda name, x: _round(x, rnd[name]) if name in rnd else x  # noqa: E731
     f64 = lambda t: t.detach().to(torch.float64).numpy()  # noqa: E731
     qq, kk, vv, gg, bb, aa = (f64(t) for t in (q, k, v, graw, b, A_log))
@@ -173,17 +248,28 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
                 dAr, dPr = r("dA", dA), r("dP", dP)
                 if pairwise:
                     M = be[:, None] * dAr
-                    XA = np.einsum("rj,jc,rjc->rc", M, Kh, E)      # row side of A
-                    YA = np.einsum("rj,rc,rjc->jc", M, Kh, E)      # column side of A
                     # P's diagonal (decay e^0 = 1) has no Gam gradient: its terms enter dQt and dKh
                     # only, so the Gam terms never add and subtract O(1) amounts that cancel exactly
                     dPs, dPd = strict * dPr, np.diag(dPr)[:, None]
-                    XP = np.einsum("rj,jc,rjc->rc", dPs, Kh, E)    # row side of P (the query)
-                    YP = np.einsum("rj,rc,rjc->jc", dPs, Qt, E)    # column side of P (the key)
+                    if form == "blocked":
+                        rk = lambda x: r("Kdec", x)  # noqa: E731
+                        rq = lambda x: r("Qdec", x)  # noqa: E731
+                        acc = (lambda x: _round(x, "f32")) if rnd else (lambda x: x)  # noqa: E731
+                        XA, YA, _, gA = _key_products(M, Kh, Qt, Gam, clamp, rk, rq, acc)
+                        XP, _, YP, gP = _key_products(dPs, Kh, Qt, Gam, clamp, rk, rq, acc)
+                        gamKey = gA[0] - gA[1] + gP[2] - gP[3]
+                    else:
+                        XA = np.einsum("rj,jc,rjc->rc", M, Kh, E)      # row side of A
+                        YA = np.einsum("rj,rc,rjc->jc", M, Kh, E)      # column side of A
+                        XP = np.einsum("rj,jc,rjc->rc", dPs, Kh, E)    # row side of P (the query)
+                        YP = np.einsum("rj,rc,rjc->jc", dPs, Qt, E)    # column side of P (the key)
                     dKgW = be[:, None] * dBW
                     dKh_c = dKgW * eG + XA + YA + YP + dPd * Qt + dKd * np.exp(GC[None, :] - Gam)
                     dQt_c = dQg * eG + XP + dPd * Kh
-                    dGam = dKgW * Kg + Kh * (XA - YA - YP) + dQg * Qg + Qt * XP
+                    if form == "blocked":
+                        dGam = dKgW * Kg + gamKey + dQg * Qg
+                    else:
+                        dGam = dKgW * Kg + Kh * (XA - YA - YP) + dQg * Qg + Qt * XP
                 else:
                     dKg = be[:, None] * dBW + be[:, None] * (dAr @ Kn)
                     dKn = dAr.T @ (be[:, None] * Kg) + dPr.T @ Qg

@@ -148,13 +148,14 @@ def _rel_l2(x, ref):
 
 @pytest.mark.parametrize("case", ["mha", "gva"])
 def test_chunked_backward_operand_formats(case):
-    """Operand formats for a tensor-core chunked backward, chosen on the chunk algebra:
-    bf16 for S0, W, dW, BV, T, dT and dA with nearest-rounded tf32 for the seven
-    operands the gradients are most sensitive to (dS, Qg, P, Kd, Delta, dDelta, dP;
-    each alone in bf16 costs 1e-3 to 1.7e-3) keeps every gradient within rel-L2 6e-4
-    of the oracle (the GPU backward's bound is 1e-3); bf16 for all fourteen does not,
-    and tf32 by truncation (the low bits dropped, a bias that adds up) comes out at
-    about twice the nearest-rounded error."""
+    """Operand formats for a tensor-core chunked backward, chosen on the blocked form of
+    the chunk algebra (each product as a kernel forms it, operands rounded where they
+    enter it, accumulators in fp32): bf16 for S0, W, dW, BV, T, dT and dA with
+    nearest-rounded tf32 for the nine operands the gradients are most sensitive to (dS,
+    Qg, P, Kd, Delta, dDelta, dP and the decayed keys and queries) keeps every gradient
+    within rel-L2 6e-4 of the oracle (the GPU backward's bound is 1e-3); bf16 for all
+    sixteen does not, and tf32 by truncation (the low bits dropped, a bias that adds up)
+    comes out at about twice the nearest-rounded error."""
     import kda_inputs as KI
     from oracle import chunk_bwd_model as CB
     if case == "mha":
@@ -165,18 +166,44 @@ def test_chunked_backward_operand_formats(case):
     do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
     dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1
     ref = OB.bwd_recurrent_inputs(inp, do, dht)
-    hi = ("dS", "Qg", "P", "Kd", "Delta", "dDelta", "dP")
+    hi = ("dS", "Qg", "P", "Kd", "Delta", "dDelta", "dP", "Kdec", "Qdec")
     lo = ("S0", "W", "dW", "BV", "T", "dT", "dA")
 
     def worst(fmt_hi, fmt_lo):
         rounding = {**{n: fmt_lo for n in lo}, **{n: fmt_hi for n in hi}}
-        got = CB.chunk_bwd_inputs(inp, do, dht, rounding=rounding)
+        got = CB.chunk_bwd_inputs(inp, do, dht, rounding=rounding, form="blocked")
         return max(_rel_l2(got[n], ref[n]) for n in ref)
 
     mixed = worst("tf32", "bf16")
     assert mixed <= 6e-4, mixed
     assert worst("bf16", "bf16") >= 1.5e-3
     assert worst("tf32_trunc", "bf16") >= 1.6 * mixed
+
+
+def test_chunked_backward_blocked_form():
+    """The blocked form (key products per pair of 16-row sub-blocks with reference
+    points, as a kernel forms them) gives the pairwise form's gradients; at about 6 nats
+    of decay per token (diagonal blocks inside the fp32 exponent clamp) and, with the
+    clamp widened, at 22 nats per token it gives the reverse-pass oracle's (1e-9; 1e-8
+    at 22 nats, where the gate gradients are about 1e-6 of the terms summed into them)."""
+    import kda_inputs as KI
+    from oracle import chunk_bwd_model as CB
+    g = torch.Generator().manual_seed(34)
+    inp = KI.make_inputs(1, 140, 1, 2, seed=51, with_state=True, seqlens=[70, 0, 1, 69])
+    do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
+    dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1
+    a = CB.chunk_bwd_inputs(inp, do, dht, form="pairwise")
+    b = CB.chunk_bwd_inputs(inp, do, dht, form="blocked")
+    for name in a:
+        assert _max_rel(b[name], a[name]) <= 1e-12, name
+    for mean, alog, clamp in ((2.0, 1.0, 85.0), (3.0, 2.0, 400.0)):
+        inp = KI.make_inputs(1, 100, 1, 2, seed=55, with_state=True, graw_mean=mean, graw_std=0.5, A_log_value=alog)
+        do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
+        dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1
+        ref = OB.bwd_recurrent_inputs(inp, do, dht)
+        got = CB.chunk_bwd_inputs(inp, do, dht, form="blocked", clamp=clamp)
+        for name in ref:
+            assert _max_rel(got[name], ref[name]) <= (1e-9 if clamp < 100 else 1e-8), (mean, name)
 
 
 def test_chunk_model_rejects_key_side_rounding():
