@@ -1,8 +1,9 @@
 """Python binding of libkda (include/kda.h): argument marshalling only.
 
-Every function here takes torch tensors, checks dtype / device / layout,
-passes raw pointers and the current CUDA stream to the C ABI and raises on a
-non-zero return code.  All arithmetic runs in the CUDA kernels of libkda.so;
+Every function here takes torch tensors, checks dtype / device / layout (CUDA
+tensors and a given stream must be on the current device, where the library
+launches), passes raw pointers and the current CUDA stream to the C ABI and
+raises on a non-zero return code.  All arithmetic runs in the CUDA kernels of libkda.so;
 there is no other code path.  If the library is missing the first call raises
 ``KdaLibraryError``.
 """
@@ -108,6 +109,9 @@ def _ptr(t: Optional[torch.Tensor]):
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
+    elif stream.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream is on {stream.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}")
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -120,6 +124,11 @@ def _check(t: Optional[torch.Tensor], name: str, dtype, shape=None, optional=Fal
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if t.device.type != device:
         raise ValueError(f"{name} must be a {'CUDA' if device == 'cuda' else 'host'} tensor")
+    if device == "cuda" and t.device.index != torch.cuda.current_device():
+        # the library launches on the calling thread's current device
+        raise ValueError(f"{name} is on {t.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()} (select it with torch.cuda.set_device "
+                         f"or torch.cuda.device)")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
