@@ -24,12 +24,15 @@
  *
  * Conventions for every entry point
  * ---------------------------------
- *  - All tensor pointers are DEVICE pointers to contiguous row-major data,
- *    owned by the caller; the library keeps no pointer after a call returns.
- *    bf16 data is passed as its 16-bit pattern (kda_bf16_t).
+ *  - All tensor pointers are DEVICE pointers (kda_fwd_host's are host
+ *    pointers) to contiguous row-major data, owned by the caller; the library
+ *    keeps no pointer after a call returns.  bf16 data is passed as its 16-bit
+ *    pattern (kda_bf16_t).
+ *  - Kernels run on the calling thread's current CUDA device: the device
+ *    pointers and `stream` must belong to it.
  *  - q, k, v, graw, out and the states must be 16-byte aligned.
  *  - Calls are asynchronous and ordered on `stream`; no entry point except
- *    kda_get_status synchronises with the host.
+ *    kda_get_status and kda_kernel_times synchronises with the host.
  *  - The return value reports host-side validation and launch errors only.
  *    Faults detected on the device (malformed cu_seqlens, a bounded wait that
  *    timed out) are recorded in a per-device status word read by
