@@ -156,10 +156,16 @@ def _key_products(M, Kh, Qt, Gam, clamp, rk, rq, acc=lambda x: x):
 
 def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=None, do=None, dht=None,
               C: int = 64, rounding: Optional[Dict[str, str]] = None, form: str = "split",
-              clamp: float = 85.0) -> Dict[str, torch.Tensor]:
+              clamp: float = 85.0, return_intermediates: bool = False):
     """Gradients as ``backward.bwd`` returns them (fp64 tensors), computed with
     the chunked formulas above (operands rounded as ``rounding`` names; key
-    products in the ``form`` "split" or "pairwise")."""
+    products in the ``form`` "split", "pairwise" or "blocked").
+
+    With ``return_intermediates`` it returns ``(grads, inter)``, ``inter`` holding
+    per (sequence n, value head h, chunk start c0) the quantities a phased kernel
+    passes between its phases: ``"S0"`` the state entering the chunk, ``"dS_end"``
+    the gradient with respect to the state leaving it, ``"dDelta"`` the gradient
+    with respect to the chunk's rows Delta (fp64 NumPy arrays)."""
     if form not in ("split", "pairwise", "blocked"):
         raise ValueError(form)
     pairwise = form in ("pairwise", "blocked")
@@ -187,6 +193,7 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
     dqt, dkh = np.zeros((B, T, H_v, K)), np.zeros((B, T, H_v, K))
     dg, dbeta, dv = np.zeros((B, T, H_v, K)), np.zeros((B, T, H_v)), np.zeros(vv.shape)
     dh0 = np.zeros((len(segs), H_v, V, K))
+    inter = {"S0": {}, "dS_end": {}, "dDelta": {}}
     for n, (bi, t0, t1) in enumerate(segs):
         for h in range(H_v):
             hq = h // G
@@ -206,6 +213,8 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
                 Vc, be, gc = vv[bi, c0:c1, h], beta_all[bi, c0:c1, h], g_all[bi, c0:c1, h]
                 dO = dO_all[bi, c0:c1, h]
                 L = c1 - c0
+                inter["S0"][(n, h, c0)] = S0.copy()
+                inter["dS_end"][(n, h, c0)] = dS.copy()
                 Gam = np.cumsum(gc, axis=0)
                 GC = Gam[-1]
                 eG = np.exp(Gam)
@@ -287,6 +296,7 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
                     dgc = np.cumsum(dGam[::-1], axis=0)[::-1] + dGC[None, :] + np.cumsum(kdk, axis=0) - kdk
                 else:
                     dgc = np.cumsum(dGam[::-1], axis=0)[::-1] + dGC[None, :]
+                inter["dDelta"][(n, h, c0)] = dDelta.copy()
                 dqt[bi, c0:c1, h] = dQt_c
                 dkh[bi, c0:c1, h] = dKh_c
                 dv[bi, c0:c1, h] = dVc
@@ -304,7 +314,8 @@ def chunk_bwd(q, k, v, graw, b, A_log, scale, initial_state=None, cu_seqlens=Non
     dA_log = (dg * g_all).sum(axis=(0, 1, 3))
     db = dbeta * beta_all * (1.0 - beta_all)
     out = dict(dq=dq, dk=dk, dv=dv, dgraw=dgraw, db=db, dA_log=dA_log, dh0=dh0)
-    return {n_: torch.from_numpy(np.ascontiguousarray(x)) for n_, x in out.items()}
+    grads = {n_: torch.from_numpy(np.ascontiguousarray(x)) for n_, x in out.items()}
+    return (grads, inter) if return_intermediates else grads
 
 
 def chunk_bwd_inputs(inp, do, dht=None, **kw):

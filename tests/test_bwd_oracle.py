@@ -246,3 +246,37 @@ def test_chunked_backward_pairwise_form_survives_strong_gates():
     with np.errstate(over="ignore", invalid="ignore", divide="ignore"):
         split = CB.chunk_bwd_inputs(inp, do, dht)
     assert not all(bool(torch.isfinite(split[n]).all()) for n in split)
+
+
+def test_chunked_backward_intermediates():
+    """What a phased backward passes between its phases, pinned independently: the state
+    entering each chunk is the C oracle's final state of the prefix before it, and the
+    gradient with respect to the state leaving a chunk is the reverse-pass oracle's dh0
+    of the suffix problem after it (that state as its initial state, the same dO and dht)."""
+    import kda_inputs as KI
+    from oracle import chunk_bwd_model as CB
+    inp = KI.make_inputs(1, 150, 1, 2, seed=56, with_state=True)       # chunks at 0, 64, 128
+    g = torch.Generator().manual_seed(35)
+    do = torch.randn(inp.v.shape, generator=g).to(torch.bfloat16)
+    dht = torch.randn((inp.N, inp.H_v, 128, 128), generator=g) * 0.1
+    grads, inter = CB.chunk_bwd_inputs(inp, do, dht, form="pairwise", return_intermediates=True)
+    ref = OB.bwd_recurrent_inputs(inp, do, dht)
+    for name in ref:
+        assert _max_rel(grads[name], ref[name]) <= 1e-9, name
+    cut = lambda t, a, b: t[:, a:b]  # noqa: E731
+    for c0 in (64, 128):
+        _, fin = oracle.fwd(cut(inp.q, 0, c0), cut(inp.k, 0, c0), cut(inp.v, 0, c0), cut(inp.graw, 0, c0),
+                            cut(inp.b, 0, c0), inp.A_log, inp.scale, inp.initial_state)
+        for h in range(inp.H_v):
+            s0 = inter["S0"][(0, h, c0)]
+            assert np.abs(s0 - fin[0, h]).max() <= 1e-12 * np.abs(fin[0, h]).max(), (c0, h)
+    T = inp.q.shape[1]
+    for c0, c1 in ((0, 64), (64, 128)):
+        s_c1 = torch.from_numpy(np.stack([inter["S0"][(0, h, c1)] for h in range(inp.H_v)])[None])
+        suf = OB.bwd_recurrent(cut(inp.q, c1, T), cut(inp.k, c1, T), cut(inp.v, c1, T), cut(inp.graw, c1, T),
+                               cut(inp.b, c1, T), inp.A_log, inp.scale, s_c1, None, do=cut(do, c1, T), dht=dht)
+        for h in range(inp.H_v):
+            assert _max_rel(torch.from_numpy(inter["dS_end"][(0, h, c0)]), suf["dh0"][0, h]) <= 1e-9, (c0, h)
+    for h in range(inp.H_v):
+        assert np.array_equal(inter["dS_end"][(0, h, 128)], dht[0, h].double().numpy())
+        assert inter["dDelta"][(0, h, 128)].shape == (T - 128, 128)
