@@ -3,6 +3,7 @@
     python -m gated_delta_rule_40_gb300.profile_case --B 1 --T 8192 --H 32 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method la --B 1 --T 8192 --H 64 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method bwd --B 1 --T 2048 --H 8 --iters 3
+    python -m gated_delta_rule_40_gb300.profile_case --method bwd --B 2 --T 16384 --H 32 --iters 2 --kernel-times
     python -m gated_delta_rule_40_gb300.profile_case --method la_decode --B 256 --H 64 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method gdn --B 1 --T 8192 --H 32 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method decode_tokens --B 256 --T 4 --H 64 --iters 4
@@ -14,7 +15,8 @@ and scan_kernel; two for ``kda_la_fwd``: plan and la_fwd_kernel; three for ``kda
 plan, bwd_recur_kernel and bwd_prologue_kernel; one for ``kda_decode_tokens``, whose
 ``--T`` is the token count Tq of the step and whose state is fp32 unless
 ``--bf16-state``).  A profiler then selects launches by kernel name and index (e.g.
-``ncu -k regex:intra_kernel -s 2 -c 1``).
+``ncu -k regex:intra_kernel -s 2 -c 1``).  ``--kernel-times`` (kda and bwd) times the
+last iteration's kernels with the library's CUDA events instead and prints them.
 """
 import argparse
 import os
@@ -36,7 +38,18 @@ def main() -> None:
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--method", choices=["kda", "gdn", "la", "bwd", "la_decode", "decode_tokens"], default="kda")
     ap.add_argument("--bf16-state", action="store_true", help="decode_tokens: bf16 state")
+    ap.add_argument("--kernel-times", action="store_true",
+                    help="time the last iteration's kernels with the library's events and print them")
     a = ap.parse_args()
+    def timed(i):
+        if a.kernel_times:
+            kda.kda_set_kernel_timing(i == a.iters - 1)
+
+    def report():
+        if a.kernel_times:
+            for name, ms in kda.kda_kernel_times():
+                print(f"  {name}: {ms:.4f} ms")
+            kda.kda_set_kernel_timing(False)
     if a.method == "decode_tokens":
         x = kda_inputs.make_inputs(a.B, a.T, a.H, a.H, seed=a.seed, with_state=True)
         q, k, v, gr, b, A = (t.cuda() for t in (x.q, x.k, x.v, x.graw, x.b, x.A_log))
@@ -79,20 +92,24 @@ def main() -> None:
         g = torch.Generator().manual_seed(a.seed + 1)
         dout = torch.randn(x.v.shape, generator=g).to(torch.bfloat16).cuda()
         q, k, v, gr, b, A, s0 = (t.cuda() for t in (x.q, x.k, x.v, x.graw, x.b, x.A_log, x.initial_state))
-        for _ in range(a.iters):
+        for i in range(a.iters):
+            timed(i)
             grads = kda.kda_bwd(q, k, v, gr, b, A, x.scale, dout, initial_state=s0)
         torch.cuda.synchronize()
         print(f"kda_bwd B={a.B} T={a.T} H={a.H} x{a.iters}: |dq| {float(grads['dq'].abs().mean()):.6f} "
               f"|dh0| {float(grads['dh0'].abs().mean()):.6f}")
+        report()
         return
     dev = lambda t: t.cuda() if t is not None else None  # noqa: E731
     q, k, v, g, b, A, s0 = map(dev, (x.q, x.k, x.v, x.graw, x.b, x.A_log, x.initial_state))
     ws = torch.empty(kda.kda_fwd_workspace_size(a.B, a.B, a.T, a.H, a.H), dtype=torch.uint8, device="cuda")
-    for _ in range(a.iters):
+    for i in range(a.iters):
+        timed(i)
         out, fin = kda.kda_fwd(q, k, v, g, b, A, x.scale, initial_state=s0, workspace=ws)
     torch.cuda.synchronize()
     print(f"kda_fwd B={a.B} T={a.T} H={a.H} x{a.iters}: |out| {float(out.float().abs().mean()):.6f} "
           f"|S| {float(fin.abs().mean()):.6f}")
+    report()
 
 
 if __name__ == "__main__":
