@@ -280,3 +280,26 @@ def test_chunked_backward_intermediates():
     for h in range(inp.H_v):
         assert np.array_equal(inter["dS_end"][(0, h, 128)], dht[0, h].double().numpy())
         assert inter["dDelta"][(0, h, 128)].shape == (T - 128, 128)
+
+
+def test_operand_rounding_helper():
+    """The model's roundings: bf16 equals torch's nearest-even conversion; tf32 keeps 10
+    fraction bits, nearest with ties to even, or truncated."""
+    from oracle import chunk_bwd_model as CB
+    x = torch.randn(4096, generator=torch.Generator().manual_seed(7), dtype=torch.float64) * 10.0
+    got = CB._round(x.numpy(), "bf16")
+    want = x.to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(got, want)
+    u = 2.0 ** -10                       # one tf32 unit in the last place at 1.0
+    cases = {1.0 + u / 2: 1.0,           # halfway, even neighbour below
+             1.0 + 3 * u / 2: 1.0 + 2 * u,   # halfway, even neighbour above
+             1.0 + u / 2 + u / 8: 1.0 + u,   # above halfway
+             1.0 + u / 2 - u / 8: 1.0,       # below halfway
+             -(1.0 + 3 * u / 4): -(1.0 + u)}
+    for v, r in cases.items():
+        assert CB._round(np.array([v]), "tf32")[0] == r, v
+    assert CB._round(np.array([1.0 + 3 * u / 4]), "tf32_trunc")[0] == 1.0
+    assert CB._round(np.array([-(1.0 + 3 * u / 4)]), "tf32_trunc")[0] == -1.0
+    assert CB._round(np.array([1.0 + u]), "tf32_trunc")[0] == 1.0 + u
+    with pytest.raises(ValueError):
+        CB._round(np.array([1.0]), "fp8")
