@@ -197,6 +197,13 @@ def cpu_baseline(inp: KI.KdaInputs, target_s: float = 12.0):
                       f"of the timed workload ({smp.token_heads()} token*heads), fp64 C oracle"}
 
 
+def bench_config(world: int) -> dict:
+    """The timed workload; both arms print the same object."""
+    return {"workload": WORKLOAD, "B": 2, "T": 16384, "H_qk": 32, "H_v": 32, "K": 128, "V": 128, "chunk": 64,
+            "seed": 0, "l2": "inputs larger than L2 (1.4 GB read per step), no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args, rank, world):
     """--impl reference: the fp64 oracle on the host cores, each step a bounded
     sample of the dense workload."""
@@ -224,7 +231,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": 2, "T": 16384, "H_qk": 32, "H_v": 32, "sample_tokens": tokens},
+            "config": bench_config(world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -232,6 +239,7 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- GPU arm
 def time_events(fn, steps, stream):
+    """Mean device time of ``steps`` back-to-back calls (one event pair around all)."""
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -242,6 +250,183 @@ def time_events(fn, steps, stream):
     return start.elapsed_time(end) / steps
 
 
+class L2Flush:
+    """Writes a buffer of twice the L2 size on the stream: whatever a previous call
+    left in L2 is evicted before the next timed call."""
+
+    def __init__(self, dev):
+        l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (128 << 20)
+        self.bytes = max(2 * int(l2), 256 << 20)
+        self.buf = torch.empty(self.bytes // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_flushed(fn, reps, stream, flush):
+    """Median / p10 / p90 device time of ``reps`` calls, each timed by its own event pair
+    on the launching stream after an L2 flush outside the timed pair."""
+    evs = []
+    for _ in range(reps):
+        flush()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        evs.append((s, e))
+    stream.synchronize()
+    t = sorted(s.elapsed_time(e) for s, e in evs)
+    pick = lambda f: t[min(len(t) - 1, int(round(f * (len(t) - 1))))]
+    return {"ms": statistics.median(t), "p10_ms": pick(0.1), "p90_ms": pick(0.9), "reps": reps}
+
+
+def fwd_alg(inp_B, inp_T, H_qk, H_v, nseq, ntok=None):
+    """Algorithmic bytes and flops of one forward call (K = V = 128, chunk 64); q and k are
+    counted once per q/k head (shared by the value heads of a group)."""
+    ntok = inp_B * inp_T if ntok is None else ntok
+    units = ntok * H_v
+    nbytes = (ntok * H_qk * 2 * 256 + ntok * H_v * (2 * 256 + 2 + 256) + nseq * H_v * STATE_BYTES_PER_SEQ_HEAD)
+    return units, nbytes, units * FLOPS_PER_TOKEN_HEAD
+
+
+def rate_fields(t, units, nbytes, flops, hbm_peak, tc_peak):
+    ms = t["ms"]
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    d = dict(t)
+    d.update({"token_heads_per_s": units / (ms * 1e-3), "TFLOP/s": flops / (ms * 1e-3) / 1e12,
+              "tensor_frac": flops / (ms * 1e-3) / 1e12 / tc_peak, "algorithmic_bytes": nbytes, "GB/s": gbs,
+              "hbm_frac": gbs / hbm_peak})
+    if gbs > hbm_peak:
+        d["note"] = "above the measured copy bandwidth: some inputs were still cache-resident"
+    return d
+
+
+def bench_configs(kda, d, inp, stream, flush, hbm_peak, tc_peak):
+    """Every forward workload of the method's benchmark pages, timed one call at a time
+    (median of flushed repetitions): the tiny case, the dense sweep over T and B (the cuLA
+    page's KDA fixed-length table), the skewed varlen batch (its varlen table) and the
+    grouped-value-head batch through both forward entry points (the FlashQLA table)."""
+    res = {}
+
+    def run(name, dd, scale, B, T, H_qk, H_v, nseq, cu=None, fn=None, reps=15, ntok=None):
+        out = torch.empty((dd["v"].shape[0], dd["v"].shape[1], H_v, 128), dtype=torch.bfloat16, device=dd["v"].device)
+        fin = None if dd.get("initial_state") is None else torch.empty_like(dd["initial_state"])
+        call = fn or kda.kda_fwd
+
+        def step():
+            call(dd["q"], dd["k"], dd["v"], dd["graw"], dd["b"], dd["A_log"], scale,
+                 initial_state=dd.get("initial_state"), cu_seqlens=cu, out=out, final_state=fin, stream=stream)
+
+        for _ in range(3):
+            step()
+        t = time_flushed(step, reps, stream, flush)
+        units, nbytes, flops = fwd_alg(B, T, H_qk, H_v, nseq, ntok)
+        res[name] = {"B": B, "T": T, "N": nseq, "H_qk": H_qk, "H_v": H_v,
+                     **rate_fields(t, units, nbytes, flops, hbm_peak, tc_peak)}
+
+    tiny = KI.workload("tiny")
+    td = {n: getattr(tiny, n).to(d["q"].device) for n in ("q", "k", "v", "graw", "b", "A_log")}
+    td["initial_state"] = None
+    run("tiny_B1_T256_H2", td, tiny.scale, 1, 256, 2, 2, 1, reps=30)
+    for B in (1, 2):
+        for T in (512, 1024, 4096, 8192, 16384):
+            sub = {n: d[n][:B, :T].contiguous() for n in ("q", "k", "v", "graw", "b")}
+            sub["A_log"] = d["A_log"]
+            sub["initial_state"] = d["initial_state"][:B].contiguous()
+            run(f"dense_B{B}_T{T}", sub, inp.scale, B, T, inp.H_qk, inp.H_v, B)
+            del sub
+    vl = KI.workload("varlen")
+    vd = {n: getattr(vl, n).to(d["q"].device) for n in ("q", "k", "v", "graw", "b", "A_log", "initial_state")}
+    run("varlen_20seqs_T16384", vd, vl.scale, 1, vl.T, vl.H_qk, vl.H_v, vl.N, cu=vl.cu_seqlens.to(d["q"].device))
+    res["varlen_20seqs_T16384"]["seqlens"] = vl.seqlens()
+    del vd
+    g = KI.workload("gva")
+    gd = {n: getattr(g, n).to(d["q"].device) for n in ("q", "k", "v", "graw", "b", "A_log", "initial_state")}
+    gcu = g.cu_seqlens.to(d["q"].device)
+    run("gva_28672+4096_general", gd, g.scale, 1, g.T, g.H_qk, g.H_v, g.N, cu=gcu)
+    gd["graw"] = g.graw[..., 0].contiguous().to(d["q"].device)
+    run("gva_28672+4096_scalar_gate", gd, g.scale, 1, g.T, g.H_qk, g.H_v, g.N, cu=gcu, fn=kda.kda_fwd_scalar_gate)
+    # the scalar-gate call reads one gate value per (token, value head): 254 B less per token*head
+    sg = res["gva_28672+4096_scalar_gate"]
+    ntok = g.T
+    sg_bytes = sg["algorithmic_bytes"] - ntok * g.H_v * 254
+    sg.update({"algorithmic_bytes": sg_bytes, "GB/s": sg_bytes / (sg["ms"] * 1e-3) / 1e9,
+               "hbm_frac": sg_bytes / (sg["ms"] * 1e-3) / 1e9 / hbm_peak})
+    del gd
+    return res
+
+
+def bench_decode(kda, dev, stream, flush, hbm_peak, rank):
+    """Single-token decode at B in {1, 4, 16, 64, 256}, H = 64 (the cuLA page's decode batch
+    column), the state read and written once in place; each repetition after an L2 flush."""
+    res = {}
+    for B in (1, 4, 16, 64, 256):
+        dec = KI.decode_inputs(B=B, H=64, seed=rank)
+        dd = {n: getattr(dec, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log", "state")}
+        dout = torch.empty((B, 64, 128), dtype=torch.bfloat16, device=dev)
+
+        def dec_step():
+            kda.kda_decode_step(dd["q"], dd["k"], dd["v"], dd["graw"], dd["b"], dd["A_log"], dec.scale, dd["state"],
+                                out=dout, stream=stream)
+
+        for _ in range(5):
+            dec_step()
+        t = time_flushed(dec_step, 30, stream, flush)
+        nbytes = B * 64 * (2 * 128 * 128 * 4 + 5 * 256 + 2)
+        gbs = nbytes / (t["ms"] * 1e-3) / 1e9
+        r = {"B": B, "H": 64, **t, "algorithmic_bytes": nbytes, "GB/s": gbs, "hbm_peak": hbm_peak,
+             "frac": gbs / hbm_peak}
+        if B <= 16:
+            r["note"] = "state of a few MB: launch-latency bound"
+        if gbs > hbm_peak:
+            r["note"] = "above the measured copy bandwidth"
+        res[f"B{B}"] = r
+        del dd, dout
+    return res
+
+
+def bench_link(dev, stream, nbytes_in, nbytes_out):
+    """Host-link rates of this machine, measured the way the end-to-end call moves data: pinned
+    host memory to device, device to pinned host memory, and both at once on two streams."""
+    hi = torch.empty(nbytes_in, dtype=torch.uint8).pin_memory()
+    di = torch.empty(nbytes_in, dtype=torch.uint8, device=dev)
+    ho = torch.empty(nbytes_out, dtype=torch.uint8).pin_memory()
+    do = torch.empty(nbytes_out, dtype=torch.uint8, device=dev)
+    other = torch.cuda.Stream(dev)
+
+    def one(fn, s):
+        fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    with torch.cuda.stream(stream):
+        h2d_ms = one(lambda: di.copy_(hi, non_blocking=True), stream)
+        d2h_ms = one(lambda: ho.copy_(do, non_blocking=True), stream)
+
+    def both():
+        with torch.cuda.stream(stream):
+            di.copy_(hi, non_blocking=True)
+        with torch.cuda.stream(other):
+            ho.copy_(do, non_blocking=True)
+        other.synchronize()
+        stream.synchronize()
+
+    both()
+    t0 = time.perf_counter()
+    both()
+    both_ms = (time.perf_counter() - t0) * 1e3
+    return {"h2d_GBps": nbytes_in / (h2d_ms * 1e-3) / 1e9, "d2h_GBps": nbytes_out / (d2h_ms * 1e-3) / 1e9,
+            "h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "concurrent_ms": both_ms,
+            "note": "the e2e step cannot be shorter than the input copy alone (h2d_ms)"}
+
+
 def run_gpu(args, rank, world, local):
     from gated_delta_rule_40_gb300 import kda
     kda.load()
@@ -249,7 +434,8 @@ def run_gpu(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
     hbm_peak = peak_value(peaks, "hbm_gbs", "hbm_GBps", "hbm") or FALLBACK_PEAKS["hbm_gbs"]
-    tc_peak = peak_value(peaks, "bf16_tflops_sustained", "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops_sustained"]
+    # every forward call here lasts milliseconds: the burst tensor peak is its ceiling
+    tc_peak = peak_value(peaks, "bf16_tflops", "bf16_tflops_sustained") or FALLBACK_PEAKS["bf16_tflops"]
 
     inp = KI.workload("dense", seed=rank)
     d = {n: getattr(inp, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log", "initial_state")}
@@ -320,53 +506,13 @@ def run_gpu(args, rank, world, local):
     e2e_steps = max(3, min(args.steps, 10))
     barrier(world)
     e2e_ms = max_over_ranks(time_events(e2e_step, e2e_steps, stream), world)
+    link = bench_link(dev, stream, h2d, d2h)
+    del pin, host_out, host_fin
 
-    # ---- scalar gate (one gate value per token and value head): the grouped-value-head
-    # workload (28672 + 4096 tokens, H_qk=16, H_v=64) through kda_fwd_scalar_gate, and the
-    # general kernel on the same inputs with the gate broadcast along K
-    sg = KI.workload("gva")
-    sd = {n: getattr(sg, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log", "initial_state", "cu_seqlens")}
-    sg_g = sg.graw[..., 0].contiguous().to(dev)
-    sg_out = torch.empty_like(sd["v"])
-    sg_fin = torch.empty_like(sd["initial_state"])
-
-    def sg_step():
-        kda.kda_fwd_scalar_gate(sd["q"], sd["k"], sd["v"], sg_g, sd["b"], sd["A_log"], sg.scale,
-                                initial_state=sd["initial_state"], cu_seqlens=sd["cu_seqlens"], out=sg_out,
-                                final_state=sg_fin, stream=stream)
-
-    def sg_general_step():
-        kda.kda_fwd(sd["q"], sd["k"], sd["v"], sd["graw"], sd["b"], sd["A_log"], sg.scale,
-                    initial_state=sd["initial_state"], cu_seqlens=sd["cu_seqlens"], out=sg_out, final_state=sg_fin,
-                    stream=stream)
-
-    for _ in range(3):
-        sg_step()
-        sg_general_step()
-    torch.cuda.synchronize()
-    sg_ms = time_events(sg_step, 10, stream)
-    sg_gen_ms = time_events(sg_general_step, 10, stream)
-    sg_units = sg.token_heads()
-    ntok = sg.q.shape[0] * sg.q.shape[1]
-    sg_bytes = (ntok * sg.H_qk * 2 * 256 + ntok * sg.H_v * (256 + 2 + 2 + 256)
-                + sg.N * sg.H_v * STATE_BYTES_PER_SEQ_HEAD)
-    del sd, sg_g, sg_out, sg_fin
-
-    # ---- decode (B=256, H=64): state GB/s against HBM
-    dec = KI.decode_inputs(B=256, H=64, seed=rank)
-    dd = {n: getattr(dec, n).to(dev) for n in ("q", "k", "v", "graw", "b", "A_log", "state")}
-    dout = torch.empty((256, 64, 128), dtype=torch.bfloat16, device=dev)
-
-    def dec_step():
-        kda.kda_decode_step(dd["q"], dd["k"], dd["v"], dd["graw"], dd["b"], dd["A_log"], dec.scale, dd["state"],
-                            out=dout, stream=stream)
-
-    for _ in range(5):
-        dec_step()
-    torch.cuda.synchronize()
-    dec_ms = time_events(dec_step, 50, stream)
-    dec_bytes = 256 * 64 * (2 * 128 * 128 * 4 + 5 * 256 + 2)
-    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    # ---- every workload of the benchmark pages, one call at a time after an L2 flush
+    flush = L2Flush(dev)
+    configs = bench_configs(kda, d, inp, stream, flush, hbm_peak, tc_peak)
+    decode = bench_decode(kda, dev, stream, flush, hbm_peak, rank)
 
     # ---- multi-token decode (kda_decode_tokens): Tq = 1 and 4 tokens per pass, fp32 and bf16 state
     multi = {}
@@ -383,11 +529,11 @@ def run_gpu(args, rank, world, local):
 
             for _ in range(3):
                 mstep()
-            torch.cuda.synchronize()
-            mms = time_events(mstep, 30, stream)
+            t = time_flushed(mstep, 20, stream, flush)
             mbytes = 256 * 64 * (2 * 128 * 128 * sbytes + tq * (5 * 256 + 2))
-            multi[f"T{tq}_{sname}_state"] = {"ms": mms, "tokens_per_s": 256 * tq / (mms * 1e-3),
-                                             "GB/s": mbytes / (mms * 1e-3) / 1e9}
+            multi[f"T{tq}_{sname}_state"] = {**t, "tokens_per_s": 256 * tq / (t["ms"] * 1e-3),
+                                             "GB/s": mbytes / (t["ms"] * 1e-3) / 1e9,
+                                             "frac": mbytes / (t["ms"] * 1e-3) / 1e9 / hbm_peak}
         del md, mst, mout
 
     # ---- lightning attention (fixed per-head decay): forward on the dense and varlen workloads
@@ -406,14 +552,13 @@ def run_gpu(args, rank, world, local):
 
         for _ in range(3):
             la_step()
-        torch.cuda.synchronize()
-        la_ms = time_events(la_step, 10, stream)
+        t = time_flushed(la_step, 10, stream, flush)
         ntok = la.B * la.T
         la_bytes = ntok * (2 * la.H_qk + 2 * la.H_v) * 256 + la.N * la.H_v * STATE_BYTES_PER_SEQ_HEAD
-        lightning[wname] = {"B": la.B, "T": la.T, "N": la.N, "H": la.H_v, "ms": la_ms,
-                            "value": la.token_heads() / (la_ms * 1e-3), "unit": UNIT,
-                            "algorithmic_bytes": la_bytes, "GB/s": la_bytes / (la_ms * 1e-3) / 1e9,
-                            "hbm_peak": hbm_peak, "frac": la_bytes / (la_ms * 1e-3) / 1e9 / hbm_peak}
+        lightning[wname] = {"B": la.B, "T": la.T, "N": la.N, "H": la.H_v, **t,
+                            "value": la.token_heads() / (t["ms"] * 1e-3), "unit": UNIT,
+                            "algorithmic_bytes": la_bytes, "GB/s": la_bytes / (t["ms"] * 1e-3) / 1e9,
+                            "hbm_peak": hbm_peak, "frac": la_bytes / (t["ms"] * 1e-3) / 1e9 / hbm_peak}
         del ld, lout, lfin
     lad = KI.la_decode_inputs(B=256, H=64, seed=rank)
     ldd = {n: getattr(lad, n).to(dev) for n in ("q", "k", "v", "slope", "state")}
@@ -425,18 +570,17 @@ def run_gpu(args, rank, world, local):
 
     for _ in range(5):
         la_dec_step()
-    torch.cuda.synchronize()
-    la_dec_ms = time_events(la_dec_step, 50, stream)
+    t = time_flushed(la_dec_step, 30, stream, flush)
     la_dec_bytes = 256 * 64 * (2 * 128 * 128 * 4 + 3 * 256)
-    lightning["la_decode"] = {"B": 256, "H": 64, "ms": la_dec_ms, "GB/s": la_dec_bytes / (la_dec_ms * 1e-3) / 1e9,
-                              "hbm_peak": hbm_peak, "frac": la_dec_bytes / (la_dec_ms * 1e-3) / 1e9 / hbm_peak}
+    lightning["la_decode"] = {"B": 256, "H": 64, **t, "GB/s": la_dec_bytes / (t["ms"] * 1e-3) / 1e9,
+                              "hbm_peak": hbm_peak, "frac": la_dec_bytes / (t["ms"] * 1e-3) / 1e9 / hbm_peak}
     del ldd, ldout
     status = kda.kda_get_status()
     if status != 0:
         raise RuntimeError(f"device status after the side measurements: {kda.status_string(status)}")
 
     # ---- backward of the forward (kda_bwd) on the dense workload: all input gradients from dL/dout
-    # and dL/dfinal_state; the token recurrence on CUDA cores, so its roofline is the fp32 FMA rate
+    # and dL/dfinal_state
     gd = torch.randn(out.shape, generator=torch.Generator().manual_seed(rank), dtype=torch.float32)
     gout = gd.to(torch.bfloat16).to(dev)
     ght = (torch.randn(fin.shape, generator=torch.Generator().manual_seed(rank + 1)) * 0.1).to(dev)
@@ -456,7 +600,7 @@ def run_gpu(args, rank, world, local):
     kda.kda_set_kernel_timing(False)
     bwd_flops = units * BWD_FLOPS_PER_TOKEN_HEAD
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = sm_count * 128 * 2 * (clk.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    alu_peak = sm_count * 128 * 2 * ((clk or {}).get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
     backward = {"workload": WORKLOAD, "ms": bwd_ms, "value": units / (bwd_ms * 1e-3), "unit": UNIT,
                 "roofline": {"bound": "alu", "achieved": bwd_flops / (bwd_ms * 1e-3) / 1e12,
                              "peak": alu_peak, "unit": "TFLOP/s",
@@ -479,10 +623,7 @@ def run_gpu(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": inp.B, "T": inp.T, "H_qk": inp.H_qk, "H_v": inp.H_v, "K": 128,
-                   "V": 128, "chunk": 64, "seed": 0,
-                   "l2": "inputs larger than L2 (1.4 GB read per step), no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": bench_config(world),
         "roofline": {"bound": "hbm", "kernel": dom,
                      "achieved": alg_bytes / (dom_ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                      "frac": alg_bytes / (dom_ms * 1e-3) / 1e9 / hbm_peak, "traffic": recorded_traffic(dom),
@@ -494,17 +635,14 @@ def run_gpu(args, rank, world, local):
                           "frac": gbs / hbm_peak, "kernel": "whole kda_fwd step"},
         "kernels": {n: {"ms": t, "share": t / ksum} for n, t in kernels.items()},
         "tensor": {"achieved_tflops": tflops, "peak_tflops": tc_peak, "frac": tflops / tc_peak,
-                   "flops_per_step": alg_flops, "peak_source": peak_src},
+                   "flops_per_step": alg_flops, "peak_source": peak_src + " (burst)"},
         "e2e": {"value": world * units / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "scalar_gate": {"workload": "grouped value heads, 28672+4096 tokens, H_qk=16 H_v=64, scalar gate",
-                        "value": sg_units / (sg_ms * 1e-3), "unit": UNIT, "ms": sg_ms,
-                        "general_path_ms": sg_gen_ms, "algorithmic_bytes": sg_bytes,
-                        "GB/s": sg_bytes / (sg_ms * 1e-3) / 1e9, "hbm_peak": hbm_peak,
-                        "frac": sg_bytes / (sg_ms * 1e-3) / 1e9 / hbm_peak},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "link": link},
+        "configs": configs,
+        "decode": {"workload": "H=64 K=V=128 fp32 state in place, L2 flushed before each repetition",
+                   "ms": decode["B256"]["ms"], "GB/s": decode["B256"]["GB/s"], "hbm_peak": hbm_peak,
+                   "frac": decode["B256"]["frac"], "batch": decode},
         "decode_tokens": {"workload": "B=256 H=64 K=V=128, Tq tokens per pass, state in place", **multi},
-        "decode": {"workload": "B=256 H=64 K=V=128 fp32 state in place", "ms": dec_ms, "GB/s": dec_gbs,
-                   "hbm_peak": hbm_peak, "frac": dec_gbs / hbm_peak},
         "backward": backward,
         "lightning": {"method": "linear attention with a fixed per-head decay (lightning attention)",
                       "slopes": "2^(-8 (h+1) / H)", **lightning},

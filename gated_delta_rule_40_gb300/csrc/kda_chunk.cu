@@ -64,7 +64,7 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
             tok = cu ? cu[i] : i * T;
             len = cu ? cu[i + 1] - cu[i] : T;
         }
-        const int nc = (len + CH - 1) / CH;
+        const int nc = (int)(((long long)len + CH - 1) / CH);
         s_scan[tid] = nc;
         __syncthreads();
         for (int off = 1; off < PLAN_THREADS; off <<= 1) {
@@ -1662,7 +1662,7 @@ cudaError_t launch_plan(const int32_t *cu, int N, int B, int T, SeqDesc *seqs, C
 
 long long max_chunks_for(int N, int B, int T, bool varlen) {
     if (varlen) return (long long)T / CH + (long long)N + 1;
-    return (long long)B * ((T + CH - 1) / CH);
+    return (long long)B * (((long long)T + CH - 1) / CH);
 }
 
 size_t fwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, FwdWorkspace *ws, char *base) {

@@ -132,9 +132,10 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
     char *base = nullptr;
     if (cudaMallocAsync((void **)&base, off, stream) != cudaSuccess) return KDA_ERR_CUDA;
     std::vector<cudaEvent_t> ev_in(np), ev_out(np);
-    cudaEvent_t ev_start, ev_end;
+    cudaEvent_t ev_start, ev_end, ev_h2d;
     cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
     cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming);
+    cudaEventCreateWithFlags(&ev_h2d, cudaEventDisableTiming);
     for (int p = 0; p < np; ++p) {
         cudaEventCreateWithFlags(&ev_in[p], cudaEventDisableTiming);
         cudaEventCreateWithFlags(&ev_out[p], cudaEventDisableTiming);
@@ -165,6 +166,8 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
         }
         ok(cudaEventRecord(ev_in[p], h2d));
     }
+    // every input copy queued so far, whether or not all of them could be queued
+    const cudaError_t eh = cudaEventRecord(ev_h2d, h2d);
     // kernels, piece by piece on the caller's stream; each piece's sequences start from, and
     // write back, their rows of the device state array
     for (int p = 0; p < np && e == cudaSuccess; ++p) {
@@ -186,12 +189,19 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
         const size_t t0 = pieces[p].t0, nt = (size_t)(pieces[p].t1 - pieces[p].t0);
         if (nt > 0) ok(cudaMemcpyAsync((char *)out + t0 * v_row, dp(o_out) + t0 * v_row, nt * v_row, D2H, d2h));
     }
-    if (final_state) ok(cudaMemcpyAsync(final_state, dp(o_st), (size_t)nseq * st_row, D2H, d2h));
-    ok(cudaEventRecord(ev_end, d2h));
-    ok(cudaStreamWaitEvent(stream, ev_end, 0));
-    const cudaError_t ef = cudaFreeAsync(base, stream);
+    if (final_state && e == cudaSuccess)
+        ok(cudaMemcpyAsync(final_state, dp(o_st), (size_t)nseq * st_row, D2H, d2h));
+    // the device buffer is released on the caller's stream only after every copy queued on
+    // either copy stream is done with it, also when a launch or a copy failed midway
+    const cudaError_t ee = cudaEventRecord(ev_end, d2h);
+    ok(ee);
+    ok(eh);
+    if (eh == cudaSuccess) ok(cudaStreamWaitEvent(stream, ev_h2d, 0));
+    if (ee == cudaSuccess) ok(cudaStreamWaitEvent(stream, ev_end, 0));
+    const cudaError_t ef = (eh == cudaSuccess && ee == cudaSuccess) ? cudaFreeAsync(base, stream) : cudaFree(base);
     cudaEventDestroy(ev_start);
     cudaEventDestroy(ev_end);
+    cudaEventDestroy(ev_h2d);
     for (int p = 0; p < np; ++p) {
         cudaEventDestroy(ev_in[p]);
         cudaEventDestroy(ev_out[p]);

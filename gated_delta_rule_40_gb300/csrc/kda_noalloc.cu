@@ -2,10 +2,10 @@
 // statically allocated device array instead of memory from cudaMalloc.
 //
 // Some callers cannot allocate device memory at the point where they run the
-// forward: code inside a CUDA-graph capture region or a custom allocator that
-// forbids out-of-band allocations, real-time serving loops that must not
-// enter the driver's allocator, and embedding hosts that own all device memory
-// and hand the library only tensors.  For them this entry point uses a
+// forward: a framework whose allocator owns all device memory and forbids
+// out-of-band allocations, real-time serving loops that must not enter the
+// driver's allocator, and embedding hosts that own all device memory and hand
+// the library only tensors.  For them this entry point uses a
 // file-scope __device__ array of KDA_NOALLOC_WS_BYTES (64 MiB), which every GPU
 // that loads the library holds until the process exits.
 #include <cstdint>

@@ -204,11 +204,12 @@ int kda_get_status(cudaStream_t stream);
 
 /*
  * kda_fwd without any device allocation, for callers that cannot allocate
- * device memory where they run the forward (inside a stream-capture region or
- * under an allocator that forbids allocations outside its own pool, in
- * latency-critical serving loops that must not enter the driver allocator, or
- * in hosts that own all device memory).  The paper has no counterpart; this
- * is a deployment variant of kda_fwd with identical arguments and results.
+ * device memory where they run the forward: a framework whose allocator owns
+ * all device memory and forbids allocations outside its own pool, a
+ * latency-critical serving loop that must not enter the driver's allocator,
+ * or an embedding host that hands the library only its own tensors.  The
+ * paper has no counterpart; this is a deployment variant of kda_fwd with
+ * identical arguments and bit-identical results (it runs the same kernels).
  *
  * The workspace is a file-scope __device__ array of KDA_NOALLOC_WS_BYTES
  * (64 MiB) that every GPU which loads the library holds until the process

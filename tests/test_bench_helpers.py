@@ -8,10 +8,15 @@ import os
 import bench
 
 
-def test_recorded_traffic_matches_current_source():
+def test_recorded_traffic_follows_the_current_source():
+    import hashlib
     rec = json.load(open(os.path.join(bench.ROOT, "profiles", "roofline_traffic.json")))
+    src = open(os.path.join(bench.ROOT, rec["source"]), "rb").read()
     t = bench.recorded_traffic(rec["kernel"])
-    assert t == rec["dram_read_bytes"] + rec["dram_write_bytes"]
+    if hashlib.sha256(src).hexdigest() == rec["source_sha256"]:
+        assert t == rec["dram_read_bytes"] + rec["dram_write_bytes"]
+    else:
+        assert t is None     # counters taken on another version of the kernel source
     assert bench.recorded_traffic("some_other_kernel") is None
 
 
@@ -41,3 +46,27 @@ def test_algorithmic_constants():
 def test_whole_job_value_is_units_over_max_time():
     assert bench.whole_job_value(1000, 2.0, 1) == 1000 / 2e-3
     assert bench.whole_job_value(1000, 2.0, 4) == 4 * 1000 / 2e-3
+
+
+def test_per_config_algorithmic_work():
+    # the dense workload counts q and k once per q/k head: with H_qk = H_v it is the headline formula
+    units, nbytes, flops = bench.fwd_alg(2, 16384, 32, 32, 2)
+    assert units == 2 * 16384 * 32
+    assert nbytes == units * bench.BYTES_PER_TOKEN_HEAD + 2 * 32 * bench.STATE_BYTES_PER_SEQ_HEAD
+    assert flops == units * bench.FLOPS_PER_TOKEN_HEAD
+    # grouped value heads: q, k read once per group of four value heads
+    _, gb, _ = bench.fwd_alg(1, 32768, 16, 64, 2)
+    assert gb == 32768 * (16 * 512 + 64 * (512 + 2 + 256)) + 2 * 64 * bench.STATE_BYTES_PER_SEQ_HEAD
+
+
+def test_rate_fields_flag_rates_above_the_copy_peak():
+    t = {"ms": 1.0, "p10_ms": 0.9, "p90_ms": 1.1, "reps": 3}
+    ok = bench.rate_fields(t, 1000, 10 ** 9, 10 ** 12, hbm_peak=2000.0, tc_peak=2000.0)
+    assert ok["GB/s"] == 1000.0 and "note" not in ok and ok["hbm_frac"] == 0.5
+    hi = bench.rate_fields(t, 1000, 3 * 10 ** 9, 10 ** 12, hbm_peak=2000.0, tc_peak=2000.0)
+    assert "note" in hi
+
+
+def test_both_arms_print_the_same_config():
+    assert bench.bench_config(1) == bench.bench_config(1)
+    assert bench.bench_config(2)["parallelism"] == "replicas x2"

@@ -176,6 +176,9 @@ def test_full_size_workload_sampled(name, qk_heads):
 
 
 # ---------------------------------------------------------------- decode
+DECODE_STATE_REL_L2 = 1e-5
+
+
 def _decode_gpu(d):
     from gated_delta_rule_40_gb300 import kda
     st = d.state.cuda()
@@ -193,6 +196,9 @@ def test_decode_matches_oracle(B, H, Hq):
     ro, rs = oracle.decode(d)
     pr = parity(out, st, ro, rs)
     assert pr.ok(), f"decode B={B}: {pr}"
+    # the step runs in fp32 end to end (one fp32 update per state element), so the state
+    # agrees with the fp64 oracle to a few fp32 roundings, not just the forward's bound
+    assert pr.state_rel <= DECODE_STATE_REL_L2, f"decode B={B}: {pr}"
 
 
 def test_decode_equals_fwd_t1():
