@@ -19,6 +19,7 @@
 // products and U, P, Kd, Delta are tf32 (fp32 accumulate); W and Qg are stored
 // in bf16 and multiply a bf16 copy of the state; the state itself is fp32.
 #include "kda_common.cuh"
+#include "kda_tma.cuh"
 
 namespace kda {
 
@@ -169,35 +170,32 @@ constexpr uint32_t REC_BYTES = 109568;
 constexpr int IN_THREADS = 256;
 constexpr int IN_CTAS_PER_SM = 2;
 constexpr int SL = 32;                  // channels per slice (one 128-byte tf32 atom)
-constexpr int GAS = 36;                 // Gam slice row stride (floats)
 constexpr int AS = CH + 4;              // A / T row stride (floats)
 constexpr int XS = 36;                  // inversion scratch row stride (floats)
 constexpr int ZS = 20;                  // 16 x 16 inversion scratch row stride (floats)
-constexpr int TBS = 36;                 // table row stride (floats)
-constexpr uint32_t RAW_T = 4096;        // one tensor of a raw slice: 64 rows x 32 bf16 (64-byte rows)
+constexpr uint32_t RAW_T = 4096;        // one tensor of a raw slice: 64 rows x 32 bf16 (64-byte rows, 64-byte swizzle)
 constexpr uint32_t RAW_SLICE = 3 * RAW_T;   // q, k, graw
 
 constexpr uint32_t IS_KG = 0;                // B of the W MMA: Kg, MN-major bf16, N = 128 (k), K = 64 (j)
 constexpr uint32_t IS_R1 = 16384;            // 52 KiB: slice operands; then A, T, scratch, P; then W, U staging
 constexpr uint32_t IS_ROWS = IS_R1;          // 256 rows x 32 ch tf32: F_k, F_q, R_k, R_q
 constexpr uint32_t IS_COLS = IS_R1 + 32768;  // 160 rows x 32 ch tf32: C_k (64), H versions (96)
-constexpr uint32_t IS_R2 = 69632;            // raw q / k / graw slices (two buffers); then V
-constexpr uint32_t IS_R3 = 94208;            // Gam slice and tables; then T'_hi, T'_lo
-constexpr uint32_t IS_GA = IS_R3;            // Gam slice, fp32 [64][36] (log2 units), 16-byte units swizzled
-constexpr uint32_t IS_TAB = IS_R3 + 9216;    // per-channel tables [20][36] fp32
+constexpr uint32_t IS_R2 = 69632;            // raw q / k / graw slices (two buffers, TMA); then V
+constexpr uint32_t IS_R3 = 94208;            // per-slice exchange of gate sums; then T'_hi, T'_lo
+constexpr uint32_t IS_XW = IS_R3;            // per-warp gate totals [8 warps][32 ch] fp32
+constexpr uint32_t IS_XG = IS_R3 + 1024;     // gate at each block's first row [4 blocks][32 ch] fp32
 constexpr uint32_t IS_MISC = 110592;
 constexpr uint32_t IS_RV = IS_MISC;          // rq, rk, beta, qk [4][64] fp32
 constexpr uint32_t IS_GCS = IS_MISC + 1024;  // exp(Gam_C) [128]
-constexpr uint32_t IS_BAR = IS_MISC + 1536;  // 2 mbarriers
-constexpr uint32_t IS_SLOT = IS_MISC + 1552; // TMEM address
-constexpr uint32_t IS_BYTES = IS_MISC + 1568 + 1024;   // + alignment slack
+constexpr uint32_t IS_BAR = IS_MISC + 1536;  // 5 mbarriers: A/P MMAs, W/U MMAs, raw buffer 0, raw buffer 1, V
+constexpr uint32_t IS_SLOT = IS_MISC + 1576; // TMEM address
+constexpr uint32_t IS_BYTES = IS_MISC + 1584 + 1024;   // + alignment slack
 // aliases once the slices are done
 constexpr uint32_t IS_A = IS_R1;             // fp32 [64][68]
 constexpr uint32_t IS_T = IS_R1 + 17408;     // fp32 [64][68]
 constexpr uint32_t IS_X = IS_R1 + 34816;     // fp32 [32][36] (or [2][16][20])
 constexpr uint32_t IS_PI = IS_R1 + 39424;    // P image staging (bf16, 8 KiB)
 constexpr uint32_t IS_V = IS_R2;             // B of the U MMA: V, MN-major bf16, N = 128 (v), K = 64 (j)
-constexpr uint32_t IS_PN = IS_R2 + RAW_SLICE + 2 * RAW_T;   // row-norm partial sums [256] float4 (graw of buffer 1)
 constexpr uint32_t IS_TWH = IS_A;            // A of the W MMA: T'_W = T diag(beta rk), hi / lo (A is dead by then)
 constexpr uint32_t IS_TWL = IS_A + 8192;
 constexpr uint32_t IS_TPH = IS_R3;           // A of the W/U MMAs: T'_hi, 64 rows (r) x 64 (j) bf16
@@ -205,11 +203,11 @@ constexpr uint32_t IS_TPL = IS_R3 + 8192;    // T'_lo
 constexpr uint32_t IS_WS = IS_R1;            // W half of the WQ image (2 x 8 KiB)
 constexpr uint32_t IS_US = IS_R1 + 16384;    // U image staging (2 x 64 x 68 fp32)
 static_assert(IS_PI + 8192 <= IS_R2 && IS_US + 2 * CH * 68 * 4 <= IS_R2, "R1 aliases overflow");
-static_assert(IS_R2 + 2 * RAW_SLICE <= IS_R3 && IS_TAB + 20 * TBS * 4 <= IS_MISC && IS_TPL + 8192 <= IS_MISC,
+static_assert(IS_R2 + 2 * RAW_SLICE <= IS_R3 && IS_XG + 512 <= IS_MISC && IS_TPL + 8192 <= IS_MISC,
               "R2 / R3 overflow");
+static_assert(IS_R2 % 1024 == 0 && RAW_SLICE % 512 == 0 && RAW_T % 512 == 0, "TMA swizzle alignment");
 static_assert(IN_CTAS_PER_SM * (IS_BYTES + 1024) <= 228 * 1024, "two CTAs per SM must fit");
 
-enum { TB_MU = 0, TB_M = 4, TB_EB = 9, TB_EA = 13, TB_D1 = 17, TB_D2 = 18, TB_D12 = 19 };
 enum { RV_RQ = 0, RV_RK = 64, RV_BETA = 128, RV_QK = 192 };
 
 struct IntraParams {
@@ -234,12 +232,11 @@ __device__ __forceinline__ uint32_t mn_off_bf16(int n, int kk) {
     return (uint32_t)((n >> 6) * 8192 + (kk >> 3) * 1024 + (kk & 7) * 128 + ((((n & 63) >> 3) ^ (kk & 7)) << 4) +
                       ((n & 7) << 1));
 }
-// raw slice rows are 64 bytes (four 16-byte units); q and k swizzle the unit
-// with (r / 2) % 4 (row-parallel readers), graw with (r / 8) % 4 (readers 8 rows apart)
-__device__ __forceinline__ uint32_t raw_off_qk(int r, int unit) { return (uint32_t)(r * 64 + ((unit ^ ((r >> 1) & 3)) << 4)); }
-__device__ __forceinline__ uint32_t raw_off_g(int r, int unit) { return (uint32_t)(r * 64 + ((unit ^ ((r >> 3) & 3)) << 4)); }
-// Gam slice: element (r, c) of the 32-channel slice; 16-byte unit swizzled with r / 8
-__device__ __forceinline__ int ga_idx(int r, int c) { return r * GAS + ((((c >> 2) ^ (r >> 3)) & 7) << 2) + (c & 3); }
+// Byte offset of the channel pair (2p, 2p + 1) of row r in a raw slice: 64-byte rows whose four
+// 16-byte units are permuted by the TMA 64-byte swizzle (unit ^= (r / 2) % 4)
+__device__ __forceinline__ uint32_t raw_pair_off(int r, int p) {
+    return (uint32_t)(r * 64 + ((((p >> 2) ^ ((r >> 1) & 3))) << 4) + 4 * (p & 3));
+}
 
 __device__ __forceinline__ void stg_hint_b32(void *p, uint32_t v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;\n" ::"l"(p), "r"(v), "l"(pol) : "memory");
@@ -277,7 +274,11 @@ __device__ __forceinline__ void split_mma(const float *X, int xs, const float *Y
     }
 }
 
-__global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const IntraParams p) {
+__global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                          const __grid_constant__ CUtensorMap tk,
+                                                                          const __grid_constant__ CUtensorMap tg,
+                                                                          const __grid_constant__ CUtensorMap tv,
+                                                                          const IntraParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     if (p.hdr[1] == 0) return;
@@ -285,11 +286,10 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     if ((long long)blockIdx.x >= n_items) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t bar_ap = sbase + IS_BAR, bar_wu = sbase + IS_BAR + 8;
+    // mbarriers: A/P MMAs (two committers), W/U MMAs, raw buffers 0 and 1, V
+    const uint32_t bar_ap = sbase + IS_BAR, bar_wu = bar_ap + 8, bar_raw = bar_ap + 16, bar_v = bar_ap + 32;
     const uint64_t pol_ef = l2_evict_first_policy();
     float *rv = reinterpret_cast<float *>(sm + IS_RV);
-    float *tab = reinterpret_cast<float *>(sm + IS_TAB);
-    float *ga = reinterpret_cast<float *>(sm + IS_GA);
     float *gcs = reinterpret_cast<float *>(sm + IS_GCS);
     float *sA = reinterpret_cast<float *>(sm + IS_A);
     float *sT = reinterpret_cast<float *>(sm + IS_T);
@@ -297,6 +297,9 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     if (tid == 0) {
         mbar_init(bar_ap, 2);
         mbar_init(bar_wu, 1);
+        mbar_init(bar_raw, 1);
+        mbar_init(bar_raw + 8, 1);
+        mbar_init(bar_v, 1);
         mbar_fence_init();
     }
     if (warp == 0) tmem_alloc(sbase + IS_SLOT, 256);
@@ -306,28 +309,32 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + IS_SLOT);
     const uint32_t t_off = tmem, t_diag = tmem + 96, t_w = tmem, t_u = tmem + 128;
 
-    const size_t qk_stride = (size_t)p.H_qk * KD, gv_stride = (size_t)p.H_v * KD;
     const int group = p.H_v / p.H_qk;
-    // raw q / k / graw of slice s (32 channels) of item (d, hh) into buffer s % 2, zero rows past its length
+    // raw q / k / graw of slice s (32 channels) of item (d, hh) into buffer s % 2 (one thread issues;
+    // rows past the tensor arrive as zeros, rows past the chunk's length are masked by the readers)
     auto issue_raw = [&](const ChunkDesc &d, int hh, int s) {
-        const int hq_ = hh / group;
-        const uint16_t *qr = p.q + ((size_t)d.tok * p.H_qk + hq_) * KD + s * SL;
-        const uint16_t *kr = p.k + ((size_t)d.tok * p.H_qk + hq_) * KD + s * SL;
-        const uint16_t *gr = p.graw + ((size_t)d.tok * p.H_v + hh) * KD + s * SL;
-        unsigned char *base = sm + IS_R2 + (s & 1) * RAW_SLICE;
-#pragma unroll
-        for (int i = 0; i < 3; ++i) {
-            const int idx = tid + IN_THREADS * i, t = idx >> 8, r = (idx >> 2) & 63, u = idx & 3;
-            unsigned char *dst = base + t * RAW_T + (t < 2 ? raw_off_qk(r, u) : raw_off_g(r, u));
-            if (r < d.len) {
-                const uint16_t *src = t == 0 ? qr + r * qk_stride : t == 1 ? kr + r * qk_stride : gr + r * gv_stride;
-                cp_async16(dst, src + u * 8);
-            } else {
-                *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-            }
-        }
-        cp_async_commit();
+        const uint32_t dst = sbase + IS_R2 + (uint32_t)(s & 1) * RAW_SLICE, mb = bar_raw + 8 * (s & 1);
+        mbar_expect_tx(mb, RAW_SLICE);
+        tma_load_3d(dst, &tq, s * SL, hh / group, d.tok, mb);
+        tma_load_3d(dst + RAW_T, &tk, s * SL, hh / group, d.tok, mb);
+        tma_load_3d(dst + 2 * RAW_T, &tg, s * SL, hh, d.tok, mb);
     };
+
+    // Thread mapping of the slice phase: channel pair cp = 2 (lane % 16) of the slice, 4-row segment
+    // seg = 2 warp + lane / 16 (rows 4 seg .. 4 seg + 3), 16-row block blk = warp / 2.  The gate prefix
+    // sum runs down the thread's own rows; segment and block sums are exchanged once per slice.
+    const int pp = lane & 15, hs = lane >> 4, seg = 2 * warp + hs, blk = warp >> 1, r0 = 4 * seg, cp = 2 * pp;
+    const bool wodd = (warp & 1) != 0;
+    uint32_t roff[4];                 // raw-slice offsets of this thread's channel pair in its four rows
+    uint32_t ooff[4];                 // tf32 operand-image offsets (row r0 + i, channels cp, cp + 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + i;
+        roff[i] = raw_pair_off(r, pp);
+        ooff[i] = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((pp >> 1) ^ (r & 7))) << 4) + 8 * (pp & 1));
+    }
+    // H versions (column operand times the block decay between the pair): rows 64 + 16 v + (r % 16) of COLS
+    const uint32_t hoff = (uint32_t)(((r0 & 15) >> 3) * 1024);   // + 1 KiB per 8 rows inside the 16-row version
 
     // The description of the next item (chunk, head, A_log) is fetched while the
     // current one is processed, and its first two raw slices are issued as soon as
@@ -338,8 +345,10 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
     int chunk_next = (int)(item / p.Hw), h_next = p.h0 + (int)(item % p.Hw);
     ChunkDesc cd_next = p.chunks[chunk_next];
     float alog_next = p.A_log[h_next];
-    issue_raw(cd_next, h_next, 0);
-    issue_raw(cd_next, h_next, 1);
+    if (tid == 0) {
+        issue_raw(cd_next, h_next, 0);
+        issue_raw(cd_next, h_next, 1);
+    }
     for (int it = 0; item < n_items; item += gridDim.x, ++it) {
         const int chunk = chunk_next, h = h_next;
         const ChunkDesc cd = cd_next;
@@ -347,7 +356,6 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         const size_t ch = (size_t)chunk * p.Hw + (h - p.h0);
         unsigned char *rec = p.rec + ch * REC_BYTES;
         const int len = cd.len;
-        const uint16_t *vrow = p.v + ((size_t)cd.tok * p.H_v + h) * KD;    // row r at + r * H_v * KD
         const long long nitem = item + gridDim.x;
         const bool has_next = nitem < n_items;
         if (has_next) {
@@ -361,89 +369,11 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             alog_next = p.A_log[h_next];
         }
 
-        // ---- 1. beta (global load, consumed after the first gate step)
+        // ---- 1. beta (global load); the previous item's bulk stores must be done reading shared
+        //         memory (W/U staging, P, exp(Gam_C)) before this item's slices overwrite it
         float bb_raw = 0.f;
         if (tid < len) bb_raw = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
-        cp_async_wait<1>();   // slice 0 landed (this thread's copies)
-        // the previous item's bulk stores must be done reading shared memory (W/U staging, P, exp(Gam_C))
         if (tid == 0) bulk_wait_read_all();
-        __syncthreads();
-
-        // gate (log2 units) of slice s, its in-chunk prefix sum and the per-channel tables.
-        // Warp w: channels 4w .. 4w + 3 of the slice; lane = (8-row segment, channel).
-        auto gate_tables = [&](int s) {
-            const unsigned char *rawb = sm + IS_R2 + (s & 1) * RAW_SLICE;
-            const int seg = lane >> 2, cl = lane & 3, cs = 4 * warp + cl;
-            // running sums of softplus (log2 units); the factor -exp(A_log) is applied once at the end
-            float loc[8], run = 0.f;
-            const unsigned char *gp = rawb + 2 * RAW_T + raw_off_g(8 * seg, cs >> 3) + (cs & 7) * 2;   // + 64 i: row 8 seg + i
-            if (len == CH) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    run += softplus_log2(bf16_to_f(*reinterpret_cast<const uint16_t *>(gp + 64 * i)));
-                    loc[i] = run;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float sp = softplus_log2(bf16_to_f(*reinterpret_cast<const uint16_t *>(gp + 64 * i)));
-                    run += 8 * seg + i < len ? sp : 0.f;
-                    loc[i] = run;
-                }
-            }
-            float incl = run;
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const float na = -a_gate, off = (incl - run) * na;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) ga[ga_idx(8 * seg + i, cs)] = fmaf(loc[i], na, off);
-            const float last = fmaf(loc[7], na, off), first = fmaf(loc[0], na, off);
-            float m[5], fi[4];
-            m[0] = 0.f;
-#pragma unroll
-            for (int kk = 1; kk <= 4; ++kk) m[kk] = __shfl_sync(0xffffffffu, last, (2 * kk - 1) * 4 + cl);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) fi[i] = __shfl_sync(0xffffffffu, first, 8 * i + cl);
-            // every lane forms the exponentials (no divergent waits); segment seg stores its share
-            const float eb1 = ex2(m[1]), eb2 = ex2(m[2]), eb3 = ex2(m[3]);
-            const float ea0 = ex2(m[4] - m[1]), ea1 = ex2(m[4] - m[2]), ea2 = ex2(m[4] - m[3]);
-            const float d1 = ex2(m[2] - m[1]), d2 = ex2(m[3] - m[2]), d12 = ex2(m[3] - m[1]), gc = ex2(m[4]);
-            float *tb = tab + cs;
-            if (seg == 0) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) tb[(TB_MU + i) * TBS] = 0.5f * (fi[i] + m[i + 1]);
-            } else if (seg == 1) {
-#pragma unroll
-                for (int kk = 0; kk < 5; ++kk) tb[(TB_M + kk) * TBS] = m[kk];
-            } else if (seg == 2) {
-                tb[TB_EB * TBS] = 1.f;
-                tb[(TB_EB + 1) * TBS] = eb1;
-                tb[(TB_EB + 2) * TBS] = eb2;
-                tb[(TB_EB + 3) * TBS] = eb3;
-            } else if (seg == 3) {
-                tb[TB_EA * TBS] = ea0;
-                tb[(TB_EA + 1) * TBS] = ea1;
-                tb[(TB_EA + 2) * TBS] = ea2;
-                tb[(TB_EA + 3) * TBS] = 1.f;
-            } else if (seg == 4) {
-                tb[TB_D1 * TBS] = d1;
-                tb[TB_D2 * TBS] = d2;
-                tb[TB_D12 * TBS] = d12;
-            } else if (seg == 5) {
-                gcs[s * SL + cs] = gc;
-            }
-        };
-
-        // ---- 2. channel slices.  Order per slice s: operands(s), MMAs(s), gate/tables(s + 1),
-        //         wait for MMAs(s); the gate of slice 0 comes first.  q and k enter the operands
-        //         unnormalised: every product below is linear in a row's q or k, so the L2
-        //         norms (summed from the staged slices) are applied afterwards: to A and P in
-        //         their epilogue, to Kg through T' for W, and by the scan to Kd and Qg.
-        float psq = 0.f, psk = 0.f, psqk = 0.f;   // this thread's partial sums of q.q, k.k, q.k
-        gate_tables(0);
         if (tid < CH) rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-bb_raw * LOG2E)) : 0.f;
         // pull the next item's rows into L2 while this one is processed
         if (has_next) {
@@ -459,99 +389,160 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                 prefetch_line_l2(src + 64);
             }
         }
-        __syncthreads();
+
+        // ---- 2. channel slices.  Per slice: gate of the thread's rows (softplus, prefix sum), exchange
+        //         of segment sums, then every operand of the slice.  q and k enter the operands
+        //         unnormalised: every product below is linear in a row's q or k, so the L2 norms
+        //         (summed here over the slices) are applied afterwards: to A and P in their epilogue,
+        //         to Kg through T' for W, and by the scan to Kd and Qg.
+        const float na = -a_gate;
+        const bool partial = len < CH;
+        float nq[4] = {0.f, 0.f, 0.f, 0.f}, nk[4] = {0.f, 0.f, 0.f, 0.f}, nqk[4] = {0.f, 0.f, 0.f, 0.f};
+        float *xw = reinterpret_cast<float *>(sm + IS_XW);
+        float *xg = reinterpret_cast<float *>(sm + IS_XG);
+#pragma unroll 1
         for (int sl = 0; sl < KD / SL; ++sl) {
             const int c0 = sl * SL;
             const unsigned char *rawb = sm + IS_R2 + (sl & 1) * RAW_SLICE;
-            // 2b. operands: thread (row r, 8-channel group g), two halves of 4 channels
+            if (!mbar_wait(bar_raw + 8 * (sl & 1), (uint32_t)(sl >> 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            // 2a. gate of rows r0 .. r0 + 3, channels c0 + cp, + 1 (log2 units), in-segment prefix sums
+            uint32_t qw[4], kw[4];
+            float2 G[4];
             {
-                const int r = tid & 63, g = tid >> 6, bi = r >> 4, rl = r & 15, r7 = r & 7;
-                // swizzled row bases: ROWS / COLS rows r + 64 i share r % 8, so they differ by 8 KiB per i;
-                // the H versions sit at COLS rows 64 + 16 v + rl
-                unsigned char *const rows_r = sm + IS_ROWS + (r >> 3) * 1024 + r7 * 128;
-                unsigned char *const cols_r = sm + IS_COLS + (r >> 3) * 1024 + r7 * 128;
-                unsigned char *const cols_v = sm + IS_COLS + (rl >> 3) * 1024 + r7 * 128;
-                // Kd^T element (k, r) of the record: k / 8 = c0 / 8 + g, k % 8 = 4 hh + e
-                unsigned char *const kd_r = rec + REC_KDT + (r >> 5) * 16384 + (c0 / 8 + g) * 1024 + (r & 3) * 4;
-                const int x4 = (r & 31) >> 2;
-                const uint4 qw = *reinterpret_cast<const uint4 *>(rawb + raw_off_qk(r, g));
-                const uint4 kw = *reinterpret_cast<const uint4 *>(rawb + RAW_T + raw_off_qk(r, g));
-                uint32_t kg2[4], qg2[4];
+                float sx = 0.f, sy = 0.f;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int cls = 8 * g + 4 * hh;
-                    const float4 G = *reinterpret_cast<const float4 *>(ga + ga_idx(r, cls));
-                    const float4 MU = *reinterpret_cast<const float4 *>(tab + (TB_MU + bi) * TBS + cls);
-                    const float4 M0 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi) * TBS + cls);
-                    const float4 M1 = *reinterpret_cast<const float4 *>(tab + (TB_M + bi + 1) * TBS + cls);
-                    const float4 EB = *reinterpret_cast<const float4 *>(tab + (TB_EB + bi) * TBS + cls);
-                    const float4 EA = *reinterpret_cast<const float4 *>(tab + (TB_EA + bi) * TBS + cls);
-                    const uint32_t q0 = hh ? qw.z : qw.x, q1 = hh ? qw.w : qw.y;
-                    const uint32_t k0 = hh ? kw.z : kw.x, k1 = hh ? kw.w : kw.y;
-                    const float gg[4] = {G.x, G.y, G.z, G.w}, mu[4] = {MU.x, MU.y, MU.z, MU.w};
-                    const float m0[4] = {M0.x, M0.y, M0.z, M0.w}, m1[4] = {M1.x, M1.y, M1.z, M1.w};
-                    const float eb[4] = {EB.x, EB.y, EB.z, EB.w}, ea[4] = {EA.x, EA.y, EA.z, EA.w};
-                    const float kh[4] = {bf16_lo(k0), bf16_hi(k0), bf16_lo(k1), bf16_hi(k1)};   // unnormalised
-                    const float qt[4] = {bf16_lo(q0), bf16_hi(q0), bf16_lo(q1), bf16_hi(q1)};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        psq = fmaf(qt[e], qt[e], psq);
-                        psk = fmaf(kh[e], kh[e], psk);
-                        psqk = fmaf(qt[e], kh[e], psqk);
+                for (int i = 0; i < 4; ++i) {
+                    qw[i] = *reinterpret_cast<const uint32_t *>(rawb + roff[i]);
+                    kw[i] = *reinterpret_cast<const uint32_t *>(rawb + RAW_T + roff[i]);
+                    const uint32_t gw = *reinterpret_cast<const uint32_t *>(rawb + 2 * RAW_T + roff[i]);
+                    float s0 = softplus_log2(bf16_lo(gw)), s1 = softplus_log2(bf16_hi(gw));
+                    if (partial && r0 + i >= len) {   // rows past the chunk: no decay, q = k = 0
+                        s0 = 0.f;
+                        s1 = 0.f;
+                        qw[i] = 0u;
+                        kw[i] = 0u;
                     }
-                    float fk[4], fq[4], dk[4], dq[4], ck[4], hk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float dr = ex2(fminf(gg[e] - mu[e], DIAG_CLAMP2));
-                        const float dc = ex2(fminf(mu[e] - gg[e], DIAG_CLAMP2));
-                        // block-relative factors (always <= 1, exact for any gate strength)
-                        const float f = ex2(gg[e] - m0[e]), hf = ex2(m1[e] - gg[e]);
-                        fk[e] = kh[e] * f;
-                        fq[e] = qt[e] * f;
-                        dk[e] = kh[e] * dr;
-                        dq[e] = qt[e] * dr;
-                        ck[e] = kh[e] * dc;
-                        hk[e] = kh[e] * hf;
-                        // Kd^T element (k = c + e, r) straight into the record (a warp writes one 128-byte line)
-                        const int kk = 4 * hh + e;
-                        stg_hint_b32(kd_r + kk * 128 + ((x4 ^ kk) << 4), tf32_bits(hk[e] * ea[e]), pol_ef);
-                    }
-                    kg2[2 * hh] = pack_bf16x2(fk[0] * eb[0], fk[1] * eb[1]);
-                    kg2[2 * hh + 1] = pack_bf16x2(fk[2] * eb[2], fk[3] * eb[3]);
-                    qg2[2 * hh] = pack_bf16x2(fq[0] * eb[0], fq[1] * eb[1]);
-                    qg2[2 * hh + 1] = pack_bf16x2(fq[2] * eb[2], fq[3] * eb[3]);
-                    const uint32_t sw = (uint32_t)(((2 * g + hh) ^ r7) << 4);   // swizzled 16-byte unit
-                    sts128(rows_r + sw, fk[0], fk[1], fk[2], fk[3]);
-                    sts128(rows_r + 8192 + sw, fq[0], fq[1], fq[2], fq[3]);
-                    sts128(rows_r + 16384 + sw, dk[0], dk[1], dk[2], dk[3]);
-                    sts128(rows_r + 24576 + sw, dq[0], dq[1], dq[2], dq[3]);
-                    sts128(cols_r + sw, ck[0], ck[1], ck[2], ck[3]);
-                    if (bi == 0) {
-                        const float4 D1 = *reinterpret_cast<const float4 *>(tab + TB_D1 * TBS + cls);
-                        const float4 D12 = *reinterpret_cast<const float4 *>(tab + TB_D12 * TBS + cls);
-                        sts128(cols_v + 8 * 1024 + sw, hk[0], hk[1], hk[2], hk[3]);
-                        sts128(cols_v + 10 * 1024 + sw, hk[0] * D1.x, hk[1] * D1.y, hk[2] * D1.z, hk[3] * D1.w);
-                        sts128(cols_v + 14 * 1024 + sw, hk[0] * D12.x, hk[1] * D12.y, hk[2] * D12.z, hk[3] * D12.w);
-                    } else if (bi == 1) {
-                        const float4 D2 = *reinterpret_cast<const float4 *>(tab + TB_D2 * TBS + cls);
-                        sts128(cols_v + 12 * 1024 + sw, hk[0], hk[1], hk[2], hk[3]);
-                        sts128(cols_v + 16 * 1024 + sw, hk[0] * D2.x, hk[1] * D2.y, hk[2] * D2.z, hk[3] * D2.w);
-                    } else if (bi == 2) {
-                        sts128(cols_v + 18 * 1024 + sw, hk[0], hk[1], hk[2], hk[3]);
-                    }
+                    sx += s0;
+                    sy += s1;
+                    G[i] = make_float2(sx * na, sy * na);
                 }
-                // Kg (bf16) into the MN-major operand: element (k = c0 + 8 g .. + 7, j = r)
-                *reinterpret_cast<uint4 *>(sm + IS_KG + mn_off_bf16(c0 + 8 * g, r)) =
-                    make_uint4(kg2[0], kg2[1], kg2[2], kg2[3]);
-                // Qg (bf16) straight into the WQ image rows 0..63
-                stg_hint_v4(rec + REC_WQ + sw128_off(r, 2 * (c0 + 8 * g), 2 * CH), make_uint4(qg2[0], qg2[1], qg2[2], qg2[3]),
-                            pol_ef);
             }
-            if (sl + 1 < KD / SL) {
-                cp_async_wait<0>();   // the next slice's raw rows (this thread's copies)
-            } else {
-                // the four partial sums of row r (threads r + 64 g) go to the graw part of raw buffer 1
-                reinterpret_cast<float4 *>(sm + IS_PN)[tid] = make_float4(psq, psk, psqk, 0.f);
+            // 2b. segment sums -> per-warp sums and the block's first-row gate, exchanged through smem
+            const float2 tseg = G[3];
+            float2 tother;
+            tother.x = __shfl_xor_sync(0xffffffffu, tseg.x, 16);
+            tother.y = __shfl_xor_sync(0xffffffffu, tseg.y, 16);
+            if (hs == 0) {
+                *reinterpret_cast<float2 *>(xw + warp * SL + cp) = make_float2(tseg.x + tother.x, tseg.y + tother.y);
+                if (!wodd) *reinterpret_cast<float2 *>(xg + blk * SL + cp) = G[0];
+            }
+            // the previous slice's MMAs must be done with ROWS / COLS before they are rewritten
+            if (tid == 0 && sl > 0 && !mbar_spin(bar_ap, (uint32_t)(sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            __syncthreads();
+            // block boundaries M_b = Gam at the end of block b - 1 (M_0 = 0, M_4 = Gam_C)
+            float2 Mb, Mb1, Wlo;
+            const float2 wt0 = *reinterpret_cast<const float2 *>(xw + 0 * SL + cp);
+            const float2 wt1 = *reinterpret_cast<const float2 *>(xw + 1 * SL + cp);
+            const float2 wt2 = *reinterpret_cast<const float2 *>(xw + 2 * SL + cp);
+            const float2 wt3 = *reinterpret_cast<const float2 *>(xw + 3 * SL + cp);
+            const float2 wt4 = *reinterpret_cast<const float2 *>(xw + 4 * SL + cp);
+            const float2 wt5 = *reinterpret_cast<const float2 *>(xw + 5 * SL + cp);
+            const float2 wt6 = *reinterpret_cast<const float2 *>(xw + 6 * SL + cp);
+            const float2 wt7 = *reinterpret_cast<const float2 *>(xw + 7 * SL + cp);
+            const float2 M1 = make_float2(wt0.x + wt1.x, wt0.y + wt1.y);
+            const float2 M2 = make_float2(M1.x + (wt2.x + wt3.x), M1.y + (wt2.y + wt3.y));
+            const float2 M3 = make_float2(M2.x + (wt4.x + wt5.x), M2.y + (wt4.y + wt5.y));
+            const float2 M4 = make_float2(M3.x + (wt6.x + wt7.x), M3.y + (wt6.y + wt7.y));
+            switch (blk) {
+                case 0: Mb = make_float2(0.f, 0.f); Mb1 = M1; Wlo = wt0; break;
+                case 1: Mb = M1; Mb1 = M2; Wlo = wt2; break;
+                case 2: Mb = M2; Mb1 = M3; Wlo = wt4; break;
+                default: Mb = M3; Mb1 = M4; Wlo = wt6; break;
+            }
+            const float2 gf = *reinterpret_cast<const float2 *>(xg + blk * SL + cp);
+            // Gam - M_blk of row r0 + i is wlo + (pre + G[i]) (<= 0).  The block total is summed in the
+            // same order, so that the block's last row has Gam - M_blk+1 = 0 exactly (its Kd factor is
+            // exactly 1 however strong the gate).  The block's midpoint reference
+            // mu = (Gam(first row) + M_blk+1) / 2 sits at hm above M_blk.
+            const float2 wlo = make_float2(wodd ? Wlo.x : 0.f, wodd ? Wlo.y : 0.f);
+            const float2 pre = make_float2(hs ? tother.x : 0.f, hs ? tother.y : 0.f);
+            float2 tot;
+            switch (blk) {
+                case 0: tot = M1; break;
+                case 1: tot = make_float2(wt2.x + wt3.x, wt2.y + wt3.y); break;
+                case 2: tot = make_float2(wt4.x + wt5.x, wt4.y + wt5.y); break;
+                default: tot = make_float2(wt6.x + wt7.x, wt6.y + wt7.y); break;
+            }
+            const float2 hm = make_float2(0.5f * (gf.x + tot.x), 0.5f * (gf.y + tot.y));
+            const float2 eb = make_float2(ex2(Mb.x), ex2(Mb.y));                       // exp(M_blk)
+            const float2 ea = make_float2(ex2(M4.x - Mb1.x), ex2(M4.y - Mb1.y));       // exp(Gam_C - M_blk+1)
+            if (warp == 0 && hs == 0)
+                *reinterpret_cast<float2 *>(gcs + c0 + cp) = make_float2(ex2(M4.x), ex2(M4.y));
+            // block decays between sub-block pairs for the H versions of this block's rows
+            float2 xa = make_float2(1.f, 1.f), xb = make_float2(1.f, 1.f);
+            if (blk == 0) {
+                xa = make_float2(ex2(M2.x - M1.x), ex2(M2.y - M1.y));   // pair (2, 0)
+                xb = make_float2(ex2(M3.x - M1.x), ex2(M3.y - M1.y));   // pair (3, 0)
+            } else if (blk == 1) {
+                xa = make_float2(ex2(M3.x - M2.x), ex2(M3.y - M2.y));   // pair (3, 1)
+            }
+            // 2c. operands of rows r0 .. r0 + 3
+            unsigned char *rows = sm + IS_ROWS;
+            unsigned char *cols = sm + IS_COLS;
+            float2 kdv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = r0 + i;
+                const float2 x = make_float2(wlo.x + (pre.x + G[i].x), wlo.y + (pre.y + G[i].y));
+                const float2 kv = make_float2(bf16_lo(kw[i]), bf16_hi(kw[i]));
+                const float2 qv = make_float2(bf16_lo(qw[i]), bf16_hi(qw[i]));
+                // block-relative factors (always <= 1, exact for any gate strength) and the diagonal
+                // block's midpoint factors (exponents clamped at 85 nats)
+                const float2 f = make_float2(ex2(x.x), ex2(x.y));
+                const float2 hf = make_float2(ex2(tot.x - x.x), ex2(tot.y - x.y));
+                const float2 dr = make_float2(ex2(fminf(x.x - hm.x, DIAG_CLAMP2)), ex2(fminf(x.y - hm.y, DIAG_CLAMP2)));
+                const float2 dc = make_float2(ex2(fminf(hm.x - x.x, DIAG_CLAMP2)), ex2(fminf(hm.y - x.y, DIAG_CLAMP2)));
+                const float2 fk = __fmul2_rn(kv, f), fq = __fmul2_rn(qv, f);
+                const float2 hk = __fmul2_rn(kv, hf);
+                *reinterpret_cast<float2 *>(rows + ooff[i]) = fk;
+                *reinterpret_cast<float2 *>(rows + 8192 + ooff[i]) = fq;
+                *reinterpret_cast<float2 *>(rows + 16384 + ooff[i]) = __fmul2_rn(kv, dr);
+                *reinterpret_cast<float2 *>(rows + 24576 + ooff[i]) = __fmul2_rn(qv, dr);
+                *reinterpret_cast<float2 *>(cols + ooff[i]) = __fmul2_rn(kv, dc);
+                // H versions: rows 64 + 16 v + r % 16 (v: pairs (1,0), (2,0), (2,1), (3,0), (3,1), (3,2))
+                const uint32_t ho = (ooff[i] & 1023u) + hoff;
+                if (blk == 0) {
+                    *reinterpret_cast<float2 *>(cols + 8 * 1024 + ho) = hk;
+                    *reinterpret_cast<float2 *>(cols + 10 * 1024 + ho) = __fmul2_rn(hk, xa);
+                    *reinterpret_cast<float2 *>(cols + 14 * 1024 + ho) = __fmul2_rn(hk, xb);
+                } else if (blk == 1) {
+                    *reinterpret_cast<float2 *>(cols + 12 * 1024 + ho) = hk;
+                    *reinterpret_cast<float2 *>(cols + 16 * 1024 + ho) = __fmul2_rn(hk, xa);
+                } else if (blk == 2) {
+                    *reinterpret_cast<float2 *>(cols + 18 * 1024 + ho) = hk;
+                }
+                kdv[i] = __fmul2_rn(hk, ea);
+                // Kg (bf16) into the MN-major B operand of the W MMA: element (k = c0 + cp, j = r)
+                const float2 kg = __fmul2_rn(fk, eb), qg = __fmul2_rn(fq, eb);
+                *reinterpret_cast<uint32_t *>(sm + IS_KG + mn_off_bf16(c0 + cp, r)) = pack_bf16x2(kg.x, kg.y);
+                // Qg (bf16) straight into rows 0..63 of the record's WQ image
+                stg_hint_b32(rec + REC_WQ + sw128_off(r, 2 * (c0 + cp), 2 * CH), pack_bf16x2(qg.x, qg.y), pol_ef);
+                // partial row sums of q.q, k.k, q.k over this thread's two channels
+                nq[i] = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, nq[i]));
+                nk[i] = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, nk[i]));
+                nqk[i] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, nqk[i]));
+            }
+            // Kd^T rows k = c0 + cp, c0 + cp + 1, columns r0 .. r0 + 3: one 16-byte unit each (tf32)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int k = c0 + cp + e;
+                const uint4 u = e == 0 ? make_uint4(tf32_bits(kdv[0].x), tf32_bits(kdv[1].x), tf32_bits(kdv[2].x),
+                                                    tf32_bits(kdv[3].x))
+                                       : make_uint4(tf32_bits(kdv[0].y), tf32_bits(kdv[1].y), tf32_bits(kdv[2].y),
+                                                    tf32_bits(kdv[3].y));
+                stg_hint_v4(rec + REC_KDT + (r0 >> 5) * 16384 + (k >> 3) * 1024 + (k & 7) * 128 +
+                                ((((seg & 7) ^ (k & 7))) << 4),
+                            u, pol_ef);
             }
             fence_async_smem();
             tc_fence_before();
@@ -560,45 +551,60 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             // committing to the slice barrier, so neither warp carries the whole issue time
             if (tid == 0 || tid == 128) {
                 tc_fence_after();
-                const bool off = tid == 0;
-                const uint32_t id = off ? idesc_tf32(128, 96) : idesc_tf32(128, 64);
-                const uint32_t arow = sbase + IS_ROWS + (off ? 0u : 16384u), bcol = sbase + IS_COLS + (off ? 8192u : 0u);
+                const bool offd = tid == 0;
+                const uint32_t id = offd ? idesc_tf32(128, 96) : idesc_tf32(128, 64);
+                const uint32_t arow = sbase + IS_ROWS + (offd ? 0u : 16384u), bcol = sbase + IS_COLS + (offd ? 8192u : 0u);
 #pragma unroll
                 for (int ks = 0; ks < SL / 8; ++ks)
-                    umma_tf32(off ? t_off : t_diag, umma_desc(arow + ks * 32, 16, 1024), umma_desc(bcol + ks * 32, 16, 1024),
+                    umma_tf32(offd ? t_off : t_diag, umma_desc(arow + ks * 32, 16, 1024), umma_desc(bcol + ks * 32, 16, 1024),
                               id, (sl > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(bar_ap);
             }
-            if (sl + 2 < KD / SL) {
-                issue_raw(cd, h, sl + 2);
-            } else if (sl + 1 == KD / SL) {
-                // V into the MN-major operand of the U MMA (the raw buffers are free now)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int idx = tid + IN_THREADS * i, r = idx >> 4, c8 = (idx & 15) * 8;
-                    unsigned char *dv = sm + IS_V + mn_off_bf16(c8, r);
-                    if (r < len) cp_async16(dv, vrow + r * gv_stride + c8);
-                    else *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
+            if (tid == 32) {
+                // raw buffer sl % 2 is free (every thread read it before the barrier): slice sl + 2,
+                // or, after the last slice, V into the MN-major operand of the U MMA
+                fence_async_smem();
+                if (sl + 2 < KD / SL) {
+                    issue_raw(cd, h, sl + 2);
+                } else if (sl + 1 == KD / SL) {
+                    mbar_expect_tx(bar_v, 2 * 8192);
+                    tma_load_3d(sbase + IS_V, &tv, 0, h, cd.tok, bar_v);
+                    tma_load_3d(sbase + IS_V + 8192, &tv, 64, h, cd.tok, bar_v);
                 }
-                cp_async_commit();
             }
-            if (sl + 1 < KD / SL) gate_tables(sl + 1);
-            // this slice's MMAs must be done with ROWS / COLS (and, after the last, with TMEM)
-            if (tid == 0 && !mbar_spin(bar_ap, sl & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
-            __syncthreads();
-            tc_fence_after();
         }
-        // row norms: rq = scale / |q|, rk = 1 / |k|; QK keeps the raw q.k (the P diagonal is
-        // q.k rk; the column scaling of the epilogue supplies rk)
-        if (tid < CH) {
-            const float4 *pn = reinterpret_cast<const float4 *>(sm + IS_PN);
-            const float4 a0 = pn[tid], a1 = pn[tid + 64], a2 = pn[tid + 128], a3 = pn[tid + 192];
-            const float sq = (a0.x + a1.x) + (a2.x + a3.x), sk = (a0.y + a1.y) + (a2.y + a3.y);
-            rv[RV_RQ + tid] = p.scale * rsqrtf(sq + L2_EPS);
-            rv[RV_RK + tid] = rsqrtf(sk + L2_EPS);
-            rv[RV_QK + tid] = (a0.z + a1.z) + (a2.z + a3.z);
+        // the last slice's MMAs (and so TMEM) complete before the epilogue
+        if (tid == 0 && !mbar_spin(bar_ap, 1u)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+        // row norms: the 16 lanes of a half-warp hold the partial sums of the same four rows over
+        // disjoint channel pairs; a reduce-scatter leaves the total of (row r0 + L / 4, quantity L % 4)
+        // in lane L of the half.  rq = scale / |q|, rk = 1 / |k|; QK keeps the raw q.k (the P diagonal
+        // is q.k rk; the column scaling of the epilogue supplies rk).
+        {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[4 * i] = nq[i];
+                v[4 * i + 1] = nk[i];
+                v[4 * i + 2] = nqk[i];
+                v[4 * i + 3] = 0.f;
+            }
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int j = 0; j < o; ++j) {
+                    const float send = up ? v[j] : v[j + o];
+                    const float keep = up ? v[j + o] : v[j];
+                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            const int L = lane & 15, row = r0 + (L >> 2), qty = L & 3;
+            if (qty == 0) rv[RV_RQ + row] = p.scale * rsqrtf(v[0] + L2_EPS);
+            else if (qty == 1) rv[RV_RK + row] = rsqrtf(v[0] + L2_EPS);
+            else if (qty == 2) rv[RV_QK + row] = v[0];
         }
         __syncthreads();
+        tc_fence_after();
 
         // ---- 3. A (times beta) to smem, P image (bf16) to staging.  Warp w: TMEM lanes
         //         32 (w & 3) .. (K rows 0..63, Q rows 64..127), 16-column blocks 2 (w >> 2) and 2 (w >> 2) + 1.
@@ -781,7 +787,15 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             *reinterpret_cast<uint4 *>(sm + IS_TWH + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4 *>(sm + IS_TWL + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
-        cp_async_wait<0>();   // V (this thread's copies)
+        // V arrives by TMA; rows past the chunk's length belong to the next sequence: zero them so
+        // that they contribute exact zeros to U (their T' columns are zero) whatever they hold
+        if (partial) {
+            if (!mbar_wait(bar_v, (uint32_t)it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            for (int idx = tid; idx < (CH - len) * 16; idx += IN_THREADS) {
+                const int r = len + (idx >> 4), u = idx & 15;
+                *reinterpret_cast<uint4 *>(sm + IS_V + (u >> 3) * 8192 + r * 128 + (u & 7) * 16) = make_uint4(0, 0, 0, 0);
+            }
+        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -790,6 +804,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         //         U^T = V^T (T'_hi + T'_lo)^T   (M = 128 v, N = 64 r, K = 64 j; A = V MN-major, B = T'
         //         K-major), so that each TMEM lane v holds one row of the U image
         if (tid == 0) {
+            if (!partial && !mbar_wait(bar_v, (uint32_t)it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
             tc_fence_after();
             const uint32_t id_w = idesc_bf16(64, 128) | (1u << 16);
             const uint32_t id_u = idesc_bf16(128, 64) | (1u << 15);
@@ -806,14 +821,14 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             umma_commit(bar_wu);
             if (!mbar_spin(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
             bulk_wait_read_all();   // the P image store is done reading before W / U staging reuses it
+            // the raw buffers (V) are free: start the next item's first two slices
+            if (has_next) {
+                issue_raw(cd_next, h_next, 0);
+                issue_raw(cd_next, h_next, 1);
+            }
         }
         __syncthreads();
         tc_fence_after();
-        // the raw buffers (V) are free: start the next item's first two slices
-        if (has_next) {
-            issue_raw(cd_next, h_next, 0);
-            issue_raw(cd_next, h_next, 1);
-        }
         {
             const int q = warp & 3;
             const uint32_t lo = (uint32_t)(q * 32) << 16;
@@ -1715,7 +1730,15 @@ static cudaError_t launch_fwd_impl(const uint16_t *q, const uint16_t *k, const u
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (nck > 0) {
+    const long long rows = (long long)B * T;
+    if (nck > 0 && rows > 0) {
+        // raw slices of q, k, graw: 32 channels x 64 rows (64-byte swizzle); V: 64 channels x 64 rows
+        // (128-byte swizzle, the MN-major operand layout of the U MMA)
+        CUtensorMap mq, mk, mg, mv;
+        if ((e = tma_map_rows_heads(&mq, q, rows, H_qk, SL, CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess) return e;
+        if ((e = tma_map_rows_heads(&mk, k, rows, H_qk, SL, CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess) return e;
+        if ((e = tma_map_rows_heads(&mg, graw, rows, H_v, SL, CU_TENSOR_MAP_SWIZZLE_64B)) != cudaSuccess) return e;
+        if ((e = tma_map_rows_heads(&mv, v, rows, H_v, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess) return e;
         IntraParams ip;
         ip.q = q; ip.k = k; ip.v = v; ip.graw = graw; ip.b = b; ip.A_log = A_log; ip.scale = scale;
         ip.H_qk = H_qk; ip.H_v = H_v; ip.h0 = h0; ip.Hw = Hw; ip.chunks = ws.chunks; ip.hdr = ws.hdr;
@@ -1726,7 +1749,7 @@ static cudaError_t launch_fwd_impl(const uint16_t *q, const uint16_t *k, const u
         const long long items = nck * (long long)Hw;
         const long long slots = (long long)nsm * IN_CTAS_PER_SM;   // persistent: two CTAs per SM
         const unsigned grid = (unsigned)(items < slots ? items : slots);
-        intra_kernel<<<grid, IN_THREADS, IS_BYTES, stream>>>(ip);
+        intra_kernel<<<grid, IN_THREADS, IS_BYTES, stream>>>(mq, mk, mg, mv, ip);
         ++*launches;
         timing_mark("intra_kernel", stream);
         e = cudaGetLastError();

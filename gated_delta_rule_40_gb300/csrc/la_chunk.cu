@@ -32,6 +32,7 @@
 #include <cudaTypedefs.h>
 
 #include "kda_common.cuh"
+#include "kda_tma.cuh"
 
 namespace kda {
 
@@ -77,13 +78,6 @@ struct LaParams {
     int H_qk, H_v, nseq;
 };
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
-                                            uint32_t mbar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];\n" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
-        : "memory");
-}
 // MMA with the A operand in tensor memory (row m in lane m; column c holds K elements 2c, 2c + 1)
 __device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                              uint32_t acc) {
@@ -412,29 +406,9 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
 
 // ---------------------------------------------------------------- host side
 namespace {
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-cudaError_t get_encoder() {
-    if (g_encode) return cudaSuccess;
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    return cudaSuccess;
-}
-
-// [rows][heads][128] bf16 as a 3-D tensor (channel, head, row), boxes of 64 channels x 1 head x 64 rows,
-// 128-byte swizzle, zero fill past the last row.
+// [rows][heads][128] bf16, boxes of 64 channels x 1 head x 64 rows, 128-byte swizzle
 cudaError_t make_map(CUtensorMap *m, const void *base, long long rows, int heads) {
-    const cuuint64_t dims[3] = {(cuuint64_t)KD, (cuuint64_t)heads, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)KD * 2, (cuuint64_t)heads * KD * 2};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)CH};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return tma_map_rows_heads(m, base, rows, heads, 64, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 size_t align256_la(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -475,7 +449,6 @@ cudaError_t launch_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *
     if (nseq == 0) return cudaSuccess;
     const long long rows = (long long)B * T;
     CUtensorMap mq, mk, mv;
-    if ((e = get_encoder()) != cudaSuccess) return e;
     // a map needs at least one row; with no tokens the kernel only copies the states
     const void *qb = rows > 0 ? (const void *)q : (const void *)hdr;
     const void *kb = rows > 0 ? (const void *)k : (const void *)hdr;
