@@ -163,7 +163,7 @@ __device__ __forceinline__ void bwd_fwd_token(float4 (&S)[BW_ROWS], const float4
 
 __global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParams p) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
+    unsigned char *sm = aligned_smem<128>(smem_raw);
     if (p.hdr[1] == 0) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float *sqt = reinterpret_cast<const float *>(sm + BW_QT), *skh = reinterpret_cast<const float *>(sm + BW_KH);

@@ -280,7 +280,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                                                                           const __grid_constant__ CUtensorMap tv,
                                                                           const IntraParams p) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sm = aligned_smem<1024>(smem_raw);
     if (p.hdr[1] == 0) return;
     const long long n_items = (long long)p.hdr[0] * p.Hw;
     if ((long long)blockIdx.x >= n_items) return;
@@ -945,7 +945,7 @@ enum { BAR_WQ0 = 0, BAR_WQ1, BAR_PK0, BAR_PK1, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MM
 
 __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sm = aligned_smem<1024>(smem_raw);
     if (p.hdr[1] == 0) return;
     const int vb = blockIdx.x & 1;
     const int h = p.h0 + (blockIdx.x >> 1) % p.Hw;
@@ -1358,7 +1358,7 @@ struct GdnParams {
 
 __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(const GdnParams p) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *sm = aligned_smem<1024>(smem_raw);
     if (p.hdr[1] == 0) return;
     const long long n_items = (long long)p.hdr[0] * p.H_v;
     if ((long long)blockIdx.x >= n_items) return;

@@ -109,6 +109,16 @@ namespace kda {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// Base of the dynamic shared memory rounded up to ALIGN bytes.  The offset is added to the array
+// itself rather than through an integer cast of its address, so the compiler keeps every pointer
+// derived from it in the shared state space and emits shared-memory loads and stores (a generic
+// pointer would cost 64-bit address arithmetic and a state-space check per access).
+template <uint32_t ALIGN>
+__device__ __forceinline__ unsigned char *aligned_smem(unsigned char *raw) {
+    const uint32_t a = smem_u32(raw);
+    return raw + ((ALIGN - (a & (ALIGN - 1u))) & (ALIGN - 1u));
+}
+
 // Byte offset of element (row, kbyte) in a K-major, 128-byte-swizzled UMMA
 // operand image with `rows` rows: 8-row x 128-byte atoms (1024 B) stacked
 // along the rows, then one such column of atoms per 128 bytes of K.  The
