@@ -18,6 +18,8 @@
 // with both exponents clamped at 85 nats.  Operand precision: the intra-chunk
 // products and U, P, Kd, Delta are tf32 (fp32 accumulate); W and Qg are stored
 // in bf16 and multiply a bf16 copy of the state; the state itself is fp32.
+#include <type_traits>
+
 #include "kda_common.cuh"
 #include "kda_tma.cuh"
 
@@ -249,8 +251,9 @@ __device__ __forceinline__ void stg_hint_v4(void *p, uint4 v, uint64_t pol) {
 
 // tf32 hi / lo split of an fp32 value: x ~ hi + lo with about 21 significant bits
 __device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = tf32_bits(x);
-    lo = tf32_bits(x - __uint_as_float(hi));
+    const float h = tf32_rn(x);
+    hi = __float_as_uint(h);
+    lo = tf32_rn_bits(x - h);
 }
 // One warp: D (16 x 8) += X (16 x 8 KS, row-major, stride xs) . Y (8 KS x 8, row-major, stride ys)
 // with mma.sync m16n8k8 tf32 and the three-term split (hi*lo + lo*hi + hi*hi).
@@ -333,8 +336,21 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         roff[i] = raw_pair_off(r, pp);
         ooff[i] = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((pp >> 1) ^ (r & 7))) << 4) + 8 * (pp & 1));
     }
-    // H versions (column operand times the block decay between the pair): rows 64 + 16 v + (r % 16) of COLS
-    const uint32_t hoff = (uint32_t)(((r0 & 15) >> 3) * 1024);   // + 1 KiB per 8 rows inside the 16-row version
+    // H versions (column operand times the block decay between the pair): rows 64 + 16 v + (r % 16) of COLS;
+    // Kg / Qg (bf16, 64-channel atoms of 128-byte rows): element (row r, channel cp) of the slice's half-atom;
+    // Kd^T (tf32, rows = channels, 128-byte rows of 32 columns): the 16-byte unit of rows r0 .. r0 + 3
+    uint32_t hoo[4], kgo[4], kdo[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + i;
+        hoo[i] = (ooff[i] & 1023u) + (uint32_t)(((r0 & 15) >> 3) * 1024);
+        kgo[i] = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((((pp >> 2) ^ (r & 7))) << 4) + 2 * (cp & 7));
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int k = cp + e;
+        kdo[e] = (uint32_t)((k >> 3) * 1024 + (k & 7) * 128 + ((((seg & 7) ^ (k & 7))) << 4));
+    }
 
     // The description of the next item (chunk, head, A_log) is fetched while the
     // current one is processed, and its first two raw slices are issued as soon as
@@ -437,7 +453,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                 if (!wodd) *reinterpret_cast<float2 *>(xg + blk * SL + cp) = G[0];
             }
             // the previous slice's MMAs must be done with ROWS / COLS before they are rewritten
-            if (tid == 0 && sl > 0 && !mbar_spin(bar_ap, (uint32_t)(sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            if (tid == 0 && sl > 0 && !mbar_wait(bar_ap, (uint32_t)(sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
             __syncthreads();
             // block boundaries M_b = Gam at the end of block b - 1 (M_0 = 0, M_4 = Gam_C)
             float2 Mb, Mb1, Wlo;
@@ -486,63 +502,72 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             } else if (blk == 1) {
                 xa = make_float2(ex2(M3.x - M2.x), ex2(M3.y - M2.y));   // pair (3, 1)
             }
-            // 2c. operands of rows r0 .. r0 + 3
-            unsigned char *rows = sm + IS_ROWS;
-            unsigned char *cols = sm + IS_COLS;
-            float2 kdv[4];
+            // 2c. operands of rows r0 .. r0 + 3.  Offsets that depend on the slice: Kg / Qg images are
+            // 64-channel atoms (the slice's half of an atom flips unit bit 2, byte offset 64), Kd^T
+            // moves by 32 rows (4 KiB) per slice.
+            const uint32_t x64 = 64u * (uint32_t)(sl & 1);
+            unsigned char *const kgs = sm + IS_KG + 8192 * (sl >> 1);
+            unsigned char *const qgs = rec + REC_WQ + 16384 * (sl >> 1);
+            unsigned char *const kds = rec + REC_KDT + (r0 >> 5) * 16384 + 4096 * sl;
+            const float2 nhm = make_float2(-hm.x, -hm.y);
+            auto operands = [&](auto blkc) {
+                constexpr int BLK = decltype(blkc)::value;
+                unsigned char *const rows = sm + IS_ROWS;
+                unsigned char *const cols = sm + IS_COLS;
+                float2 kdv[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int r = r0 + i;
-                const float2 x = make_float2(wlo.x + (pre.x + G[i].x), wlo.y + (pre.y + G[i].y));
-                const float2 kv = make_float2(bf16_lo(kw[i]), bf16_hi(kw[i]));
-                const float2 qv = make_float2(bf16_lo(qw[i]), bf16_hi(qw[i]));
-                // block-relative factors (always <= 1, exact for any gate strength) and the diagonal
-                // block's midpoint factors (exponents clamped at 85 nats)
-                const float2 f = make_float2(ex2(x.x), ex2(x.y));
-                const float2 hf = make_float2(ex2(tot.x - x.x), ex2(tot.y - x.y));
-                const float2 dr = make_float2(ex2(fminf(x.x - hm.x, DIAG_CLAMP2)), ex2(fminf(x.y - hm.y, DIAG_CLAMP2)));
-                const float2 dc = make_float2(ex2(fminf(hm.x - x.x, DIAG_CLAMP2)), ex2(fminf(hm.y - x.y, DIAG_CLAMP2)));
-                const float2 fk = __fmul2_rn(kv, f), fq = __fmul2_rn(qv, f);
-                const float2 hk = __fmul2_rn(kv, hf);
-                *reinterpret_cast<float2 *>(rows + ooff[i]) = fk;
-                *reinterpret_cast<float2 *>(rows + 8192 + ooff[i]) = fq;
-                *reinterpret_cast<float2 *>(rows + 16384 + ooff[i]) = __fmul2_rn(kv, dr);
-                *reinterpret_cast<float2 *>(rows + 24576 + ooff[i]) = __fmul2_rn(qv, dr);
-                *reinterpret_cast<float2 *>(cols + ooff[i]) = __fmul2_rn(kv, dc);
-                // H versions: rows 64 + 16 v + r % 16 (v: pairs (1,0), (2,0), (2,1), (3,0), (3,1), (3,2))
-                const uint32_t ho = (ooff[i] & 1023u) + hoff;
-                if (blk == 0) {
-                    *reinterpret_cast<float2 *>(cols + 8 * 1024 + ho) = hk;
-                    *reinterpret_cast<float2 *>(cols + 10 * 1024 + ho) = __fmul2_rn(hk, xa);
-                    *reinterpret_cast<float2 *>(cols + 14 * 1024 + ho) = __fmul2_rn(hk, xb);
-                } else if (blk == 1) {
-                    *reinterpret_cast<float2 *>(cols + 12 * 1024 + ho) = hk;
-                    *reinterpret_cast<float2 *>(cols + 16 * 1024 + ho) = __fmul2_rn(hk, xa);
-                } else if (blk == 2) {
-                    *reinterpret_cast<float2 *>(cols + 18 * 1024 + ho) = hk;
+                for (int i = 0; i < 4; ++i) {
+                    const float2 x = __fadd2_rn(wlo, __fadd2_rn(pre, G[i]));
+                    const float2 nx = make_float2(-x.x, -x.y);
+                    const float2 kv = make_float2(bf16_lo(kw[i]), bf16_hi(kw[i]));
+                    const float2 qv = make_float2(bf16_lo(qw[i]), bf16_hi(qw[i]));
+                    // block-relative factors (always <= 1, exact for any gate strength) and the
+                    // diagonal block's midpoint factors (exponents clamped at 85 nats)
+                    const float2 ah = __fadd2_rn(tot, nx), ar = __fadd2_rn(x, nhm), ac = __fadd2_rn(hm, nx);
+                    const float2 f = make_float2(ex2(x.x), ex2(x.y));
+                    const float2 hf = make_float2(ex2(ah.x), ex2(ah.y));
+                    const float2 dr = make_float2(ex2(fminf(ar.x, DIAG_CLAMP2)), ex2(fminf(ar.y, DIAG_CLAMP2)));
+                    const float2 dc = make_float2(ex2(fminf(ac.x, DIAG_CLAMP2)), ex2(fminf(ac.y, DIAG_CLAMP2)));
+                    const float2 fk = __fmul2_rn(kv, f), fq = __fmul2_rn(qv, f);
+                    const float2 hk = __fmul2_rn(kv, hf);
+                    *reinterpret_cast<float2 *>(rows + ooff[i]) = fk;
+                    *reinterpret_cast<float2 *>(rows + 8192 + ooff[i]) = fq;
+                    *reinterpret_cast<float2 *>(rows + 16384 + ooff[i]) = __fmul2_rn(kv, dr);
+                    *reinterpret_cast<float2 *>(rows + 24576 + ooff[i]) = __fmul2_rn(qv, dr);
+                    *reinterpret_cast<float2 *>(cols + ooff[i]) = __fmul2_rn(kv, dc);
+                    // H versions: rows 64 + 16 v + r % 16 (v: pairs (1,0), (2,0), (2,1), (3,0), (3,1), (3,2))
+                    if (BLK == 0) {
+                        *reinterpret_cast<float2 *>(cols + 8 * 1024 + hoo[i]) = hk;
+                        *reinterpret_cast<float2 *>(cols + 10 * 1024 + hoo[i]) = __fmul2_rn(hk, xa);
+                        *reinterpret_cast<float2 *>(cols + 14 * 1024 + hoo[i]) = __fmul2_rn(hk, xb);
+                    } else if (BLK == 1) {
+                        *reinterpret_cast<float2 *>(cols + 12 * 1024 + hoo[i]) = hk;
+                        *reinterpret_cast<float2 *>(cols + 16 * 1024 + hoo[i]) = __fmul2_rn(hk, xa);
+                    } else if (BLK == 2) {
+                        *reinterpret_cast<float2 *>(cols + 18 * 1024 + hoo[i]) = hk;
+                    }
+                    kdv[i] = __fmul2_rn(hk, ea);
+                    // Kg (bf16) into the MN-major B operand of the W MMA (element (k = c0 + cp, j = r)),
+                    // Qg (bf16) straight into rows 0..63 of the record's WQ image
+                    const float2 kg = __fmul2_rn(fk, eb), qg = __fmul2_rn(fq, eb);
+                    *reinterpret_cast<uint32_t *>(kgs + (kgo[i] ^ x64)) = pack_bf16x2(kg.x, kg.y);
+                    stg_hint_b32(qgs + (kgo[i] ^ x64), pack_bf16x2(qg.x, qg.y), pol_ef);
+                    // partial row sums of q.q, k.k, q.k over this thread's two channels
+                    nq[i] = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, nq[i]));
+                    nk[i] = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, nk[i]));
+                    nqk[i] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, nqk[i]));
                 }
-                kdv[i] = __fmul2_rn(hk, ea);
-                // Kg (bf16) into the MN-major B operand of the W MMA: element (k = c0 + cp, j = r)
-                const float2 kg = __fmul2_rn(fk, eb), qg = __fmul2_rn(fq, eb);
-                *reinterpret_cast<uint32_t *>(sm + IS_KG + mn_off_bf16(c0 + cp, r)) = pack_bf16x2(kg.x, kg.y);
-                // Qg (bf16) straight into rows 0..63 of the record's WQ image
-                stg_hint_b32(rec + REC_WQ + sw128_off(r, 2 * (c0 + cp), 2 * CH), pack_bf16x2(qg.x, qg.y), pol_ef);
-                // partial row sums of q.q, k.k, q.k over this thread's two channels
-                nq[i] = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, nq[i]));
-                nk[i] = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, nk[i]));
-                nqk[i] = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, nqk[i]));
-            }
-            // Kd^T rows k = c0 + cp, c0 + cp + 1, columns r0 .. r0 + 3: one 16-byte unit each (tf32)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int k = c0 + cp + e;
-                const uint4 u = e == 0 ? make_uint4(tf32_bits(kdv[0].x), tf32_bits(kdv[1].x), tf32_bits(kdv[2].x),
-                                                    tf32_bits(kdv[3].x))
-                                       : make_uint4(tf32_bits(kdv[0].y), tf32_bits(kdv[1].y), tf32_bits(kdv[2].y),
-                                                    tf32_bits(kdv[3].y));
-                stg_hint_v4(rec + REC_KDT + (r0 >> 5) * 16384 + (k >> 3) * 1024 + (k & 7) * 128 +
-                                ((((seg & 7) ^ (k & 7))) << 4),
-                            u, pol_ef);
+                // Kd^T rows k = c0 + cp, c0 + cp + 1, columns r0 .. r0 + 3: one 16-byte unit each (tf32)
+                stg_hint_v4(kds + kdo[0], make_uint4(tf32_rn_bits(kdv[0].x), tf32_rn_bits(kdv[1].x),
+                                                     tf32_rn_bits(kdv[2].x), tf32_rn_bits(kdv[3].x)), pol_ef);
+                stg_hint_v4(kds + kdo[1], make_uint4(tf32_rn_bits(kdv[0].y), tf32_rn_bits(kdv[1].y),
+                                                     tf32_rn_bits(kdv[2].y), tf32_rn_bits(kdv[3].y)), pol_ef);
+            };
+            switch (blk) {
+                case 0: operands(std::integral_constant<int, 0>{}); break;
+                case 1: operands(std::integral_constant<int, 1>{}); break;
+                case 2: operands(std::integral_constant<int, 2>{}); break;
+                default: operands(std::integral_constant<int, 3>{}); break;
             }
             fence_async_smem();
             tc_fence_before();
@@ -574,7 +599,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             }
         }
         // the last slice's MMAs (and so TMEM) complete before the epilogue
-        if (tid == 0 && !mbar_spin(bar_ap, 1u)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+        if (tid == 0 && !mbar_wait(bar_ap, 1u)) set_status(KDA_ERR_DEVICE_TIMEOUT);
         // row norms: the 16 lanes of a half-warp hold the partial sums of the same four rows over
         // disjoint channel pairs; a reduce-scatter leaves the total of (row r0 + L / 4, quantity L % 4)
         // in lane L of the half.  rq = scale / |q|, rk = 1 / |k|; QK keeps the raw q.k (the P diagonal
@@ -819,7 +844,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                     umma_bf16(t_u, umma_desc(sbase + IS_V + ks * 2048, 8192, 1024), tp, id_u, acc);
                 }
             umma_commit(bar_wu);
-            if (!mbar_spin(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            if (!mbar_wait(bar_wu, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
             bulk_wait_read_all();   // the P image store is done reading before W / U staging reuses it
             // the raw buffers (V) are free: start the next item's first two slices
             if (has_next) {
@@ -1155,9 +1180,11 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                         const float4 ka = *reinterpret_cast<const float4 *>(rkr + jj);
                         const float4 kb = *reinterpret_cast<const float4 *>(rkr + jj + 4);
                         *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j, VB)) =
-                            make_uint4(tf32_bits(d0 * ka.x), tf32_bits(d1 * ka.y), tf32_bits(d2 * ka.z), tf32_bits(d3 * ka.w));
+                            make_uint4(tf32_rn_bits(d0 * ka.x), tf32_rn_bits(d1 * ka.y), tf32_rn_bits(d2 * ka.z),
+                                       tf32_rn_bits(d3 * ka.w));
                         *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j + 16, VB)) =
-                            make_uint4(tf32_bits(d4 * kb.x), tf32_bits(d5 * kb.y), tf32_bits(d6 * kb.z), tf32_bits(d7 * kb.w));
+                            make_uint4(tf32_rn_bits(d4 * kb.x), tf32_rn_bits(d5 * kb.y), tf32_rn_bits(d6 * kb.z),
+                                       tf32_rn_bits(d7 * kb.w));
                         *reinterpret_cast<uint4 *>(sm + SS_DTB + sw128_off(vme, 2 * j, VB)) =
                             make_uint4(pack_bf16x2(d0, d1), pack_bf16x2(d2, d3), pack_bf16x2(d4, d5),
                                        pack_bf16x2(d6, d7));
@@ -1517,9 +1544,9 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
                     const int k0 = c + 2 * e;
                     // Kd^T element (k, r) of the record: k / 8 = c / 8, k % 8 = 2 e (+1)
                     stg_hint_b32(kd_r + (k0 >> 3) * 1024 + (k0 & 7) * 128 + ((x4 ^ (k0 & 7)) << 4),
-                                 tf32_bits(bf16_lo(ka[e]) * ed), pol_ef);
+                                 tf32_rn_bits(bf16_lo(ka[e]) * ed), pol_ef);
                     stg_hint_b32(kd_r + (k0 >> 3) * 1024 + ((k0 + 1) & 7) * 128 + ((x4 ^ ((k0 + 1) & 7)) << 4),
-                                 tf32_bits(bf16_hi(ka[e]) * ed), pol_ef);
+                                 tf32_rn_bits(bf16_hi(ka[e]) * ed), pol_ef);
                 }
                 stg_hint_v4(rec + REC_WQ + sw128_off(r, 2 * c, 2 * CH), make_uint4(qg[0], qg[1], qg[2], qg[3]), pol_ef);
             }

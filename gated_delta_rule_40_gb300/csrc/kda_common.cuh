@@ -34,13 +34,13 @@ __device__ __forceinline__ float lg2(float x) {
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// Round an fp32 value to the nearest tf32 (ties away), returned as its bit pattern
-// (low 13 bits cleared).
-__device__ __forceinline__ uint32_t tf32_bits(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
+// A tf32 MMA operand rounded to nearest (ties away from zero), as an fp32 bit pattern.  The tensor
+// core reads only the upper 19 bits of a tf32 operand, so adding half a tf32 unit in the last place
+// (2^12 in the fp32 encoding) before that truncation rounds the magnitude to nearest, ties away from
+// zero, in one integer add.  Finite inputs (an infinity would become a NaN pattern).
+__device__ __forceinline__ uint32_t tf32_rn_bits(float x) { return __float_as_uint(x) + 0x1000u; }
+// The nearest tf32 number itself (the ignored bits cleared), for splitting x into tf32 hi + lo terms.
+__device__ __forceinline__ float tf32_rn(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ float bf16_to_f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
