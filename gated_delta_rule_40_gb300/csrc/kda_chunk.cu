@@ -19,6 +19,7 @@
 // products and U, P, Kd, Delta are tf32 (fp32 accumulate); W and Qg are stored
 // in bf16 and multiply a bf16 copy of the state; the state itself is fp32.
 #include <type_traits>
+#include <utility>
 
 #include "kda_common.cuh"
 #include "kda_tma.cuh"
@@ -40,6 +41,7 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
     __shared__ int s_carry;
     __shared__ int s_scan[PLAN_THREADS];
     __shared__ int s_len[LPT_MAX_SEQ];
+    grid_dep_launch();
     const int tid = threadIdx.x;
     const int nseq = cu ? N : B;
     if (tid == 0) {
@@ -284,6 +286,8 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                                                                           const IntraParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<1024>(smem_raw);
+    grid_dep_wait();     // the plan's tables
+    grid_dep_launch();   // the scan's CTAs may be placed as this kernel's CTAs retire
     if (p.hdr[1] == 0) return;
     const long long n_items = (long long)p.hdr[0] * p.Hw;
     if ((long long)blockIdx.x >= n_items) return;
@@ -971,6 +975,7 @@ enum { BAR_WQ0 = 0, BAR_WQ1, BAR_PK0, BAR_PK1, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MM
 __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<1024>(smem_raw);
+    grid_dep_wait();   // the chunk records of the intra-chunk kernel
     if (p.hdr[1] == 0) return;
     const int vb = blockIdx.x & 1;
     const int h = p.h0 + (blockIdx.x >> 1) % p.Hw;
@@ -1386,6 +1391,8 @@ struct GdnParams {
 __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(const GdnParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<1024>(smem_raw);
+    grid_dep_wait();
+    grid_dep_launch();
     if (p.hdr[1] == 0) return;
     const long long n_items = (long long)p.hdr[0] * p.H_v;
     if ((long long)blockIdx.x >= n_items) return;
@@ -1693,6 +1700,24 @@ struct FwdWorkspace {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled while the previous
+// kernel on the stream runs, and waits for it with grid_dep_wait() before touching its results.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                    Args &&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 void timing_begin(cudaStream_t s);
 void timing_mark(const char *name, cudaStream_t s);
 
@@ -1776,11 +1801,11 @@ static cudaError_t launch_fwd_impl(const uint16_t *q, const uint16_t *k, const u
         const long long items = nck * (long long)Hw;
         const long long slots = (long long)nsm * IN_CTAS_PER_SM;   // persistent: two CTAs per SM
         const unsigned grid = (unsigned)(items < slots ? items : slots);
-        intra_kernel<<<grid, IN_THREADS, IS_BYTES, stream>>>(mq, mk, mg, mv, ip);
+        if ((e = launch_dependent(intra_kernel, dim3(grid), dim3(IN_THREADS), IS_BYTES, stream, mq, mk, mg, mv, ip)) !=
+            cudaSuccess)
+            return e;
         ++*launches;
         timing_mark("intra_kernel", stream);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
     }
     if (nseq > 0) {
         ScanParams sp;
@@ -1789,11 +1814,11 @@ static cudaError_t launch_fwd_impl(const uint16_t *q, const uint16_t *k, const u
         sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = h0; sp.Hw = Hw;
         sp.state_bf16 = state_bf16 ? 1 : 0;
         const long long nblk = (long long)nseq * Hw * 2;
-        scan_kernel<<<(unsigned)nblk, SC_THREADS, SS_BYTES, stream>>>(sp);
+        if ((e = launch_dependent(scan_kernel, dim3((unsigned)nblk), dim3(SC_THREADS), SS_BYTES, stream, sp)) !=
+            cudaSuccess)
+            return e;
         ++*launches;
         timing_mark("scan_kernel", stream);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
@@ -1827,10 +1852,11 @@ cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const u
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
         const long long items = nck * (long long)H_v, slots = (long long)nsm * IN_CTAS_PER_SM;
-        intra_gdn_kernel<<<(unsigned)(items < slots ? items : slots), IN_THREADS, GD_BYTES, stream>>>(gp);
+        if ((e = launch_dependent(intra_gdn_kernel, dim3((unsigned)(items < slots ? items : slots)), dim3(IN_THREADS),
+                                  GD_BYTES, stream, gp)) != cudaSuccess)
+            return e;
         ++*launches;
         timing_mark("intra_gdn_kernel", stream);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (nseq > 0) {
         ScanParams sp;
@@ -1838,10 +1864,11 @@ cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const u
         sp.seqs = ws.seqs; sp.order = ws.order; sp.hdr = ws.hdr;
         sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = 0; sp.Hw = H_v;
         sp.state_bf16 = 0;
-        scan_kernel<<<(unsigned)((long long)nseq * H_v * 2), SC_THREADS, SS_BYTES, stream>>>(sp);
+        if ((e = launch_dependent(scan_kernel, dim3((unsigned)((long long)nseq * H_v * 2)), dim3(SC_THREADS),
+                                  SS_BYTES, stream, sp)) != cudaSuccess)
+            return e;
         ++*launches;
         timing_mark("scan_kernel", stream);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

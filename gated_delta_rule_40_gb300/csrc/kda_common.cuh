@@ -230,6 +230,16 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 }  // namespace kda
 
 namespace kda {
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation may
+// start while the previous kernel on the stream is still running; grid_dep_wait() blocks until
+// that kernel has completed and its memory is visible (it returns at once when the kernel was
+// launched normally), and grid_dep_launch() lets the next kernel on the stream be scheduled
+// early.  Nothing spins on memory: the dependency is resolved by the launch hardware.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+}  // namespace kda
+
+namespace kda {
 // Prefetch the 128-byte line holding p into L2.
 __device__ __forceinline__ void prefetch_line_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
