@@ -99,15 +99,29 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
         }
         return;
     }
-    for (int i = tid; i < nseq; i += PLAN_THREADS) {
-        const SeqDesc sd = seqs[i];
-        for (int c = 0; c < sd.nchunk; ++c) {
+    if (!cu) {
+        // B sequences of T tokens: chunk g is chunk g % nc of sequence g / nc (all threads)
+        const int nc = (int)(((long long)T + CH - 1) / CH);
+        for (int g = tid; g < total; g += PLAN_THREADS) {
+            const int i = g / nc, c = g - i * nc;
             ChunkDesc cd;
             cd.seq = i;
-            cd.tok = sd.tok + c * CH;
-            cd.len = min(CH, sd.len - c * CH);
+            cd.tok = i * T + c * CH;
+            cd.len = min(CH, T - c * CH);
             cd.idx = c;
-            chunks[sd.chunk0 + c] = cd;
+            chunks[g] = cd;
+        }
+    } else {
+        for (int i = tid; i < nseq; i += PLAN_THREADS) {
+            const SeqDesc sd = seqs[i];
+            for (int c = 0; c < sd.nchunk; ++c) {
+                ChunkDesc cd;
+                cd.seq = i;
+                cd.tok = sd.tok + c * CH;
+                cd.len = min(CH, sd.len - c * CH);
+                cd.idx = c;
+                chunks[sd.chunk0 + c] = cd;
+            }
         }
     }
     if (nseq <= LPT_MAX_SEQ) {
