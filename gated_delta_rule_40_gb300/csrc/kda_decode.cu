@@ -123,6 +123,22 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
     const int hq = h / (H_v / H_qk);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
+    // ---- the warp's 16 state rows, requested first so that their latency overlaps the token
+    //      preparation below (fp32 in registers; a bf16 state is widened after the loads land)
+    const int r0 = warp * DEC_ROWS;
+    const size_t st0 = ((size_t)bh * KD + r0) * KD;
+    float4 s[DEC_ROWS];
+    uint2 sw[BF16_STATE ? DEC_ROWS : 1];
+    if (BF16_STATE) {
+        const uint16_t *S = reinterpret_cast<const uint16_t *>(state) + st0;
+#pragma unroll
+        for (int i = 0; i < DEC_ROWS; ++i) sw[i] = __ldcs(reinterpret_cast<const uint2 *>(S + (size_t)i * KD) + lane);
+    } else {
+        const float *S = reinterpret_cast<const float *>(state) + st0;
+#pragma unroll
+        for (int i = 0; i < DEC_ROWS; ++i) s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)i * KD) + lane);
+    }
+
     // ---- token preparation: warp t handles token t; lane owns channels 4 lane .. 4 lane + 3
     if (warp < Tq) {
         const int t = warp;
@@ -163,22 +179,10 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
         }
     }
     __syncthreads();
-
-    // ---- the warp's 16 state rows, fp32 in registers
-    const int r0 = warp * DEC_ROWS;
-    const size_t st0 = ((size_t)bh * KD + r0) * KD;
-    float4 s[DEC_ROWS];
     if (BF16_STATE) {
-        const uint16_t *S = reinterpret_cast<const uint16_t *>(state) + st0;
 #pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i) {
-            const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(S + (size_t)i * KD) + lane);
-            s[i] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-        }
-    } else {
-        const float *S = reinterpret_cast<const float *>(state) + st0;
-#pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i) s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)i * KD) + lane);
+        for (int i = 0; i < DEC_ROWS; ++i)
+            s[i] = make_float4(bf16_lo(sw[i].x), bf16_hi(sw[i].x), bf16_lo(sw[i].y), bf16_hi(sw[i].y));
     }
     for (int t = 0; t < Tq; ++t) {
         const float4 dec = *reinterpret_cast<const float4 *>(&s_dec[t][4 * lane]);
