@@ -28,7 +28,10 @@ cudaError_t launch_fwd_heads(const uint16_t *q, const uint16_t *k, const uint16_
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kPieces = 4;
+// At most kMaxPieces pieces of at least kMinPieceTokens tokens each: more pieces shorten the
+// exposed tail (the last piece's kernels and output copy) at the price of more launches.
+constexpr int kMaxPieces = 16;
+constexpr long long kMinPieceTokens = 2048;
 std::mutex g_stream_mutex;
 cudaStream_t g_h2d[kMaxDevices] = {nullptr}, g_d2h[kMaxDevices] = {nullptr};
 
@@ -73,7 +76,8 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
         if (cu[i + 1] < cu[i]) return KDA_ERR_BAD_SEQLENS;
 
     // pieces [t0, t1): about tokens / P each, cut at a chunk boundary of the sequence they fall in
-    const int P = tokens >= (long long)kPieces * 4096 ? kPieces : 1;
+    const long long pmax = tokens / kMinPieceTokens;
+    const int P = pmax < 1 ? 1 : (pmax > kMaxPieces ? kMaxPieces : (int)pmax);
     std::vector<int> cuts = {0};
     for (int p = 1; p < P; ++p) {
         const long long target = tokens * p / P;
