@@ -5,6 +5,7 @@
     python -m gated_delta_rule_40_gb300.profile_case --method bwd --B 1 --T 2048 --H 8 --iters 3
     python -m gated_delta_rule_40_gb300.profile_case --method bwd --B 2 --T 16384 --H 32 --iters 2 --kernel-times
     python -m gated_delta_rule_40_gb300.profile_case --method la_decode --B 256 --H 64 --iters 4
+    python -m gated_delta_rule_40_gb300.profile_case --method decode --B 256 --H 64 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method gdn --B 1 --T 8192 --H 32 --iters 4
     python -m gated_delta_rule_40_gb300.profile_case --method decode_tokens --B 256 --T 4 --H 64 --iters 4
 
@@ -14,7 +15,7 @@ kernel launches of ``kda_fwd`` (three for ``kda_fwd_scalar_gate``: plan, intra_g
 and scan_kernel; two for ``kda_la_fwd``: plan and la_fwd_kernel; three for ``kda_bwd``:
 plan, bwd_recur_kernel and bwd_prologue_kernel; one for ``kda_decode_tokens``, whose
 ``--T`` is the token count Tq of the step and whose state is fp32 unless
-``--bf16-state``).  A profiler then selects launches by kernel name and index (e.g.
+``--bf16-state``; one for ``kda_decode_step``).  A profiler then selects launches by kernel name and index (e.g.
 ``ncu -k regex:intra_kernel -s 2 -c 1``).  ``--kernel-times`` (kda and bwd) times the
 last iteration's kernels with the library's CUDA events instead and prints them.
 """
@@ -36,7 +37,8 @@ def main() -> None:
     ap.add_argument("--H", type=int, default=32, help="value heads (= q/k heads)")
     ap.add_argument("--iters", type=int, default=4)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--method", choices=["kda", "gdn", "la", "bwd", "la_decode", "decode_tokens"], default="kda")
+    ap.add_argument("--method", choices=["kda", "gdn", "la", "bwd", "la_decode", "decode_tokens", "decode"],
+                    default="kda")
     ap.add_argument("--bf16-state", action="store_true", help="decode_tokens: bf16 state")
     ap.add_argument("--kernel-times", action="store_true",
                     help="time the last iteration's kernels with the library's events and print them")
@@ -59,6 +61,14 @@ def main() -> None:
         torch.cuda.synchronize()
         print(f"kda_decode_tokens B={a.B} Tq={a.T} H={a.H} state {st.dtype} x{a.iters}: "
               f"|o| {float(o.float().abs().mean()):.6f}")
+        return
+    if a.method == "decode":
+        d = kda_inputs.decode_inputs(B=a.B, H=a.H, seed=a.seed)
+        q, k, v, gr, b, A, st = (t.cuda() for t in (d.q, d.k, d.v, d.graw, d.b, d.A_log, d.state))
+        for _ in range(a.iters):
+            o = kda.kda_decode_step(q, k, v, gr, b, A, d.scale, st)
+        torch.cuda.synchronize()
+        print(f"kda_decode_step B={a.B} H={a.H} x{a.iters}: |o| {float(o.float().abs().mean()):.6f}")
         return
     if a.method == "la_decode":
         d = kda_inputs.la_decode_inputs(B=a.B, H=a.H, seed=a.seed)
