@@ -1,39 +1,40 @@
-// KDA backward: gradients of the forward with respect to q, k, v, graw, b,
-// A_log and the initial state, given the gradients of the outputs (do) and of
+// KDA backward in the chunk (UT / WY) form: gradients of the forward with respect to q, k,
+// v, graw, b, A_log and the initial state, given the gradients of the outputs (do) and of
 // the final states (dht).
 //
-// Per sequence and value head, token t (qt, kh normalised, e = exp(g), beta):
-//   S' = S_{t-1} Diag(e),  d = S' kh,  delta = beta (v - d),  S_t = S' + delta kh^T,  o = S_t qt
-// and, walking t backwards with dS = dL/dS_t (rows v of the state are
-// independent in both directions; only the per-token parameter gradients sum
-// over v):
-//   dS   += do qt^T                     dqt  = S_t^T do
-//   ddel  = dS kh                       dkh  = dS^T delta + S'^T dd,   dd = -beta ddel
-//   dv    = beta ddel                   dbeta = ddel . (v - d)
-//   dS'   = dS + dd kh^T                de    = colsum(S_{t-1} * dS')
-//   dS_{t-1} = dS' Diag(e)
-// then the prologue's Jacobians map dqt, dkh, de, dbeta to dq, dk, dgraw,
-// dA_log, db (dq and dk sum over the value heads of a query/key group).
+// Per chunk of C = 64 rows (S_0 the state entering it; Gam the inclusive in-chunk prefix sum
+// of g = -exp(A_log) softplus(graw), per channel; Gam_C its last row; Kh, Qt the normalised
+// keys and scaled queries; beta = sigmoid(b)):
+//   Kg = Kh e^Gam,  Qg = Qt e^Gam,  Kd = Kh e^(Gam_C - Gam)
+//   A = strict_lower(diag(beta) Kh Kh^T with pair decays e^(Gam_r - Gam_j)),  T = (I + A)^-1
+//   P = lower(Qt Kh^T with the same decays)
+//   W = T diag(beta) Kg,  U = T diag(beta) V,  Delta = U - W S_0^T
+//   O = Qg S_0^T + P Delta,   S_C = S_0 Diag(e^Gam_C) + Delta^T Kd
+// and its backward, given dO and dS_C (the gradient of the state leaving the chunk):
+//   dDelta = P^T dO + Kd dS_C^T        dKd = Delta dS_C     dQg = dO S_0     dW = -dDelta S_0
+//   dS_0   = dS_C Diag(e^Gam_C) - (Kd dS_C^T)^T W + dO^T (Qg - P W)
+//   dP = lower(dO Delta^T),  dT = dDelta (beta V)^T + dW (beta Kg)^T,  dA = strict_lower(-T^T dT T^T)
+// then the products A, P, W, U and the decayed copies pass their gradients to Kh, Qt, V,
+// beta and Gam (the pair products per 16-row sub-block pair, against the sub-block's
+// reference point as the forward builds A and P), and dg_s = sum_{r >= s} dGam_r + dGam_C
+// terms + the exclusive prefix sum of dKd * Kd (Kd_r depends on g_s for s > r only).
 //
-// bwd_recur_kernel: persistent CTAs of 8 warps, two per SM, one (sequence,
-// value head, quarter of the state rows) item at a time: the 128 rows of a
-// chain are independent, so four CTAs share a chain.  Warp w owns rows
-// 4w .. 4w + 3 of the quarter, lane owns channels 4 lane .. 4 lane + 3, so S and
-// dS live in registers (16 values each).  A first pass runs the recurrence and
-// stores the state at every 16-token block start; the backward pass then takes
-// the blocks in reverse: it recomputes the block's states from its checkpoint
-// into a per-CTA scratch area (256 KiB; each thread reads back only what it
-// wrote; the scratch of all resident CTAs stays within L2), then walks the
-// block's tokens backwards.  The per-token vectors (qt,
-// kh, e, v, do, beta) of a block are staged in shared memory; the sums over the
-// quarter's rows of dqt, dkh, de and dbeta are reduced across warps through
-// shared memory (one barrier per token, alternating areas) and written per
-// (token, head, quarter) for bwd_prologue_kernel, which adds the quarters and the
-// value heads of a group.  The per-row dot products of a warp's four rows use one
-// four-value warp reduce-scatter.  This is the token recurrence on CUDA cores in
-// fp32, a correct first form; its cost is O(T K V) per chain with no tensor-core
-// use.
+// Kernels (one "item" is a (chunk, value head) pair):
+//   bwdc_prep_kernel     per item: the chunk's rows, A and P, T, W, U, Kd and N = Qg - P W
+//                        (the operands of both state chains and of the gradient kernels)
+//   bwdc_chain_kernel    per (sequence, value head, 64-row V block), chunks in order: the
+//                        state entering every chunk (forward) or, chunks in reverse, the
+//                        state gradient leaving every chunk (backward); dh0
+//   bwdc_gradv_kernel    per (item, V half): the products that contract over the value
+//                        dimension (Delta, dDelta, dKd, dQg, dW, dP, dT's V term), dv
+//   bwdc_gradk_kernel    per item: dT, dA, the decayed pair products, dGam and dg
+//   bwdc_jacobian_kernel per (query/key head, 64 tokens): the norms', gate's and sigmoid's
+//                        Jacobians (dq and dk sum over the value heads of a group)
+// Every product runs on the tensor cores (mma.sync m16n8k8, tf32 operands rounded to
+// nearest, fp32 accumulation) from fp32 tiles in shared memory; the state chains keep the
+// state in fp32 and apply the per-channel decay in fp32 outside the products.
 #include "kda_common.cuh"
+#include "kda_invert.cuh"
 
 namespace kda {
 
@@ -42,294 +43,1010 @@ cudaError_t launch_plan(const int32_t *cu, int N, int B, int T, SeqDesc *seqs, C
 long long max_chunks_for(int N, int B, int T, bool varlen);
 void timing_mark(const char *name, cudaStream_t s);
 
-constexpr int BW_WARPS = 8;
-constexpr int BW_THREADS = BW_WARPS * 32;
-constexpr int BW_PARTS = 4;                            // CTAs per chain
-constexpr int BW_ROWS = KD / BW_PARTS / BW_WARPS;      // 4 state rows per warp
-constexpr int BW_CT = 16;                              // tokens per block (checkpoint interval)
-constexpr int BW_BPC = CH / BW_CT;                     // blocks per 64-token chunk
-static_assert(CH % BW_CT == 0, "blocks tile a chunk");
-constexpr uint32_t BW_VEC = BW_CT * KD * 4;            // one [BW_CT][128] fp32 table
-constexpr uint32_t BW_QT = 0, BW_KH = BW_VEC, BW_E = 2 * BW_VEC, BW_V = 3 * BW_VEC, BW_DO = 4 * BW_VEC;
-constexpr uint32_t BW_BETA = 5 * BW_VEC;            // [BW_CT]
-constexpr uint32_t BW_RED = BW_BETA + 128;          // 2 x [8 warps][3][128] (alternating tokens)
-constexpr uint32_t BW_REDB = BW_RED + 2 * BW_WARPS * 3 * KD * 4;   // 2 x [8]
-constexpr uint32_t BW_BYTES = BW_REDB + 64;
-static_assert(2 * (BW_BYTES + 128 + 1024) <= 228 * 1024, "two backward CTAs per SM");
+// ---------------------------------------------------------------- fp32 tiles
+// A tile holds rows x W fp32 (W = 64 or 128) densely, with the 16-byte units of row r
+// permuted: unit u sits at u ^ s(r), s(r) = 2 (r & 3) + ((r >> 2) & 1).  The two fragment
+// shapes of mma.sync (eight rows x four consecutive columns, four rows x eight consecutive
+// columns) then touch 32 distinct banks, and a tile moves between global and shared memory
+// as one contiguous block.
+template <int W>
+__device__ __forceinline__ int toff(int r, int c) {
+    return r * W + ((((c >> 2) ^ (((r & 3) << 1) | ((r >> 2) & 1)))) << 2) + (c & 3);
+}
 
-struct BwdParams {
+// acc (16 TM x 8 TN at (m0, n0)) += A (m0.., k) B (k, n0..) for k in [k0, k1), fa / fb return
+// fp32 values, rounded to the nearest tf32 on the way in.
+template <int TM, int TN, class FA, class FB>
+__device__ __forceinline__ void mma_tile(float (&acc)[TM][TN][4], int m0, int n0, int k0, int k1, FA fa, FB fb,
+                                         int g, int t) {
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 8) {
+        uint32_t a[TM][4], b[TN][2];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int m = m0 + 16 * i + g;
+            a[i][0] = tf32_rn_bits(fa(m, k + t));
+            a[i][1] = tf32_rn_bits(fa(m + 8, k + t));
+            a[i][2] = tf32_rn_bits(fa(m, k + t + 4));
+            a[i][3] = tf32_rn_bits(fa(m + 8, k + t + 4));
+        }
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int n = n0 + 8 * j + g;
+            b[j][0] = tf32_rn_bits(fb(k + t, n));
+            b[j][1] = tf32_rn_bits(fb(k + t + 4, n));
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) mma_tf32(acc[i][j], a[i], b[j]);
+    }
+}
+// fe(row, col, v[col], v[col + 1]) for every accumulator pair of the tile (col even)
+template <int TM, int TN, class FE>
+__device__ __forceinline__ void tile_out(const float (&acc)[TM][TN][4], int m0, int n0, int g, int t, FE fe) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) {
+            const int r = m0 + 16 * i + g, c = n0 + 8 * j + 2 * t;
+            fe(r, c, acc[i][j][0], acc[i][j][1]);
+            fe(r + 8, c, acc[i][j][2], acc[i][j][3]);
+        }
+}
+template <int TM, int TN>
+__device__ __forceinline__ void tile_zero(float (&acc)[TM][TN][4]) {
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
+}
+// C (M x N) = sum over k in [0, K) of A B, the 16 TM x 8 TN output tiles dealt to the warps in turn.
+template <int M, int N, int TM, int TN, int NW, class FA, class FB, class FE>
+__device__ __forceinline__ void cta_gemm(int K, FA fa, FB fb, FE fe, int warp, int lane) {
+    constexpr int TNS = N / (8 * TN), TMS = M / (16 * TM);
+    static_assert(TNS * 8 * TN == N && TMS * 16 * TM == M, "tiles cover the product");
+    const int g = lane >> 2, t = lane & 3;
+    for (int tile = warp; tile < TMS * TNS; tile += NW) {
+        const int m0 = (tile / TNS) * 16 * TM, n0 = (tile % TNS) * 8 * TN;
+        float acc[TM][TN][4];
+        tile_zero(acc);
+        mma_tile<TM, TN>(acc, m0, n0, 0, K, fa, fb, g, t);
+        tile_out<TM, TN>(acc, m0, n0, g, t, fe);
+    }
+}
+
+__device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src_smem),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void st2(float *p, float a, float b) { *reinterpret_cast<float2 *>(p) = make_float2(a, b); }
+__device__ __forceinline__ float ex2n(float x) { return ex2(x * LOG2E); }   // e^x
+
+// ---------------------------------------------------------------- workspace records
+// Per item, written by the prep kernel (fp32 tiles):
+//   W, Kd, N = Qg - P W  [64 rows][128];  U as two [64 rows][64 v] halves;  P, T, KK [64][64]
+//   (KK = the key products of A before the beta scaling);  D = e^Gam_C [128];  beta [64]
+constexpr uint32_t BR_W = 0, BR_KD = 32768, BR_N = 65536, BR_U = 98304, BR_P = 131072, BR_T = 147456,
+                   BR_KK = 163840, BR_D = 180224, BR_BETA = 180736, BR_BYTES = 181248;
+constexpr uint32_t ST_BYTES = 65536;   // a state per item: [2 V blocks][64 v][128 k] fp32 tiles
+// Per (item, V half), written by bwdc_gradv_kernel (sums over that half's 64 value columns):
+//   dKd, dQg, dW [64][128];  dP (lower), dT's V term [64][64];  dbeta's V term [64];  colsum(S_0 dS_C) [128]
+constexpr uint32_t CP_DKD = 0, CP_DQG = 32768, CP_DW = 65536, CP_DP = 98304, CP_DT = 114688, CP_DB = 131072,
+                   CP_DGC = 131328, CP_BYTES = 131840;
+
+struct BwdcParams {
     const uint16_t *q, *k, *v, *graw, *b, *dout;
     const float *A_log, *init, *dht;
     float scale;
     int H_qk, H_v, nseq;
     const SeqDesc *seqs;
+    const ChunkDesc *chunks;
     const int *order;
     const int *hdr;
-    float *ckpt;      // [BW_BPC chunk + block][H_v][V][K]
-    float *scratch;   // [gridDim.x][BW_CT][32 rows][K]
-    float *dqt, *dkh, *de, *dbeta;   // [token][H_v][part][128] (dbeta [token][H_v][part])
-    float *dv, *dh0;                 // [token][H_v][V], [N][H_v][V][K]
+    unsigned char *rec;     // [item] BR_BYTES
+    float *S0, *dSC;        // [item] ST_BYTES: state entering / state gradient leaving each chunk
+    unsigned char *part;    // [item][2] CP_BYTES
+    float *dqt, *dkh, *dg;  // [token][H_v][128]: gradients of Qt, Kh, g
+    float *dbeta;           // [token][H_v]
+    float *dv, *dh0;
 };
 
-// Per-token vectors of tokens tok0 .. tok0 + len - 1 into the shared tables; warp w takes tokens w, w + 8, ...
-__device__ __forceinline__ void bwd_stage_chunk(const BwdParams &p, unsigned char *sm, int tok0, int len, int h,
-                                                int hq, float a_gate, bool with_do, int warp, int lane) {
-    float *sqt = reinterpret_cast<float *>(sm + BW_QT), *skh = reinterpret_cast<float *>(sm + BW_KH);
-    float *se = reinterpret_cast<float *>(sm + BW_E), *sv = reinterpret_cast<float *>(sm + BW_V);
-    float *sdo = reinterpret_cast<float *>(sm + BW_DO), *sbeta = reinterpret_cast<float *>(sm + BW_BETA);
-    for (int r = warp; r < len; r += BW_WARPS) {
-        const size_t tok = (size_t)tok0 + r;
-        const size_t qo = (tok * p.H_qk + hq) * KD + 4 * lane, vo = (tok * p.H_v + h) * KD + 4 * lane;
-        const uint2 qw = *reinterpret_cast<const uint2 *>(p.q + qo), kw = *reinterpret_cast<const uint2 *>(p.k + qo);
-        const uint2 gw = *reinterpret_cast<const uint2 *>(p.graw + vo), vw = *reinterpret_cast<const uint2 *>(p.v + vo);
-        const float qv[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
-        const float kv[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
-        const float gv[4] = {bf16_lo(gw.x), bf16_hi(gw.x), bf16_lo(gw.y), bf16_hi(gw.y)};
-        const float vv[4] = {bf16_lo(vw.x), bf16_hi(vw.x), bf16_lo(vw.y), bf16_hi(vw.y)};
-        float sq = 0.f, sk = 0.f;
+constexpr int BC_THREADS = 256, BC_WARPS = 8;
+
+// The chunk's rows into shared memory: Kh = k / |k| and Qt = scale q / |q| (fp32 tiles),
+// Gam (fp32 tile; rows past len repeat the last valid row, their g being 0), beta = sigmoid(b)
+// (0 past len) and D = e^Gam_C.  All threads take part; returns synchronised.
+__device__ void bwdc_rows(const BwdcParams &p, int tok0, int len, int h, int hq, float a, float *sKh, float *sQt,
+                          float *sG, float *sBeta, float *sD, int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int r = warp; r < CH; r += BC_WARPS) {
+        float4 kh = make_float4(0.f, 0.f, 0.f, 0.f), qt = kh, gg = kh;
+        float beta = 0.f;
+        if (r < len) {
+            const size_t tok = (size_t)tok0 + r;
+            const size_t qo = (tok * p.H_qk + hq) * KD + 4 * lane, vo = (tok * p.H_v + h) * KD + 4 * lane;
+            const uint2 qw = *reinterpret_cast<const uint2 *>(p.q + qo), kw = *reinterpret_cast<const uint2 *>(p.k + qo);
+            const uint2 gw = *reinterpret_cast<const uint2 *>(p.graw + vo);
+            const float qv[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
+            const float kv[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
+            float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            sq = fmaf(qv[i], qv[i], sq);
-            sk = fmaf(kv[i], kv[i], sk);
+            for (int i = 0; i < 4; ++i) {
+                sq = fmaf(qv[i], qv[i], sq);
+                sk = fmaf(kv[i], kv[i], sk);
+            }
+            sq = warp_sum(sq);
+            sk = warp_sum(sk);
+            const float rq = p.scale * rsqrtf(sq + L2_EPS), rk = rsqrtf(sk + L2_EPS);
+            qt = make_float4(qv[0] * rq, qv[1] * rq, qv[2] * rq, qv[3] * rq);
+            kh = make_float4(kv[0] * rk, kv[1] * rk, kv[2] * rk, kv[3] * rk);
+            // g = -a softplus(graw), natural units
+            const float na = -a * (1.0f / LOG2E);
+            gg = make_float4(na * softplus_log2(bf16_lo(gw.x)), na * softplus_log2(bf16_hi(gw.x)),
+                             na * softplus_log2(bf16_lo(gw.y)), na * softplus_log2(bf16_hi(gw.y)));
+            beta = 1.0f / (1.0f + ex2(-bf16_to_f(p.b[tok * p.H_v + h]) * LOG2E));
         }
-        sq = warp_sum(sq);
-        sk = warp_sum(sk);
-        const float rq = p.scale * rsqrtf(sq + L2_EPS), rk = rsqrtf(sk + L2_EPS);
-        float4 a, bq, c, d;
-        a.x = qv[0] * rq; a.y = qv[1] * rq; a.z = qv[2] * rq; a.w = qv[3] * rq;
-        bq.x = kv[0] * rk; bq.y = kv[1] * rk; bq.z = kv[2] * rk; bq.w = kv[3] * rk;
-        c.x = ex2(-a_gate * softplus_log2(gv[0])); c.y = ex2(-a_gate * softplus_log2(gv[1]));
-        c.z = ex2(-a_gate * softplus_log2(gv[2])); c.w = ex2(-a_gate * softplus_log2(gv[3]));
-        d.x = vv[0]; d.y = vv[1]; d.z = vv[2]; d.w = vv[3];
-        reinterpret_cast<float4 *>(sqt + r * KD)[lane] = a;
-        reinterpret_cast<float4 *>(skh + r * KD)[lane] = bq;
-        reinterpret_cast<float4 *>(se + r * KD)[lane] = c;
-        reinterpret_cast<float4 *>(sv + r * KD)[lane] = d;
-        if (with_do) {
-            const uint2 ow = *reinterpret_cast<const uint2 *>(p.dout + vo);
-            reinterpret_cast<float4 *>(sdo + r * KD)[lane] =
-                make_float4(bf16_lo(ow.x), bf16_hi(ow.x), bf16_lo(ow.y), bf16_hi(ow.y));
+        const int o = toff<KD>(r, 4 * lane);
+        *reinterpret_cast<float4 *>(sKh + o) = kh;
+        *reinterpret_cast<float4 *>(sQt + o) = qt;
+        *reinterpret_cast<float4 *>(sG + o) = gg;
+        if (lane == 0) sBeta[r] = beta;
+    }
+    __syncthreads();
+    if (tid < KD) {
+        float s = 0.f;
+        for (int r = 0; r < CH; ++r) {
+            const int o = toff<KD>(r, tid);
+            s += sG[o];
+            sG[o] = s;
         }
-        if (lane == 0) {
-            const float bb = bf16_to_f(p.b[tok * p.H_v + h]);
-            sbeta[r] = 1.0f / (1.0f + ex2(-bb * LOG2E));
-        }
+        sD[tid] = ex2n(s);
     }
+    __syncthreads();
 }
 
-// Warp sums of four per-lane partials (one per state row), returned on every lane.  A
-// reduce-scatter (xor 16 keeps two rows, xor 8 one, xor 4, 2, 1 finish it) leaves lane l with
-// the sum of row 2 b4 + b3 (b = bits of l); four broadcasts return them: 10 shuffles instead
-// of 20 for four butterflies.
-__device__ __forceinline__ void warp_sum4(float (&a)[4], int lane) {
-    const bool u16 = (lane & 16) != 0, u8 = (lane & 8) != 0;
-    float b0 = u16 ? a[2] : a[0], b1 = u16 ? a[3] : a[1];
-    const float s0 = u16 ? a[0] : a[2], s1 = u16 ? a[1] : a[3];
-    b0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-    b1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-    float c = u8 ? b1 : b0;
-    c += __shfl_xor_sync(0xffffffffu, u8 ? b0 : b1, 8);
-    c += __shfl_xor_sync(0xffffffffu, c, 4);
-    c += __shfl_xor_sync(0xffffffffu, c, 2);
-    c += __shfl_xor_sync(0xffffffffu, c, 1);
-    a[0] = __shfl_sync(0xffffffffu, c, 0);
-    a[1] = __shfl_sync(0xffffffffu, c, 8);
-    a[2] = __shfl_sync(0xffffffffu, c, 16);
-    a[3] = __shfl_sync(0xffffffffu, c, 24);
-}
-static_assert(BW_ROWS == 4, "warp_sum4 reduces four rows");
-
-__device__ __forceinline__ float dot4(const float4 a, const float4 b) {
-    return a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-}
-
-// One forward token on this thread's 4 rows x 4 channels: S <- S Diag(e) + beta (v - S Diag(e) kh) kh^T.
-__device__ __forceinline__ void bwd_fwd_token(float4 (&S)[BW_ROWS], const float4 kh, const float4 e, float beta,
-                                              const float *vrow, int r0, int lane) {
-    float d[BW_ROWS];
-#pragma unroll
-    for (int i = 0; i < BW_ROWS; ++i) {
-        S[i].x *= e.x; S[i].y *= e.y; S[i].z *= e.z; S[i].w *= e.w;
-        d[i] = dot4(S[i], kh);
+// Decay factors of the sub-block pair (i, b), b <= i, for channel c: e^(Gam_r - Gam_j) =
+// rowf(r) colf(j) for r in block i, j in block b.  Below the diagonal the reference point is
+// Gam at the last row of block i - 1 (both factors <= 1); on it, the block's midpoint with
+// both exponents clamped at 85 nats (exact unless a channel decays by more than 170 nats
+// across the block).
+struct PairRef {
+    float ref;
+    bool diag;
+    __device__ __forceinline__ float rowf(float gam) const {
+        return diag ? ex2n(fminf(gam - ref, 85.0f)) : ex2n(gam - ref);
     }
-    warp_sum4(d, lane);
-#pragma unroll
-    for (int i = 0; i < BW_ROWS; ++i) {
-        const float del = beta * (vrow[r0 + i] - d[i]);
-        S[i].x = fmaf(del, kh.x, S[i].x); S[i].y = fmaf(del, kh.y, S[i].y);
-        S[i].z = fmaf(del, kh.z, S[i].z); S[i].w = fmaf(del, kh.w, S[i].w);
+    __device__ __forceinline__ float colf(float gam) const {
+        return diag ? ex2n(fminf(ref - gam, 85.0f)) : ex2n(ref - gam);
     }
+};
+__device__ __forceinline__ PairRef pair_ref(const float *sG, int i, int b, int c) {
+    PairRef pr;
+    pr.diag = (i == b);
+    pr.ref = pr.diag ? 0.5f * (sG[toff<KD>(16 * i, c)] + sG[toff<KD>(16 * i + 15, c)]) : sG[toff<KD>(16 * i - 1, c)];
+    return pr;
+}
+__device__ __forceinline__ void pair_of(int pr, int &i, int &b) {
+    // (0,0) (1,0) (1,1) (2,0) (2,1) (2,2) (3,0) (3,1) (3,2) (3,3)
+    i = pr < 1 ? 0 : pr < 3 ? 1 : pr < 6 ? 2 : 3;
+    b = pr - (i * (i + 1)) / 2;
 }
 
-__global__ __launch_bounds__(BW_THREADS, 2) void bwd_recur_kernel(const BwdParams p) {
+// =====================================================================
+// Prep: per item the chunk's rows, KK (A before beta) and P by sub-block pairs, T, W, U, Kd,
+// N; written to the item's record.  One item per CTA at a time.
+// =====================================================================
+constexpr uint32_t PS_KH = 0, PS_QT = 32768, PS_G = 65536, PS_W = 98304, PS_KK = 131072, PS_P = 147456,
+                   PS_A = 163840, PS_T = 181248, PS_X = 198656, PS_MISC = 203264, PS_BYTES = 204288;
+constexpr uint32_t PS_V = PS_QT;   // V (fp32 tile) once Qt is no longer read
+static_assert(PS_T == PS_A + CH * AS * 4 && PS_X == PS_T + CH * AS * 4 && PS_MISC >= PS_X + 32 * XS * 4,
+              "prep layout");
+
+__global__ __launch_bounds__(BC_THREADS, 1) void bwdc_prep_kernel(const BwdcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<128>(smem_raw);
     if (p.hdr[1] == 0) return;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float *sqt = reinterpret_cast<const float *>(sm + BW_QT), *skh = reinterpret_cast<const float *>(sm + BW_KH);
-    const float *se = reinterpret_cast<const float *>(sm + BW_E), *sv = reinterpret_cast<const float *>(sm + BW_V);
-    const float *sdo = reinterpret_cast<const float *>(sm + BW_DO), *sbeta = reinterpret_cast<const float *>(sm + BW_BETA);
-    float *red = reinterpret_cast<float *>(sm + BW_RED), *redb = reinterpret_cast<float *>(sm + BW_REDB);
-    float *scr = p.scratch + (size_t)blockIdx.x * BW_CT * (KD / BW_PARTS) * KD;
-    const int n_items = p.nseq * p.H_v * BW_PARTS;
+    float *sKh = reinterpret_cast<float *>(sm + PS_KH), *sQt = reinterpret_cast<float *>(sm + PS_QT);
+    float *sG = reinterpret_cast<float *>(sm + PS_G), *sW = reinterpret_cast<float *>(sm + PS_W);
+    float *sKK = reinterpret_cast<float *>(sm + PS_KK), *sP = reinterpret_cast<float *>(sm + PS_P);
+    float *sA = reinterpret_cast<float *>(sm + PS_A), *sT = reinterpret_cast<float *>(sm + PS_T);
+    float *sX = reinterpret_cast<float *>(sm + PS_X), *sV = reinterpret_cast<float *>(sm + PS_V);
+    float *sBeta = reinterpret_cast<float *>(sm + PS_MISC), *sD = sBeta + 64;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const long long n_items = (long long)p.hdr[0] * p.H_v;
     const int group = p.H_v / p.H_qk;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int h = (int)(item % p.H_v);
+        const ChunkDesc cd = p.chunks[item / p.H_v];
+        const int hq = h / group, len = cd.len;
+        const float a = ex2n(p.A_log[h]);
+        float *rec = reinterpret_cast<float *>(p.rec + (size_t)item * BR_BYTES);
+        __syncthreads();   // the previous item's reads of shared memory are done
+        bwdc_rows(p, cd.tok, len, h, hq, a, sKh, sQt, sG, sBeta, sD, tid);
 
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int part = item % BW_PARTS, h = (item / BW_PARTS) % p.H_v;
-        const int seq = p.order[item / (BW_PARTS * p.H_v)], hq = h / group;
-        const SeqDesc sd = p.seqs[seq];
-        const int nblk = (sd.len + BW_CT - 1) / BW_CT;
-        const float a_gate = ex2(p.A_log[h] * LOG2E);
-        // rows of this thread in the full [V][K] matrix, and their offset within the quarter
-        const int r0 = part * (KD / BW_PARTS) + warp * BW_ROWS, q0 = warp * BW_ROWS;
-        const size_t sh = ((size_t)seq * p.H_v + h) * KD * KD;
-        auto slice = [&](size_t base, int i) { return base + (size_t)(r0 + i) * KD + 4 * lane; };
-        auto sslice = [&](int r, int i) { return ((size_t)r * (KD / BW_PARTS) + q0 + i) * KD + 4 * lane; };
-        float4 S[BW_ROWS];
+        // ---- KK and P per sub-block pair (one warp per pair): 16 x 16, K = 128 channels
+        for (int pr = warp; pr < 10; pr += BC_WARPS) {
+            int i, b;
+            pair_of(pr, i, b);
+            float kk[2][4], pp[2][4];
 #pragma unroll
-        for (int i = 0; i < BW_ROWS; ++i)
-            S[i] = p.init ? *reinterpret_cast<const float4 *>(p.init + slice(sh, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-
-        // ---- pass 1: the recurrence, storing the state at each block start
-        for (int c = 0; c < nblk; ++c) {
-            const int len = min(BW_CT, sd.len - c * BW_CT), tok0 = sd.tok + c * BW_CT;
-            const size_t cb = ((size_t)(BW_BPC * sd.chunk0 + c) * p.H_v + h) * KD * KD;
+            for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(p.ckpt + slice(cb, i)) = S[i];
-            __syncthreads();   // the previous block's tables are no longer read
-            bwd_stage_chunk(p, sm, tok0, len, h, hq, a_gate, false, warp, lane);
-            __syncthreads();
-            for (int r = 0; r < len; ++r)
-                bwd_fwd_token(S, reinterpret_cast<const float4 *>(skh + r * KD)[lane],
-                              reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0, lane);
-        }
-
-        // ---- pass 2: blocks in reverse
-        float4 dS[BW_ROWS];
-#pragma unroll
-        for (int i = 0; i < BW_ROWS; ++i)
-            dS[i] = p.dht ? *reinterpret_cast<const float4 *>(p.dht + slice(sh, i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = nblk - 1; c >= 0; --c) {
-            const int len = min(BW_CT, sd.len - c * BW_CT), tok0 = sd.tok + c * BW_CT;
-            const size_t cb = ((size_t)(BW_BPC * sd.chunk0 + c) * p.H_v + h) * KD * KD;
-            __syncthreads();
-            bwd_stage_chunk(p, sm, tok0, len, h, hq, a_gate, true, warp, lane);
-            __syncthreads();
-            // recompute the block's states; scratch[r] = state before token r (this thread's slice)
-#pragma unroll
-            for (int i = 0; i < BW_ROWS; ++i) S[i] = *reinterpret_cast<const float4 *>(p.ckpt + slice(cb, i));
-            for (int r = 0; r < len; ++r) {
-#pragma unroll
-                for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(scr + sslice(r, i)) = S[i];
-                if (r + 1 < len)
-                    bwd_fwd_token(S, reinterpret_cast<const float4 *>(skh + r * KD)[lane],
-                                  reinterpret_cast<const float4 *>(se + r * KD)[lane], sbeta[r], sv + r * KD, r0, lane);
-            }
-            // tokens backwards; the states of token r - 1 are loaded while token r is processed, and the
-            // reduction areas alternate so one barrier per token suffices
-            float4 spn[BW_ROWS];
-#pragma unroll
-            for (int i = 0; i < BW_ROWS; ++i) spn[i] = *reinterpret_cast<const float4 *>(scr + sslice(len - 1, i));
-            for (int r = len - 1; r >= 0; --r) {
-                const float4 kh = reinterpret_cast<const float4 *>(skh + r * KD)[lane];
-                const float4 qt = reinterpret_cast<const float4 *>(sqt + r * KD)[lane];
-                const float4 e = reinterpret_cast<const float4 *>(se + r * KD)[lane];
-                const float beta = sbeta[r];
-                float4 pq = make_float4(0.f, 0.f, 0.f, 0.f), pk = pq, pe = pq;
-                float pb = 0.f;
-                float4 sp[BW_ROWS];
-#pragma unroll
-                for (int i = 0; i < BW_ROWS; ++i) sp[i] = spn[i];
-                if (r > 0) {
-#pragma unroll
-                    for (int i = 0; i < BW_ROWS; ++i) spn[i] = *reinterpret_cast<const float4 *>(scr + sslice(r - 1, i));
+                for (int e = 0; e < 4; ++e) kk[j][e] = pp[j][e] = 0.f;
+            for (int k0 = 0; k0 < KD; k0 += 8) {
+                const PairRef f0 = pair_ref(sG, i, b, k0 + t), f1 = pair_ref(sG, i, b, k0 + t + 4);
+                const int r0 = 16 * i + g;
+                uint32_t ak[4], aq[4], bb[2][2];
+                {
+                    const float e00 = f0.rowf(sG[toff<KD>(r0, k0 + t)]), e10 = f0.rowf(sG[toff<KD>(r0 + 8, k0 + t)]);
+                    const float e01 = f1.rowf(sG[toff<KD>(r0, k0 + t + 4)]);
+                    const float e11 = f1.rowf(sG[toff<KD>(r0 + 8, k0 + t + 4)]);
+                    ak[0] = tf32_rn_bits(sKh[toff<KD>(r0, k0 + t)] * e00);
+                    ak[1] = tf32_rn_bits(sKh[toff<KD>(r0 + 8, k0 + t)] * e10);
+                    ak[2] = tf32_rn_bits(sKh[toff<KD>(r0, k0 + t + 4)] * e01);
+                    ak[3] = tf32_rn_bits(sKh[toff<KD>(r0 + 8, k0 + t + 4)] * e11);
+                    aq[0] = tf32_rn_bits(sQt[toff<KD>(r0, k0 + t)] * e00);
+                    aq[1] = tf32_rn_bits(sQt[toff<KD>(r0 + 8, k0 + t)] * e10);
+                    aq[2] = tf32_rn_bits(sQt[toff<KD>(r0, k0 + t + 4)] * e01);
+                    aq[3] = tf32_rn_bits(sQt[toff<KD>(r0 + 8, k0 + t + 4)] * e11);
                 }
-                // S' = S_{t-1} Diag(e) and d = S' kh for the four rows
-                float4 s1[BW_ROWS], g[BW_ROWS];
-                float d[BW_ROWS], dd4[BW_ROWS], del[BW_ROWS];
 #pragma unroll
-                for (int i = 0; i < BW_ROWS; ++i) {
-                    s1[i].x = sp[i].x * e.x; s1[i].y = sp[i].y * e.y; s1[i].z = sp[i].z * e.z; s1[i].w = sp[i].w * e.w;
-                    d[i] = dot4(s1[i], kh);
-                }
-                warp_sum4(d, lane);
-                // delta, S_t; dS += do qt^T; dqt += S_t^T do; ddel = dS kh
-#pragma unroll
-                for (int i = 0; i < BW_ROWS; ++i) {
-                    const float dor = sdo[r * KD + r0 + i];
-                    del[i] = beta * (sv[r * KD + r0 + i] - d[i]);
-                    float4 st;
-                    st.x = fmaf(del[i], kh.x, s1[i].x); st.y = fmaf(del[i], kh.y, s1[i].y);
-                    st.z = fmaf(del[i], kh.z, s1[i].z); st.w = fmaf(del[i], kh.w, s1[i].w);
-                    g[i] = dS[i];
-                    g[i].x = fmaf(dor, qt.x, g[i].x); g[i].y = fmaf(dor, qt.y, g[i].y);
-                    g[i].z = fmaf(dor, qt.z, g[i].z); g[i].w = fmaf(dor, qt.w, g[i].w);
-                    pq.x = fmaf(st.x, dor, pq.x); pq.y = fmaf(st.y, dor, pq.y);
-                    pq.z = fmaf(st.z, dor, pq.z); pq.w = fmaf(st.w, dor, pq.w);
-                    dd4[i] = dot4(g[i], kh);
-                }
-                warp_sum4(dd4, lane);   // ddel per row
-#pragma unroll
-                for (int i = 0; i < BW_ROWS; ++i) {
-                    const float ddel = dd4[i];
-                    // dkh += dS^T delta ; dv ; dbeta
-                    pk.x = fmaf(g[i].x, del[i], pk.x); pk.y = fmaf(g[i].y, del[i], pk.y);
-                    pk.z = fmaf(g[i].z, del[i], pk.z); pk.w = fmaf(g[i].w, del[i], pk.w);
-                    if (lane == 0) p.dv[((size_t)(tok0 + r) * p.H_v + h) * KD + r0 + i] = beta * ddel;
-                    pb = fmaf(ddel, sv[r * KD + r0 + i] - d[i], pb);
-                    // dd = -beta ddel ; dS' = dS + dd kh^T ; dkh += S'^T dd ; de += S_{t-1} * dS'
-                    const float dd = -beta * ddel;
-                    g[i].x = fmaf(dd, kh.x, g[i].x); g[i].y = fmaf(dd, kh.y, g[i].y);
-                    g[i].z = fmaf(dd, kh.z, g[i].z); g[i].w = fmaf(dd, kh.w, g[i].w);
-                    pk.x = fmaf(s1[i].x, dd, pk.x); pk.y = fmaf(s1[i].y, dd, pk.y);
-                    pk.z = fmaf(s1[i].z, dd, pk.z); pk.w = fmaf(s1[i].w, dd, pk.w);
-                    pe.x = fmaf(sp[i].x, g[i].x, pe.x); pe.y = fmaf(sp[i].y, g[i].y, pe.y);
-                    pe.z = fmaf(sp[i].z, g[i].z, pe.z); pe.w = fmaf(sp[i].w, g[i].w, pe.w);
-                    // dS_{t-1} = dS' Diag(e)
-                    dS[i].x = g[i].x * e.x; dS[i].y = g[i].y * e.y; dS[i].z = g[i].z * e.z; dS[i].w = g[i].w * e.w;
-                }
-                // sums over the quarter's rows (8 warps)
-                float *rd = red + (r & 1) * (BW_WARPS * 3 * KD), *rdb = redb + (r & 1) * BW_WARPS;
-                reinterpret_cast<float4 *>(rd + (warp * 3 + 0) * KD)[lane] = pq;
-                reinterpret_cast<float4 *>(rd + (warp * 3 + 1) * KD)[lane] = pk;
-                reinterpret_cast<float4 *>(rd + (warp * 3 + 2) * KD)[lane] = pe;
-                if (lane == 0) rdb[warp] = pb;
-                __syncthreads();
-                const size_t tp = ((size_t)(tok0 + r) * p.H_v + h) * BW_PARTS + part;
-                for (int x = tid; x < 3 * KD; x += BW_THREADS) {
-                    const int which = x / KD, ch = x % KD;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int w = 0; w < BW_WARPS; ++w) acc += rd[(w * 3 + which) * KD + ch];
-                    float *dst = which == 0 ? p.dqt : which == 1 ? p.dkh : p.de;
-                    dst[tp * KD + ch] = acc;
-                }
-                if (tid == 0) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int w = 0; w < BW_WARPS; ++w) acc += rdb[w];
-                    p.dbeta[tp] = acc;
+                for (int jn = 0; jn < 2; ++jn) {
+                    const int j = 16 * b + 8 * jn + g;
+                    bb[jn][0] = tf32_rn_bits(sKh[toff<KD>(j, k0 + t)] * f0.colf(sG[toff<KD>(j, k0 + t)]));
+                    bb[jn][1] = tf32_rn_bits(sKh[toff<KD>(j, k0 + t + 4)] * f1.colf(sG[toff<KD>(j, k0 + t + 4)]));
+                    mma_tf32(kk[jn], ak, bb[jn]);
+                    mma_tf32(pp[jn], aq, bb[jn]);
                 }
             }
-        }
+            // masks by selection (above the diagonal the clamped factors may overflow)
 #pragma unroll
-        for (int i = 0; i < BW_ROWS; ++i) *reinterpret_cast<float4 *>(p.dh0 + slice(sh, i)) = dS[i];
+            for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = 16 * i + g + 8 * hh, c = 16 * b + 8 * jn + 2 * t;
+                    const float k0v = (i > b || c < r) ? kk[jn][2 * hh] : 0.f;
+                    const float k1v = (i > b || c + 1 < r) ? kk[jn][2 * hh + 1] : 0.f;
+                    const float p0v = (i > b || c <= r) ? pp[jn][2 * hh] : 0.f;
+                    const float p1v = (i > b || c + 1 <= r) ? pp[jn][2 * hh + 1] : 0.f;
+                    st2(sKK + toff<CH>(r, c), k0v, k1v);
+                    st2(sP + toff<CH>(r, c), p0v, p1v);
+                }
+        }
+        // the six blocks above the diagonal are zero
+        for (int idx = tid; idx < 6 * 256; idx += BC_THREADS) {
+            const int blk = idx >> 8, e = idx & 255;
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            const int o = toff<CH>(16 * bi + (e >> 4), 16 * bj + (e & 15));
+            sKK[o] = 0.f;
+            sP[o] = 0.f;
+        }
+        __syncthreads();
+        // A = beta KK for the inversion; KK and P to the record
+        for (int idx = tid; idx < CH * CH; idx += BC_THREADS) {
+            const int r = idx >> 6, j = idx & 63;
+            sA[r * AS + j] = sBeta[r] * sKK[toff<CH>(r, j)];
+        }
+        for (int idx = tid; idx < CH * CH / 4; idx += BC_THREADS) {
+            reinterpret_cast<float4 *>(rec + BR_KK / 4)[idx] = reinterpret_cast<const float4 *>(sKK)[idx];
+            reinterpret_cast<float4 *>(rec + BR_P / 4)[idx] = reinterpret_cast<const float4 *>(sP)[idx];
+        }
+        __syncthreads();
+        invert_unit_lower64<BC_THREADS>(sA, sT, sX, tid, warp, lane);
+        for (int idx = tid; idx < CH * CH; idx += BC_THREADS) {
+            const int r = idx >> 6, j = idx & 63;
+            rec[BR_T / 4 + toff<CH>(r, j)] = sT[r * AS + j];
+        }
+        if (tid < KD) rec[BR_D / 4 + tid] = sD[tid];
+        if (tid < CH) rec[BR_BETA / 4 + tid] = sBeta[tid];
+        // ---- W = T (beta Kg) -> shared (for N) and the record; Kd = Kh e^(Gam_C - Gam)
+        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
+            CH, [&](int r, int j) { return sT[r * AS + j]; },
+            [&](int j, int c) { return sBeta[j] * sKh[toff<KD>(j, c)] * ex2n(sG[toff<KD>(j, c)]); },
+            [&](int r, int c, float v0, float v1) {
+                st2(sW + toff<KD>(r, c), v0, v1);
+                st2(rec + BR_W / 4 + toff<KD>(r, c), v0, v1);
+            },
+            warp, lane);
+        for (int idx = tid; idx < CH * KD / 4; idx += BC_THREADS) {
+            const int r = idx >> 5, c = 4 * (idx & 31), o = toff<KD>(r, c);
+            const float4 kh = *reinterpret_cast<const float4 *>(sKh + o), gm = *reinterpret_cast<const float4 *>(sG + o);
+            const int oc = toff<KD>(CH - 1, c);
+            const float4 gc = *reinterpret_cast<const float4 *>(sG + oc);
+            *reinterpret_cast<float4 *>(rec + BR_KD / 4 + o) =
+                make_float4(kh.x * ex2n(gc.x - gm.x), kh.y * ex2n(gc.y - gm.y), kh.z * ex2n(gc.z - gm.z),
+                            kh.w * ex2n(gc.w - gm.w));
+        }
+        __syncthreads();
+        // ---- N = Qt e^Gam - P W
+        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
+            CH, [&](int r, int j) { return sP[toff<CH>(r, j)]; }, [&](int j, int c) { return sW[toff<KD>(j, c)]; },
+            [&](int r, int c, float v0, float v1) {
+                const int o = toff<KD>(r, c);
+                st2(rec + BR_N / 4 + o, sQt[o] * ex2n(sG[o]) - v0, sQt[o + 1] * ex2n(sG[o + 1]) - v1);
+            },
+            warp, lane);
+        __syncthreads();
+        // ---- V (fp32) over Qt, then U = T (beta V) as two 64-column halves
+        for (int idx = tid; idx < CH * KD / 8; idx += BC_THREADS) {
+            const int r = idx >> 4, c = 8 * (idx & 15);
+            float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+            if (r < len) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(p.v + ((size_t)(cd.tok + r) * p.H_v + h) * KD + c);
+                lo = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                hi = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+            }
+            *reinterpret_cast<float4 *>(sV + toff<KD>(r, c)) = lo;
+            *reinterpret_cast<float4 *>(sV + toff<KD>(r, c + 4)) = hi;
+        }
+        __syncthreads();
+        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
+            CH, [&](int r, int j) { return sT[r * AS + j]; },
+            [&](int j, int c) { return sBeta[j] * sV[toff<KD>(j, c)]; },
+            [&](int r, int c, float v0, float v1) {
+                st2(rec + BR_U / 4 + (c >> 6) * (CH * CH) + toff<CH>(r, c & 63), v0, v1);
+            },
+            warp, lane);
     }
 }
 
-// The prologue's Jacobians, one warp per (query/key head, token range); lane = channels
+// =====================================================================
+// State chains: one CTA per (sequence, value head, 64-row V block), the 64 x 128 state X in
+// fp32 (a tile in shared memory).  Per chunk (forward: in order; backward: in reverse):
+//   forward   E = X W^T,   Z = U^T - E,  X <- X Diag(D) + Z Kd              (X = S, stored as S_0)
+//   backward  E = X Kd^T,  Z = -E,       X <- X Diag(D) + Z W + dO^T N      (X = dS, stored as dS_C)
+// The item operands (32 KiB tiles W, Kd, N) stream through a ring of slots by bulk copies,
+// issued one chunk ahead by thread 0 once the slots' previous contents are consumed; the
+// per-chunk extras (D, and U's V block or the chunk's dO rows) through a double buffer.
+// Every wait is bounded; a timeout records KDA_ERR_DEVICE_TIMEOUT and the CTA stops.
+// =====================================================================
+template <bool BWD>
+struct ChainCfg {
+    static constexpr int OPS = BWD ? 3 : 2;             // ring tiles per chunk
+    static constexpr int SLOTS = BWD ? 5 : 4;
+    static constexpr uint32_t DO_STRIDE = 128;          // dO row stride (bytes)
+    static constexpr uint32_t AUX = BWD ? 512 + CH * DO_STRIDE : 512 + CH * CH * 4;   // D, then dO rows or U block
+    static constexpr uint32_t X = 0, Z = 32768, RING = 49152, AUXB = RING + SLOTS * 32768;
+    static constexpr uint32_t BAR = AUXB + 2 * AUX, BYTES = BAR + 8 * (SLOTS + 2);
+};
+static_assert(ChainCfg<true>::BYTES + 128 <= 232448 && ChainCfg<false>::BYTES + 128 <= 232448, "chain smem");
+
+template <bool BWD>
+__global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcParams p) {
+    using Cfg = ChainCfg<BWD>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = aligned_smem<128>(smem_raw);
+    if (p.hdr[1] == 0) return;
+    const int vb = blockIdx.x & 1;
+    const int h = (blockIdx.x >> 1) % p.H_v;
+    const int rank = (blockIdx.x >> 1) / p.H_v;
+    if (rank >= p.nseq) return;
+    const int seq = p.order[rank];
+    const SeqDesc sd = p.seqs[seq];
+    const int n = sd.nchunk;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    float *sX = reinterpret_cast<float *>(sm + Cfg::X), *sZ = reinterpret_cast<float *>(sm + Cfg::Z);
+    const uint32_t sbase = smem_u32(sm), bar = sbase + Cfg::BAR;
+    const size_t sh = ((size_t)seq * p.H_v + h) * KD * KD + (size_t)vb * CH * KD;   // rows of init / dht / dh0
+
+    if (tid == 0) {
+        for (int i = 0; i < Cfg::SLOTS + 2; ++i) mbar_init(bar + 8 * i, 1);
+        mbar_fence_init();
+    }
+    // X from the initial state (forward) or the final state's gradient (backward)
+    const float *x0 = BWD ? p.dht : p.init;
+    for (int idx = tid; idx < CH * KD / 4; idx += BC_THREADS) {
+        const int r = idx >> 5, c = 4 * (idx & 31);
+        const float4 v = x0 ? *reinterpret_cast<const float4 *>(x0 + sh + (size_t)r * KD + c)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(sX + toff<KD>(r, c)) = v;
+    }
+    fence_async_smem();
+    __syncthreads();
+
+    auto chunk_of = [&](int s) { return BWD ? n - 1 - s : s; };
+    auto item_of = [&](int s) { return ((size_t)sd.chunk0 + chunk_of(s)) * p.H_v + h; };
+    auto issue = [&](int s) {   // thread 0: the ring tiles and extras of step s
+        const unsigned char *rec = p.rec + item_of(s) * BR_BYTES;
+        const uint32_t offs[3] = {BWD ? BR_KD : BR_W, BWD ? BR_W : BR_KD, BR_N};
+#pragma unroll
+        for (int op = 0; op < Cfg::OPS; ++op) {
+            const int slot = (Cfg::OPS * s + op) % Cfg::SLOTS;
+            mbar_expect_tx(bar + 8 * slot, 32768);
+            bulk_g2s(sbase + Cfg::RING + slot * 32768, rec + offs[op], 32768, bar + 8 * slot);
+        }
+        const uint32_t ab = bar + 8 * (Cfg::SLOTS + (s & 1)), aux = sbase + Cfg::AUXB + (s & 1) * Cfg::AUX;
+        if (BWD) {
+            const int c = chunk_of(s), len = min(CH, sd.len - c * CH), tok0 = sd.tok + c * CH;
+            mbar_expect_tx(ab, 512 + 128 * len);
+            bulk_g2s(aux, rec + BR_D, 512, ab);
+            for (int r = 0; r < len; ++r)
+                bulk_g2s(aux + 512 + r * Cfg::DO_STRIDE, p.dout + ((size_t)(tok0 + r) * p.H_v + h) * KD + vb * CH,
+                         128, ab);
+        } else {
+            mbar_expect_tx(ab, 512 + CH * CH * 4);
+            bulk_g2s(aux, rec + BR_D, 512, ab);
+            bulk_g2s(aux + 512, rec + BR_U + vb * (CH * CH * 4), CH * CH * 4, ab);
+        }
+    };
+    if (tid == 0 && n > 0) issue(0);
+
+    float *outbase = BWD ? p.dSC : p.S0;
+    bool ok = true;
+    for (int s = 0; s < n; ++s) {
+        // all of step s's operands (bounded wait; the CTA decides together)
+        bool mine = true;
+#pragma unroll
+        for (int op = 0; op < Cfg::OPS; ++op) {
+            const int pos = Cfg::OPS * s + op;
+            mine = mine && mbar_wait(bar + 8 * (pos % Cfg::SLOTS), (pos / Cfg::SLOTS) & 1);
+        }
+        mine = mine && mbar_wait(bar + 8 * (Cfg::SLOTS + (s & 1)), (s >> 1) & 1);
+        if (!__syncthreads_and(mine)) {
+            if (tid == 0) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            ok = false;
+            break;
+        }
+        const float *op1 = reinterpret_cast<const float *>(sm + Cfg::RING + ((Cfg::OPS * s) % Cfg::SLOTS) * 32768);
+        const float *op2 = reinterpret_cast<const float *>(sm + Cfg::RING + ((Cfg::OPS * s + 1) % Cfg::SLOTS) * 32768);
+        const float *op3 = reinterpret_cast<const float *>(sm + Cfg::RING + ((Cfg::OPS * s + 2) % Cfg::SLOTS) * 32768);
+        const unsigned char *aux = sm + Cfg::AUXB + (s & 1) * Cfg::AUX;
+        const float *sD = reinterpret_cast<const float *>(aux);
+        const int c = chunk_of(s), len = min(CH, sd.len - c * CH);
+        // the state entering this step, to the workspace
+        if (tid == 0) {
+            bulk_s2g(outbase + item_of(s) * (ST_BYTES / 4) + vb * (CH * KD), sbase + Cfg::X, 32768);
+            bulk_commit();
+        }
+        // ---- E (64 v x 64 r) = X op1^T, then Z
+        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
+            KD, [&](int v, int k) { return sX[toff<KD>(v, k)]; }, [&](int k, int r) { return op1[toff<KD>(r, k)]; },
+            [&](int v, int r, float e0, float e1) {
+                float z0 = -e0, z1 = -e1;
+                if (!BWD) {
+                    const float *u = reinterpret_cast<const float *>(aux + 512);   // U block [r][v]
+                    z0 += u[toff<CH>(r, v)];
+                    z1 += u[toff<CH>(r + 1, v)];
+                }
+                st2(sZ + toff<CH>(v, r), z0, z1);
+            },
+            warp, lane);
+        __syncthreads();   // Z complete; op1 consumed
+        if (tid == 0 && s + 1 < n) issue(s + 1);
+        // ---- X <- X Diag(D) + Z op2 (+ dO^T N)
+        {
+            const int m0 = 32 * (warp >> 2), n0 = 32 * (warp & 3);
+            float acc[2][4][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = m0 + 16 * i + g, cc = n0 + 8 * j + 2 * t;
+                    const float d0 = sD[cc], d1 = sD[cc + 1];
+                    acc[i][j][0] = sX[toff<KD>(r, cc)] * d0;
+                    acc[i][j][1] = sX[toff<KD>(r, cc + 1)] * d1;
+                    acc[i][j][2] = sX[toff<KD>(r + 8, cc)] * d0;
+                    acc[i][j][3] = sX[toff<KD>(r + 8, cc + 1)] * d1;
+                }
+            mma_tile<2, 4>(acc, m0, n0, 0, CH, [&](int v, int r) { return sZ[toff<CH>(v, r)]; },
+                           [&](int r, int cc) { return op2[toff<KD>(r, cc)]; }, g, t);
+            if (BWD) {
+                const unsigned char *dorow = aux + 512;
+                mma_tile<2, 4>(
+                    acc, m0, n0, 0, CH,
+                    [&](int v, int r) {
+                        return r < len ? bf16_to_f(*reinterpret_cast<const uint16_t *>(dorow + r * Cfg::DO_STRIDE + 2 * v))
+                                       : 0.f;
+                    },
+                    [&](int r, int cc) { return op3[toff<KD>(r, cc)]; }, g, t);
+            }
+            if (tid == 0) bulk_wait_read_all();   // the store of X has read it
+            __syncthreads();                      // every warp is done reading X, Z and the operands
+            tile_out<2, 4>(acc, m0, n0, g, t, [&](int r, int cc, float v0, float v1) { st2(sX + toff<KD>(r, cc), v0, v1); });
+        }
+        fence_async_smem();
+    }
+    __syncthreads();
+    if (BWD && ok) {
+        for (int idx = tid; idx < CH * KD / 4; idx += BC_THREADS) {
+            const int r = idx >> 5, cc = 4 * (idx & 31);
+            *reinterpret_cast<float4 *>(p.dh0 + sh + (size_t)r * KD + cc) =
+                *reinterpret_cast<const float4 *>(sX + toff<KD>(r, cc));
+        }
+    }
+    if (tid == 0) bulk_wait_all();
+    // a failed CTA may leave copies in flight: let them land before the CTA's memory goes away
+    if (!ok && tid == 0)
+        for (int i = 0; i < Cfg::SLOTS + 2; ++i) {
+            mbar_wait(bar + 8 * i, 0, 1u << 14);
+            mbar_wait(bar + 8 * i, 1, 1u << 14);
+        }
+}
+
+// =====================================================================
+// Gradients over the value dimension, per (item, V half vh) (64 value columns):
+//   Delta_h = U_h - W S0_h^T,  dDelta_h = P^T dO_h + Kd dS_h^T        (64 r x 64 v)
+//   dKd += Delta_h dS_h,  dQg += dO_h S0_h,  dW += -dDelta_h S0_h      (64 r x 128 k)
+//   dP += dO_h Delta_h^T,  dT += dDelta_h (beta V_h)^T                 (64 x 64)
+//   dv_h = beta (T^T dDelta_h),  dbeta += rowsum(T^T dDelta_h * V_h),  dGam_C += colsum(S0_h * dS_h)
+// (S0_h, dS_h: rows vh of the states), the sums written per half to the item's partials.
+// =====================================================================
+constexpr uint32_t GV_W = 0, GV_KD = 32768, GV_S0 = 65536, GV_DS = 98304, GV_U = 131072, GV_P = 147456,
+                   GV_T = 163840, GV_DO = 180224, GV_V = 196608, GV_DDL = 212992, GV_MISC = 229376,
+                   GV_BAR = GV_MISC + 1536, GV_BYTES = GV_BAR + 16;
+static_assert(GV_BYTES + 128 <= 232448, "gradv smem");
+
+__global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = aligned_smem<128>(smem_raw);
+    if (p.hdr[1] == 0) return;
+    float *sW = reinterpret_cast<float *>(sm + GV_W), *sKd = reinterpret_cast<float *>(sm + GV_KD);
+    float *sS0 = reinterpret_cast<float *>(sm + GV_S0), *sDS = reinterpret_cast<float *>(sm + GV_DS);
+    float *sU = reinterpret_cast<float *>(sm + GV_U), *sP = reinterpret_cast<float *>(sm + GV_P);
+    float *sT = reinterpret_cast<float *>(sm + GV_T), *sDO = reinterpret_cast<float *>(sm + GV_DO);
+    float *sV = reinterpret_cast<float *>(sm + GV_V), *sDD = reinterpret_cast<float *>(sm + GV_DDL);
+    float *sD = reinterpret_cast<float *>(sm + GV_MISC), *sBeta = sD + 128, *sDB = sD + 192, *sGC = sD + 256;
+    const uint32_t sbase = smem_u32(sm), bar = sbase + GV_BAR;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long n_units = 2LL * p.hdr[0] * p.H_v;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    uint32_t phase = 0;
+    for (long long unit = blockIdx.x; unit < n_units; unit += gridDim.x, phase ^= 1) {
+        const long long item = unit >> 1;
+        const int vh = (int)(unit & 1);
+        const int h = (int)(item % p.H_v);
+        const ChunkDesc cd = p.chunks[item / p.H_v];
+        const int len = cd.len;
+        const unsigned char *rec = p.rec + (size_t)item * BR_BYTES;
+        unsigned char *part = p.part + ((size_t)item * 2 + vh) * CP_BYTES;
+        __syncthreads();   // the previous unit's reads of shared memory are done
+        if (tid == 0) {
+            mbar_expect_tx(bar, 4 * 32768 + 3 * 16384 + 768);
+            bulk_g2s(sbase + GV_W, rec + BR_W, 32768, bar);
+            bulk_g2s(sbase + GV_KD, rec + BR_KD, 32768, bar);
+            bulk_g2s(sbase + GV_S0, p.S0 + item * (ST_BYTES / 4) + vh * (CH * KD), 32768, bar);
+            bulk_g2s(sbase + GV_DS, p.dSC + item * (ST_BYTES / 4) + vh * (CH * KD), 32768, bar);
+            bulk_g2s(sbase + GV_U, rec + BR_U + vh * 16384, 16384, bar);
+            bulk_g2s(sbase + GV_P, rec + BR_P, 16384, bar);
+            bulk_g2s(sbase + GV_T, rec + BR_T, 16384, bar);
+            bulk_g2s(sbase + GV_MISC, rec + BR_D, 768, bar);   // D [128], beta [64]
+        }
+        // dO and V of this half (fp32 tiles, zero past len)
+        for (int idx = tid; idx < 2 * CH * 8; idx += BC_THREADS) {
+            const int which = idx >> 9, r = (idx >> 3) & 63, c = 8 * (idx & 7);
+            float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+            if (r < len) {
+                const uint16_t *src = which ? p.v : p.dout;
+                const uint4 w = *reinterpret_cast<const uint4 *>(src + ((size_t)(cd.tok + r) * p.H_v + h) * KD + vh * CH + c);
+                lo = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                hi = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+            }
+            float *dst = which ? sV : sDO;
+            *reinterpret_cast<float4 *>(dst + toff<CH>(r, c)) = lo;
+            *reinterpret_cast<float4 *>(dst + toff<CH>(r, c + 4)) = hi;
+        }
+        if (tid < 64) sDB[tid] = 0.f;
+        if (tid < 128) sGC[tid] = 0.f;
+        const bool mine = mbar_wait(bar, phase);
+        if (!__syncthreads_and(mine)) {
+            if (tid == 0) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            break;
+        }
+        // ---- Delta (in place of U) and dDelta
+        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
+            KD, [&](int r, int k) { return sW[toff<KD>(r, k)]; }, [&](int k, int v) { return sS0[toff<KD>(v, k)]; },
+            [&](int r, int v, float e0, float e1) {
+                const int o = toff<CH>(r, v);
+                st2(sU + o, sU[o] - e0, sU[o + 1] - e1);
+            },
+            warp, lane);
+        {
+            const int g = lane >> 2, t = lane & 3, m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1);
+            float acc[1][4][4];
+            tile_zero(acc);
+            mma_tile<1, 4>(acc, m0, n0, 0, CH, [&](int r, int j) { return sP[toff<CH>(j, r)]; },
+                           [&](int j, int v) { return sDO[toff<CH>(j, v)]; }, g, t);
+            mma_tile<1, 4>(acc, m0, n0, 0, KD, [&](int r, int k) { return sKd[toff<KD>(r, k)]; },
+                           [&](int k, int v) { return sDS[toff<KD>(v, k)]; }, g, t);
+            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int v, float v0, float v1) { st2(sDD + toff<CH>(r, v), v0, v1); });
+        }
+        __syncthreads();
+        float *pDKD = reinterpret_cast<float *>(part + CP_DKD), *pDQG = reinterpret_cast<float *>(part + CP_DQG);
+        float *pDW = reinterpret_cast<float *>(part + CP_DW), *pDP = reinterpret_cast<float *>(part + CP_DP);
+        float *pDT = reinterpret_cast<float *>(part + CP_DT);
+        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
+            CH, [&](int r, int v) { return sU[toff<CH>(r, v)]; }, [&](int v, int k) { return sDS[toff<KD>(v, k)]; },
+            [&](int r, int k, float v0, float v1) { st2(pDKD + toff<KD>(r, k), v0, v1); }, warp, lane);
+        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
+            CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; }, [&](int v, int k) { return sS0[toff<KD>(v, k)]; },
+            [&](int r, int k, float v0, float v1) { st2(pDQG + toff<KD>(r, k), v0, v1); }, warp, lane);
+        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
+            CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; }, [&](int v, int k) { return sS0[toff<KD>(v, k)]; },
+            [&](int r, int k, float v0, float v1) { st2(pDW + toff<KD>(r, k), -v0, -v1); }, warp, lane);
+        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
+            CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; }, [&](int v, int j) { return sU[toff<CH>(j, v)]; },
+            [&](int r, int j, float v0, float v1) {
+                st2(pDP + toff<CH>(r, j), j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
+            },
+            warp, lane);
+        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
+            CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
+            [&](int v, int j) { return sBeta[j] * sV[toff<CH>(j, v)]; },
+            [&](int r, int j, float v0, float v1) { st2(pDT + toff<CH>(r, j), v0, v1); }, warp, lane);
+        // dBV = T^T dDelta: dv and dbeta's V term
+        {
+            const int g = lane >> 2, t = lane & 3, m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1);
+            float acc[1][4][4];
+            tile_zero(acc);
+            mma_tile<1, 4>(acc, m0, n0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
+                           [&](int j, int v) { return sDD[toff<CH>(j, v)]; }, g, t);
+            float rs[2] = {0.f, 0.f};
+            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int v, float v0, float v1) {
+                const int o = toff<CH>(r, v);
+                rs[(r - m0) >> 3] += v0 * sV[o] + v1 * sV[o + 1];
+                if (r < len) {
+                    const float be = sBeta[r];
+                    st2(p.dv + ((size_t)(cd.tok + r) * p.H_v + h) * KD + vh * CH + v, be * v0, be * v1);
+                }
+            });
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 1);
+                rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 2);
+            }
+            if (t == 0) {
+                atomicAdd(sDB + m0 + g, rs[0]);
+                atomicAdd(sDB + m0 + g + 8, rs[1]);
+            }
+        }
+        // colsum(S0_h * dS_h) per channel
+        {
+            const int c = tid & 127, v0 = 32 * (tid >> 7);
+            float s = 0.f;
+            for (int v = v0; v < v0 + 32; ++v) s = fmaf(sS0[toff<KD>(v, c)], sDS[toff<KD>(v, c)], s);
+            atomicAdd(sGC + c, s);
+        }
+        __syncthreads();
+        if (tid < 64) reinterpret_cast<float *>(part + CP_DB)[tid] = sDB[tid];
+        if (tid < 128) reinterpret_cast<float *>(part + CP_DGC)[tid] = sGC[tid];
+    }
+}
+
+// =====================================================================
+// Gradients over the keys, per item: dT = dT_V + dW (beta Kg)^T, dA = strict_lower(-T^T dT T^T),
+// dbeta, then (warp w owns channels 16 w .. 16 w + 15, its accumulators in registers)
+// dBW = T^T dW, the decayed pair products of M = beta dA and dP's strict part, and
+//   dKh = beta dBW e^Gam + (pair products) + diag(dP) Qt + dKd e^(Gam_C - Gam)
+//   dQt = dQg e^Gam + (pair products) + diag(dP) Kh
+//   dGam = beta dBW Kg + (pair products' Gam terms) + dQg Qg
+// and dg per channel from dGam's suffix sums, dGam_C and the exclusive prefix sums of dKd Kd.
+// =====================================================================
+constexpr uint32_t GK_KH = 0, GK_QT = 32768, GK_G = 65536, GK_DW = 98304, GK_T = 131072, GK_KK = 147456,
+                   GK_DT = 163840, GK_X = 180224, GK_DP = 196608, GK_MISC = 212992, GK_BAR = GK_MISC + 2048,
+                   GK_BYTES = GK_BAR + 16;
+static_assert(GK_BYTES + 128 <= 232448, "gradk smem");
+
+__global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = aligned_smem<128>(smem_raw);
+    if (p.hdr[1] == 0) return;
+    float *sKh = reinterpret_cast<float *>(sm + GK_KH), *sQt = reinterpret_cast<float *>(sm + GK_QT);
+    float *sG = reinterpret_cast<float *>(sm + GK_G), *sDW = reinterpret_cast<float *>(sm + GK_DW);
+    float *sT = reinterpret_cast<float *>(sm + GK_T), *sKK = reinterpret_cast<float *>(sm + GK_KK);
+    float *sDT = reinterpret_cast<float *>(sm + GK_DT), *sX = reinterpret_cast<float *>(sm + GK_X);
+    float *sDP = reinterpret_cast<float *>(sm + GK_DP);
+    float *sBeta = reinterpret_cast<float *>(sm + GK_MISC), *sD = sBeta + 64, *sDGC = sBeta + 192,
+          *sDB = sBeta + 320;
+    const uint32_t sbase = smem_u32(sm), bar = sbase + GK_BAR;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const long long n_items = (long long)p.hdr[0] * p.H_v;
+    const int group = p.H_v / p.H_qk;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    uint32_t phase = 0;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x, phase ^= 1) {
+        const int h = (int)(item % p.H_v);
+        const ChunkDesc cd = p.chunks[item / p.H_v];
+        const int hq = h / group, len = cd.len;
+        const float a = ex2n(p.A_log[h]);
+        const unsigned char *rec = p.rec + (size_t)item * BR_BYTES;
+        const unsigned char *pt0 = p.part + (size_t)item * 2 * CP_BYTES, *pt1 = pt0 + CP_BYTES;
+        __syncthreads();
+        if (tid == 0) {
+            mbar_expect_tx(bar, 2 * 16384);
+            bulk_g2s(sbase + GK_T, rec + BR_T, 16384, bar);
+            bulk_g2s(sbase + GK_KK, rec + BR_KK, 16384, bar);
+        }
+        // the two halves' partial sums: dW, dT's V term, dP; dbeta's V term, colsum(S0 dS_C)
+        for (int idx = tid; idx < CH * KD / 4; idx += BC_THREADS) {
+            const float4 x = reinterpret_cast<const float4 *>(pt0 + CP_DW)[idx];
+            const float4 y = reinterpret_cast<const float4 *>(pt1 + CP_DW)[idx];
+            reinterpret_cast<float4 *>(sDW)[idx] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+        }
+        for (int idx = tid; idx < CH * CH / 4; idx += BC_THREADS) {
+            float4 x = reinterpret_cast<const float4 *>(pt0 + CP_DT)[idx];
+            float4 y = reinterpret_cast<const float4 *>(pt1 + CP_DT)[idx];
+            reinterpret_cast<float4 *>(sDT)[idx] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+            x = reinterpret_cast<const float4 *>(pt0 + CP_DP)[idx];
+            y = reinterpret_cast<const float4 *>(pt1 + CP_DP)[idx];
+            reinterpret_cast<float4 *>(sDP)[idx] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+        }
+        if (tid < 64)
+            sDB[tid] = reinterpret_cast<const float *>(pt0 + CP_DB)[tid] + reinterpret_cast<const float *>(pt1 + CP_DB)[tid];
+        bwdc_rows(p, cd.tok, len, h, hq, a, sKh, sQt, sG, sBeta, sD, tid);
+        if (tid < 128)
+            sDGC[tid] = (reinterpret_cast<const float *>(pt0 + CP_DGC)[tid] +
+                         reinterpret_cast<const float *>(pt1 + CP_DGC)[tid]) * sD[tid];
+        const bool mine = mbar_wait(bar, phase);
+        if (!__syncthreads_and(mine)) {
+            if (tid == 0) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            break;
+        }
+        // ---- dT += dW (beta Kg)^T
+        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
+            KD, [&](int r, int k) { return sDW[toff<KD>(r, k)]; },
+            [&](int k, int j) { return sBeta[j] * sKh[toff<KD>(j, k)] * ex2n(sG[toff<KD>(j, k)]); },
+            [&](int r, int j, float v0, float v1) {
+                const int o = toff<CH>(r, j);
+                st2(sDT + o, sDT[o] + v0, sDT[o + 1] + v1);
+            },
+            warp, lane);
+        __syncthreads();
+        // ---- X = dT T^T
+        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
+            CH, [&](int r, int j) { return sDT[toff<CH>(r, j)]; }, [&](int j, int i) { return sT[toff<CH>(i, j)]; },
+            [&](int r, int i, float v0, float v1) { st2(sX + toff<CH>(r, i), v0, v1); }, warp, lane);
+        __syncthreads();
+        // ---- dA = strict_lower(-T^T X); dbeta += rowsum(dA KK); M = beta dA over dT
+        {
+            const int m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1);
+            float acc[1][4][4];
+            tile_zero(acc);
+            mma_tile<1, 4>(acc, m0, n0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
+                           [&](int j, int i) { return sX[toff<CH>(j, i)]; }, g, t);
+            float rs[2] = {0.f, 0.f};
+            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int i, float v0, float v1) {
+                const int o = toff<CH>(r, i);
+                const float d0 = i < r ? -v0 : 0.f, d1 = i + 1 < r ? -v1 : 0.f;
+                rs[(r - m0) >> 3] += d0 * sKK[o] + d1 * sKK[o + 1];
+                const float be = sBeta[r];
+                st2(sDT + o, be * d0, be * d1);
+            });
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 1);
+                rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 2);
+            }
+            if (t == 0) {
+                atomicAdd(sDB + m0 + g, rs[0]);
+                atomicAdd(sDB + m0 + g + 8, rs[1]);
+            }
+        }
+        // ---- this warp's channels: dBW = T^T dW and the beta dBW terms
+        const int cw = 16 * warp;
+        float akh[4][2][4], aqt[4][2][4], agm[4][2][4];
+        {
+            float bw[4][2][4];
+            tile_zero(bw);
+            mma_tile<4, 2>(bw, 0, cw, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
+                           [&](int j, int c) { return sDW[toff<KD>(j, c)]; }, g, t);
+            float rs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rs[e] = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 16 * i + g + 8 * (e >> 1), c = cw + 8 * jn + 2 * t + (e & 1);
+                        const int o = toff<KD>(r, c);
+                        const float eg = ex2n(sG[o]), kh = sKh[o];
+                        const float x = sBeta[r] * bw[i][jn][e] * eg;
+                        akh[i][jn][e] = x;
+                        agm[i][jn][e] = x * kh;
+                        aqt[i][jn][e] = 0.f;
+                        rs[2 * i + (e >> 1)] += bw[i][jn][e] * kh * eg;
+                    }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 1);
+                rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 2);
+            }
+            if (t == 0)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) atomicAdd(sDB + 16 * (e >> 1) + g + 8 * (e & 1), rs[e]);
+        }
+        __syncthreads();   // M complete
+        // ---- decayed pair products on this warp's channels
+#pragma unroll
+        for (int pr = 0; pr < 10; ++pr) {
+            const int i = pr < 1 ? 0 : pr < 3 ? 1 : pr < 6 ? 2 : 3;
+            const int b = pr - (i * (i + 1)) / 2;
+            const bool dg_ = (i == b);
+            // references for the channels this lane touches: B operands (cw + g, cw + 8 + g),
+            // accumulators (cw + 2t, +1, cw + 8 + 2t, +1)
+            PairRef fb[2], fc[2][2];
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn) {
+                fb[jn] = pair_ref(sG, i, b, cw + 8 * jn + g);
+                fc[jn][0] = pair_ref(sG, i, b, cw + 8 * jn + 2 * t);
+                fc[jn][1] = pair_ref(sG, i, b, cw + 8 * jn + 2 * t + 1);
+            }
+            auto mval = [&](int r, int j) { return sDT[toff<CH>(r, j)]; };   // strictly lower already
+            auto pval = [&](int r, int j) {
+                return (!dg_ || j < r) ? sDP[toff<CH>(r, j)] : 0.f;
+            };
+            // row side: MH = M_ib Hk, PH = dPs_ib Hk (rows of block i)
+            float mh[2][4], ph[2][4], y[2][4];
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mh[jn][e] = ph[jn][e] = y[jn][e] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int r0 = 16 * i + g, j0 = 16 * b + 8 * ks + t;
+                uint32_t am[4], ap[4], bh[2][2];
+                am[0] = tf32_rn_bits(mval(r0, j0));
+                am[1] = tf32_rn_bits(mval(r0 + 8, j0));
+                am[2] = tf32_rn_bits(mval(r0, j0 + 4));
+                am[3] = tf32_rn_bits(mval(r0 + 8, j0 + 4));
+                ap[0] = tf32_rn_bits(pval(r0, j0));
+                ap[1] = tf32_rn_bits(pval(r0 + 8, j0));
+                ap[2] = tf32_rn_bits(pval(r0, j0 + 4));
+                ap[3] = tf32_rn_bits(pval(r0 + 8, j0 + 4));
+#pragma unroll
+                for (int jn = 0; jn < 2; ++jn) {
+                    const int c = cw + 8 * jn + g;
+                    bh[jn][0] = tf32_rn_bits(sKh[toff<KD>(j0, c)] * fb[jn].colf(sG[toff<KD>(j0, c)]));
+                    bh[jn][1] = tf32_rn_bits(sKh[toff<KD>(j0 + 4, c)] * fb[jn].colf(sG[toff<KD>(j0 + 4, c)]));
+                    mma_tf32(mh[jn], am, bh[jn]);
+                    mma_tf32(ph[jn], ap, bh[jn]);
+                }
+            }
+            // column side: y = M_ib^T Fk + dPs_ib^T Fq (rows of block b)
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int j0 = 16 * b + g, r0 = 16 * i + 8 * ks + t;
+                uint32_t am[4], ap[4], bk[2][2], bq[2][2];
+                am[0] = tf32_rn_bits(mval(r0, j0));
+                am[1] = tf32_rn_bits(mval(r0, j0 + 8));
+                am[2] = tf32_rn_bits(mval(r0 + 4, j0));
+                am[3] = tf32_rn_bits(mval(r0 + 4, j0 + 8));
+                ap[0] = tf32_rn_bits(pval(r0, j0));
+                ap[1] = tf32_rn_bits(pval(r0, j0 + 8));
+                ap[2] = tf32_rn_bits(pval(r0 + 4, j0));
+                ap[3] = tf32_rn_bits(pval(r0 + 4, j0 + 8));
+#pragma unroll
+                for (int jn = 0; jn < 2; ++jn) {
+                    const int c = cw + 8 * jn + g;
+                    const int o0 = toff<KD>(r0, c), o1 = toff<KD>(r0 + 4, c);
+                    const float f0 = fb[jn].rowf(sG[o0]), f1 = fb[jn].rowf(sG[o1]);
+                    bk[jn][0] = tf32_rn_bits(sKh[o0] * f0);
+                    bk[jn][1] = tf32_rn_bits(sKh[o1] * f1);
+                    bq[jn][0] = tf32_rn_bits(sQt[o0] * f0);
+                    bq[jn][1] = tf32_rn_bits(sQt[o1] * f1);
+                    mma_tf32(y[jn], am, bk[jn]);
+                    mma_tf32(y[jn], ap, bq[jn]);
+                }
+            }
+            // accumulate: row side into rows of block i, column side into rows of block b
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = cw + 8 * jn + 2 * t + (e & 1);
+                    const PairRef &f = fc[jn][e & 1];
+                    {
+                        const int r = 16 * i + g + 8 * (e >> 1), o = toff<KD>(r, c);
+                        const float rf = f.rowf(sG[o]);
+                        const float fk = tf32_rn(sKh[o] * rf), fq = tf32_rn(sQt[o] * rf);
+                        akh[i][jn][e] += rf * mh[jn][e];
+                        aqt[i][jn][e] += rf * ph[jn][e];
+                        agm[i][jn][e] += fk * mh[jn][e] + fq * ph[jn][e];
+                    }
+                    {
+                        const int j = 16 * b + g + 8 * (e >> 1), o = toff<KD>(j, c);
+                        const float cf = f.colf(sG[o]);
+                        const float hk = tf32_rn(sKh[o] * cf);
+                        akh[b][jn][e] += cf * y[jn][e];
+                        agm[b][jn][e] -= hk * y[jn][e];
+                    }
+                }
+        }
+        // ---- the remaining terms, dqt / dkh out, dGam and dKd Kd to shared memory
+        const float *q0 = reinterpret_cast<const float *>(pt0 + CP_DKD), *q1 = reinterpret_cast<const float *>(pt1 + CP_DKD);
+        const float *w0 = reinterpret_cast<const float *>(pt0 + CP_DQG), *w1 = reinterpret_cast<const float *>(pt1 + CP_DQG);
+        float kdk[4][2][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = 16 * i + g + 8 * hh, c = cw + 8 * jn + 2 * t, o = toff<KD>(r, c);
+                    const float2 dk0 = *reinterpret_cast<const float2 *>(q0 + o), dk1 = *reinterpret_cast<const float2 *>(q1 + o);
+                    const float2 dq0 = *reinterpret_cast<const float2 *>(w0 + o), dq1 = *reinterpret_cast<const float2 *>(w1 + o);
+                    const float dpd = sDP[toff<CH>(r, r)];
+                    const float dkd[2] = {dk0.x + dk1.x, dk0.y + dk1.y}, dqg[2] = {dq0.x + dq1.x, dq0.y + dq1.y};
+                    float okh[2], oqt[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int e = 2 * hh + u;
+                        const float gm = sG[o + u], gc = sG[toff<KD>(CH - 1, c + u)];
+                        const float eg = ex2n(gm), ed = ex2n(gc - gm), qt = sQt[o + u], kh = sKh[o + u];
+                        okh[u] = akh[i][jn][e] + dpd * qt + dkd[u] * ed;
+                        oqt[u] = aqt[i][jn][e] + dqg[u] * eg + dpd * kh;
+                        agm[i][jn][e] += dqg[u] * qt * eg;
+                        kdk[i][jn][e] = dkd[u] * kh * ed;
+                    }
+                    if (r < len) {
+                        const size_t go = ((size_t)(cd.tok + r) * p.H_v + h) * KD + c;
+                        st2(p.dkh + go, okh[0], okh[1]);
+                        st2(p.dqt + go, oqt[0], oqt[1]);
+                    }
+                }
+        __syncthreads();   // every warp is done reading dW and Qt
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jn = 0; jn < 2; ++jn)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = 16 * i + g + 8 * hh, c = cw + 8 * jn + 2 * t, o = toff<KD>(r, c);
+                    st2(sDW + o, agm[i][jn][2 * hh], agm[i][jn][2 * hh + 1]);
+                    st2(sQt + o, kdk[i][jn][2 * hh], kdk[i][jn][2 * hh + 1]);
+                }
+        __syncthreads();
+        // ---- dg = suffix sums of dGam + dGam_C + exclusive prefix sums of dKd Kd; dbeta
+        if (tid < KD) {
+            const int c = tid;
+            float pre = 0.f;
+            for (int r = 0; r < CH; ++r) {
+                const int o = toff<KD>(r, c);
+                const float x = sQt[o];
+                sQt[o] = pre;
+                pre += x;
+            }
+            float suf = 0.f;
+            const float dgc = sDGC[c];
+            for (int r = CH - 1; r >= 0; --r) {
+                const int o = toff<KD>(r, c);
+                suf += sDW[o];
+                if (r < len) p.dg[((size_t)(cd.tok + r) * p.H_v + h) * KD + c] = suf + dgc + sQt[o];
+            }
+        } else if (tid < KD + CH) {
+            const int r = tid - KD;
+            if (r < len) p.dbeta[(size_t)(cd.tok + r) * p.H_v + h] = sDB[r];
+        }
+    }
+}
+
+// =====================================================================
+// The prologue's Jacobians, one warp per (query/key head, 64 tokens); lane = channels
 // 4 lane .. 4 lane + 3:
-//   dq = scale r_q dqt_sum - scale r_q^3 q (q . dqt_sum),  r_q = 1 / sqrt(|q|^2 + eps)   (dk alike, scale 1)
-//   dgraw = de e (-a) sigmoid(graw),  dA_log += sum_c de e g,  db = dbeta beta (1 - beta)
-// with dqt_sum / dkh_sum / de / dbeta the sums over the four row quarters (and, for dqt and dkh,
-// over the value heads of the group).  dA_log is accumulated per warp and added once per head
-// (per token and head when a group has more than 16 value heads).
+//   dq = scale r_q (dqt_sum - r_q^2 q (q . dqt_sum)),  r_q = 1 / sqrt(|q|^2 + eps)   (dk alike, scale 1)
+//   dgraw = dg (-a) sigmoid(graw),  dA_log += sum_c dg g,  db = dbeta beta (1 - beta)
+// with dqt_sum / dkh_sum the sums over the value heads of the group.  dA_log is accumulated
+// per warp and added once per head (per token and head when a group has more than 16 value
+// heads).
+// =====================================================================
 constexpr int BP_WARPS = 8;
 constexpr int BP_TOKENS = 64;   // tokens per warp
 
-__global__ __launch_bounds__(BP_WARPS * 32) void bwd_prologue_kernel(const BwdParams p, float *dq, float *dk,
-                                                                     float *dgraw, float *db, float *dA_log,
-                                                                     long long tokens) {
+__global__ __launch_bounds__(BP_WARPS * 32) void bwdc_jacobian_kernel(const BwdcParams p, float *dq, float *dk,
+                                                                      float *dgraw, float *db, float *dA_log,
+                                                                      long long tokens) {
     const int lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * BP_WARPS + (threadIdx.x >> 5);
     const long long n_ranges = (tokens + BP_TOKENS - 1) / BP_TOKENS;
@@ -347,15 +1064,13 @@ __global__ __launch_bounds__(BP_WARPS * 32) void bwd_prologue_kernel(const BwdPa
         const float qv[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
         const float kv[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
         float sq[4] = {0.f, 0.f, 0.f, 0.f}, sk[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int g = 0; g < group; ++g)
-#pragma unroll
-            for (int pt = 0; pt < BW_PARTS; ++pt) {
-                const size_t ho = (((size_t)tok * p.H_v + hq * group + g) * BW_PARTS + pt) * KD + 4 * lane;
-                const float4 a = *reinterpret_cast<const float4 *>(p.dqt + ho);
-                const float4 b = *reinterpret_cast<const float4 *>(p.dkh + ho);
-                sq[0] += a.x; sq[1] += a.y; sq[2] += a.z; sq[3] += a.w;
-                sk[0] += b.x; sk[1] += b.y; sk[2] += b.z; sk[3] += b.w;
-            }
+        for (int g = 0; g < group; ++g) {
+            const size_t ho = ((size_t)tok * p.H_v + hq * group + g) * KD + 4 * lane;
+            const float4 a = *reinterpret_cast<const float4 *>(p.dqt + ho);
+            const float4 b = *reinterpret_cast<const float4 *>(p.dkh + ho);
+            sq[0] += a.x; sq[1] += a.y; sq[2] += a.z; sq[3] += a.w;
+            sk[0] += b.x; sk[1] += b.y; sk[2] += b.z; sk[3] += b.w;
+        }
         float nq = 0.f, nk = 0.f, qd = 0.f, kd = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -380,25 +1095,18 @@ __global__ __launch_bounds__(BP_WARPS * 32) void bwd_prologue_kernel(const BwdPa
         for (int g = 0; g < group; ++g) {
             const int h = hq * group + g;
             const size_t vo = ((size_t)tok * p.H_v + h) * KD + 4 * lane;
-            const float a = ex2(p.A_log[h] * LOG2E);
+            const float a = ex2n(p.A_log[h]);
             const uint2 gw2 = *reinterpret_cast<const uint2 *>(p.graw + vo);
             const float gr[4] = {bf16_lo(gw2.x), bf16_hi(gw2.x), bf16_lo(gw2.y), bf16_hi(gw2.y)};
-            float de[4] = {0.f, 0.f, 0.f, 0.f}, dbeta = 0.f;
-#pragma unroll
-            for (int pt = 0; pt < BW_PARTS; ++pt) {
-                const float4 x = *reinterpret_cast<const float4 *>(p.de + (((size_t)tok * p.H_v + h) * BW_PARTS + pt) * KD + 4 * lane);
-                de[0] += x.x; de[1] += x.y; de[2] += x.z; de[3] += x.w;
-                dbeta += p.dbeta[((size_t)tok * p.H_v + h) * BW_PARTS + pt];
-            }
+            const float4 dg4 = *reinterpret_cast<const float4 *>(p.dg + vo);
+            const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
             float out[4], acc = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float sp = softplus_log2(gr[i]) * (1.0f / LOG2E);   // softplus (natural units)
-                const float gg = -a * sp, ee = __expf(gg);
                 const float sig = 1.0f / (1.0f + __expf(-gr[i]));
-                const float dg = de[i] * ee;
-                out[i] = dg * (-a) * sig;
-                acc = fmaf(dg, gg, acc);
+                out[i] = dgv[i] * (-a) * sig;
+                acc = fmaf(dgv[i], -a * sp, acc);
             }
             *reinterpret_cast<float4 *>(dgraw + vo) = make_float4(out[0], out[1], out[2], out[3]);
             acc = warp_sum(acc);
@@ -412,7 +1120,7 @@ __global__ __launch_bounds__(BP_WARPS * 32) void bwd_prologue_kernel(const BwdPa
             if (lane == 0) {
                 const float bb = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
                 const float beta = 1.0f / (1.0f + __expf(-bb));
-                db[(size_t)tok * p.H_v + h] = dbeta * beta * (1.0f - beta);
+                db[(size_t)tok * p.H_v + h] = p.dbeta[(size_t)tok * p.H_v + h] * beta * (1.0f - beta);
             }
         }
     }
@@ -426,28 +1134,31 @@ __global__ __launch_bounds__(BP_WARPS * 32) void bwd_prologue_kernel(const BwdPa
 // ---------------------------------------------------------------- host side
 namespace {
 size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+int sm_count() {
+    int dev = 0, nsm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    return nsm > 0 ? nsm : 1;
 }
+}  // namespace
 
-size_t bwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, int grid) {
+size_t bwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, int /*grid*/) {
     const long long nseq = varlen ? N : B, nck = max_chunks_for(N, B, T, varlen), tokens = (long long)B * T;
+    const size_t items = (size_t)(nck > 0 ? nck : 1) * H_v, tk = (size_t)(tokens > 0 ? tokens : 1) * H_v;
     size_t off = a256(256);
     off = a256(off + sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1));
     off = a256(off + sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1));
     off = a256(off + sizeof(int) * (size_t)(nseq > 0 ? nseq : 1));
-    off = a256(off + (size_t)BW_BPC * (nck > 0 ? nck : 1) * H_v * KD * KD * 4);       // checkpoints
-    off = a256(off + (size_t)grid * BW_CT * (KD / BW_PARTS) * KD * 4);          // scratch
-    off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * KD * 4 * 3);   // dqt, dkh, de
-    off = a256(off + (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * 4);            // dbeta
+    off = a256(off + items * BR_BYTES);
+    off = a256(off + items * ST_BYTES);
+    off = a256(off + items * ST_BYTES);
+    off = a256(off + items * 2 * CP_BYTES);
+    off = a256(off + tk * KD * 4 * 3);   // dqt, dkh, dg
+    off = a256(off + tk * 4);            // dbeta
     return off;
 }
 
-int bwd_grid(int nseq, int H_v) {
-    int dev = 0, nsm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-    const long long items = (long long)nseq * H_v * BW_PARTS, slots = 2LL * nsm;
-    return (int)(items < slots ? (items > 0 ? items : 1) : slots);
-}
+int bwd_grid(int, int) { return sm_count(); }
 
 cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *graw,
                        const uint16_t *b, const float *A_log, float scale, const float *init, const int32_t *cu, int N,
@@ -457,6 +1168,7 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     const bool varlen = cu != nullptr;
     const int nseq = varlen ? N : B;
     const long long nck = max_chunks_for(N, B, T, varlen), tokens = (long long)B * T;
+    const size_t items = (size_t)(nck > 0 ? nck : 1) * H_v, tk = (size_t)(tokens > 0 ? tokens : 1) * H_v;
     char *base = static_cast<char *>(ws_ptr);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -468,16 +1180,20 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     SeqDesc *seqs = reinterpret_cast<SeqDesc *>(take(sizeof(SeqDesc) * (size_t)(nseq > 0 ? nseq : 1)));
     ChunkDesc *chunks = reinterpret_cast<ChunkDesc *>(take(sizeof(ChunkDesc) * (size_t)(nck > 0 ? nck : 1)));
     int *order = reinterpret_cast<int *>(take(sizeof(int) * (size_t)(nseq > 0 ? nseq : 1)));
-    BwdParams bp;
-    bp.ckpt = reinterpret_cast<float *>(take((size_t)BW_BPC * (nck > 0 ? nck : 1) * H_v * KD * KD * 4));
-    bp.scratch = reinterpret_cast<float *>(take((size_t)grid * BW_CT * (KD / BW_PARTS) * KD * 4));
-    const size_t tv = (size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * KD;
-    float *t3 = reinterpret_cast<float *>(take(tv * 4 * 3));
-    bp.dqt = t3; bp.dkh = t3 + tv; bp.de = t3 + 2 * tv;
-    bp.dbeta = reinterpret_cast<float *>(take((size_t)(tokens > 0 ? tokens : 1) * H_v * BW_PARTS * 4));
+    BwdcParams bp;
+    bp.rec = reinterpret_cast<unsigned char *>(take(items * BR_BYTES));
+    bp.S0 = reinterpret_cast<float *>(take(items * ST_BYTES));
+    bp.dSC = reinterpret_cast<float *>(take(items * ST_BYTES));
+    bp.part = reinterpret_cast<unsigned char *>(take(items * 2 * CP_BYTES));
+    float *t3 = reinterpret_cast<float *>(take(tk * KD * 4 * 3));
+    bp.dqt = t3;
+    bp.dkh = t3 + tk * KD;
+    bp.dg = t3 + 2 * tk * KD;
+    bp.dbeta = reinterpret_cast<float *>(take(tk * 4));
     bp.q = q; bp.k = k; bp.v = v; bp.graw = graw; bp.b = b; bp.dout = dout;
     bp.A_log = A_log; bp.init = init; bp.dht = dht; bp.scale = scale;
-    bp.H_qk = H_qk; bp.H_v = H_v; bp.nseq = nseq; bp.seqs = seqs; bp.order = order; bp.hdr = hdr;
+    bp.H_qk = H_qk; bp.H_v = H_v; bp.nseq = nseq;
+    bp.seqs = seqs; bp.chunks = chunks; bp.order = order; bp.hdr = hdr;
     bp.dv = dv; bp.dh0 = dh0;
     *launches = 0;
     cudaError_t e = launch_plan(cu, N, B, T, seqs, chunks, order, hdr, nck, stream);
@@ -485,22 +1201,54 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     ++*launches;
     if ((e = cudaMemsetAsync(dA_log, 0, sizeof(float) * H_v, stream)) != cudaSuccess) return e;
     timing_mark("plan_kernel", stream);
-    if (nseq > 0) {
-        if ((e = cudaFuncSetAttribute(bwd_recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)(BW_BYTES + 128))) != cudaSuccess)
-            return e;
-        bwd_recur_kernel<<<grid, BW_THREADS, BW_BYTES + 128, stream>>>(bp);
+    const int nsm = grid > 0 ? grid : sm_count();
+    auto smem_attr = [](auto kern, uint32_t bytes) {
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(bytes + 128));
+    };
+    if (nck > 0) {
+        const long long n_items = nck * H_v;
+        const int g_items = (int)(n_items < nsm ? n_items : nsm);
+        if ((e = smem_attr(bwdc_prep_kernel, PS_BYTES)) != cudaSuccess) return e;
+        bwdc_prep_kernel<<<g_items, BC_THREADS, PS_BYTES + 128, stream>>>(bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        timing_mark("bwd_recur_kernel", stream);
+        timing_mark("bwdc_prep_kernel", stream);
+    }
+    if (nseq > 0) {
+        const unsigned chains = (unsigned)((long long)nseq * H_v * 2);
+        if ((e = smem_attr(bwdc_chain_kernel<false>, ChainCfg<false>::BYTES)) != cudaSuccess) return e;
+        if ((e = smem_attr(bwdc_chain_kernel<true>, ChainCfg<true>::BYTES)) != cudaSuccess) return e;
+        bwdc_chain_kernel<false><<<chains, BC_THREADS, ChainCfg<false>::BYTES + 128, stream>>>(bp);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        timing_mark("bwdc_chain_kernel<fwd>", stream);
+        bwdc_chain_kernel<true><<<chains, BC_THREADS, ChainCfg<true>::BYTES + 128, stream>>>(bp);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        timing_mark("bwdc_chain_kernel<bwd>", stream);
+    }
+    if (nck > 0) {
+        const long long n_items = nck * H_v;
+        const int g_items = (int)(n_items < nsm ? n_items : nsm);
+        const int g_units = (int)(2 * n_items < nsm ? 2 * n_items : nsm);
+        if ((e = smem_attr(bwdc_gradv_kernel, GV_BYTES)) != cudaSuccess) return e;
+        if ((e = smem_attr(bwdc_gradk_kernel, GK_BYTES)) != cudaSuccess) return e;
+        bwdc_gradv_kernel<<<g_units, BC_THREADS, GV_BYTES + 128, stream>>>(bp);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        timing_mark("bwdc_gradv_kernel", stream);
+        bwdc_gradk_kernel<<<g_items, BC_THREADS, GK_BYTES + 128, stream>>>(bp);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        timing_mark("bwdc_gradk_kernel", stream);
     }
     if (tokens > 0) {
         const long long warps = ((tokens + BP_TOKENS - 1) / BP_TOKENS) * H_qk;
-        bwd_prologue_kernel<<<(unsigned)((warps + BP_WARPS - 1) / BP_WARPS), BP_WARPS * 32, 0, stream>>>(
+        bwdc_jacobian_kernel<<<(unsigned)((warps + BP_WARPS - 1) / BP_WARPS), BP_WARPS * 32, 0, stream>>>(
             bp, dq, dk, dgraw, db, dA_log, tokens);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        timing_mark("bwd_prologue_kernel", stream);
+        timing_mark("bwdc_jacobian_kernel", stream);
     }
     return cudaSuccess;
 }

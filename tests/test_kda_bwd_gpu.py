@@ -1,10 +1,14 @@
 """GPU parity tests of kda_bwd (the backward of the KDA forward) against the
 fp64 autograd oracle, through the C ABI.
 
-The GPU computes the token recurrence backwards in fp32 from the exact bf16 /
-fp32 inputs, so the gradients differ from the fp64 oracle by fp32 rounding
-accumulated over the sequence: each gradient tensor must match to relative L2
-<= 1e-3 and max-abs <= 1e-2 of its largest reference magnitude."""
+The GPU computes the chunked (UT / WY) backward on tensor cores with tf32
+operands rounded to nearest and fp32 accumulation, so the gradients differ from
+the fp64 oracle by the operands' roundings (a few 1e-4 relative): each gradient
+tensor must match to relative L2 <= 1e-3 and max-abs <= 1e-2 of its largest
+reference magnitude.  dA_log is a sum over tokens and channels of dg * g whose
+terms cancel (by 50 to 200 fold on these inputs), so its error is bounded
+relative to the sum of the terms' magnitudes, sum |dg g| (per value head),
+which the reference's dgraw gives: dg g = dgraw softplus(graw) / sigmoid(graw)."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +21,21 @@ pytestmark = pytest.mark.gpu
 
 REL = 1e-3
 MAX_FRAC = 1e-2
+DALOG_FRAC = 1e-4   # |dA_log - ref| per head, relative to sum |dg g| of that head
+
+
+def _dalog_scale(inp, dgraw_ref):
+    """sum over tokens and channels of |dg g| per value head, from the reference dgraw."""
+    gr = inp.graw.double().numpy()
+    sp = np.maximum(gr, 0.0) + np.log1p(np.exp(-np.abs(gr)))
+    sig = 1.0 / (1.0 + np.exp(-gr))
+    return np.abs(np.asarray(dgraw_ref) * sp / sig).sum(axis=(0, 1, 3))
+
+
+def _check_dalog(inp, got, ref, tag=""):
+    scale = _dalog_scale(inp, ref["dgraw"])
+    err = np.abs(got - ref["dA_log"])
+    assert (err <= DALOG_FRAC * scale + 1e-30).all(), f"{tag}dA_log: error {err} vs sum|dg g| {scale}"
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -49,7 +68,8 @@ def _check(inp, seed, with_dht=True):
     do, dht = _grads(inp, seed, with_dht)
     got = _run(inp, do, dht)
     ref = {k_: v_.numpy() for k_, v_ in OB.bwd_inputs(inp, do, dht).items()}
-    for name in ("dq", "dk", "dv", "dgraw", "db", "dA_log", "dh0"):
+    _check_dalog(inp, got["dA_log"], ref)
+    for name in ("dq", "dk", "dv", "dgraw", "db", "dh0"):
         a, r = got[name], ref[name]
         assert a.shape == r.shape, (name, a.shape, r.shape)
         assert np.isfinite(a).all(), name
@@ -84,7 +104,7 @@ def test_bwd_zero_tokens_passes_dht():
 
 
 def test_bwd_longer_sequence():
-    """T = 1024 (16 chunks): checkpoints and the chunk-by-chunk reverse pass."""
+    """T = 1024 (16 chunks): both state chains over many chunks."""
     _check(KI.make_inputs(1, 1024, 1, 1, seed=705, with_state=True), seed=6)
 
 
@@ -106,7 +126,11 @@ def test_bwd_full_size_dense_sampled_heads():
         sel = {"dq": got["dq"][:, :, hq:hq + 1], "dk": got["dk"][:, :, hq:hq + 1], "dv": got["dv"][:, :, hq:hq + 1],
                "dgraw": got["dgraw"][:, :, hq:hq + 1], "db": got["db"][:, :, hq:hq + 1],
                "dA_log": got["dA_log"][hq:hq + 1], "dh0": got["dh0"][:, hq:hq + 1]}
+        _check_dalog(sub, sel["dA_log"].double().cpu().numpy(), {k_: v_.numpy() for k_, v_ in ref.items()},
+                     f"head {hq} ")
         for name, a in sel.items():
+            if name == "dA_log":
+                continue
             a = a.double().cpu().numpy()
             r = ref[name].numpy()
             e = rel_l2(a, r)
