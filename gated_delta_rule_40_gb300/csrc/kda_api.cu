@@ -303,11 +303,11 @@ int kda_decode_step(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
     return KDA_OK;
 }
 
-int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
-            const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
-            const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V, const kda_bf16_t *dout,
-            const float *dht, float *dq, float *dk, float *dv, float *dgraw, float *db, float *dA_log, float *dh0,
-            cudaStream_t stream) {
+namespace {
+int validate_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+                 const kda_bf16_t *b, const float *A_log, const float *initial_state, const int32_t *cu_seqlens, int N,
+                 int B, int T, int H_qk, int H_v, int K, int V, const kda_bf16_t *dout, const float *dht, float *dq,
+                 float *dk, float *dv, float *dgraw, float *db, float *dA_log, float *dh0) {
     int rc = validate_fwd(q, k, v, graw, b, A_log, initial_state, nullptr, cu_seqlens, N, B, T, H_qk, H_v, K, V,
                           dout);
     if (rc != KDA_OK) return rc;
@@ -317,18 +317,52 @@ int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const
     if ((dht && !aligned16(dht)) || !aligned16(dh0) ||
         (tokens > 0 && (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dgraw))))
         return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+}  // namespace
+
+size_t kda_bwd_workspace_size(int N, int B, int T, int H_qk, int H_v, int K, int V) {
+    if (K != kda::KD || V != kda::KD || B < 0 || T < 0 || H_qk <= 0 || H_v <= 0 || N < 0) return 0;
+    const size_t a = kda::bwd_workspace_bytes(N, B, T, H_v, true, 0);
+    const size_t b = kda::bwd_workspace_bytes(N, B, T, H_v, false, 0);
+    return a > b ? a : b;
+}
+
+int kda_bwd_ws(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+               const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
+               const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V,
+               const kda_bf16_t *dout, const float *dht, float *dq, float *dk, float *dv, float *dgraw, float *db,
+               float *dA_log, float *dh0, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    int rc = validate_bwd(q, k, v, graw, b, A_log, initial_state, cu_seqlens, N, B, T, H_qk, H_v, K, V, dout, dht,
+                          dq, dk, dv, dgraw, db, dA_log, dh0);
+    if (rc != KDA_OK) return rc;
     const bool varlen = cu_seqlens != nullptr;
-    const int grid = kda::bwd_grid(varlen ? N : B, H_v);
-    const size_t need = kda::bwd_workspace_bytes(varlen ? N : 0, B, T, H_v, varlen, grid);
-    void *ws = nullptr;
-    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    const size_t need = kda::bwd_workspace_bytes(varlen ? N : 0, B, T, H_v, varlen, 0);
+    if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need) return KDA_ERR_WORKSPACE;
     int launches = 0;
     kda::timing_begin(stream);
     const cudaError_t e = kda::launch_bwd(q, k, v, graw, b, A_log, scale, initial_state, cu_seqlens, varlen ? N : 0,
-                                          B, T, H_qk, H_v, dout, dht, dq, dk, dv, dgraw, db, dA_log, dh0, ws, grid,
-                                          stream, &launches);
-    rc = e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
-    if (rc == KDA_OK) t_last_launches = launches;
+                                          B, T, H_qk, H_v, dout, dht, dq, dk, dv, dgraw, db, dA_log, dh0, ws,
+                                          kda::bwd_grid(varlen ? N : B, H_v), stream, &launches);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    t_last_launches = launches;
+    return KDA_OK;
+}
+
+int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+            const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
+            const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V, const kda_bf16_t *dout,
+            const float *dht, float *dq, float *dk, float *dv, float *dgraw, float *db, float *dA_log, float *dh0,
+            cudaStream_t stream) {
+    int rc = validate_bwd(q, k, v, graw, b, A_log, initial_state, cu_seqlens, N, B, T, H_qk, H_v, K, V, dout, dht,
+                          dq, dk, dv, dgraw, db, dA_log, dh0);
+    if (rc != KDA_OK) return rc;
+    const bool varlen = cu_seqlens != nullptr;
+    const size_t need = kda::bwd_workspace_bytes(varlen ? N : 0, B, T, H_v, varlen, 0);
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    rc = kda_bwd_ws(q, k, v, graw, b, A_log, scale, initial_state, cu_seqlens, N, B, T, H_qk, H_v, K, V, dout, dht,
+                    dq, dk, dv, dgraw, db, dA_log, dh0, ws, need, stream);
     if (cudaFreeAsync(ws, stream) != cudaSuccess && rc == KDA_OK) rc = KDA_ERR_CUDA;
     return rc;
 }

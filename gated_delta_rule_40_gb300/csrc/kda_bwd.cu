@@ -131,7 +131,7 @@ __device__ __forceinline__ float ex2n(float x) { return ex2(x * LOG2E); }   // e
 constexpr uint32_t BR_W = 0, BR_KD = 32768, BR_N = 65536, BR_U = 98304, BR_P = 131072, BR_T = 147456,
                    BR_KK = 163840, BR_D = 180224, BR_BETA = 180736, BR_BYTES = 181248;
 constexpr uint32_t ST_BYTES = 65536;   // a state per item: [2 V blocks][64 v][128 k] fp32 tiles
-// Per (item, V half), written by bwdc_gradv_kernel (sums over that half's 64 value columns):
+// Per item, written by bwdc_gradv_kernel (sums over the 128 value columns):
 //   dKd, dQg, dW [64][128];  dP (lower), dT's V term [64][64];  dbeta's V term [64];  colsum(S_0 dS_C) [128]
 constexpr uint32_t CP_DKD = 0, CP_DQG = 32768, CP_DW = 65536, CP_DP = 98304, CP_DT = 114688, CP_DB = 131072,
                    CP_DGC = 131328, CP_BYTES = 131840;
@@ -147,7 +147,7 @@ struct BwdcParams {
     const int *hdr;
     unsigned char *rec;     // [item] BR_BYTES
     float *S0, *dSC;        // [item] ST_BYTES: state entering / state gradient leaving each chunk
-    unsigned char *part;    // [item][2] CP_BYTES
+    unsigned char *part;    // [item] CP_BYTES
     float *dqt, *dkh, *dg;  // [token][H_v][128]: gradients of Qt, Kh, g
     float *dbeta;           // [token][H_v]
     float *dv, *dh0;
@@ -195,14 +195,29 @@ __device__ void bwdc_rows(const BwdcParams &p, int tok0, int len, int h, int hq,
         if (lane == 0) sBeta[r] = beta;
     }
     __syncthreads();
-    if (tid < KD) {
+    // prefix sums down each channel: rows 0..31 and 32..63 by two threads, then the second
+    // half adds the first half's total
+    static_assert(BC_THREADS == 2 * KD, "two threads per channel");
+    {
+        const int c = tid & (KD - 1), r0 = 32 * (tid >> 7);
         float s = 0.f;
-        for (int r = 0; r < CH; ++r) {
-            const int o = toff<KD>(r, tid);
+        for (int r = r0; r < r0 + 32; ++r) {
+            const int o = toff<KD>(r, c);
             s += sG[o];
             sG[o] = s;
         }
-        sD[tid] = ex2n(s);
+    }
+    __syncthreads();
+    if (tid >= KD) {
+        const int c = tid - KD;
+        const float base = sG[toff<KD>(31, c)];
+        float last = 0.f;
+        for (int r = 32; r < CH; ++r) {
+            const int o = toff<KD>(r, c);
+            last = sG[o] + base;
+            sG[o] = last;
+        }
+        sD[c] = ex2n(last);
     }
     __syncthreads();
 }
@@ -449,30 +464,35 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
 
     auto chunk_of = [&](int s) { return BWD ? n - 1 - s : s; };
     auto item_of = [&](int s) { return ((size_t)sd.chunk0 + chunk_of(s)) * p.H_v + h; };
-    auto issue = [&](int s) {   // thread 0: the ring tiles and extras of step s
+    auto issue = [&](int s) {   // warp 0: the ring tiles and extras of step s
         const unsigned char *rec = p.rec + item_of(s) * BR_BYTES;
         const uint32_t offs[3] = {BWD ? BR_KD : BR_W, BWD ? BR_W : BR_KD, BR_N};
-#pragma unroll
-        for (int op = 0; op < Cfg::OPS; ++op) {
-            const int slot = (Cfg::OPS * s + op) % Cfg::SLOTS;
-            mbar_expect_tx(bar + 8 * slot, 32768);
-            bulk_g2s(sbase + Cfg::RING + slot * 32768, rec + offs[op], 32768, bar + 8 * slot);
-        }
         const uint32_t ab = bar + 8 * (Cfg::SLOTS + (s & 1)), aux = sbase + Cfg::AUXB + (s & 1) * Cfg::AUX;
+        const int c = chunk_of(s), len = min(CH, sd.len - c * CH), tok0 = sd.tok + c * CH;
+        if (lane == 0) {
+#pragma unroll
+            for (int op = 0; op < Cfg::OPS; ++op) {
+                const int slot = (Cfg::OPS * s + op) % Cfg::SLOTS;
+                mbar_expect_tx(bar + 8 * slot, 32768);
+                bulk_g2s(sbase + Cfg::RING + slot * 32768, rec + offs[op], 32768, bar + 8 * slot);
+            }
+            if (BWD) {
+                mbar_expect_tx(ab, 512 + 128 * len);
+                bulk_g2s(aux, rec + BR_D, 512, ab);
+            } else {
+                mbar_expect_tx(ab, 512 + CH * CH * 4);
+                bulk_g2s(aux, rec + BR_D, 512, ab);
+                bulk_g2s(aux + 512, rec + BR_U + vb * (CH * CH * 4), CH * CH * 4, ab);
+            }
+        }
         if (BWD) {
-            const int c = chunk_of(s), len = min(CH, sd.len - c * CH), tok0 = sd.tok + c * CH;
-            mbar_expect_tx(ab, 512 + 128 * len);
-            bulk_g2s(aux, rec + BR_D, 512, ab);
-            for (int r = 0; r < len; ++r)
+            __syncwarp();   // the expected byte count is posted before any row lands
+            for (int r = lane; r < len; r += 32)
                 bulk_g2s(aux + 512 + r * Cfg::DO_STRIDE, p.dout + ((size_t)(tok0 + r) * p.H_v + h) * KD + vb * CH,
                          128, ab);
-        } else {
-            mbar_expect_tx(ab, 512 + CH * CH * 4);
-            bulk_g2s(aux, rec + BR_D, 512, ab);
-            bulk_g2s(aux + 512, rec + BR_U + vb * (CH * CH * 4), CH * CH * 4, ab);
         }
     };
-    if (tid == 0 && n > 0) issue(0);
+    if (warp == 0 && n > 0) issue(0);
 
     float *outbase = BWD ? p.dSC : p.S0;
     bool ok = true;
@@ -515,7 +535,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
             },
             warp, lane);
         __syncthreads();   // Z complete; op1 consumed
-        if (tid == 0 && s + 1 < n) issue(s + 1);
+        if (warp == 0 && s + 1 < n) issue(s + 1);
         // ---- X <- X Diag(D) + Z op2 (+ dO^T N)
         {
             const int m0 = 32 * (warp >> 2), n0 = 32 * (warp & 3);
@@ -567,16 +587,17 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
 }
 
 // =====================================================================
-// Gradients over the value dimension, per (item, V half vh) (64 value columns):
+// Gradients over the value dimension, per item, the two 64-column halves of V in turn
+// (S0_h, dS_h: rows of that half of the states):
 //   Delta_h = U_h - W S0_h^T,  dDelta_h = P^T dO_h + Kd dS_h^T        (64 r x 64 v)
-//   dKd += Delta_h dS_h,  dQg += dO_h S0_h,  dW += -dDelta_h S0_h      (64 r x 128 k)
-//   dP += dO_h Delta_h^T,  dT += dDelta_h (beta V_h)^T                 (64 x 64)
+//   dKd += Delta_h dS_h,  dQg += dO_h S0_h,  dW += -dDelta_h S0_h      (64 r x 128 k, registers)
+//   dP += dO_h Delta_h^T,  dT += dDelta_h (beta V_h)^T                 (64 x 64, registers)
 //   dv_h = beta (T^T dDelta_h),  dbeta += rowsum(T^T dDelta_h * V_h),  dGam_C += colsum(S0_h * dS_h)
-// (S0_h, dS_h: rows vh of the states), the sums written per half to the item's partials.
+// then the sums to the item's record of value-side gradients.
 // =====================================================================
 constexpr uint32_t GV_W = 0, GV_KD = 32768, GV_S0 = 65536, GV_DS = 98304, GV_U = 131072, GV_P = 147456,
                    GV_T = 163840, GV_DO = 180224, GV_V = 196608, GV_DDL = 212992, GV_MISC = 229376,
-                   GV_BAR = GV_MISC + 1536, GV_BYTES = GV_BAR + 16;
+                   GV_BAR = GV_MISC + 2304, GV_BYTES = GV_BAR + 16;
 static_assert(GV_BYTES + 128 <= 232448, "gradv smem");
 
 __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcParams p) {
@@ -588,134 +609,151 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
     float *sU = reinterpret_cast<float *>(sm + GV_U), *sP = reinterpret_cast<float *>(sm + GV_P);
     float *sT = reinterpret_cast<float *>(sm + GV_T), *sDO = reinterpret_cast<float *>(sm + GV_DO);
     float *sV = reinterpret_cast<float *>(sm + GV_V), *sDD = reinterpret_cast<float *>(sm + GV_DDL);
-    float *sD = reinterpret_cast<float *>(sm + GV_MISC), *sBeta = sD + 128, *sDB = sD + 192, *sGC = sD + 256;
-    const uint32_t sbase = smem_u32(sm), bar = sbase + GV_BAR;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const long long n_units = 2LL * p.hdr[0] * p.H_v;
+    // D [128], beta [64], then the two warps' row sums of dbeta's V term [2][64] and the two
+    // threads' column sums of S0 dS [2][128] (added in a fixed order: reproducible results)
+    float *sD = reinterpret_cast<float *>(sm + GV_MISC), *sBeta = sD + 128, *sDB = sD + 192, *sGC = sD + 320;
+    const uint32_t sbase = smem_u32(sm), bar_item = sbase + GV_BAR, bar_half = bar_item + 8;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const long long n_items = (long long)p.hdr[0] * p.H_v;
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar_item, 1);
+        mbar_init(bar_half, 1);
         mbar_fence_init();
     }
     __syncthreads();
-    uint32_t phase = 0;
-    for (long long unit = blockIdx.x; unit < n_units; unit += gridDim.x, phase ^= 1) {
-        const long long item = unit >> 1;
-        const int vh = (int)(unit & 1);
+    // fixed output tiles of this warp: 32 x 32 of the 64 x 128 products, 16 x 32 of the 64 x 64 ones
+    const int bm0 = 32 * (warp >> 2), bn0 = 32 * (warp & 3), sm0 = 16 * (warp >> 1), sn0 = 32 * (warp & 1);
+    uint32_t ph_item = 0, ph_half = 0;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ph_item ^= 1) {
         const int h = (int)(item % p.H_v);
         const ChunkDesc cd = p.chunks[item / p.H_v];
         const int len = cd.len;
         const unsigned char *rec = p.rec + (size_t)item * BR_BYTES;
-        unsigned char *part = p.part + ((size_t)item * 2 + vh) * CP_BYTES;
-        __syncthreads();   // the previous unit's reads of shared memory are done
-        if (tid == 0) {
-            mbar_expect_tx(bar, 4 * 32768 + 3 * 16384 + 768);
-            bulk_g2s(sbase + GV_W, rec + BR_W, 32768, bar);
-            bulk_g2s(sbase + GV_KD, rec + BR_KD, 32768, bar);
-            bulk_g2s(sbase + GV_S0, p.S0 + item * (ST_BYTES / 4) + vh * (CH * KD), 32768, bar);
-            bulk_g2s(sbase + GV_DS, p.dSC + item * (ST_BYTES / 4) + vh * (CH * KD), 32768, bar);
-            bulk_g2s(sbase + GV_U, rec + BR_U + vh * 16384, 16384, bar);
-            bulk_g2s(sbase + GV_P, rec + BR_P, 16384, bar);
-            bulk_g2s(sbase + GV_T, rec + BR_T, 16384, bar);
-            bulk_g2s(sbase + GV_MISC, rec + BR_D, 768, bar);   // D [128], beta [64]
-        }
-        // dO and V of this half (fp32 tiles, zero past len)
-        for (int idx = tid; idx < 2 * CH * 8; idx += BC_THREADS) {
-            const int which = idx >> 9, r = (idx >> 3) & 63, c = 8 * (idx & 7);
-            float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
-            if (r < len) {
-                const uint16_t *src = which ? p.v : p.dout;
-                const uint4 w = *reinterpret_cast<const uint4 *>(src + ((size_t)(cd.tok + r) * p.H_v + h) * KD + vh * CH + c);
-                lo = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-                hi = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+        unsigned char *part = p.part + (size_t)item * CP_BYTES;
+        float akd[2][4][4], aqg[2][4][4], aw[2][4][4], ap[1][4][4], at[1][4][4];
+        float dbr[2] = {0.f, 0.f}, gcs = 0.f;   // this thread's dbeta row sums and S0 dS column sum
+        tile_zero(akd);
+        tile_zero(aqg);
+        tile_zero(aw);
+        tile_zero(ap);
+        tile_zero(at);
+        bool ok = true;
+        for (int vh = 0; vh < 2; ++vh, ph_half ^= 1) {
+            __syncthreads();   // the previous half's (item's) reads of shared memory are done
+            if (tid == 0) {
+                if (vh == 0) {
+                    mbar_expect_tx(bar_item, 2 * 32768 + 2 * 16384 + 768);
+                    bulk_g2s(sbase + GV_W, rec + BR_W, 32768, bar_item);
+                    bulk_g2s(sbase + GV_KD, rec + BR_KD, 32768, bar_item);
+                    bulk_g2s(sbase + GV_P, rec + BR_P, 16384, bar_item);
+                    bulk_g2s(sbase + GV_T, rec + BR_T, 16384, bar_item);
+                    bulk_g2s(sbase + GV_MISC, rec + BR_D, 768, bar_item);   // D [128], beta [64]
+                }
+                mbar_expect_tx(bar_half, 2 * 32768 + 16384);
+                bulk_g2s(sbase + GV_S0, p.S0 + item * (ST_BYTES / 4) + vh * (CH * KD), 32768, bar_half);
+                bulk_g2s(sbase + GV_DS, p.dSC + item * (ST_BYTES / 4) + vh * (CH * KD), 32768, bar_half);
+                bulk_g2s(sbase + GV_U, rec + BR_U + vh * 16384, 16384, bar_half);
             }
-            float *dst = which ? sV : sDO;
-            *reinterpret_cast<float4 *>(dst + toff<CH>(r, c)) = lo;
-            *reinterpret_cast<float4 *>(dst + toff<CH>(r, c + 4)) = hi;
+            // dO and V of this half (fp32 tiles, zero past len)
+            for (int idx = tid; idx < 2 * CH * 8; idx += BC_THREADS) {
+                const int which = idx >> 9, r = (idx >> 3) & 63, c = 8 * (idx & 7);
+                float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+                if (r < len) {
+                    const uint16_t *src = which ? p.v : p.dout;
+                    const uint4 w =
+                        *reinterpret_cast<const uint4 *>(src + ((size_t)(cd.tok + r) * p.H_v + h) * KD + vh * CH + c);
+                    lo = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+                    hi = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+                }
+                float *dst = which ? sV : sDO;
+                *reinterpret_cast<float4 *>(dst + toff<CH>(r, c)) = lo;
+                *reinterpret_cast<float4 *>(dst + toff<CH>(r, c + 4)) = hi;
+            }
+            bool mine = (vh > 0 || mbar_wait(bar_item, ph_item)) && mbar_wait(bar_half, ph_half);
+            if (!__syncthreads_and(mine)) {
+                ok = false;
+                break;
+            }
+            // ---- Delta (in place of U) and dDelta
+            cta_gemm<CH, CH, 1, 4, BC_WARPS>(
+                KD, [&](int r, int k) { return sW[toff<KD>(r, k)]; }, [&](int k, int v) { return sS0[toff<KD>(v, k)]; },
+                [&](int r, int v, float e0, float e1) {
+                    const int o = toff<CH>(r, v);
+                    st2(sU + o, sU[o] - e0, sU[o + 1] - e1);
+                },
+                warp, lane);
+            {
+                float acc[1][4][4];
+                tile_zero(acc);
+                mma_tile<1, 4>(acc, sm0, sn0, 0, CH, [&](int r, int j) { return sP[toff<CH>(j, r)]; },
+                               [&](int j, int v) { return sDO[toff<CH>(j, v)]; }, g, t);
+                mma_tile<1, 4>(acc, sm0, sn0, 0, KD, [&](int r, int k) { return sKd[toff<KD>(r, k)]; },
+                               [&](int k, int v) { return sDS[toff<KD>(v, k)]; }, g, t);
+                tile_out<1, 4>(acc, sm0, sn0, g, t,
+                               [&](int r, int v, float v0, float v1) { st2(sDD + toff<CH>(r, v), v0, v1); });
+            }
+            __syncthreads();
+            // ---- the sums over this half's value columns
+            mma_tile<2, 4>(akd, bm0, bn0, 0, CH, [&](int r, int v) { return sU[toff<CH>(r, v)]; },
+                           [&](int v, int k) { return sDS[toff<KD>(v, k)]; }, g, t);
+            mma_tile<2, 4>(aqg, bm0, bn0, 0, CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; },
+                           [&](int v, int k) { return sS0[toff<KD>(v, k)]; }, g, t);
+            mma_tile<2, 4>(aw, bm0, bn0, 0, CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
+                           [&](int v, int k) { return sS0[toff<KD>(v, k)]; }, g, t);
+            mma_tile<1, 4>(ap, sm0, sn0, 0, CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; },
+                           [&](int v, int j) { return sU[toff<CH>(j, v)]; }, g, t);
+            mma_tile<1, 4>(at, sm0, sn0, 0, CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
+                           [&](int v, int j) { return sBeta[j] * sV[toff<CH>(j, v)]; }, g, t);
+            // dBV = T^T dDelta: dv and dbeta's V term
+            {
+                float acc[1][4][4];
+                tile_zero(acc);
+                mma_tile<1, 4>(acc, sm0, sn0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
+                               [&](int j, int v) { return sDD[toff<CH>(j, v)]; }, g, t);
+                float rs[2] = {0.f, 0.f};
+                tile_out<1, 4>(acc, sm0, sn0, g, t, [&](int r, int v, float v0, float v1) {
+                    const int o = toff<CH>(r, v);
+                    rs[(r - sm0) >> 3] += v0 * sV[o] + v1 * sV[o + 1];
+                    if (r < len) {
+                        const float be = sBeta[r];
+                        st2(p.dv + ((size_t)(cd.tok + r) * p.H_v + h) * KD + vh * CH + v, be * v0, be * v1);
+                    }
+                });
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 1);
+                    rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 2);
+                    dbr[e] += rs[e];
+                }
+            }
+            // colsum(S0_h * dS_h) per channel (this thread: 32 of the half's rows)
+            {
+                const int c = tid & 127, v0 = 32 * (tid >> 7);
+                for (int v = v0; v < v0 + 32; ++v) gcs = fmaf(sS0[toff<KD>(v, c)], sDS[toff<KD>(v, c)], gcs);
+            }
         }
-        if (tid < 64) sDB[tid] = 0.f;
-        if (tid < 128) sGC[tid] = 0.f;
-        const bool mine = mbar_wait(bar, phase);
-        if (!__syncthreads_and(mine)) {
+        if (!ok) {
             if (tid == 0) set_status(KDA_ERR_DEVICE_TIMEOUT);
             break;
         }
-        // ---- Delta (in place of U) and dDelta
-        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
-            KD, [&](int r, int k) { return sW[toff<KD>(r, k)]; }, [&](int k, int v) { return sS0[toff<KD>(v, k)]; },
-            [&](int r, int v, float e0, float e1) {
-                const int o = toff<CH>(r, v);
-                st2(sU + o, sU[o] - e0, sU[o + 1] - e1);
-            },
-            warp, lane);
-        {
-            const int g = lane >> 2, t = lane & 3, m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1);
-            float acc[1][4][4];
-            tile_zero(acc);
-            mma_tile<1, 4>(acc, m0, n0, 0, CH, [&](int r, int j) { return sP[toff<CH>(j, r)]; },
-                           [&](int j, int v) { return sDO[toff<CH>(j, v)]; }, g, t);
-            mma_tile<1, 4>(acc, m0, n0, 0, KD, [&](int r, int k) { return sKd[toff<KD>(r, k)]; },
-                           [&](int k, int v) { return sDS[toff<KD>(v, k)]; }, g, t);
-            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int v, float v0, float v1) { st2(sDD + toff<CH>(r, v), v0, v1); });
-        }
-        __syncthreads();
         float *pDKD = reinterpret_cast<float *>(part + CP_DKD), *pDQG = reinterpret_cast<float *>(part + CP_DQG);
         float *pDW = reinterpret_cast<float *>(part + CP_DW), *pDP = reinterpret_cast<float *>(part + CP_DP);
         float *pDT = reinterpret_cast<float *>(part + CP_DT);
-        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
-            CH, [&](int r, int v) { return sU[toff<CH>(r, v)]; }, [&](int v, int k) { return sDS[toff<KD>(v, k)]; },
-            [&](int r, int k, float v0, float v1) { st2(pDKD + toff<KD>(r, k), v0, v1); }, warp, lane);
-        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
-            CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; }, [&](int v, int k) { return sS0[toff<KD>(v, k)]; },
-            [&](int r, int k, float v0, float v1) { st2(pDQG + toff<KD>(r, k), v0, v1); }, warp, lane);
-        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
-            CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; }, [&](int v, int k) { return sS0[toff<KD>(v, k)]; },
-            [&](int r, int k, float v0, float v1) { st2(pDW + toff<KD>(r, k), -v0, -v1); }, warp, lane);
-        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
-            CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; }, [&](int v, int j) { return sU[toff<CH>(j, v)]; },
-            [&](int r, int j, float v0, float v1) {
-                st2(pDP + toff<CH>(r, j), j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
-            },
-            warp, lane);
-        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
-            CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
-            [&](int v, int j) { return sBeta[j] * sV[toff<CH>(j, v)]; },
-            [&](int r, int j, float v0, float v1) { st2(pDT + toff<CH>(r, j), v0, v1); }, warp, lane);
-        // dBV = T^T dDelta: dv and dbeta's V term
-        {
-            const int g = lane >> 2, t = lane & 3, m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1);
-            float acc[1][4][4];
-            tile_zero(acc);
-            mma_tile<1, 4>(acc, m0, n0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
-                           [&](int j, int v) { return sDD[toff<CH>(j, v)]; }, g, t);
-            float rs[2] = {0.f, 0.f};
-            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int v, float v0, float v1) {
-                const int o = toff<CH>(r, v);
-                rs[(r - m0) >> 3] += v0 * sV[o] + v1 * sV[o + 1];
-                if (r < len) {
-                    const float be = sBeta[r];
-                    st2(p.dv + ((size_t)(cd.tok + r) * p.H_v + h) * KD + vh * CH + v, be * v0, be * v1);
-                }
-            });
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 1);
-                rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 2);
-            }
-            if (t == 0) {
-                atomicAdd(sDB + m0 + g, rs[0]);
-                atomicAdd(sDB + m0 + g + 8, rs[1]);
-            }
+        tile_out<2, 4>(akd, bm0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDKD + toff<KD>(r, k), v0, v1); });
+        tile_out<2, 4>(aqg, bm0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDQG + toff<KD>(r, k), v0, v1); });
+        tile_out<2, 4>(aw, bm0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDW + toff<KD>(r, k), -v0, -v1); });
+        tile_out<1, 4>(ap, sm0, sn0, g, t, [&](int r, int j, float v0, float v1) {
+            st2(pDP + toff<CH>(r, j), j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
+        });
+        tile_out<1, 4>(at, sm0, sn0, g, t, [&](int r, int j, float v0, float v1) { st2(pDT + toff<CH>(r, j), v0, v1); });
+        if (t == 0) {
+            sDB[(warp & 1) * 64 + sm0 + g] = dbr[0];
+            sDB[(warp & 1) * 64 + sm0 + g + 8] = dbr[1];
         }
-        // colsum(S0_h * dS_h) per channel
-        {
-            const int c = tid & 127, v0 = 32 * (tid >> 7);
-            float s = 0.f;
-            for (int v = v0; v < v0 + 32; ++v) s = fmaf(sS0[toff<KD>(v, c)], sDS[toff<KD>(v, c)], s);
-            atomicAdd(sGC + c, s);
-        }
+        sGC[(tid >> 7) * 128 + (tid & 127)] = gcs;
         __syncthreads();
-        if (tid < 64) reinterpret_cast<float *>(part + CP_DB)[tid] = sDB[tid];
-        if (tid < 128) reinterpret_cast<float *>(part + CP_DGC)[tid] = sGC[tid];
+        if (tid < 64) reinterpret_cast<float *>(part + CP_DB)[tid] = sDB[tid] + sDB[64 + tid];
+        if (tid < 128) reinterpret_cast<float *>(part + CP_DGC)[tid] = sGC[tid] + sGC[128 + tid];
     }
 }
 
@@ -729,7 +767,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
 // and dg per channel from dGam's suffix sums, dGam_C and the exclusive prefix sums of dKd Kd.
 // =====================================================================
 constexpr uint32_t GK_KH = 0, GK_QT = 32768, GK_G = 65536, GK_DW = 98304, GK_T = 131072, GK_KK = 147456,
-                   GK_DT = 163840, GK_X = 180224, GK_DP = 196608, GK_MISC = 212992, GK_BAR = GK_MISC + 2048,
+                   GK_DT = 163840, GK_X = 180224, GK_DP = 196608, GK_MISC = 212992, GK_BAR = GK_MISC + 4096,
                    GK_BYTES = GK_BAR + 16;
 static_assert(GK_BYTES + 128 <= 232448, "gradk smem");
 
@@ -742,8 +780,10 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
     float *sT = reinterpret_cast<float *>(sm + GK_T), *sKK = reinterpret_cast<float *>(sm + GK_KK);
     float *sDT = reinterpret_cast<float *>(sm + GK_DT), *sX = reinterpret_cast<float *>(sm + GK_X);
     float *sDP = reinterpret_cast<float *>(sm + GK_DP);
+    // beta [64], D [128], dGam_C [128], dbeta's V term [64], then the dbeta row sums of the
+    // dA products (two warps per row block) [2][64] and of the dBW products (one per warp) [8][64]
     float *sBeta = reinterpret_cast<float *>(sm + GK_MISC), *sD = sBeta + 64, *sDGC = sBeta + 192,
-          *sDB = sBeta + 320;
+          *sDB = sBeta + 320, *sDBa = sBeta + 384, *sDBw = sBeta + 512;
     const uint32_t sbase = smem_u32(sm), bar = sbase + GK_BAR;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const long long n_items = (long long)p.hdr[0] * p.H_v;
@@ -760,33 +800,19 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
         const int hq = h / group, len = cd.len;
         const float a = ex2n(p.A_log[h]);
         const unsigned char *rec = p.rec + (size_t)item * BR_BYTES;
-        const unsigned char *pt0 = p.part + (size_t)item * 2 * CP_BYTES, *pt1 = pt0 + CP_BYTES;
+        const unsigned char *pt = p.part + (size_t)item * CP_BYTES;
         __syncthreads();
         if (tid == 0) {
-            mbar_expect_tx(bar, 2 * 16384);
+            mbar_expect_tx(bar, 2 * 16384 + 32768 + 2 * 16384);
             bulk_g2s(sbase + GK_T, rec + BR_T, 16384, bar);
             bulk_g2s(sbase + GK_KK, rec + BR_KK, 16384, bar);
+            bulk_g2s(sbase + GK_DW, pt + CP_DW, 32768, bar);
+            bulk_g2s(sbase + GK_DT, pt + CP_DT, 16384, bar);
+            bulk_g2s(sbase + GK_DP, pt + CP_DP, 16384, bar);
         }
-        // the two halves' partial sums: dW, dT's V term, dP; dbeta's V term, colsum(S0 dS_C)
-        for (int idx = tid; idx < CH * KD / 4; idx += BC_THREADS) {
-            const float4 x = reinterpret_cast<const float4 *>(pt0 + CP_DW)[idx];
-            const float4 y = reinterpret_cast<const float4 *>(pt1 + CP_DW)[idx];
-            reinterpret_cast<float4 *>(sDW)[idx] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
-        }
-        for (int idx = tid; idx < CH * CH / 4; idx += BC_THREADS) {
-            float4 x = reinterpret_cast<const float4 *>(pt0 + CP_DT)[idx];
-            float4 y = reinterpret_cast<const float4 *>(pt1 + CP_DT)[idx];
-            reinterpret_cast<float4 *>(sDT)[idx] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
-            x = reinterpret_cast<const float4 *>(pt0 + CP_DP)[idx];
-            y = reinterpret_cast<const float4 *>(pt1 + CP_DP)[idx];
-            reinterpret_cast<float4 *>(sDP)[idx] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
-        }
-        if (tid < 64)
-            sDB[tid] = reinterpret_cast<const float *>(pt0 + CP_DB)[tid] + reinterpret_cast<const float *>(pt1 + CP_DB)[tid];
+        if (tid < 64) sDB[tid] = reinterpret_cast<const float *>(pt + CP_DB)[tid];
         bwdc_rows(p, cd.tok, len, h, hq, a, sKh, sQt, sG, sBeta, sD, tid);
-        if (tid < 128)
-            sDGC[tid] = (reinterpret_cast<const float *>(pt0 + CP_DGC)[tid] +
-                         reinterpret_cast<const float *>(pt1 + CP_DGC)[tid]) * sD[tid];
+        if (tid < 128) sDGC[tid] = reinterpret_cast<const float *>(pt + CP_DGC)[tid] * sD[tid];
         const bool mine = mbar_wait(bar, phase);
         if (!__syncthreads_and(mine)) {
             if (tid == 0) set_status(KDA_ERR_DEVICE_TIMEOUT);
@@ -828,8 +854,8 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
                 rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 2);
             }
             if (t == 0) {
-                atomicAdd(sDB + m0 + g, rs[0]);
-                atomicAdd(sDB + m0 + g + 8, rs[1]);
+                sDBa[(warp & 1) * 64 + m0 + g] = rs[0];
+                sDBa[(warp & 1) * 64 + m0 + g + 8] = rs[1];
             }
         }
         // ---- this warp's channels: dBW = T^T dW and the beta dBW terms
@@ -865,7 +891,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             }
             if (t == 0)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) atomicAdd(sDB + 16 * (e >> 1) + g + 8 * (e & 1), rs[e]);
+                for (int e = 0; e < 8; ++e) sDBw[warp * 64 + 16 * (e >> 1) + g + 8 * (e & 1)] = rs[e];
         }
         __syncthreads();   // M complete
         // ---- decayed pair products on this warp's channels
@@ -965,8 +991,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
                 }
         }
         // ---- the remaining terms, dqt / dkh out, dGam and dKd Kd to shared memory
-        const float *q0 = reinterpret_cast<const float *>(pt0 + CP_DKD), *q1 = reinterpret_cast<const float *>(pt1 + CP_DKD);
-        const float *w0 = reinterpret_cast<const float *>(pt0 + CP_DQG), *w1 = reinterpret_cast<const float *>(pt1 + CP_DQG);
+        const float *pkd = reinterpret_cast<const float *>(pt + CP_DKD), *pqg = reinterpret_cast<const float *>(pt + CP_DQG);
         float kdk[4][2][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -975,10 +1000,9 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int r = 16 * i + g + 8 * hh, c = cw + 8 * jn + 2 * t, o = toff<KD>(r, c);
-                    const float2 dk0 = *reinterpret_cast<const float2 *>(q0 + o), dk1 = *reinterpret_cast<const float2 *>(q1 + o);
-                    const float2 dq0 = *reinterpret_cast<const float2 *>(w0 + o), dq1 = *reinterpret_cast<const float2 *>(w1 + o);
+                    const float2 dk2 = *reinterpret_cast<const float2 *>(pkd + o), dq2 = *reinterpret_cast<const float2 *>(pqg + o);
                     const float dpd = sDP[toff<CH>(r, r)];
-                    const float dkd[2] = {dk0.x + dk1.x, dk0.y + dk1.y}, dqg[2] = {dq0.x + dq1.x, dq0.y + dq1.y};
+                    const float dkd[2] = {dk2.x, dk2.y}, dqg[2] = {dq2.x, dq2.y};
                     float okh[2], oqt[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
@@ -1008,56 +1032,67 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
                     st2(sQt + o, kdk[i][jn][2 * hh], kdk[i][jn][2 * hh + 1]);
                 }
         __syncthreads();
-        // ---- dg = suffix sums of dGam + dGam_C + exclusive prefix sums of dKd Kd; dbeta
-        if (tid < KD) {
-            const int c = tid;
+        // ---- dg = suffix sums of dGam + dGam_C + exclusive prefix sums of dKd Kd (two threads
+        // per channel: rows 0..31 and 32..63, each half's total passed to the other); dbeta
+        {
+            const int c = tid & (KD - 1), half = tid >> 7, r0 = 32 * half;
             float pre = 0.f;
-            for (int r = 0; r < CH; ++r) {
+            for (int r = r0; r < r0 + 32; ++r) {
                 const int o = toff<KD>(r, c);
                 const float x = sQt[o];
                 sQt[o] = pre;
                 pre += x;
             }
             float suf = 0.f;
-            const float dgc = sDGC[c];
-            for (int r = CH - 1; r >= 0; --r) {
+            for (int r = r0 + 31; r >= r0; --r) {
                 const int o = toff<KD>(r, c);
                 suf += sDW[o];
-                if (r < len) p.dg[((size_t)(cd.tok + r) * p.H_v + h) * KD + c] = suf + dgc + sQt[o];
+                sDW[o] = suf;
             }
-        } else if (tid < KD + CH) {
-            const int r = tid - KD;
-            if (r < len) p.dbeta[(size_t)(cd.tok + r) * p.H_v + h] = sDB[r];
+            if (half == 0) sX[c] = pre;        // dKd Kd summed over rows 0..31
+            else sX[KD + c] = suf;             // dGam summed over rows 32..63
+        }
+        __syncthreads();
+        {
+            const int c = tid & (KD - 1), half = tid >> 7, r0 = 32 * half;
+            const float add = (half ? sX[c] : sX[KD + c]) + sDGC[c];
+            const int r1 = min(r0 + 32, len);
+            for (int r = r0; r < r1; ++r) {
+                const int o = toff<KD>(r, c);
+                p.dg[((size_t)(cd.tok + r) * p.H_v + h) * KD + c] = sDW[o] + sQt[o] + add;
+            }
+        }
+        if (tid < len) {
+            float db = sDB[tid] + sDBa[tid] + sDBa[64 + tid];
+#pragma unroll
+            for (int w = 0; w < BC_WARPS; ++w) db += sDBw[w * 64 + tid];
+            p.dbeta[(size_t)(cd.tok + tid) * p.H_v + h] = db;
         }
     }
 }
 
 // =====================================================================
-// The prologue's Jacobians, one warp per (query/key head, 64 tokens); lane = channels
+// The prologue's Jacobians, one warp per (query/key head, 16 tokens); lane = channels
 // 4 lane .. 4 lane + 3:
 //   dq = scale r_q (dqt_sum - r_q^2 q (q . dqt_sum)),  r_q = 1 / sqrt(|q|^2 + eps)   (dk alike, scale 1)
-//   dgraw = dg (-a) sigmoid(graw),  dA_log += sum_c dg g,  db = dbeta beta (1 - beta)
-// with dqt_sum / dkh_sum the sums over the value heads of the group.  dA_log is accumulated
-// per warp and added once per head (per token and head when a group has more than 16 value
-// heads).
+//   dgraw = dg (-a) sigmoid(graw),  db = dbeta beta (1 - beta)
+// with dqt_sum / dkh_sum the sums over the value heads of the group; the warp's share of
+// dA_log = sum dg g per value head goes to dal[range][h], which bwdc_dalog_kernel adds up in a
+// fixed order (no atomics: the gradients are reproducible bit for bit).
 // =====================================================================
 constexpr int BP_WARPS = 8;
-constexpr int BP_TOKENS = 64;   // tokens per warp
+constexpr int BP_TOKENS = 16;   // tokens per warp
 
 __global__ __launch_bounds__(BP_WARPS * 32) void bwdc_jacobian_kernel(const BwdcParams p, float *dq, float *dk,
-                                                                      float *dgraw, float *db, float *dA_log,
+                                                                      float *dgraw, float *db, float *dal,
                                                                       long long tokens) {
     const int lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * BP_WARPS + (threadIdx.x >> 5);
     const long long n_ranges = (tokens + BP_TOKENS - 1) / BP_TOKENS;
     if (gw >= n_ranges * p.H_qk) return;
     const int hq = (int)(gw % p.H_qk);
-    const long long t0 = (gw / p.H_qk) * BP_TOKENS, t1 = min(t0 + BP_TOKENS, tokens);
+    const long long range = gw / p.H_qk, t0 = range * BP_TOKENS, t1 = min(t0 + BP_TOKENS, tokens);
     const int group = p.H_v / p.H_qk;
-    constexpr int MAXG = 16;
-    float dal[MAXG];
-#pragma unroll
-    for (int g = 0; g < MAXG; ++g) dal[g] = 0.f;
     for (long long tok = t0; tok < t1; ++tok) {
         const size_t qo = ((size_t)tok * p.H_qk + hq) * KD + 4 * lane;
         const uint2 qw = *reinterpret_cast<const uint2 *>(p.q + qo), kw = *reinterpret_cast<const uint2 *>(p.k + qo);
@@ -1091,16 +1126,19 @@ __global__ __launch_bounds__(BP_WARPS * 32) void bwdc_jacobian_kernel(const Bwdc
         ok.z = rk * (sk[2] - rk * rk * kv[2] * kd); ok.w = rk * (sk[3] - rk * rk * kv[3] * kd);
         *reinterpret_cast<float4 *>(dq + qo) = oq;
         *reinterpret_cast<float4 *>(dk + qo) = ok;
+    }
 #pragma unroll 1
-        for (int g = 0; g < group; ++g) {
-            const int h = hq * group + g;
+    for (int g = 0; g < group; ++g) {
+        const int h = hq * group + g;
+        const float a = ex2n(p.A_log[h]);
+        float acc = 0.f;
+        for (long long tok = t0; tok < t1; ++tok) {
             const size_t vo = ((size_t)tok * p.H_v + h) * KD + 4 * lane;
-            const float a = ex2n(p.A_log[h]);
             const uint2 gw2 = *reinterpret_cast<const uint2 *>(p.graw + vo);
             const float gr[4] = {bf16_lo(gw2.x), bf16_hi(gw2.x), bf16_lo(gw2.y), bf16_hi(gw2.y)};
             const float4 dg4 = *reinterpret_cast<const float4 *>(p.dg + vo);
             const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
-            float out[4], acc = 0.f;
+            float out[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float sp = softplus_log2(gr[i]) * (1.0f / LOG2E);   // softplus (natural units)
@@ -1109,26 +1147,31 @@ __global__ __launch_bounds__(BP_WARPS * 32) void bwdc_jacobian_kernel(const Bwdc
                 acc = fmaf(dgv[i], -a * sp, acc);
             }
             *reinterpret_cast<float4 *>(dgraw + vo) = make_float4(out[0], out[1], out[2], out[3]);
-            acc = warp_sum(acc);
-            if (group <= MAXG) {
-#pragma unroll
-                for (int gg2 = 0; gg2 < MAXG; ++gg2)
-                    if (gg2 == g) dal[gg2] += acc;
-            } else if (lane == 0) {
-                atomicAdd(&dA_log[h], acc);
-            }
             if (lane == 0) {
                 const float bb = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
                 const float beta = 1.0f / (1.0f + __expf(-bb));
                 db[(size_t)tok * p.H_v + h] = p.dbeta[(size_t)tok * p.H_v + h] * beta * (1.0f - beta);
             }
         }
+        acc = warp_sum(acc);
+        if (lane == 0) dal[range * p.H_v + h] = acc;
     }
-    if (lane == 0 && group <= MAXG) {
-#pragma unroll
-        for (int g = 0; g < MAXG; ++g)
-            if (g < group) atomicAdd(&dA_log[hq * group + g], dal[g]);
+}
+
+// dA_log[h] = sum over the token ranges of dal[range][h], one CTA per head, in a fixed order.
+__global__ __launch_bounds__(256) void bwdc_dalog_kernel(const float *dal, long long n_ranges, int H_v,
+                                                          float *dA_log) {
+    __shared__ float red[256];
+    const int h = blockIdx.x, tid = threadIdx.x;
+    float acc = 0.f;
+    for (long long r = tid; r < n_ranges; r += 256) acc += dal[r * H_v + h];
+    red[tid] = acc;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (tid < o) red[tid] += red[tid + o];
+        __syncthreads();
     }
+    if (tid == 0) dA_log[h] = red[0];
 }
 
 // ---------------------------------------------------------------- host side
@@ -1152,9 +1195,10 @@ size_t bwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, int /*grid
     off = a256(off + items * BR_BYTES);
     off = a256(off + items * ST_BYTES);
     off = a256(off + items * ST_BYTES);
-    off = a256(off + items * 2 * CP_BYTES);
+    off = a256(off + items * CP_BYTES);
     off = a256(off + tk * KD * 4 * 3);   // dqt, dkh, dg
     off = a256(off + tk * 4);            // dbeta
+    off = a256(off + (size_t)((tokens > 0 ? tokens : 1) + BP_TOKENS - 1) / BP_TOKENS * H_v * 4);   // dA_log parts
     return off;
 }
 
@@ -1184,12 +1228,14 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     bp.rec = reinterpret_cast<unsigned char *>(take(items * BR_BYTES));
     bp.S0 = reinterpret_cast<float *>(take(items * ST_BYTES));
     bp.dSC = reinterpret_cast<float *>(take(items * ST_BYTES));
-    bp.part = reinterpret_cast<unsigned char *>(take(items * 2 * CP_BYTES));
+    bp.part = reinterpret_cast<unsigned char *>(take(items * CP_BYTES));
     float *t3 = reinterpret_cast<float *>(take(tk * KD * 4 * 3));
     bp.dqt = t3;
     bp.dkh = t3 + tk * KD;
     bp.dg = t3 + 2 * tk * KD;
     bp.dbeta = reinterpret_cast<float *>(take(tk * 4));
+    const long long n_ranges = (tokens + BP_TOKENS - 1) / BP_TOKENS;
+    float *dal = reinterpret_cast<float *>(take((size_t)((tokens > 0 ? tokens : 1) + BP_TOKENS - 1) / BP_TOKENS * H_v * 4));
     bp.q = q; bp.k = k; bp.v = v; bp.graw = graw; bp.b = b; bp.dout = dout;
     bp.A_log = A_log; bp.init = init; bp.dht = dht; bp.scale = scale;
     bp.H_qk = H_qk; bp.H_v = H_v; bp.nseq = nseq;
@@ -1230,10 +1276,9 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     if (nck > 0) {
         const long long n_items = nck * H_v;
         const int g_items = (int)(n_items < nsm ? n_items : nsm);
-        const int g_units = (int)(2 * n_items < nsm ? 2 * n_items : nsm);
         if ((e = smem_attr(bwdc_gradv_kernel, GV_BYTES)) != cudaSuccess) return e;
         if ((e = smem_attr(bwdc_gradk_kernel, GK_BYTES)) != cudaSuccess) return e;
-        bwdc_gradv_kernel<<<g_units, BC_THREADS, GV_BYTES + 128, stream>>>(bp);
+        bwdc_gradv_kernel<<<g_items, BC_THREADS, GV_BYTES + 128, stream>>>(bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_gradv_kernel", stream);
@@ -1245,7 +1290,10 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     if (tokens > 0) {
         const long long warps = ((tokens + BP_TOKENS - 1) / BP_TOKENS) * H_qk;
         bwdc_jacobian_kernel<<<(unsigned)((warps + BP_WARPS - 1) / BP_WARPS), BP_WARPS * 32, 0, stream>>>(
-            bp, dq, dk, dgraw, db, dA_log, tokens);
+            bp, dq, dk, dgraw, db, dal, tokens);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        bwdc_dalog_kernel<<<H_v, 256, 0, stream>>>(dal, n_ranges, H_v, dA_log);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_jacobian_kernel", stream);

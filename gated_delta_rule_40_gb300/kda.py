@@ -70,8 +70,13 @@ def load() -> ctypes.CDLL:
     lib.kda_decode_tokens.restype = I
     lib.kda_fwd_bf16_state.argtypes = [P, P, P, P, P, P, F, P, P, P, I, I, I, I, I, I, I, P, P]
     lib.kda_fwd_bf16_state.restype = I
-    lib.kda_bwd.argtypes = [P, P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P]
+    bwd_args = [P, P, P, P, P, P, F, P, P, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P]
+    lib.kda_bwd.argtypes = bwd_args + [P]
     lib.kda_bwd.restype = I
+    lib.kda_bwd_ws.argtypes = bwd_args + [P, Z, P]
+    lib.kda_bwd_ws.restype = I
+    lib.kda_bwd_workspace_size.argtypes = [I] * 7
+    lib.kda_bwd_workspace_size.restype = Z
     lib.kda_la_fwd.argtypes = [P, P, P, P, F, P, P, P, I, I, I, I, I, I, I, P, P]
     lib.kda_la_fwd.restype = I
     lib.kda_la_decode.argtypes = [P, P, P, P, F, P, I, I, I, I, I, P, P]
@@ -421,12 +426,19 @@ def kda_la_decode(q, k, v, slope, scale: float, state, out=None, stream=None) ->
     return out
 
 
+def kda_bwd_workspace_size(N: int, B: int, T: int, H_qk: int, H_v: int, K: int = 128, V: int = 128) -> int:
+    return int(load().kda_bwd_workspace_size(N, B, T, H_qk, H_v, K, V))
+
+
 def kda_bwd(q, k, v, graw, b, A_log, scale: float, dout, initial_state=None, cu_seqlens=None, dht=None,
-            stream=None) -> dict:
+            stream=None, workspace=None) -> dict:
     """Backward of ``kda_fwd``: returns fp32 gradients ``dq, dk`` [B,T,H_qk,K],
     ``dv`` [B,T,H_v,V], ``dgraw`` [B,T,H_v,K], ``db`` [B,T,H_v], ``dA_log``
     [H_v] and ``dh0`` [N,H_v,V,K] of a loss given ``dout`` (bf16, shape of
-    out) and optionally ``dht`` (fp32, shape of the final state)."""
+    out) and optionally ``dht`` (fp32, shape of the final state).  The
+    workspace (``kda_bwd_workspace_size`` bytes, uint8 on the device) is
+    ``workspace`` if given, else taken from torch's caching allocator, so that
+    repeated calls reuse the same memory (kda_bwd_ws)."""
     lib = load()
     B, T, H_qk, K = q.shape
     H_v, V = v.shape[2], v.shape[3]
@@ -450,11 +462,16 @@ def kda_bwd(q, k, v, graw, b, A_log, scale: float, dout, initial_state=None, cu_
          "db": torch.empty((B, T, H_v), dtype=f32, device=dev),
          "dA_log": torch.empty((H_v,), dtype=f32, device=dev),
          "dh0": torch.empty((N, H_v, V, K), dtype=f32, device=dev)}
-    rc = lib.kda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
-                     _ptr(initial_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V, _ptr(dout), _ptr(dht),
-                     _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dgraw"]), _ptr(g["db"]), _ptr(g["dA_log"]),
-                     _ptr(g["dh0"]), _stream(stream))
-    _raise(rc, "kda_bwd")
+    if workspace is None:
+        nbytes = int(lib.kda_bwd_workspace_size(N, B, T, H_qk, H_v, K, V))
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    _check(workspace, "workspace", torch.uint8)
+    rc = lib.kda_bwd_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(graw), _ptr(b), _ptr(A_log), ctypes.c_float(scale),
+                        _ptr(initial_state), _ptr(cu_seqlens), N, B, T, H_qk, H_v, K, V, _ptr(dout), _ptr(dht),
+                        _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dgraw"]), _ptr(g["db"]),
+                        _ptr(g["dA_log"]), _ptr(g["dh0"]), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                        _stream(stream))
+    _raise(rc, "kda_bwd_ws")
     return g
 
 

@@ -12,8 +12,9 @@
 Inputs come from ``kda_inputs`` (same recipe as the tests and the benchmark);
 the workspace is allocated once, so every iteration is exactly the three
 kernel launches of ``kda_fwd`` (three for ``kda_fwd_scalar_gate``: plan, intra_gdn_kernel
-and scan_kernel; two for ``kda_la_fwd``: plan and la_fwd_kernel; three for ``kda_bwd``:
-plan, bwd_recur_kernel and bwd_prologue_kernel; one for ``kda_decode_tokens``, whose
+and scan_kernel; two for ``kda_la_fwd``: plan and la_fwd_kernel; eight for ``kda_bwd``:
+plan, bwdc_prep_kernel, bwdc_chain_kernel forward and backward, bwdc_gradv_kernel,
+bwdc_gradk_kernel, bwdc_jacobian_kernel and bwdc_dalog_kernel; one for ``kda_decode_tokens``, whose
 ``--T`` is the token count Tq of the step and whose state is fp32 unless
 ``--bf16-state``; one for ``kda_decode_step``).  A profiler then selects launches by kernel name and index (e.g.
 ``ncu -k regex:intra_kernel -s 2 -c 1``).  ``--kernel-times`` (kda and bwd) times the

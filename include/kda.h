@@ -244,14 +244,16 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
  *   dA_log   [H_v] fp32               dh0 [N, H_v, V, K] fp32 (dL/dinitial_state)
  *
  * All outputs are written (dA_log is zeroed, then accumulated).  Gradient
- * buffers must be 16-byte aligned (db excepted).  Asynchronous on `stream`; the
- * workspace comes from cudaMallocAsync on `stream`: state checkpoints every 16
- * tokens (4 KiB per token and value head), per-token partial sums of four
- * row quarters (6 KiB per token and value head) and 256 KiB of scratch per
- * resident CTA, i.e. about 10 KiB per token and value head (10.8 GB for B=2,
- * T=16384, H_v=32); a failed allocation returns KDA_ERR_CUDA.  This is the
- * token recurrence run backwards on CUDA cores in fp32 (persistent CTAs, four
- * per (sequence, value head) chain, one per quarter of the state rows); errors
+ * buffers must be 16-byte aligned (db excepted).  Asynchronous on `stream`.  The
+ * gradients are computed in the chunk (UT / WY) form of the forward, 64 tokens per
+ * chunk, on tensor cores (mma.sync, tf32 operands rounded to nearest, fp32
+ * accumulation, fp32 states): per (chunk, value head) the chunk's operands, then
+ * the state entering each chunk (a forward chain) and the state gradient leaving
+ * it (a reverse chain), then the chunks' gradients in parallel.  The workspace
+ * holds, per (chunk, value head), those operands, both states and the value-side
+ * gradient sums (about 434 KiB), plus 1.5 KiB per token and value head (8.9 GB
+ * for B=2, T=16384, H_v=32); kda_bwd takes it from cudaMallocAsync on `stream`
+ * (a failed allocation returns KDA_ERR_CUDA), kda_bwd_ws from the caller.  Errors
  * as kda_fwd.
  */
 int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
@@ -259,6 +261,20 @@ int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const
             const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V,
             const kda_bf16_t *dout, const float *dht, float *dq, float *dk, float *dv, float *dgraw,
             float *db, float *dA_log, float *dh0, cudaStream_t stream);
+
+/* Bytes of device workspace kda_bwd_ws needs for these sizes (0 on invalid
+ * sizes).  The bound covers any cu_seqlens with N sequences and T tokens. */
+size_t kda_bwd_workspace_size(int N, int B, int T, int H_qk, int H_v, int K, int V);
+
+/* kda_bwd with a caller-owned workspace: `ws` is a device pointer, 256-byte
+ * aligned, of at least kda_bwd_workspace_size(...) bytes (KDA_ERR_WORKSPACE
+ * otherwise).  The workspace must not be used by anything else until the work
+ * queued on `stream` completes. */
+int kda_bwd_ws(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
+               const kda_bf16_t *b, const float *A_log, float scale, const float *initial_state,
+               const int32_t *cu_seqlens, int N, int B, int T, int H_qk, int H_v, int K, int V,
+               const kda_bf16_t *dout, const float *dht, float *dq, float *dk, float *dv, float *dgraw,
+               float *db, float *dA_log, float *dh0, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Lightning attention: linear attention with a fixed per-head decay.  The cuLA

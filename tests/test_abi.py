@@ -30,7 +30,7 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = kda.declared_symbols()
     assert {"kda_fwd", "kda_fwd_ws", "kda_fwd_workspace_size", "kda_decode_step", "kda_status_string",
-            "kda_get_status", "kda_last_launch_count"} <= set(names)
+            "kda_get_status", "kda_last_launch_count", "kda_bwd", "kda_bwd_ws", "kda_bwd_workspace_size"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 
@@ -84,6 +84,21 @@ def test_fwd_rejects_misaligned_pointers(lib):
 def test_fwd_ws_rejects_small_workspace(lib):
     rc = lib.kda_fwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_float(0.1), None, None, None, 0, 1, 64,
                         1, 1, 128, 128, FAKE, FAKE, ctypes.c_size_t(16), None)
+    assert rc == kda.KDA_ERR_WORKSPACE
+
+
+def test_bwd_workspace_size(lib):
+    # per (chunk, value head) about 434 KiB, plus 1.5 KiB per token and value head
+    dense = kda.kda_bwd_workspace_size(0, 2, 16384, 32, 32)
+    assert 8.5e9 < dense < 9.5e9
+    assert kda.kda_bwd_workspace_size(20, 1, 16384, 32, 32) >= kda.kda_bwd_workspace_size(0, 1, 16384, 32, 32)
+    assert kda.kda_bwd_workspace_size(0, 1, 64, 1, 1, K=64) == 0
+
+
+def test_bwd_ws_rejects_small_workspace(lib):
+    f = ctypes.c_float(0.1)
+    rc = lib.kda_bwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, f, None, None, 0, 1, 64, 1, 1, 128, 128, FAKE, None,
+                        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_size_t(16), None)
     assert rc == kda.KDA_ERR_WORKSPACE
 
 

@@ -55,13 +55,17 @@ def _grads(inp, seed, with_dht=True):
     return do, dht
 
 
-def _run(inp, do, dht):
+def _run_raw(inp, do, dht):
     from gated_delta_rule_40_gb300 import kda
     dev = lambda t: None if t is None else t.cuda()  # noqa: E731
     got = kda.kda_bwd(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.graw), dev(inp.b), dev(inp.A_log), inp.scale,
                       dev(do), initial_state=dev(inp.initial_state), cu_seqlens=dev(inp.cu_seqlens), dht=dev(dht))
     torch.cuda.synchronize()
-    return {k_: v_.double().cpu().numpy() for k_, v_ in got.items()}
+    return got
+
+
+def _run(inp, do, dht):
+    return {k_: v_.double().cpu().numpy() for k_, v_ in _run_raw(inp, do, dht).items()}
 
 
 def _check(inp, seed, with_dht=True):
@@ -142,3 +146,27 @@ def test_bwd_large_value_head_group():
     """20 value heads share one q/k head (more than the 16 the Jacobian kernel keeps dA_log
     partials for in registers): dq and dk sum over all 20, dA_log per head."""
     _check(KI.make_inputs(1, 40, 1, 20, seed=706, with_state=True), seed=8)
+
+
+def test_bwd_allocating_entry_equals_workspace_entry():
+    """kda_bwd (workspace from cudaMallocAsync) and kda_bwd_ws (the binding's default, a
+    torch buffer) run the same kernels: bit-identical gradients."""
+    import ctypes
+    from gated_delta_rule_40_gb300 import kda
+    inp = KI.make_inputs(1, 150, 1, 2, seed=709, with_state=True, seqlens=[90, 60])
+    do, dht = _grads(inp, 9)
+    got = {k_: v_ for k_, v_ in _run_raw(inp, do, dht).items()}
+    lib = kda.load()
+    d = {n: (None if t is None else t.cuda()) for n, t in (("q", inp.q), ("k", inp.k), ("v", inp.v), ("g", inp.graw),
+                                                          ("b", inp.b), ("a", inp.A_log), ("s", inp.initial_state),
+                                                          ("cu", inp.cu_seqlens), ("do", do), ("dht", dht))}
+    out = {n: torch.empty_like(t) for n, t in got.items()}
+    p = lambda t: ctypes.c_void_p(0 if t is None else t.data_ptr())  # noqa: E731
+    rc = lib.kda_bwd(p(d["q"]), p(d["k"]), p(d["v"]), p(d["g"]), p(d["b"]), p(d["a"]), ctypes.c_float(inp.scale),
+                     p(d["s"]), p(d["cu"]), 2, 1, 150, 1, 2, 128, 128, p(d["do"]), p(d["dht"]), p(out["dq"]),
+                     p(out["dk"]), p(out["dv"]), p(out["dgraw"]), p(out["db"]), p(out["dA_log"]), p(out["dh0"]),
+                     ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == kda.KDA_OK
+    torch.cuda.synchronize()
+    for name in got:
+        assert torch.equal(out[name], got[name]), name
