@@ -157,25 +157,43 @@ constexpr int BC_THREADS = 256, BC_WARPS = 8;
 
 // The chunk's rows into shared memory: Kh = k / |k| and Qt = scale q / |q| (fp32 tiles),
 // Gam (fp32 tile; rows past len repeat the last valid row, their g being 0), beta = sigmoid(b)
-// (0 past len) and D = e^Gam_C.  All threads take part; returns synchronised.
+// (0 past len) and D = e^Gam_C.  All NT threads take part (sTot: NT floats of scratch);
+// returns synchronised.
+template <int NT>
 __device__ void bwdc_rows(const BwdcParams &p, int tok0, int len, int h, int hq, float a, float *sKh, float *sQt,
-                          float *sG, float *sBeta, float *sD, int tid) {
+                          float *sG, float *sBeta, float *sD, float *sTot, int tid) {
+    constexpr int NW = NT / 32, RPW = CH / NW;   // rows per warp
     const int warp = tid >> 5, lane = tid & 31;
-    for (int r = warp; r < CH; r += BC_WARPS) {
-        float4 kh = make_float4(0.f, 0.f, 0.f, 0.f), qt = kh, gg = kh;
-        float beta = 0.f;
+    // the warp's rows: all loads first, then the arithmetic
+    uint2 qw[RPW], kw[RPW], gw[RPW];
+    float bv[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int r = warp + NW * i;
+        qw[i] = kw[i] = gw[i] = make_uint2(0u, 0u);
+        bv[i] = 0.f;
         if (r < len) {
             const size_t tok = (size_t)tok0 + r;
             const size_t qo = (tok * p.H_qk + hq) * KD + 4 * lane, vo = (tok * p.H_v + h) * KD + 4 * lane;
-            const uint2 qw = *reinterpret_cast<const uint2 *>(p.q + qo), kw = *reinterpret_cast<const uint2 *>(p.k + qo);
-            const uint2 gw = *reinterpret_cast<const uint2 *>(p.graw + vo);
-            const float qv[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
-            const float kv[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
+            qw[i] = *reinterpret_cast<const uint2 *>(p.q + qo);
+            kw[i] = *reinterpret_cast<const uint2 *>(p.k + qo);
+            gw[i] = *reinterpret_cast<const uint2 *>(p.graw + vo);
+            bv[i] = bf16_to_f(p.b[tok * p.H_v + h]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int r = warp + NW * i;
+        float4 kh = make_float4(0.f, 0.f, 0.f, 0.f), qt = kh, gg = kh;
+        float beta = 0.f;
+        if (r < len) {
+            const float qv[4] = {bf16_lo(qw[i].x), bf16_hi(qw[i].x), bf16_lo(qw[i].y), bf16_hi(qw[i].y)};
+            const float kv[4] = {bf16_lo(kw[i].x), bf16_hi(kw[i].x), bf16_lo(kw[i].y), bf16_hi(kw[i].y)};
             float sq = 0.f, sk = 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                sq = fmaf(qv[i], qv[i], sq);
-                sk = fmaf(kv[i], kv[i], sk);
+            for (int e = 0; e < 4; ++e) {
+                sq = fmaf(qv[e], qv[e], sq);
+                sk = fmaf(kv[e], kv[e], sk);
             }
             sq = warp_sum(sq);
             sk = warp_sum(sk);
@@ -184,9 +202,9 @@ __device__ void bwdc_rows(const BwdcParams &p, int tok0, int len, int h, int hq,
             kh = make_float4(kv[0] * rk, kv[1] * rk, kv[2] * rk, kv[3] * rk);
             // g = -a softplus(graw), natural units
             const float na = -a * (1.0f / LOG2E);
-            gg = make_float4(na * softplus_log2(bf16_lo(gw.x)), na * softplus_log2(bf16_hi(gw.x)),
-                             na * softplus_log2(bf16_lo(gw.y)), na * softplus_log2(bf16_hi(gw.y)));
-            beta = 1.0f / (1.0f + ex2(-bf16_to_f(p.b[tok * p.H_v + h]) * LOG2E));
+            gg = make_float4(na * softplus_log2(bf16_lo(gw[i].x)), na * softplus_log2(bf16_hi(gw[i].x)),
+                             na * softplus_log2(bf16_lo(gw[i].y)), na * softplus_log2(bf16_hi(gw[i].y)));
+            beta = 1.0f / (1.0f + ex2(-bv[i] * LOG2E));
         }
         const int o = toff<KD>(r, 4 * lane);
         *reinterpret_cast<float4 *>(sKh + o) = kh;
@@ -195,29 +213,30 @@ __device__ void bwdc_rows(const BwdcParams &p, int tok0, int len, int h, int hq,
         if (lane == 0) sBeta[r] = beta;
     }
     __syncthreads();
-    // prefix sums down each channel: rows 0..31 and 32..63 by two threads, then the second
-    // half adds the first half's total
-    static_assert(BC_THREADS == 2 * KD, "two threads per channel");
+    // prefix sums down each channel: NT / 128 threads per channel, each over a segment of rows,
+    // then every segment adds the totals of the segments above it
+    constexpr int SEG = NT / KD, SR = CH / SEG;
+    const int c = tid & (KD - 1), seg = tid / KD;
     {
-        const int c = tid & (KD - 1), r0 = 32 * (tid >> 7);
-        float s = 0.f;
-        for (int r = r0; r < r0 + 32; ++r) {
+        float sacc = 0.f;
+        for (int r = SR * seg; r < SR * (seg + 1); ++r) {
             const int o = toff<KD>(r, c);
-            s += sG[o];
-            sG[o] = s;
+            sacc += sG[o];
+            sG[o] = sacc;
         }
+        sTot[seg * KD + c] = sacc;
     }
     __syncthreads();
-    if (tid >= KD) {
-        const int c = tid - KD;
-        const float base = sG[toff<KD>(31, c)];
+    if (seg > 0) {
+        float base = 0.f;
+        for (int s2 = 0; s2 < seg; ++s2) base += sTot[s2 * KD + c];
         float last = 0.f;
-        for (int r = 32; r < CH; ++r) {
+        for (int r = SR * seg; r < SR * (seg + 1); ++r) {
             const int o = toff<KD>(r, c);
             last = sG[o] + base;
             sG[o] = last;
         }
-        sD[c] = ex2n(last);
+        if (seg == SEG - 1) sD[c] = ex2n(last);
     }
     __syncthreads();
 }
@@ -251,15 +270,16 @@ __device__ __forceinline__ void pair_of(int pr, int &i, int &b) {
 
 // =====================================================================
 // Prep: per item the chunk's rows, KK (A before beta) and P by sub-block pairs, T, W, U, Kd,
-// N; written to the item's record.  One item per CTA at a time.
+// N; written to the item's record.  One item per CTA (16 warps) at a time.
 // =====================================================================
+constexpr int PN_THREADS = 512, PN_WARPS = 16;
 constexpr uint32_t PS_KH = 0, PS_QT = 32768, PS_G = 65536, PS_W = 98304, PS_KK = 131072, PS_P = 147456,
                    PS_A = 163840, PS_T = 181248, PS_X = 198656, PS_MISC = 203264, PS_BYTES = 204288;
 constexpr uint32_t PS_V = PS_QT;   // V (fp32 tile) once Qt is no longer read
-static_assert(PS_T == PS_A + CH * AS * 4 && PS_X == PS_T + CH * AS * 4 && PS_MISC >= PS_X + 32 * XS * 4,
-              "prep layout");
+static_assert(PS_T == PS_A + CH * AS * 4 && PS_X == PS_T + CH * AS * 4 && PS_MISC >= PS_X + 32 * XS * 4 &&
+              PS_MISC >= PS_X + PN_THREADS * 4, "prep layout");
 
-__global__ __launch_bounds__(BC_THREADS, 1) void bwdc_prep_kernel(const BwdcParams p) {
+__global__ __launch_bounds__(PN_THREADS, 1) void bwdc_prep_kernel(const BwdcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<128>(smem_raw);
     if (p.hdr[1] == 0) return;
@@ -279,59 +299,49 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
         const float a = ex2n(p.A_log[h]);
         float *rec = reinterpret_cast<float *>(p.rec + (size_t)item * BR_BYTES);
         __syncthreads();   // the previous item's reads of shared memory are done
-        bwdc_rows(p, cd.tok, len, h, hq, a, sKh, sQt, sG, sBeta, sD, tid);
+        bwdc_rows<PN_THREADS>(p, cd.tok, len, h, hq, a, sKh, sQt, sG, sBeta, sD, sX, tid);
 
-        // ---- KK and P per sub-block pair (one warp per pair): 16 x 16, K = 128 channels
-        for (int pr = warp; pr < 10; pr += BC_WARPS) {
+        // ---- KK and P per sub-block pair and 8-column half (20 units, one warp each):
+        //      16 x 8, K = 128 channels
+        for (int u = warp; u < 20; u += PN_WARPS) {
             int i, b;
-            pair_of(pr, i, b);
-            float kk[2][4], pp[2][4];
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) kk[j][e] = pp[j][e] = 0.f;
+            pair_of(u >> 1, i, b);
+            const int jn = u & 1;
+            float kk[4] = {0.f, 0.f, 0.f, 0.f}, pp[4] = {0.f, 0.f, 0.f, 0.f};
+            const int r0 = 16 * i + g, j = 16 * b + 8 * jn + g;
+#pragma unroll 4
             for (int k0 = 0; k0 < KD; k0 += 8) {
                 const PairRef f0 = pair_ref(sG, i, b, k0 + t), f1 = pair_ref(sG, i, b, k0 + t + 4);
-                const int r0 = 16 * i + g;
-                uint32_t ak[4], aq[4], bb[2][2];
-                {
-                    const float e00 = f0.rowf(sG[toff<KD>(r0, k0 + t)]), e10 = f0.rowf(sG[toff<KD>(r0 + 8, k0 + t)]);
-                    const float e01 = f1.rowf(sG[toff<KD>(r0, k0 + t + 4)]);
-                    const float e11 = f1.rowf(sG[toff<KD>(r0 + 8, k0 + t + 4)]);
-                    ak[0] = tf32_rn_bits(sKh[toff<KD>(r0, k0 + t)] * e00);
-                    ak[1] = tf32_rn_bits(sKh[toff<KD>(r0 + 8, k0 + t)] * e10);
-                    ak[2] = tf32_rn_bits(sKh[toff<KD>(r0, k0 + t + 4)] * e01);
-                    ak[3] = tf32_rn_bits(sKh[toff<KD>(r0 + 8, k0 + t + 4)] * e11);
-                    aq[0] = tf32_rn_bits(sQt[toff<KD>(r0, k0 + t)] * e00);
-                    aq[1] = tf32_rn_bits(sQt[toff<KD>(r0 + 8, k0 + t)] * e10);
-                    aq[2] = tf32_rn_bits(sQt[toff<KD>(r0, k0 + t + 4)] * e01);
-                    aq[3] = tf32_rn_bits(sQt[toff<KD>(r0 + 8, k0 + t + 4)] * e11);
-                }
-#pragma unroll
-                for (int jn = 0; jn < 2; ++jn) {
-                    const int j = 16 * b + 8 * jn + g;
-                    bb[jn][0] = tf32_rn_bits(sKh[toff<KD>(j, k0 + t)] * f0.colf(sG[toff<KD>(j, k0 + t)]));
-                    bb[jn][1] = tf32_rn_bits(sKh[toff<KD>(j, k0 + t + 4)] * f1.colf(sG[toff<KD>(j, k0 + t + 4)]));
-                    mma_tf32(kk[jn], ak, bb[jn]);
-                    mma_tf32(pp[jn], aq, bb[jn]);
-                }
+                const float e00 = f0.rowf(sG[toff<KD>(r0, k0 + t)]), e10 = f0.rowf(sG[toff<KD>(r0 + 8, k0 + t)]);
+                const float e01 = f1.rowf(sG[toff<KD>(r0, k0 + t + 4)]), e11 = f1.rowf(sG[toff<KD>(r0 + 8, k0 + t + 4)]);
+                uint32_t ak[4], aq[4], bb[2];
+                ak[0] = tf32_rn_bits(sKh[toff<KD>(r0, k0 + t)] * e00);
+                ak[1] = tf32_rn_bits(sKh[toff<KD>(r0 + 8, k0 + t)] * e10);
+                ak[2] = tf32_rn_bits(sKh[toff<KD>(r0, k0 + t + 4)] * e01);
+                ak[3] = tf32_rn_bits(sKh[toff<KD>(r0 + 8, k0 + t + 4)] * e11);
+                aq[0] = tf32_rn_bits(sQt[toff<KD>(r0, k0 + t)] * e00);
+                aq[1] = tf32_rn_bits(sQt[toff<KD>(r0 + 8, k0 + t)] * e10);
+                aq[2] = tf32_rn_bits(sQt[toff<KD>(r0, k0 + t + 4)] * e01);
+                aq[3] = tf32_rn_bits(sQt[toff<KD>(r0 + 8, k0 + t + 4)] * e11);
+                bb[0] = tf32_rn_bits(sKh[toff<KD>(j, k0 + t)] * f0.colf(sG[toff<KD>(j, k0 + t)]));
+                bb[1] = tf32_rn_bits(sKh[toff<KD>(j, k0 + t + 4)] * f1.colf(sG[toff<KD>(j, k0 + t + 4)]));
+                mma_tf32(kk, ak, bb);
+                mma_tf32(pp, aq, bb);
             }
             // masks by selection (above the diagonal the clamped factors may overflow)
 #pragma unroll
-            for (int jn = 0; jn < 2; ++jn)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * i + g + 8 * hh, c = 16 * b + 8 * jn + 2 * t;
-                    const float k0v = (i > b || c < r) ? kk[jn][2 * hh] : 0.f;
-                    const float k1v = (i > b || c + 1 < r) ? kk[jn][2 * hh + 1] : 0.f;
-                    const float p0v = (i > b || c <= r) ? pp[jn][2 * hh] : 0.f;
-                    const float p1v = (i > b || c + 1 <= r) ? pp[jn][2 * hh + 1] : 0.f;
-                    st2(sKK + toff<CH>(r, c), k0v, k1v);
-                    st2(sP + toff<CH>(r, c), p0v, p1v);
-                }
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = 16 * i + g + 8 * hh, c = 16 * b + 8 * jn + 2 * t;
+                const float k0v = (i > b || c < r) ? kk[2 * hh] : 0.f;
+                const float k1v = (i > b || c + 1 < r) ? kk[2 * hh + 1] : 0.f;
+                const float p0v = (i > b || c <= r) ? pp[2 * hh] : 0.f;
+                const float p1v = (i > b || c + 1 <= r) ? pp[2 * hh + 1] : 0.f;
+                st2(sKK + toff<CH>(r, c), k0v, k1v);
+                st2(sP + toff<CH>(r, c), p0v, p1v);
+            }
         }
         // the six blocks above the diagonal are zero
-        for (int idx = tid; idx < 6 * 256; idx += BC_THREADS) {
+        for (int idx = tid; idx < 6 * 256; idx += PN_THREADS) {
             const int blk = idx >> 8, e = idx & 255;
             const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
             const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
@@ -341,44 +351,43 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
         }
         __syncthreads();
         // A = beta KK for the inversion; KK and P to the record
-        for (int idx = tid; idx < CH * CH; idx += BC_THREADS) {
-            const int r = idx >> 6, j = idx & 63;
-            sA[r * AS + j] = sBeta[r] * sKK[toff<CH>(r, j)];
+        for (int idx = tid; idx < CH * CH; idx += PN_THREADS) {
+            const int r = idx >> 6, jj = idx & 63;
+            sA[r * AS + jj] = sBeta[r] * sKK[toff<CH>(r, jj)];
         }
-        for (int idx = tid; idx < CH * CH / 4; idx += BC_THREADS) {
+        for (int idx = tid; idx < CH * CH / 4; idx += PN_THREADS) {
             reinterpret_cast<float4 *>(rec + BR_KK / 4)[idx] = reinterpret_cast<const float4 *>(sKK)[idx];
             reinterpret_cast<float4 *>(rec + BR_P / 4)[idx] = reinterpret_cast<const float4 *>(sP)[idx];
         }
         __syncthreads();
-        invert_unit_lower64<BC_THREADS>(sA, sT, sX, tid, warp, lane);
-        for (int idx = tid; idx < CH * CH; idx += BC_THREADS) {
-            const int r = idx >> 6, j = idx & 63;
-            rec[BR_T / 4 + toff<CH>(r, j)] = sT[r * AS + j];
+        invert_unit_lower64<PN_THREADS>(sA, sT, sX, tid, warp, lane);
+        for (int idx = tid; idx < CH * CH; idx += PN_THREADS) {
+            const int r = idx >> 6, jj = idx & 63;
+            rec[BR_T / 4 + toff<CH>(r, jj)] = sT[r * AS + jj];
         }
         if (tid < KD) rec[BR_D / 4 + tid] = sD[tid];
         if (tid < CH) rec[BR_BETA / 4 + tid] = sBeta[tid];
         // ---- W = T (beta Kg) -> shared (for N) and the record; Kd = Kh e^(Gam_C - Gam)
-        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
-            CH, [&](int r, int j) { return sT[r * AS + j]; },
-            [&](int j, int c) { return sBeta[j] * sKh[toff<KD>(j, c)] * ex2n(sG[toff<KD>(j, c)]); },
+        cta_gemm<CH, KD, 1, 4, PN_WARPS>(
+            CH, [&](int r, int jj) { return sT[r * AS + jj]; },
+            [&](int jj, int c) { return sBeta[jj] * sKh[toff<KD>(jj, c)] * ex2n(sG[toff<KD>(jj, c)]); },
             [&](int r, int c, float v0, float v1) {
                 st2(sW + toff<KD>(r, c), v0, v1);
                 st2(rec + BR_W / 4 + toff<KD>(r, c), v0, v1);
             },
             warp, lane);
-        for (int idx = tid; idx < CH * KD / 4; idx += BC_THREADS) {
+        for (int idx = tid; idx < CH * KD / 4; idx += PN_THREADS) {
             const int r = idx >> 5, c = 4 * (idx & 31), o = toff<KD>(r, c);
             const float4 kh = *reinterpret_cast<const float4 *>(sKh + o), gm = *reinterpret_cast<const float4 *>(sG + o);
-            const int oc = toff<KD>(CH - 1, c);
-            const float4 gc = *reinterpret_cast<const float4 *>(sG + oc);
+            const float4 gc = *reinterpret_cast<const float4 *>(sG + toff<KD>(CH - 1, c));
             *reinterpret_cast<float4 *>(rec + BR_KD / 4 + o) =
                 make_float4(kh.x * ex2n(gc.x - gm.x), kh.y * ex2n(gc.y - gm.y), kh.z * ex2n(gc.z - gm.z),
                             kh.w * ex2n(gc.w - gm.w));
         }
         __syncthreads();
         // ---- N = Qt e^Gam - P W
-        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
-            CH, [&](int r, int j) { return sP[toff<CH>(r, j)]; }, [&](int j, int c) { return sW[toff<KD>(j, c)]; },
+        cta_gemm<CH, KD, 1, 4, PN_WARPS>(
+            CH, [&](int r, int jj) { return sP[toff<CH>(r, jj)]; }, [&](int jj, int c) { return sW[toff<KD>(jj, c)]; },
             [&](int r, int c, float v0, float v1) {
                 const int o = toff<KD>(r, c);
                 st2(rec + BR_N / 4 + o, sQt[o] * ex2n(sG[o]) - v0, sQt[o + 1] * ex2n(sG[o + 1]) - v1);
@@ -386,7 +395,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
             warp, lane);
         __syncthreads();
         // ---- V (fp32) over Qt, then U = T (beta V) as two 64-column halves
-        for (int idx = tid; idx < CH * KD / 8; idx += BC_THREADS) {
+        for (int idx = tid; idx < CH * KD / 8; idx += PN_THREADS) {
             const int r = idx >> 4, c = 8 * (idx & 15);
             float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
             if (r < len) {
@@ -398,9 +407,9 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
             *reinterpret_cast<float4 *>(sV + toff<KD>(r, c + 4)) = hi;
         }
         __syncthreads();
-        cta_gemm<CH, KD, 2, 4, BC_WARPS>(
-            CH, [&](int r, int j) { return sT[r * AS + j]; },
-            [&](int j, int c) { return sBeta[j] * sV[toff<KD>(j, c)]; },
+        cta_gemm<CH, KD, 1, 4, PN_WARPS>(
+            CH, [&](int r, int jj) { return sT[r * AS + jj]; },
+            [&](int jj, int c) { return sBeta[jj] * sV[toff<KD>(jj, c)]; },
             [&](int r, int c, float v0, float v1) {
                 st2(rec + BR_U / 4 + (c >> 6) * (CH * CH) + toff<CH>(r, c & 63), v0, v1);
             },
@@ -587,20 +596,21 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
 }
 
 // =====================================================================
-// Gradients over the value dimension, per item, the two 64-column halves of V in turn
-// (S0_h, dS_h: rows of that half of the states):
+// Gradients over the value dimension, per item (16 warps), the two 64-column halves of V in
+// turn (S0_h, dS_h: rows of that half of the states):
 //   Delta_h = U_h - W S0_h^T,  dDelta_h = P^T dO_h + Kd dS_h^T        (64 r x 64 v)
 //   dKd += Delta_h dS_h,  dQg += dO_h S0_h,  dW += -dDelta_h S0_h      (64 r x 128 k, registers)
 //   dP += dO_h Delta_h^T,  dT += dDelta_h (beta V_h)^T                 (64 x 64, registers)
 //   dv_h = beta (T^T dDelta_h),  dbeta += rowsum(T^T dDelta_h * V_h),  dGam_C += colsum(S0_h * dS_h)
 // then the sums to the item's record of value-side gradients.
 // =====================================================================
+constexpr int GN_THREADS = 512;
 constexpr uint32_t GV_W = 0, GV_KD = 32768, GV_S0 = 65536, GV_DS = 98304, GV_U = 131072, GV_P = 147456,
                    GV_T = 163840, GV_DO = 180224, GV_V = 196608, GV_DDL = 212992, GV_MISC = 229376,
-                   GV_BAR = GV_MISC + 2304, GV_BYTES = GV_BAR + 16;
+                   GV_BAR = GV_MISC + 768, GV_BYTES = GV_BAR + 16;
 static_assert(GV_BYTES + 128 <= 232448, "gradv smem");
 
-__global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcParams p) {
+__global__ __launch_bounds__(GN_THREADS, 1) void bwdc_gradv_kernel(const BwdcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<128>(smem_raw);
     if (p.hdr[1] == 0) return;
@@ -609,9 +619,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
     float *sU = reinterpret_cast<float *>(sm + GV_U), *sP = reinterpret_cast<float *>(sm + GV_P);
     float *sT = reinterpret_cast<float *>(sm + GV_T), *sDO = reinterpret_cast<float *>(sm + GV_DO);
     float *sV = reinterpret_cast<float *>(sm + GV_V), *sDD = reinterpret_cast<float *>(sm + GV_DDL);
-    // D [128], beta [64], then the two warps' row sums of dbeta's V term [2][64] and the two
-    // threads' column sums of S0 dS [2][128] (added in a fixed order: reproducible results)
-    float *sD = reinterpret_cast<float *>(sm + GV_MISC), *sBeta = sD + 128, *sDB = sD + 192, *sGC = sD + 320;
+    float *sD = reinterpret_cast<float *>(sm + GV_MISC), *sBeta = sD + 128;
     const uint32_t sbase = smem_u32(sm), bar_item = sbase + GV_BAR, bar_half = bar_item + 8;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const long long n_items = (long long)p.hdr[0] * p.H_v;
@@ -621,8 +629,8 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
         mbar_fence_init();
     }
     __syncthreads();
-    // fixed output tiles of this warp: 32 x 32 of the 64 x 128 products, 16 x 32 of the 64 x 64 ones
-    const int bm0 = 32 * (warp >> 2), bn0 = 32 * (warp & 3), sm0 = 16 * (warp >> 1), sn0 = 32 * (warp & 1);
+    // fixed output tiles of this warp: 16 x 32 of the 64 x 128 products, 16 x 16 of the 64 x 64 ones
+    const int m0 = 16 * (warp >> 2), bn0 = 32 * (warp & 3), sn0 = 16 * (warp & 3);
     uint32_t ph_item = 0, ph_half = 0;
     for (long long item = blockIdx.x; item < n_items; item += gridDim.x, ph_item ^= 1) {
         const int h = (int)(item % p.H_v);
@@ -630,16 +638,17 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
         const int len = cd.len;
         const unsigned char *rec = p.rec + (size_t)item * BR_BYTES;
         unsigned char *part = p.part + (size_t)item * CP_BYTES;
-        float akd[2][4][4], aqg[2][4][4], aw[2][4][4], ap[1][4][4], at[1][4][4];
-        float dbr[2] = {0.f, 0.f}, gcs = 0.f;   // this thread's dbeta row sums and S0 dS column sum
+        float akd[1][4][4], aqg[1][4][4], aw[1][4][4], ap[1][2][4], at[1][2][4];
         tile_zero(akd);
         tile_zero(aqg);
         tile_zero(aw);
         tile_zero(ap);
         tile_zero(at);
+        float dbr[2] = {0.f, 0.f}, gcs = 0.f;   // this thread's dbeta row sums and S0 dS column sum
         bool ok = true;
         for (int vh = 0; vh < 2; ++vh, ph_half ^= 1) {
-            __syncthreads();   // the previous half's (item's) reads of shared memory are done
+            fence_async_smem();   // this thread's writes to shared memory before the bulk copies that reuse it
+            __syncthreads();      // the previous half's (item's) reads of shared memory are done
             if (tid == 0) {
                 if (vh == 0) {
                     mbar_expect_tx(bar_item, 2 * 32768 + 2 * 16384 + 768);
@@ -655,7 +664,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
                 bulk_g2s(sbase + GV_U, rec + BR_U + vh * 16384, 16384, bar_half);
             }
             // dO and V of this half (fp32 tiles, zero past len)
-            for (int idx = tid; idx < 2 * CH * 8; idx += BC_THREADS) {
+            for (int idx = tid; idx < 2 * CH * 8; idx += GN_THREADS) {
                 const int which = idx >> 9, r = (idx >> 3) & 63, c = 8 * (idx & 7);
                 float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
                 if (r < len) {
@@ -675,45 +684,45 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
                 break;
             }
             // ---- Delta (in place of U) and dDelta
-            cta_gemm<CH, CH, 1, 4, BC_WARPS>(
-                KD, [&](int r, int k) { return sW[toff<KD>(r, k)]; }, [&](int k, int v) { return sS0[toff<KD>(v, k)]; },
-                [&](int r, int v, float e0, float e1) {
+            {
+                float acc[1][2][4];
+                tile_zero(acc);
+                mma_tile<1, 2>(acc, m0, sn0, 0, KD, [&](int r, int k) { return sW[toff<KD>(r, k)]; },
+                               [&](int k, int v) { return sS0[toff<KD>(v, k)]; }, g, t);
+                float dd[1][2][4];
+                tile_zero(dd);
+                mma_tile<1, 2>(dd, m0, sn0, 0, CH, [&](int r, int j) { return sP[toff<CH>(j, r)]; },
+                               [&](int j, int v) { return sDO[toff<CH>(j, v)]; }, g, t);
+                mma_tile<1, 2>(dd, m0, sn0, 0, KD, [&](int r, int k) { return sKd[toff<KD>(r, k)]; },
+                               [&](int k, int v) { return sDS[toff<KD>(v, k)]; }, g, t);
+                tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int v, float e0, float e1) {
                     const int o = toff<CH>(r, v);
                     st2(sU + o, sU[o] - e0, sU[o + 1] - e1);
-                },
-                warp, lane);
-            {
-                float acc[1][4][4];
-                tile_zero(acc);
-                mma_tile<1, 4>(acc, sm0, sn0, 0, CH, [&](int r, int j) { return sP[toff<CH>(j, r)]; },
-                               [&](int j, int v) { return sDO[toff<CH>(j, v)]; }, g, t);
-                mma_tile<1, 4>(acc, sm0, sn0, 0, KD, [&](int r, int k) { return sKd[toff<KD>(r, k)]; },
-                               [&](int k, int v) { return sDS[toff<KD>(v, k)]; }, g, t);
-                tile_out<1, 4>(acc, sm0, sn0, g, t,
-                               [&](int r, int v, float v0, float v1) { st2(sDD + toff<CH>(r, v), v0, v1); });
+                });
+                tile_out<1, 2>(dd, m0, sn0, g, t, [&](int r, int v, float v0, float v1) { st2(sDD + toff<CH>(r, v), v0, v1); });
             }
             __syncthreads();
             // ---- the sums over this half's value columns
-            mma_tile<2, 4>(akd, bm0, bn0, 0, CH, [&](int r, int v) { return sU[toff<CH>(r, v)]; },
+            mma_tile<1, 4>(akd, m0, bn0, 0, CH, [&](int r, int v) { return sU[toff<CH>(r, v)]; },
                            [&](int v, int k) { return sDS[toff<KD>(v, k)]; }, g, t);
-            mma_tile<2, 4>(aqg, bm0, bn0, 0, CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; },
+            mma_tile<1, 4>(aqg, m0, bn0, 0, CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; },
                            [&](int v, int k) { return sS0[toff<KD>(v, k)]; }, g, t);
-            mma_tile<2, 4>(aw, bm0, bn0, 0, CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
+            mma_tile<1, 4>(aw, m0, bn0, 0, CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
                            [&](int v, int k) { return sS0[toff<KD>(v, k)]; }, g, t);
-            mma_tile<1, 4>(ap, sm0, sn0, 0, CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; },
+            mma_tile<1, 2>(ap, m0, sn0, 0, CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; },
                            [&](int v, int j) { return sU[toff<CH>(j, v)]; }, g, t);
-            mma_tile<1, 4>(at, sm0, sn0, 0, CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
+            mma_tile<1, 2>(at, m0, sn0, 0, CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
                            [&](int v, int j) { return sBeta[j] * sV[toff<CH>(j, v)]; }, g, t);
             // dBV = T^T dDelta: dv and dbeta's V term
             {
-                float acc[1][4][4];
+                float acc[1][2][4];
                 tile_zero(acc);
-                mma_tile<1, 4>(acc, sm0, sn0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
+                mma_tile<1, 2>(acc, m0, sn0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
                                [&](int j, int v) { return sDD[toff<CH>(j, v)]; }, g, t);
                 float rs[2] = {0.f, 0.f};
-                tile_out<1, 4>(acc, sm0, sn0, g, t, [&](int r, int v, float v0, float v1) {
+                tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int v, float v0, float v1) {
                     const int o = toff<CH>(r, v);
-                    rs[(r - sm0) >> 3] += v0 * sV[o] + v1 * sV[o + 1];
+                    rs[(r - m0) >> 3] += v0 * sV[o] + v1 * sV[o + 1];
                     if (r < len) {
                         const float be = sBeta[r];
                         st2(p.dv + ((size_t)(cd.tok + r) * p.H_v + h) * KD + vh * CH + v, be * v0, be * v1);
@@ -726,10 +735,10 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
                     dbr[e] += rs[e];
                 }
             }
-            // colsum(S0_h * dS_h) per channel (this thread: 32 of the half's rows)
+            // colsum(S0_h * dS_h) per channel (this thread: 16 of the half's rows)
             {
-                const int c = tid & 127, v0 = 32 * (tid >> 7);
-                for (int v = v0; v < v0 + 32; ++v) gcs = fmaf(sS0[toff<KD>(v, c)], sDS[toff<KD>(v, c)], gcs);
+                const int c = tid & 127, v0 = 16 * (tid >> 7);
+                for (int v = v0; v < v0 + 16; ++v) gcs = fmaf(sS0[toff<KD>(v, c)], sDS[toff<KD>(v, c)], gcs);
             }
         }
         if (!ok) {
@@ -739,39 +748,48 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
         float *pDKD = reinterpret_cast<float *>(part + CP_DKD), *pDQG = reinterpret_cast<float *>(part + CP_DQG);
         float *pDW = reinterpret_cast<float *>(part + CP_DW), *pDP = reinterpret_cast<float *>(part + CP_DP);
         float *pDT = reinterpret_cast<float *>(part + CP_DT);
-        tile_out<2, 4>(akd, bm0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDKD + toff<KD>(r, k), v0, v1); });
-        tile_out<2, 4>(aqg, bm0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDQG + toff<KD>(r, k), v0, v1); });
-        tile_out<2, 4>(aw, bm0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDW + toff<KD>(r, k), -v0, -v1); });
-        tile_out<1, 4>(ap, sm0, sn0, g, t, [&](int r, int j, float v0, float v1) {
+        tile_out<1, 4>(akd, m0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDKD + toff<KD>(r, k), v0, v1); });
+        tile_out<1, 4>(aqg, m0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDQG + toff<KD>(r, k), v0, v1); });
+        tile_out<1, 4>(aw, m0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDW + toff<KD>(r, k), -v0, -v1); });
+        tile_out<1, 2>(ap, m0, sn0, g, t, [&](int r, int j, float v0, float v1) {
             st2(pDP + toff<CH>(r, j), j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
         });
-        tile_out<1, 4>(at, sm0, sn0, g, t, [&](int r, int j, float v0, float v1) { st2(pDT + toff<CH>(r, j), v0, v1); });
+        tile_out<1, 2>(at, m0, sn0, g, t, [&](int r, int j, float v0, float v1) { st2(pDT + toff<CH>(r, j), v0, v1); });
+        // the partial row / column sums through the (now free) dO tile, added in a fixed order
+        __syncthreads();
+        float *sDB = sDO, *sGC = sDO + 4 * 64;   // [4 warps of a row block][64], [4 row segments][128]
         if (t == 0) {
-            sDB[(warp & 1) * 64 + sm0 + g] = dbr[0];
-            sDB[(warp & 1) * 64 + sm0 + g + 8] = dbr[1];
+            sDB[(warp & 3) * 64 + m0 + g] = dbr[0];
+            sDB[(warp & 3) * 64 + m0 + g + 8] = dbr[1];
         }
         sGC[(tid >> 7) * 128 + (tid & 127)] = gcs;
         __syncthreads();
-        if (tid < 64) reinterpret_cast<float *>(part + CP_DB)[tid] = sDB[tid] + sDB[64 + tid];
-        if (tid < 128) reinterpret_cast<float *>(part + CP_DGC)[tid] = sGC[tid] + sGC[128 + tid];
+        if (tid < 64)
+            reinterpret_cast<float *>(part + CP_DB)[tid] = (sDB[tid] + sDB[64 + tid]) + (sDB[128 + tid] + sDB[192 + tid]);
+        else if (tid >= 128 && tid < 256) {
+            const int c = tid - 128;
+            reinterpret_cast<float *>(part + CP_DGC)[c] = (sGC[c] + sGC[128 + c]) + (sGC[256 + c] + sGC[384 + c]);
+        }
     }
 }
 
 // =====================================================================
-// Gradients over the keys, per item: dT = dT_V + dW (beta Kg)^T, dA = strict_lower(-T^T dT T^T),
-// dbeta, then (warp w owns channels 16 w .. 16 w + 15, its accumulators in registers)
-// dBW = T^T dW, the decayed pair products of M = beta dA and dP's strict part, and
+// Gradients over the keys, per item (16 warps): dT = dT_V + dW (beta Kg)^T,
+// dA = strict_lower(-T^T dT T^T), dbeta, then (warp w owns channels 8 w .. 8 w + 7, its
+// accumulators in registers) dBW = T^T dW, the decayed pair products of M = beta dA and dP's
+// strict part, and
 //   dKh = beta dBW e^Gam + (pair products) + diag(dP) Qt + dKd e^(Gam_C - Gam)
 //   dQt = dQg e^Gam + (pair products) + diag(dP) Kh
 //   dGam = beta dBW Kg + (pair products' Gam terms) + dQg Qg
 // and dg per channel from dGam's suffix sums, dGam_C and the exclusive prefix sums of dKd Kd.
 // =====================================================================
+constexpr int KN_THREADS = 512, KN_WARPS = 16;
 constexpr uint32_t GK_KH = 0, GK_QT = 32768, GK_G = 65536, GK_DW = 98304, GK_T = 131072, GK_KK = 147456,
-                   GK_DT = 163840, GK_X = 180224, GK_DP = 196608, GK_MISC = 212992, GK_BAR = GK_MISC + 4096,
+                   GK_DT = 163840, GK_X = 180224, GK_DP = 196608, GK_MISC = 212992, GK_BAR = GK_MISC + 8192,
                    GK_BYTES = GK_BAR + 16;
 static_assert(GK_BYTES + 128 <= 232448, "gradk smem");
 
-__global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcParams p) {
+__global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<128>(smem_raw);
     if (p.hdr[1] == 0) return;
@@ -780,10 +798,10 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
     float *sT = reinterpret_cast<float *>(sm + GK_T), *sKK = reinterpret_cast<float *>(sm + GK_KK);
     float *sDT = reinterpret_cast<float *>(sm + GK_DT), *sX = reinterpret_cast<float *>(sm + GK_X);
     float *sDP = reinterpret_cast<float *>(sm + GK_DP);
-    // beta [64], D [128], dGam_C [128], dbeta's V term [64], then the dbeta row sums of the
-    // dA products (two warps per row block) [2][64] and of the dBW products (one per warp) [8][64]
+    // beta [64], D [128], dGam_C [128], dbeta's V term [64], then the dbeta row sums of the dA
+    // products (four warps per row block) [4][64] and of the dBW products (one per warp) [16][64]
     float *sBeta = reinterpret_cast<float *>(sm + GK_MISC), *sD = sBeta + 64, *sDGC = sBeta + 192,
-          *sDB = sBeta + 320, *sDBa = sBeta + 384, *sDBw = sBeta + 512;
+          *sDB = sBeta + 320, *sDBa = sBeta + 384, *sDBw = sBeta + 640;
     const uint32_t sbase = smem_u32(sm), bar = sbase + GK_BAR;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     const long long n_items = (long long)p.hdr[0] * p.H_v;
@@ -793,6 +811,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
         mbar_fence_init();
     }
     __syncthreads();
+    const int m0 = 16 * (warp >> 2), sn0 = 16 * (warp & 3);   // 16 x 16 tiles of the 64 x 64 products
     uint32_t phase = 0;
     for (long long item = blockIdx.x; item < n_items; item += gridDim.x, phase ^= 1) {
         const int h = (int)(item % p.H_v);
@@ -801,6 +820,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
         const float a = ex2n(p.A_log[h]);
         const unsigned char *rec = p.rec + (size_t)item * BR_BYTES;
         const unsigned char *pt = p.part + (size_t)item * CP_BYTES;
+        fence_async_smem();   // this thread's writes to shared memory before the bulk copies that reuse it
         __syncthreads();
         if (tid == 0) {
             mbar_expect_tx(bar, 2 * 16384 + 32768 + 2 * 16384);
@@ -811,7 +831,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             bulk_g2s(sbase + GK_DP, pt + CP_DP, 16384, bar);
         }
         if (tid < 64) sDB[tid] = reinterpret_cast<const float *>(pt + CP_DB)[tid];
-        bwdc_rows(p, cd.tok, len, h, hq, a, sKh, sQt, sG, sBeta, sD, tid);
+        bwdc_rows<KN_THREADS>(p, cd.tok, len, h, hq, a, sKh, sQt, sG, sBeta, sD, sX, tid);
         if (tid < 128) sDGC[tid] = reinterpret_cast<const float *>(pt + CP_DGC)[tid] * sD[tid];
         const bool mine = mbar_wait(bar, phase);
         if (!__syncthreads_and(mine)) {
@@ -819,29 +839,35 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             break;
         }
         // ---- dT += dW (beta Kg)^T
-        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
-            KD, [&](int r, int k) { return sDW[toff<KD>(r, k)]; },
-            [&](int k, int j) { return sBeta[j] * sKh[toff<KD>(j, k)] * ex2n(sG[toff<KD>(j, k)]); },
-            [&](int r, int j, float v0, float v1) {
+        {
+            float acc[1][2][4];
+            tile_zero(acc);
+            mma_tile<1, 2>(acc, m0, sn0, 0, KD, [&](int r, int k) { return sDW[toff<KD>(r, k)]; },
+                           [&](int k, int j) { return sBeta[j] * sKh[toff<KD>(j, k)] * ex2n(sG[toff<KD>(j, k)]); }, g,
+                           t);
+            tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int j, float v0, float v1) {
                 const int o = toff<CH>(r, j);
                 st2(sDT + o, sDT[o] + v0, sDT[o + 1] + v1);
-            },
-            warp, lane);
+            });
+        }
         __syncthreads();
         // ---- X = dT T^T
-        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
-            CH, [&](int r, int j) { return sDT[toff<CH>(r, j)]; }, [&](int j, int i) { return sT[toff<CH>(i, j)]; },
-            [&](int r, int i, float v0, float v1) { st2(sX + toff<CH>(r, i), v0, v1); }, warp, lane);
-        __syncthreads();
-        // ---- dA = strict_lower(-T^T X); dbeta += rowsum(dA KK); M = beta dA over dT
         {
-            const int m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1);
-            float acc[1][4][4];
+            float acc[1][2][4];
             tile_zero(acc);
-            mma_tile<1, 4>(acc, m0, n0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
+            mma_tile<1, 2>(acc, m0, sn0, 0, CH, [&](int r, int j) { return sDT[toff<CH>(r, j)]; },
+                           [&](int j, int i) { return sT[toff<CH>(i, j)]; }, g, t);
+            tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int i, float v0, float v1) { st2(sX + toff<CH>(r, i), v0, v1); });
+        }
+        __syncthreads();
+        // ---- dA = strict_lower(-T^T X); dbeta row sums of dA KK; M = beta dA over dT
+        {
+            float acc[1][2][4];
+            tile_zero(acc);
+            mma_tile<1, 2>(acc, m0, sn0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
                            [&](int j, int i) { return sX[toff<CH>(j, i)]; }, g, t);
             float rs[2] = {0.f, 0.f};
-            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int i, float v0, float v1) {
+            tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int i, float v0, float v1) {
                 const int o = toff<CH>(r, i);
                 const float d0 = i < r ? -v0 : 0.f, d1 = i + 1 < r ? -v1 : 0.f;
                 rs[(r - m0) >> 3] += d0 * sKK[o] + d1 * sKK[o + 1];
@@ -854,17 +880,17 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
                 rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 2);
             }
             if (t == 0) {
-                sDBa[(warp & 1) * 64 + m0 + g] = rs[0];
-                sDBa[(warp & 1) * 64 + m0 + g + 8] = rs[1];
+                sDBa[(warp & 3) * 64 + m0 + g] = rs[0];
+                sDBa[(warp & 3) * 64 + m0 + g + 8] = rs[1];
             }
         }
         // ---- this warp's channels: dBW = T^T dW and the beta dBW terms
-        const int cw = 16 * warp;
-        float akh[4][2][4], aqt[4][2][4], agm[4][2][4];
+        const int cw = 8 * warp;
+        float akh[4][1][4], aqt[4][1][4], agm[4][1][4];
         {
-            float bw[4][2][4];
+            float bw[4][1][4];
             tile_zero(bw);
-            mma_tile<4, 2>(bw, 0, cw, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
+            mma_tile<4, 1>(bw, 0, cw, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
                            [&](int j, int c) { return sDW[toff<KD>(j, c)]; }, g, t);
             float rs[8];
 #pragma unroll
@@ -872,18 +898,16 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int jn = 0; jn < 2; ++jn)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = 16 * i + g + 8 * (e >> 1), c = cw + 8 * jn + 2 * t + (e & 1);
-                        const int o = toff<KD>(r, c);
-                        const float eg = ex2n(sG[o]), kh = sKh[o];
-                        const float x = sBeta[r] * bw[i][jn][e] * eg;
-                        akh[i][jn][e] = x;
-                        agm[i][jn][e] = x * kh;
-                        aqt[i][jn][e] = 0.f;
-                        rs[2 * i + (e >> 1)] += bw[i][jn][e] * kh * eg;
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 16 * i + g + 8 * (e >> 1), c = cw + 2 * t + (e & 1);
+                    const int o = toff<KD>(r, c);
+                    const float eg = ex2n(sG[o]), kh = sKh[o];
+                    const float x = sBeta[r] * bw[i][0][e] * eg;
+                    akh[i][0][e] = x;
+                    agm[i][0][e] = x * kh;
+                    aqt[i][0][e] = 0.f;
+                    rs[2 * i + (e >> 1)] += bw[i][0][e] * kh * eg;
+                }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 rs[e] += __shfl_xor_sync(0xffffffffu, rs[e], 1);
@@ -900,29 +924,19 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             const int i = pr < 1 ? 0 : pr < 3 ? 1 : pr < 6 ? 2 : 3;
             const int b = pr - (i * (i + 1)) / 2;
             const bool dg_ = (i == b);
-            // references for the channels this lane touches: B operands (cw + g, cw + 8 + g),
-            // accumulators (cw + 2t, +1, cw + 8 + 2t, +1)
-            PairRef fb[2], fc[2][2];
-#pragma unroll
-            for (int jn = 0; jn < 2; ++jn) {
-                fb[jn] = pair_ref(sG, i, b, cw + 8 * jn + g);
-                fc[jn][0] = pair_ref(sG, i, b, cw + 8 * jn + 2 * t);
-                fc[jn][1] = pair_ref(sG, i, b, cw + 8 * jn + 2 * t + 1);
-            }
+            // references for the channels this lane touches: B operands (cw + g), accumulators
+            // (cw + 2t, cw + 2t + 1)
+            const PairRef fb = pair_ref(sG, i, b, cw + g);
+            const PairRef fc[2] = {pair_ref(sG, i, b, cw + 2 * t), pair_ref(sG, i, b, cw + 2 * t + 1)};
             auto mval = [&](int r, int j) { return sDT[toff<CH>(r, j)]; };   // strictly lower already
-            auto pval = [&](int r, int j) {
-                return (!dg_ || j < r) ? sDP[toff<CH>(r, j)] : 0.f;
-            };
+            auto pval = [&](int r, int j) { return (!dg_ || j < r) ? sDP[toff<CH>(r, j)] : 0.f; };
             // row side: MH = M_ib Hk, PH = dPs_ib Hk (rows of block i)
-            float mh[2][4], ph[2][4], y[2][4];
-#pragma unroll
-            for (int jn = 0; jn < 2; ++jn)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mh[jn][e] = ph[jn][e] = y[jn][e] = 0.f;
+            float mh[4] = {0.f, 0.f, 0.f, 0.f}, ph[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f};
+            const int c = cw + g;
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 const int r0 = 16 * i + g, j0 = 16 * b + 8 * ks + t;
-                uint32_t am[4], ap[4], bh[2][2];
+                uint32_t am[4], ap[4], bh[2];
                 am[0] = tf32_rn_bits(mval(r0, j0));
                 am[1] = tf32_rn_bits(mval(r0 + 8, j0));
                 am[2] = tf32_rn_bits(mval(r0, j0 + 4));
@@ -931,20 +945,16 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
                 ap[1] = tf32_rn_bits(pval(r0 + 8, j0));
                 ap[2] = tf32_rn_bits(pval(r0, j0 + 4));
                 ap[3] = tf32_rn_bits(pval(r0 + 8, j0 + 4));
-#pragma unroll
-                for (int jn = 0; jn < 2; ++jn) {
-                    const int c = cw + 8 * jn + g;
-                    bh[jn][0] = tf32_rn_bits(sKh[toff<KD>(j0, c)] * fb[jn].colf(sG[toff<KD>(j0, c)]));
-                    bh[jn][1] = tf32_rn_bits(sKh[toff<KD>(j0 + 4, c)] * fb[jn].colf(sG[toff<KD>(j0 + 4, c)]));
-                    mma_tf32(mh[jn], am, bh[jn]);
-                    mma_tf32(ph[jn], ap, bh[jn]);
-                }
+                bh[0] = tf32_rn_bits(sKh[toff<KD>(j0, c)] * fb.colf(sG[toff<KD>(j0, c)]));
+                bh[1] = tf32_rn_bits(sKh[toff<KD>(j0 + 4, c)] * fb.colf(sG[toff<KD>(j0 + 4, c)]));
+                mma_tf32(mh, am, bh);
+                mma_tf32(ph, ap, bh);
             }
             // column side: y = M_ib^T Fk + dPs_ib^T Fq (rows of block b)
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
                 const int j0 = 16 * b + g, r0 = 16 * i + 8 * ks + t;
-                uint32_t am[4], ap[4], bk[2][2], bq[2][2];
+                uint32_t am[4], ap[4], bk[2], bq[2];
                 am[0] = tf32_rn_bits(mval(r0, j0));
                 am[1] = tf32_rn_bits(mval(r0, j0 + 8));
                 am[2] = tf32_rn_bits(mval(r0 + 4, j0));
@@ -953,119 +963,105 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
                 ap[1] = tf32_rn_bits(pval(r0, j0 + 8));
                 ap[2] = tf32_rn_bits(pval(r0 + 4, j0));
                 ap[3] = tf32_rn_bits(pval(r0 + 4, j0 + 8));
-#pragma unroll
-                for (int jn = 0; jn < 2; ++jn) {
-                    const int c = cw + 8 * jn + g;
-                    const int o0 = toff<KD>(r0, c), o1 = toff<KD>(r0 + 4, c);
-                    const float f0 = fb[jn].rowf(sG[o0]), f1 = fb[jn].rowf(sG[o1]);
-                    bk[jn][0] = tf32_rn_bits(sKh[o0] * f0);
-                    bk[jn][1] = tf32_rn_bits(sKh[o1] * f1);
-                    bq[jn][0] = tf32_rn_bits(sQt[o0] * f0);
-                    bq[jn][1] = tf32_rn_bits(sQt[o1] * f1);
-                    mma_tf32(y[jn], am, bk[jn]);
-                    mma_tf32(y[jn], ap, bq[jn]);
-                }
+                const int o0 = toff<KD>(r0, c), o1 = toff<KD>(r0 + 4, c);
+                const float f0 = fb.rowf(sG[o0]), f1 = fb.rowf(sG[o1]);
+                bk[0] = tf32_rn_bits(sKh[o0] * f0);
+                bk[1] = tf32_rn_bits(sKh[o1] * f1);
+                bq[0] = tf32_rn_bits(sQt[o0] * f0);
+                bq[1] = tf32_rn_bits(sQt[o1] * f1);
+                mma_tf32(y, am, bk);
+                mma_tf32(y, ap, bq);
             }
             // accumulate: row side into rows of block i, column side into rows of block b
 #pragma unroll
-            for (int jn = 0; jn < 2; ++jn)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = cw + 8 * jn + 2 * t + (e & 1);
-                    const PairRef &f = fc[jn][e & 1];
-                    {
-                        const int r = 16 * i + g + 8 * (e >> 1), o = toff<KD>(r, c);
-                        const float rf = f.rowf(sG[o]);
-                        const float fk = tf32_rn(sKh[o] * rf), fq = tf32_rn(sQt[o] * rf);
-                        akh[i][jn][e] += rf * mh[jn][e];
-                        aqt[i][jn][e] += rf * ph[jn][e];
-                        agm[i][jn][e] += fk * mh[jn][e] + fq * ph[jn][e];
-                    }
-                    {
-                        const int j = 16 * b + g + 8 * (e >> 1), o = toff<KD>(j, c);
-                        const float cf = f.colf(sG[o]);
-                        const float hk = tf32_rn(sKh[o] * cf);
-                        akh[b][jn][e] += cf * y[jn][e];
-                        agm[b][jn][e] -= hk * y[jn][e];
-                    }
+            for (int e = 0; e < 4; ++e) {
+                const int cc = cw + 2 * t + (e & 1);
+                const PairRef &f = fc[e & 1];
+                {
+                    const int r = 16 * i + g + 8 * (e >> 1), o = toff<KD>(r, cc);
+                    const float rf = f.rowf(sG[o]);
+                    const float fk = tf32_rn(sKh[o] * rf), fq = tf32_rn(sQt[o] * rf);
+                    akh[i][0][e] += rf * mh[e];
+                    aqt[i][0][e] += rf * ph[e];
+                    agm[i][0][e] += fk * mh[e] + fq * ph[e];
                 }
+                {
+                    const int j = 16 * b + g + 8 * (e >> 1), o = toff<KD>(j, cc);
+                    const float cf = f.colf(sG[o]);
+                    const float hk = tf32_rn(sKh[o] * cf);
+                    akh[b][0][e] += cf * y[e];
+                    agm[b][0][e] -= hk * y[e];
+                }
+            }
         }
-        // ---- the remaining terms, dqt / dkh out, dGam and dKd Kd to shared memory
+        // ---- the remaining terms, dqt / dkh out, dGam and dKd Kd over dW and Qt (since the
+        // barrier after M, this warp alone reads or writes its channels' columns of those two tiles)
+        __syncwarp();
         const float *pkd = reinterpret_cast<const float *>(pt + CP_DKD), *pqg = reinterpret_cast<const float *>(pt + CP_DQG);
-        float kdk[4][2][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int jn = 0; jn < 2; ++jn)
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = 16 * i + g + 8 * hh, c = cw + 2 * t, o = toff<KD>(r, c);
+                const float2 dk2 = *reinterpret_cast<const float2 *>(pkd + o), dq2 = *reinterpret_cast<const float2 *>(pqg + o);
+                const float dpd = sDP[toff<CH>(r, r)];
+                const float dkd[2] = {dk2.x, dk2.y}, dqg[2] = {dq2.x, dq2.y};
+                float okh[2], oqt[2], gam[2], kdk[2];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * i + g + 8 * hh, c = cw + 8 * jn + 2 * t, o = toff<KD>(r, c);
-                    const float2 dk2 = *reinterpret_cast<const float2 *>(pkd + o), dq2 = *reinterpret_cast<const float2 *>(pqg + o);
-                    const float dpd = sDP[toff<CH>(r, r)];
-                    const float dkd[2] = {dk2.x, dk2.y}, dqg[2] = {dq2.x, dq2.y};
-                    float okh[2], oqt[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int e = 2 * hh + u;
-                        const float gm = sG[o + u], gc = sG[toff<KD>(CH - 1, c + u)];
-                        const float eg = ex2n(gm), ed = ex2n(gc - gm), qt = sQt[o + u], kh = sKh[o + u];
-                        okh[u] = akh[i][jn][e] + dpd * qt + dkd[u] * ed;
-                        oqt[u] = aqt[i][jn][e] + dqg[u] * eg + dpd * kh;
-                        agm[i][jn][e] += dqg[u] * qt * eg;
-                        kdk[i][jn][e] = dkd[u] * kh * ed;
-                    }
-                    if (r < len) {
-                        const size_t go = ((size_t)(cd.tok + r) * p.H_v + h) * KD + c;
-                        st2(p.dkh + go, okh[0], okh[1]);
-                        st2(p.dqt + go, oqt[0], oqt[1]);
-                    }
+                for (int u = 0; u < 2; ++u) {
+                    const int e = 2 * hh + u;
+                    const float gm = sG[o + u], gc = sG[toff<KD>(CH - 1, c + u)];
+                    const float eg = ex2n(gm), ed = ex2n(gc - gm), qt = sQt[o + u], kh = sKh[o + u];
+                    okh[u] = akh[i][0][e] + dpd * qt + dkd[u] * ed;
+                    oqt[u] = aqt[i][0][e] + dqg[u] * eg + dpd * kh;
+                    gam[u] = agm[i][0][e] + dqg[u] * qt * eg;
+                    kdk[u] = dkd[u] * kh * ed;
                 }
-        __syncthreads();   // every warp is done reading dW and Qt
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int jn = 0; jn < 2; ++jn)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * i + g + 8 * hh, c = cw + 8 * jn + 2 * t, o = toff<KD>(r, c);
-                    st2(sDW + o, agm[i][jn][2 * hh], agm[i][jn][2 * hh + 1]);
-                    st2(sQt + o, kdk[i][jn][2 * hh], kdk[i][jn][2 * hh + 1]);
+                st2(sDW + o, gam[0], gam[1]);
+                st2(sQt + o, kdk[0], kdk[1]);
+                if (r < len) {
+                    const size_t go = ((size_t)(cd.tok + r) * p.H_v + h) * KD + c;
+                    st2(p.dkh + go, okh[0], okh[1]);
+                    st2(p.dqt + go, oqt[0], oqt[1]);
                 }
+            }
         __syncthreads();
-        // ---- dg = suffix sums of dGam + dGam_C + exclusive prefix sums of dKd Kd (two threads
-        // per channel: rows 0..31 and 32..63, each half's total passed to the other); dbeta
+        // ---- dg = suffix sums of dGam + dGam_C + exclusive prefix sums of dKd Kd (four threads
+        // per channel over 16-row segments, the segment totals passed through shared memory); dbeta
         {
-            const int c = tid & (KD - 1), half = tid >> 7, r0 = 32 * half;
+            const int c = tid & (KD - 1), seg = tid >> 7, r0 = 16 * seg;
             float pre = 0.f;
-            for (int r = r0; r < r0 + 32; ++r) {
+            for (int r = r0; r < r0 + 16; ++r) {
                 const int o = toff<KD>(r, c);
                 const float x = sQt[o];
                 sQt[o] = pre;
                 pre += x;
             }
             float suf = 0.f;
-            for (int r = r0 + 31; r >= r0; --r) {
+            for (int r = r0 + 15; r >= r0; --r) {
                 const int o = toff<KD>(r, c);
                 suf += sDW[o];
                 sDW[o] = suf;
             }
-            if (half == 0) sX[c] = pre;        // dKd Kd summed over rows 0..31
-            else sX[KD + c] = suf;             // dGam summed over rows 32..63
+            sX[seg * KD + c] = pre;               // dKd Kd summed over the segment
+            sX[4 * KD + seg * KD + c] = suf;      // dGam summed over the segment
         }
         __syncthreads();
         {
-            const int c = tid & (KD - 1), half = tid >> 7, r0 = 32 * half;
-            const float add = (half ? sX[c] : sX[KD + c]) + sDGC[c];
-            const int r1 = min(r0 + 32, len);
+            const int c = tid & (KD - 1), seg = tid >> 7, r0 = 16 * seg;
+            float add = sDGC[c];
+            for (int s2 = 0; s2 < seg; ++s2) add += sX[s2 * KD + c];
+            for (int s2 = seg + 1; s2 < 4; ++s2) add += sX[4 * KD + s2 * KD + c];
+            const int r1 = min(r0 + 16, len);
             for (int r = r0; r < r1; ++r) {
                 const int o = toff<KD>(r, c);
                 p.dg[((size_t)(cd.tok + r) * p.H_v + h) * KD + c] = sDW[o] + sQt[o] + add;
             }
         }
         if (tid < len) {
-            float db = sDB[tid] + sDBa[tid] + sDBa[64 + tid];
+            float db = sDB[tid] + (sDBa[tid] + sDBa[64 + tid]) + (sDBa[128 + tid] + sDBa[192 + tid]);
 #pragma unroll
-            for (int w = 0; w < BC_WARPS; ++w) db += sDBw[w * 64 + tid];
+            for (int w = 0; w < KN_WARPS; ++w) db += sDBw[w * 64 + tid];
             p.dbeta[(size_t)(cd.tok + tid) * p.H_v + h] = db;
         }
     }
@@ -1255,7 +1251,7 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         const long long n_items = nck * H_v;
         const int g_items = (int)(n_items < nsm ? n_items : nsm);
         if ((e = smem_attr(bwdc_prep_kernel, PS_BYTES)) != cudaSuccess) return e;
-        bwdc_prep_kernel<<<g_items, BC_THREADS, PS_BYTES + 128, stream>>>(bp);
+        bwdc_prep_kernel<<<g_items, PN_THREADS, PS_BYTES + 128, stream>>>(bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_prep_kernel", stream);
@@ -1278,11 +1274,11 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         const int g_items = (int)(n_items < nsm ? n_items : nsm);
         if ((e = smem_attr(bwdc_gradv_kernel, GV_BYTES)) != cudaSuccess) return e;
         if ((e = smem_attr(bwdc_gradk_kernel, GK_BYTES)) != cudaSuccess) return e;
-        bwdc_gradv_kernel<<<g_items, BC_THREADS, GV_BYTES + 128, stream>>>(bp);
+        bwdc_gradv_kernel<<<g_items, GN_THREADS, GV_BYTES + 128, stream>>>(bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_gradv_kernel", stream);
-        bwdc_gradk_kernel<<<g_items, BC_THREADS, GK_BYTES + 128, stream>>>(bp);
+        bwdc_gradk_kernel<<<g_items, KN_THREADS, GK_BYTES + 128, stream>>>(bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_gradk_kernel", stream);

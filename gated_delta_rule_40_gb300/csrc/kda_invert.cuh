@@ -91,20 +91,28 @@ __device__ __forceinline__ void invert_unit_lower64(const float *sA, float *sT, 
     }
     __syncthreads();
     {
-        const int m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        split_mma<4>(sA + (32 + m0) * AS, AS, sT + n0, AS, gid, tig, d);
-        sX[(m0 + gid) * XS + n0 + 2 * tig] = d[0];
-        sX[(m0 + gid) * XS + n0 + 2 * tig + 1] = d[1];
-        sX[(m0 + gid + 8) * XS + n0 + 2 * tig] = d[2];
-        sX[(m0 + gid + 8) * XS + n0 + 2 * tig + 1] = d[3];
+        // the 32 x 32 lower-left block: eight 16 x 8 tiles, one per warp (warps past the
+        // eighth only take part in the barriers)
+        static_assert(NT >= 256, "eight warps compute the lower-left block");
+        const bool act = warp < 8;
+        const int m0 = 16 * ((warp & 7) >> 2), n0 = 8 * (warp & 3);
+        if (act) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            split_mma<4>(sA + (32 + m0) * AS, AS, sT + n0, AS, gid, tig, d);
+            sX[(m0 + gid) * XS + n0 + 2 * tig] = d[0];
+            sX[(m0 + gid) * XS + n0 + 2 * tig + 1] = d[1];
+            sX[(m0 + gid + 8) * XS + n0 + 2 * tig] = d[2];
+            sX[(m0 + gid + 8) * XS + n0 + 2 * tig + 1] = d[3];
+        }
         __syncthreads();
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
-        split_mma<4>(sT + (32 + m0) * AS + 32, AS, sX + n0, XS, gid, tig, t);
-        sT[(32 + m0 + gid) * AS + n0 + 2 * tig] = -t[0];
-        sT[(32 + m0 + gid) * AS + n0 + 2 * tig + 1] = -t[1];
-        sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig] = -t[2];
-        sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig + 1] = -t[3];
+        if (act) {
+            float t[4] = {0.f, 0.f, 0.f, 0.f};
+            split_mma<4>(sT + (32 + m0) * AS + 32, AS, sX + n0, XS, gid, tig, t);
+            sT[(32 + m0 + gid) * AS + n0 + 2 * tig] = -t[0];
+            sT[(32 + m0 + gid) * AS + n0 + 2 * tig + 1] = -t[1];
+            sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig] = -t[2];
+            sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig + 1] = -t[3];
+        }
     }
     __syncthreads();
 }
