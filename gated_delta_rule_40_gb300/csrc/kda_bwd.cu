@@ -153,7 +153,6 @@ struct BwdcParams {
     float *dv, *dh0;
 };
 
-constexpr int BC_THREADS = 256, BC_WARPS = 8;
 
 // The chunk's rows into shared memory: Kh = k / |k| and Qt = scale q / |q| (fp32 tiles),
 // Gam (fp32 tile; rows past len repeat the last valid row, their g being 0), beta = sigmoid(b)
@@ -427,6 +426,7 @@ __global__ __launch_bounds__(PN_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
 // per-chunk extras (D, and U's V block or the chunk's dO rows) through a double buffer.
 // Every wait is bounded; a timeout records KDA_ERR_DEVICE_TIMEOUT and the CTA stops.
 // =====================================================================
+constexpr int CN_THREADS = 256, CN_WARPS = 8;
 template <bool BWD>
 struct ChainCfg {
     static constexpr int OPS = BWD ? 3 : 2;             // ring tiles per chunk
@@ -439,7 +439,7 @@ struct ChainCfg {
 static_assert(ChainCfg<true>::BYTES + 128 <= 232448 && ChainCfg<false>::BYTES + 128 <= 232448, "chain smem");
 
 template <bool BWD>
-__global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcParams p) {
+__global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcParams p) {
     using Cfg = ChainCfg<BWD>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<128>(smem_raw);
@@ -462,7 +462,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
     }
     // X from the initial state (forward) or the final state's gradient (backward)
     const float *x0 = BWD ? p.dht : p.init;
-    for (int idx = tid; idx < CH * KD / 4; idx += BC_THREADS) {
+    for (int idx = tid; idx < CH * KD / 4; idx += CN_THREADS) {
         const int r = idx >> 5, c = 4 * (idx & 31);
         const float4 v = x0 ? *reinterpret_cast<const float4 *>(x0 + sh + (size_t)r * KD + c)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -531,7 +531,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
             bulk_commit();
         }
         // ---- E (64 v x 64 r) = X op1^T, then Z
-        cta_gemm<CH, CH, 1, 4, BC_WARPS>(
+        cta_gemm<CH, CH, 1, 4, CN_WARPS>(
             KD, [&](int v, int k) { return sX[toff<KD>(v, k)]; }, [&](int k, int r) { return op1[toff<KD>(r, k)]; },
             [&](int v, int r, float e0, float e1) {
                 float z0 = -e0, z1 = -e1;
@@ -580,7 +580,7 @@ __global__ __launch_bounds__(BC_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
     }
     __syncthreads();
     if (BWD && ok) {
-        for (int idx = tid; idx < CH * KD / 4; idx += BC_THREADS) {
+        for (int idx = tid; idx < CH * KD / 4; idx += CN_THREADS) {
             const int r = idx >> 5, cc = 4 * (idx & 31);
             *reinterpret_cast<float4 *>(p.dh0 + sh + (size_t)r * KD + cc) =
                 *reinterpret_cast<const float4 *>(sX + toff<KD>(r, cc));
@@ -1079,7 +1079,7 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
 constexpr int BP_WARPS = 8;
 constexpr int BP_TOKENS = 16;   // tokens per warp
 
-__global__ __launch_bounds__(BP_WARPS * 32) void bwdc_jacobian_kernel(const BwdcParams p, float *dq, float *dk,
+__global__ __launch_bounds__(BP_WARPS * 32, 2) void bwdc_jacobian_kernel(const BwdcParams p, float *dq, float *dk,
                                                                       float *dgraw, float *db, float *dal,
                                                                       long long tokens) {
     const int lane = threadIdx.x & 31;
@@ -1089,64 +1089,104 @@ __global__ __launch_bounds__(BP_WARPS * 32) void bwdc_jacobian_kernel(const Bwdc
     const int hq = (int)(gw % p.H_qk);
     const long long range = gw / p.H_qk, t0 = range * BP_TOKENS, t1 = min(t0 + BP_TOKENS, tokens);
     const int group = p.H_v / p.H_qk;
-    for (long long tok = t0; tok < t1; ++tok) {
-        const size_t qo = ((size_t)tok * p.H_qk + hq) * KD + 4 * lane;
-        const uint2 qw = *reinterpret_cast<const uint2 *>(p.q + qo), kw = *reinterpret_cast<const uint2 *>(p.k + qo);
-        const float qv[4] = {bf16_lo(qw.x), bf16_hi(qw.x), bf16_lo(qw.y), bf16_hi(qw.y)};
-        const float kv[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
-        float sq[4] = {0.f, 0.f, 0.f, 0.f}, sk[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int g = 0; g < group; ++g) {
-            const size_t ho = ((size_t)tok * p.H_v + hq * group + g) * KD + 4 * lane;
-            const float4 a = *reinterpret_cast<const float4 *>(p.dqt + ho);
-            const float4 b = *reinterpret_cast<const float4 *>(p.dkh + ho);
-            sq[0] += a.x; sq[1] += a.y; sq[2] += a.z; sq[3] += a.w;
-            sk[0] += b.x; sk[1] += b.y; sk[2] += b.z; sk[3] += b.w;
-        }
-        float nq = 0.f, nk = 0.f, qd = 0.f, kd = 0.f;
+    constexpr int U = 4;   // tokens in flight: their loads are issued before any of them is used
+    for (long long tb = t0; tb < t1; tb += U) {
+        uint2 qw[U], kw[U];
+        float4 sq[U], sk[U];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            nq = fmaf(qv[i], qv[i], nq);
-            nk = fmaf(kv[i], kv[i], nk);
-            qd = fmaf(qv[i], sq[i], qd);
-            kd = fmaf(kv[i], sk[i], kd);
+        for (int u = 0; u < U; ++u) {
+            const long long tok = tb + u;
+            qw[u] = kw[u] = make_uint2(0u, 0u);
+            sq[u] = sk[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (tok < t1) {
+                const size_t qo = ((size_t)tok * p.H_qk + hq) * KD + 4 * lane;
+                qw[u] = *reinterpret_cast<const uint2 *>(p.q + qo);
+                kw[u] = *reinterpret_cast<const uint2 *>(p.k + qo);
+                for (int g = 0; g < group; ++g) {
+                    const size_t ho = ((size_t)tok * p.H_v + hq * group + g) * KD + 4 * lane;
+                    const float4 x = *reinterpret_cast<const float4 *>(p.dqt + ho);
+                    const float4 y = *reinterpret_cast<const float4 *>(p.dkh + ho);
+                    sq[u].x += x.x; sq[u].y += x.y; sq[u].z += x.z; sq[u].w += x.w;
+                    sk[u].x += y.x; sk[u].y += y.y; sk[u].z += y.z; sk[u].w += y.w;
+                }
+            }
         }
-        nq = warp_sum(nq);
-        nk = warp_sum(nk);
-        qd = warp_sum(qd);
-        kd = warp_sum(kd);
-        const float rq = rsqrtf(nq + L2_EPS), rk = rsqrtf(nk + L2_EPS);
-        float4 oq, ok;
-        oq.x = p.scale * rq * (sq[0] - rq * rq * qv[0] * qd); oq.y = p.scale * rq * (sq[1] - rq * rq * qv[1] * qd);
-        oq.z = p.scale * rq * (sq[2] - rq * rq * qv[2] * qd); oq.w = p.scale * rq * (sq[3] - rq * rq * qv[3] * qd);
-        ok.x = rk * (sk[0] - rk * rk * kv[0] * kd); ok.y = rk * (sk[1] - rk * rk * kv[1] * kd);
-        ok.z = rk * (sk[2] - rk * rk * kv[2] * kd); ok.w = rk * (sk[3] - rk * rk * kv[3] * kd);
-        *reinterpret_cast<float4 *>(dq + qo) = oq;
-        *reinterpret_cast<float4 *>(dk + qo) = ok;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long tok = tb + u;
+            const float qv[4] = {bf16_lo(qw[u].x), bf16_hi(qw[u].x), bf16_lo(qw[u].y), bf16_hi(qw[u].y)};
+            const float kv[4] = {bf16_lo(kw[u].x), bf16_hi(kw[u].x), bf16_lo(kw[u].y), bf16_hi(kw[u].y)};
+            const float dqs[4] = {sq[u].x, sq[u].y, sq[u].z, sq[u].w}, dks[4] = {sk[u].x, sk[u].y, sk[u].z, sk[u].w};
+            float nq = 0.f, nk = 0.f, qd = 0.f, kd = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                nq = fmaf(qv[i], qv[i], nq);
+                nk = fmaf(kv[i], kv[i], nk);
+                qd = fmaf(qv[i], dqs[i], qd);
+                kd = fmaf(kv[i], dks[i], kd);
+            }
+            nq = warp_sum(nq);
+            nk = warp_sum(nk);
+            qd = warp_sum(qd);
+            kd = warp_sum(kd);
+            if (tok < t1) {
+                const size_t qo = ((size_t)tok * p.H_qk + hq) * KD + 4 * lane;
+                const float rq = rsqrtf(nq + L2_EPS), rk = rsqrtf(nk + L2_EPS);
+                float4 oq, ok;
+                oq.x = p.scale * rq * (dqs[0] - rq * rq * qv[0] * qd); oq.y = p.scale * rq * (dqs[1] - rq * rq * qv[1] * qd);
+                oq.z = p.scale * rq * (dqs[2] - rq * rq * qv[2] * qd); oq.w = p.scale * rq * (dqs[3] - rq * rq * qv[3] * qd);
+                ok.x = rk * (dks[0] - rk * rk * kv[0] * kd); ok.y = rk * (dks[1] - rk * rk * kv[1] * kd);
+                ok.z = rk * (dks[2] - rk * rk * kv[2] * kd); ok.w = rk * (dks[3] - rk * rk * kv[3] * kd);
+                *reinterpret_cast<float4 *>(dq + qo) = oq;
+                *reinterpret_cast<float4 *>(dk + qo) = ok;
+            }
+        }
     }
 #pragma unroll 1
     for (int g = 0; g < group; ++g) {
         const int h = hq * group + g;
         const float a = ex2n(p.A_log[h]);
         float acc = 0.f;
-        for (long long tok = t0; tok < t1; ++tok) {
-            const size_t vo = ((size_t)tok * p.H_v + h) * KD + 4 * lane;
-            const uint2 gw2 = *reinterpret_cast<const uint2 *>(p.graw + vo);
-            const float gr[4] = {bf16_lo(gw2.x), bf16_hi(gw2.x), bf16_lo(gw2.y), bf16_hi(gw2.y)};
-            const float4 dg4 = *reinterpret_cast<const float4 *>(p.dg + vo);
-            const float dgv[4] = {dg4.x, dg4.y, dg4.z, dg4.w};
-            float out[4];
+        for (long long tb = t0; tb < t1; tb += U) {
+            uint2 gw[U];
+            float4 dg4[U];
+            float bb[U], dbt[U];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float sp = softplus_log2(gr[i]) * (1.0f / LOG2E);   // softplus (natural units)
-                const float sig = 1.0f / (1.0f + __expf(-gr[i]));
-                out[i] = dgv[i] * (-a) * sig;
-                acc = fmaf(dgv[i], -a * sp, acc);
+            for (int u = 0; u < U; ++u) {
+                const long long tok = tb + u;
+                gw[u] = make_uint2(0u, 0u);
+                dg4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                bb[u] = dbt[u] = 0.f;
+                if (tok < t1) {
+                    const size_t vo = ((size_t)tok * p.H_v + h) * KD + 4 * lane;
+                    gw[u] = *reinterpret_cast<const uint2 *>(p.graw + vo);
+                    dg4[u] = *reinterpret_cast<const float4 *>(p.dg + vo);
+                    if (lane == 0) {
+                        bb[u] = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
+                        dbt[u] = p.dbeta[(size_t)tok * p.H_v + h];
+                    }
+                }
             }
-            *reinterpret_cast<float4 *>(dgraw + vo) = make_float4(out[0], out[1], out[2], out[3]);
-            if (lane == 0) {
-                const float bb = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
-                const float beta = 1.0f / (1.0f + __expf(-bb));
-                db[(size_t)tok * p.H_v + h] = p.dbeta[(size_t)tok * p.H_v + h] * beta * (1.0f - beta);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const long long tok = tb + u;
+                if (tok >= t1) break;
+                const size_t vo = ((size_t)tok * p.H_v + h) * KD + 4 * lane;
+                const float gr[4] = {bf16_lo(gw[u].x), bf16_hi(gw[u].x), bf16_lo(gw[u].y), bf16_hi(gw[u].y)};
+                const float dgv[4] = {dg4[u].x, dg4[u].y, dg4[u].z, dg4[u].w};
+                float out[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float sp = softplus_log2(gr[i]) * (1.0f / LOG2E);   // softplus (natural units)
+                    const float sig = 1.0f / (1.0f + __expf(-gr[i]));
+                    out[i] = dgv[i] * (-a) * sig;
+                    acc = fmaf(dgv[i], -a * sp, acc);
+                }
+                *reinterpret_cast<float4 *>(dgraw + vo) = make_float4(out[0], out[1], out[2], out[3]);
+                if (lane == 0) {
+                    const float beta = 1.0f / (1.0f + __expf(-bb[u]));
+                    db[(size_t)tok * p.H_v + h] = dbt[u] * beta * (1.0f - beta);
+                }
             }
         }
         acc = warp_sum(acc);
@@ -1260,11 +1300,11 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
         const unsigned chains = (unsigned)((long long)nseq * H_v * 2);
         if ((e = smem_attr(bwdc_chain_kernel<false>, ChainCfg<false>::BYTES)) != cudaSuccess) return e;
         if ((e = smem_attr(bwdc_chain_kernel<true>, ChainCfg<true>::BYTES)) != cudaSuccess) return e;
-        bwdc_chain_kernel<false><<<chains, BC_THREADS, ChainCfg<false>::BYTES + 128, stream>>>(bp);
+        bwdc_chain_kernel<false><<<chains, CN_THREADS, ChainCfg<false>::BYTES + 128, stream>>>(bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_chain_kernel<fwd>", stream);
-        bwdc_chain_kernel<true><<<chains, BC_THREADS, ChainCfg<true>::BYTES + 128, stream>>>(bp);
+        bwdc_chain_kernel<true><<<chains, CN_THREADS, ChainCfg<true>::BYTES + 128, stream>>>(bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_chain_kernel<bwd>", stream);
