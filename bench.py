@@ -41,10 +41,20 @@ BYTES_PER_TOKEN_HEAD = 1282
 STATE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4
 FLOPS_PER_TOKEN_HEAD = 139264
 # Decode step: state read + write (2 x 64 KiB per (b, h)) plus q/k/v/graw/b/out (~1.3 KB)
-# Backward (token recurrence run twice forwards and once backwards on CUDA cores): per token and
-# value head 2 x 3 K V (recomputed updates) + 11 K V (the backward step's products) multiply-adds,
-# 2 flops each.
-BWD_FLOPS_PER_TOKEN_HEAD = 2 * (2 * 3 + 11) * 128 * 128
+# Backward in the chunk form (tf32 tensor-core products), multiply-adds per (64-token chunk, value
+# head): prep 10 sub-block pairs x 16x16x128 for A and for P, W and U (64x128x64 each), N (64x128x64);
+# forward chain 2 V blocks x (64x64x128 + 64x128x64); backward chain 2 x (64x64x128 + 2 x 64x128x64);
+# value side Delta 64x128x128, dDelta 64x128x(64 + 128), dKd / dQg / dW 64x128x128 each, dP and dT
+# 64x64x128 each, dBV 64x128x64; key side dT 64x64x128, X and dA 64x64x64 each, dBW 64x128x64, pair
+# products 10 x 4 x 16x128x16.  2 flops each, per token and value head (64 tokens per chunk).
+BWD_MACS_PER_CHUNK_HEAD = (10 * 2 * 16 * 16 * 128 + 3 * 64 * 128 * 64
+                           + 2 * (64 * 64 * 128 + 64 * 128 * 64) + 2 * (64 * 64 * 128 + 2 * 64 * 128 * 64)
+                           + 64 * 128 * 128 + 64 * 128 * 192 + 3 * 64 * 128 * 128 + 2 * 64 * 64 * 128
+                           + 64 * 128 * 64
+                           + 64 * 64 * 128 + 2 * 64 * 64 * 64 + 64 * 128 * 64 + 10 * 4 * 16 * 128 * 16)
+BWD_FLOPS_PER_TOKEN_HEAD = 2 * BWD_MACS_PER_CHUNK_HEAD // 64
+# nominal dense tf32 : bf16 tensor rates (1.1 : 2.25 PFLOP/s per GPU)
+TF32_PER_BF16 = 1.1 / 2.25
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -599,13 +609,12 @@ def run_gpu(args, rank, world, local):
     bwd_kernels = {name: t for name, t in kda.kda_kernel_times()}
     kda.kda_set_kernel_timing(False)
     bwd_flops = units * BWD_FLOPS_PER_TOKEN_HEAD
-    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    alu_peak = sm_count * 128 * 2 * ((clk or {}).get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    tf32_peak = tc_peak * TF32_PER_BF16
     backward = {"workload": WORKLOAD, "ms": bwd_ms, "value": units / (bwd_ms * 1e-3), "unit": UNIT,
-                "roofline": {"bound": "alu", "achieved": bwd_flops / (bwd_ms * 1e-3) / 1e12,
-                             "peak": alu_peak, "unit": "TFLOP/s",
-                             "frac": bwd_flops / (bwd_ms * 1e-3) / 1e12 / alu_peak,
-                             "peak_source": "SMs x 128 fp32 lanes x 2 flops x max SM clock",
+                "roofline": {"bound": "tensor", "achieved": bwd_flops / (bwd_ms * 1e-3) / 1e12,
+                             "peak": tf32_peak, "unit": "TFLOP/s",
+                             "frac": bwd_flops / (bwd_ms * 1e-3) / 1e12 / tf32_peak,
+                             "peak_source": f"{peak_src} bf16 burst x nominal tf32/bf16 ratio {TF32_PER_BF16:.3f}",
                              "flops_per_token_head": BWD_FLOPS_PER_TOKEN_HEAD},
                 "kernels_ms": bwd_kernels}
     del gout, ght

@@ -40,7 +40,11 @@ def test_algorithmic_constants():
     # q, k, v, graw (4 x 256 B) + b (2 B) + out (256 B)
     assert bench.BYTES_PER_TOKEN_HEAD == 4 * 2 * K + 2 + 2 * V
     assert bench.STATE_BYTES_PER_SEQ_HEAD == 2 * K * V * 4
-    assert bench.BWD_FLOPS_PER_TOKEN_HEAD == 2 * (2 * 3 + 11) * K * V
+    # chunk-form backward in units of one 64 x 64 x 128 product (u) per (chunk, value head):
+    # prep 1.25 u (A, P sub-block pairs) + 3 u (W, U, N); chains 4 u + 6 u; value side 14 u;
+    # key side 3 u + 2.5 u (pair products) = 33.75 u, 2 flops per multiply-add, 64 tokens
+    u = 64 * 64 * 128
+    assert bench.BWD_FLOPS_PER_TOKEN_HEAD == 2 * int(33.75 * u) // 64
 
 
 def test_whole_job_value_is_units_over_max_time():
