@@ -54,34 +54,123 @@ __device__ __forceinline__ int toff(int r, int c) {
     return r * W + ((((c >> 2) ^ (((r & 3) << 1) | ((r >> 2) & 1)))) << 2) + (c & 3);
 }
 
-// acc (16 TM x 8 TN at (m0, n0)) += A (m0.., k) B (k, n0..) for k in [k0, k1), fa / fb return
-// fp32 values, rounded to the nearest tf32 on the way in.
-template <int TM, int TN, class FA, class FB>
-__device__ __forceinline__ void mma_tile(float (&acc)[TM][TN][4], int m0, int n0, int k0, int k1, FA fa, FB fb,
-                                         int g, int t) {
-#pragma unroll 2
-    for (int k = k0; k < k1; k += 8) {
-        uint32_t a[TM][4], b[TN][2];
+__device__ __forceinline__ int tswz(int r) { return ((r & 3) << 1) | ((r >> 2) & 1); }
+
+// Four 8 x 8 b16 matrices from shared memory: lanes 8 i .. 8 i + 7 give the row addresses of
+// matrix i; register i of lane l holds row l / 4, 32-bit column l % 4 of matrix i.  On an fp32
+// tile, an 8 x 4 block of fp32 values is one such matrix, and lane l receives (l / 4, l % 4):
+// the tf32 fragment element for (g, t).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// ---- fragment loaders: la(a, k) fills a[TM][4] (rows m0.. of A, columns k..k+7), lb(b, k)
+// fills b[TN][2] (rows k..k+7 of B, columns n0..).  "K-contiguous" loaders read a tile whose
+// rows are the fragment's M (or N) index and whose columns are K, with ldmatrix; RND adds the
+// round-to-nearest step for values that are not tf32 numbers already.
+template <int W, int TM, bool RND>
+struct AKc {   // A (m, k) = tile[m][k], tile row stride W floats (unit-permuted) or AS (plain, W = 0)
+    uint32_t base[TM];
+    int sw[TM], hi;
+    __device__ __forceinline__ AKc(const float *tile, int m0, int lane) {
+        hi = lane >> 4;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int r = m0 + 16 * i + (lane & 7) + ((lane >> 3) & 1) * 8;
+            base[i] = smem_u32(tile) + (uint32_t)(r * (W ? W : AS) * 4);
+            sw[i] = W ? tswz(r) : 0;
+        }
+    }
+    __device__ __forceinline__ void operator()(uint32_t (&a)[TM][4], int k) const {
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            ldsm_x4(a[i], base[i] + ((((k >> 2) + hi) ^ sw[i]) << 4));
+            if (RND)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a[i][e] += 0x1000u;
+        }
+    }
+};
+template <int W, int TN, bool RND>
+struct BKc {   // B (k, n) = tile[n][k], TN even
+    static_assert(TN % 2 == 0, "pairs of n8 tiles");
+    uint32_t base[TN / 2];
+    int sw[TN / 2], hi;
+    __device__ __forceinline__ BKc(const float *tile, int n0, int lane) {
+        hi = (lane >> 3) & 1;
+#pragma unroll
+        for (int q = 0; q < TN / 2; ++q) {
+            const int r = n0 + 16 * q + (lane & 7) + (lane >> 4) * 8;
+            base[q] = smem_u32(tile) + (uint32_t)(r * W * 4);
+            sw[q] = tswz(r);
+        }
+    }
+    __device__ __forceinline__ void operator()(uint32_t (&b)[TN][2], int k) const {
+#pragma unroll
+        for (int q = 0; q < TN / 2; ++q) {
+            uint32_t r[4];
+            ldsm_x4(r, base[q] + ((((k >> 2) + hi) ^ sw[q]) << 4));
+            if (RND)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) r[e] += 0x1000u;
+            b[2 * q][0] = r[0];
+            b[2 * q][1] = r[1];
+            b[2 * q + 1][0] = r[2];
+            b[2 * q + 1][1] = r[3];
+        }
+    }
+};
+// scalar loaders from value accessors f(m, k) / f(k, n); RND false when the values are tf32 numbers
+template <int TM, bool RND, class F>
+struct AFn {
+    F f;
+    int m0, g, t;
+    __device__ __forceinline__ void operator()(uint32_t (&a)[TM][4], int k) const {
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             const int m = m0 + 16 * i + g;
-            a[i][0] = tf32_rn_bits(fa(m, k + t));
-            a[i][1] = tf32_rn_bits(fa(m + 8, k + t));
-            a[i][2] = tf32_rn_bits(fa(m, k + t + 4));
-            a[i][3] = tf32_rn_bits(fa(m + 8, k + t + 4));
+            const float v[4] = {f(m, k + t), f(m + 8, k + t), f(m, k + t + 4), f(m + 8, k + t + 4)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[i][e] = RND ? tf32_rn_bits(v[e]) : __float_as_uint(v[e]);
         }
+    }
+};
+template <int TN, bool RND, class F>
+struct BFn {
+    F f;
+    int n0, g, t;
+    __device__ __forceinline__ void operator()(uint32_t (&b)[TN][2], int k) const {
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
             const int n = n0 + 8 * j + g;
-            b[j][0] = tf32_rn_bits(fb(k + t, n));
-            b[j][1] = tf32_rn_bits(fb(k + t + 4, n));
+            const float v0 = f(k + t, n), v1 = f(k + t + 4, n);
+            b[j][0] = RND ? tf32_rn_bits(v0) : __float_as_uint(v0);
+            b[j][1] = RND ? tf32_rn_bits(v1) : __float_as_uint(v1);
         }
+    }
+};
+template <int TM, bool RND, class F>
+__device__ __forceinline__ AFn<TM, RND, F> afn(F f, int m0, int g, int t) { return AFn<TM, RND, F>{f, m0, g, t}; }
+template <int TN, bool RND, class F>
+__device__ __forceinline__ BFn<TN, RND, F> bfn(F f, int n0, int g, int t) { return BFn<TN, RND, F>{f, n0, g, t}; }
+
+// acc += A B over k in [k0, k1) with fragment loaders
+template <int TM, int TN, class LA, class LB>
+__device__ __forceinline__ void mma_frag(float (&acc)[TM][TN][4], int k0, int k1, const LA &la, const LB &lb) {
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 8) {
+        uint32_t a[TM][4], b[TN][2];
+        la(a, k);
+        lb(b, k);
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int j = 0; j < TN; ++j) mma_tf32(acc[i][j], a[i], b[j]);
     }
 }
+
 // fe(row, col, v[col], v[col + 1]) for every accumulator pair of the tile (col even)
 template <int TM, int TN, class FE>
 __device__ __forceinline__ void tile_out(const float (&acc)[TM][TN][4], int m0, int n0, int g, int t, FE fe) {
@@ -101,21 +190,6 @@ __device__ __forceinline__ void tile_zero(float (&acc)[TM][TN][4]) {
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
 }
-// C (M x N) = sum over k in [0, K) of A B, the 16 TM x 8 TN output tiles dealt to the warps in turn.
-template <int M, int N, int TM, int TN, int NW, class FA, class FB, class FE>
-__device__ __forceinline__ void cta_gemm(int K, FA fa, FB fb, FE fe, int warp, int lane) {
-    constexpr int TNS = N / (8 * TN), TMS = M / (16 * TM);
-    static_assert(TNS * 8 * TN == N && TMS * 16 * TM == M, "tiles cover the product");
-    const int g = lane >> 2, t = lane & 3;
-    for (int tile = warp; tile < TMS * TNS; tile += NW) {
-        const int m0 = (tile / TNS) * 16 * TM, n0 = (tile % TNS) * 8 * TN;
-        float acc[TM][TN][4];
-        tile_zero(acc);
-        mma_tile<TM, TN>(acc, m0, n0, 0, K, fa, fb, g, t);
-        tile_out<TM, TN>(acc, m0, n0, g, t, fe);
-    }
-}
-
 __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src_smem, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src_smem),
                  "r"(bytes)
@@ -336,7 +410,7 @@ __global__ __launch_bounds__(PN_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
                 const float p0v = (i > b || c <= r) ? pp[2 * hh] : 0.f;
                 const float p1v = (i > b || c + 1 <= r) ? pp[2 * hh + 1] : 0.f;
                 st2(sKK + toff<CH>(r, c), k0v, k1v);
-                st2(sP + toff<CH>(r, c), p0v, p1v);
+                st2(sP + toff<CH>(r, c), tf32_rn(p0v), tf32_rn(p1v));   // P: a tensor-core operand only
             }
         }
         // the six blocks above the diagonal are zero
@@ -362,36 +436,44 @@ __global__ __launch_bounds__(PN_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
         invert_unit_lower64<PN_THREADS>(sA, sT, sX, tid, warp, lane);
         for (int idx = tid; idx < CH * CH; idx += PN_THREADS) {
             const int r = idx >> 6, jj = idx & 63;
-            rec[BR_T / 4 + toff<CH>(r, jj)] = sT[r * AS + jj];
+            rec[BR_T / 4 + toff<CH>(r, jj)] = tf32_rn(sT[r * AS + jj]);
         }
         if (tid < KD) rec[BR_D / 4 + tid] = sD[tid];
         if (tid < CH) rec[BR_BETA / 4 + tid] = sBeta[tid];
-        // ---- W = T (beta Kg) -> shared (for N) and the record; Kd = Kh e^(Gam_C - Gam)
-        cta_gemm<CH, KD, 1, 4, PN_WARPS>(
-            CH, [&](int r, int jj) { return sT[r * AS + jj]; },
-            [&](int jj, int c) { return sBeta[jj] * sKh[toff<KD>(jj, c)] * ex2n(sG[toff<KD>(jj, c)]); },
-            [&](int r, int c, float v0, float v1) {
-                st2(sW + toff<KD>(r, c), v0, v1);
-                st2(rec + BR_W / 4 + toff<KD>(r, c), v0, v1);
-            },
-            warp, lane);
+        // ---- W = T (beta Kg) -> shared (for N) and the record; Kd = Kh e^(Gam_C - Gam).  W, Kd, N,
+        // P and T are tensor-core operands only wherever they are read: stored as tf32 numbers
+        const int m0 = 16 * (warp >> 2), n0 = 32 * (warp & 3);   // this warp's 16 x 32 tile of 64 x 128
+        {
+            float acc[1][4][4];
+            tile_zero(acc);
+            mma_frag(acc, 0, CH, AKc<0, 1, true>(sT, m0, lane),
+                     bfn<4, true>([&](int jj, int c) { return sBeta[jj] * sKh[toff<KD>(jj, c)] * ex2n(sG[toff<KD>(jj, c)]); },
+                                  n0, g, t));
+            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int c, float v0, float v1) {
+                st2(sW + toff<KD>(r, c), tf32_rn(v0), tf32_rn(v1));
+                st2(rec + BR_W / 4 + toff<KD>(r, c), tf32_rn(v0), tf32_rn(v1));
+            });
+        }
         for (int idx = tid; idx < CH * KD / 4; idx += PN_THREADS) {
             const int r = idx >> 5, c = 4 * (idx & 31), o = toff<KD>(r, c);
             const float4 kh = *reinterpret_cast<const float4 *>(sKh + o), gm = *reinterpret_cast<const float4 *>(sG + o);
             const float4 gc = *reinterpret_cast<const float4 *>(sG + toff<KD>(CH - 1, c));
             *reinterpret_cast<float4 *>(rec + BR_KD / 4 + o) =
-                make_float4(kh.x * ex2n(gc.x - gm.x), kh.y * ex2n(gc.y - gm.y), kh.z * ex2n(gc.z - gm.z),
-                            kh.w * ex2n(gc.w - gm.w));
+                make_float4(tf32_rn(kh.x * ex2n(gc.x - gm.x)), tf32_rn(kh.y * ex2n(gc.y - gm.y)),
+                            tf32_rn(kh.z * ex2n(gc.z - gm.z)), tf32_rn(kh.w * ex2n(gc.w - gm.w)));
         }
         __syncthreads();
         // ---- N = Qt e^Gam - P W
-        cta_gemm<CH, KD, 1, 4, PN_WARPS>(
-            CH, [&](int r, int jj) { return sP[toff<CH>(r, jj)]; }, [&](int jj, int c) { return sW[toff<KD>(jj, c)]; },
-            [&](int r, int c, float v0, float v1) {
+        {
+            float acc[1][4][4];
+            tile_zero(acc);
+            mma_frag(acc, 0, CH, AKc<CH, 1, false>(sP, m0, lane),
+                     bfn<4, false>([&](int jj, int c) { return sW[toff<KD>(jj, c)]; }, n0, g, t));
+            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int c, float v0, float v1) {
                 const int o = toff<KD>(r, c);
-                st2(rec + BR_N / 4 + o, sQt[o] * ex2n(sG[o]) - v0, sQt[o + 1] * ex2n(sG[o + 1]) - v1);
-            },
-            warp, lane);
+                st2(rec + BR_N / 4 + o, tf32_rn(sQt[o] * ex2n(sG[o]) - v0), tf32_rn(sQt[o + 1] * ex2n(sG[o + 1]) - v1));
+            });
+        }
         __syncthreads();
         // ---- V (fp32) over Qt, then U = T (beta V) as two 64-column halves
         for (int idx = tid; idx < CH * KD / 8; idx += PN_THREADS) {
@@ -406,13 +488,15 @@ __global__ __launch_bounds__(PN_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
             *reinterpret_cast<float4 *>(sV + toff<KD>(r, c + 4)) = hi;
         }
         __syncthreads();
-        cta_gemm<CH, KD, 1, 4, PN_WARPS>(
-            CH, [&](int r, int jj) { return sT[r * AS + jj]; },
-            [&](int jj, int c) { return sBeta[jj] * sV[toff<KD>(jj, c)]; },
-            [&](int r, int c, float v0, float v1) {
+        {
+            float acc[1][4][4];
+            tile_zero(acc);
+            mma_frag(acc, 0, CH, AKc<0, 1, true>(sT, m0, lane),
+                     bfn<4, true>([&](int jj, int c) { return sBeta[jj] * sV[toff<KD>(jj, c)]; }, n0, g, t));
+            tile_out<1, 4>(acc, m0, n0, g, t, [&](int r, int c, float v0, float v1) {
                 st2(rec + BR_U / 4 + (c >> 6) * (CH * CH) + toff<CH>(r, c & 63), v0, v1);
-            },
-            warp, lane);
+            });
+        }
     }
 }
 
@@ -530,19 +614,23 @@ __global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
             bulk_s2g(outbase + item_of(s) * (ST_BYTES / 4) + vb * (CH * KD), sbase + Cfg::X, 32768);
             bulk_commit();
         }
-        // ---- E (64 v x 64 r) = X op1^T, then Z
-        cta_gemm<CH, CH, 1, 4, CN_WARPS>(
-            KD, [&](int v, int k) { return sX[toff<KD>(v, k)]; }, [&](int k, int r) { return op1[toff<KD>(r, k)]; },
-            [&](int v, int r, float e0, float e1) {
+        // ---- E (64 v x 64 r) = X op1^T, then Z (a tensor-core operand only: stored as tf32 numbers)
+        {
+            static_assert(CN_WARPS == 8, "eight 16 x 32 tiles of E");
+            const int m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1);
+            float acc[1][4][4];
+            tile_zero(acc);
+            mma_frag(acc, 0, KD, AKc<KD, 1, true>(sX, m0, lane), BKc<KD, 4, false>(op1, n0, lane));
+            tile_out<1, 4>(acc, m0, n0, g, t, [&](int v, int r, float e0, float e1) {
                 float z0 = -e0, z1 = -e1;
                 if (!BWD) {
                     const float *u = reinterpret_cast<const float *>(aux + 512);   // U block [r][v]
                     z0 += u[toff<CH>(r, v)];
                     z1 += u[toff<CH>(r + 1, v)];
                 }
-                st2(sZ + toff<CH>(v, r), z0, z1);
-            },
-            warp, lane);
+                st2(sZ + toff<CH>(v, r), tf32_rn(z0), tf32_rn(z1));
+            });
+        }
         __syncthreads();   // Z complete; op1 consumed
         if (warp == 0 && s + 1 < n) issue(s + 1);
         // ---- X <- X Diag(D) + Z op2 (+ dO^T N)
@@ -560,17 +648,18 @@ __global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
                     acc[i][j][2] = sX[toff<KD>(r + 8, cc)] * d0;
                     acc[i][j][3] = sX[toff<KD>(r + 8, cc + 1)] * d1;
                 }
-            mma_tile<2, 4>(acc, m0, n0, 0, CH, [&](int v, int r) { return sZ[toff<CH>(v, r)]; },
-                           [&](int r, int cc) { return op2[toff<KD>(r, cc)]; }, g, t);
+            mma_frag(acc, 0, CH, AKc<CH, 2, false>(sZ, m0, lane),
+                     bfn<4, false>([&](int r, int cc) { return op2[toff<KD>(r, cc)]; }, n0, g, t));
             if (BWD) {
                 const unsigned char *dorow = aux + 512;
-                mma_tile<2, 4>(
-                    acc, m0, n0, 0, CH,
-                    [&](int v, int r) {
-                        return r < len ? bf16_to_f(*reinterpret_cast<const uint16_t *>(dorow + r * Cfg::DO_STRIDE + 2 * v))
-                                       : 0.f;
-                    },
-                    [&](int r, int cc) { return op3[toff<KD>(r, cc)]; }, g, t);
+                mma_frag(acc, 0, CH,
+                         afn<2, false>(
+                             [&](int v, int r) {
+                                 return r < len ? bf16_to_f(*reinterpret_cast<const uint16_t *>(dorow + r * Cfg::DO_STRIDE + 2 * v))
+                                                : 0.f;
+                             },
+                             m0, g, t),
+                         bfn<4, false>([&](int r, int cc) { return op3[toff<KD>(r, cc)]; }, n0, g, t));
             }
             if (tid == 0) bulk_wait_read_all();   // the store of X has read it
             __syncthreads();                      // every warp is done reading X, Z and the operands
@@ -683,42 +772,42 @@ __global__ __launch_bounds__(GN_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
                 ok = false;
                 break;
             }
-            // ---- Delta (in place of U) and dDelta
+            // ---- Delta (in place of U) and dDelta, both tensor-core operands only from here on
+            // (stored as tf32 numbers); W, Kd, P, T arrive as tf32 numbers, S0, dS as fp32
             {
                 float acc[1][2][4];
                 tile_zero(acc);
-                mma_tile<1, 2>(acc, m0, sn0, 0, KD, [&](int r, int k) { return sW[toff<KD>(r, k)]; },
-                               [&](int k, int v) { return sS0[toff<KD>(v, k)]; }, g, t);
+                mma_frag(acc, 0, KD, AKc<KD, 1, false>(sW, m0, lane), BKc<KD, 2, true>(sS0, sn0, lane));
                 float dd[1][2][4];
                 tile_zero(dd);
-                mma_tile<1, 2>(dd, m0, sn0, 0, CH, [&](int r, int j) { return sP[toff<CH>(j, r)]; },
-                               [&](int j, int v) { return sDO[toff<CH>(j, v)]; }, g, t);
-                mma_tile<1, 2>(dd, m0, sn0, 0, KD, [&](int r, int k) { return sKd[toff<KD>(r, k)]; },
-                               [&](int k, int v) { return sDS[toff<KD>(v, k)]; }, g, t);
+                mma_frag(dd, 0, CH, afn<1, false>([&](int r, int j) { return sP[toff<CH>(j, r)]; }, m0, g, t),
+                         bfn<2, false>([&](int j, int v) { return sDO[toff<CH>(j, v)]; }, sn0, g, t));
+                mma_frag(dd, 0, KD, AKc<KD, 1, false>(sKd, m0, lane), BKc<KD, 2, true>(sDS, sn0, lane));
                 tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int v, float e0, float e1) {
                     const int o = toff<CH>(r, v);
-                    st2(sU + o, sU[o] - e0, sU[o + 1] - e1);
+                    st2(sU + o, tf32_rn(sU[o] - e0), tf32_rn(sU[o + 1] - e1));
                 });
-                tile_out<1, 2>(dd, m0, sn0, g, t, [&](int r, int v, float v0, float v1) { st2(sDD + toff<CH>(r, v), v0, v1); });
+                tile_out<1, 2>(dd, m0, sn0, g, t,
+                               [&](int r, int v, float v0, float v1) { st2(sDD + toff<CH>(r, v), tf32_rn(v0), tf32_rn(v1)); });
             }
             __syncthreads();
             // ---- the sums over this half's value columns
-            mma_tile<1, 4>(akd, m0, bn0, 0, CH, [&](int r, int v) { return sU[toff<CH>(r, v)]; },
-                           [&](int v, int k) { return sDS[toff<KD>(v, k)]; }, g, t);
-            mma_tile<1, 4>(aqg, m0, bn0, 0, CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; },
-                           [&](int v, int k) { return sS0[toff<KD>(v, k)]; }, g, t);
-            mma_tile<1, 4>(aw, m0, bn0, 0, CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
-                           [&](int v, int k) { return sS0[toff<KD>(v, k)]; }, g, t);
-            mma_tile<1, 2>(ap, m0, sn0, 0, CH, [&](int r, int v) { return sDO[toff<CH>(r, v)]; },
-                           [&](int v, int j) { return sU[toff<CH>(j, v)]; }, g, t);
-            mma_tile<1, 2>(at, m0, sn0, 0, CH, [&](int r, int v) { return sDD[toff<CH>(r, v)]; },
-                           [&](int v, int j) { return sBeta[j] * sV[toff<CH>(j, v)]; }, g, t);
+            {
+                const auto lDelta = AKc<CH, 1, false>(sU, m0, lane), lDO = AKc<CH, 1, false>(sDO, m0, lane);
+                const auto lDD = AKc<CH, 1, false>(sDD, m0, lane);
+                mma_frag(akd, 0, CH, lDelta, bfn<4, true>([&](int v, int k) { return sDS[toff<KD>(v, k)]; }, bn0, g, t));
+                const auto lS0 = bfn<4, true>([&](int v, int k) { return sS0[toff<KD>(v, k)]; }, bn0, g, t);
+                mma_frag(aqg, 0, CH, lDO, lS0);
+                mma_frag(aw, 0, CH, lDD, lS0);
+                mma_frag(ap, 0, CH, lDO, BKc<CH, 2, false>(sU, sn0, lane));
+                mma_frag(at, 0, CH, lDD, bfn<2, true>([&](int v, int j) { return sBeta[j] * sV[toff<CH>(j, v)]; }, sn0, g, t));
+            }
             // dBV = T^T dDelta: dv and dbeta's V term
             {
                 float acc[1][2][4];
                 tile_zero(acc);
-                mma_tile<1, 2>(acc, m0, sn0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
-                               [&](int j, int v) { return sDD[toff<CH>(j, v)]; }, g, t);
+                mma_frag(acc, 0, CH, afn<1, false>([&](int r, int j) { return sT[toff<CH>(j, r)]; }, m0, g, t),
+                         bfn<2, false>([&](int j, int v) { return sDD[toff<CH>(j, v)]; }, sn0, g, t));
                 float rs[2] = {0.f, 0.f};
                 tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int v, float v0, float v1) {
                     const int o = toff<CH>(r, v);
@@ -750,7 +839,9 @@ __global__ __launch_bounds__(GN_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
         float *pDT = reinterpret_cast<float *>(part + CP_DT);
         tile_out<1, 4>(akd, m0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDKD + toff<KD>(r, k), v0, v1); });
         tile_out<1, 4>(aqg, m0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDQG + toff<KD>(r, k), v0, v1); });
-        tile_out<1, 4>(aw, m0, bn0, g, t, [&](int r, int k, float v0, float v1) { st2(pDW + toff<KD>(r, k), -v0, -v1); });
+        // dW: a tensor-core operand only where it is read (stored as tf32 numbers)
+        tile_out<1, 4>(aw, m0, bn0, g, t,
+                       [&](int r, int k, float v0, float v1) { st2(pDW + toff<KD>(r, k), tf32_rn(-v0), tf32_rn(-v1)); });
         tile_out<1, 2>(ap, m0, sn0, g, t, [&](int r, int j, float v0, float v1) {
             st2(pDP + toff<CH>(r, j), j <= r ? v0 : 0.f, j + 1 <= r ? v1 : 0.f);
         });
@@ -838,16 +929,17 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             if (tid == 0) set_status(KDA_ERR_DEVICE_TIMEOUT);
             break;
         }
-        // ---- dT += dW (beta Kg)^T
+        // ---- dT += dW (beta Kg)^T  (dW, T arrive as tf32 numbers; dT, X and M, tensor-core
+        // operands only, are stored as tf32 numbers)
         {
             float acc[1][2][4];
             tile_zero(acc);
-            mma_tile<1, 2>(acc, m0, sn0, 0, KD, [&](int r, int k) { return sDW[toff<KD>(r, k)]; },
-                           [&](int k, int j) { return sBeta[j] * sKh[toff<KD>(j, k)] * ex2n(sG[toff<KD>(j, k)]); }, g,
-                           t);
+            mma_frag(acc, 0, KD, AKc<KD, 1, false>(sDW, m0, lane),
+                     bfn<2, true>([&](int k, int j) { return sBeta[j] * sKh[toff<KD>(j, k)] * ex2n(sG[toff<KD>(j, k)]); },
+                                  sn0, g, t));
             tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int j, float v0, float v1) {
                 const int o = toff<CH>(r, j);
-                st2(sDT + o, sDT[o] + v0, sDT[o + 1] + v1);
+                st2(sDT + o, tf32_rn(sDT[o] + v0), tf32_rn(sDT[o + 1] + v1));
             });
         }
         __syncthreads();
@@ -855,24 +947,24 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
         {
             float acc[1][2][4];
             tile_zero(acc);
-            mma_tile<1, 2>(acc, m0, sn0, 0, CH, [&](int r, int j) { return sDT[toff<CH>(r, j)]; },
-                           [&](int j, int i) { return sT[toff<CH>(i, j)]; }, g, t);
-            tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int i, float v0, float v1) { st2(sX + toff<CH>(r, i), v0, v1); });
+            mma_frag(acc, 0, CH, AKc<CH, 1, false>(sDT, m0, lane), BKc<CH, 2, false>(sT, sn0, lane));
+            tile_out<1, 2>(acc, m0, sn0, g, t,
+                           [&](int r, int i, float v0, float v1) { st2(sX + toff<CH>(r, i), tf32_rn(v0), tf32_rn(v1)); });
         }
         __syncthreads();
         // ---- dA = strict_lower(-T^T X); dbeta row sums of dA KK; M = beta dA over dT
         {
             float acc[1][2][4];
             tile_zero(acc);
-            mma_tile<1, 2>(acc, m0, sn0, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
-                           [&](int j, int i) { return sX[toff<CH>(j, i)]; }, g, t);
+            mma_frag(acc, 0, CH, afn<1, false>([&](int r, int j) { return sT[toff<CH>(j, r)]; }, m0, g, t),
+                     bfn<2, false>([&](int j, int i) { return sX[toff<CH>(j, i)]; }, sn0, g, t));
             float rs[2] = {0.f, 0.f};
             tile_out<1, 2>(acc, m0, sn0, g, t, [&](int r, int i, float v0, float v1) {
                 const int o = toff<CH>(r, i);
                 const float d0 = i < r ? -v0 : 0.f, d1 = i + 1 < r ? -v1 : 0.f;
                 rs[(r - m0) >> 3] += d0 * sKK[o] + d1 * sKK[o + 1];
                 const float be = sBeta[r];
-                st2(sDT + o, be * d0, be * d1);
+                st2(sDT + o, tf32_rn(be * d0), tf32_rn(be * d1));
             });
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -890,8 +982,8 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
         {
             float bw[4][1][4];
             tile_zero(bw);
-            mma_tile<4, 1>(bw, 0, cw, 0, CH, [&](int r, int j) { return sT[toff<CH>(j, r)]; },
-                           [&](int j, int c) { return sDW[toff<KD>(j, c)]; }, g, t);
+            mma_frag(bw, 0, CH, afn<4, false>([&](int r, int j) { return sT[toff<CH>(j, r)]; }, 0, g, t),
+                     bfn<1, false>([&](int j, int c) { return sDW[toff<KD>(j, c)]; }, cw, g, t));
             float rs[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) rs[e] = 0.f;
@@ -928,7 +1020,7 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             // (cw + 2t, cw + 2t + 1)
             const PairRef fb = pair_ref(sG, i, b, cw + g);
             const PairRef fc[2] = {pair_ref(sG, i, b, cw + 2 * t), pair_ref(sG, i, b, cw + 2 * t + 1)};
-            auto mval = [&](int r, int j) { return sDT[toff<CH>(r, j)]; };   // strictly lower already
+            auto mval = [&](int r, int j) { return sDT[toff<CH>(r, j)]; };   // strictly lower, tf32 numbers
             auto pval = [&](int r, int j) { return (!dg_ || j < r) ? sDP[toff<CH>(r, j)] : 0.f; };
             // row side: MH = M_ib Hk, PH = dPs_ib Hk (rows of block i)
             float mh[4] = {0.f, 0.f, 0.f, 0.f}, ph[4] = {0.f, 0.f, 0.f, 0.f}, y[4] = {0.f, 0.f, 0.f, 0.f};
@@ -937,10 +1029,10 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             for (int ks = 0; ks < 2; ++ks) {
                 const int r0 = 16 * i + g, j0 = 16 * b + 8 * ks + t;
                 uint32_t am[4], ap[4], bh[2];
-                am[0] = tf32_rn_bits(mval(r0, j0));
-                am[1] = tf32_rn_bits(mval(r0 + 8, j0));
-                am[2] = tf32_rn_bits(mval(r0, j0 + 4));
-                am[3] = tf32_rn_bits(mval(r0 + 8, j0 + 4));
+                am[0] = __float_as_uint(mval(r0, j0));
+                am[1] = __float_as_uint(mval(r0 + 8, j0));
+                am[2] = __float_as_uint(mval(r0, j0 + 4));
+                am[3] = __float_as_uint(mval(r0 + 8, j0 + 4));
                 ap[0] = tf32_rn_bits(pval(r0, j0));
                 ap[1] = tf32_rn_bits(pval(r0 + 8, j0));
                 ap[2] = tf32_rn_bits(pval(r0, j0 + 4));
@@ -955,10 +1047,10 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             for (int ks = 0; ks < 2; ++ks) {
                 const int j0 = 16 * b + g, r0 = 16 * i + 8 * ks + t;
                 uint32_t am[4], ap[4], bk[2], bq[2];
-                am[0] = tf32_rn_bits(mval(r0, j0));
-                am[1] = tf32_rn_bits(mval(r0, j0 + 8));
-                am[2] = tf32_rn_bits(mval(r0 + 4, j0));
-                am[3] = tf32_rn_bits(mval(r0 + 4, j0 + 8));
+                am[0] = __float_as_uint(mval(r0, j0));
+                am[1] = __float_as_uint(mval(r0, j0 + 8));
+                am[2] = __float_as_uint(mval(r0 + 4, j0));
+                am[3] = __float_as_uint(mval(r0 + 4, j0 + 8));
                 ap[0] = tf32_rn_bits(pval(r0, j0));
                 ap[1] = tf32_rn_bits(pval(r0, j0 + 8));
                 ap[2] = tf32_rn_bits(pval(r0 + 4, j0));
