@@ -112,34 +112,40 @@ def test_bwd_longer_sequence():
     _check(KI.make_inputs(1, 1024, 1, 1, seed=705, with_state=True), seed=6)
 
 
-def test_bwd_full_size_dense_sampled_heads():
-    """The benchmark's dense workload (B=2, T=16384, H=32) at full size; the fp64
-    reverse-pass oracle (checkpointed, pinned to autograd) recomputes every
-    gradient of q/k heads 0 and 31 (each chain is independent)."""
+@pytest.mark.parametrize("name,qk_heads", [("dense", [0, 31]), ("varlen", [5]), ("gva", [3])])
+def test_bwd_full_size_sampled_heads(name, qk_heads):
+    """The workloads at full size (dense B=2 T=16384 H=32, the skewed 20-sequence varlen
+    packing, grouped value heads 16/64 over 28672+4096 tokens); the fp64 reverse-pass oracle
+    (checkpointed, pinned to autograd) recomputes every gradient of a few q/k heads and the
+    value heads that read them (each chain is independent)."""
     from gated_delta_rule_40_gb300 import kda
     from kda_testutil import head_subset
-    inp = KI.workload("dense")
+    inp = KI.workload(name)
     do, dht = _grads(inp, 7)
     dev = lambda t: None if t is None else t.cuda()  # noqa: E731
     got = kda.kda_bwd(dev(inp.q), dev(inp.k), dev(inp.v), dev(inp.graw), dev(inp.b), dev(inp.A_log), inp.scale,
-                      dev(do), initial_state=dev(inp.initial_state), dht=dev(dht))
+                      dev(do), initial_state=dev(inp.initial_state), cu_seqlens=dev(inp.cu_seqlens), dht=dev(dht))
     torch.cuda.synchronize()
-    for hq in (0, 31):
-        sub = head_subset(inp, [hq])
-        ref = OB.bwd_recurrent_inputs(sub, do[:, :, hq:hq + 1].contiguous(), dht[:, hq:hq + 1].contiguous())
-        sel = {"dq": got["dq"][:, :, hq:hq + 1], "dk": got["dk"][:, :, hq:hq + 1], "dv": got["dv"][:, :, hq:hq + 1],
-               "dgraw": got["dgraw"][:, :, hq:hq + 1], "db": got["db"][:, :, hq:hq + 1],
-               "dA_log": got["dA_log"][hq:hq + 1], "dh0": got["dh0"][:, hq:hq + 1]}
-        _check_dalog(sub, sel["dA_log"].double().cpu().numpy(), {k_: v_.numpy() for k_, v_ in ref.items()},
-                     f"head {hq} ")
-        for name, a in sel.items():
-            if name == "dA_log":
-                continue
-            a = a.double().cpu().numpy()
-            r = ref[name].numpy()
-            e = rel_l2(a, r)
-            m = np.abs(a - r).max() / max(np.abs(r).max(), 1e-30)
-            assert e <= REL and m <= MAX_FRAC, f"head {hq} {name}: rel-L2 {e:.2e}, max {m:.2e}"
+    G = inp.H_v // inp.H_qk
+    sub = head_subset(inp, qk_heads)
+    vh = torch.tensor(sub.meta["v_heads"])
+    qh = torch.tensor(qk_heads)
+    ref = OB.bwd_recurrent_inputs(sub, do.index_select(2, vh).contiguous(),
+                                  None if dht is None else dht.index_select(1, vh).contiguous())
+    sel = {"dq": got["dq"].index_select(2, qh.cuda()), "dk": got["dk"].index_select(2, qh.cuda()),
+           "dv": got["dv"].index_select(2, vh.cuda()), "dgraw": got["dgraw"].index_select(2, vh.cuda()),
+           "db": got["db"].index_select(2, vh.cuda()), "dA_log": got["dA_log"].index_select(0, vh.cuda()),
+           "dh0": got["dh0"].index_select(1, vh.cuda())}
+    refn = {k_: v_.numpy() for k_, v_ in ref.items()}
+    _check_dalog(sub, sel["dA_log"].double().cpu().numpy(), refn, f"{name} ")
+    for n_, a in sel.items():
+        if n_ == "dA_log":
+            continue
+        a = a.double().cpu().numpy()
+        r = refn[n_]
+        e = rel_l2(a, r)
+        m = np.abs(a - r).max() / max(np.abs(r).max(), 1e-30)
+        assert e <= REL and m <= MAX_FRAC, f"{name} {n_} (group {G}): rel-L2 {e:.2e}, max {m:.2e}"
 
 
 def test_bwd_large_value_head_group():
