@@ -222,8 +222,9 @@ struct BwdcParams {
     unsigned char *rec;     // [item] BR_BYTES
     float *S0, *dSC;        // [item] ST_BYTES: state entering / state gradient leaving each chunk
     unsigned char *part;    // [item] CP_BYTES
-    float *dqt, *dkh, *dg;  // [token][H_v][128]: gradients of Qt, Kh, g
-    float *dbeta;           // [token][H_v]
+    float *dqt, *dkh;       // [token][H_v][128]: gradients of Qt, Kh
+    float *dgraw, *db;      // outputs [token][H_v][128], [token][H_v]
+    float *dal;             // [item]: the item's share of dA_log
     float *dv, *dh0;
 };
 
@@ -1119,7 +1120,18 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             }
         __syncthreads();
         // ---- dg = suffix sums of dGam + dGam_C + exclusive prefix sums of dKd Kd (four threads
-        // per channel over 16-row segments, the segment totals passed through shared memory); dbeta
+        // per channel over 16-row segments, the segment totals passed through shared memory), then
+        // the gate's and the sigmoid's Jacobians: dgraw = dg (-a) sigmoid(graw), the item's share of
+        // dA_log = sum dg g (g = -a softplus(graw)), db = dbeta beta (1 - beta)
+        // this thread's 16 gate pre-activations, requested before the scans so that their latency
+        // overlaps them
+        float gr16[16];
+        {
+            const int c = tid & (KD - 1), r0 = 16 * (tid >> 7);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                gr16[i] = r0 + i < len ? bf16_to_f(p.graw[((size_t)(cd.tok + r0 + i) * p.H_v + h) * KD + c]) : 0.f;
+        }
         {
             const int c = tid & (KD - 1), seg = tid >> 7, r0 = 16 * seg;
             float pre = 0.f;
@@ -1144,42 +1156,57 @@ __global__ __launch_bounds__(KN_THREADS, 1) void bwdc_gradk_kernel(const BwdcPar
             float add = sDGC[c];
             for (int s2 = 0; s2 < seg; ++s2) add += sX[s2 * KD + c];
             for (int s2 = seg + 1; s2 < 4; ++s2) add += sX[4 * KD + s2 * KD + c];
-            const int r1 = min(r0 + 16, len);
-            for (int r = r0; r < r1; ++r) {
-                const int o = toff<KD>(r, c);
-                p.dg[((size_t)(cd.tok + r) * p.H_v + h) * KD + c] = sDW[o] + sQt[o] + add;
+            float dal = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = r0 + i;
+                if (r < len) {
+                    const int o = toff<KD>(r, c);
+                    const float dgv = sDW[o] + sQt[o] + add;
+                    const float gr = gr16[i];
+                    const float sp = softplus_log2(gr) * (1.0f / LOG2E);   // softplus (natural units)
+                    const float sig = 1.0f / (1.0f + __expf(-gr));
+                    p.dgraw[((size_t)(cd.tok + r) * p.H_v + h) * KD + c] = dgv * (-a) * sig;
+                    dal = fmaf(dgv, -a * sp, dal);
+                }
             }
+            dal = warp_sum(dal);
+            if (lane == 0) sX[8 * KD + warp] = dal;
         }
         if (tid < len) {
             float db = sDB[tid] + (sDBa[tid] + sDBa[64 + tid]) + (sDBa[128 + tid] + sDBa[192 + tid]);
 #pragma unroll
             for (int w = 0; w < KN_WARPS; ++w) db += sDBw[w * 64 + tid];
-            p.dbeta[(size_t)(cd.tok + tid) * p.H_v + h] = db;
+            const float be = sBeta[tid];
+            p.db[(size_t)(cd.tok + tid) * p.H_v + h] = db * be * (1.0f - be);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float dal = 0.f;
+            for (int w = 0; w < KN_WARPS; ++w) dal += sX[8 * KD + w];
+            p.dal[item] = dal;
         }
     }
 }
 
 // =====================================================================
-// The prologue's Jacobians, one warp per (query/key head, 16 tokens); lane = channels
+// The norms' Jacobians, one warp per (query/key head, 16 tokens); lane = channels
 // 4 lane .. 4 lane + 3:
 //   dq = scale r_q (dqt_sum - r_q^2 q (q . dqt_sum)),  r_q = 1 / sqrt(|q|^2 + eps)   (dk alike, scale 1)
-//   dgraw = dg (-a) sigmoid(graw),  db = dbeta beta (1 - beta)
-// with dqt_sum / dkh_sum the sums over the value heads of the group; the warp's share of
-// dA_log = sum dg g per value head goes to dal[range][h], which bwdc_dalog_kernel adds up in a
-// fixed order (no atomics: the gradients are reproducible bit for bit).
+// with dqt_sum / dkh_sum the sums over the value heads of the group (the gate's and the
+// sigmoid's Jacobians run at the end of bwdc_gradk_kernel).
 // =====================================================================
 constexpr int BP_WARPS = 8;
 constexpr int BP_TOKENS = 16;   // tokens per warp
 
 __global__ __launch_bounds__(BP_WARPS * 32, 2) void bwdc_jacobian_kernel(const BwdcParams p, float *dq, float *dk,
-                                                                      float *dgraw, float *db, float *dal,
-                                                                      long long tokens) {
+                                                                         long long tokens) {
     const int lane = threadIdx.x & 31;
     const long long gw = (long long)blockIdx.x * BP_WARPS + (threadIdx.x >> 5);
     const long long n_ranges = (tokens + BP_TOKENS - 1) / BP_TOKENS;
     if (gw >= n_ranges * p.H_qk) return;
     const int hq = (int)(gw % p.H_qk);
-    const long long range = gw / p.H_qk, t0 = range * BP_TOKENS, t1 = min(t0 + BP_TOKENS, tokens);
+    const long long t0 = (gw / p.H_qk) * BP_TOKENS, t1 = min(t0 + BP_TOKENS, tokens);
     const int group = p.H_v / p.H_qk;
     constexpr int U = 4;   // tokens in flight: their loads are issued before any of them is used
     for (long long tb = t0; tb < t1; tb += U) {
@@ -1234,65 +1261,17 @@ __global__ __launch_bounds__(BP_WARPS * 32, 2) void bwdc_jacobian_kernel(const B
             }
         }
     }
-#pragma unroll 1
-    for (int g = 0; g < group; ++g) {
-        const int h = hq * group + g;
-        const float a = ex2n(p.A_log[h]);
-        float acc = 0.f;
-        for (long long tb = t0; tb < t1; tb += U) {
-            uint2 gw[U];
-            float4 dg4[U];
-            float bb[U], dbt[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const long long tok = tb + u;
-                gw[u] = make_uint2(0u, 0u);
-                dg4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                bb[u] = dbt[u] = 0.f;
-                if (tok < t1) {
-                    const size_t vo = ((size_t)tok * p.H_v + h) * KD + 4 * lane;
-                    gw[u] = *reinterpret_cast<const uint2 *>(p.graw + vo);
-                    dg4[u] = *reinterpret_cast<const float4 *>(p.dg + vo);
-                    if (lane == 0) {
-                        bb[u] = bf16_to_f(p.b[(size_t)tok * p.H_v + h]);
-                        dbt[u] = p.dbeta[(size_t)tok * p.H_v + h];
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const long long tok = tb + u;
-                if (tok >= t1) break;
-                const size_t vo = ((size_t)tok * p.H_v + h) * KD + 4 * lane;
-                const float gr[4] = {bf16_lo(gw[u].x), bf16_hi(gw[u].x), bf16_lo(gw[u].y), bf16_hi(gw[u].y)};
-                const float dgv[4] = {dg4[u].x, dg4[u].y, dg4[u].z, dg4[u].w};
-                float out[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float sp = softplus_log2(gr[i]) * (1.0f / LOG2E);   // softplus (natural units)
-                    const float sig = 1.0f / (1.0f + __expf(-gr[i]));
-                    out[i] = dgv[i] * (-a) * sig;
-                    acc = fmaf(dgv[i], -a * sp, acc);
-                }
-                *reinterpret_cast<float4 *>(dgraw + vo) = make_float4(out[0], out[1], out[2], out[3]);
-                if (lane == 0) {
-                    const float beta = 1.0f / (1.0f + __expf(-bb[u]));
-                    db[(size_t)tok * p.H_v + h] = dbt[u] * beta * (1.0f - beta);
-                }
-            }
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) dal[range * p.H_v + h] = acc;
-    }
 }
 
-// dA_log[h] = sum over the token ranges of dal[range][h], one CTA per head, in a fixed order.
-__global__ __launch_bounds__(256) void bwdc_dalog_kernel(const float *dal, long long n_ranges, int H_v,
-                                                          float *dA_log) {
+// dA_log[h] = sum over the chunks of the items' shares dal[chunk][h], one CTA per head, in a
+// fixed order (no atomics: the gradients are reproducible bit for bit).
+__global__ __launch_bounds__(256) void bwdc_dalog_kernel(const BwdcParams p, float *dA_log) {
     __shared__ float red[256];
+    if (p.hdr[1] == 0) return;
     const int h = blockIdx.x, tid = threadIdx.x;
+    const long long n = p.hdr[0];
     float acc = 0.f;
-    for (long long r = tid; r < n_ranges; r += 256) acc += dal[r * H_v + h];
+    for (long long r = tid; r < n; r += 256) acc += p.dal[r * p.H_v + h];
     red[tid] = acc;
     __syncthreads();
     for (int o = 128; o > 0; o >>= 1) {
@@ -1324,9 +1303,8 @@ size_t bwd_workspace_bytes(int N, int B, int T, int H_v, bool varlen, int /*grid
     off = a256(off + items * ST_BYTES);
     off = a256(off + items * ST_BYTES);
     off = a256(off + items * CP_BYTES);
-    off = a256(off + tk * KD * 4 * 3);   // dqt, dkh, dg
-    off = a256(off + tk * 4);            // dbeta
-    off = a256(off + (size_t)((tokens > 0 ? tokens : 1) + BP_TOKENS - 1) / BP_TOKENS * H_v * 4);   // dA_log parts
+    off = a256(off + tk * KD * 4 * 2);   // dqt, dkh
+    off = a256(off + items * 4);         // dA_log shares
     return off;
 }
 
@@ -1357,13 +1335,12 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     bp.S0 = reinterpret_cast<float *>(take(items * ST_BYTES));
     bp.dSC = reinterpret_cast<float *>(take(items * ST_BYTES));
     bp.part = reinterpret_cast<unsigned char *>(take(items * CP_BYTES));
-    float *t3 = reinterpret_cast<float *>(take(tk * KD * 4 * 3));
-    bp.dqt = t3;
-    bp.dkh = t3 + tk * KD;
-    bp.dg = t3 + 2 * tk * KD;
-    bp.dbeta = reinterpret_cast<float *>(take(tk * 4));
-    const long long n_ranges = (tokens + BP_TOKENS - 1) / BP_TOKENS;
-    float *dal = reinterpret_cast<float *>(take((size_t)((tokens > 0 ? tokens : 1) + BP_TOKENS - 1) / BP_TOKENS * H_v * 4));
+    float *t2 = reinterpret_cast<float *>(take(tk * KD * 4 * 2));
+    bp.dqt = t2;
+    bp.dkh = t2 + tk * KD;
+    bp.dal = reinterpret_cast<float *>(take(items * 4));
+    bp.dgraw = dgraw;
+    bp.db = db;
     bp.q = q; bp.k = k; bp.v = v; bp.graw = graw; bp.b = b; bp.dout = dout;
     bp.A_log = A_log; bp.init = init; bp.dht = dht; bp.scale = scale;
     bp.H_qk = H_qk; bp.H_v = H_v; bp.nseq = nseq;
@@ -1418,10 +1395,10 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     if (tokens > 0) {
         const long long warps = ((tokens + BP_TOKENS - 1) / BP_TOKENS) * H_qk;
         bwdc_jacobian_kernel<<<(unsigned)((warps + BP_WARPS - 1) / BP_WARPS), BP_WARPS * 32, 0, stream>>>(
-            bp, dq, dk, dgraw, db, dal, tokens);
+            bp, dq, dk, tokens);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwdc_dalog_kernel<<<H_v, 256, 0, stream>>>(dal, n_ranges, H_v, dA_log);
+        bwdc_dalog_kernel<<<H_v, 256, 0, stream>>>(bp, dA_log);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_jacobian_kernel", stream);

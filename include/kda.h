@@ -251,7 +251,7 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
  * the state entering each chunk (a forward chain) and the state gradient leaving
  * it (a reverse chain), then the chunks' gradients in parallel.  The workspace
  * holds, per (chunk, value head), those operands, both states and the value-side
- * gradient sums (about 434 KiB), plus 1.5 KiB per token and value head (8.9 GB
+ * gradient sums (about 434 KiB), plus 1 KiB per token and value head (8.4 GB
  * for B=2, T=16384, H_v=32); kda_bwd takes it from cudaMallocAsync on `stream`
  * (a failed allocation returns KDA_ERR_CUDA), kda_bwd_ws from the caller.  Errors
  * as kda_fwd.
