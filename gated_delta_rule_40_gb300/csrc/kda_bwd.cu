@@ -34,7 +34,10 @@
 // nearest, fp32 accumulation) from fp32 tiles in shared memory; the state chains keep the
 // state in fp32 and apply the per-channel decay in fp32 outside the products.
 #include "kda_common.cuh"
+#include <cstring>
+
 #include "kda_invert.cuh"
+#include "kda_tma.cuh"
 
 namespace kda {
 
@@ -516,18 +519,25 @@ template <bool BWD>
 struct ChainCfg {
     static constexpr int OPS = BWD ? 3 : 2;             // ring tiles per chunk
     static constexpr int SLOTS = BWD ? 5 : 4;
-    static constexpr uint32_t DO_STRIDE = 128;          // dO row stride (bytes)
-    static constexpr uint32_t AUX = BWD ? 512 + CH * DO_STRIDE : 512 + CH * CH * 4;   // D, then dO rows or U block
+    // extras per chunk: backward: the chunk's dO block (64 rows x 64 bf16, a TMA box with the
+    // 128-byte swizzle, 1024-byte aligned), then D; forward: D, then U's V block
+    static constexpr uint32_t AUX_D = BWD ? 8192 : 0, AUX_M = BWD ? 0 : 512;
+    static constexpr uint32_t AUX = BWD ? 9216 : 512 + CH * CH * 4;
     static constexpr uint32_t X = 0, Z = 32768, RING = 49152, AUXB = RING + SLOTS * 32768;
-    static constexpr uint32_t BAR = AUXB + 2 * AUX, BYTES = BAR + 8 * (SLOTS + 2);
+    // the backward's barriers sit in the unused tail of its second extras buffer
+    static constexpr uint32_t BAR = BWD ? AUXB + AUX + 8704 : AUXB + 2 * AUX;
+    static constexpr uint32_t BYTES = BWD ? AUXB + 2 * AUX : BAR + 8 * (SLOTS + 2);
 };
-static_assert(ChainCfg<true>::BYTES + 128 <= 232448 && ChainCfg<false>::BYTES + 128 <= 232448, "chain smem");
+static_assert(ChainCfg<true>::BAR + 8 * (ChainCfg<true>::SLOTS + 2) <= ChainCfg<true>::BYTES &&
+              ChainCfg<true>::AUXB % 1024 == 0 && ChainCfg<true>::AUX % 1024 == 0, "chain layout");
+static_assert(ChainCfg<true>::BYTES + 1024 <= 232448 && ChainCfg<false>::BYTES + 1024 <= 232448, "chain smem");
 
 template <bool BWD>
-__global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcParams p) {
+__global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const __grid_constant__ CUtensorMap tdo,
+                                                                     const BwdcParams p) {
     using Cfg = ChainCfg<BWD>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = aligned_smem<128>(smem_raw);
+    unsigned char *sm = aligned_smem<1024>(smem_raw);
     if (p.hdr[1] == 0) return;
     const int vb = blockIdx.x & 1;
     const int h = (blockIdx.x >> 1) % p.H_v;
@@ -558,35 +568,29 @@ __global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
 
     auto chunk_of = [&](int s) { return BWD ? n - 1 - s : s; };
     auto item_of = [&](int s) { return ((size_t)sd.chunk0 + chunk_of(s)) * p.H_v + h; };
-    auto issue = [&](int s) {   // warp 0: the ring tiles and extras of step s
+    auto issue = [&](int s) {   // thread 0: the ring tiles and extras of step s
         const unsigned char *rec = p.rec + item_of(s) * BR_BYTES;
         const uint32_t offs[3] = {BWD ? BR_KD : BR_W, BWD ? BR_W : BR_KD, BR_N};
         const uint32_t ab = bar + 8 * (Cfg::SLOTS + (s & 1)), aux = sbase + Cfg::AUXB + (s & 1) * Cfg::AUX;
-        const int c = chunk_of(s), len = min(CH, sd.len - c * CH), tok0 = sd.tok + c * CH;
-        if (lane == 0) {
 #pragma unroll
-            for (int op = 0; op < Cfg::OPS; ++op) {
-                const int slot = (Cfg::OPS * s + op) % Cfg::SLOTS;
-                mbar_expect_tx(bar + 8 * slot, 32768);
-                bulk_g2s(sbase + Cfg::RING + slot * 32768, rec + offs[op], 32768, bar + 8 * slot);
-            }
-            if (BWD) {
-                mbar_expect_tx(ab, 512 + 128 * len);
-                bulk_g2s(aux, rec + BR_D, 512, ab);
-            } else {
-                mbar_expect_tx(ab, 512 + CH * CH * 4);
-                bulk_g2s(aux, rec + BR_D, 512, ab);
-                bulk_g2s(aux + 512, rec + BR_U + vb * (CH * CH * 4), CH * CH * 4, ab);
-            }
+        for (int op = 0; op < Cfg::OPS; ++op) {
+            const int slot = (Cfg::OPS * s + op) % Cfg::SLOTS;
+            mbar_expect_tx(bar + 8 * slot, 32768);
+            bulk_g2s(sbase + Cfg::RING + slot * 32768, rec + offs[op], 32768, bar + 8 * slot);
         }
         if (BWD) {
-            __syncwarp();   // the expected byte count is posted before any row lands
-            for (int r = lane; r < len; r += 32)
-                bulk_g2s(aux + 512 + r * Cfg::DO_STRIDE, p.dout + ((size_t)(tok0 + r) * p.H_v + h) * KD + vb * CH,
-                         128, ab);
+            // the chunk's 64 dO rows, channels of this V block, in one tensor copy (rows past the
+            // sequence are read but never used; past the tensor they are zero)
+            mbar_expect_tx(ab, 512 + CH * CH * 2);
+            bulk_g2s(aux + Cfg::AUX_D, rec + BR_D, 512, ab);
+            tma_load_3d(aux, &tdo, vb * CH, h, sd.tok + chunk_of(s) * CH, ab);
+        } else {
+            mbar_expect_tx(ab, 512 + CH * CH * 4);
+            bulk_g2s(aux, rec + BR_D, 512, ab);
+            bulk_g2s(aux + Cfg::AUX_M, rec + BR_U + vb * (CH * CH * 4), CH * CH * 4, ab);
         }
     };
-    if (warp == 0 && n > 0) issue(0);
+    if (tid == 0 && n > 0) issue(0);
 
     float *outbase = BWD ? p.dSC : p.S0;
     bool ok = true;
@@ -608,7 +612,7 @@ __global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
         const float *op2 = reinterpret_cast<const float *>(sm + Cfg::RING + ((Cfg::OPS * s + 1) % Cfg::SLOTS) * 32768);
         const float *op3 = reinterpret_cast<const float *>(sm + Cfg::RING + ((Cfg::OPS * s + 2) % Cfg::SLOTS) * 32768);
         const unsigned char *aux = sm + Cfg::AUXB + (s & 1) * Cfg::AUX;
-        const float *sD = reinterpret_cast<const float *>(aux);
+        const float *sD = reinterpret_cast<const float *>(aux + Cfg::AUX_D);
         const int c = chunk_of(s), len = min(CH, sd.len - c * CH);
         // the state entering this step, to the workspace
         if (tid == 0) {
@@ -625,7 +629,7 @@ __global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
             tile_out<1, 4>(acc, m0, n0, g, t, [&](int v, int r, float e0, float e1) {
                 float z0 = -e0, z1 = -e1;
                 if (!BWD) {
-                    const float *u = reinterpret_cast<const float *>(aux + 512);   // U block [r][v]
+                    const float *u = reinterpret_cast<const float *>(aux + Cfg::AUX_M);   // U block [r][v]
                     z0 += u[toff<CH>(r, v)];
                     z1 += u[toff<CH>(r + 1, v)];
                 }
@@ -633,7 +637,7 @@ __global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
             });
         }
         __syncthreads();   // Z complete; op1 consumed
-        if (warp == 0 && s + 1 < n) issue(s + 1);
+        if (tid == 0 && s + 1 < n) issue(s + 1);
         // ---- X <- X Diag(D) + Z op2 (+ dO^T N)
         {
             const int m0 = 32 * (warp >> 2), n0 = 32 * (warp & 3);
@@ -652,12 +656,12 @@ __global__ __launch_bounds__(CN_THREADS, 1) void bwdc_chain_kernel(const BwdcPar
             mma_frag(acc, 0, CH, AKc<CH, 2, false>(sZ, m0, lane),
                      bfn<4, false>([&](int r, int cc) { return op2[toff<KD>(r, cc)]; }, n0, g, t));
             if (BWD) {
-                const unsigned char *dorow = aux + 512;
+                // dO[r][v] in the TMA box: 128-byte rows, 16-byte unit u of row r at u ^ (r % 8)
                 mma_frag(acc, 0, CH,
                          afn<2, false>(
                              [&](int v, int r) {
-                                 return r < len ? bf16_to_f(*reinterpret_cast<const uint16_t *>(dorow + r * Cfg::DO_STRIDE + 2 * v))
-                                                : 0.f;
+                                 const uint32_t off = (uint32_t)(r * 128 + ((((2 * v) >> 4) ^ (r & 7)) << 4) + ((2 * v) & 15));
+                                 return r < len ? bf16_to_f(*reinterpret_cast<const uint16_t *>(aux + off)) : 0.f;
                              },
                              m0, g, t),
                          bfn<4, false>([&](int r, int cc) { return op3[toff<KD>(r, cc)]; }, n0, g, t));
@@ -1367,13 +1371,21 @@ cudaError_t launch_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, 
     }
     if (nseq > 0) {
         const unsigned chains = (unsigned)((long long)nseq * H_v * 2);
-        if ((e = smem_attr(bwdc_chain_kernel<false>, ChainCfg<false>::BYTES)) != cudaSuccess) return e;
-        if ((e = smem_attr(bwdc_chain_kernel<true>, ChainCfg<true>::BYTES)) != cudaSuccess) return e;
-        bwdc_chain_kernel<false><<<chains, CN_THREADS, ChainCfg<false>::BYTES + 128, stream>>>(bp);
+        if ((e = cudaFuncSetAttribute(bwdc_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)(ChainCfg<false>::BYTES + 1024))) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(bwdc_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)(ChainCfg<true>::BYTES + 1024))) != cudaSuccess)
+            return e;
+        // dO as [token][H_v][128] bf16, boxes of 64 channels x 64 rows (the reverse chain's extras)
+        CUtensorMap tdo;
+        memset(&tdo, 0, sizeof(tdo));
+        if (tokens > 0 && (e = tma_map_rows_heads(&tdo, dout, tokens, H_v, CH, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+        bwdc_chain_kernel<false><<<chains, CN_THREADS, ChainCfg<false>::BYTES + 1024, stream>>>(tdo, bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_chain_kernel<fwd>", stream);
-        bwdc_chain_kernel<true><<<chains, CN_THREADS, ChainCfg<true>::BYTES + 128, stream>>>(bp);
+        bwdc_chain_kernel<true><<<chains, CN_THREADS, ChainCfg<true>::BYTES + 1024, stream>>>(tdo, bp);
         ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         timing_mark("bwdc_chain_kernel<bwd>", stream);
