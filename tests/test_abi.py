@@ -96,9 +96,11 @@ def test_bwd_workspace_size(lib):
 
 
 def test_bwd_ws_rejects_small_workspace(lib):
+    # T = 0 with NULL token tensors: only dA_log, dh0 and the workspace are real addresses, so a
+    # regressed size check could touch nothing but the 16 MiB buffer behind FAKE
     f = ctypes.c_float(0.1)
-    rc = lib.kda_bwd_ws(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, f, None, None, 0, 1, 64, 1, 1, 128, 128, FAKE, None,
-                        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_size_t(16), None)
+    rc = lib.kda_bwd_ws(None, None, None, None, None, FAKE, f, None, None, 0, 1, 0, 1, 1, 128, 128, None, None,
+                        None, None, None, None, None, FAKE, FAKE, FAKE, ctypes.c_size_t(16), None)
     assert rc == kda.KDA_ERR_WORKSPACE
 
 
