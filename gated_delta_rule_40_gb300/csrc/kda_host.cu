@@ -23,6 +23,8 @@ cudaError_t launch_fwd_heads(const uint16_t *q, const uint16_t *k, const uint16_
                              const uint16_t *b, const float *A_log, float scale, const float *init, float *fin,
                              const int32_t *cu, int N, int B, int T, int H_qk, int H_v, int h0, int Hw, bool plan,
                              uint16_t *out, void *ws_ptr, cudaStream_t stream, int *launches);
+cudaError_t ws_alloc(void **p, size_t bytes, cudaStream_t stream);
+cudaError_t ws_free(void *p, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -134,7 +136,7 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
     int rc = copy_streams(&h2d, &d2h);
     if (rc != KDA_OK) return rc;
     char *base = nullptr;
-    if (cudaMallocAsync((void **)&base, off, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::ws_alloc((void **)&base, off, stream) != cudaSuccess) return KDA_ERR_CUDA;
     std::vector<cudaEvent_t> ev_in(np), ev_out(np);
     cudaEvent_t ev_start, ev_end, ev_h2d;
     cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
@@ -202,7 +204,7 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
     ok(eh);
     if (eh == cudaSuccess) ok(cudaStreamWaitEvent(stream, ev_h2d, 0));
     if (ee == cudaSuccess) ok(cudaStreamWaitEvent(stream, ev_end, 0));
-    const cudaError_t ef = (eh == cudaSuccess && ee == cudaSuccess) ? cudaFreeAsync(base, stream) : cudaFree(base);
+    const cudaError_t ef = (eh == cudaSuccess && ee == cudaSuccess) ? kda::ws_free(base, stream) : cudaFree(base);
     cudaEventDestroy(ev_start);
     cudaEventDestroy(ev_end);
     cudaEventDestroy(ev_h2d);

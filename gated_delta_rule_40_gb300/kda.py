@@ -93,6 +93,8 @@ def load() -> ctypes.CDLL:
     lib.kda_set_kernel_timing.restype = I
     lib.kda_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_char_p), I]
     lib.kda_kernel_times.restype = I
+    lib.kda_release_cached_memory.argtypes = []
+    lib.kda_release_cached_memory.restype = I
     _lib = lib
     return lib
 
@@ -337,6 +339,12 @@ def kda_kernel_times() -> list:
     if n < 0:
         raise KdaError(n, "kda_kernel_times")
     return [(names[i].decode(), float(ms[i])) for i in range(n)]
+
+
+def kda_release_cached_memory() -> None:
+    """Hand the workspace pool's unused device memory back to the driver (the allocating
+    entry points keep their largest workspace mapped between calls)."""
+    _raise(load().kda_release_cached_memory(), "kda_release_cached_memory")
 
 
 DECODE_MAX_TOKENS = 8

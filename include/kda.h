@@ -87,8 +87,8 @@ enum {
  * Each sequence starts from its own initial state; feeding final_state into
  * initial_state of a call on the continuation equals one call on the whole
  * sequence.  A zero-length sequence copies its initial state (or zeros) to
- * final_state.  Allocates its workspace with cudaMallocAsync / cudaFreeAsync
- * on `stream`; use kda_fwd_ws to supply it instead.
+ * final_state.  Takes its workspace from the library's workspace pool on
+ * `stream` (see kda_release_cached_memory); use kda_fwd_ws to supply it instead.
  */
 int kda_fwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v,
             const kda_bf16_t *graw, const kda_bf16_t *b, const float *A_log, float scale,
@@ -134,7 +134,7 @@ int kda_fwd_scalar_gate(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16
  * a chunk boundary and its state carried on the device, which is the chunking
  * and arithmetic of a single call.  cu_seqlens is checked on the host: a
  * malformed array returns KDA_ERR_BAD_SEQLENS before anything is queued.
- * Device buffers come from cudaMallocAsync / cudaFreeAsync on `stream`; two
+ * Device buffers come from the library's workspace pool on `stream`; two
  * copy streams per device are created on the first call and kept.
  * Asynchronous like kda_fwd: the results are in host memory once `stream` has
  * passed the call (e.g. after cudaStreamSynchronize), and the host buffers must
@@ -252,8 +252,8 @@ int kda_fwd_noalloc(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *
  * it (a reverse chain), then the chunks' gradients in parallel.  The workspace
  * holds, per (chunk, value head), those operands, both states and the value-side
  * gradient sums (about 434 KiB), plus 1 KiB per token and value head (8.4 GB
- * for B=2, T=16384, H_v=32); kda_bwd takes it from cudaMallocAsync on `stream`
- * (a failed allocation returns KDA_ERR_CUDA), kda_bwd_ws from the caller.  Errors
+ * for B=2, T=16384, H_v=32); kda_bwd takes it from the library's workspace
+ * pool on `stream` (a failed allocation returns KDA_ERR_CUDA), kda_bwd_ws from the caller.  Errors
  * as kda_fwd.
  */
 int kda_bwd(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, const kda_bf16_t *graw,
@@ -296,7 +296,7 @@ int kda_bwd_ws(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16_t *v, co
  * K = V = 128 and H_v a multiple of H_qk (value head h reads q/k head
  * h / (H_v / H_qk)); q, k, v and out 16-byte aligned.  One fused kernel per
  * call (after the sequence plan) streams q, k, v once and writes out once; a
- * few KB of plan tables come from cudaMallocAsync on `stream`.  Errors and
+ * few KB of plan tables come from the library's workspace pool on `stream`.  Errors and
  * asynchrony as kda_fwd (a malformed cu_seqlens sets KDA_ERR_BAD_SEQLENS in
  * the status word and writes nothing).
  */
@@ -340,6 +340,22 @@ int kda_last_launch_count(void);
  */
 int kda_set_kernel_timing(int enable);
 int kda_kernel_times(float *ms, const char **names, int max_n);
+
+/*
+ * The allocating entry points (kda_fwd, kda_fwd_bf16_state,
+ * kda_fwd_scalar_gate, kda_fwd_host, kda_bwd, kda_la_fwd) take their device
+ * workspace from one stream-ordered memory pool per device, created on first
+ * use with an unbounded release threshold: what a call frees on its stream
+ * stays mapped in the pool after the caller synchronises, and the next call
+ * reuses it instead of mapping fresh pages, as a caching allocator does (the
+ * device's default pool would hand the pages back at every synchronisation, and
+ * mapping the 1.8 GB workspace of a B=2, T=16384, H_v=32 forward again costs
+ * about as much as the forward).  The pool therefore keeps the largest
+ * workspace used so far.  kda_release_cached_memory returns every byte of
+ * every device's pool that no queued call still uses to the driver; it returns
+ * KDA_OK, or KDA_ERR_CUDA if the driver refused.
+ */
+int kda_release_cached_memory(void);
 
 #ifdef __cplusplus
 }

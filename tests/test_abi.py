@@ -30,7 +30,8 @@ def lib():
 def test_exports_every_declared_symbol(lib):
     names = kda.declared_symbols()
     assert {"kda_fwd", "kda_fwd_ws", "kda_fwd_workspace_size", "kda_decode_step", "kda_status_string",
-            "kda_get_status", "kda_last_launch_count", "kda_bwd", "kda_bwd_ws", "kda_bwd_workspace_size"} <= set(names)
+            "kda_get_status", "kda_last_launch_count", "kda_bwd", "kda_bwd_ws", "kda_bwd_workspace_size",
+            "kda_release_cached_memory"} <= set(names)
     for n in names:
         assert hasattr(lib, n), n
 

@@ -109,6 +109,37 @@ def test_no_final_state_and_workspace_path():
     assert torch.equal(out_a, out_b) and torch.equal(fin_a, fin_b) and torch.equal(out_a, out_c)
 
 
+def test_workspace_pool_keeps_and_releases_memory():
+    """The allocating entry keeps its workspace mapped in the library's pool across a
+    synchronisation (free device memory stays lower by at least the workspace), the
+    release entry hands it back, and calls before and after the release agree bit for bit."""
+    from gated_delta_rule_40_gb300 import kda
+    inp = KI.make_inputs(1, 4096, 2, 8, seed=111, with_state=True)
+    d = to_dev(inp)
+    need = kda.kda_fwd_workspace_size(1, 1, 4096, 2, 8)
+    assert need > 32 << 20
+
+    def call():
+        return kda.kda_fwd(d["q"], d["k"], d["v"], d["graw"], d["b"], d["A_log"], d["scale"],
+                           initial_state=d["initial_state"])
+
+    kda.kda_release_cached_memory()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    out_a, fin_a = call()
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    # outputs (4 MiB + 4 MiB) come from torch's caching allocator, the workspace from the pool
+    assert free0 - free1 >= need
+    kda.kda_release_cached_memory()
+    free2 = torch.cuda.mem_get_info()[0]
+    assert free2 - free1 >= need
+    out_b, fin_b = call()
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b) and torch.equal(fin_a, fin_b)
+    assert kda.kda_get_status() == 0
+
+
 def test_split_call_equals_single_call():
     inp = KI.make_inputs(1, 400, 1, 2, seed=110, with_state=True)
     out, fin = gpu_fwd(inp)
