@@ -704,76 +704,9 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             bulk_commit();
         }
 
-        // ---- 4. T = (I + A)^{-1}.  Diagonal 16 x 16 blocks by forward substitution; then
-        //         T10 = -T11 A10 T00 and T32 = -T33 A32 T22; then the lower-left 32 x 32 block
-        //         T21 = -T2 (A21 T1) with T1, T2 the diagonal 32 x 32 blocks.
-        if (tid < 64) {
-            const int bi = tid >> 4, c = tid & 15, o = 16 * bi;
-            // right-looking: once t[j] is final, subtract its column from the later rows
-            float t[SUB];
-#pragma unroll
-            for (int r = 0; r < SUB; ++r) t[r] = (r == c) ? 1.f : 0.f;
-#pragma unroll
-            for (int j = 0; j < SUB; ++j)
-#pragma unroll
-                for (int r = j + 1; r < SUB; ++r) t[r] = fmaf(-sA[(o + r) * AS + o + j], t[j], t[r]);
-#pragma unroll
-            for (int r = 0; r < SUB; ++r) sT[(o + r) * AS + o + c] = t[r];
-        } else {
-            for (int idx = tid - 64; idx < 6 * 256; idx += IN_THREADS - 64) {
-                const int blk = idx >> 8, e = idx & 255;
-                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                sT[(16 * bi + (e >> 4)) * AS + 16 * bj + (e & 15)] = 0.f;
-            }
-        }
-        __syncthreads();
-        {
-            // Z_b = A_{i,j} T_jj, then T_ij = -T_ii Z_b for (i, j) = (1, 0), (3, 2), on mma.sync with
-            // the three-term split; warps 0..3: block b = w >> 1, 8-column half w & 1
-            const int gid = lane >> 2, tig = lane & 3, b = warp >> 1, n0 = 8 * (warp & 1);
-            const int bi = 2 * b + 1, bj = 2 * b;
-            float *z = sX + b * 16 * ZS;
-            if (warp < 4) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                split_mma<2>(sA + (16 * bi) * AS + 16 * bj, AS, sT + (16 * bj) * AS + 16 * bj + n0, AS, gid, tig, d);
-                z[gid * ZS + n0 + 2 * tig] = d[0];
-                z[gid * ZS + n0 + 2 * tig + 1] = d[1];
-                z[(gid + 8) * ZS + n0 + 2 * tig] = d[2];
-                z[(gid + 8) * ZS + n0 + 2 * tig + 1] = d[3];
-            }
-            __syncthreads();
-            if (warp < 4) {
-                float t[4] = {0.f, 0.f, 0.f, 0.f};
-                split_mma<2>(sT + (16 * bi) * AS + 16 * bi, AS, z + n0, ZS, gid, tig, t);
-                float *dst = sT + (16 * bi) * AS + 16 * bj + n0;
-                dst[gid * AS + 2 * tig] = -t[0];
-                dst[gid * AS + 2 * tig + 1] = -t[1];
-                dst[(gid + 8) * AS + 2 * tig] = -t[2];
-                dst[(gid + 8) * AS + 2 * tig + 1] = -t[3];
-            }
-        }
-        __syncthreads();
-        {
-            // X = A21 T1 (rows 32..63, columns 0..31), then T21 = -T2 X, on mma.sync (m16n8k8 tf32)
-            // with both operands split into tf32 hi + lo terms (hi*lo + lo*hi + hi*hi, about fp32
-            // accuracy).  Warp w owns the 16 x 8 output tile (rows 16 (w >> 2), columns 8 (w & 3)).
-            const int gid = lane >> 2, tig = lane & 3, m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            split_mma<4>(sA + (32 + m0) * AS, AS, sT + n0, AS, gid, tig, d);
-            sX[(m0 + gid) * XS + n0 + 2 * tig] = d[0];
-            sX[(m0 + gid) * XS + n0 + 2 * tig + 1] = d[1];
-            sX[(m0 + gid + 8) * XS + n0 + 2 * tig] = d[2];
-            sX[(m0 + gid + 8) * XS + n0 + 2 * tig + 1] = d[3];
-            __syncthreads();
-            float t[4] = {0.f, 0.f, 0.f, 0.f};
-            split_mma<4>(sT + (32 + m0) * AS + 32, AS, sX + n0, XS, gid, tig, t);
-            sT[(32 + m0 + gid) * AS + n0 + 2 * tig] = -t[0];
-            sT[(32 + m0 + gid) * AS + n0 + 2 * tig + 1] = -t[1];
-            sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig] = -t[2];
-            sT[(32 + m0 + gid + 8) * AS + n0 + 2 * tig + 1] = -t[3];
-        }
-        __syncthreads();
+        // ---- 4. T = (I + A)^{-1} (blocked: diagonal 16 x 16 blocks by forward substitution, the
+        //         off-diagonal blocks as split-tf32 products on mma.sync; synchronises the CTA)
+        invert_unit_lower64<IN_THREADS>(sA, sT, sX, tid, warp, lane);
         // T' = T diag(beta) (for U) and T'_W = T diag(beta rk) (for W: Kg is unnormalised), each
         // split into bf16 hi + lo, as A operands (K-major, 64 r x 64 j)
         for (int idx = tid; idx < CH * (CH / 8); idx += IN_THREADS) {
