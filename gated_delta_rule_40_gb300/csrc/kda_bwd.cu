@@ -236,6 +236,44 @@ struct BwdcParams {
 // Gam (fp32 tile; rows past len repeat the last valid row, their g being 0), beta = sigmoid(b)
 // (0 past len) and D = e^Gam_C.  All NT threads take part (sTot: NT floats of scratch);
 // returns synchronised.
+// L2 prefetch of one item's token rows, issued one item ahead so that the next item's row loads
+// hit L2.  `mask` selects the tensors: RP_QKG (q and k of the item's q/k head, graw and b of its
+// value head), RP_V (v), RP_DO (dO); two 128-byte lines per row of q, k, graw, v, dO and one for
+// b.  The requests are spread over the CTA's threads.
+enum { RP_QKG = 1, RP_V = 2, RP_DO = 4 };
+template <int NT>
+__device__ __forceinline__ void prefetch_rows_l2(const BwdcParams &p, const ChunkDesc &cd, int h, int hq, int mask,
+                                                 int tid) {
+    for (int u = tid; u < CH * 11; u += NT) {
+        const int r = u / 11, w = u % 11;
+        if (r >= cd.len) continue;
+        const size_t tok = (size_t)cd.tok + r;
+        const uint16_t *src = nullptr;
+        if (w < 6) {
+            if (!(mask & RP_QKG)) continue;
+            src = w < 2 ? p.q + (tok * p.H_qk + hq) * KD : w < 4 ? p.k + (tok * p.H_qk + hq) * KD
+                                                              : p.graw + (tok * p.H_v + h) * KD;
+        } else if (w < 8) {
+            if (!(mask & RP_V)) continue;
+            src = p.v + (tok * p.H_v + h) * KD;
+        } else if (w < 10) {
+            if (!(mask & RP_DO)) continue;
+            src = p.dout + (tok * p.H_v + h) * KD;
+        } else {
+            if (mask & RP_QKG) prefetch_line_l2(p.b + tok * p.H_v + h);
+            continue;
+        }
+        prefetch_line_l2(src + 64 * (w & 1));
+    }
+}
+
+// L2 prefetch of a contiguous global range (16-byte aligned, a multiple of 16 bytes) in bulk
+// requests of at most 32 KiB, from one thread.
+__device__ __forceinline__ void prefetch_range_l2(const void *src, uint32_t bytes) {
+    const unsigned char *c = static_cast<const unsigned char *>(src);
+    for (uint32_t o = 0; o < bytes; o += 32768u) prefetch_l2(c + o, bytes - o < 32768u ? bytes - o : 32768u);
+}
+
 template <int NT>
 __device__ void bwdc_rows(const BwdcParams &p, int tok0, int len, int h, int hq, float a, float *sKh, float *sQt,
                           float *sG, float *sBeta, float *sD, float *sTot, int tid) {
@@ -375,6 +413,11 @@ __global__ __launch_bounds__(PN_THREADS, 1) void bwdc_prep_kernel(const BwdcPara
         const int hq = h / group, len = cd.len;
         const float a = ex2n(p.A_log[h]);
         float *rec = reinterpret_cast<float *>(p.rec + (size_t)item * BR_BYTES);
+        if (item + gridDim.x < n_items) {   // the next item's rows into L2
+            const long long nx = item + gridDim.x;
+            const int nh = (int)(nx % p.H_v);
+            prefetch_rows_l2<PN_THREADS>(p, p.chunks[nx / p.H_v], nh, nh / group, RP_QKG | RP_V, tid);
+        }
         __syncthreads();   // the previous item's reads of shared memory are done
         bwdc_rows<PN_THREADS>(p, cd.tok, len, h, hq, a, sKh, sQt, sG, sBeta, sD, sX, tid);
 
@@ -776,6 +819,22 @@ __global__ __launch_bounds__(GN_THREADS, 1) void bwdc_gradv_kernel(const BwdcPar
             if (!__syncthreads_and(mine)) {
                 ok = false;
                 break;
+            }
+            if (vh == 1 && item + gridDim.x < n_items) {
+                // this item's copies have landed: the next item's tiles, states and rows into L2
+                // while this half computes
+                const long long nx = item + gridDim.x;
+                const int nh = (int)(nx % p.H_v);
+                prefetch_rows_l2<GN_THREADS>(p, p.chunks[nx / p.H_v], nh, 0, RP_V | RP_DO, tid);
+                if (tid == 0) {
+                    const unsigned char *nrec = p.rec + (size_t)nx * BR_BYTES;
+                    prefetch_range_l2(nrec + BR_W, 2 * 32768);   // W, Kd
+                    prefetch_range_l2(nrec + BR_U, 32768);       // U
+                    prefetch_range_l2(nrec + BR_P, 2 * 16384);   // P, T
+                    prefetch_range_l2(nrec + BR_D, 768);         // D, beta
+                    prefetch_range_l2(p.S0 + nx * (ST_BYTES / 4), ST_BYTES);
+                    prefetch_range_l2(p.dSC + nx * (ST_BYTES / 4), ST_BYTES);
+                }
             }
             // ---- Delta (in place of U) and dDelta, both tensor-core operands only from here on
             // (stored as tf32 numbers); W, Kd, P, T arrive as tf32 numbers, S0, dS as fp32
