@@ -20,6 +20,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Tiled 3-D store of one box from shared memory (completion tracked by the issuing thread's bulk
+// groups: cp.async.bulk.commit_group / wait_group).  The shared-memory writes it reads must be
+// made visible to the async proxy (fence.proxy.async) and ordered before it by a barrier.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int y, int z, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(src)
+                 : "memory");
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (looked up once).
 inline cudaError_t tma_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn_out) {
     static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
@@ -37,8 +46,9 @@ inline cudaError_t tma_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn_out) {
 }
 
 // [rows][heads][128] bf16 as a 3-D tensor (channel, head, row); boxes of box_ch channels x 1 head
-// x 64 rows, with the given shared-memory swizzle, zero fill past the last row.  box_ch x 2 bytes
-// must equal the swizzle span (32 channels with 64-byte swizzle, 64 with 128-byte swizzle).
+// x 64 rows, with the given shared-memory swizzle, zero fill past the last row.  With a swizzle,
+// box_ch x 2 bytes must equal its span (32 channels with 64-byte swizzle, 64 with 128-byte
+// swizzle); without one, box_ch = 128 (whole 256-byte rows).
 inline cudaError_t tma_map_rows_heads(CUtensorMap *m, const void *base, long long rows, int heads, int box_ch,
                                       CUtensorMapSwizzle swizzle) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;

@@ -26,7 +26,9 @@
 // stores the remainder Kd_lo in a double buffer, so the state update keeps
 // ~16 bits; S and P enter the output products rounded to bf16, like the output
 // itself.  P carries the factor scale, and the output O = scale exp(Gam_r) Y1 + Y2
-// is transposed through shared memory and written with 16-byte stores.  Every
+// is transposed through shared memory (double-buffered) and leaves by one TMA tensor
+// store per full chunk (16-byte stores of the valid rows for a sequence's last,
+// partial chunk, whose other rows belong to the next sequence).  Every
 // wait is bounded; a timeout records KDA_ERR_DEVICE_TIMEOUT and all roles stop.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -100,6 +102,7 @@ __device__ __forceinline__ void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]
 __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_constant__ CUtensorMap tq,
                                                                const __grid_constant__ CUtensorMap tk,
                                                                const __grid_constant__ CUtensorMap tv,
+                                                               const __grid_constant__ CUtensorMap tout,
                                                                const LaParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -354,7 +357,10 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             return true;
         };
         // output of chunk c: O[r][v] = scale (exp(Gam_r) Y1^T[v][r] + Y2^T[v][r]) for r = 16 cg .. 16 cg + 15,
-        // through the staging buffer to 16-byte stores of whole rows
+        // through staging buffer c & 1: a full chunk leaves by one TMA store issued by thread 0, a
+        // partial one by 16-byte stores of its valid rows.  Before the barrier thread 0 waits for
+        // its previous store (chunk c - 1, the other buffer) to finish reading, so that after it
+        // every thread may rewrite that buffer for chunk c + 1.
         auto emit = [&](int c) {
             const int b = c & 1, len = min(CH, sd.len - c * CH);
             uint16_t *os = reinterpret_cast<uint16_t *>(sm + LA_OS + b * 16384);
@@ -376,13 +382,22 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                     f *= lam;
                 }
             }
+            fence_async_smem();
+            if (tid == 0) bulk_wait_read_all();
             named_bar(1, LA_EPI);
+            if (len == CH) {
+                if (tid == 0) {
+                    tma_store_3d(&tout, 0, h, sd.tok + c * CH, sbase + LA_OS + b * 16384);
+                    bulk_commit();
+                }
+            } else {
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int u = tid + LA_EPI * i, r = u >> 4, c16 = u & 15;
-                if (r < len)
-                    *reinterpret_cast<uint4 *>(p.out + ((size_t)(sd.tok + c * CH + r) * p.H_v + h) * KD + 8 * c16) =
-                        *reinterpret_cast<const uint4 *>(os + r * KD + 8 * c16);
+                for (int i = 0; i < 2; ++i) {
+                    const int u = tid + LA_EPI * i, r = u >> 4, c16 = u & 15;
+                    if (r < len)
+                        *reinterpret_cast<uint4 *>(p.out + ((size_t)(sd.tok + c * CH + r) * p.H_v + h) * KD + 8 * c16) =
+                            *reinterpret_cast<const uint4 *>(os + r * KD + 8 * c16);
+                }
             }
         };
         bool ok = n == 0 || e1(0);
@@ -393,6 +408,7 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
             emit(c);
         }
         if (!ok) fail();
+        if (tid == 0) bulk_wait_all();   // the last output stores are done with shared memory
         if (ok && p.fin) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
@@ -448,22 +464,26 @@ cudaError_t launch_la_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *
     ++*launches;
     if (nseq == 0) return cudaSuccess;
     const long long rows = (long long)B * T;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     // a map needs at least one row; with no tokens the kernel only copies the states
     const void *qb = rows > 0 ? (const void *)q : (const void *)hdr;
     const void *kb = rows > 0 ? (const void *)k : (const void *)hdr;
     const void *vb = rows > 0 ? (const void *)v : (const void *)hdr;
+    const void *ob = rows > 0 ? (const void *)out : (const void *)hdr;
     const long long r = rows > 0 ? rows : 1;
     if ((e = make_map(&mq, qb, r, rows > 0 ? H_qk : 1)) != cudaSuccess) return e;
     if ((e = make_map(&mk, kb, r, rows > 0 ? H_qk : 1)) != cudaSuccess) return e;
     if ((e = make_map(&mv, vb, r, rows > 0 ? H_v : 1)) != cudaSuccess) return e;
+    // the output: whole 256-byte rows, no swizzle (the staging buffer is row-major [64 r][128 v])
+    if ((e = tma_map_rows_heads(&mo, ob, r, rows > 0 ? H_v : 1, 128, CU_TENSOR_MAP_SWIZZLE_NONE)) != cudaSuccess)
+        return e;
     if ((e = cudaFuncSetAttribute(la_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LA_BYTES)) !=
         cudaSuccess)
         return e;
     LaParams lp;
     lp.seqs = seqs; lp.order = order; lp.hdr = hdr; lp.slope = slope; lp.scale = scale;
     lp.init = init; lp.fin = fin; lp.out = out; lp.H_qk = H_qk; lp.H_v = H_v; lp.nseq = nseq;
-    la_fwd_kernel<<<(unsigned)((long long)nseq * H_v), LA_THREADS, LA_BYTES, stream>>>(mq, mk, mv, lp);
+    la_fwd_kernel<<<(unsigned)((long long)nseq * H_v), LA_THREADS, LA_BYTES, stream>>>(mq, mk, mv, mo, lp);
     ++*launches;
     return cudaGetLastError();
 }
