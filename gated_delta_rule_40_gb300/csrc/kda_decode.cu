@@ -14,10 +14,14 @@ namespace kda {
 constexpr int DEC_WARPS = 8;
 constexpr int DEC_ROWS = KD / DEC_WARPS;  // state rows per warp
 
-__global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_kernel(
+// The state is stored in fp32, or in bf16 (BF16: each row widened to fp32 for the step and
+// rounded once on store; with 8-byte rows per lane the kernel fits four CTAs per SM, so more
+// of the state is in flight).
+template <bool BF16>
+__global__ __launch_bounds__(DEC_WARPS * 32, BF16 ? 4 : 2) void decode_kernel(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ k, const uint16_t *__restrict__ v,
     const uint16_t *__restrict__ graw, const uint16_t *__restrict__ b, const float *__restrict__ A_log,
-    float scale, float *__restrict__ state, int H_qk, int H_v, uint16_t *__restrict__ out) {
+    float scale, void *__restrict__ state, int H_qk, int H_v, uint16_t *__restrict__ out) {
     const int bh = blockIdx.x;
     const int bi = bh / H_v, h = bh - bi * H_v;
     const int hq = h / (H_v / H_qk);
@@ -26,6 +30,19 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_kernel(
     // Lane owns channels 4*lane .. 4*lane+3.
     const size_t qk_off = ((size_t)bi * H_qk + hq) * KD + 4 * lane;
     const size_t hv_off = ((size_t)bi * H_v + h) * KD;
+    // the warp's 16 state rows are requested first, so that their latency overlaps the token's
+    // preparation below
+    const int r0 = warp * DEC_ROWS;
+    float *S = reinterpret_cast<float *>(state) + (hv_off + r0) * KD;
+    uint16_t *Sb = reinterpret_cast<uint16_t *>(state) + (hv_off + r0) * KD;
+    float4 s[BF16 ? 1 : DEC_ROWS];
+    uint2 sb[BF16 ? DEC_ROWS : 1];
+#pragma unroll
+    for (int i = 0; i < DEC_ROWS; ++i) {
+        if (BF16) sb[i] = __ldcs(reinterpret_cast<const uint2 *>(Sb + (size_t)i * KD) + lane);
+        else s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)i * KD) + lane);
+    }
+    const float vrow = bf16_to_f(v[hv_off + r0 + (lane & (DEC_ROWS - 1))]);
     const uint2 qw = *reinterpret_cast<const uint2 *>(q + qk_off);
     const uint2 kw = *reinterpret_cast<const uint2 *>(k + qk_off);
     const uint2 gw = *reinterpret_cast<const uint2 *>(graw + hv_off + 4 * lane);
@@ -54,17 +71,12 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_kernel(
     const float bb = bf16_to_f(b[(size_t)bi * H_v + h]);
     const float beta = 1.0f / (1.0f + ex2(-bb * LOG2E));
 
-    const int r0 = warp * DEC_ROWS;
-    float *S = state + (hv_off + r0) * KD;
-    float4 s[DEC_ROWS];
-#pragma unroll
-    for (int i = 0; i < DEC_ROWS; ++i) s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)i * KD) + lane);
-    const float vrow = bf16_to_f(v[hv_off + r0 + (lane & (DEC_ROWS - 1))]);
 
     float o_mine = 0.f;
 #pragma unroll
     for (int i = 0; i < DEC_ROWS; ++i) {
-        float4 x = s[i];
+        float4 x = BF16 ? make_float4(bf16_lo(sb[i].x), bf16_hi(sb[i].x), bf16_lo(sb[i].y), bf16_hi(sb[i].y))
+                        : s[BF16 ? 0 : i];
         x.x *= dec[0];
         x.y *= dec[1];
         x.z *= dec[2];
@@ -82,7 +94,11 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_kernel(
         x.y = fmaf(delta, kh[1], x.y);
         x.z = fmaf(delta, kh[2], x.z);
         x.w = fmaf(delta, kh[3], x.w);
-        __stcs(reinterpret_cast<float4 *>(S + (size_t)i * KD) + lane, x);
+        if (BF16)
+            __stcs(reinterpret_cast<uint2 *>(Sb + (size_t)i * KD) + lane,
+                   make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w)));
+        else
+            __stcs(reinterpret_cast<float4 *>(S + (size_t)i * KD) + lane, x);
         if (lane == i) o_mine = fmaf(delta, kq, dq);
     }
     if (lane < DEC_ROWS) out[hv_off + r0 + lane] = f_to_bf16(o_mine);
@@ -93,8 +109,8 @@ cudaError_t launch_decode(const uint16_t *q, const uint16_t *k, const uint16_t *
                           int H_v, uint16_t *out, cudaStream_t stream) {
     const long long nblk = (long long)B * H_v;
     if (nblk == 0) return cudaSuccess;
-    decode_kernel<<<(unsigned)nblk, DEC_WARPS * 32, 0, stream>>>(q, k, v, graw, b, A_log, scale, state, H_qk,
-                                                               H_v, out);
+    decode_kernel<false><<<(unsigned)nblk, DEC_WARPS * 32, 0, stream>>>(q, k, v, graw, b, A_log, scale, state, H_qk,
+                                                                      H_v, out);
     return cudaGetLastError();
 }
 
@@ -248,7 +264,10 @@ cudaError_t launch_decode_tokens(const uint16_t *q, const uint16_t *k, const uin
                                  int B, int Tq, int H_qk, int H_v, uint16_t *out, cudaStream_t stream) {
     const long long nblk = (long long)B * H_v;
     if (nblk == 0) return cudaSuccess;
-    if (bf16_state)
+    if (bf16_state && Tq == 1)   // one token: the single-token kernel on the bf16 state (same layouts)
+        decode_kernel<true><<<(unsigned)nblk, DEC_WARPS * 32, 0, stream>>>(q, k, v, graw, b, A_log, scale, state,
+                                                                          H_qk, H_v, out);
+    else if (bf16_state)
         decode_tokens_kernel<true><<<(unsigned)nblk, DEC_WARPS * 32, 0, stream>>>(q, k, v, graw, b, A_log, scale,
                                                                                    state, Tq, H_qk, H_v, out);
     else
