@@ -121,7 +121,8 @@ cudaError_t launch_decode(const uint16_t *q, const uint16_t *k, const uint16_t *
 // state in one pass (read once, Tq updates in registers, written once), the
 // state stored in fp32 or bf16.  Warp t < Tq first prepares token t (normalised
 // q and k, per-channel decay, beta, k.q, v) in shared memory; then each warp
-// streams 16 state rows through all Tq tokens.
+// streams 16 state rows through all Tq tokens, each lane holding 16 channels of
+// four rows so that a row's two dot products reduce over eight lanes.
 // =====================================================================
 namespace kda {
 
@@ -140,19 +141,26 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     // ---- the warp's 16 state rows, requested first so that their latency overlaps the token
-    //      preparation below (fp32 in registers; a bf16 state is widened after the loads land)
-    const int r0 = warp * DEC_ROWS;
-    const size_t st0 = ((size_t)bh * KD + r0) * KD;
-    float4 s[DEC_ROWS];
-    uint2 sw[BF16_STATE ? DEC_ROWS : 1];
+    //      preparation below (fp32 in registers; a bf16 state is widened after the loads land).
+    //      Lane (g, c) = (lane / 8, lane % 8) keeps channels 32 u + 4 c .. 32 u + 4 c + 3, u = 0..3,
+    //      of rows r0 + 4 j + g, j = 0..3 (the eight lanes of a row read 128 contiguous bytes per
+    //      load), so that a row's dot products reduce over eight lanes.
+    const int r0 = warp * DEC_ROWS, g = lane >> 3, c4 = 4 * (lane & 7);
+    const size_t st0 = ((size_t)bh * KD + r0 + g) * KD + c4;   // row r0 + g, channel 4 c
+    float4 s[4][4];                                              // [row j][channel quad u]
+    uint2 sw[BF16_STATE ? 4 : 1][BF16_STATE ? 4 : 1];
     if (BF16_STATE) {
         const uint16_t *S = reinterpret_cast<const uint16_t *>(state) + st0;
 #pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i) sw[i] = __ldcs(reinterpret_cast<const uint2 *>(S + (size_t)i * KD) + lane);
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sw[j][u] = __ldcs(reinterpret_cast<const uint2 *>(S + (size_t)4 * j * KD + 32 * u));
     } else {
         const float *S = reinterpret_cast<const float *>(state) + st0;
 #pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i) s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)i * KD) + lane);
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) s[j][u] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)4 * j * KD + 32 * u));
     }
 
     // ---- token preparation: warp t handles token t; lane owns channels 4 lane .. 4 lane + 3
@@ -197,31 +205,45 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
     __syncthreads();
     if (BF16_STATE) {
 #pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i)
-            s[i] = make_float4(bf16_lo(sw[i].x), bf16_hi(sw[i].x), bf16_lo(sw[i].y), bf16_hi(sw[i].y));
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint2 w = sw[j][u];
+                s[j][u] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+            }
     }
     for (int t = 0; t < Tq; ++t) {
-        const float4 dec = *reinterpret_cast<const float4 *>(&s_dec[t][4 * lane]);
-        const float4 kh = *reinterpret_cast<const float4 *>(&s_kh[t][4 * lane]);
-        const float4 qt = *reinterpret_cast<const float4 *>(&s_qt[t][4 * lane]);
-        // per row i: dk_i = s'_i . kh (value 2 i) and dq_i = s'_i . qt (value 2 i + 1), lane partials
-        float red[2 * DEC_ROWS];
+        float4 dec[4], kh[4], qt[4];
 #pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i) {
-            float4 x = s[i];
-            x.x *= dec.x;
-            x.y *= dec.y;
-            x.z *= dec.z;
-            x.w *= dec.w;
-            s[i] = x;
-            red[2 * i] = x.x * kh.x + x.y * kh.y + x.z * kh.z + x.w * kh.w;
-            red[2 * i + 1] = x.x * qt.x + x.y * qt.y + x.z * qt.z + x.w * qt.w;
+        for (int u = 0; u < 4; ++u) {
+            dec[u] = *reinterpret_cast<const float4 *>(&s_dec[t][32 * u + c4]);
+            kh[u] = *reinterpret_cast<const float4 *>(&s_kh[t][32 * u + c4]);
+            qt[u] = *reinterpret_cast<const float4 *>(&s_qt[t][32 * u + c4]);
         }
-        // reduce-scatter over the warp: at each level a lane keeps half of its values (the half
-        // selected by its lane bit) and adds the partner's copy of that half; after five levels
-        // lane l holds the warp total of value l (31 shuffles for 32 sums)
+        // per row j: dk_j = s'_j . kh (value 2 j) and dq_j = s'_j . qt (value 2 j + 1), lane partials
+        float red[8];
 #pragma unroll
-        for (int o = 16, n = 16; o >= 1; o >>= 1, n >>= 1) {
+        for (int j = 0; j < 4; ++j) {
+            float dk = 0.f, dq = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float4 x = s[j][u];
+                x.x *= dec[u].x;
+                x.y *= dec[u].y;
+                x.z *= dec[u].z;
+                x.w *= dec[u].w;
+                s[j][u] = x;
+                dk = fmaf(x.x, kh[u].x, fmaf(x.y, kh[u].y, fmaf(x.z, kh[u].z, fmaf(x.w, kh[u].w, dk))));
+                dq = fmaf(x.x, qt[u].x, fmaf(x.y, qt[u].y, fmaf(x.z, qt[u].z, fmaf(x.w, qt[u].w, dq))));
+            }
+            red[2 * j] = dk;
+            red[2 * j + 1] = dq;
+        }
+        // reduce-scatter over the eight lanes of a row group: at each level a lane keeps half of
+        // its values (the half selected by its lane bit) and adds the partner's copy of that half;
+        // after three levels lane (g, c) holds the total of value c (7 shuffles for 8 sums)
+#pragma unroll
+        for (int o = 4, n = 4; o >= 1; o >>= 1, n >>= 1) {
             const bool upper = (lane & o) != 0;
 #pragma unroll
             for (int i = 0; i < n; ++i) {
@@ -230,32 +252,39 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
                 red[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
         }
-        // lane 2 i: dk_i -> delta_i; lane 2 i + 1: dq_i -> o_i = dq_i + delta_i (k.q)
-        const int row = lane >> 1;
+        // lane (g, 2 j): dk_j -> delta_j; lane (g, 2 j + 1): dq_j -> o = dq_j + delta_j (k.q); row r0 + 4 j + g
+        const int jm = (lane & 7) >> 1, row = r0 + 4 * jm + g;
         const float dk_or_dq = red[0];
-        const float delta_mine = s_beta[t] * (s_v[t][r0 + row] - dk_or_dq);
+        const float delta_mine = s_beta[t] * (s_v[t][row] - dk_or_dq);
         const float delta_pair = __shfl_xor_sync(0xffffffffu, delta_mine, 1);
         if (lane & 1)
-            out[(((size_t)bi * Tq + t) * H_v + h) * KD + r0 + row] = f_to_bf16(fmaf(delta_pair, s_kq[t], dk_or_dq));
+            out[(((size_t)bi * Tq + t) * H_v + h) * KD + row] = f_to_bf16(fmaf(delta_pair, s_kq[t], dk_or_dq));
 #pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i) {
-            const float delta = __shfl_sync(0xffffffffu, delta_mine, 2 * i);
-            s[i].x = fmaf(delta, kh.x, s[i].x);
-            s[i].y = fmaf(delta, kh.y, s[i].y);
-            s[i].z = fmaf(delta, kh.z, s[i].z);
-            s[i].w = fmaf(delta, kh.w, s[i].w);
+        for (int j = 0; j < 4; ++j) {
+            const float delta = __shfl_sync(0xffffffffu, delta_mine, 8 * g + 2 * j);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                s[j][u].x = fmaf(delta, kh[u].x, s[j][u].x);
+                s[j][u].y = fmaf(delta, kh[u].y, s[j][u].y);
+                s[j][u].z = fmaf(delta, kh[u].z, s[j][u].z);
+                s[j][u].w = fmaf(delta, kh[u].w, s[j][u].w);
+            }
         }
     }
     if (BF16_STATE) {
         uint16_t *S = reinterpret_cast<uint16_t *>(state) + st0;
 #pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i)
-            __stcs(reinterpret_cast<uint2 *>(S + (size_t)i * KD) + lane,
-                   make_uint2(pack_bf16x2(s[i].x, s[i].y), pack_bf16x2(s[i].z, s[i].w)));
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                __stcs(reinterpret_cast<uint2 *>(S + (size_t)4 * j * KD + 32 * u),
+                       make_uint2(pack_bf16x2(s[j][u].x, s[j][u].y), pack_bf16x2(s[j][u].z, s[j][u].w)));
     } else {
         float *S = reinterpret_cast<float *>(state) + st0;
 #pragma unroll
-        for (int i = 0; i < DEC_ROWS; ++i) __stcs(reinterpret_cast<float4 *>(S + (size_t)i * KD) + lane, s[i]);
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) __stcs(reinterpret_cast<float4 *>(S + (size_t)4 * j * KD + 32 * u), s[j][u]);
     }
 }
 
