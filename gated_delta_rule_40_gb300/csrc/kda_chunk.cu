@@ -379,20 +379,6 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         if (tid < len) bb_raw = bf16_to_f(p.b[((size_t)cd.tok + tid) * p.H_v + h]);
         if (tid == 0) bulk_wait_read_all();
         if (tid < CH) rv[RV_BETA + tid] = tid < len ? 1.0f / (1.0f + ex2(-bb_raw * LOG2E)) : 0.f;
-        // pull the next item's rows into L2 while this one is processed
-        if (has_next) {
-            const int r = tid & 63, which = tid >> 6;
-            if (r < cd_next.len) {
-                const size_t tok = (size_t)cd_next.tok + r;
-                const int nhq = h_next / group;
-                const uint16_t *src = which == 0 ? p.q + (tok * p.H_qk + nhq) * KD
-                                    : which == 1 ? p.k + (tok * p.H_qk + nhq) * KD
-                                    : which == 2 ? p.graw + (tok * p.H_v + h_next) * KD
-                                                 : p.v + (tok * p.H_v + h_next) * KD;
-                prefetch_line_l2(src);
-                prefetch_line_l2(src + 64);
-            }
-        }
 
         // ---- 2. channel slices.  Per slice: gate of the thread's rows (softplus, prefix sum), exchange
         //         of segment sums, then every operand of the slice.  q and k enter the operands
@@ -1294,23 +1280,6 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
             const size_t row = ((size_t)cd.tok + tid) * p.H_v + h;
             graw_r = bf16_to_f(p.graw[row]);
             b_r = bf16_to_f(p.b[row]);
-        }
-        // pull the next item's rows into L2
-        {
-            const long long nitem = item + gridDim.x;
-            if (nitem < n_items) {
-                const int nchunk = (int)(nitem / p.H_v), nh = (int)(nitem % p.H_v);
-                const ChunkDesc nd = p.chunks[nchunk];
-                const int r = tid & 63, which = tid >> 6;
-                if (which < 3 && r < nd.len) {
-                    const size_t tok = (size_t)nd.tok + r;
-                    const uint16_t *src = which == 0 ? p.q + (tok * p.H_qk + nh / group) * KD
-                                        : which == 1 ? p.k + (tok * p.H_qk + nh / group) * KD
-                                                     : p.v + (tok * p.H_v + nh) * KD;
-                    prefetch_line_l2(src);
-                    prefetch_line_l2(src + 64);
-                }
-            }
         }
         cp_async_wait<0>();
         // the previous item's bulk stores must be done reading shared memory (staging, P, tables)
