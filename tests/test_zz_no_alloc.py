@@ -90,3 +90,38 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     # launch (NULL data pointers, so a regression of the size check fails argument validation
     # instead of touching memory)
     assert _rc_for_size(lib, 2, 16384, 32) == kda.KDA_ERR_WORKSPACE
+
+
+def test_noalloc_replays_from_a_cuda_graph():
+    """One warm-up call (the array's device address), then the allocation-free forward captured
+    into a CUDA graph on a small varlen case; two replays on new inputs copied into the captured
+    tensors each equal kda_fwd on those inputs bit for bit."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_40_gb300 import kda
+    lens = [100, 37, 250, 63]
+    base = KI.make_inputs(1, sum(lens), 2, 4, seed=211, with_state=True, seqlens=lens)
+    d = to_dev(base)
+    args = (d["q"], d["k"], d["v"], d["graw"], d["b"], d["A_log"], d["scale"])
+    out = torch.empty((1, sum(lens), 4, 128), dtype=torch.bfloat16, device="cuda")
+    fin = torch.empty_like(d["initial_state"])
+    kda.kda_fwd_noalloc(*args, initial_state=d["initial_state"], cu_seqlens=d["cu_seqlens"], out=out,
+                        final_state=fin)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        kda.kda_fwd_noalloc(*args, initial_state=d["initial_state"], cu_seqlens=d["cu_seqlens"], out=out,
+                            final_state=fin)
+    for seed in (212, 213):
+        new = to_dev(KI.make_inputs(1, sum(lens), 2, 4, seed=seed, with_state=True, seqlens=lens))
+        for n in ("q", "k", "v", "graw", "b", "A_log", "initial_state"):
+            d[n].copy_(new[n])
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_fin = kda.kda_fwd(new["q"], new["k"], new["v"], new["graw"], new["b"], new["A_log"],
+                                       new["scale"], initial_state=new["initial_state"],
+                                       cu_seqlens=new["cu_seqlens"])
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out)
+        assert torch.equal(fin, ref_fin)
+    assert kda.kda_get_status() == 0
