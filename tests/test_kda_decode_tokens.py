@@ -88,3 +88,37 @@ def test_decode_tokens_rejects_token_count(Tq):
     with pytest.raises(kda.KdaError) as e:
         kda.kda_decode_tokens(q, q, q, q, b, torch.zeros(H, device="cuda"), 0.1, st)
     assert e.value.code == kda.KDA_ERR_INVALID_ARG
+
+
+def test_decode_steps_replay_from_a_cuda_graph():
+    """A serving loop captures its decode step once and replays it: kda_decode_step and
+    kda_decode_tokens captured into one CUDA graph (in place on their states) and replayed twice
+    equal the same calls made directly, bit for bit."""
+    from gated_delta_rule_40_gb300 import kda
+    d = KI.decode_inputs(B=8, H=8, H_qk=4, seed=540)
+    m = KI.make_inputs(8, 4, 4, 8, seed=541, with_state=True)
+    dd = {n: getattr(d, n).cuda() for n in ("q", "k", "v", "graw", "b", "A_log")}
+    md = {n: getattr(m, n).cuda() for n in ("q", "k", "v", "graw", "b", "A_log")}
+    st1, st2 = d.state.cuda(), m.initial_state.to(torch.bfloat16).cuda()
+    r1, r2 = st1.clone(), st2.clone()
+    o1 = torch.empty((8, 8, 128), dtype=torch.bfloat16, device="cuda")
+    o2 = torch.empty((8, 4, 8, 128), dtype=torch.bfloat16, device="cuda")
+
+    def step(a, b, oa, ob):
+        kda.kda_decode_step(dd["q"], dd["k"], dd["v"], dd["graw"], dd["b"], dd["A_log"], d.scale, a, out=oa)
+        kda.kda_decode_tokens(md["q"], md["k"], md["v"], md["graw"], md["b"], md["A_log"], m.scale, b, out=ob)
+
+    step(st1, st2, o1, o2)   # warm-up outside the capture
+    r1.copy_(st1)
+    r2.copy_(st2)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step(st1, st2, o1, o2)
+    ro1, ro2 = torch.empty_like(o1), torch.empty_like(o2)
+    for _ in range(2):
+        g.replay()
+        step(r1, r2, ro1, ro2)
+        torch.cuda.synchronize()
+        assert torch.equal(st1, r1) and torch.equal(st2, r2)
+        assert torch.equal(o1, ro1) and torch.equal(o2, ro2)
