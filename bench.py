@@ -436,17 +436,22 @@ def bench_link(dev, stream, host_in, host_out):
         d2h_ms = one(d2h, stream)
 
     def both():
+        # device time from an event on the launching stream to one after both copy streams
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        other.wait_stream(stream)
         with torch.cuda.stream(stream):
             h2d()
         with torch.cuda.stream(other):
             d2h()
-        other.synchronize()
-        stream.synchronize()
+        stream.wait_stream(other)
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b)
 
     both()
-    t0 = time.perf_counter()
-    both()
-    both_ms = (time.perf_counter() - t0) * 1e3
+    both_ms = both()
     return {"h2d_GBps": nbytes_in / (h2d_ms * 1e-3) / 1e9, "d2h_GBps": nbytes_out / (d2h_ms * 1e-3) / 1e9,
             "h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "concurrent_ms": both_ms,
             "note": "measured on the e2e call's own pinned buffers; the e2e step cannot be shorter than "
