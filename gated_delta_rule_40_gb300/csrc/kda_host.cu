@@ -30,8 +30,9 @@ cudaError_t ws_free(void *p, cudaStream_t stream);
 namespace {
 
 constexpr int kMaxDevices = 64;
-// At most kMaxPieces pieces of at least kMinPieceTokens tokens each: more pieces shorten the
-// exposed tail (the last piece's kernels and output copy) at the price of more launches.
+// Up to kMaxPieces equal pieces of at least kMinPieceTokens tokens each (the last one cut into
+// a half and two quarters when there are four or more): more pieces shorten the exposed tail
+// (the last piece's kernels and output copy) at the price of more launches.
 constexpr int kMaxPieces = 16;
 constexpr long long kMinPieceTokens = 2048;
 std::mutex g_stream_mutex;
@@ -77,12 +78,19 @@ extern "C" int kda_fwd_host(const kda_bf16_t *q, const kda_bf16_t *k, const kda_
     for (int i = 0; i < nseq; ++i)
         if (cu[i + 1] < cu[i]) return KDA_ERR_BAD_SEQLENS;
 
-    // pieces [t0, t1): about tokens / P each, cut at a chunk boundary of the sequence they fall in
+    // pieces [t0, t1): about tokens / P each, cut at a chunk boundary of the sequence they fall in;
+    // with four or more pieces the last one is cut again at 1/2 and 3/4, so that the work left
+    // once the last input has arrived (that piece's kernels and output copy) is a quarter piece
     const long long pmax = tokens / kMinPieceTokens;
     const int P = pmax < 1 ? 1 : (pmax > kMaxPieces ? kMaxPieces : (int)pmax);
+    std::vector<long long> targets;
+    for (int p = 1; p < P; ++p) targets.push_back(tokens * p / P);
+    if (P >= 4) {
+        targets.push_back((tokens * (2 * P - 1)) / (2 * P));
+        targets.push_back((tokens * (4 * P - 1)) / (4 * P));
+    }
     std::vector<int> cuts = {0};
-    for (int p = 1; p < P; ++p) {
-        const long long target = tokens * p / P;
+    for (const long long target : targets) {
         int s = 0;
         while (s < nseq && cu[s + 1] <= target) ++s;
         long long t = s < nseq ? cu[s] + ((target - cu[s] + CH / 2) / CH) * CH : tokens;

@@ -128,8 +128,9 @@ int kda_fwd_scalar_gate(const kda_bf16_t *q, const kda_bf16_t *k, const kda_bf16
  * tensor (cu_seqlens included) in host memory.  Pinned (page-locked) buffers let
  * the copies run at the host link's bandwidth; pageable ones work, more slowly.
  * The call copies the inputs to the device, runs the forward and copies out and
- * final_state back, in up to four pieces of consecutive tokens so that one
- * piece's copies overlap the previous piece's kernels (the link, not the
+ * final_state back, in up to eighteen pieces of consecutive tokens (at least
+ * 2048 tokens each, the last one split into a half and two quarters) so that
+ * one piece's copies overlap the previous piece's kernels (the link, not the
  * kernels, bounds such a call).  A sequence crossing a piece boundary is cut at
  * a chunk boundary and its state carried on the device, which is the chunking
  * and arithmetic of a single call.  cu_seqlens is checked on the host: a
