@@ -63,7 +63,21 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
         }
         return;
     }
-    for (int base = 0; base < nseq; base += PLAN_THREADS) {
+    if (!cu) {
+        // B sequences of T tokens: the tables in closed form (no scan of chunk counts)
+        const int nc = (int)(((long long)T + CH - 1) / CH);
+        for (int i = tid; i < nseq; i += PLAN_THREADS) {
+            SeqDesc sd;
+            sd.tok = i * T;
+            sd.len = T;
+            sd.chunk0 = i * nc;
+            sd.nchunk = nc;
+            seqs[i] = sd;
+        }
+        if (tid == 0) s_carry = nseq * nc;
+        __syncthreads();
+    }
+    for (int base = 0; cu && base < nseq; base += PLAN_THREADS) {
         const int i = base + tid;
         int len = 0, tok = 0;
         if (i < nseq) {
@@ -125,8 +139,11 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
             }
         }
     }
-    if (nseq <= LPT_MAX_SEQ) {
-        for (int i = tid; i < nseq; i += PLAN_THREADS) s_len[i] = cu ? cu[i + 1] - cu[i] : T;
+    if (!cu) {
+        // equal lengths: the order is the identity
+        for (int i = tid; i < nseq; i += PLAN_THREADS) order[i] = i;
+    } else if (nseq <= LPT_MAX_SEQ) {
+        for (int i = tid; i < nseq; i += PLAN_THREADS) s_len[i] = cu[i + 1] - cu[i];
         __syncthreads();
         for (int i = tid; i < nseq; i += PLAN_THREADS) {
             const int li = s_len[i];
