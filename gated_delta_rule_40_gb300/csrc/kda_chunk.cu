@@ -1365,12 +1365,15 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
             umma_commit(bar_ap);
         }
         if (tid < KD) gcs[tid] = reinterpret_cast<const float *>(sm + GD_SCR)[1];
-        // ---- 4. meanwhile: Qg = q exp(Gam_r) (bf16) and Kd^T = k exp(Gam_C - Gam_r) (tf32) straight
-        //         into the record (raw rows; the scan applies rq and rk).  Thread: row r, 32 channels.
+        // ---- 4. meanwhile: Qg = q exp(Gam_r) (bf16) straight into the record and Kd^T =
+        //         k exp(Gam_C - Gam_r) (tf32) into two 16 KiB staging halves in the record's layout
+        //         (rows r < 32 in the T region, r >= 32 behind the P image: neither is written
+        //         before the inversion), each stored by one bulk copy (raw rows; the scan applies rq
+        //         and rk).  Thread: row r, 32 channels.
         {
             const int r = tid & 63, g = tid >> 6;
             const float er = eg[r], ed = ex2(gam[CH - 1] - gam[r]);
-            unsigned char *const kd_r = rec + REC_KDT + (r >> 5) * 16384 + (r & 3) * 4;
+            unsigned char *const kd_r = sm + (r < 32 ? GD_T : GD_TP + 8192) + (r & 3) * 4;
             const int x4 = (r & 31) >> 2;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -1384,17 +1387,23 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
                     qg[e] = pack_bf16x2(bf16_lo(qa[e]) * er, bf16_hi(qa[e]) * er);
                     const int k0 = c + 2 * e;
                     // Kd^T element (k, r) of the record: k / 8 = c / 8, k % 8 = 2 e (+1)
-                    stg_hint_b32(kd_r + (k0 >> 3) * 1024 + (k0 & 7) * 128 + ((x4 ^ (k0 & 7)) << 4),
-                                 tf32_rn_bits(bf16_lo(ka[e]) * ed), pol_ef);
-                    stg_hint_b32(kd_r + (k0 >> 3) * 1024 + ((k0 + 1) & 7) * 128 + ((x4 ^ ((k0 + 1) & 7)) << 4),
-                                 tf32_rn_bits(bf16_hi(ka[e]) * ed), pol_ef);
+                    *reinterpret_cast<uint32_t *>(kd_r + (k0 >> 3) * 1024 + (k0 & 7) * 128 + ((x4 ^ (k0 & 7)) << 4)) =
+                        tf32_rn_bits(bf16_lo(ka[e]) * ed);
+                    *reinterpret_cast<uint32_t *>(kd_r + (k0 >> 3) * 1024 + ((k0 + 1) & 7) * 128 +
+                                                  ((x4 ^ ((k0 + 1) & 7)) << 4)) = tf32_rn_bits(bf16_hi(ka[e]) * ed);
                 }
                 stg_hint_v4(rec + REC_WQ + sw128_off(r, 2 * c, 2 * CH), make_uint4(qg[0], qg[1], qg[2], qg[3]), pol_ef);
             }
         }
+        fence_async_smem();   // the Kd^T staging, for the bulk copies below
         if (tid == 0 && !mbar_spin(bar_ap, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
         __syncthreads();
         tc_fence_after();
+        if (tid == 0) {
+            bulk_s2g_hint(rec + REC_KDT, sbase + GD_T, 16384, pol_ef);
+            bulk_s2g_hint(rec + REC_KDT + 16384, sbase + GD_TP + 8192, 16384, pol_ef);
+            bulk_commit();
+        }
         // the [K; Q] operand is free: V and K (MN-major) for the W / U MMAs
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -1442,6 +1451,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
         }
         fence_async_smem();
         tc_fence_before();
+        if (tid == 0) bulk_wait_read_all();   // the Kd^T staging is read before the inversion and T' reuse it
         __syncthreads();
         if (tid == 0) {
             bulk_s2g_hint(rec + REC_P, sbase + GD_PI, 8192, pol_ef);
