@@ -217,6 +217,7 @@ constexpr uint32_t IS_R2 = 69632;            // raw q / k / graw slices (two buf
 constexpr uint32_t IS_R3 = 94208;            // per-slice exchange of gate sums; then T'_hi, T'_lo
 constexpr uint32_t IS_XW = IS_R3;            // per-warp gate totals [8 warps][32 ch] fp32
 constexpr uint32_t IS_XG = IS_R3 + 1024;     // gate at each block's first row [4 blocks][32 ch] fp32
+constexpr uint32_t IS_QGS = IS_R3 + 2048;    // Qg of two slices (one 64-channel atom, 8 KiB) for a bulk store
 constexpr uint32_t IS_MISC = 110592;
 constexpr uint32_t IS_RV = IS_MISC;          // rq, rk, beta, qk [4][64] fp32
 constexpr uint32_t IS_GCS = IS_MISC + 1024;  // exp(Gam_C) [128]
@@ -236,6 +237,7 @@ constexpr uint32_t IS_TPL = IS_R3 + 8192;    // T'_lo
 constexpr uint32_t IS_WS = IS_R1;            // W half of the WQ image (2 x 8 KiB)
 constexpr uint32_t IS_US = IS_R1 + 16384;    // U image staging (2 x 64 x 68 fp32)
 static_assert(IS_PI + 8192 <= IS_R2 && IS_US + 2 * CH * 68 * 4 <= IS_R2, "R1 aliases overflow");
+static_assert(IS_XG + 512 <= IS_QGS && IS_QGS + 8192 <= IS_MISC && IS_QGS % 128 == 0, "Qg staging overflow");
 static_assert(IS_R2 + 2 * RAW_SLICE <= IS_R3 && IS_XG + 512 <= IS_MISC && IS_TPL + 8192 <= IS_MISC,
               "R2 / R3 overflow");
 static_assert(IS_R2 % 1024 == 0 && RAW_SLICE % 512 == 0 && RAW_T % 512 == 0, "TMA swizzle alignment");
@@ -443,8 +445,10 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                 *reinterpret_cast<float2 *>(xw + warp * SL + cp) = make_float2(tseg.x + tother.x, tseg.y + tother.y);
                 if (!wodd) *reinterpret_cast<float2 *>(xg + blk * SL + cp) = G[0];
             }
-            // the previous slice's MMAs must be done with ROWS / COLS before they are rewritten
+            // the previous slice's MMAs must be done with ROWS / COLS before they are rewritten, and
+            // from slice 2 on the bulk store of the first two slices' Qg (thread 64's) with its staging
             if (tid == 0 && sl > 0 && !mbar_wait(bar_ap, (uint32_t)(sl - 1) & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
+            if (tid == 64 && sl == 2) bulk_wait_read_all();
             __syncthreads();
             // block boundaries M_b = Gam at the end of block b - 1 (M_0 = 0, M_4 = Gam_C)
             float2 Mb, Mb1, Wlo;
@@ -498,7 +502,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             // moves by 32 rows (4 KiB) per slice.
             const uint32_t x64 = 64u * (uint32_t)(sl & 1);
             unsigned char *const kgs = sm + IS_KG + 8192 * (sl >> 1);
-            unsigned char *const qgs = rec + REC_WQ + 16384 * (sl >> 1);
+            unsigned char *const qgs = sm + IS_QGS;
             unsigned char *const kds = rec + REC_KDT + (r0 >> 5) * 16384 + 4096 * sl;
             const float2 nhm = make_float2(-hm.x, -hm.y);
             auto operands = [&](auto blkc) {
@@ -539,10 +543,10 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                     }
                     kdv[i] = __fmul2_rn(hk, ea);
                     // Kg (bf16) into the MN-major B operand of the W MMA (element (k = c0 + cp, j = r)),
-                    // Qg (bf16) straight into rows 0..63 of the record's WQ image
+                    // Qg (bf16) into the staging of rows 0..63 of one atom of the record's WQ image
                     const float2 kg = __fmul2_rn(fk, eb), qg = __fmul2_rn(fq, eb);
                     *reinterpret_cast<uint32_t *>(kgs + (kgo[i] ^ x64)) = pack_bf16x2(kg.x, kg.y);
-                    stg_hint_b32(qgs + (kgo[i] ^ x64), pack_bf16x2(qg.x, qg.y), pol_ef);
+                    *reinterpret_cast<uint32_t *>(qgs + (kgo[i] ^ x64)) = pack_bf16x2(qg.x, qg.y);
                     // partial row sums of q.q, k.k, q.k over this thread's two channels
                     nq[i] = fmaf(qv.x, qv.x, fmaf(qv.y, qv.y, nq[i]));
                     nk[i] = fmaf(kv.x, kv.x, fmaf(kv.y, kv.y, nk[i]));
@@ -575,6 +579,11 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                     umma_tf32(offd ? t_off : t_diag, umma_desc(arow + ks * 32, 16, 1024), umma_desc(bcol + ks * 32, 16, 1024),
                               id, (sl > 0 || ks > 0) ? 1u : 0u);
                 umma_commit(bar_ap);
+            }
+            if (tid == 64 && (sl & 1)) {
+                // Qg of slices sl - 1 and sl: rows 0..63 of one 64-channel atom of the WQ image
+                bulk_s2g_hint(rec + REC_WQ + 16384 * (sl >> 1), sbase + IS_QGS, 8192, pol_ef);
+                bulk_commit();
             }
             if (tid == 32) {
                 // raw buffer sl % 2 is free (every thread read it before the barrier): slice sl + 2,
@@ -699,6 +708,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         }
         fence_async_smem();
         tc_fence_before();
+        if (tid == 64) bulk_wait_read_all();   // the Qg staging is read before T' reuses R3
         __syncthreads();
         if (tid == 0) {
             bulk_s2g_hint(rec + REC_P, sbase + IS_PI, 8192, pol_ef);
@@ -833,7 +843,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
             bulk_commit();
         }
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0 || tid == 64) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
