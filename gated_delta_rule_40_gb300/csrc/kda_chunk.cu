@@ -171,6 +171,9 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
 //   KDT Kd^T: rows k = 0..127 x 64 (r), tf32                      (32 KiB)
 //   U   [V block 0 | V block 1], each [64 v][68] fp32 (64 r + 4 pad)  (34 KiB)
 //   GC  exp(Gam_C) per channel, fp32                              (512 B)
+//   RN  rq [64], rk [64], fp32                                     (512 B)
+// The scalar-gate kernel leaves KDT unwritten and stores f_r = rk_r exp(Gam_C - Gam_r) in the
+// rk slot (its scan reads the raw key rows instead).
 constexpr uint32_t REC_WQ = 0, REC_P = 32768, REC_KDT = 40960, REC_U = 73728, REC_GC = 108544, REC_RN = 109056;
 constexpr uint32_t REC_U_BLOCK = 64 * 68 * 4;   // 17408 B per V block
 constexpr uint32_t REC_BYTES = 109568;
@@ -895,14 +898,21 @@ struct ScanParams {
     const float *init;
     float *fin;
     uint16_t *out;
-    int H_v, nseq;
+    int H_qk, H_v, nseq;
     int h0, Hw;   // value-head window [h0, h0 + Hw); records are [chunk][Hw]
     int state_bf16;   // init / fin hold bf16 values (the recurrence itself stays fp32)
 };
 
 enum { BAR_WQ0 = 0, BAR_WQ1, BAR_PK0, BAR_PK1, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MMA2, BAR_SBR, BAR_DTR };
 
-__global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p) {
+// SG (scalar gate): the records carry no Kd^T.  Kd = diag(rk exp(Gam_C - Gam_r)) K is then a row
+// scaling of the raw keys, so the state update reads the key rows of the input (TMA map tk, one
+// 64-row tile per chunk) and takes the row factors f_r = rk_r exp(Gam_C - Gam_r) (the record's
+// rk slot) on Delta instead:  Z = K^T (diag(f) Delta^T)^T, with K exact in bf16 and f Delta split
+// into bf16 hi + lo (about 16 bits).  The general gate uses the record's tf32 Kd^T; tk is unused.
+template <bool SG>
+__global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_constant__ CUtensorMap tk,
+                                                             const ScanParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<1024>(smem_raw);
     grid_dep_wait();   // the chunk records of the intra-chunk kernel
@@ -954,9 +964,19 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
             auto issue_pk = [&](int c) {
                 const unsigned char *r = rec_of(c);
                 const uint32_t b = bar + 8 * (BAR_PK0 + (c & 1));
-                mbar_expect_tx(b, 8192 + 32768);
-                bulk_g2s(sbase + SS_P + (c & 1) * 8192, r + REC_P, 8192, b);
-                bulk_g2s(sbase + SS_KDT + (c & 1) * 32768, r + REC_KDT, 32768, b);
+                if constexpr (SG) {
+                    // P and the chunk's raw key rows (two 64-channel boxes, 128-byte swizzle: the
+                    // MN-major A operand of the state update, M = k)
+                    const int hq = h / (p.H_v / p.H_qk), row = sd.tok + c * CH;
+                    mbar_expect_tx(b, 8192 + 16384);
+                    bulk_g2s(sbase + SS_P + (c & 1) * 8192, r + REC_P, 8192, b);
+                    tma_load_3d(sbase + SS_KDT + (c & 1) * 32768, &tk, 0, hq, row, b);
+                    tma_load_3d(sbase + SS_KDT + (c & 1) * 32768 + 8192, &tk, 64, hq, row, b);
+                } else {
+                    mbar_expect_tx(b, 8192 + 32768);
+                    bulk_g2s(sbase + SS_P + (c & 1) * 8192, r + REC_P, 8192, b);
+                    bulk_g2s(sbase + SS_KDT + (c & 1) * 32768, r + REC_KDT, 32768, b);
+                }
             };
             auto issue_u = [&](int c) {
                 const unsigned char *r = rec_of(c);
@@ -966,6 +986,7 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
             };
             const uint32_t id1 = idesc_bf16(64, 128) | (1u << 15);   // A (S) MN-major
             const uint32_t id2 = idesc_bf16(64, 64), id3 = idesc_tf32(128, VB);
+            const uint32_t id3s = idesc_bf16(128, VB) | (1u << 15);   // A (raw K) MN-major
             if (n > 0) {
                 issue_wq(0);
                 issue_pk(0);
@@ -993,18 +1014,45 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                 }
                 if (c + 2 < n) {
                     const unsigned char *r2 = rec_of(c + 2);
-                    prefetch_l2(r2 + REC_WQ, 32768 + 8192 + 32768);
+                    prefetch_l2(r2 + REC_WQ, SG ? 32768 + 8192 : 32768 + 8192 + 32768);
+                    if constexpr (SG) {
+                        const int hq = h / (p.H_v / p.H_qk), row = sd.tok + (c + 2) * CH;
+                        tma_prefetch_3d(&tk, 0, hq, row);
+                        tma_prefetch_3d(&tk, 64, hq, row);
+                    }
                     prefetch_l2(r2 + REC_U + vb * REC_U_BLOCK, REC_U_BLOCK);
                     prefetch_l2(r2 + REC_GC, 1024);
                 }
                 if (!mbar_wait(bar + 8 * BAR_DTR, c & 1)) { fail(); break; }
                 if (!mbar_wait(bar + 8 * (BAR_PK0 + b), pp)) { fail(); break; }
-                tc_fence_after();
+                if constexpr (SG) {
+                    const int lenc = min(CH, sd.len - c * CH);
+                    if (lenc < CH) {
+                        // key rows past the chunk's length belong to the next sequence: zero them, so
+                        // that they contribute exact zeros whatever they hold (their f Delta rows are 0)
+                        unsigned char *kt = sm + SS_KDT + b * 32768;
+                        for (int i = lenc * 8; i < CH * 8; ++i) {
+                            *reinterpret_cast<uint4 *>(kt + 16 * i) = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(kt + 8192 + 16 * i) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_async_smem();
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int ks = 0; ks < CH / 8; ++ks) {
-                    const int kb = ks * 32;
-                    umma_tf32(tZ, umma_desc(sbase + SS_KDT + b * 32768 + (kb >> 7) * 16384 + (kb & 127), 16, 1024),
-                              umma_desc(sbase + SS_DT + (kb >> 7) * 8192 + (kb & 127), 16, 1024), id3, ks > 0);
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int ks = 0; ks < CH / 16; ++ks)
+                            umma_bf16(tZ, umma_desc(sbase + SS_KDT + b * 32768 + ks * 2048, 8192, 1024),
+                                      umma_desc(sbase + SS_DT + part * 8192 + ks * 32, 16, 1024), id3s,
+                                      (part > 0 || ks > 0) ? 1u : 0u);
+                } else {
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < CH / 8; ++ks) {
+                        const int kb = ks * 32;
+                        umma_tf32(tZ, umma_desc(sbase + SS_KDT + b * 32768 + (kb >> 7) * 16384 + (kb & 127), 16, 1024),
+                                  umma_desc(sbase + SS_DT + (kb >> 7) * 8192 + (kb & 127), 16, 1024), id3, ks > 0);
+                    }
                 }
                 umma_commit(bar + 8 * BAR_MMA3);
 #pragma unroll
@@ -1101,7 +1149,8 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                 tmem_wait_ld();
                 if (vact) {
                     const float *urow = reinterpret_cast<const float *>(sm + SS_U) + vme * 68 + 32 * vhalf;
-                    // Kd in the record is unnormalised: the state update takes Delta_r rk_r
+                    // Kd in the record is unnormalised: the state update takes Delta_r rk_r (scalar gate:
+                    // Delta_r f_r, the record's rk slot holding f_r = rk_r exp(Gam_C - Gam_r))
                     const float *rkr = reinterpret_cast<const float *>(sm + SS_GC) + 192 + 32 * vhalf;
 #pragma unroll
                     for (int jj = 0; jj < 32; jj += 8) {
@@ -1114,12 +1163,27 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const ScanParams p)
                         const float d6 = ub.z - __uint_as_float(ys[jj + 6]), d7 = ub.w - __uint_as_float(ys[jj + 7]);
                         const float4 ka = *reinterpret_cast<const float4 *>(rkr + jj);
                         const float4 kb = *reinterpret_cast<const float4 *>(rkr + jj + 4);
-                        *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j, VB)) =
-                            make_uint4(tf32_rn_bits(d0 * ka.x), tf32_rn_bits(d1 * ka.y), tf32_rn_bits(d2 * ka.z),
-                                       tf32_rn_bits(d3 * ka.w));
-                        *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j + 16, VB)) =
-                            make_uint4(tf32_rn_bits(d4 * kb.x), tf32_rn_bits(d5 * kb.y), tf32_rn_bits(d6 * kb.z),
-                                       tf32_rn_bits(d7 * kb.w));
+                        if constexpr (SG) {
+                            // f Delta as bf16 hi (SS_DT) + lo (SS_DT + 8 KiB): 64 rows (v) x 64 (r), K-major
+                            const float e[8] = {d0 * ka.x, d1 * ka.y, d2 * ka.z, d3 * ka.w,
+                                                d4 * kb.x, d5 * kb.y, d6 * kb.z, d7 * kb.w};
+                            uint32_t hi[4], lo[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                hi[i] = pack_bf16x2(e[2 * i], e[2 * i + 1]);
+                                lo[i] = pack_bf16x2(e[2 * i] - bf16_lo(hi[i]), e[2 * i + 1] - bf16_hi(hi[i]));
+                            }
+                            const uint32_t off = sw128_off(vme, 2 * j, VB);
+                            *reinterpret_cast<uint4 *>(sm + SS_DT + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *reinterpret_cast<uint4 *>(sm + SS_DT + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        } else {
+                            *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j, VB)) =
+                                make_uint4(tf32_rn_bits(d0 * ka.x), tf32_rn_bits(d1 * ka.y), tf32_rn_bits(d2 * ka.z),
+                                           tf32_rn_bits(d3 * ka.w));
+                            *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j + 16, VB)) =
+                                make_uint4(tf32_rn_bits(d4 * kb.x), tf32_rn_bits(d5 * kb.y), tf32_rn_bits(d6 * kb.z),
+                                           tf32_rn_bits(d7 * kb.w));
+                        }
                         *reinterpret_cast<uint4 *>(sm + SS_DTB + sw128_off(vme, 2 * j, VB)) =
                             make_uint4(pack_bf16x2(d0, d1), pack_bf16x2(d2, d3), pack_bf16x2(d4, d5),
                                        pack_bf16x2(d6, d7));
@@ -1215,8 +1279,10 @@ __device__ __forceinline__ void store_wu(unsigned char *ws, unsigned char *us, u
 //   A[r,j] = beta_r rk_r rk_j exp(Gam_r - Gam_j) (k_r . k_j),   P[r,j] = rq_r rk_j exp(Gam_r - Gam_j) (q_r . k_j)
 // come from one bf16 MMA of the raw inputs (exact products, fp32 accumulate)
 // followed by a 64 x 64 decay mask, and W = T diag(beta rk exp(Gam)) K takes the
-// staged raw K as its operand.  The record is the general kernel's (raw Qg, Kd
-// and P with the row scales rq, rk), so the same scan follows.
+// staged raw K as its operand.  The record is the general kernel's without Kd^T:
+// Kd = diag(f) K with f_r = rk_r exp(Gam_C - Gam_r) is a row scaling of the raw keys,
+// so the record carries f in the rk slot and the scan's scalar-gate variant reads
+// the key rows of the input itself.
 // Persistent CTAs of 8 warps, two per SM, one (chunk, value head) item at a time.
 // =====================================================================
 constexpr uint32_t GD_QK = 0;               // [K rows 0..63; Q rows 64..127] K-major bf16 (2 x 16 KiB atoms);
@@ -1317,7 +1383,7 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
         //         its prefix sum over the chunk (warps 0, 1: one row per lane)
         {
             const int r = tid >> 2, part = tid & 3;
-            float sq = 0.f, sk = 0.f, sqk = 0.f;
+            float sq = 0.f, sk = 0.f;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int ub = 16 * (4 * part + u);
@@ -1329,19 +1395,16 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
                     const float k0 = bf16_lo(ka[e]), k1 = bf16_hi(ka[e]), q0 = bf16_lo(qa[e]), q1 = bf16_hi(qa[e]);
                     sq = fmaf(q0, q0, fmaf(q1, q1, sq));
                     sk = fmaf(k0, k0, fmaf(k1, k1, sk));
-                    sqk = fmaf(q0, k0, fmaf(q1, k1, sqk));
                 }
             }
 #pragma unroll
             for (int o = 1; o < 4; o <<= 1) {
                 sq += __shfl_xor_sync(0xffffffffu, sq, o);
                 sk += __shfl_xor_sync(0xffffffffu, sk, o);
-                sqk += __shfl_xor_sync(0xffffffffu, sqk, o);
             }
             if (part == 0) {
                 rv[RV_RQ + r] = p.scale * rsqrtf(sq + L2_EPS);
                 rv[RV_RK + r] = rsqrtf(sk + L2_EPS);
-                rv[RV_QK + r] = sqk;
             }
         }
         if (warp < 2) {
@@ -1375,45 +1438,27 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
             umma_commit(bar_ap);
         }
         if (tid < KD) gcs[tid] = reinterpret_cast<const float *>(sm + GD_SCR)[1];
-        // ---- 4. meanwhile: Qg = q exp(Gam_r) (bf16) straight into the record and Kd^T =
-        //         k exp(Gam_C - Gam_r) (tf32) into two 16 KiB staging halves in the record's layout
-        //         (rows r < 32 in the T region, r >= 32 behind the P image: neither is written
-        //         before the inversion), each stored by one bulk copy (raw rows; the scan applies rq
-        //         and rk).  Thread: row r, 32 channels.
+        // ---- 4. meanwhile: Qg = q exp(Gam_r) (bf16, raw rows; the scan applies rq) straight into the
+        //         record, and the state update's row factors f_r = rk_r exp(Gam_C - Gam_r) (0 past len)
+        //         into the slot of the unused raw q.k.  Thread: row r, 32 channels.
         {
             const int r = tid & 63, g = tid >> 6;
-            const float er = eg[r], ed = ex2(gam[CH - 1] - gam[r]);
-            unsigned char *const kd_r = sm + (r < 32 ? GD_T : GD_TP + 8192) + (r & 3) * 4;
-            const int x4 = (r & 31) >> 2;
+            const float er = eg[r];
+            if (g == 0) rv[RV_QK + r] = r < len ? rv[RV_RK + r] * ex2(gam[CH - 1] - gam[r]) : 0.f;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int c = 32 * g + 8 * u;   // channels c .. c + 7
                 const uint4 qw = *reinterpret_cast<const uint4 *>(sm + GD_QK + sw128_off(64 + r, 2 * c, 2 * CH));
-                const uint4 kw = *reinterpret_cast<const uint4 *>(sm + GD_QK + sw128_off(r, 2 * c, 2 * CH));
-                const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w}, ka[4] = {kw.x, kw.y, kw.z, kw.w};
+                const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w};
                 uint32_t qg[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    qg[e] = pack_bf16x2(bf16_lo(qa[e]) * er, bf16_hi(qa[e]) * er);
-                    const int k0 = c + 2 * e;
-                    // Kd^T element (k, r) of the record: k / 8 = c / 8, k % 8 = 2 e (+1)
-                    *reinterpret_cast<uint32_t *>(kd_r + (k0 >> 3) * 1024 + (k0 & 7) * 128 + ((x4 ^ (k0 & 7)) << 4)) =
-                        tf32_rn_bits(bf16_lo(ka[e]) * ed);
-                    *reinterpret_cast<uint32_t *>(kd_r + (k0 >> 3) * 1024 + ((k0 + 1) & 7) * 128 +
-                                                  ((x4 ^ ((k0 + 1) & 7)) << 4)) = tf32_rn_bits(bf16_hi(ka[e]) * ed);
-                }
+                for (int e = 0; e < 4; ++e) qg[e] = pack_bf16x2(bf16_lo(qa[e]) * er, bf16_hi(qa[e]) * er);
                 stg_hint_v4(rec + REC_WQ + sw128_off(r, 2 * c, 2 * CH), make_uint4(qg[0], qg[1], qg[2], qg[3]), pol_ef);
             }
         }
-        fence_async_smem();   // the Kd^T staging, for the bulk copies below
         if (tid == 0 && !mbar_spin(bar_ap, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {
-            bulk_s2g_hint(rec + REC_KDT, sbase + GD_T, 16384, pol_ef);
-            bulk_s2g_hint(rec + REC_KDT + 16384, sbase + GD_TP + 8192, 16384, pol_ef);
-            bulk_commit();
-        }
         // the [K; Q] operand is free: V and K (MN-major) for the W / U MMAs
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -1461,12 +1506,12 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
         }
         fence_async_smem();
         tc_fence_before();
-        if (tid == 0) bulk_wait_read_all();   // the Kd^T staging is read before the inversion and T' reuse it
         __syncthreads();
         if (tid == 0) {
             bulk_s2g_hint(rec + REC_P, sbase + GD_PI, 8192, pol_ef);
             bulk_s2g_hint(rec + REC_GC, sbase + GD_GCS, 512, pol_ef);
-            bulk_s2g_hint(rec + REC_RN, sbase + GD_RV, 512, pol_ef);
+            bulk_s2g_hint(rec + REC_RN, sbase + GD_RV + 4 * RV_RQ, 256, pol_ef);         // rq
+            bulk_s2g_hint(rec + REC_RN + 256, sbase + GD_RV + 4 * RV_QK, 256, pol_ef);   // f, in the rk slot
             bulk_commit();
         }
 
@@ -1624,7 +1669,7 @@ static cudaError_t launch_fwd_impl(const uint16_t *q, const uint16_t *k, const u
         cudaError_t e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)IS_BYTES);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS_BYTES);
+        e = cudaFuncSetAttribute(scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS_BYTES);
         if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaSuccess;
@@ -1665,11 +1710,13 @@ static cudaError_t launch_fwd_impl(const uint16_t *q, const uint16_t *k, const u
         ScanParams sp;
         sp.rec = ws.rec;
         sp.seqs = ws.seqs; sp.order = ws.order; sp.hdr = ws.hdr;
-        sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = h0; sp.Hw = Hw;
+        sp.init = init; sp.fin = fin; sp.out = out; sp.H_qk = H_qk; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = h0;
+        sp.Hw = Hw;
         sp.state_bf16 = state_bf16 ? 1 : 0;
         const long long nblk = (long long)nseq * Hw * 2;
-        if ((e = launch_dependent(scan_kernel, dim3((unsigned)nblk), dim3(SC_THREADS), SS_BYTES, stream, sp)) !=
-            cudaSuccess)
+        const CUtensorMap unused{};   // the general gate's state update reads Kd^T from the records
+        if ((e = launch_dependent(scan_kernel<false>, dim3((unsigned)nblk), dim3(SC_THREADS), SS_BYTES, stream, unused,
+                                  sp)) != cudaSuccess)
             return e;
         ++*launches;
         timing_mark("scan_kernel", stream);
@@ -1691,7 +1738,7 @@ cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const u
     *launches = 0;
     cudaError_t e = cudaFuncSetAttribute(intra_gdn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GD_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS_BYTES);
+    e = cudaFuncSetAttribute(scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS_BYTES);
     if (e != cudaSuccess) return e;
     timing_begin(stream);
     plan_kernel<<<1, PLAN_THREADS, 0, stream>>>(cu, N, B, T, ws.seqs, ws.chunks, ws.order, ws.hdr, nck);
@@ -1716,10 +1763,16 @@ cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const u
         ScanParams sp;
         sp.rec = ws.rec;
         sp.seqs = ws.seqs; sp.order = ws.order; sp.hdr = ws.hdr;
-        sp.init = init; sp.fin = fin; sp.out = out; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = 0; sp.Hw = H_v;
+        sp.init = init; sp.fin = fin; sp.out = out; sp.H_qk = H_qk; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = 0;
+        sp.Hw = H_v;
         sp.state_bf16 = 0;
-        if ((e = launch_dependent(scan_kernel, dim3((unsigned)((long long)nseq * H_v * 2)), dim3(SC_THREADS),
-                                  SS_BYTES, stream, sp)) != cudaSuccess)
+        // the state update's raw key rows: 64 channels x 64 rows per box, 128-byte swizzle
+        CUtensorMap mk{};
+        const long long rows = (long long)B * T;
+        if (rows > 0 && (e = tma_map_rows_heads(&mk, k, rows, H_qk, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return e;
+        if ((e = launch_dependent(scan_kernel<true>, dim3((unsigned)((long long)nseq * H_v * 2)), dim3(SC_THREADS),
+                                  SS_BYTES, stream, mk, sp)) != cudaSuccess)
             return e;
         ++*launches;
         timing_mark("scan_kernel", stream);

@@ -20,6 +20,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Prefetch of one box of a tiled 3-D tensor into L2 (no shared memory, no completion tracking)
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // Tiled 3-D store of one box from shared memory (completion tracked by the issuing thread's bulk
 // groups: cp.async.bulk.commit_group / wait_group).  The shared-memory writes it reads must be
 // made visible to the async proxy (fence.proxy.async) and ordered before it by a barrier.
