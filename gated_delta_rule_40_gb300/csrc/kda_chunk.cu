@@ -172,8 +172,9 @@ __global__ __launch_bounds__(PLAN_THREADS) void plan_kernel(const int32_t *__res
 //   U   [V block 0 | V block 1], each [64 v][68] fp32 (64 r + 4 pad)  (34 KiB)
 //   GC  exp(Gam_C) per channel, fp32                              (512 B)
 //   RN  rq [64], rk [64], fp32                                     (512 B)
-// The scalar-gate kernel leaves KDT unwritten and stores f_r = rk_r exp(Gam_C - Gam_r) in the
-// rk slot (its scan reads the raw key rows instead).
+// The scalar-gate kernel leaves KDT and the Qg rows of WQ unwritten, stores f_r = rk_r
+// exp(Gam_C - Gam_r) in the rk slot, rq_r exp(Gam_r) in entries 64..127 of GC and P times rq
+// (its scan reads the raw key and query rows instead).
 constexpr uint32_t REC_WQ = 0, REC_P = 32768, REC_KDT = 40960, REC_U = 73728, REC_GC = 108544, REC_RN = 109056;
 constexpr uint32_t REC_U_BLOCK = 64 * 68 * 4;   // 17408 B per V block
 constexpr uint32_t REC_BYTES = 109568;
@@ -885,10 +886,11 @@ constexpr uint32_t SS_U = 188416;      // 17 KiB      U block, fp32 [64 v][68]
 constexpr uint32_t SS_OS = 205824;     // 8 KiB       output transpose, bf16 [64 r][64 v]
 constexpr uint32_t SS_GC = 214016;     // 1 KiB       exp(Gam_C) [128], then rq [64], rk [64] (record order)
 constexpr uint32_t SS_RQ = 215040;     // 256 B       rq of the chunk whose output is emitted next
-constexpr uint32_t SS_BAR = 215296;    // mbarriers
-constexpr uint32_t SS_SLOT = 215424;   // TMEM address slot
-constexpr uint32_t SS_FLAG = 215428;   // abort flag
-constexpr uint32_t SS_BYTES = 215488 + 1024;   // + alignment slack
+constexpr uint32_t SS_RQE = 215296;    // 256 B       scalar gate: rq exp(Gam_r) of that chunk
+constexpr uint32_t SS_BAR = 215552;    // mbarriers
+constexpr uint32_t SS_SLOT = 215680;   // TMEM address slot
+constexpr uint32_t SS_FLAG = 215684;   // abort flag
+constexpr uint32_t SS_BYTES = 215744 + 1024;   // + alignment slack
 
 struct ScanParams {
     const unsigned char *rec;
@@ -905,13 +907,19 @@ struct ScanParams {
 
 enum { BAR_WQ0 = 0, BAR_WQ1, BAR_PK0, BAR_PK1, BAR_U, BAR_MMA1, BAR_MMA3, BAR_MMA2, BAR_SBR, BAR_DTR };
 
-// SG (scalar gate): the records carry no Kd^T.  Kd = diag(rk exp(Gam_C - Gam_r)) K is then a row
-// scaling of the raw keys, so the state update reads the key rows of the input (TMA map tk, one
-// 64-row tile per chunk) and takes the row factors f_r = rk_r exp(Gam_C - Gam_r) (the record's
-// rk slot) on Delta instead:  Z = K^T (diag(f) Delta^T)^T, with K exact in bf16 and f Delta split
-// into bf16 hi + lo (about 16 bits).  The general gate uses the record's tf32 Kd^T; tk is unused.
+// SG (scalar gate): the records carry neither Kd^T nor Qg, both row scalings of raw inputs.
+//   Kd = diag(f) K, f_r = rk_r exp(Gam_C - Gam_r) (the record's rk slot): the state update reads
+//     the chunk's key rows from the input (TMA map tk) and takes f on Delta instead,
+//     Z = K^T (diag(f) Delta^T)^T, with K exact in bf16 and f Delta split into bf16 hi + lo.
+//   Qg = diag(exp(Gam_r)) Q: MMA1's B operand takes the raw query rows (TMA map tq) in place of
+//     Qg, and P Delta accumulates in its own TMEM columns (the record's P carries rq), so that
+//     the output is O[r] = rq_r exp(Gam_r) (Q S^T)[r] + (P Delta)[r]; exp(Gam_C) is
+//     channel-independent, so the record's exp(Gam_C) row keeps it in entries 0..63 and
+//     rq_r exp(Gam_r) in 64..127.
+// The general gate uses the record's Qg and tf32 Kd^T; tk and tq are unused.
 template <bool SG>
 __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_constant__ CUtensorMap tk,
+                                                             const __grid_constant__ CUtensorMap tq,
                                                              const ScanParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = aligned_smem<1024>(smem_raw);
@@ -946,6 +954,7 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + SS_SLOT);
     const uint32_t tZ = tmem + 256;   // 64 columns, lanes = k
+    const uint32_t tP0 = tmem + 320;  // scalar gate: P Delta, two buffers of 64 columns
 
     auto rec_of = [&](int c) { return p.rec + (((size_t)sd.chunk0 + c) * p.Hw + (h - p.h0)) * REC_BYTES; };
     auto fail = [&]() {
@@ -957,9 +966,19 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
         // ------------------------------------------------------------ issuer
         if (lane == 0) {
             auto issue_wq = [&](int c) {
-                const uint32_t b = bar + 8 * (BAR_WQ0 + (c & 1));
+                const uint32_t b = bar + 8 * (BAR_WQ0 + (c & 1)), dst = sbase + SS_WQ + (c & 1) * 32768;
                 mbar_expect_tx(b, 32768);
-                bulk_g2s(sbase + SS_WQ + (c & 1) * 32768, rec_of(c) + REC_WQ, 32768, b);
+                if constexpr (SG) {
+                    // [Q; W]: the raw query rows (one 64-channel box per K atom) and the record's W
+                    const int hq = h / (p.H_v / p.H_qk), row = sd.tok + c * CH;
+                    const unsigned char *r = rec_of(c);
+                    tma_load_3d(dst, &tq, 0, hq, row, b);
+                    tma_load_3d(dst + 16384, &tq, 64, hq, row, b);
+                    bulk_g2s(dst + 8192, r + REC_WQ + 8192, 8192, b);
+                    bulk_g2s(dst + 16384 + 8192, r + REC_WQ + 16384 + 8192, 8192, b);
+                } else {
+                    bulk_g2s(dst, rec_of(c) + REC_WQ, 32768, b);
+                }
             };
             auto issue_pk = [&](int c) {
                 const unsigned char *r = rec_of(c);
@@ -1014,11 +1033,16 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
                 }
                 if (c + 2 < n) {
                     const unsigned char *r2 = rec_of(c + 2);
-                    prefetch_l2(r2 + REC_WQ, SG ? 32768 + 8192 : 32768 + 8192 + 32768);
                     if constexpr (SG) {
+                        prefetch_l2(r2 + REC_WQ + 8192, 8192);                // W, first K atom
+                        prefetch_l2(r2 + REC_WQ + 16384 + 8192, 8192 + 8192);  // W, second atom; P
                         const int hq = h / (p.H_v / p.H_qk), row = sd.tok + (c + 2) * CH;
                         tma_prefetch_3d(&tk, 0, hq, row);
                         tma_prefetch_3d(&tk, 64, hq, row);
+                        tma_prefetch_3d(&tq, 0, hq, row);
+                        tma_prefetch_3d(&tq, 64, hq, row);
+                    } else {
+                        prefetch_l2(r2 + REC_WQ, 32768 + 8192 + 32768);
                     }
                     prefetch_l2(r2 + REC_U + vb * REC_U_BLOCK, REC_U_BLOCK);
                     prefetch_l2(r2 + REC_GC, 1024);
@@ -1055,10 +1079,11 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
                     }
                 }
                 umma_commit(bar + 8 * BAR_MMA3);
+                // P Delta onto Qg S^T (general gate) or into its own accumulator (scalar gate)
 #pragma unroll
                 for (int ks = 0; ks < CH / 16; ++ks) {
-                    umma_bf16(tY, umma_desc(sbase + SS_DTB + ks * 32, 16, 1024),
-                              umma_desc(sbase + SS_P + b * 8192 + ks * 32, 16, 1024), id2, 1);
+                    umma_bf16(SG ? tP0 + b * 64 : tY, umma_desc(sbase + SS_DTB + ks * 32, 16, 1024),
+                              umma_desc(sbase + SS_P + b * 8192 + ks * 32, 16, 1024), id2, (SG && ks == 0) ? 0u : 1u);
                 }
                 umma_commit(bar + 8 * BAR_MMA2);
                 // the U buffer is free once Delta of chunk c is written (after the MMAs: off the chain)
@@ -1087,18 +1112,37 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
             const uint32_t tY = tmem + (cc & 1) * 128;
             uint32_t y0[32];
             tmem_ld32_nowait(tY + lane_off + 32 * vhalf, y0);
-            tmem_wait_ld();
             uint16_t *os = reinterpret_cast<uint16_t *>(sm + SS_OS);
-            if (vact) {
-                // the record's Qg and P carry 1 / rq_r: O[r][v] = rq_r Y^T[v][r]
-                const float *rq = reinterpret_cast<const float *>(sm + SS_RQ) + 32 * vhalf;
+            if constexpr (SG) {
+                // O[r][v] = rq_r exp(Gam_r) (Q S^T)^T[v][r] + (P Delta)^T[v][r]  (the record's P carries rq)
+                uint32_t y2[32];
+                tmem_ld32_nowait(tP0 + (cc & 1) * 64 + lane_off + 32 * vhalf, y2);
+                tmem_wait_ld();
+                const float *rqe = reinterpret_cast<const float *>(sm + SS_RQE) + 32 * vhalf;
+                if (vact) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 f = *reinterpret_cast<const float4 *>(rq + j);
-                    os[(32 * vhalf + j) * VB + vme] = f_to_bf16(__uint_as_float(y0[j]) * f.x);
-                    os[(32 * vhalf + j + 1) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 1]) * f.y);
-                    os[(32 * vhalf + j + 2) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 2]) * f.z);
-                    os[(32 * vhalf + j + 3) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 3]) * f.w);
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 fe = *reinterpret_cast<const float4 *>(rqe + j);
+                        const float fb[4] = {fe.x, fe.y, fe.z, fe.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            os[(32 * vhalf + j + i) * VB + vme] =
+                                f_to_bf16(fmaf(__uint_as_float(y0[j + i]), fb[i], __uint_as_float(y2[j + i])));
+                    }
+                }
+            } else {
+                tmem_wait_ld();
+                const float *rq = reinterpret_cast<const float *>(sm + SS_RQ) + 32 * vhalf;
+                if (vact) {
+                    // the record's Qg and P carry 1 / rq_r: O[r][v] = rq_r Y^T[v][r]
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 f = *reinterpret_cast<const float4 *>(rq + j);
+                        os[(32 * vhalf + j) * VB + vme] = f_to_bf16(__uint_as_float(y0[j]) * f.x);
+                        os[(32 * vhalf + j + 1) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 1]) * f.y);
+                        os[(32 * vhalf + j + 2) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 2]) * f.z);
+                        os[(32 * vhalf + j + 3) * VB + vme] = f_to_bf16(__uint_as_float(y0[j + 3]) * f.w);
+                    }
                 }
             }
             named_bar(1, SC_EPI);
@@ -1138,10 +1182,13 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
             // ---- Delta^T = U^T - (W S^T)^T, as tf32 (B of MMA3) and bf16 (A of MMA2)
             if (!mbar_spin(bar + 8 * BAR_MMA1, c & 1) || !mbar_spin(bar + 8 * BAR_U, c & 1)) fail();
             tc_fence_after();
-            const float g = reinterpret_cast<const float *>(sm + SS_GC)[kme];
-            // keep this chunk's rq for its output, emitted during the next chunk (the record area
-            // is reloaded before that)
-            if (tid < CH) reinterpret_cast<float *>(sm + SS_RQ)[tid] = reinterpret_cast<const float *>(sm + SS_GC)[128 + tid];
+            const float g = reinterpret_cast<const float *>(sm + SS_GC)[SG ? 0 : kme];
+            // keep this chunk's rq (and, scalar gate, rq exp(Gam_r)) for its output, emitted during
+            // the next chunk (the record area is reloaded before that)
+            if (tid < CH) {
+                reinterpret_cast<float *>(sm + SS_RQ)[tid] = reinterpret_cast<const float *>(sm + SS_GC)[128 + tid];
+                if (SG) reinterpret_cast<float *>(sm + SS_RQE)[tid] = reinterpret_cast<const float *>(sm + SS_GC)[64 + tid];
+            }
             {
                 // this thread: v = vme, r = 32 vhalf .. 32 vhalf + 31
                 uint32_t ys[32];
@@ -1279,10 +1326,11 @@ __device__ __forceinline__ void store_wu(unsigned char *ws, unsigned char *us, u
 //   A[r,j] = beta_r rk_r rk_j exp(Gam_r - Gam_j) (k_r . k_j),   P[r,j] = rq_r rk_j exp(Gam_r - Gam_j) (q_r . k_j)
 // come from one bf16 MMA of the raw inputs (exact products, fp32 accumulate)
 // followed by a 64 x 64 decay mask, and W = T diag(beta rk exp(Gam)) K takes the
-// staged raw K as its operand.  The record is the general kernel's without Kd^T:
-// Kd = diag(f) K with f_r = rk_r exp(Gam_C - Gam_r) is a row scaling of the raw keys,
-// so the record carries f in the rk slot and the scan's scalar-gate variant reads
-// the key rows of the input itself.
+// staged raw K as its operand.  The record is the general kernel's without Kd^T and
+// Qg, both row scalings of the raw inputs (Kd = diag(f) K with f_r = rk_r
+// exp(Gam_C - Gam_r), Qg = diag(exp(Gam_r)) Q): it carries f in the rk slot,
+// rq_r exp(Gam_r) in the upper half of the exp(Gam_C) row and P with its factor rq,
+// and the scan's scalar-gate variant reads the key and query rows of the input itself.
 // Persistent CTAs of 8 warps, two per SM, one (chunk, value head) item at a time.
 // =====================================================================
 constexpr uint32_t GD_QK = 0;               // [K rows 0..63; Q rows 64..127] K-major bf16 (2 x 16 KiB atoms);
@@ -1437,25 +1485,13 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
             }
             umma_commit(bar_ap);
         }
-        if (tid < KD) gcs[tid] = reinterpret_cast<const float *>(sm + GD_SCR)[1];
-        // ---- 4. meanwhile: Qg = q exp(Gam_r) (bf16, raw rows; the scan applies rq) straight into the
-        //         record, and the state update's row factors f_r = rk_r exp(Gam_C - Gam_r) (0 past len)
-        //         into the slot of the unused raw q.k.  Thread: row r, 32 channels.
-        {
-            const int r = tid & 63, g = tid >> 6;
-            const float er = eg[r];
-            if (g == 0) rv[RV_QK + r] = r < len ? rv[RV_RK + r] * ex2(gam[CH - 1] - gam[r]) : 0.f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = 32 * g + 8 * u;   // channels c .. c + 7
-                const uint4 qw = *reinterpret_cast<const uint4 *>(sm + GD_QK + sw128_off(64 + r, 2 * c, 2 * CH));
-                const uint32_t qa[4] = {qw.x, qw.y, qw.z, qw.w};
-                uint32_t qg[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) qg[e] = pack_bf16x2(bf16_lo(qa[e]) * er, bf16_hi(qa[e]) * er);
-                stg_hint_v4(rec + REC_WQ + sw128_off(r, 2 * c, 2 * CH), make_uint4(qg[0], qg[1], qg[2], qg[3]), pol_ef);
-            }
-        }
+        // ---- 4. meanwhile, the scan's row factors (Qg and Kd are row scalings of the raw q and k,
+        //         which the scan reads itself): the record's exp(Gam_C) row holds exp(Gam_C) in entries
+        //         0..63 and rq_r exp(Gam_r) in 64..127; f_r = rk_r exp(Gam_C - Gam_r) (0 past len) goes
+        //         to the slot of the raw q.k (unused here), stored in the record's rk slot
+        if (tid < CH) gcs[tid] = reinterpret_cast<const float *>(sm + GD_SCR)[1];
+        else if (tid < 2 * CH) gcs[tid] = rv[RV_RQ + tid - CH] * eg[tid - CH];
+        if (tid < CH) rv[RV_QK + tid] = tid < len ? rv[RV_RK + tid] * ex2(gam[CH - 1] - gam[tid]) : 0.f;
         if (tid == 0 && !mbar_spin(bar_ap, it & 1)) set_status(KDA_ERR_DEVICE_TIMEOUT);
         __syncthreads();
         tc_fence_after();
@@ -1478,7 +1514,8 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
             tmem_ld32_nowait(t_ap + lo + 32 * hf, x);
             tmem_wait_ld();
             const float gr = gam[r];
-            const float rs = isq ? 1.f : rv[RV_BETA + r] * rv[RV_RK + r];   // row scale (P / rq, A)
+            // row scale: rq for P (the scan adds P Delta unscaled), beta rk for A
+            const float rs = isq ? rv[RV_RQ + r] : rv[RV_BETA + r] * rv[RV_RK + r];
             float o[32];
 #pragma unroll
             for (int jj = 0; jj < 32; jj += 4) {
@@ -1714,9 +1751,9 @@ static cudaError_t launch_fwd_impl(const uint16_t *q, const uint16_t *k, const u
         sp.Hw = Hw;
         sp.state_bf16 = state_bf16 ? 1 : 0;
         const long long nblk = (long long)nseq * Hw * 2;
-        const CUtensorMap unused{};   // the general gate's state update reads Kd^T from the records
+        const CUtensorMap unused{};   // the general gate reads Kd^T and Qg from the records
         if ((e = launch_dependent(scan_kernel<false>, dim3((unsigned)nblk), dim3(SC_THREADS), SS_BYTES, stream, unused,
-                                  sp)) != cudaSuccess)
+                                  unused, sp)) != cudaSuccess)
             return e;
         ++*launches;
         timing_mark("scan_kernel", stream);
@@ -1766,13 +1803,14 @@ cudaError_t launch_fwd_scalar_gate(const uint16_t *q, const uint16_t *k, const u
         sp.init = init; sp.fin = fin; sp.out = out; sp.H_qk = H_qk; sp.H_v = H_v; sp.nseq = nseq; sp.h0 = 0;
         sp.Hw = H_v;
         sp.state_bf16 = 0;
-        // the state update's raw key rows: 64 channels x 64 rows per box, 128-byte swizzle
-        CUtensorMap mk{};
+        // the raw key and query rows: 64 channels x 64 rows per box, 128-byte swizzle
+        CUtensorMap mk{}, mq{};
         const long long rows = (long long)B * T;
-        if (rows > 0 && (e = tma_map_rows_heads(&mk, k, rows, H_qk, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+        if (rows > 0 && ((e = tma_map_rows_heads(&mk, k, rows, H_qk, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess ||
+                         (e = tma_map_rows_heads(&mq, q, rows, H_qk, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess))
             return e;
         if ((e = launch_dependent(scan_kernel<true>, dim3((unsigned)((long long)nseq * H_v * 2)), dim3(SC_THREADS),
-                                  SS_BYTES, stream, mk, sp)) != cudaSuccess)
+                                  SS_BYTES, stream, mk, mq, sp)) != cudaSuccess)
             return e;
         ++*launches;
         timing_mark("scan_kernel", stream);
