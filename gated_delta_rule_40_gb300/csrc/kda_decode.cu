@@ -220,24 +220,25 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
             kh[u] = *reinterpret_cast<const float4 *>(&s_kh[t][32 * u + c4]);
             qt[u] = *reinterpret_cast<const float4 *>(&s_qt[t][32 * u + c4]);
         }
-        // per row j: dk_j = s'_j . kh (value 2 j) and dq_j = s'_j . qt (value 2 j + 1), lane partials
+        // per row j: dk_j = s'_j . kh (value 2 j) and dq_j = s'_j . qt (value 2 j + 1), lane partials.
+        // Packed fp32 pairs (one instruction per two multiplies or fused multiply-adds): the
+        // even and odd channels of a quad accumulate separately and are added at the end.
         float red[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            float dk = 0.f, dq = 0.f;
+            float2 dk = make_float2(0.f, 0.f), dq = make_float2(0.f, 0.f);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                float4 x = s[j][u];
-                x.x *= dec[u].x;
-                x.y *= dec[u].y;
-                x.z *= dec[u].z;
-                x.w *= dec[u].w;
-                s[j][u] = x;
-                dk = fmaf(x.x, kh[u].x, fmaf(x.y, kh[u].y, fmaf(x.z, kh[u].z, fmaf(x.w, kh[u].w, dk))));
-                dq = fmaf(x.x, qt[u].x, fmaf(x.y, qt[u].y, fmaf(x.z, qt[u].z, fmaf(x.w, qt[u].w, dq))));
+                const float2 xa = __fmul2_rn(make_float2(s[j][u].x, s[j][u].y), make_float2(dec[u].x, dec[u].y));
+                const float2 xb = __fmul2_rn(make_float2(s[j][u].z, s[j][u].w), make_float2(dec[u].z, dec[u].w));
+                s[j][u] = make_float4(xa.x, xa.y, xb.x, xb.y);
+                dk = __ffma2_rn(xa, make_float2(kh[u].x, kh[u].y), dk);
+                dk = __ffma2_rn(xb, make_float2(kh[u].z, kh[u].w), dk);
+                dq = __ffma2_rn(xa, make_float2(qt[u].x, qt[u].y), dq);
+                dq = __ffma2_rn(xb, make_float2(qt[u].z, qt[u].w), dq);
             }
-            red[2 * j] = dk;
-            red[2 * j + 1] = dq;
+            red[2 * j] = dk.x + dk.y;
+            red[2 * j + 1] = dq.x + dq.y;
         }
         // reduce-scatter over the eight lanes of a row group: at each level a lane keeps half of
         // its values (the half selected by its lane bit) and adds the partner's copy of that half;
@@ -262,12 +263,12 @@ __global__ __launch_bounds__(DEC_WARPS * 32, 2) void decode_tokens_kernel(
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float delta = __shfl_sync(0xffffffffu, delta_mine, 8 * g + 2 * j);
+            const float2 d2 = make_float2(delta, delta);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                s[j][u].x = fmaf(delta, kh[u].x, s[j][u].x);
-                s[j][u].y = fmaf(delta, kh[u].y, s[j][u].y);
-                s[j][u].z = fmaf(delta, kh[u].z, s[j][u].z);
-                s[j][u].w = fmaf(delta, kh[u].w, s[j][u].w);
+                const float2 a = __ffma2_rn(d2, make_float2(kh[u].x, kh[u].y), make_float2(s[j][u].x, s[j][u].y));
+                const float2 c = __ffma2_rn(d2, make_float2(kh[u].z, kh[u].w), make_float2(s[j][u].z, s[j][u].w));
+                s[j][u] = make_float4(a.x, a.y, c.x, c.y);
             }
         }
     }
