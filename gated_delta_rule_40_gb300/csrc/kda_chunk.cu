@@ -1204,16 +1204,25 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
                         const int j = 32 * vhalf + jj;
                         const float4 ua = *reinterpret_cast<const float4 *>(urow + jj);
                         const float4 ub = *reinterpret_cast<const float4 *>(urow + jj + 4);
-                        const float d0 = ua.x - __uint_as_float(ys[jj + 0]), d1 = ua.y - __uint_as_float(ys[jj + 1]);
-                        const float d2 = ua.z - __uint_as_float(ys[jj + 2]), d3 = ua.w - __uint_as_float(ys[jj + 3]);
-                        const float d4 = ub.x - __uint_as_float(ys[jj + 4]), d5 = ub.y - __uint_as_float(ys[jj + 5]);
-                        const float d6 = ub.z - __uint_as_float(ys[jj + 6]), d7 = ub.w - __uint_as_float(ys[jj + 7]);
+                        // Delta = U - Y and its scaled copy, on packed fp32 pairs
+                        const float2 m1 = make_float2(-1.f, -1.f);
+                        const float2 p01 = __ffma2_rn(make_float2(__uint_as_float(ys[jj + 0]), __uint_as_float(ys[jj + 1])), m1,
+                                                      make_float2(ua.x, ua.y));
+                        const float2 p23 = __ffma2_rn(make_float2(__uint_as_float(ys[jj + 2]), __uint_as_float(ys[jj + 3])), m1,
+                                                      make_float2(ua.z, ua.w));
+                        const float2 p45 = __ffma2_rn(make_float2(__uint_as_float(ys[jj + 4]), __uint_as_float(ys[jj + 5])), m1,
+                                                      make_float2(ub.x, ub.y));
+                        const float2 p67 = __ffma2_rn(make_float2(__uint_as_float(ys[jj + 6]), __uint_as_float(ys[jj + 7])), m1,
+                                                      make_float2(ub.z, ub.w));
+                        const float d0 = p01.x, d1 = p01.y, d2 = p23.x, d3 = p23.y, d4 = p45.x, d5 = p45.y, d6 = p67.x,
+                                    d7 = p67.y;
                         const float4 ka = *reinterpret_cast<const float4 *>(rkr + jj);
                         const float4 kb = *reinterpret_cast<const float4 *>(rkr + jj + 4);
+                        const float2 e01 = __fmul2_rn(p01, make_float2(ka.x, ka.y)), e23 = __fmul2_rn(p23, make_float2(ka.z, ka.w));
+                        const float2 e45 = __fmul2_rn(p45, make_float2(kb.x, kb.y)), e67 = __fmul2_rn(p67, make_float2(kb.z, kb.w));
                         if constexpr (SG) {
                             // f Delta as bf16 hi (SS_DT) + lo (SS_DT + 8 KiB): 64 rows (v) x 64 (r), K-major
-                            const float e[8] = {d0 * ka.x, d1 * ka.y, d2 * ka.z, d3 * ka.w,
-                                                d4 * kb.x, d5 * kb.y, d6 * kb.z, d7 * kb.w};
+                            const float e[8] = {e01.x, e01.y, e23.x, e23.y, e45.x, e45.y, e67.x, e67.y};
                             uint32_t hi[4], lo[4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
@@ -1225,11 +1234,9 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
                             *reinterpret_cast<uint4 *>(sm + SS_DT + 8192 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         } else {
                             *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j, VB)) =
-                                make_uint4(tf32_rn_bits(d0 * ka.x), tf32_rn_bits(d1 * ka.y), tf32_rn_bits(d2 * ka.z),
-                                           tf32_rn_bits(d3 * ka.w));
+                                make_uint4(tf32_rn_bits(e01.x), tf32_rn_bits(e01.y), tf32_rn_bits(e23.x), tf32_rn_bits(e23.y));
                             *reinterpret_cast<uint4 *>(sm + SS_DT + sw128_off(vme, 4 * j + 16, VB)) =
-                                make_uint4(tf32_rn_bits(d4 * kb.x), tf32_rn_bits(d5 * kb.y), tf32_rn_bits(d6 * kb.z),
-                                           tf32_rn_bits(d7 * kb.w));
+                                make_uint4(tf32_rn_bits(e45.x), tf32_rn_bits(e45.y), tf32_rn_bits(e67.x), tf32_rn_bits(e67.y));
                         }
                         *reinterpret_cast<uint4 *>(sm + SS_DTB + sw128_off(vme, 2 * j, VB)) =
                             make_uint4(pack_bf16x2(d0, d1), pack_bf16x2(d2, d3), pack_bf16x2(d4, d5),
@@ -1249,7 +1256,12 @@ __global__ __launch_bounds__(SC_THREADS, 1) void scan_kernel(const __grid_consta
                 tmem_ld32_nowait(tZ + lane_off + 32 * vhalf, z0);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) S[j] = fmaf(S[j], g, __uint_as_float(z0[j]));
+                for (int j = 0; j < 32; j += 2) {
+                    const float2 r = __ffma2_rn(make_float2(S[j], S[j + 1]), make_float2(g, g),
+                                                make_float2(__uint_as_float(z0[j]), __uint_as_float(z0[j + 1])));
+                    S[j] = r.x;
+                    S[j + 1] = r.y;
+                }
             }
             tc_fence_before();
         }
