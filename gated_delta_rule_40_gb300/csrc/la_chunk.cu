@@ -325,9 +325,11 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                 uint32_t kh[4], kl[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float d0 = bf16_lo(ka[e]) * ed, d1 = bf16_hi(ka[e]) * ed;
-                    kh[e] = pack_bf16x2(d0, d1);
-                    kl[e] = pack_bf16x2(d0 - bf16_lo(kh[e]), d1 - bf16_hi(kh[e]));
+                    // packed fp32 pairs: d = k ed, lo = d - bf16(d)
+                    const float2 d = __fmul2_rn(make_float2(bf16_lo(ka[e]), bf16_hi(ka[e])), make_float2(ed, ed));
+                    kh[e] = pack_bf16x2(d.x, d.y);
+                    const float2 r = __ffma2_rn(make_float2(bf16_lo(kh[e]), bf16_hi(kh[e])), make_float2(-1.f, -1.f), d);
+                    kl[e] = pack_bf16x2(r.x, r.y);
                 }
                 *reinterpret_cast<uint4 *>(stg + LA_K + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
                 *reinterpret_cast<uint4 *>(sm + LA_KL + (c & 1) * 16384 + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
@@ -351,7 +353,12 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                 tmem_ld16_nowait(tmem + LT_Z + lane_off + 32 * cg + 16 * hlf, z);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) S[16 * hlf + j] = fmaf(S[16 * hlf + j], g, __uint_as_float(z[j]));
+                for (int j = 0; j < 16; j += 2) {
+                    const float2 r = __ffma2_rn(make_float2(S[16 * hlf + j], S[16 * hlf + j + 1]), make_float2(g, g),
+                                                make_float2(__uint_as_float(z[j]), __uint_as_float(z[j + 1])));
+                    S[16 * hlf + j] = r.x;
+                    S[16 * hlf + j + 1] = r.y;
+                }
             }
             write_sa();
             return true;
@@ -376,11 +383,18 @@ __global__ __launch_bounds__(LA_THREADS, 1) void la_fwd_kernel(const __grid_cons
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar + 8 * (LB_OUT0 + b));
                 }
+                // rows 16 cg + 8 hlf + j take f = eq0 lambda^(8 hlf + j); row pairs walk by lambda^2
+                float2 fp = make_float2(f, f * lam);
+                const float2 l2 = make_float2(lam * lam, lam * lam);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    os[(16 * cg + 8 * hlf + j) * KD + vme] = f_to_bf16(fmaf(f, __uint_as_float(y1[j]), __uint_as_float(y2[j])));
-                    f *= lam;
+                for (int j = 0; j < 8; j += 2) {
+                    const float2 r = __ffma2_rn(fp, make_float2(__uint_as_float(y1[j]), __uint_as_float(y1[j + 1])),
+                                                make_float2(__uint_as_float(y2[j]), __uint_as_float(y2[j + 1])));
+                    os[(16 * cg + 8 * hlf + j) * KD + vme] = f_to_bf16(r.x);
+                    os[(16 * cg + 8 * hlf + j + 1) * KD + vme] = f_to_bf16(r.y);
+                    fp = __fmul2_rn(fp, l2);
                 }
+                f = fp.x;
             }
             fence_async_smem();
             if (tid == 0) bulk_wait_read_all();
