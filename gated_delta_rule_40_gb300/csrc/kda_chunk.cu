@@ -678,11 +678,14 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                     if (cb < bia) load_pair(ca, cbb, o);
                     else if (cb == bia) load_pair(cd, cbb, o);
                     else load_pair(cd, cd, o);
+                    const float2 be2 = make_float2(be, be);
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        *reinterpret_cast<float4 *>(sA + r * AS + 16 * cb + j) =
-                            make_float4(o[j] * be * ck[j], o[j + 1] * be * ck[j + 1], o[j + 2] * be * ck[j + 2],
-                                        o[j + 3] * be * ck[j + 3]);
+                    for (int j = 0; j < 16; j += 4) {
+                        const float2 a0 = __fmul2_rn(__fmul2_rn(make_float2(o[j], o[j + 1]), be2), make_float2(ck[j], ck[j + 1]));
+                        const float2 a1 = __fmul2_rn(__fmul2_rn(make_float2(o[j + 2], o[j + 3]), be2),
+                                                     make_float2(ck[j + 2], ck[j + 3]));
+                        *reinterpret_cast<float4 *>(sA + r * AS + 16 * cb + j) = make_float4(a0.x, a0.y, a1.x, a1.y);
+                    }
                 } else {
                     if (cb < bia) {
                         load_pair(ca, cbb, o);
@@ -701,7 +704,11 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
                         for (int j = 0; j < 16; ++j) o[j] = 0.f;
                     }
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) o[j] *= ck[j];
+                    for (int j = 0; j < 16; j += 2) {
+                        const float2 pj = __fmul2_rn(make_float2(o[j], o[j + 1]), make_float2(ck[j], ck[j + 1]));
+                        o[j] = pj.x;
+                        o[j + 1] = pj.y;
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; j += 8)
                         *reinterpret_cast<uint4 *>(sm + IS_PI + sw128_off(r, 2 * (16 * cb + j), CH)) =
@@ -728,21 +735,23 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_kernel(const
         // split into bf16 hi + lo, as A operands (K-major, 64 r x 64 j)
         for (int idx = tid; idx < CH * (CH / 8); idx += IN_THREADS) {
             const int r = idx >> 3, j = (idx & 7) * 8;
-            float x[8], xw[8];
             uint32_t hi[4], lo[4], hw[4], lw[4];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                x[e] = sT[r * AS + j + e] * rv[RV_BETA + j + e];
-                xw[e] = x[e] * rv[RV_RK + j + e];
-            }
+            // packed fp32 pairs: x = T beta, xw = x rk, and the hi / lo splits
+            const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-                const uint32_t h2 = pack_bf16x2(x[e], x[e + 1]);
+                const float2 t2 = *reinterpret_cast<const float2 *>(sT + r * AS + j + e);
+                const float2 b2 = *reinterpret_cast<const float2 *>(rv + RV_BETA + j + e);
+                const float2 k2 = *reinterpret_cast<const float2 *>(rv + RV_RK + j + e);
+                const float2 x2 = __fmul2_rn(t2, b2), xw2 = __fmul2_rn(x2, k2);
+                const uint32_t h2 = pack_bf16x2(x2.x, x2.y);
                 hi[e >> 1] = h2;
-                lo[e >> 1] = pack_bf16x2(x[e] - bf16_lo(h2), x[e + 1] - bf16_hi(h2));
-                const uint32_t w2 = pack_bf16x2(xw[e], xw[e + 1]);
+                const float2 l2 = __ffma2_rn(make_float2(bf16_lo(h2), bf16_hi(h2)), m1, x2);
+                lo[e >> 1] = pack_bf16x2(l2.x, l2.y);
+                const uint32_t w2 = pack_bf16x2(xw2.x, xw2.y);
                 hw[e >> 1] = w2;
-                lw[e >> 1] = pack_bf16x2(xw[e] - bf16_lo(w2), xw[e + 1] - bf16_hi(w2));
+                const float2 lw2 = __ffma2_rn(make_float2(bf16_lo(w2), bf16_hi(w2)), m1, xw2);
+                lw[e >> 1] = pack_bf16x2(lw2.x, lw2.y);
             }
             const uint32_t off = sw128_off(r, 2 * j, CH);
             *reinterpret_cast<uint4 *>(sm + IS_TPH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
