@@ -1581,21 +1581,23 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
         // T' = T diag(beta) (for U) and T'_W = T diag(beta rk exp(Gam)) (for W on the raw K)
         for (int idx = tid; idx < CH * (CH / 8); idx += IN_THREADS) {
             const int r = idx >> 3, j = (idx & 7) * 8;
-            float x[8], xw[8];
             uint32_t hi[4], lo[4], hw[4], lw[4];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                x[e] = sT[r * AS + j + e] * rv[RV_BETA + j + e];
-                xw[e] = x[e] * rv[RV_RK + j + e] * eg[j + e];
-            }
+            // packed fp32 pairs: x = T beta, xw = x rk exp(Gam), and the hi / lo splits
+            const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-                const uint32_t h2 = pack_bf16x2(x[e], x[e + 1]);
+                const float2 x2 = __fmul2_rn(*reinterpret_cast<const float2 *>(sT + r * AS + j + e),
+                                             *reinterpret_cast<const float2 *>(rv + RV_BETA + j + e));
+                const float2 xw2 = __fmul2_rn(__fmul2_rn(x2, *reinterpret_cast<const float2 *>(rv + RV_RK + j + e)),
+                                              *reinterpret_cast<const float2 *>(eg + j + e));
+                const uint32_t h2 = pack_bf16x2(x2.x, x2.y);
                 hi[e >> 1] = h2;
-                lo[e >> 1] = pack_bf16x2(x[e] - bf16_lo(h2), x[e + 1] - bf16_hi(h2));
-                const uint32_t w2 = pack_bf16x2(xw[e], xw[e + 1]);
+                const float2 l2 = __ffma2_rn(make_float2(bf16_lo(h2), bf16_hi(h2)), m1, x2);
+                lo[e >> 1] = pack_bf16x2(l2.x, l2.y);
+                const uint32_t w2 = pack_bf16x2(xw2.x, xw2.y);
                 hw[e >> 1] = w2;
-                lw[e >> 1] = pack_bf16x2(xw[e] - bf16_lo(w2), xw[e + 1] - bf16_hi(w2));
+                const float2 lw2 = __ffma2_rn(make_float2(bf16_lo(w2), bf16_hi(w2)), m1, xw2);
+                lw[e >> 1] = pack_bf16x2(lw2.x, lw2.y);
             }
             const uint32_t off = sw128_off(r, 2 * j, CH);
             *reinterpret_cast<uint4 *>(sm + GD_TPH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
