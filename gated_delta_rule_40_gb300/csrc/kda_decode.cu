@@ -77,12 +77,24 @@ __global__ __launch_bounds__(DEC_WARPS * 32, BF16 ? 4 : 2) void decode_kernel(
     for (int i = 0; i < DEC_ROWS; ++i) {
         float4 x = BF16 ? make_float4(bf16_lo(sb[i].x), bf16_hi(sb[i].x), bf16_lo(sb[i].y), bf16_hi(sb[i].y))
                         : s[BF16 ? 0 : i];
-        x.x *= dec[0];
-        x.y *= dec[1];
-        x.z *= dec[2];
-        x.w *= dec[3];
-        float dk = x.x * kh[0] + x.y * kh[1] + x.z * kh[2] + x.w * kh[3];
-        float dq = x.x * qt[0] + x.y * qt[1] + x.z * qt[2] + x.w * qt[3];
+        float dk, dq;
+        if constexpr (BF16) {
+            x.x *= dec[0];
+            x.y *= dec[1];
+            x.z *= dec[2];
+            x.w *= dec[3];
+            dk = x.x * kh[0] + x.y * kh[1] + x.z * kh[2] + x.w * kh[3];
+            dq = x.x * qt[0] + x.y * qt[1] + x.z * qt[2] + x.w * qt[3];
+        } else {
+            // packed fp32 pairs: the decay, then the two dot products on even / odd channel halves
+            const float2 xa = __fmul2_rn(make_float2(x.x, x.y), make_float2(dec[0], dec[1]));
+            const float2 xb = __fmul2_rn(make_float2(x.z, x.w), make_float2(dec[2], dec[3]));
+            x = make_float4(xa.x, xa.y, xb.x, xb.y);
+            const float2 dk2 = __ffma2_rn(xb, make_float2(kh[2], kh[3]), __fmul2_rn(xa, make_float2(kh[0], kh[1])));
+            const float2 dq2 = __ffma2_rn(xb, make_float2(qt[2], qt[3]), __fmul2_rn(xa, make_float2(qt[0], qt[1])));
+            dk = dk2.x + dk2.y;
+            dq = dq2.x + dq2.y;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             dk += __shfl_xor_sync(0xffffffffu, dk, o);
@@ -90,10 +102,16 @@ __global__ __launch_bounds__(DEC_WARPS * 32, BF16 ? 4 : 2) void decode_kernel(
         }
         const float vi = __shfl_sync(0xffffffffu, vrow, i);
         const float delta = beta * (vi - dk);
-        x.x = fmaf(delta, kh[0], x.x);
-        x.y = fmaf(delta, kh[1], x.y);
-        x.z = fmaf(delta, kh[2], x.z);
-        x.w = fmaf(delta, kh[3], x.w);
+        if constexpr (BF16) {
+            x.x = fmaf(delta, kh[0], x.x);
+            x.y = fmaf(delta, kh[1], x.y);
+            x.z = fmaf(delta, kh[2], x.z);
+            x.w = fmaf(delta, kh[3], x.w);
+        } else {
+            const float2 ua = __ffma2_rn(make_float2(delta, delta), make_float2(kh[0], kh[1]), make_float2(x.x, x.y));
+            const float2 ub = __ffma2_rn(make_float2(delta, delta), make_float2(kh[2], kh[3]), make_float2(x.z, x.w));
+            x = make_float4(ua.x, ua.y, ub.x, ub.y);
+        }
         if (BF16)
             __stcs(reinterpret_cast<uint2 *>(Sb + (size_t)i * KD) + lane,
                    make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w)));
