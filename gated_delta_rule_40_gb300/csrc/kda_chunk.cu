@@ -1545,9 +1545,14 @@ __global__ __launch_bounds__(IN_THREADS, IN_CTAS_PER_SM) void intra_gdn_kernel(c
                 const float4 kj = *reinterpret_cast<const float4 *>(rv + RV_RK + j);
                 const float gv[4] = {gj.x, gj.y, gj.z, gj.w}, kv[4] = {kj.x, kj.y, kj.z, kj.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool keep = isq ? (j + e <= r) : (j + e < r);
-                    o[jj + e] = keep ? __uint_as_float(x[jj + e]) * ex2(gr - gv[e]) * rs * kv[e] : 0.f;
+                for (int e = 0; e < 4; e += 2) {
+                    // packed fp32 pairs: D e^(Gam_r - Gam_j) rs rk_j for columns j + e, j + e + 1
+                    const float2 v = __fmul2_rn(
+                        __fmul2_rn(make_float2(__uint_as_float(x[jj + e]), __uint_as_float(x[jj + e + 1])),
+                                   make_float2(ex2(gr - gv[e]), ex2(gr - gv[e + 1]))),
+                        __fmul2_rn(make_float2(rs, rs), make_float2(kv[e], kv[e + 1])));
+                    o[jj + e] = (isq ? (j + e <= r) : (j + e < r)) ? v.x : 0.f;
+                    o[jj + e + 1] = (isq ? (j + e + 1 <= r) : (j + e + 1 < r)) ? v.y : 0.f;
                 }
             }
             if (!isq) {
